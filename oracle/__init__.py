@@ -1,0 +1,188 @@
+"""fp64 CPU oracle for the CAT forward pass — TEST INFRASTRUCTURE.
+
+Only the tests, the smoke check and the benchmark's CPU-baseline leg may
+import this package.  The product path (the CUDA library and its binding)
+never does, and this package never imports the product.  It shares nothing
+with the CUDA side except the seeded input generator in ``synth``.
+
+What it computes (notes page "CAT: Circular-Convolutional Attention for
+Sub-Quadratic Transformers", section 方法详解, designs "circulant attention
+matrix construction" and "FFT acceleration"):
+
+    z  = X · W_A              z[b, h, n]
+    z* = softmax_n(z)         over the N tokens of each (b, h)
+    O  = circ(z*) · V_h       circ(z*)[i, j] = z*[(i - j) mod N]
+       = IFFT(FFT(z*) ⊙ FFT(V_h))   column by column
+
+All arithmetic is fp64 in ``cat_oracle.c``; this module only marshals numpy
+arrays.  ``brute_circulant`` builds the N x N matrix explicitly (tiny N only)
+and multiplies with numpy, so it is an independent third evaluation.
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+_LIB = None
+
+
+def _lib():
+    global _LIB
+    if _LIB is None:
+        path = _build.build()
+        lib = ctypes.CDLL(path)
+        dp = ctypes.POINTER(ctypes.c_double)
+        lp = ctypes.POINTER(ctypes.c_long)
+        L = ctypes.c_long
+        lib.oracle_scores.argtypes = [dp, dp, L, L, L, L, dp]
+        lib.oracle_scores.restype = None
+        lib.oracle_softmax.argtypes = [dp, dp, L, L]
+        lib.oracle_softmax.restype = None
+        lib.oracle_circ_direct.argtypes = [dp, dp, L, L, L, L, dp]
+        lib.oracle_circ_direct.restype = None
+        lib.oracle_circ_direct_rows.argtypes = [dp, dp, L, L, L, L, lp, L, dp]
+        lib.oracle_circ_direct_rows.restype = None
+        lib.oracle_dft.argtypes = [dp, dp, L, ctypes.c_int]
+        lib.oracle_dft.restype = ctypes.c_int
+        lib.oracle_circ_fft.argtypes = [dp, dp, L, L, L, L, dp, dp]
+        lib.oracle_circ_fft.restype = ctypes.c_int
+        lib.oracle_spectrum.argtypes = [dp, L, L, dp]
+        lib.oracle_spectrum.restype = ctypes.c_int
+        lib.oracle_num_threads.argtypes = []
+        lib.oracle_num_threads.restype = ctypes.c_int
+        _LIB = lib
+    return _LIB
+
+
+def _f64(a):
+    """Contiguous float64 numpy copy of a numpy array or a CPU torch tensor."""
+    if hasattr(a, "detach"):  # torch tensor (any dtype, incl. bfloat16)
+        a = a.detach().to("cpu").double().numpy()
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def _p(a):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def num_threads() -> int:
+    """OpenMP threads the oracle uses."""
+    return int(_lib().oracle_num_threads())
+
+
+def scores(X, WA):
+    """z[b, h, n] = sum_d X[b, n, d] W_A[d, h]."""
+    X, WA = _f64(X), _f64(WA)
+    B, N, D = X.shape
+    H = WA.shape[1]
+    assert WA.shape[0] == D
+    z = np.empty((B, H, N), np.float64)
+    _lib().oracle_scores(_p(X), _p(WA), B, N, D, H, _p(z))
+    return z
+
+
+def softmax(z):
+    """Softmax over the last axis (the N tokens)."""
+    z = _f64(z)
+    N = z.shape[-1]
+    out = np.empty_like(z)
+    _lib().oracle_softmax(_p(z), _p(out), z.size // N if N else 0, N)
+    return out
+
+
+def zstar(X, WA):
+    """z* = softmax_n(X · W_A), shape [B, H, N]."""
+    return softmax(scores(X, WA))
+
+
+def dft(x, inverse=False):
+    """Complex DFT of a 1-D array (recursive radix-2 + naive odd-length DFT)."""
+    x = np.asarray(x, dtype=np.complex128)
+    re = np.ascontiguousarray(x.real, dtype=np.float64)
+    im = np.ascontiguousarray(x.imag, dtype=np.float64)
+    rc = _lib().oracle_dft(_p(re), _p(im), re.size, 1 if inverse else 0)
+    if rc != 0:
+        raise MemoryError("oracle_dft")
+    return re + 1j * im
+
+
+def spectrum(zs):
+    """Zf[..., k] = sum_n z*[..., n] exp(-2πi kn/N) (complex128)."""
+    zs = _f64(zs)
+    N = zs.shape[-1]
+    out = np.empty(zs.shape + (2,), np.float64)
+    rc = _lib().oracle_spectrum(_p(zs), zs.size // N, N, _p(out))
+    if rc != 0:
+        raise MemoryError("oracle_spectrum")
+    return out[..., 0] + 1j * out[..., 1]
+
+
+def circ_direct(zs, V):
+    """O = circ(z*) V by the O(N^2) definition.  zs [B,H,N], V [B,N,D]."""
+    zs, V = _f64(zs), _f64(V)
+    B, N, D = V.shape
+    H = zs.shape[1]
+    O = np.empty((B, N, D), np.float64)
+    _lib().oracle_circ_direct(_p(zs), _p(V), B, N, D, H, _p(O))
+    return O
+
+
+def circ_direct_rows(zs, V, rows):
+    """The O(N^2) definition at the listed output rows only: [B, len(rows), D]."""
+    zs, V = _f64(zs), _f64(V)
+    B, N, D = V.shape
+    H = zs.shape[1]
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).astype(np.int_))
+    O = np.empty((B, rows.size, D), np.float64)
+    _lib().oracle_circ_direct_rows(
+        _p(zs), _p(V), B, N, D, H,
+        rows.ctypes.data_as(ctypes.POINTER(ctypes.c_long)), rows.size, _p(O))
+    return O
+
+
+def circ_fft(zs, V, return_max_imag=False):
+    """O = IFFT(FFT(z*) ⊙ FFT(V_h)) per column, fp64."""
+    zs, V = _f64(zs), _f64(V)
+    B, N, D = V.shape
+    H = zs.shape[1]
+    O = np.empty((B, N, D), np.float64)
+    mi = ctypes.c_double(0.0)
+    rc = _lib().oracle_circ_fft(_p(zs), _p(V), B, N, D, H, _p(O),
+                                ctypes.pointer(mi))
+    if rc != 0:
+        raise MemoryError("oracle_circ_fft")
+    return (O, mi.value) if return_max_imag else O
+
+
+def brute_circulant(zs_row):
+    """The explicit N x N matrix circ(z*)[i, j] = z*[(i - j) mod N]."""
+    z = np.asarray(zs_row, dtype=np.float64)
+    N = z.size
+    i = np.arange(N)[:, None]
+    j = np.arange(N)[None, :]
+    return z[(i - j) % N]
+
+
+def forward(X, WA, V, mode="auto"):
+    """Whole forward: returns (O [B,N,D], z* [B,H,N]) in fp64.
+
+    mode: "direct" (O(N^2) definition), "fft" (convolution theorem), or
+    "auto" (direct while B·N²·D stays under ~2e9 multiply-adds, else fft).
+    """
+    X, WA, V = _f64(X), _f64(WA), _f64(V)
+    B, N, D = V.shape
+    zs = zstar(X, WA)
+    if mode == "auto":
+        mode = "direct" if B * N * N * D <= 2e9 else "fft"
+    if mode == "direct":
+        return circ_direct(zs, V), zs
+    if mode == "fft":
+        return circ_fft(zs, V), zs
+    raise ValueError(mode)
+
+
+__all__ = ["scores", "softmax", "zstar", "dft", "spectrum", "circ_direct",
+           "circ_direct_rows", "circ_fft", "brute_circulant", "forward",
+           "num_threads"]

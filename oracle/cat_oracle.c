@@ -1,0 +1,303 @@
+/*
+ * fp64 CPU oracle for the CAT forward pass (circular-convolutional attention).
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may call, link or
+ * load this file; only the tests, the smoke check and the benchmark's CPU
+ * baseline do.  It shares no code, header, table or helper with the CUDA
+ * library: it is a plain restatement of the definitions, written to be
+ * checked by eye.
+ *
+ * Source of every formula: the notes page "CAT: Circular-Convolutional
+ * Attention for Sub-Quadratic Transformers" (NeurIPS 2025, arXiv 2504.06704),
+ * section 方法详解 (method), sub-sections 整体框架 (overall framework) and
+ * 关键设计 (key designs: "circulant attention matrix construction" and
+ * "FFT acceleration").  In that notation, per head h:
+ *
+ *     Z      = X · W_A[:, h]                 (one score per token)
+ *     Z*     = softmax(Z) over the N tokens
+ *     circ(Z*)[i, j] = Z*[(i - j) mod N]     (row i = i-th cyclic shift)
+ *     O_h    = circ(Z*) · V_h  =  IFFT( FFT(Z*) ⊙ FFT(V_h) )
+ *
+ * Readings taken where the page is open (each listed in the design notes):
+ *   - W_A is D x H (one column per head), as the parameter count (D+H)·D
+ *     requires, although the page prints D x 1;
+ *   - "row softmax" of the N x 1 score vector is a softmax over the N tokens;
+ *   - the shift direction is the one the convolution theorem in the "FFT
+ *     acceleration" design fixes: circ[i, j] = z*[(i - j) mod N];
+ *   - head h owns the contiguous value columns [h·D/H, (h+1)·D/H);
+ *   - no temperature, bias, mask or output projection.
+ *
+ * Layouts (all row-major, fp64):
+ *   X, V, O : [B, N, D]      W_A : [D, H]      z, z* : [B, H, N]
+ *
+ * Parallelism: OpenMP over independent output elements only; every sum is a
+ * plain left-to-right loop in the order the definition writes it.
+ */
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifndef M_PI
+#define M_PI 3.14159265358979323846
+#endif
+
+/* Z = X · W_A  (整体框架 / circulant attention matrix construction).
+ * z[b, h, n] = sum_d X[b, n, d] * W_A[d, h]. */
+void oracle_scores(const double *X, const double *WA, long B, long N, long D,
+                   long H, double *z) {
+  long b, n;
+#pragma omp parallel for collapse(2) schedule(static)
+  for (b = 0; b < B; ++b) {
+    for (n = 0; n < N; ++n) {
+      const double *x = X + (b * N + n) * D;
+      for (long h = 0; h < H; ++h) {
+        double acc = 0.0;
+        for (long d = 0; d < D; ++d) acc += x[d] * WA[d * H + h];
+        z[(b * H + h) * N + n] = acc;
+      }
+    }
+  }
+}
+
+/* Z* = softmax(Z) over the N entries of each of `rows` rows
+ * (circulant attention matrix construction): subtract the row maximum,
+ * exponentiate, divide by the sum. */
+void oracle_softmax(const double *z, double *zs, long rows, long N) {
+  long r;
+#pragma omp parallel for schedule(static)
+  for (r = 0; r < rows; ++r) {
+    const double *zr = z + r * N;
+    double *out = zs + r * N;
+    double m = zr[0];
+    for (long n = 1; n < N; ++n)
+      if (zr[n] > m) m = zr[n];
+    double s = 0.0;
+    for (long n = 0; n < N; ++n) {
+      out[n] = exp(zr[n] - m);
+      s += out[n];
+    }
+    for (long n = 0; n < N; ++n) out[n] /= s;
+  }
+}
+
+/* Index of the head that owns value column c. */
+static long head_of(long c, long D, long H) { return c / (D / H); }
+
+/* O = circ(Z*) · V by the plain definition, O(B·N²·D):
+ * O[b, i, c] = sum_j z*[b, h(c), (i - j) mod N] * V[b, j, c]. */
+void oracle_circ_direct(const double *zs, const double *V, long B, long N,
+                        long D, long H, double *O) {
+  long b, i;
+#pragma omp parallel for collapse(2) schedule(static)
+  for (b = 0; b < B; ++b) {
+    for (i = 0; i < N; ++i) {
+      for (long c = 0; c < D; ++c) {
+        const double *w = zs + (b * H + head_of(c, D, H)) * N;
+        double acc = 0.0;
+        for (long j = 0; j < N; ++j) {
+          long s = i - j;
+          if (s < 0) s += N;
+          acc += w[s] * V[(b * N + j) * D + c];
+        }
+        O[(b * N + i) * D + c] = acc;
+      }
+    }
+  }
+}
+
+/* The same definition evaluated only at the output rows listed in `rows`
+ * (nrows of them) for every batch and column: Orows[b, r, c]. */
+void oracle_circ_direct_rows(const double *zs, const double *V, long B, long N,
+                             long D, long H, const long *rows, long nrows,
+                             double *Orows) {
+  long b, r;
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+  for (b = 0; b < B; ++b) {
+    for (r = 0; r < nrows; ++r) {
+      long i = rows[r];
+      for (long c = 0; c < D; ++c) {
+        const double *w = zs + (b * H + head_of(c, D, H)) * N;
+        double acc = 0.0;
+        for (long j = 0; j < N; ++j) {
+          long s = i - j;
+          if (s < 0) s += N;
+          acc += w[s] * V[(b * N + j) * D + c];
+        }
+        Orows[(b * nrows + r) * D + c] = acc;
+      }
+    }
+  }
+}
+
+/* Textbook discrete Fourier transform, forward sign exp(-2πi kn/N), no
+ * scaling.  Even lengths: one recursive radix-2 decimation-in-time split
+ *     X[k]       = E[k] + w^k O[k]
+ *     X[k + N/2] = E[k] - w^k O[k],   w = exp(-2πi/N),
+ * with E, O the transforms of the even- and odd-indexed samples.  Odd
+ * lengths: the naive O(N²) sum.  Twiddles come straight from cos/sin of the
+ * exact angle (reduced mod N first), never from a recurrence. */
+static void dft_rec(const double *re, const double *im, long N, long stride,
+                    double *ore, double *oim, double *work) {
+  if (N == 1) {
+    ore[0] = re[0];
+    oim[0] = im[0];
+    return;
+  }
+  if (N % 2 == 1) {
+    for (long k = 0; k < N; ++k) {
+      double ar = 0.0, ai = 0.0;
+      for (long n = 0; n < N; ++n) {
+        long kn = (k * n) % N;
+        double ang = -2.0 * M_PI * (double)kn / (double)N;
+        double c = cos(ang), s = sin(ang);
+        double xr = re[n * stride], xi = im[n * stride];
+        ar += xr * c - xi * s;
+        ai += xr * s + xi * c;
+      }
+      ore[k] = ar;
+      oim[k] = ai;
+    }
+    return;
+  }
+  long h = N / 2;
+  /* E into ore[0..h), O into ore[h..N); work gives the recursion scratch. */
+  dft_rec(re, im, h, 2 * stride, ore, oim, work);
+  dft_rec(re + stride, im + stride, h, 2 * stride, ore + h, oim + h, work);
+  for (long k = 0; k < h; ++k) {
+    double ang = -2.0 * M_PI * (double)k / (double)N;
+    double c = cos(ang), s = sin(ang);
+    double er = ore[k], ei = oim[k];
+    double orr = ore[h + k], oi = oim[h + k];
+    double tr = orr * c - oi * s;
+    double ti = orr * s + oi * c;
+    work[k] = er + tr;
+    work[N + k] = ei + ti;
+    work[h + k] = er - tr;
+    work[N + h + k] = ei - ti;
+  }
+  memcpy(ore, work, (size_t)N * sizeof(double));
+  memcpy(oim, work + N, (size_t)N * sizeof(double));
+}
+
+/* In-place DFT of one length-N complex signal (re, im).  inverse != 0 uses
+ * exp(+2πi kn/N) and divides by N.  Returns 0, or -1 if memory ran out. */
+int oracle_dft(double *re, double *im, long N, int inverse) {
+  if (N <= 0) return 0;
+  double *in = (double *)malloc(sizeof(double) * 2 * (size_t)N);
+  double *out = (double *)malloc(sizeof(double) * 2 * (size_t)N);
+  double *work = (double *)malloc(sizeof(double) * 2 * (size_t)N);
+  if (!in || !out || !work) {
+    free(in);
+    free(out);
+    free(work);
+    return -1;
+  }
+  /* Inverse via conjugation: IDFT(x) = conj(DFT(conj(x))) / N. */
+  double sgn = inverse ? -1.0 : 1.0;
+  for (long n = 0; n < N; ++n) {
+    in[n] = re[n];
+    in[N + n] = sgn * im[n];
+  }
+  dft_rec(in, in + N, N, 1, out, out + N, work);
+  for (long n = 0; n < N; ++n) {
+    re[n] = inverse ? out[n] / (double)N : out[n];
+    im[n] = inverse ? -out[N + n] / (double)N : out[N + n];
+  }
+  free(in);
+  free(out);
+  free(work);
+  return 0;
+}
+
+/* O = IFFT(FFT(Z*) ⊙ FFT(V_h)) column by column (FFT acceleration design).
+ * Each value column is transformed on its own as a real signal.  max_imag
+ * receives max |Im| of the inverse transforms, which is zero in exact
+ * arithmetic because both factors are real.  Returns 0 or -1 (memory). */
+int oracle_circ_fft(const double *zs, const double *V, long B, long N, long D,
+                    long H, double *O, double *max_imag) {
+  long rows = B * H;
+  double *zf = (double *)malloc(sizeof(double) * 2 * (size_t)(rows * N));
+  if (!zf) return -1;
+  int fail = 0;
+  long r;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (r = 0; r < rows; ++r) {
+    double *fr = zf + 2 * r * N, *fi = fr + N;
+    for (long n = 0; n < N; ++n) {
+      fr[n] = zs[r * N + n];
+      fi[n] = 0.0;
+    }
+    if (oracle_dft(fr, fi, N, 0) != 0) fail = 1;
+  }
+  double mi = 0.0;
+  long b, c;
+#pragma omp parallel for collapse(2) schedule(dynamic, 1) reduction(max : mi)
+  for (b = 0; b < B; ++b) {
+    for (c = 0; c < D; ++c) {
+      double *vr = (double *)malloc(sizeof(double) * 2 * (size_t)N);
+      if (!vr) {
+        fail = 1;
+        continue;
+      }
+      double *vi = vr + N;
+      for (long n = 0; n < N; ++n) {
+        vr[n] = V[(b * N + n) * D + c];
+        vi[n] = 0.0;
+      }
+      if (oracle_dft(vr, vi, N, 0) != 0) fail = 1;
+      const double *fr = zf + 2 * (b * H + head_of(c, D, H)) * N;
+      const double *fi = fr + N;
+      for (long k = 0; k < N; ++k) { /* Hadamard product */
+        double pr = fr[k] * vr[k] - fi[k] * vi[k];
+        double pi = fr[k] * vi[k] + fi[k] * vr[k];
+        vr[k] = pr;
+        vi[k] = pi;
+      }
+      if (oracle_dft(vr, vi, N, 1) != 0) fail = 1;
+      for (long n = 0; n < N; ++n) {
+        O[(b * N + n) * D + c] = vr[n];
+        if (fabs(vi[n]) > mi) mi = fabs(vi[n]);
+      }
+      free(vr);
+    }
+  }
+  free(zf);
+  if (max_imag) *max_imag = mi;
+  return fail ? -1 : 0;
+}
+
+/* Spectrum of the softmax row: Zf[r, k] = sum_n z*[r, n] exp(-2πi kn/N),
+ * stored as interleaved (re, im) pairs, rows x N x 2. */
+int oracle_spectrum(const double *zs, long rows, long N, double *zf) {
+  int fail = 0;
+  long r;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (r = 0; r < rows; ++r) {
+    double *t = (double *)malloc(sizeof(double) * 2 * (size_t)N);
+    if (!t) {
+      fail = 1;
+      continue;
+    }
+    for (long n = 0; n < N; ++n) {
+      t[n] = zs[r * N + n];
+      t[N + n] = 0.0;
+    }
+    if (oracle_dft(t, t + N, N, 0) != 0) fail = 1;
+    for (long k = 0; k < N; ++k) {
+      zf[2 * (r * N + k)] = t[k];
+      zf[2 * (r * N + k) + 1] = t[N + k];
+    }
+    free(t);
+  }
+  return fail ? -1 : 0;
+}
+
+/* Number of OpenMP threads the oracle will use (1 without OpenMP). */
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+  extern int omp_get_max_threads(void);
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}

@@ -1,0 +1,47 @@
+"""Seeded synthetic inputs for the CAT forward pass.
+
+This module holds no arithmetic of the method: it only draws random numbers
+and rounds them to the run's storage type.  Both the fp64 oracle and the CUDA
+path consume exactly the arrays it returns.
+
+Recipe (the workloads of the CAT notes page — ViT patch tokens and GPT-2
+masked-LM tokens — have no public inputs here, so i.i.d. Gaussians stand in):
+  * numpy ``Generator(PCG64(seed))``, draws in the order X, W_A, V, each drawn
+    as float32 standard normals;
+  * X, V ~ N(0, 1) of shape [B, N, D];  W_A ~ N(0, 1/D) · wa_scale, [D, H];
+  * then rounded to the storage dtype (float32 as drawn; bfloat16 by torch's
+    round-to-nearest-even conversion).
+"""
+import numpy as np
+import torch
+
+DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16}
+
+# The configurations the benchmark and parity tests use: (B, N, D, H, dtype).
+CONFIGS = {
+    "tiny": dict(B=1, N=256, D=64, H=2, dtype="f32"),
+    "vit196": dict(B=64, N=196, D=384, H=6, dtype="f32"),
+    "gpt2_f32": dict(B=16, N=1024, D=768, H=12, dtype="f32"),
+    "gpt2_bf16": dict(B=16, N=1024, D=768, H=12, dtype="bf16"),
+    "long16k": dict(B=4, N=16384, D=1024, H=16, dtype="bf16"),
+    "long128k": dict(B=1, N=131072, D=1024, H=16, dtype="bf16"),
+}
+
+
+def make_inputs(B, N, D, H, dtype="f32", seed=0, wa_scale=1.0):
+    """Return CPU torch tensors (X [B,N,D], W_A [D,H], V [B,N,D]) in ``dtype``."""
+    if dtype not in DTYPES:
+        raise ValueError("dtype must be one of %s" % sorted(DTYPES))
+    rng = np.random.Generator(np.random.PCG64(seed))
+    X = rng.standard_normal((B, N, D), dtype=np.float32)
+    WA = rng.standard_normal((D, H), dtype=np.float32)
+    WA *= np.float32(wa_scale / np.sqrt(D)) if D > 0 else np.float32(0)
+    V = rng.standard_normal((B, N, D), dtype=np.float32)
+    tdt = DTYPES[dtype]
+    return (torch.from_numpy(X).to(tdt), torch.from_numpy(WA).to(tdt),
+            torch.from_numpy(V).to(tdt))
+
+
+def make_config(name, seed=0, wa_scale=1.0):
+    c = CONFIGS[name]
+    return make_inputs(c["B"], c["N"], c["D"], c["H"], c["dtype"], seed, wa_scale)
