@@ -1,0 +1,404 @@
+"""Benchmark of the CAT forward (circular-convolutional attention) on GB300.
+
+One step = one cat_forward over one batch of the workload: score
+projection, softmax over the tokens, spectrum of z*, and the circulant
+product IFFT(FFT(z*) ⊙ FFT(V)) for every column (the hot path of the CAT
+notes page, section 方法详解).  Inputs are seeded synthetic tensors already
+resident in HBM; X + V + O are larger than L2, so no flush is needed
+between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+                    [--config long16k] [--no-secondary]
+
+Prints ONE JSON line (rank 0).  With --impl reference the fp64 CPU oracle
+is timed instead, on a bounded sample of the same workload.
+"""
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "CAT attention tokens·heads/s at N=16384 & 131072; % of HBM/FP32 roofline"
+UNIT = "tokens·heads/s"
+PRIMARY = "long16k"
+SECONDARY = "long128k"
+
+# GB300: 152 SMs x 128 FP32 lanes x 2 flops (FMA) x 2070 MHz maximum SM clock.
+SMS, FP32_LANES, MAX_SM_MHZ = 152, 128, 2070.0
+FP32_PEAK_TFLOPS = SMS * FP32_LANES * 2 * MAX_SM_MHZ * 1e6 / 1e12
+FALLBACK_HBM_GBS = 6800.0
+
+# DRAM bytes per launch of the circulant-product stage, from an ncu capture
+# of the same source (profiles/).  Keyed by workload; None = not captured
+# for the current kernels.
+NCU_TRAFFIC = {}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def cfg_of(name):
+    c = dict(synth.CONFIGS[name])
+    c["es"] = 2 if c["dtype"] == "bf16" else 4
+    return c
+
+
+def fft_flops(N):
+    return 5.0 * N * math.log2(N) if N > 1 else 0.0
+
+
+def algorithmic(c):
+    """Bytes and FFT flops of one forward, and of its circulant-product stage."""
+    B, N, D, H, es = c["B"], c["N"], c["D"], c["H"], c["es"]
+    npair = (D // H + 1) // 2
+    pair_tf = 2 * B * H * npair          # forward + inverse per packed pair
+    conv_flops = pair_tf * fft_flops(N)
+    total_flops = conv_flops + B * H * fft_flops(N)   # + spectrum of z*
+    conv_bytes = 2 * B * N * D * es       # V read, O written
+    total_bytes = 3 * B * N * D * es + D * H * es
+    return dict(conv_flops=conv_flops, total_flops=total_flops, conv_bytes=conv_bytes,
+                total_bytes=total_bytes, score_flops=2.0 * B * N * D * H)
+
+
+class ClockSampler:
+    """nvidia-smi clock and throttle sampling while the timed loop runs."""
+
+    Q = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [r.split(", ") for r in self.file.read().strip().splitlines() if r.strip()]
+        os.unlink(self.file.name)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx = float(r[2])
+                for n, v in zip(names, r[4:8]):
+                    if v.strip() == "Active":
+                        reasons.add(n)
+            except Exception:
+                continue
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_init(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "gb300" and torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world, device):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------ CPU oracle
+
+def oracle_sample(c, heads):
+    """A bounded sample of the workload for the fp64 oracle: batch 0 and the
+    first `heads` heads (their W_A columns and value columns)."""
+    X, WA, V = synth.make_inputs(1, c["N"], c["D"], c["H"], c["dtype"], seed=0)
+    dh = c["D"] // c["H"]
+    WAs = WA[:, :heads].contiguous()
+    Vs = V[:, :, : heads * dh].contiguous()
+    # The head split only needs D/H = dh: keep dh columns per sampled head.
+    return X, WAs, Vs
+
+
+def time_oracle(c, heads, reps=1):
+    import oracle
+    X, WAs, Vs = oracle_sample(c, heads)
+    X64, W64, V64 = (t.double().numpy() for t in (X, WAs, Vs))
+    units = c["N"] * heads
+    times = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        _forward_sample(oracle, X64, W64, V64, heads)
+        times.append(time.perf_counter() - t0)
+    return units, times, oracle.num_threads()
+
+
+def _forward_sample(oracle, X, WA, V, heads):
+    # z* for the sampled heads from the full X rows, then the circulant
+    # product of each sampled head's columns (the oracle's FFT mode).
+    zs = oracle.zstar(X, WA)                  # [1, heads, N]
+    return oracle.circ_fft(zs, V)             # V holds heads·dh columns
+
+
+def sample_heads(c):
+    # All heads of batch 0: a few seconds of fp64 work on a many-core host.
+    return c["H"]
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    c = cfg_of(args.config)
+    c["name"] = args.config
+    heads = args.sample_heads or sample_heads(c)
+    for _ in range(args.warmup):
+        time_oracle(c, heads)
+    times = []
+    for _ in range(args.steps):
+        units, t, cores = time_oracle(c, heads)
+        times.extend(t)
+    tot = sum(times)
+    value = units * len(times) / tot
+    sample = ("batch 0, heads 0..%d of %s (B=%d N=%d D=%d H=%d %s): z* from the full rows, "
+              "fp64 FFT-mode circulant product of %d value columns"
+              % (heads - 1, args.config, c["B"], c["N"], c["D"], c["H"], c["dtype"],
+                 heads * (c["D"] // c["H"])))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * tot / len(times), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.config, "B": c["B"], "N": c["N"], "D": c["D"], "H": c["H"],
+                   "storage": c["dtype"]},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------ GPU path
+
+def measure_workload(name, steps, warmup, device, world, sampler=None):
+    import fft_circulant_attention_gb300 as cat
+    c = cfg_of(name)
+    X, WA, V = synth.make_inputs(c["B"], c["N"], c["D"], c["H"], c["dtype"], seed=0)
+    Xd, Wd, Vd = (t.to(device) for t in (X, WA, V))
+    Od = torch.empty_like(Vd)
+    stream = torch.cuda.current_stream(device)
+    plan = cat.Plan(c["B"], c["N"], c["D"], c["H"], c["dtype"], stream=stream)
+    for _ in range(warmup):
+        plan.forward(Xd, Wd, Vd, Od)
+    plan.sync()
+    plan.timing(steps)
+    barrier(world)
+    torch.cuda.synchronize(device)
+    if sampler:
+        sampler.start()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        plan.forward(Xd, Wd, Vd, Od)
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    clocks = sampler.stop() if sampler else None
+    barrier(world)
+    ms_total = e0.elapsed_time(e1)
+    stage_ms, ncalls = plan.stage_times()
+    plan.sync()
+    desc = plan.describe()
+    launches = int(desc.split("launches=")[1].split()[0])
+    plan.timing(0)
+    ms_total = max_over_ranks(ms_total, world, device)
+
+    # End to end through the C ABI with pinned host buffers: every step
+    # copies X, W_A, V in and O out inside the timed region.
+    Xp, Wp, Vp = (t.pin_memory() for t in (X, WA, V))
+    Op = torch.empty_like(Vp).pin_memory()
+    e2e_steps = max(3, min(steps, 20))
+    plan.forward_host(Xp, Wp, Vp, Op)
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        plan.forward_host(Xp, Wp, Vp, Op)
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world, device)
+    plan.close()
+    del Xd, Vd, Od
+    torch.cuda.empty_cache()
+
+    units = c["B"] * c["N"] * c["H"]
+    ms_step = ms_total / steps
+    a = algorithmic(c)
+    hbm, hbm_kind = load_peaks()
+    conv_ms = stage_ms[2] / max(ncalls, 1)
+    t_conv = conv_ms * 1e-3
+    conv_tflops = a["conv_flops"] / t_conv / 1e12
+    conv_gbs = a["conv_bytes"] / t_conv / 1e9
+    t_roof_conv = max(a["conv_bytes"] / (hbm * 1e9), a["conv_flops"] / (FP32_PEAK_TFLOPS * 1e12))
+    bound = "alu" if a["conv_flops"] / FP32_PEAK_TFLOPS / 1e12 >= a["conv_bytes"] / hbm / 1e9 \
+        else "hbm"
+    roof = {
+        "kernel": "circulant product (%s)" % desc.split()[0].replace("path=", ""),
+        "bound": bound,
+        "achieved": conv_tflops if bound == "alu" else conv_gbs,
+        "peak": FP32_PEAK_TFLOPS if bound == "alu" else hbm,
+        "unit": "TFLOP/s" if bound == "alu" else "GB/s",
+        "frac": (conv_tflops / FP32_PEAK_TFLOPS) if bound == "alu" else conv_gbs / hbm,
+        "traffic": NCU_TRAFFIC.get(name),
+        "peak_source": ("FP32: 152 SMs x 128 lanes x 2 x 2070 MHz (derived); HBM: %s %.0f GB/s"
+                        % (hbm_kind, hbm)),
+        "hbm_gbs_achieved": conv_gbs,
+        "hbm_frac": conv_gbs / hbm,
+        "ms_per_launch": conv_ms,
+        "roofline_frac_of_stage": t_roof_conv / t_conv,
+    }
+    t_roof = max(a["total_bytes"] / (hbm * 1e9), a["total_flops"] / (FP32_PEAK_TFLOPS * 1e12))
+    e2e_val = world * units * e2e_steps / e2e_s
+    es = c["es"]
+    return {
+        "name": name, "c": c, "value": world * units / (ms_step * 1e-3), "ms_per_step": ms_step,
+        "stage_ms": [s / max(ncalls, 1) for s in stage_ms], "roofline": roof,
+        "path_roofline_frac": t_roof / (ms_step * 1e-3), "t_roof_us": t_roof * 1e6,
+        "launches": launches, "desc": desc, "clocks": clocks,
+        "e2e": {"value": e2e_val, "unit": UNIT,
+                "h2d_bytes_per_step": 2 * c["B"] * c["N"] * c["D"] * es + c["D"] * c["H"] * es,
+                "d2h_bytes_per_step": c["B"] * c["N"] * c["D"] * es,
+                "ms_per_step": 1e3 * e2e_s / e2e_steps},
+    }
+
+
+def run_gb300(args, world, rank, local):
+    import fft_circulant_attention_gb300 as cat
+    from fft_circulant_attention_gb300 import build
+    build.build()
+    cat.lib()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    sampler = ClockSampler(local) if rank == 0 else None
+    prim = measure_workload(args.config, args.steps, args.warmup, device, world, sampler)
+    sec = None
+    if not args.no_secondary and args.config != SECONDARY:
+        sec = measure_workload(SECONDARY, max(3, args.steps // 4), args.warmup, device, world)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        c = cfg_of(args.config)
+        c["name"] = args.config
+        heads = args.sample_heads or sample_heads(c)
+        units, times, cores = time_oracle(c, heads)
+        cpu = {"value": units / times[0], "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": "batch 0, head%s 0..%d of %s: z* from the full rows and the fp64 "
+                         "FFT-mode circulant product of those heads' columns"
+                         % ("s" if heads > 1 else "", heads - 1, args.config),
+               "seconds": times[0]}
+    if rank != 0:
+        return
+    c = prim["c"]
+    line = {
+        "metric": METRIC, "value": prim["value"], "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": prim["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": args.config, "B": c["B"], "N": c["N"], "D": c["D"], "H": c["H"],
+                   "storage": c["dtype"], "l2": "inputs larger than L2 (X+V+O %.0f MB)"
+                   % (3 * c["B"] * c["N"] * c["D"] * c["es"] / 1e6),
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "plan": prim["desc"]},
+        "roofline": prim["roofline"],
+        "path_roofline_frac": prim["path_roofline_frac"],
+        "stage_ms": {"score": prim["stage_ms"][0], "softmax_spectrum": prim["stage_ms"][1],
+                     "circulant_product": prim["stage_ms"][2]},
+        "e2e": prim["e2e"],
+        "gpu_launches": prim["launches"] * args.steps,
+        "clocks": prim["clocks"],
+        "cpu_baseline": cpu,
+    }
+    if sec is not None:
+        sc = sec["c"]
+        line["secondary"] = {
+            "workload": SECONDARY, "B": sc["B"], "N": sc["N"], "D": sc["D"], "H": sc["H"],
+            "value": sec["value"], "ms_per_step": sec["ms_per_step"],
+            "path_roofline_frac": sec["path_roofline_frac"], "roofline": sec["roofline"],
+            "stage_ms": sec["stage_ms"], "e2e": sec["e2e"], "plan": sec["desc"]}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--config", default=PRIMARY, choices=sorted(synth.CONFIGS))
+    ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sample-heads", type=int, default=0)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    world, rank, local = dist_init(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_gb300(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,251 @@
+"""Python binding of libcat, the GB300 CAT forward library (include/cat.h).
+
+CAT (circular-convolutional attention), from the notes page "CAT:
+Circular-Convolutional Attention for Sub-Quadratic Transformers", section
+方法详解: per batch b and head h, z = X·W_A[:, h], z* = softmax over the N
+tokens, and O_h = circ(z*)·V_h = IFFT(FFT(z*) ⊙ FFT(V_h)).
+
+This module only marshals arguments (tensor -> device pointer, stream ->
+handle, status -> exception).  Every step of the computation runs in the
+CUDA kernels of ``libcat.so``; there is no other implementation behind it,
+and importing it fails loudly when the library has not been built.
+
+The functions carry the C names: ``cat_plan_create``, ``cat_forward``,
+``cat_forward_zstar``, ``cat_forward_host``, ``cat_plan_sync``,
+``cat_plan_describe``, ``cat_plan_set_stream``, ``cat_plan_destroy`` and
+``cat_status_string``.  ``Plan`` wraps them for convenience.
+"""
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libcat.so")
+
+CAT_F32, CAT_BF16 = 0, 1
+CAT_OK = 0
+STATUS = {
+    0: "CAT_OK", -1: "CAT_ERR_INVALID_ARG", -2: "CAT_ERR_UNSUPPORTED_N",
+    -3: "CAT_ERR_MISALIGNED", -4: "CAT_ERR_PLAN_MISMATCH", -5: "CAT_ERR_ALLOC",
+    -6: "CAT_ERR_CUDA", -7: "CAT_ERR_DEVICE_STATUS", -8: "CAT_ERR_ALIAS",
+}
+for _code, _name in STATUS.items():
+    globals()[_name] = _code
+
+# Every symbol include/cat.h declares, with (restype, argtypes).
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+SIGNATURES = {
+    "cat_plan_create": (_I, [ctypes.POINTER(_P), _I, _I, _I, _I, _I, _P]),
+    "cat_plan_destroy": (_I, [_P]),
+    "cat_plan_set_stream": (_I, [_P, _P]),
+    "cat_forward": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I]),
+    "cat_forward_zstar": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I]),
+    "cat_forward_host": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I]),
+    "cat_plan_sync": (_I, [_P]),
+    "cat_plan_describe": (_I, [_P, ctypes.c_char_p, _I]),
+    "cat_plan_timing": (_I, [_P, _I]),
+    "cat_plan_stage_times": (_I, [_P, ctypes.POINTER(ctypes.c_float), _I,
+                                  ctypes.POINTER(_I)]),
+    "cat_status_string": (ctypes.c_char_p, [_I]),
+}
+
+_LIB = None
+
+
+class CatError(RuntimeError):
+    """A libcat call returned a non-zero status."""
+
+    def __init__(self, status, where=""):
+        self.status = status
+        super().__init__("%s%s (%d)" % (where + ": " if where else "",
+                                        STATUS.get(status, "CAT_ERR_UNKNOWN"), status))
+
+
+def lib():
+    """The loaded libcat.so (ctypes.CDLL).  Raises if it has not been built."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                "libcat.so is missing at %s: build it with "
+                "`python -c 'import __graft_entry__ as g; g.build()'`" % LIB_PATH)
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _LIB = L
+    return _LIB
+
+
+def _ptr(x):
+    """Device or host address of a tensor / numpy array / int (None -> 0)."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    if hasattr(x, "ctypes"):
+        return x.ctypes.data
+    raise TypeError("cannot take the address of %r" % type(x))
+
+
+def _stream(s):
+    if s is None:
+        return None
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def _check(st, where):
+    if st != CAT_OK:
+        raise CatError(st, where)
+
+
+def dtype_code(dtype):
+    """CAT_F32 / CAT_BF16 from a code, a name or a torch dtype."""
+    if isinstance(dtype, int):
+        return dtype
+    name = str(dtype).replace("torch.", "")
+    if name in ("float32", "f32", "float"):
+        return CAT_F32
+    if name in ("bfloat16", "bf16"):
+        return CAT_BF16
+    raise ValueError("unsupported dtype %r" % (dtype,))
+
+
+def cat_status_string(status):
+    return lib().cat_status_string(status).decode()
+
+
+def cat_plan_create(B, N, D, H, dtype, stream=None):
+    """Create a plan; returns its handle (an int).  Raises CatError."""
+    h = ctypes.c_void_p()
+    _check(lib().cat_plan_create(ctypes.byref(h), B, N, D, H, dtype_code(dtype),
+                                 _stream(stream)), "cat_plan_create")
+    return h.value
+
+
+def cat_plan_destroy(plan):
+    _check(lib().cat_plan_destroy(plan), "cat_plan_destroy")
+
+
+def cat_plan_set_stream(plan, stream):
+    _check(lib().cat_plan_set_stream(plan, _stream(stream)), "cat_plan_set_stream")
+
+
+def cat_forward(plan, X, W_A, V, O, B, N, D, H, dtype):
+    _check(lib().cat_forward(plan, _ptr(X), _ptr(W_A), _ptr(V), _ptr(O), B, N, D, H,
+                             dtype_code(dtype)), "cat_forward")
+
+
+def cat_forward_zstar(plan, X, W_A, zstar, B, N, D, H, dtype):
+    _check(lib().cat_forward_zstar(plan, _ptr(X), _ptr(W_A), _ptr(zstar), B, N, D, H,
+                                   dtype_code(dtype)), "cat_forward_zstar")
+
+
+def cat_forward_host(plan, X, W_A, V, O, B, N, D, H, dtype):
+    _check(lib().cat_forward_host(plan, _ptr(X), _ptr(W_A), _ptr(V), _ptr(O), B, N, D, H,
+                                  dtype_code(dtype)), "cat_forward_host")
+
+
+def cat_plan_sync(plan):
+    _check(lib().cat_plan_sync(plan), "cat_plan_sync")
+
+
+def cat_plan_timing(plan, max_calls):
+    _check(lib().cat_plan_timing(plan, max_calls), "cat_plan_timing")
+
+
+def cat_plan_stage_times(plan):
+    """(ms per stage [score, softmax/spectrum, circulant product], calls)."""
+    ms = (ctypes.c_float * 3)()
+    n = ctypes.c_int(0)
+    _check(lib().cat_plan_stage_times(plan, ms, 3, ctypes.byref(n)), "cat_plan_stage_times")
+    return [float(v) for v in ms], n.value
+
+
+def cat_plan_describe(plan):
+    buf = ctypes.create_string_buffer(512)
+    _check(lib().cat_plan_describe(plan, buf, 512), "cat_plan_describe")
+    return buf.value.decode()
+
+
+class Plan:
+    """Owns one libcat plan for a fixed (B, N, D, H, dtype).
+
+    ``forward(X, W_A, V, O=None)`` takes CUDA tensors of the plan's dtype
+    (X, V, O: [B, N, D]; W_A: [D, H]) and enqueues the forward on the plan's
+    stream (torch's current stream when the plan was made, unless given).
+    """
+
+    def __init__(self, B, N, D, H, dtype, stream=None):
+        import torch
+        self.B, self.N, self.D, self.H = B, N, D, H
+        self.dtype = dtype_code(dtype)
+        self.torch_dtype = torch.bfloat16 if self.dtype == CAT_BF16 else torch.float32
+        if stream is None and torch.cuda.is_available():
+            stream = torch.cuda.current_stream()
+        self.handle = cat_plan_create(B, N, D, H, self.dtype, stream)
+
+    def _shape(self):
+        return (self.B, self.N, self.D, self.H, self.dtype)
+
+    def forward(self, X, W_A, V, O=None):
+        import torch
+        if O is None:
+            O = torch.empty_like(V)
+        for t in (X, W_A, V, O):
+            if not t.is_contiguous() or t.dtype != self.torch_dtype:
+                raise ValueError("tensors must be contiguous %s" % self.torch_dtype)
+        cat_forward(self.handle, X, W_A, V, O, *self._shape())
+        return O
+
+    def zstar(self, X, W_A, out=None):
+        import torch
+        if out is None:
+            out = torch.empty((self.B, self.H, self.N), dtype=torch.float32, device=X.device)
+        cat_forward_zstar(self.handle, X, W_A, out, *self._shape())
+        return out
+
+    def forward_host(self, X, W_A, V, O):
+        cat_forward_host(self.handle, X, W_A, V, O, *self._shape())
+        return O
+
+    def sync(self):
+        cat_plan_sync(self.handle)
+
+    def describe(self):
+        return cat_plan_describe(self.handle)
+
+    def timing(self, max_calls):
+        cat_plan_timing(self.handle, max_calls)
+
+    def stage_times(self):
+        return cat_plan_stage_times(self.handle)
+
+    def close(self):
+        if self.handle:
+            cat_plan_destroy(self.handle)
+            self.handle = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+__all__ = ["CatError", "Plan", "lib", "dtype_code", "cat_plan_create", "cat_plan_destroy",
+           "cat_plan_set_stream", "cat_forward", "cat_forward_zstar", "cat_forward_host",
+           "cat_plan_sync", "cat_plan_describe", "cat_plan_timing", "cat_plan_stage_times",
+           "cat_status_string", "CAT_F32", "CAT_BF16",
+           "SIGNATURES", "LIB_PATH"]

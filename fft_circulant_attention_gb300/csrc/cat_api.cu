@@ -1,0 +1,461 @@
+// C ABI of libcat: plan construction, validation and the forward entry
+// points declared in cat.h.  Host code only; the kernels live in score.cu,
+// conv_smem.cu and fourstep.cu.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <vector>
+
+#include "../../include/cat.h"
+#include "cat_internal.h"
+
+using cat::RadixPlan;
+
+namespace {
+
+constexpr int kSmemMaxN = 16384;             // longest single-CTA transform
+constexpr size_t kConvSmemBudget = 64 << 10;  // preferred per-CTA tile (bytes)
+constexpr size_t kFsSmemBudget = 100 << 10;
+constexpr size_t kScratchBudget = 80ull << 20;  // live four-step scratch (L2-sized)
+
+bool seven_smooth(long n) {
+  if (n < 1) return false;
+  for (int p : {2, 3, 5, 7})
+    while (n % p == 0) n /= p;
+  return n == 1;
+}
+
+// Radices for a transform of length L (7-smooth): 8s, then a 4 or 2 for the
+// rest of the power of two, then 7s, 5s, 3s.
+bool make_radix_plan(int L, RadixPlan* rp) {
+  std::memset(rp, 0, sizeof(*rp));
+  rp->L = L;
+  int n = L, k = 0;
+  auto push = [&](int r) {
+    if (k >= cat::kMaxPasses) return false;
+    rp->radix[k++] = r;
+    n /= r;
+    return true;
+  };
+  while (n % 8 == 0)
+    if (!push(8)) return false;
+  if (n % 4 == 0 && !push(4)) return false;
+  if (n % 2 == 0 && !push(2)) return false;
+  for (int r : {7, 5, 3})
+    while (n % r == 0)
+      if (!push(r)) return false;
+  if (n != 1) return false;
+  rp->npass = k;
+  return true;
+}
+
+int round_up(int x, int m) { return (x + m - 1) / m * m; }
+
+// Threads for `count` transforms of length L: about 16 values per thread,
+// at least one warp, at most 1024.
+int fft_threads(long count, int L) {
+  long t = (count * L + 15) / 16;
+  if (t < 32) t = 32;
+  if (t > 1024) t = 1024;
+  return round_up((int)t, 32);
+}
+
+// Pairs per CTA given a per-pair shared footprint, balanced across groups.
+void split_pairs(int npair, int gmax, int* G, int* groups) {
+  if (gmax < 1) gmax = 1;
+  if (gmax > npair) gmax = npair;
+  int g = (npair + gmax - 1) / gmax;
+  *groups = g;
+  *G = (npair + g - 1) / g;
+}
+
+int map_cuda(cudaError_t e) { return e == cudaSuccess ? CAT_OK : CAT_ERR_CUDA; }
+
+bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb) {
+  uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
+  return x < y + nb && y < x + na;
+}
+
+int check_shape(const cat_plan_s* p, int B, int N, int D, int H, int dtype) {
+  if (B != p->B || N != p->N || D != p->D || H != p->H || dtype != p->dtype)
+    return CAT_ERR_PLAN_MISMATCH;
+  return CAT_OK;
+}
+
+int validate_shape(int B, int N, int D, int H, int dtype) {
+  if (B < 0 || N < 1 || D < 1 || H < 1 || H > D) return CAT_ERR_INVALID_ARG;
+  if (dtype != CAT_F32 && dtype != CAT_BF16) return CAT_ERR_INVALID_ARG;
+  if (D > CAT_MAX_D || D % H != 0) return CAT_ERR_INVALID_ARG;
+  if (N > CAT_MAX_N || !seven_smooth(N)) return CAT_ERR_UNSUPPORTED_N;
+  // Largest element index must fit the kernels' size_t arithmetic; the
+  // int-typed grid counts need B·H·N within 2^31.
+  if ((long long)B * H * (long long)N > (1ll << 31)) return CAT_ERR_INVALID_ARG;
+  return CAT_OK;
+}
+
+// Split N (> kSmemMaxN) into N1·N2, both 7-smooth and <= kSmemMaxN, with
+// N1 >= N2 and N1 / N2 as small as possible.
+bool split_fourstep(int N, int* N1, int* N2) {
+  int best = -1;
+  for (int a = 2; a <= kSmemMaxN && a < N; ++a) {
+    if (N % a) continue;
+    int b = N / a;
+    if (b > kSmemMaxN || a < b || b < 2) continue;
+    if (!seven_smooth(a) || !seven_smooth(b)) continue;
+    if (best < 0 || a < best) best = a;
+  }
+  if (best < 0) return false;
+  *N1 = best;
+  *N2 = N / best;
+  return true;
+}
+
+void free_events(cat_plan_s* p) {
+  if (p->ev) {
+    for (int i = 0; i < 4 * p->timing_cap; ++i)
+      if (p->ev[i]) cudaEventDestroy(p->ev[i]);
+    delete[] p->ev;
+  }
+  p->ev = nullptr;
+  p->timing_cap = p->timing_n = 0;
+}
+
+void free_plan(cat_plan_s* p) {
+  if (!p) return;
+  free_events(p);
+  cudaFree(p->z);
+  cudaFree(p->zf);
+  cudaFree(p->tw);
+  cudaFree(p->scratch);
+  cudaFree(p->status);
+  cudaFree(p->hx);
+  cudaFree(p->hwa);
+  cudaFree(p->hv);
+  cudaFree(p->ho);
+  delete p;
+}
+
+int score_launches(int H, int D) {
+  int hpp = score_heads_per_pass(D);
+  return (H + hpp - 1) / hpp;
+}
+
+int choose_path(cat_plan_s* p) {
+  const int N = p->N;
+  // CAT_FORCE_PATH=fourstep sends short sequences down the multi-pass path
+  // too (debugging and testing of that path at small sizes).
+  const char* force = std::getenv("CAT_FORCE_PATH");
+  int n1 = 0, n2 = 0;
+  const bool force_fs = force && std::strcmp(force, "fourstep") == 0 && split_fourstep(N, &n1, &n2);
+  if (N <= kSmemMaxN && !force_fs) {
+    p->path = cat::PATH_SMEM;
+    if (!make_radix_plan(N, &p->rpN)) return CAT_ERR_UNSUPPORTED_N;
+    cat::SmemCfg& s = p->sm;
+    size_t per = (size_t)N * sizeof(float2);
+    int gmax = (int)(kConvSmemBudget / per);
+    split_pairs(p->npair, gmax, &s.G, &s.groups);
+    s.tstride = N;
+    s.smem = (size_t)s.G * s.tstride * sizeof(float2);
+    s.threads = fft_threads(s.G, N);
+    s.spec_threads = fft_threads(1, N);
+    s.spec_smem = per;
+    if ((long)s.G * N > (long)cat::vals_capacity(p->rpN) * s.threads) return CAT_ERR_UNSUPPORTED_N;
+    if ((long)N > (long)cat::vals_capacity(p->rpN) * s.spec_threads) return CAT_ERR_UNSUPPORTED_N;
+    p->launches = score_launches(p->H, p->D) + 2;
+    return CAT_OK;
+  }
+  p->path = cat::PATH_FOURSTEP;
+  cat::FourStepCfg& f = p->fs;
+  if (!split_fourstep(N, &f.N1, &f.N2)) return CAT_ERR_UNSUPPORTED_N;
+  if (!make_radix_plan(f.N1, &f.rp1) || !make_radix_plan(f.N2, &f.rp2))
+    return CAT_ERR_UNSUPPORTED_N;
+  if (!make_radix_plan(N, &p->rpN)) return CAT_ERR_UNSUPPORTED_N;
+  const size_t c8 = sizeof(float2);
+  // Pairs per CTA: pass B holds TB·(G+1) signals of length N1.
+  int gmax = (int)(kFsSmemBudget / ((size_t)f.N1 * c8)) - 1;
+  if (gmax > 16) gmax = 16;
+  split_pairs(p->npair, gmax, &f.G, &f.groups);
+  f.P = p->npair + 1;
+  // Tiles: as many n1 (k2) slots as fit the budget, dividing N1 (N2).
+  f.TA = 1;
+  for (int t = 2; t <= 64; ++t)
+    if (f.N1 % t == 0 && (size_t)t * (f.G + 1) * f.N2 * c8 <= kFsSmemBudget) f.TA = t;
+  f.TB = 1;
+  for (int t = 2; t <= 64; ++t)
+    if (f.N2 % t == 0 && (size_t)t * (f.G + 1) * f.N1 * c8 <= kFsSmemBudget) f.TB = t;
+  f.smemA = (size_t)f.TA * (f.G + 1) * f.N2 * c8;
+  f.smemB = (size_t)f.TB * (f.G + 1) * f.N1 * c8;
+  f.smemC = (size_t)f.TA * f.G * f.N2 * c8;
+  f.threadsA = fft_threads((long)f.TA * (f.G + 1), f.N2);
+  f.threadsB = fft_threads((long)f.TB * (f.G + 1), f.N1);
+  f.threadsC = fft_threads((long)f.TA * f.G, f.N2);
+  if ((long)f.TA * (f.G + 1) * f.N2 > (long)cat::vals_capacity(f.rp2) * f.threadsA ||
+      (long)f.TB * (f.G + 1) * f.N1 > (long)cat::vals_capacity(f.rp1) * f.threadsB ||
+      (long)f.TA * f.G * f.N2 > (long)cat::vals_capacity(f.rp2) * f.threadsC)
+    return CAT_ERR_UNSUPPORTED_N;
+  size_t per_bh = (size_t)N * f.P * c8;
+  long chunk = (long)(kScratchBudget / per_bh);
+  if (const char* env = std::getenv("CAT_CHUNK_BH")) chunk = std::atol(env);
+  if (chunk < 1) chunk = 1;
+  long rows = (long)p->B * p->H;
+  if (chunk > rows) chunk = rows > 0 ? rows : 1;
+  f.chunk_bh = (int)chunk;
+  p->scratch_bytes = (size_t)f.chunk_bh * per_bh;
+  p->launches = score_launches(p->H, p->D) + 1 + 3 * (int)((rows + chunk - 1) / chunk);
+  return CAT_OK;
+}
+
+void describe(cat_plan_s* p) {
+  char rad[128] = {0};
+  auto radstr = [](const RadixPlan& rp, char* out, size_t len) {
+    size_t o = 0;
+    for (int i = 0; i < rp.npass && o + 4 < len; ++i)
+      o += (size_t)std::snprintf(out + o, len - o, i ? "x%d" : "%d", rp.radix[i]);
+  };
+  if (p->path == cat::PATH_SMEM) {
+    radstr(p->rpN, rad, sizeof(rad));
+    std::snprintf(p->desc, sizeof(p->desc),
+                  "path=smem N=%d radices=%s G=%d groups=%d threads=%d smem=%zu "
+                  "spec_threads=%d workspace=%zu launches=%d",
+                  p->N, rad, p->sm.G, p->sm.groups, p->sm.threads, p->sm.smem,
+                  p->sm.spec_threads, p->workspace_bytes, p->launches);
+  } else {
+    char r1[64] = {0}, r2[64] = {0};
+    radstr(p->fs.rp1, r1, sizeof(r1));
+    radstr(p->fs.rp2, r2, sizeof(r2));
+    std::snprintf(p->desc, sizeof(p->desc),
+                  "path=fourstep N=%d N1=%d(%s) N2=%d(%s) G=%d groups=%d TA=%d TB=%d "
+                  "threads=%d/%d/%d smem=%zu/%zu/%zu chunk_bh=%d scratch=%zu workspace=%zu "
+                  "launches=%d",
+                  p->N, p->fs.N1, r1, p->fs.N2, r2, p->fs.G, p->fs.groups, p->fs.TA, p->fs.TB,
+                  p->fs.threadsA, p->fs.threadsB, p->fs.threadsC, p->fs.smemA, p->fs.smemB,
+                  p->fs.smemC, p->fs.chunk_bh, p->scratch_bytes, p->workspace_bytes,
+                  p->launches);
+  }
+}
+
+// Score, softmax and (shared-memory path) spectrum of z* into the plan.
+int run_front(cat_plan_s* p, const void* X, const void* WA) {
+  cudaError_t e = cat::launch_score(p, X, WA);
+  if (e != cudaSuccess) return CAT_ERR_CUDA;
+  if (p->path == cat::PATH_SMEM)
+    e = cat::launch_softmax_spectrum(p);
+  else
+    e = cat::launch_softmax(p);
+  return map_cuda(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+int cat_plan_create(cat_plan_t* out, int B, int N, int D, int H, int dtype, void* stream) {
+  if (!out) return CAT_ERR_INVALID_ARG;
+  *out = nullptr;
+  int st = validate_shape(B, N, D, H, dtype);
+  if (st != CAT_OK) return st;
+  cat_plan_s* p = new (std::nothrow) cat_plan_s();
+  if (!p) return CAT_ERR_ALLOC;
+  p->B = B; p->N = N; p->D = D; p->H = H; p->dtype = dtype;
+  p->dh = D / H;
+  p->npair = (p->dh + 1) / 2;
+  p->stream = (cudaStream_t)stream;
+  st = choose_path(p);
+  if (st != CAT_OK) { delete p; return st; }
+
+  if (cudaGetDevice(&p->device) != cudaSuccess) { delete p; return CAT_ERR_CUDA; }
+  const size_t rowsN = (size_t)B * H * N;
+  auto alloc = [&](void** ptr, size_t bytes) {
+    if (bytes == 0) bytes = 16;
+    return cudaMalloc(ptr, bytes) == cudaSuccess;
+  };
+  bool ok = alloc((void**)&p->z, rowsN * sizeof(float)) &&
+            alloc((void**)&p->tw, (size_t)N * sizeof(float2)) &&
+            alloc((void**)&p->status, sizeof(unsigned int));
+  if (ok && p->path == cat::PATH_SMEM) ok = alloc((void**)&p->zf, rowsN * sizeof(float2));
+  if (ok && p->path == cat::PATH_FOURSTEP) ok = alloc((void**)&p->scratch, p->scratch_bytes);
+  if (!ok) { cudaGetLastError(); free_plan(p); return CAT_ERR_ALLOC; }
+  p->workspace_bytes = rowsN * sizeof(float) + (size_t)N * sizeof(float2) +
+                       (p->zf ? rowsN * sizeof(float2) : 0) + p->scratch_bytes;
+
+  // Twiddle table exp(-2πi j/N), evaluated in fp64 and rounded once.
+  std::vector<float2> tw((size_t)N);
+  const double two_pi = 6.283185307179586476925286766559;
+  for (int j = 0; j < N; ++j) {
+    double a = -two_pi * (double)j / (double)N;
+    tw[j] = make_float2((float)std::cos(a), (float)std::sin(a));
+  }
+  cudaError_t e = cudaMemcpy(p->tw, tw.data(), (size_t)N * sizeof(float2), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemset(p->status, 0, sizeof(unsigned int));
+  if (e == cudaSuccess) e = cat::setup_score_kernels(p);
+  if (e == cudaSuccess)
+    e = p->path == cat::PATH_SMEM ? cat::setup_smem_kernels(p) : cat::setup_fourstep_kernels(p);
+  if (e != cudaSuccess) { free_plan(p); return CAT_ERR_CUDA; }
+  describe(p);
+  if (std::getenv("CAT_LOG")) std::fprintf(stderr, "[cat] %s\n", p->desc);
+  *out = p;
+  return CAT_OK;
+}
+
+int cat_plan_destroy(cat_plan_t plan) {
+  if (!plan) return CAT_OK;
+  int dev = -1;
+  const int plan_dev = plan->device;
+  cudaGetDevice(&dev);
+  if (dev != plan_dev) cudaSetDevice(plan_dev);
+  cudaError_t e = cudaStreamSynchronize(plan->stream);
+  free_plan(plan);
+  if (dev >= 0 && dev != plan_dev) cudaSetDevice(dev);
+  return map_cuda(e);
+}
+
+int cat_plan_set_stream(cat_plan_t plan, void* stream) {
+  if (!plan) return CAT_ERR_INVALID_ARG;
+  plan->stream = (cudaStream_t)stream;
+  return CAT_OK;
+}
+
+int cat_forward(cat_plan_t p, const void* X, const void* WA, const void* V, void* O, int B, int N,
+                int D, int H, int dtype) {
+  if (!p) return CAT_ERR_INVALID_ARG;
+  int st = check_shape(p, B, N, D, H, dtype);
+  if (st != CAT_OK) return st;
+  if (B == 0) return CAT_OK;
+  if (!X || !WA || !V || !O) return CAT_ERR_INVALID_ARG;
+  if (((uintptr_t)X | (uintptr_t)WA | (uintptr_t)V | (uintptr_t)O) & 15) return CAT_ERR_MISALIGNED;
+  const size_t es = dtype == CAT_BF16 ? 2 : 4;
+  const size_t nx = (size_t)B * N * D * es, nw = (size_t)D * H * es;
+  if (ranges_overlap(O, nx, X, nx) || ranges_overlap(O, nx, WA, nw) || ranges_overlap(O, nx, V, nx))
+    return CAT_ERR_ALIAS;
+  cudaEvent_t* ev = nullptr;
+  if (p->timing_n < p->timing_cap) ev = p->ev + 4 * p->timing_n++;
+  if (ev) cudaEventRecord(ev[0], p->stream);
+  cudaError_t e = cat::launch_score(p, X, WA);
+  if (e != cudaSuccess) return CAT_ERR_CUDA;
+  if (ev) cudaEventRecord(ev[1], p->stream);
+  e = p->path == cat::PATH_SMEM ? cat::launch_softmax_spectrum(p) : cat::launch_softmax(p);
+  if (e != cudaSuccess) return CAT_ERR_CUDA;
+  if (ev) cudaEventRecord(ev[2], p->stream);
+  e = p->path == cat::PATH_SMEM ? cat::launch_conv_smem(p, V, O)
+                                : cat::launch_fourstep_conv(p, V, O);
+  if (ev) cudaEventRecord(ev[3], p->stream);
+  return map_cuda(e);
+}
+
+int cat_forward_zstar(cat_plan_t p, const void* X, const void* WA, float* zstar, int B, int N,
+                      int D, int H, int dtype) {
+  if (!p) return CAT_ERR_INVALID_ARG;
+  int st = check_shape(p, B, N, D, H, dtype);
+  if (st != CAT_OK) return st;
+  if (B == 0) return CAT_OK;
+  if (!X || !WA || !zstar) return CAT_ERR_INVALID_ARG;
+  if (((uintptr_t)X | (uintptr_t)WA | (uintptr_t)zstar) & 15) return CAT_ERR_MISALIGNED;
+  st = run_front(p, X, WA);
+  if (st != CAT_OK) return st;
+  return map_cuda(cudaMemcpyAsync(zstar, p->z, (size_t)B * H * N * sizeof(float),
+                                  cudaMemcpyDeviceToDevice, p->stream));
+}
+
+int cat_forward_host(cat_plan_t p, const void* X, const void* WA, const void* V, void* O, int B,
+                     int N, int D, int H, int dtype) {
+  if (!p) return CAT_ERR_INVALID_ARG;
+  int st = check_shape(p, B, N, D, H, dtype);
+  if (st != CAT_OK) return st;
+  if (B == 0) return CAT_OK;
+  if (!X || !WA || !V || !O) return CAT_ERR_INVALID_ARG;
+  const size_t es = dtype == CAT_BF16 ? 2 : 4;
+  const size_t nx = (size_t)B * N * D * es, nw = (size_t)D * H * es;
+  if (!p->hx) {
+    bool ok = cudaMalloc(&p->hx, nx) == cudaSuccess && cudaMalloc(&p->hwa, nw) == cudaSuccess &&
+              cudaMalloc(&p->hv, nx) == cudaSuccess && cudaMalloc(&p->ho, nx) == cudaSuccess;
+    if (!ok) {
+      cudaGetLastError();
+      cudaFree(p->hx); cudaFree(p->hwa); cudaFree(p->hv); cudaFree(p->ho);
+      p->hx = p->hwa = p->hv = p->ho = nullptr;
+      return CAT_ERR_ALLOC;
+    }
+  }
+  cudaError_t e = cudaMemcpyAsync(p->hx, X, nx, cudaMemcpyHostToDevice, p->stream);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(p->hwa, WA, nw, cudaMemcpyHostToDevice, p->stream);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(p->hv, V, nx, cudaMemcpyHostToDevice, p->stream);
+  if (e != cudaSuccess) return CAT_ERR_CUDA;
+  st = cat_forward(p, p->hx, p->hwa, p->hv, p->ho, B, N, D, H, dtype);
+  if (st != CAT_OK) return st;
+  e = cudaMemcpyAsync(O, p->ho, nx, cudaMemcpyDeviceToHost, p->stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(p->stream);
+  return map_cuda(e);
+}
+
+int cat_plan_sync(cat_plan_t p) {
+  if (!p) return CAT_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(p->stream) != cudaSuccess) return CAT_ERR_CUDA;
+  unsigned int word = 0;
+  if (cudaMemcpy(&word, p->status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return CAT_ERR_CUDA;
+  if (word != 0) {
+    if (std::getenv("CAT_LOG")) std::fprintf(stderr, "[cat] device status 0x%x\n", word);
+    cudaMemset(p->status, 0, sizeof(unsigned int));
+    return CAT_ERR_DEVICE_STATUS;
+  }
+  return CAT_OK;
+}
+
+int cat_plan_timing(cat_plan_t p, int max_calls) {
+  if (!p || max_calls < 0) return CAT_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(p->stream) != cudaSuccess) return CAT_ERR_CUDA;
+  free_events(p);
+  if (max_calls == 0) return CAT_OK;
+  p->ev = new (std::nothrow) cudaEvent_t[4 * (size_t)max_calls]();
+  if (!p->ev) return CAT_ERR_ALLOC;
+  p->timing_cap = max_calls;
+  for (int i = 0; i < 4 * max_calls; ++i) {
+    if (cudaEventCreate(&p->ev[i]) != cudaSuccess) {
+      free_events(p);
+      return CAT_ERR_CUDA;
+    }
+  }
+  return CAT_OK;
+}
+
+int cat_plan_stage_times(cat_plan_t p, float* ms, int cap, int* ncalls) {
+  if (!p || !ms || cap < 3) return CAT_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(p->stream) != cudaSuccess) return CAT_ERR_CUDA;
+  ms[0] = ms[1] = ms[2] = 0.f;
+  for (int c = 0; c < p->timing_n; ++c) {
+    cudaEvent_t* ev = p->ev + 4 * c;
+    for (int s = 0; s < 3; ++s) {
+      float t = 0.f;
+      if (cudaEventElapsedTime(&t, ev[s], ev[s + 1]) != cudaSuccess) return CAT_ERR_CUDA;
+      ms[s] += t;
+    }
+  }
+  if (ncalls) *ncalls = p->timing_n;
+  return CAT_OK;
+}
+
+int cat_plan_describe(cat_plan_t p, char* buf, int len) {
+  if (!p || !buf || len <= 0) return CAT_ERR_INVALID_ARG;
+  std::snprintf(buf, (size_t)len, "%s", p->desc);
+  return CAT_OK;
+}
+
+const char* cat_status_string(int status) {
+  switch (status) {
+    case CAT_OK: return "CAT_OK";
+    case CAT_ERR_INVALID_ARG: return "CAT_ERR_INVALID_ARG";
+    case CAT_ERR_UNSUPPORTED_N: return "CAT_ERR_UNSUPPORTED_N";
+    case CAT_ERR_MISALIGNED: return "CAT_ERR_MISALIGNED";
+    case CAT_ERR_PLAN_MISMATCH: return "CAT_ERR_PLAN_MISMATCH";
+    case CAT_ERR_ALLOC: return "CAT_ERR_ALLOC";
+    case CAT_ERR_CUDA: return "CAT_ERR_CUDA";
+    case CAT_ERR_DEVICE_STATUS: return "CAT_ERR_DEVICE_STATUS";
+    case CAT_ERR_ALIAS: return "CAT_ERR_ALIAS";
+    default: return "CAT_ERR_UNKNOWN";
+  }
+}
+
+}  // extern "C"

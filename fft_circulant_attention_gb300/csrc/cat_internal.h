@@ -1,0 +1,90 @@
+// Internal plan structure and kernel launchers of libcat (not part of the ABI).
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+
+#include "fft_device.cuh"
+
+namespace cat {
+
+enum Path { PATH_SMEM = 0, PATH_FOURSTEP = 1 };
+
+// Launch shape of the single-CTA shared-memory path (N up to 16384): one CTA
+// transforms G packed column pairs of one (b, h).
+struct SmemCfg {
+  int G;             // column pairs per CTA
+  int groups;        // CTAs per (b, h) = ceil(npair / G)
+  int tstride;       // shared-memory stride between transforms (complex)
+  int threads;       // CTA size of the conv kernel
+  size_t smem;       // dynamic shared memory of the conv kernel (bytes)
+  int spec_threads;  // CTA size of the softmax+spectrum kernel
+  size_t spec_smem;
+};
+
+// Four-step decomposition N = N1·N2 with row n = n1 + N1·n2 and bin
+// k = N2·k1 + k2.  Column pass A: per n1, DFT over n2 (length N2), then the
+// twiddle exp(-2πi n1·k2/N).  Row pass B: per k2, DFT over n1 (length N1),
+// product with the spectrum of z*, inverse DFT back to n1, conjugate
+// twiddle.  Column pass C: per n1, inverse DFT over k2 back to n2.
+// Scratch row layout per (b, h): [k2][n1][P] complex, P = npair + 1 signals
+// (the last one carries z* through pass A).
+struct FourStepCfg {
+  int N1, N2;
+  RadixPlan rp1, rp2;   // radices of N1 (pass B) and N2 (passes A, C)
+  int G, groups;        // pairs per CTA, CTAs per (b, h) along the pairs
+  int TA;               // n1 values per CTA in passes A and C (divides N1)
+  int TB;               // k2 values per CTA in pass B (divides N2)
+  int P;                // signals per scratch row = npair + 1
+  int threadsA, threadsB, threadsC;
+  size_t smemA, smemB, smemC;
+  int chunk_bh;         // (b, h) rows whose scratch is live at once
+};
+
+}  // namespace cat
+
+struct cat_plan_s {
+  int B, N, D, H, dtype;
+  int dh, npair;            // head width, packed pairs per head = ceil(dh/2)
+  int device;
+  cudaStream_t stream;
+  int path;
+  cat::RadixPlan rpN;       // radices of N (shared-memory path)
+  cat::SmemCfg sm;
+  cat::FourStepCfg fs;
+  int score_threads, score_tok;  // score kernel: CTA size, tokens per CTA
+  // workspace (device)
+  float* z;                 // [B, H, N] scores, then z* in place
+  float2* zf;               // [B, H, N] spectrum of z* divided by N (smem path)
+  float2* tw;               // [N] exp(-2πi j/N)
+  float2* scratch;          // four-step scratch, chunk_bh·N·P complex
+  size_t scratch_bytes;
+  unsigned int* status;     // device status word
+  size_t workspace_bytes;
+  // device staging for host-buffer calls (allocated at the first such call)
+  void* hx; void* hwa; void* hv; void* ho;
+  // stage timing: 4 events per recorded call (before score, after score,
+  // after softmax/spectrum, after the circulant product)
+  cudaEvent_t* ev;
+  int timing_cap, timing_n;
+  int launches;             // kernel launches per cat_forward
+  char desc[512];
+};
+
+// Heads the score kernel covers per pass over X for model width D.
+int score_heads_per_pass(int D);
+
+namespace cat {
+
+// Launchers (enqueue on plan->stream).  Each returns cudaGetLastError().
+cudaError_t launch_score(const cat_plan_s* p, const void* X, const void* WA);
+cudaError_t launch_softmax(const cat_plan_s* p);
+cudaError_t launch_softmax_spectrum(const cat_plan_s* p);
+cudaError_t launch_conv_smem(const cat_plan_s* p, const void* V, void* O);
+cudaError_t launch_fourstep_conv(const cat_plan_s* p, const void* V, void* O);
+
+// One-time kernel attribute setup (dynamic shared memory limits).
+cudaError_t setup_score_kernels(const cat_plan_s* p);
+cudaError_t setup_smem_kernels(const cat_plan_s* p);
+cudaError_t setup_fourstep_kernels(const cat_plan_s* p);
+
+}  // namespace cat

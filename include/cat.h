@@ -1,0 +1,164 @@
+/*
+ * cat.h — C ABI of the GB300 CAT forward library (libcat.so).
+ *
+ * CAT (circular-convolutional attention), as defined on the notes page
+ * "CAT: Circular-Convolutional Attention for Sub-Quadratic Transformers",
+ * section 方法详解 (method):
+ *   - 整体框架 (overall framework): CAT replaces multi-head self-attention;
+ *     its parameters are W_A (attention projection, one column per head) and
+ *     W_V (value projection).  V = X·W_V is an INPUT here: the value
+ *     projection is an ordinary dense GEMM and is not part of this library.
+ *   - 关键设计, "circulant attention matrix construction": per head h,
+ *     Z = X·W_A[:, h], Z* = softmax over the N tokens, and circ(Z*) is the
+ *     N x N circulant whose rows are successive cyclic shifts.
+ *   - 关键设计, "FFT acceleration": circ(Z*)·V = IFFT(FFT(Z*) ⊙ FFT(V)),
+ *     exact, O(N log N); this orientation gives circ(Z*)[i,j] = Z*[(i-j) mod N].
+ *
+ * Data layout (all dense, row-major, caller-owned device memory unless a
+ * function says otherwise):
+ *   X   [B, N, D]   tokens
+ *   W_A [D, H]      one score column per head
+ *   V   [B, N, D]   projected values; head h owns columns [h·D/H, (h+1)·D/H)
+ *   O   [B, N, D]   output, same layout as V
+ *   z*  [B, H, N]   fp32 softmax weights (only from cat_forward_zstar)
+ * X, W_A, V and O all have the plan's dtype.  All arithmetic is fp32:
+ * bf16 inputs are widened exactly, bf16 outputs are rounded to nearest-even.
+ *
+ * Every function returns a cat_status (0 = CAT_OK, negative = error) and
+ * never aborts, exits or traps.  GPU work is enqueued asynchronously on the
+ * plan's stream; errors raised by kernels are reported by cat_plan_sync.
+ */
+#ifndef CAT_H_
+#define CAT_H_
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Opaque plan: shape, dtype, stream, device workspace, twiddle tables. */
+typedef struct cat_plan_s *cat_plan_t;
+
+/* Storage type of X, W_A, V and O. */
+typedef enum { CAT_F32 = 0, CAT_BF16 = 1 } cat_dtype_t;
+
+/* Status codes. */
+enum {
+  CAT_OK = 0,
+  CAT_ERR_INVALID_ARG = -1,   /* bad shape, null pointer, D % H != 0, ...   */
+  CAT_ERR_UNSUPPORTED_N = -2, /* N has a prime factor > 7 or exceeds limits */
+  CAT_ERR_MISALIGNED = -3,    /* a device pointer is not 16-byte aligned    */
+  CAT_ERR_PLAN_MISMATCH = -4, /* call shape/dtype differs from the plan's   */
+  CAT_ERR_ALLOC = -5,         /* device or host allocation failed           */
+  CAT_ERR_CUDA = -6,          /* a CUDA runtime call or launch failed       */
+  CAT_ERR_DEVICE_STATUS = -7, /* a kernel reported an internal check failure*/
+  CAT_ERR_ALIAS = -8          /* O overlaps X, W_A or V                     */
+};
+
+/* Limits of this build. */
+#define CAT_MAX_N (1 << 22)   /* longest sequence                          */
+#define CAT_MAX_D 8192        /* widest model dimension                    */
+
+/*
+ * cat_plan_create — validate a problem shape and build everything the
+ * forward pass needs: the execution path (single-CTA shared-memory FFT for
+ * N up to 16384, four-step multi-CTA FFT above), fp32 twiddle tables
+ * computed in fp64 on the host, and the device workspace (scores, softmax
+ * weights, their spectra, four-step scratch).  The plan owns that memory.
+ *
+ *   out    : receives the plan (set to NULL on failure)
+ *   B      : batch size, >= 0 (B = 0 makes cat_forward a no-op)
+ *   N      : sequence length, 1 <= N <= CAT_MAX_N, 7-smooth (only prime
+ *            factors 2, 3, 5, 7)
+ *   D, H   : model width and head count, 1 <= H <= D <= CAT_MAX_D, D % H == 0
+ *   dtype  : CAT_F32 or CAT_BF16
+ *   stream : cudaStream_t to enqueue on (NULL = legacy default stream); the
+ *            caller keeps ownership and must keep it alive while the plan
+ *            uses it.
+ * Errors: CAT_ERR_INVALID_ARG, CAT_ERR_UNSUPPORTED_N, CAT_ERR_ALLOC,
+ * CAT_ERR_CUDA.  Uses the CUDA device current at the call.
+ */
+int cat_plan_create(cat_plan_t *out, int B, int N, int D, int H, int dtype,
+                    void *stream);
+
+/* Release a plan and its device memory.  NULL is accepted (no-op).
+ * Synchronises the plan's stream first.  Destroying twice is undefined. */
+int cat_plan_destroy(cat_plan_t plan);
+
+/* Change the stream later calls enqueue on. */
+int cat_plan_set_stream(cat_plan_t plan, void *stream);
+
+/*
+ * cat_forward — O = CAT(X, W_A, V) for every batch and head (both designs
+ * of the notes page cited above): scores, softmax over tokens, spectrum of
+ * z* once per (b, h), then per value column IFFT(FFT(z*) ⊙ FFT(v)).
+ *
+ * X, W_A, V: device pointers, read only.  O: device pointer, written.
+ * All four must be 16-byte aligned and O must not overlap the others.
+ * B, N, D, H, dtype must equal the plan's (CAT_ERR_PLAN_MISMATCH).
+ * Asynchronous on the plan's stream; the plan's workspace is reused, so two
+ * calls on one plan must not run concurrently on different streams.
+ */
+int cat_forward(cat_plan_t plan, const void *X, const void *W_A, const void *V,
+                void *O, int B, int N, int D, int H, int dtype);
+
+/*
+ * cat_forward_zstar — only the first two steps (score projection and
+ * softmax over the N tokens, "circulant attention matrix construction"):
+ * writes z* as fp32 [B, H, N] to the device pointer zstar (16-byte aligned).
+ */
+int cat_forward_zstar(cat_plan_t plan, const void *X, const void *W_A,
+                      float *zstar, int B, int N, int D, int H, int dtype);
+
+/*
+ * cat_forward_host — the same forward on HOST buffers: copies X, W_A, V to
+ * plan-owned device buffers (allocated at the first call and kept by the
+ * plan), runs cat_forward, copies O back, and synchronises the stream before
+ * returning.  Pinned (page-locked) host memory gives asynchronous copies;
+ * pageable memory works but is slower.  X, W_A, V are read, O is written.
+ */
+int cat_forward_host(cat_plan_t plan, const void *X, const void *W_A,
+                     const void *V, void *O, int B, int N, int D, int H,
+                     int dtype);
+
+/*
+ * cat_plan_sync — wait for the plan's stream, then read the device status
+ * word the kernels set when an internal check fails (a bad index that was
+ * skipped instead of accessed).  Returns CAT_OK, CAT_ERR_DEVICE_STATUS
+ * (the word is cleared after reporting) or CAT_ERR_CUDA.
+ */
+int cat_plan_sync(cat_plan_t plan);
+
+/*
+ * cat_plan_describe — copy a one-line, NUL-terminated description of the
+ * plan (path, factorisation, launch shapes, workspace bytes) into buf
+ * (capacity len bytes, truncated if needed).
+ */
+int cat_plan_describe(cat_plan_t plan, char *buf, int len);
+
+/*
+ * cat_plan_timing — stage timing for profiling.  max_calls > 0 arms the plan
+ * to record CUDA events around its three stages (score; softmax and, for
+ * N <= 16384, the spectrum of z*; the circulant product) on its stream for
+ * the next max_calls cat_forward calls, discarding earlier records;
+ * max_calls = 0 turns recording off.  Synchronises the plan's stream.
+ * The plan owns the events.  Errors: CAT_ERR_INVALID_ARG, CAT_ERR_ALLOC,
+ * CAT_ERR_CUDA.
+ */
+int cat_plan_timing(cat_plan_t plan, int max_calls);
+
+/*
+ * cat_plan_stage_times — wait for the plan's stream and write into ms[0..2]
+ * (host array, cap >= 3) the milliseconds each stage took, summed over the
+ * calls recorded since cat_plan_timing; *ncalls (may be NULL) receives how
+ * many calls that was.  Errors: CAT_ERR_INVALID_ARG, CAT_ERR_CUDA.
+ */
+int cat_plan_stage_times(cat_plan_t plan, float *ms, int cap, int *ncalls);
+
+/* Static string for a status code ("CAT_OK", "CAT_ERR_INVALID_ARG", ...). */
+const char *cat_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CAT_H_ */

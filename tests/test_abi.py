@@ -1,0 +1,105 @@
+"""The C ABI library loads and exports what include/cat.h declares (no GPU).
+
+Only calls that fail validation before touching CUDA are made here: they
+must return the documented status codes and never abort.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import fft_circulant_attention_gb300 as cat
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "cat.h")
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?\w+\s*\**\s*(cat_\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from fft_circulant_attention_gb300 import build
+    build.build()
+    return cat.lib()
+
+
+def test_header_declares_the_entry_points():
+    names = _declared()
+    for n in ("cat_plan_create", "cat_forward", "cat_plan_destroy", "cat_status_string"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+        assert name in cat.SIGNATURES, "binding lacks %s" % name
+
+
+def test_binding_names_match_header():
+    assert sorted(cat.SIGNATURES) == _declared()
+
+
+def test_status_strings(lib):
+    for code, name in cat.STATUS.items():
+        assert cat.cat_status_string(code) == name
+    assert cat.cat_status_string(12345) == "CAT_ERR_UNKNOWN"
+
+
+def _create(lib, *args):
+    h = ctypes.c_void_p()
+    st = lib.cat_plan_create(ctypes.byref(h), *args)
+    return st, h.value
+
+
+@pytest.mark.parametrize("args,code", [
+    ((1, 0, 64, 2, 0, None), cat.CAT_ERR_INVALID_ARG),      # N = 0
+    ((-1, 16, 64, 2, 0, None), cat.CAT_ERR_INVALID_ARG),    # B < 0
+    ((1, 16, 64, 3, 0, None), cat.CAT_ERR_INVALID_ARG),     # D % H != 0
+    ((1, 16, 4, 8, 0, None), cat.CAT_ERR_INVALID_ARG),      # H > D
+    ((1, 16, 64, 0, 0, None), cat.CAT_ERR_INVALID_ARG),     # H = 0
+    ((1, 16, 64, 2, 7, None), cat.CAT_ERR_INVALID_ARG),     # bad dtype
+    ((1, 11, 64, 2, 0, None), cat.CAT_ERR_UNSUPPORTED_N),   # prime factor 11
+    ((1, 13 * 16, 64, 2, 0, None), cat.CAT_ERR_UNSUPPORTED_N),
+    ((1, 1 << 23, 64, 2, 0, None), cat.CAT_ERR_UNSUPPORTED_N),  # above CAT_MAX_N
+    ((1, 16, 1 << 15, 2, 0, None), cat.CAT_ERR_INVALID_ARG),    # above CAT_MAX_D
+])
+def test_create_rejects_bad_shapes(lib, args, code):
+    st, h = _create(lib, *args)
+    assert st == code
+    assert not h
+
+
+def test_null_out_pointer(lib):
+    assert lib.cat_plan_create(None, 1, 16, 64, 2, 0, None) == cat.CAT_ERR_INVALID_ARG
+
+
+def test_null_plan_calls(lib):
+    assert lib.cat_plan_destroy(None) == cat.CAT_OK
+    assert lib.cat_forward(None, None, None, None, None, 1, 16, 64, 2, 0) == cat.CAT_ERR_INVALID_ARG
+    assert lib.cat_forward_zstar(None, None, None, None, 1, 16, 64, 2, 0) == cat.CAT_ERR_INVALID_ARG
+    assert lib.cat_forward_host(None, None, None, None, None, 1, 16, 64, 2, 0) == cat.CAT_ERR_INVALID_ARG
+    assert lib.cat_plan_sync(None) == cat.CAT_ERR_INVALID_ARG
+    assert lib.cat_plan_set_stream(None, None) == cat.CAT_ERR_INVALID_ARG
+    buf = ctypes.create_string_buffer(16)
+    assert lib.cat_plan_describe(None, buf, 16) == cat.CAT_ERR_INVALID_ARG
+
+
+def test_python_raises_caterror(lib):
+    with pytest.raises(cat.CatError) as e:
+        cat.cat_plan_create(1, 11, 64, 2, "f32")
+    assert e.value.status == cat.CAT_ERR_UNSUPPORTED_N
+
+
+def test_dtype_codes():
+    import torch
+    assert cat.dtype_code(torch.float32) == cat.CAT_F32
+    assert cat.dtype_code(torch.bfloat16) == cat.CAT_BF16
+    assert cat.dtype_code("bf16") == cat.CAT_BF16
+    with pytest.raises(ValueError):
+        cat.dtype_code(torch.float16)

@@ -1,0 +1,248 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle.
+
+Every case draws seeded synthetic inputs, runs cat_forward on cuda:0 and
+compares element by element with the oracle (the plain definitions of the
+CAT notes page, section 方法详解: score, softmax over tokens, circulant
+product).  Bounds: O within 2e-5·max|V| (fp32 storage) or 8e-3·max|V|
+(bf16 storage); z* within 1e-5 relative.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import fft_circulant_attention_gb300 as cat
+import oracle
+import synth
+from _gpu_helpers import check_out, check_zstar, parity, run_gpu, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _needs_gpu(cuda_device):
+    from fft_circulant_attention_gb300 import build
+    build.build()
+    yield
+
+
+# ---------------------------------------------------------------- workloads
+
+SMALL_CONFIGS = {
+    "tiny": dict(B=1, N=256, D=64, H=2, dtype="f32"),
+    "vit196": dict(B=64, N=196, D=384, H=6, dtype="f32"),
+    "gpt2_f32": dict(B=16, N=1024, D=768, H=12, dtype="f32"),
+    "gpt2_bf16": dict(B=16, N=1024, D=768, H=12, dtype="bf16"),
+    "gpt2_peaked": dict(B=16, N=1024, D=768, H=12, dtype="f32", wa_scale=8.0),
+    "gpt2_peaked_bf16": dict(B=16, N=1024, D=768, H=12, dtype="bf16", wa_scale=8.0),
+}
+
+
+@pytest.mark.parametrize("name", list(SMALL_CONFIGS))
+def test_workload_parity(name):
+    cfg = dict(SMALL_CONFIGS[name])
+    errO, errZ = parity(**cfg)
+    print("%s: max|dO|/max|V| = %.2e, max rel dz* = %.2e" % (name, errO, errZ))
+
+
+def _sampled_rows(N, k, seed):
+    rng = np.random.default_rng(seed)
+    rows = {0, 1, N // 2, N - 1}
+    rows.update(int(r) for r in rng.choice(N, size=k, replace=False))
+    return sorted(rows)
+
+
+@pytest.mark.parametrize("name,nrows", [("long16k", 28), ("long128k", 12)])
+def test_long_workload_sampled(name, nrows):
+    """Full-size long-sequence workloads in the benchmark's launch shape:
+    all of z* against the oracle, and O at sampled rows (every batch and
+    column) against the O(N) per-element definition."""
+    c = synth.CONFIGS[name]
+    X, WA, V = synth.make_inputs(c["B"], c["N"], c["D"], c["H"], c["dtype"], seed=0)
+    O, zs = run_gpu(X, WA, V, c["dtype"])
+    zs_ref = oracle.zstar(X, WA)
+    errZ = check_zstar(zs, zs_ref)
+    rows = _sampled_rows(c["N"], nrows, 1)
+    O_ref = oracle.circ_direct_rows(zs_ref, V, rows)
+    errO = check_out(O[:, rows], O_ref, V, c["dtype"])
+    # Column sums are kept by a circulant whose columns sum to one.
+    Vs = V.double().sum(1).numpy()
+    Os = O.double().sum(1).numpy()
+    assert np.abs(Os - Vs).max() <= 8e-3 * np.abs(V.double().numpy()).max() * np.sqrt(c["N"])
+    print("%s: max|dO|/max|V| = %.2e (%d rows), max rel dz* = %.2e" % (name, errO, len(rows), errZ))
+
+
+# --------------------------------------------------------- length sweeps
+
+SMEM_NS = [1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 12, 14, 15, 16, 21, 25, 27, 32, 35, 49, 64, 96,
+           100, 125, 128, 196, 210, 243, 256, 343, 512, 1000, 1024, 2048, 2401, 4096,
+           8192, 15625, 16384]
+
+
+@pytest.mark.parametrize("N", SMEM_NS)
+def test_length_sweep_f32(N):
+    mode = "direct" if N <= 4096 else "fft"
+    parity(2, N, 8, 2, "f32", seed=N, mode=mode)
+
+
+@pytest.mark.parametrize("N", [7, 64, 196, 1000, 16384])
+def test_length_sweep_bf16(N):
+    parity(1, N, 16, 2, "bf16", seed=N, mode="direct" if N <= 4096 else "fft")
+
+
+FOURSTEP_NS = [32768, 49152, 65536, 3 * 5 * 7 * 512]
+
+
+@pytest.mark.parametrize("N", FOURSTEP_NS)
+def test_fourstep_lengths(N):
+    """Lengths above the single-CTA limit take the four-step path."""
+    parity(1, N, 8, 2, "f32", seed=N, mode="fft")
+
+
+@pytest.fixture
+def force_fourstep():
+    os.environ["CAT_FORCE_PATH"] = "fourstep"
+    yield
+    del os.environ["CAT_FORCE_PATH"]
+
+
+@pytest.mark.parametrize("N,D,H,dtype", [
+    (4, 8, 2, "f32"), (12, 8, 2, "f32"), (64, 16, 2, "f32"), (196, 24, 3, "f32"),
+    (1024, 64, 2, "bf16"), (4096, 16, 4, "f32"), (16384, 8, 1, "f32"),
+    (100, 6, 2, "bf16"), (256, 18, 3, "f32"),
+])
+def test_fourstep_forced(force_fourstep, N, D, H, dtype):
+    """The four-step path on short sequences, where the oracle is cheap."""
+    with cat.Plan(1, N, D, H, dtype) as p:
+        assert "fourstep" in p.describe()
+    parity(2, N, D, H, dtype, seed=N + D, mode="direct" if N <= 4096 else "fft")
+
+
+# ------------------------------------------------------------- edge cases
+
+@pytest.mark.parametrize("B,N,D,H,dtype", [
+    (2, 64, 6, 2, "f32"),      # odd head width (a half pair per head)
+    (2, 64, 9, 3, "bf16"),     # odd head width, bf16, unaligned pairs
+    (1, 128, 64, 32, "f32"),   # more than 16 heads (two score passes)
+    (1, 128, 40, 20, "bf16"),
+    (3, 50, 6, 1, "f32"),      # D not a multiple of the vector width
+    (1, 1, 8, 2, "f32"),       # single token
+    (1, 2, 2, 2, "bf16"),      # head width 1
+    (5, 96, 256, 1, "bf16"),   # one head owning all columns
+])
+def test_shapes(B, N, D, H, dtype):
+    parity(B, N, D, H, dtype, seed=B * 1000 + N, mode="direct")
+
+
+def test_single_token_is_identity():
+    X, WA, V = synth.make_inputs(3, 1, 16, 4, "f32", seed=3)
+    O, zs = run_gpu(X, WA, V, "f32")
+    assert torch.equal(zs, torch.ones_like(zs))
+    assert torch.equal(O, V)
+
+
+def test_empty_batch():
+    with cat.Plan(0, 64, 8, 2, "f32") as p:
+        X = torch.empty((0, 64, 8), device="cuda:0")
+        W = torch.empty((8, 2), device="cuda:0")
+        O = p.forward(X, W, X.clone())
+        p.sync()
+    assert O.shape == (0, 64, 8)
+
+
+def _one_hot_inputs(N, D, H, shifts, dtype):
+    _, _, V = synth.make_inputs(1, N, D, H, dtype, seed=11)
+    X = torch.zeros((1, N, D))
+    WA = torch.zeros((D, H))
+    for h, s in enumerate(shifts):
+        WA[h, h] = 1.0
+        X[0, :, h] = -100.0
+        X[0, s, h] = 100.0
+    return X.to(V.dtype), WA.to(V.dtype), V
+
+
+@pytest.mark.parametrize("N,dtype", [(40, "f32"), (196, "bf16"), (4096, "f32"), (32768, "bf16")])
+def test_one_hot_is_cyclic_shift(N, dtype):
+    """z* one-hot at s_h gives O[i] = V[(i - s_h) mod N] for head h."""
+    D, H = 8, 4
+    shifts = [0, 1, 7, N - 3]
+    X, WA, V = _one_hot_inputs(N, D, H, shifts, dtype)
+    O, zs = run_gpu(X, WA, V, dtype)
+    dh = D // H
+    vmax = float(V.double().abs().max())
+    tol = 2e-5 if dtype == "f32" else 8e-3
+    for h, s in enumerate(shifts):
+        assert float(zs[0, h, s]) == 1.0
+        cols = slice(h * dh, (h + 1) * dh)
+        ref = torch.roll(V[0, :, cols].double(), s, dims=0)
+        assert float((O[0, :, cols].double() - ref).abs().max()) <= tol * vmax
+
+
+@pytest.mark.parametrize("N,dtype", [(27, "f32"), (1024, "bf16"), (65536, "f32")])
+def test_uniform_gives_column_mean(N, dtype):
+    X, WA, V = synth.make_inputs(2, N, 12, 3, dtype, seed=12)
+    WA = torch.zeros_like(WA)
+    O, zs = run_gpu(X, WA, V, dtype)
+    assert float((zs.double() - 1.0 / N).abs().max()) <= 1e-5 / N
+    ref = V.double().mean(1, keepdim=True).expand_as(O)
+    tol = 2e-5 if dtype == "f32" else 8e-3
+    assert float((O.double() - ref).abs().max()) <= tol * float(V.double().abs().max())
+
+
+# ------------------------------------------------------- API behaviour
+
+def test_host_buffer_entry_matches_device_entry():
+    B, N, D, H = 2, 1024, 64, 4
+    X, WA, V = synth.make_inputs(B, N, D, H, "bf16", seed=5)
+    Od, _ = run_gpu(X, WA, V, "bf16", want_zstar=False)
+    Xp, Wp, Vp = (t.pin_memory() for t in (X, WA, V))
+    Oh = torch.empty_like(Vp).pin_memory()
+    with cat.Plan(B, N, D, H, "bf16") as p:
+        p.forward_host(Xp, Wp, Vp, Oh)
+        p.forward_host(Xp, Wp, Vp, Oh)   # staging buffers are reused
+        p.sync()
+    assert torch.equal(Oh, Od)
+
+
+def test_deterministic():
+    X, WA, V = to_dev(*synth.make_inputs(2, 2048, 64, 4, "f32", seed=6))
+    with cat.Plan(2, 2048, 64, 4, "f32") as p:
+        a = p.forward(X, WA, V).clone()
+        for _ in range(3):
+            assert torch.equal(p.forward(X, WA, V), a)
+        p.sync()
+
+
+def test_error_paths_leave_context_usable():
+    X, WA, V = to_dev(*synth.make_inputs(1, 64, 8, 2, "f32", seed=7))
+    with cat.Plan(1, 64, 8, 2, "f32") as p:
+        O = torch.empty_like(V)
+        raw = torch.empty(V.numel() + 1, device="cuda:0")
+        with pytest.raises(cat.CatError) as e:       # misaligned by 4 bytes
+            cat.cat_forward(p.handle, X, WA, V, raw.data_ptr() + 4, 1, 64, 8, 2, 0)
+        assert e.value.status == cat.CAT_ERR_MISALIGNED
+        with pytest.raises(cat.CatError) as e:       # shape differs from the plan
+            cat.cat_forward(p.handle, X, WA, V, O, 1, 32, 8, 2, 0)
+        assert e.value.status == cat.CAT_ERR_PLAN_MISMATCH
+        with pytest.raises(cat.CatError) as e:       # O overlaps V
+            cat.cat_forward(p.handle, X, WA, V, V, 1, 64, 8, 2, 0)
+        assert e.value.status == cat.CAT_ERR_ALIAS
+        with pytest.raises(cat.CatError) as e:
+            cat.cat_forward(p.handle, None, WA, V, O, 1, 64, 8, 2, 0)
+        assert e.value.status == cat.CAT_ERR_INVALID_ARG
+        p.forward(X, WA, V, O)
+        p.sync()
+    O_ref, _ = oracle.forward(X.cpu(), WA.cpu(), V.cpu(), mode="direct")
+    assert float(np.abs(O.cpu().double().numpy() - O_ref).max()) <= 2e-5 * float(V.abs().max())
+
+
+def test_plan_on_a_side_stream():
+    s = torch.cuda.Stream()
+    X, WA, V = to_dev(*synth.make_inputs(2, 512, 32, 2, "f32", seed=8))
+    with torch.cuda.stream(s):
+        with cat.Plan(2, 512, 32, 2, "f32", stream=s) as p:
+            O = p.forward(X, WA, V)
+            p.sync()
+    O_ref, _ = oracle.forward(X.cpu(), WA.cpu(), V.cpu(), mode="direct")
+    assert float(np.abs(O.cpu().double().numpy() - O_ref).max()) <= 2e-5 * float(V.abs().max())
