@@ -127,7 +127,8 @@ void free_events(cat_plan_s* p) {
 void free_plan(cat_plan_s* p) {
   if (!p) return;
   free_events(p);
-  cudaFree(p->z);
+  cudaFree(p->z2);
+  cudaFree(p->zs);
   cudaFree(p->zf);
   cudaFree(p->tw);
   cudaFree(p->scratch);
@@ -273,13 +274,14 @@ int cat_plan_create(cat_plan_t* out, int B, int N, int D, int H, int dtype, void
     if (bytes == 0) bytes = 16;
     return cudaMalloc(ptr, bytes) == cudaSuccess;
   };
-  bool ok = alloc((void**)&p->z, rowsN * sizeof(float)) &&
+  bool ok = alloc((void**)&p->z2, rowsN * sizeof(float2)) &&
+            alloc((void**)&p->zs, rowsN * sizeof(float)) &&
             alloc((void**)&p->tw, (size_t)N * sizeof(float2)) &&
             alloc((void**)&p->status, sizeof(unsigned int));
   if (ok && p->path == cat::PATH_SMEM) ok = alloc((void**)&p->zf, rowsN * sizeof(float2));
   if (ok && p->path == cat::PATH_FOURSTEP) ok = alloc((void**)&p->scratch, p->scratch_bytes);
   if (!ok) { cudaGetLastError(); free_plan(p); return CAT_ERR_ALLOC; }
-  p->workspace_bytes = rowsN * sizeof(float) + (size_t)N * sizeof(float2) +
+  p->workspace_bytes = rowsN * (sizeof(float) + sizeof(float2)) + (size_t)N * sizeof(float2) +
                        (p->zf ? rowsN * sizeof(float2) : 0) + p->scratch_bytes;
 
   // Twiddle table exp(-2πi j/N), evaluated in fp64 and rounded once.
@@ -356,7 +358,7 @@ int cat_forward_zstar(cat_plan_t p, const void* X, const void* WA, float* zstar,
   if (((uintptr_t)X | (uintptr_t)WA | (uintptr_t)zstar) & 15) return CAT_ERR_MISALIGNED;
   st = run_front(p, X, WA);
   if (st != CAT_OK) return st;
-  return map_cuda(cudaMemcpyAsync(zstar, p->z, (size_t)B * H * N * sizeof(float),
+  return map_cuda(cudaMemcpyAsync(zstar, p->zs, (size_t)B * H * N * sizeof(float),
                                   cudaMemcpyDeviceToDevice, p->stream));
 }
 

@@ -53,7 +53,8 @@ struct cat_plan_s {
   cat::FourStepCfg fs;
   int score_threads, score_tok;  // score kernel: CTA size, tokens per CTA
   // workspace (device)
-  float* z;                 // [B, H, N] scores, then z* in place
+  float2* z2;               // [B, H, N] scores as double-float (hi, lo)
+  float* zs;                // [B, H, N] z* (softmax weights)
   float2* zf;               // [B, H, N] spectrum of z* divided by N (smem path)
   float2* tw;               // [N] exp(-2πi j/N)
   float2* scratch;          // four-step scratch, chunk_bh·N·P complex

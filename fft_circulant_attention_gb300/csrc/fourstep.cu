@@ -235,7 +235,7 @@ static cudaError_t run_t(const cat_plan_s* p, const T* V, T* O) {
     int nb = rows - bh0 < f.chunk_bh ? rows - bh0 : f.chunk_bh;
     int ga = nb * (f.N1 / f.TA) * f.groups;
     fs_pass_a<T><<<ga, f.threadsA, f.smemA, p->stream>>>(
-        V, p->z, p->scratch, p->tw, f.rp2, p->N, f.N1, p->D, p->H, p->dh, p->npair, f.G,
+        V, p->zs, p->scratch, p->tw, f.rp2, p->N, f.N1, p->D, p->H, p->dh, p->npair, f.G,
         f.groups, f.TA, f.P, bh0, p->status);
     int gb = nb * (f.N2 / f.TB) * f.groups;
     fs_pass_b<<<gb, f.threadsB, f.smemB, p->stream>>>(p->scratch, p->tw, f.rp1, p->N, f.N2,

@@ -52,17 +52,35 @@ template <> struct Vec16<__nv_bfloat16> {
   }
 };
 
+// Adds p to the double-float accumulator (hi, lo): hi + p is split exactly
+// into its rounded sum and rounding error (Knuth's TwoSum), the error joins
+// lo.
+__device__ __forceinline__ void two_sum_acc(float& hi, float& lo, float p) {
+  float s = hi + p;
+  float bp = s - hi;
+  float err = (hi - (s - bp)) + (p - bp);
+  hi = s;
+  lo += err;
+}
+
 // One pass over X computes HT heads [h0, h0 + HT) for kScoreTokPerCta
 // tokens of one batch.  W_A's HT columns sit in shared memory as fp32
 // [D][HP] (HP = HT rounded up to 4); every lane of a warp reads the same
 // W_A row at the same time (a broadcast).  Each thread owns two tokens and
 // walks their rows in 16-byte vectors when the layout allows (VEC), else
-// element by element.  Accumulation is fp32 FMA in increasing d.
+// element by element.
+// Accuracy: the products of each run of kChunk consecutive d are summed by
+// fp32 FMA into a fresh register; the chunk sums are combined with TwoSum
+// into a double-float (hi, lo), so the result carries no rounding from the
+// large running total.  z is stored as the pair (hi, lo).
+constexpr int kChunk = 16;
+
 template <typename T, int HT, bool VEC>
 __global__ void __launch_bounds__(kScoreThreads)
-score_kernel(const T* __restrict__ X, const T* __restrict__ WA, float* __restrict__ z,
+score_kernel(const T* __restrict__ X, const T* __restrict__ WA, float2* __restrict__ z,
              int N, int D, int H, int h0) {
   constexpr int HP = (HT + 3) & ~3;
+  constexpr int TP = kScoreTokPerThread;
   extern __shared__ float4 ws4[];
   float* ws = reinterpret_cast<float*>(ws4);
   const int b = blockIdx.y;
@@ -72,30 +90,38 @@ score_kernel(const T* __restrict__ X, const T* __restrict__ WA, float* __restric
   }
   __syncthreads();
   const int nbase = blockIdx.x * kScoreTokPerCta + threadIdx.x;
-  int nn[kScoreTokPerThread];
-  bool ok[kScoreTokPerThread];
+  int nn[TP];
+  bool ok[TP];
 #pragma unroll
-  for (int t = 0; t < kScoreTokPerThread; ++t) {
+  for (int t = 0; t < TP; ++t) {
     nn[t] = nbase + t * kScoreThreads;
     ok[t] = nn[t] < N;
   }
-  float acc[kScoreTokPerThread][HT];
+  float hi[TP][HT], lo[TP][HT];
 #pragma unroll
-  for (int t = 0; t < kScoreTokPerThread; ++t)
+  for (int t = 0; t < TP; ++t)
 #pragma unroll
-    for (int h = 0; h < HT; ++h) acc[t][h] = 0.f;
+    for (int h = 0; h < HT; ++h) hi[t][h] = lo[t][h] = 0.f;
 
-  const T* xr[kScoreTokPerThread];
+  const T* xr[TP];
 #pragma unroll
-  for (int t = 0; t < kScoreTokPerThread; ++t)
-    xr[t] = X + ((size_t)b * N + (ok[t] ? nn[t] : 0)) * D;
+  for (int t = 0; t < TP; ++t) xr[t] = X + ((size_t)b * N + (ok[t] ? nn[t] : 0)) * D;
 
-  if (VEC) {
-    constexpr int V = Vec16<T>::n;
-    for (int d0 = 0; d0 < D; d0 += V) {
-      float xv[kScoreTokPerThread][V];
+  constexpr int V = VEC ? Vec16<T>::n : 1;
+  for (int c0 = 0; c0 < D; c0 += kChunk) {
+    const int c1 = min(D, c0 + kChunk);
+    float part[TP][HT];
 #pragma unroll
-      for (int t = 0; t < kScoreTokPerThread; ++t) Vec16<T>::load(xr[t] + d0, xv[t]);
+    for (int t = 0; t < TP; ++t)
+#pragma unroll
+      for (int h = 0; h < HT; ++h) part[t][h] = 0.f;
+    for (int d0 = c0; d0 < c1; d0 += V) {
+      float xv[TP][V];
+#pragma unroll
+      for (int t = 0; t < TP; ++t) {
+        if (VEC) Vec16<T>::load(xr[t] + d0, xv[t]);
+        else xv[t][0] = ld_elem(xr[t] + d0);
+      }
 #pragma unroll
       for (int j = 0; j < V; ++j) {
         const float4* wrow = ws4 + (size_t)(d0 + j) * (HP / 4);
@@ -107,32 +133,24 @@ score_kernel(const T* __restrict__ X, const T* __restrict__ WA, float* __restric
           for (int e = 0; e < 4; ++e) {
             if (q * 4 + e < HT) {
 #pragma unroll
-              for (int t = 0; t < kScoreTokPerThread; ++t)
-                acc[t][q * 4 + e] = fmaf(xv[t][j], wv[e], acc[t][q * 4 + e]);
+              for (int t = 0; t < TP; ++t)
+                part[t][q * 4 + e] = fmaf(xv[t][j], wv[e], part[t][q * 4 + e]);
             }
           }
         }
       }
     }
-  } else {
-    for (int d = 0; d < D; ++d) {
-      float xv[kScoreTokPerThread];
 #pragma unroll
-      for (int t = 0; t < kScoreTokPerThread; ++t) xv[t] = ld_elem(xr[t] + d);
-      const float* wrow = ws + (size_t)d * HP;
+    for (int t = 0; t < TP; ++t)
 #pragma unroll
-      for (int h = 0; h < HT; ++h) {
-        float w = wrow[h];
-#pragma unroll
-        for (int t = 0; t < kScoreTokPerThread; ++t) acc[t][h] = fmaf(xv[t], w, acc[t][h]);
-      }
-    }
+      for (int h = 0; h < HT; ++h) two_sum_acc(hi[t][h], lo[t][h], part[t][h]);
   }
 #pragma unroll
-  for (int t = 0; t < kScoreTokPerThread; ++t) {
+  for (int t = 0; t < TP; ++t) {
     if (ok[t]) {
 #pragma unroll
-      for (int h = 0; h < HT; ++h) z[((size_t)b * H + h0 + h) * N + nn[t]] = acc[t][h];
+      for (int h = 0; h < HT; ++h)
+        z[((size_t)b * H + h0 + h) * N + nn[t]] = make_float2(hi[t][h], lo[t][h]);
     }
   }
 }
@@ -150,7 +168,7 @@ static cudaError_t run_score(const cat_plan_s* p, const T* X, const T* WA, int h
   auto k = score_kernel<T, HT, VEC>;
   if (setup) return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   dim3 grid((p->N + kScoreTokPerCta - 1) / kScoreTokPerCta, p->B);
-  k<<<grid, kScoreThreads, smem, p->stream>>>(X, WA, p->z, p->N, p->D, p->H, h0);
+  k<<<grid, kScoreThreads, smem, p->stream>>>(X, WA, p->z2, p->N, p->D, p->H, h0);
   return cudaGetLastError();
 }
 
@@ -190,35 +208,53 @@ cudaError_t launch_score(const cat_plan_s* p, const void* X, const void* WA) {
   return score_dispatch(p, (const float*)X, (const float*)WA, false);
 }
 
-// Softmax over the N tokens of each (b, h) row, in place (z -> z*), one CTA
-// per row, streaming through global memory: max, then sum of exp(z - max),
-// then z* = exp(z - max) / sum.
-__global__ void __launch_bounds__(1024) softmax_kernel(float* __restrict__ z, int N) {
+// exp(z - m) for a score held as the double-float (hi, lo): the difference
+// hi - m is split exactly (TwoSum) and its rounding error, plus lo, enters
+// as the first-order factor (1 + delta).
+__device__ __forceinline__ float exp_shifted(float2 zhl, float m) {
+  float s = zhl.x - m;
+  float bp = s - zhl.x;
+  float err = (zhl.x - (s - bp)) + (-m - bp);
+  float e = expf(s);
+  return fmaf(e, err + zhl.y, e);
+}
+
+// Softmax over the N tokens of each (b, h) row, one CTA per row, streaming
+// through global memory: m = max of the scores, S = sum of exp(z - m), then
+// z* = exp(z - m) / S written to zs.
+__global__ void __launch_bounds__(1024)
+softmax_kernel(const float2* __restrict__ z, float* __restrict__ zs, int N) {
   __shared__ float red[32];
-  float* row = z + (size_t)blockIdx.x * N;
+  const float2* row = z + (size_t)blockIdx.x * N;
+  float* out = zs + (size_t)blockIdx.x * N;
   float m = -INFINITY;
-  for (int n = threadIdx.x; n < N; n += blockDim.x) m = fmaxf(m, row[n]);
+  for (int n = threadIdx.x; n < N; n += blockDim.x) m = fmaxf(m, row[n].x);
   m = block_reduce<true>(m, red);
   float s = 0.f;
-  for (int n = threadIdx.x; n < N; n += blockDim.x) s += expf(row[n] - m);
+  for (int n = threadIdx.x; n < N; n += blockDim.x) {
+    float e = exp_shifted(row[n], m);
+    out[n] = e;
+    s += e;
+  }
   s = block_reduce<false>(s, red);
   const float inv = 1.0f / s;
-  for (int n = threadIdx.x; n < N; n += blockDim.x) row[n] = expf(row[n] - m) * inv;
+  for (int n = threadIdx.x; n < N; n += blockDim.x) out[n] *= inv;
 }
 
 cudaError_t launch_softmax(const cat_plan_s* p) {
   int rows = p->B * p->H;
   if (rows == 0) return cudaSuccess;
-  softmax_kernel<<<rows, 1024, 0, p->stream>>>(p->z, p->N);
+  softmax_kernel<<<rows, 1024, 0, p->stream>>>(p->z2, p->zs, p->N);
   return cudaGetLastError();
 }
 
 // Softmax of one (b, h) row held in shared memory, then its spectrum:
 // zf[k] = (1/N) sum_n z*[n] exp(-2πi kn/N).  One CTA per row; N <= 16384.
-// z* is also written back over the scores.
+// z* is also written to zs.
 __global__ void __launch_bounds__(1024)
-softmax_spectrum_kernel(float* __restrict__ z, float2* __restrict__ zf, RadixPlan rp,
-                        const float2* __restrict__ W, unsigned int* status) {
+softmax_spectrum_kernel(const float2* __restrict__ z, float* __restrict__ zs,
+                        float2* __restrict__ zf, RadixPlan rp, const float2* __restrict__ W,
+                        unsigned int* status) {
   extern __shared__ float2 sbuf[];
   __shared__ float red[32];
   const int N = rp.L;
@@ -226,32 +262,33 @@ softmax_spectrum_kernel(float* __restrict__ z, float2* __restrict__ zf, RadixPla
     report(status, 0x101);
     return;
   }
-  float* row = z + (size_t)blockIdx.x * N;
+  const float2* row = z + (size_t)blockIdx.x * N;
   float m = -INFINITY;
   for (int n = threadIdx.x; n < N; n += blockDim.x) {
-    float v = row[n];
-    sbuf[n].x = v;
-    m = fmaxf(m, v);
+    float2 v = row[n];
+    sbuf[n] = v;
+    m = fmaxf(m, v.x);
   }
   m = block_reduce<true>(m, red);
   float s = 0.f;
   for (int n = threadIdx.x; n < N; n += blockDim.x) {
-    float e = expf(sbuf[n].x - m);
+    float e = exp_shifted(sbuf[n], m);
     sbuf[n].x = e;
     s += e;
   }
   s = block_reduce<false>(s, red);
   const float inv = 1.0f / s;
+  float* out = zs + (size_t)blockIdx.x * N;
   for (int n = threadIdx.x; n < N; n += blockDim.x) {
     float v = sbuf[n].x * inv;
-    row[n] = v;
+    out[n] = v;
     sbuf[n] = make_float2(v, 0.f);
   }
   __syncthreads();
   block_fft<false>(sbuf, rp, 1, N, W, 1);
   const float invN = 1.0f / (float)N;
-  float2* out = zf + (size_t)blockIdx.x * N;
-  for (int k = threadIdx.x; k < N; k += blockDim.x) out[k] = cscale(sbuf[k], invN);
+  float2* spec = zf + (size_t)blockIdx.x * N;
+  for (int k = threadIdx.x; k < N; k += blockDim.x) spec[k] = cscale(sbuf[k], invN);
 }
 
 cudaError_t setup_score_kernels(const cat_plan_s* p) {
@@ -269,7 +306,7 @@ cudaError_t launch_softmax_spectrum(const cat_plan_s* p) {
   int rows = p->B * p->H;
   if (rows == 0) return cudaSuccess;
   softmax_spectrum_kernel<<<rows, p->sm.spec_threads, p->sm.spec_smem, p->stream>>>(
-      p->z, p->zf, p->rpN, p->tw, p->status);
+      p->z2, p->zs, p->zf, p->rpN, p->tw, p->status);
   return cudaGetLastError();
 }
 
