@@ -76,12 +76,34 @@ int score_heads_per_pass(int D);
 
 namespace cat {
 
+// Let `kernel` use all the dynamic shared memory the current device allows
+// a block (its opt-in limit minus the kernel's static shared memory).  The
+// limit is a property of the kernel, shared by every plan in the process,
+// so it is always raised to the device maximum and never lowered to one
+// plan's need.
+template <typename K>
+cudaError_t allow_max_smem(K kernel) {
+  int dev = 0, optin = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  cudaFuncAttributes a;
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, kernel);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             optin - (int)a.sharedSizeBytes);
+  return e;
+}
+
 // Launchers (enqueue on plan->stream).  Each returns cudaGetLastError().
 cudaError_t launch_score(const cat_plan_s* p, const void* X, const void* WA);
 cudaError_t launch_softmax(const cat_plan_s* p);
 cudaError_t launch_softmax_spectrum(const cat_plan_s* p);
 cudaError_t launch_conv_smem(const cat_plan_s* p, const void* V, void* O);
 cudaError_t launch_fourstep_conv(const cat_plan_s* p, const void* V, void* O);
+
+// Shape validation and shared-memory-path configuration without allocation.
+int validate(int B, int N, int D, int H, int dtype);
+int configure_smem_path(cat_plan_s* p);
 
 // One-time kernel attribute setup (dynamic shared memory limits).
 cudaError_t setup_score_kernels(const cat_plan_s* p);

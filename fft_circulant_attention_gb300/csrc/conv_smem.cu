@@ -83,11 +83,8 @@ conv_smem_kernel(const T* __restrict__ V, T* __restrict__ O, const float2* __res
 }
 
 cudaError_t setup_smem_kernels(const cat_plan_s* p) {
-  if (p->dtype == 1)
-    return cudaFuncSetAttribute(conv_smem_kernel<__nv_bfloat16>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p->sm.smem);
-  return cudaFuncSetAttribute(conv_smem_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)p->sm.smem);
+  if (p->dtype == 1) return allow_max_smem(conv_smem_kernel<__nv_bfloat16>);
+  return allow_max_smem(conv_smem_kernel<float>);
 }
 
 cudaError_t launch_conv_smem(const cat_plan_s* p, const void* V, void* O) {

@@ -213,14 +213,11 @@ fs_pass_c(const float2* __restrict__ scr, T* __restrict__ O, const float2* __res
 
 template <typename T>
 static cudaError_t setup_t(const cat_plan_s* p) {
-  cudaError_t e = cudaFuncSetAttribute(fs_pass_a<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)p->fs.smemA);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(fs_pass_c<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)p->fs.smemC);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(fs_pass_b, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)p->fs.smemB);
+  (void)p;
+  cudaError_t e = allow_max_smem(fs_pass_a<T>);
+  if (e == cudaSuccess) e = allow_max_smem(fs_pass_c<T>);
+  if (e == cudaSuccess) e = allow_max_smem(fs_pass_b);
+  return e;
 }
 
 cudaError_t setup_fourstep_kernels(const cat_plan_s* p) {

@@ -166,7 +166,7 @@ static cudaError_t run_score(const cat_plan_s* p, const T* X, const T* WA, int h
   constexpr int HP = (HT + 3) & ~3;
   size_t smem = (size_t)HP * p->D * sizeof(float);
   auto k = score_kernel<T, HT, VEC>;
-  if (setup) return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (setup) return allow_max_smem(k);
   dim3 grid((p->N + kScoreTokPerCta - 1) / kScoreTokPerCta, p->B);
   k<<<grid, kScoreThreads, smem, p->stream>>>(X, WA, p->z2, p->N, p->D, p->H, h0);
   return cudaGetLastError();
@@ -296,9 +296,7 @@ cudaError_t setup_score_kernels(const cat_plan_s* p) {
       ? score_dispatch<__nv_bfloat16>(p, nullptr, nullptr, true)
       : score_dispatch<float>(p, nullptr, nullptr, true);
   if (e != cudaSuccess) return e;
-  if (p->path == PATH_SMEM)
-    e = cudaFuncSetAttribute(softmax_spectrum_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)p->sm.spec_smem);
+  if (p->path == PATH_SMEM) e = allow_max_smem(softmax_spectrum_kernel);
   return e;
 }
 

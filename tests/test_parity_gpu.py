@@ -246,3 +246,19 @@ def test_plan_on_a_side_stream():
             p.sync()
     O_ref, _ = oracle.forward(X.cpu(), WA.cpu(), V.cpu(), mode="direct")
     assert float(np.abs(O.cpu().double().numpy() - O_ref).max()) <= 2e-5 * float(V.abs().max())
+
+
+def test_plans_of_different_lengths_coexist():
+    """Two live plans whose kernels need different shared memory: creating
+    the smaller one must not break the larger one's launches."""
+    big = synth.make_inputs(1, 16384, 16, 2, "f32", seed=21)
+    small = synth.make_inputs(2, 256, 16, 2, "f32", seed=22)
+    with cat.Plan(1, 16384, 16, 2, "f32") as pb:
+        with cat.Plan(2, 256, 16, 2, "f32") as ps:
+            Ob = pb.forward(*to_dev(*big))
+            Os = ps.forward(*to_dev(*small))
+            pb.sync()
+            ps.sync()
+    for (X, WA, V), O in ((big, Ob), (small, Os)):
+        O_ref, _ = oracle.forward(X, WA, V, mode="fft")
+        assert float(np.abs(O.cpu().double().numpy() - O_ref).max()) <= 2e-5 * float(V.abs().max())
