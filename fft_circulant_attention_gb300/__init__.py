@@ -27,6 +27,7 @@ STATUS = {
     0: "CAT_OK", -1: "CAT_ERR_INVALID_ARG", -2: "CAT_ERR_UNSUPPORTED_N",
     -3: "CAT_ERR_MISALIGNED", -4: "CAT_ERR_PLAN_MISMATCH", -5: "CAT_ERR_ALLOC",
     -6: "CAT_ERR_CUDA", -7: "CAT_ERR_DEVICE_STATUS", -8: "CAT_ERR_ALIAS",
+    -9: "CAT_ERR_TOO_LARGE",
 }
 for _code, _name in STATUS.items():
     globals()[_name] = _code
@@ -46,6 +47,7 @@ SIGNATURES = {
     "cat_plan_timing": (_I, [_P, _I]),
     "cat_plan_stage_times": (_I, [_P, ctypes.POINTER(ctypes.c_float), _I,
                                   ctypes.POINTER(_I)]),
+    "cat_forward_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "cat_status_string": (ctypes.c_char_p, [_I]),
 }
 
@@ -151,6 +153,14 @@ def cat_forward_host(plan, X, W_A, V, O, B, N, D, H, dtype):
                                   dtype_code(dtype)), "cat_forward_host")
 
 
+def cat_forward_noalloc(X, W_A, V, O, B, N, D, H, dtype, stream=None):
+    """The forward without a plan or any allocation (fixed device workspace;
+    B·H·N and N bounded).  Enqueued on `stream` (default: the legacy default
+    stream)."""
+    _check(lib().cat_forward_noalloc(_ptr(X), _ptr(W_A), _ptr(V), _ptr(O), B, N, D, H,
+                                     dtype_code(dtype), _stream(stream)), "cat_forward_noalloc")
+
+
 def cat_plan_sync(plan):
     _check(lib().cat_plan_sync(plan), "cat_plan_sync")
 
@@ -247,5 +257,6 @@ class Plan:
 __all__ = ["CatError", "Plan", "lib", "dtype_code", "cat_plan_create", "cat_plan_destroy",
            "cat_plan_set_stream", "cat_forward", "cat_forward_zstar", "cat_forward_host",
            "cat_plan_sync", "cat_plan_describe", "cat_plan_timing", "cat_plan_stage_times",
+           "cat_forward_noalloc",
            "cat_status_string", "CAT_F32", "CAT_BF16",
            "SIGNATURES", "LIB_PATH"]

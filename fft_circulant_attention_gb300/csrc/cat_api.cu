@@ -252,6 +252,35 @@ int run_front(cat_plan_s* p, const void* X, const void* WA) {
 
 }  // namespace
 
+namespace cat {
+
+// Launch configuration of the shared-memory path for an already-validated
+// shape (N <= 16384), without touching the device or allocating: fills the
+// radix plan, the SmemCfg and the launch count of *p.
+int configure_smem_path(cat_plan_s* p) {
+  const int N = p->N;
+  if (N > kSmemMaxN) return CAT_ERR_UNSUPPORTED_N;
+  p->path = cat::PATH_SMEM;
+  if (!make_radix_plan(N, &p->rpN)) return CAT_ERR_UNSUPPORTED_N;
+  cat::SmemCfg& s = p->sm;
+  size_t per = (size_t)N * sizeof(float2);
+  split_pairs(p->npair, (int)(kConvSmemBudget / per), &s.G, &s.groups);
+  s.tstride = N;
+  s.smem = (size_t)s.G * s.tstride * sizeof(float2);
+  s.threads = fft_threads(s.G, N);
+  s.spec_threads = fft_threads(1, N);
+  s.spec_smem = per;
+  if ((long)s.G * N > (long)cat::vals_capacity(p->rpN) * s.threads) return CAT_ERR_UNSUPPORTED_N;
+  if ((long)N > (long)cat::vals_capacity(p->rpN) * s.spec_threads) return CAT_ERR_UNSUPPORTED_N;
+  p->launches = score_launches(p->H, p->D) + 2;
+  return CAT_OK;
+}
+
+// Shape validation shared with the plan constructor.
+int validate(int B, int N, int D, int H, int dtype) { return validate_shape(B, N, D, H, dtype); }
+
+}  // namespace cat
+
 extern "C" {
 
 int cat_plan_create(cat_plan_t* out, int B, int N, int D, int H, int dtype, void* stream) {
@@ -456,6 +485,7 @@ const char* cat_status_string(int status) {
     case CAT_ERR_CUDA: return "CAT_ERR_CUDA";
     case CAT_ERR_DEVICE_STATUS: return "CAT_ERR_DEVICE_STATUS";
     case CAT_ERR_ALIAS: return "CAT_ERR_ALIAS";
+    case CAT_ERR_TOO_LARGE: return "CAT_ERR_TOO_LARGE";
     default: return "CAT_ERR_UNKNOWN";
   }
 }

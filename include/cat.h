@@ -51,7 +51,8 @@ enum {
   CAT_ERR_ALLOC = -5,         /* device or host allocation failed           */
   CAT_ERR_CUDA = -6,          /* a CUDA runtime call or launch failed       */
   CAT_ERR_DEVICE_STATUS = -7, /* a kernel reported an internal check failure*/
-  CAT_ERR_ALIAS = -8          /* O overlaps X, W_A or V                     */
+  CAT_ERR_ALIAS = -8,         /* O overlaps X, W_A or V                     */
+  CAT_ERR_TOO_LARGE = -9      /* beyond cat_forward_noalloc's fixed workspace */
 };
 
 /* Limits of this build. */
@@ -153,6 +154,41 @@ int cat_plan_timing(cat_plan_t plan, int max_calls);
  * many calls that was.  Errors: CAT_ERR_INVALID_ARG, CAT_ERR_CUDA.
  */
 int cat_plan_stage_times(cat_plan_t plan, float *ms, int cap, int *ncalls);
+
+/* Limits of cat_forward_noalloc's fixed device workspace. */
+#define CAT_NOALLOC_MAX_ROWS (1 << 18) /* B·H·N                                 */
+#define CAT_NOALLOC_MAX_N 16384        /* sequence length                       */
+
+/*
+ * cat_forward_noalloc — the same forward as cat_forward (short-sequence
+ * shared-memory path), for callers that cannot allocate device memory: a
+ * process whose device memory has been handed to a caching or pooled
+ * allocator (where cudaMalloc would fail or fragment the pool), or a
+ * latency-critical caller that cannot absorb the device-wide
+ * synchronisation cudaMalloc and cudaFree imply.  It needs no plan and
+ * never calls cudaMalloc, cudaFree or any allocating routine.  The notes
+ * page has no counterpart to this entry point; it only changes where the
+ * workspace lives.
+ *
+ * The workspace (scores, z*, spectra, twiddles, status word; about 5 MiB)
+ * is one fixed array in the library's device image, which every GPU that
+ * loads the library holds until the process exits.  Its size bounds the
+ * problem: B·H·N <= CAT_NOALLOC_MAX_ROWS and N <= CAT_NOALLOC_MAX_N, else
+ * CAT_ERR_TOO_LARGE.  Other shape rules and errors are those of
+ * cat_plan_create and cat_forward.
+ *
+ * X, W_A, V (read) and O (written): device pointers as for cat_forward.
+ * stream: cudaStream_t to enqueue on (NULL = legacy default stream).
+ * The call is asynchronous.  The first call on each device also does a
+ * one-time set-up on the host (it looks up the array's device address and
+ * raises the kernels' shared-memory limits), so make that first call before
+ * any stream capture.  All calls share the one array and it keeps the last
+ * call's contents: calls whose GPU work overlaps (on different streams, or
+ * from different host threads) race on it and must be ordered by the
+ * caller.
+ */
+int cat_forward_noalloc(const void *X, const void *W_A, const void *V, void *O, int B,
+                        int N, int D, int H, int dtype, void *stream);
 
 /* Static string for a status code ("CAT_OK", "CAT_ERR_INVALID_ARG", ...). */
 const char *cat_status_string(int status);
