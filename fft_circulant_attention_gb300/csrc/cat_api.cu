@@ -21,6 +21,7 @@ constexpr int kSmemMaxN = 16384;             // longest single-CTA transform
 constexpr size_t kConvSmemBudget = 64 << 10;  // preferred per-CTA tile (bytes)
 constexpr size_t kFsSmemBudget = 100 << 10;
 constexpr size_t kScratchBudget = 80ull << 20;  // live four-step scratch (L2-sized)
+constexpr size_t kFastScratchBudget = 64ull << 20;
 
 bool seven_smooth(long n) {
   if (n < 1) return false;
@@ -132,6 +133,7 @@ void free_plan(cat_plan_s* p) {
   cudaFree(p->zf);
   cudaFree(p->tw);
   cudaFree(p->scratch);
+  cudaFree(p->zscr);
   cudaFree(p->status);
   cudaFree(p->hx);
   cudaFree(p->hwa);
@@ -152,6 +154,34 @@ int choose_path(cat_plan_s* p) {
   const char* force = std::getenv("CAT_FORCE_PATH");
   int n1 = 0, n2 = 0;
   const bool force_fs = force && std::strcmp(force, "fourstep") == 0 && split_fourstep(N, &n1, &n2);
+  const bool allow_fast = !(force && (std::strcmp(force, "fourstep") == 0 ||
+                                      std::strcmp(force, "smem") == 0));
+  // Fast three-pass path: head width 64 and N = 512·N2, N2 in {32..256}.
+  if (allow_fast && p->dh == 64 && N % 512 == 0) {
+    const int N2 = N / 512;
+    if (N2 == 32 || N2 == 64 || N2 == 128 || N2 == 256) {
+      p->path = cat::PATH_FAST;
+      cat::FourStepCfg& f = p->fs;
+      f.N1 = 512;
+      f.N2 = N2;
+      if (!make_radix_plan(f.N1, &f.rp1) || !make_radix_plan(N2, &f.rp2) ||
+          !make_radix_plan(N, &p->rpN))
+        return CAT_ERR_UNSUPPORTED_N;
+      f.G = 32;
+      f.groups = 1;
+      f.P = 32;
+      const size_t per_bh = (size_t)N * 32 * sizeof(float2);
+      long chunk = (long)(kFastScratchBudget / per_bh);
+      if (const char* env = std::getenv("CAT_CHUNK_BH")) chunk = std::atol(env);
+      if (chunk < 1) chunk = 1;
+      const long rows = (long)p->B * p->H;
+      if (chunk > rows) chunk = rows > 0 ? rows : 1;
+      f.chunk_bh = (int)chunk;
+      p->scratch_bytes = (size_t)f.chunk_bh * per_bh;
+      p->launches = score_launches(p->H, p->D) + 3 + 3 * (int)((rows + chunk - 1) / chunk);
+      return CAT_OK;
+    }
+  }
   if (N <= kSmemMaxN && !force_fs) {
     p->path = cat::PATH_SMEM;
     if (!make_radix_plan(N, &p->rpN)) return CAT_ERR_UNSUPPORTED_N;
@@ -224,6 +254,11 @@ void describe(cat_plan_s* p) {
                   "spec_threads=%d workspace=%zu launches=%d",
                   p->N, rad, p->sm.G, p->sm.groups, p->sm.threads, p->sm.smem,
                   p->sm.spec_threads, p->workspace_bytes, p->launches);
+  } else if (p->path == cat::PATH_FAST) {
+    std::snprintf(p->desc, sizeof(p->desc),
+                  "path=fast N=%d N1=%d N2=%d chunk_bh=%d scratch=%zu workspace=%zu launches=%d",
+                  p->N, p->fs.N1, p->fs.N2, p->fs.chunk_bh, p->scratch_bytes,
+                  p->workspace_bytes, p->launches);
   } else {
     char r1[64] = {0}, r2[64] = {0};
     radstr(p->fs.rp1, r1, sizeof(r1));
@@ -307,11 +342,14 @@ int cat_plan_create(cat_plan_t* out, int B, int N, int D, int H, int dtype, void
             alloc((void**)&p->zs, rowsN * sizeof(float)) &&
             alloc((void**)&p->tw, (size_t)N * sizeof(float2)) &&
             alloc((void**)&p->status, sizeof(unsigned int));
-  if (ok && p->path == cat::PATH_SMEM) ok = alloc((void**)&p->zf, rowsN * sizeof(float2));
-  if (ok && p->path == cat::PATH_FOURSTEP) ok = alloc((void**)&p->scratch, p->scratch_bytes);
+  if (ok && (p->path == cat::PATH_SMEM || p->path == cat::PATH_FAST))
+    ok = alloc((void**)&p->zf, rowsN * sizeof(float2));
+  if (ok && p->path == cat::PATH_FAST) ok = alloc((void**)&p->zscr, rowsN * sizeof(float2));
+  if (ok && p->path != cat::PATH_SMEM) ok = alloc((void**)&p->scratch, p->scratch_bytes);
   if (!ok) { cudaGetLastError(); free_plan(p); return CAT_ERR_ALLOC; }
   p->workspace_bytes = rowsN * (sizeof(float) + sizeof(float2)) + (size_t)N * sizeof(float2) +
-                       (p->zf ? rowsN * sizeof(float2) : 0) + p->scratch_bytes;
+                       (p->zf ? rowsN * sizeof(float2) : 0) +
+                       (p->zscr ? rowsN * sizeof(float2) : 0) + p->scratch_bytes;
 
   // Twiddle table exp(-2πi j/N), evaluated in fp64 and rounded once.
   std::vector<float2> tw((size_t)N);
@@ -324,7 +362,9 @@ int cat_plan_create(cat_plan_t* out, int B, int N, int D, int H, int dtype, void
   if (e == cudaSuccess) e = cudaMemset(p->status, 0, sizeof(unsigned int));
   if (e == cudaSuccess) e = cat::setup_score_kernels(p);
   if (e == cudaSuccess)
-    e = p->path == cat::PATH_SMEM ? cat::setup_smem_kernels(p) : cat::setup_fourstep_kernels(p);
+    e = p->path == cat::PATH_SMEM       ? cat::setup_smem_kernels(p)
+        : p->path == cat::PATH_FOURSTEP ? cat::setup_fourstep_kernels(p)
+                                        : cat::setup_fast_kernels(p);
   if (e != cudaSuccess) { free_plan(p); return CAT_ERR_CUDA; }
   describe(p);
   if (std::getenv("CAT_LOG")) std::fprintf(stderr, "[cat] %s\n", p->desc);
@@ -371,8 +411,9 @@ int cat_forward(cat_plan_t p, const void* X, const void* WA, const void* V, void
   e = p->path == cat::PATH_SMEM ? cat::launch_softmax_spectrum(p) : cat::launch_softmax(p);
   if (e != cudaSuccess) return CAT_ERR_CUDA;
   if (ev) cudaEventRecord(ev[2], p->stream);
-  e = p->path == cat::PATH_SMEM ? cat::launch_conv_smem(p, V, O)
-                                : cat::launch_fourstep_conv(p, V, O);
+  e = p->path == cat::PATH_SMEM       ? cat::launch_conv_smem(p, V, O)
+      : p->path == cat::PATH_FOURSTEP ? cat::launch_fourstep_conv(p, V, O)
+                                      : cat::launch_fast_conv(p, V, O);
   if (ev) cudaEventRecord(ev[3], p->stream);
   return map_cuda(e);
 }

@@ -7,7 +7,7 @@
 
 namespace cat {
 
-enum Path { PATH_SMEM = 0, PATH_FOURSTEP = 1 };
+enum Path { PATH_SMEM = 0, PATH_FOURSTEP = 1, PATH_FAST = 2 };
 
 // Launch shape of the single-CTA shared-memory path (N up to 16384): one CTA
 // transforms G packed column pairs of one (b, h).
@@ -57,6 +57,7 @@ struct cat_plan_s {
   float* zs;                // [B, H, N] z* (softmax weights)
   float2* zf;               // [B, H, N] spectrum of z* divided by N (smem path)
   float2* tw;               // [N] exp(-2πi j/N)
+  float2* zscr;             // [B, H, N] fast path: z* after its first DFT pass
   float2* scratch;          // four-step scratch, chunk_bh·N·P complex
   size_t scratch_bytes;
   unsigned int* status;     // device status word
@@ -100,6 +101,7 @@ cudaError_t launch_softmax(const cat_plan_s* p);
 cudaError_t launch_softmax_spectrum(const cat_plan_s* p);
 cudaError_t launch_conv_smem(const cat_plan_s* p, const void* V, void* O);
 cudaError_t launch_fourstep_conv(const cat_plan_s* p, const void* V, void* O);
+cudaError_t launch_fast_conv(const cat_plan_s* p, const void* V, void* O);
 
 // Shape validation and shared-memory-path configuration without allocation.
 int validate(int B, int N, int D, int H, int dtype);
@@ -109,5 +111,6 @@ int configure_smem_path(cat_plan_s* p);
 cudaError_t setup_score_kernels(const cat_plan_s* p);
 cudaError_t setup_smem_kernels(const cat_plan_s* p);
 cudaError_t setup_fourstep_kernels(const cat_plan_s* p);
+cudaError_t setup_fast_kernels(const cat_plan_s* p);
 
 }  // namespace cat

@@ -262,3 +262,30 @@ def test_plans_of_different_lengths_coexist():
     for (X, WA, V), O in ((big, Ob), (small, Os)):
         O_ref, _ = oracle.forward(X, WA, V, mode="fft")
         assert float(np.abs(O.cpu().double().numpy() - O_ref).max()) <= 2e-5 * float(V.abs().max())
+
+
+@pytest.mark.parametrize("N,B,H,dtype", [
+    (16384, 2, 1, "f32"), (16384, 1, 2, "bf16"), (32768, 1, 1, "f32"),
+    (65536, 1, 1, "bf16"), (131072, 1, 1, "f32"), (131072, 1, 2, "bf16"),
+])
+def test_fast_path_lengths(N, B, H, dtype):
+    """Head width 64 and N = 512·N2 (N2 = 32..256) take the three-pass fast
+    path; checked against the oracle's convolution-theorem evaluation."""
+    D = 64 * H
+    with cat.Plan(B, N, D, H, dtype) as p:
+        assert "path=fast" in p.describe()
+    parity(B, N, D, H, dtype, seed=N + H, mode="fft")
+
+
+def test_fast_path_chunks(monkeypatch):
+    """Several (b, h) chunks of scratch in one forward (chunk of 3 rows for
+    B·H = 8) give the same result as one chunk."""
+    X, WA, V = to_dev(*synth.make_inputs(2, 16384, 256, 4, "bf16", seed=31))
+    outs = []
+    for chunk in ("3", "8"):
+        monkeypatch.setenv("CAT_CHUNK_BH", chunk)
+        with cat.Plan(2, 16384, 256, 4, "bf16") as p:
+            assert "chunk_bh=%s" % chunk in p.describe()
+            outs.append(p.forward(X, WA, V))
+            p.sync()
+    assert torch.equal(outs[0], outs[1])
