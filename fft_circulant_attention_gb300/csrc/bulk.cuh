@@ -1,0 +1,118 @@
+// Bulk asynchronous copies global -> shared (cp.async.bulk) completed on
+// shared-memory mbarriers, with bounded waits.
+//
+// A copy moves a contiguous run of bytes (16-byte aligned at both ends, a
+// multiple of 16 bytes long) and reports its bytes to an mbarrier
+// (complete_tx).  The consumer first registers the expected byte count on
+// the barrier (arrive.expect_tx), then all copies are issued, then the
+// consumer waits for the barrier's phase to flip.  Waits give up after a
+// bounded number of polls and report through the plan's status word, so a
+// lost copy can never hang the GPU.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "fft_device.cuh"
+
+namespace cat {
+
+// Polls of mbarrier.try_wait (each blocks for a hardware-chosen time) before
+// a wait is declared lost.
+constexpr uint32_t kMaxPolls = 1u << 22;
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+}
+
+// Make barrier initialisation visible to the async proxy and the CTA.
+__device__ __forceinline__ void mbar_fence_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// Arrive once and add `bytes` to the barrier's expected transaction count.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Wait for the phase with the given parity to complete.  Returns false (and
+// records `code` in the status word) if it did not within kMaxPolls polls.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned int* status,
+                                          unsigned int code) {
+  for (uint32_t i = 0; i < kMaxPolls; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  report(status, code);
+  return false;
+}
+
+// Bulk copy of `bytes` bytes from global `src` to shared `dst`, completing
+// on `bar`.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// Tiled tensor copy (TMA) of the box at element coordinates (c0..c3) of a
+// 4-D tensor map into shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, int c0, int c1,
+                                            int c2, int c3, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+      "r"(smem_addr(bar))
+      : "memory");
+}
+
+// Tiled 2-D tensor copy (TMA) of the box at (c0, c1) into shared memory.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// Plain arrive (count 1) on an mbarrier.
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// Host: encode a 2-D bf16 tensor map with 128-byte swizzle (box inner
+// extent 128 bytes).  Returns false if the driver rejected it.
+bool encode_map_2d_sw128(CUtensorMap* map, const void* base, unsigned long long cols,
+                         unsigned long long rows, unsigned long long row_bytes,
+                         unsigned int box_cols, unsigned int box_rows);
+
+// Host: encode a 4-D tiled tensor map (no interleave, no swizzle).  dims and
+// box are innermost first; strides are the byte strides of dims 1..3.
+// Returns false if the driver rejected the description.
+bool encode_map_4d(CUtensorMap* map, const void* base, CUtensorMapDataType type,
+                   const unsigned long long dims[4], const unsigned long long strides[3],
+                   const unsigned int box[4]);
+
+}  // namespace cat

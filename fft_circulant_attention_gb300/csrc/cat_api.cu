@@ -130,6 +130,7 @@ void free_plan(cat_plan_s* p) {
   free_events(p);
   cudaFree(p->z2);
   cudaFree(p->zs);
+  cudaFree(p->part);
   cudaFree(p->zf);
   cudaFree(p->tw);
   cudaFree(p->scratch);
@@ -178,7 +179,7 @@ int choose_path(cat_plan_s* p) {
       if (chunk > rows) chunk = rows > 0 ? rows : 1;
       f.chunk_bh = (int)chunk;
       p->scratch_bytes = (size_t)f.chunk_bh * per_bh;
-      p->launches = score_launches(p->H, p->D) + 3 + 3 * (int)((rows + chunk - 1) / chunk);
+      p->launches = score_launches(p->H, p->D) + 4 + 3 * (int)((rows + chunk - 1) / chunk);
       return CAT_OK;
     }
   }
@@ -236,7 +237,7 @@ int choose_path(cat_plan_s* p) {
   if (chunk > rows) chunk = rows > 0 ? rows : 1;
   f.chunk_bh = (int)chunk;
   p->scratch_bytes = (size_t)f.chunk_bh * per_bh;
-  p->launches = score_launches(p->H, p->D) + 1 + 3 * (int)((rows + chunk - 1) / chunk);
+  p->launches = score_launches(p->H, p->D) + 2 + 3 * (int)((rows + chunk - 1) / chunk);
   return CAT_OK;
 }
 
@@ -329,10 +330,18 @@ int cat_plan_create(cat_plan_t* out, int B, int N, int D, int H, int dtype, void
   p->dh = D / H;
   p->npair = (p->dh + 1) / 2;
   p->stream = (cudaStream_t)stream;
+  if (const char* sc = std::getenv("CAT_SCORE")) {
+    p->score_cuda_cores = std::strcmp(sc, "cuda") == 0;
+    p->score_path = std::strcmp(sc, "mma") == 0 ? 1 : 0;
+  }
   st = choose_path(p);
   if (st != CAT_OK) { delete p; return st; }
 
-  if (cudaGetDevice(&p->device) != cudaSuccess) { delete p; return CAT_ERR_CUDA; }
+  if (cudaGetDevice(&p->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&p->sms, cudaDevAttrMultiProcessorCount, p->device) != cudaSuccess) {
+    delete p;
+    return CAT_ERR_CUDA;
+  }
   const size_t rowsN = (size_t)B * H * N;
   auto alloc = [&](void** ptr, size_t bytes) {
     if (bytes == 0) bytes = 16;
@@ -340,6 +349,7 @@ int cat_plan_create(cat_plan_t* out, int B, int N, int D, int H, int dtype, void
   };
   bool ok = alloc((void**)&p->z2, rowsN * sizeof(float2)) &&
             alloc((void**)&p->zs, rowsN * sizeof(float)) &&
+            alloc((void**)&p->part, (size_t)B * H * cat::softmax_parts(N) * sizeof(float2)) &&
             alloc((void**)&p->tw, (size_t)N * sizeof(float2)) &&
             alloc((void**)&p->status, sizeof(unsigned int));
   if (ok && (p->path == cat::PATH_SMEM || p->path == cat::PATH_FAST))

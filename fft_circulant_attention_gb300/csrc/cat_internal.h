@@ -1,5 +1,6 @@
 // Internal plan structure and kernel launchers of libcat (not part of the ABI).
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 
@@ -43,18 +44,22 @@ struct FourStepCfg {
 }  // namespace cat
 
 struct cat_plan_s {
+  CUtensorMap tm_c;         // fast path: scratch view for pass C (TMA)
   int B, N, D, H, dtype;
   int dh, npair;            // head width, packed pairs per head = ceil(dh/2)
   int device;
+  int sms;                  // multiprocessors of the device
   cudaStream_t stream;
   int path;
   cat::RadixPlan rpN;       // radices of N (shared-memory path)
   cat::SmemCfg sm;
   cat::FourStepCfg fs;
-  int score_threads, score_tok;  // score kernel: CTA size, tokens per CTA
+  int score_cuda_cores;     // 1: bf16 scores on the CUDA-core kernel (testing)
+  int score_path;           // 1: bf16 scores on the register-fed MMA kernel (testing)
   // workspace (device)
   float2* z2;               // [B, H, N] scores as double-float (hi, lo)
   float* zs;                // [B, H, N] z* (softmax weights)
+  float2* part;             // [B, H, P] softmax partials (max, sum) per chunk
   float2* zf;               // [B, H, N] spectrum of z* divided by N (smem path)
   float2* tw;               // [N] exp(-2πi j/N)
   float2* zscr;             // [B, H, N] fast path: z* after its first DFT pass
@@ -74,6 +79,11 @@ struct cat_plan_s {
 
 // Heads the score kernel covers per pass over X for model width D.
 int score_heads_per_pass(int D);
+
+namespace cat {
+// Chunks per row of the multi-CTA softmax.
+int softmax_parts(int N);
+}
 
 namespace cat {
 
@@ -111,6 +121,6 @@ int configure_smem_path(cat_plan_s* p);
 cudaError_t setup_score_kernels(const cat_plan_s* p);
 cudaError_t setup_smem_kernels(const cat_plan_s* p);
 cudaError_t setup_fourstep_kernels(const cat_plan_s* p);
-cudaError_t setup_fast_kernels(const cat_plan_s* p);
+cudaError_t setup_fast_kernels(cat_plan_s* p);
 
 }  // namespace cat

@@ -10,7 +10,9 @@
 //               times w_N^{-n1 k2};
 //   C (per n1): inverse DFT over k2, store the output rows n1 + N1·n2.
 // A warp's 32 lanes are the head's 32 pairs, so every global access of V,
-// O and the scratch is a contiguous run of the head's row.
+// O and the scratch is a contiguous run of the head's row; in passes A and C
+// consecutive CTAs take consecutive heads of the same rows, so the rows of
+// V and O stream through DRAM whole.
 //
 // Within a pass each thread holds 32 values in registers and the transform
 // is a sequence of Stockham steps (radix R, span Ls; task i takes the
@@ -20,12 +22,13 @@
 // holding exactly the bins the first inverse step needs, so pass B takes
 // the product and starts the inverse without touching shared memory.
 //
-// The spectrum of z* is computed once per (b, h) by spec_a/spec_b (generic
-// Stockham in shared memory) and stored in the order pass B's threads hold
+// The spectrum of z* is computed once per (b, h) by zspec_a/zspec_b (the
+// same register transforms) and stored in the order pass B's threads hold
 // the bins: thread j of the CTA for k2 holds k1 = 2j + e + 32s (e < 2,
 // s < 16), stored at ((k2·16 + j)·16 + s)·2 + e.
 #include <cuda_bf16.h>
 
+#include "bulk.cuh"
 #include "cat_internal.h"
 #include "elem.cuh"
 #include "fft_reg.cuh"
@@ -58,11 +61,11 @@ __device__ __forceinline__ void ld_sh2(const float2* p, float2& a, float2& b) {
 template <typename T, int N2>
 __global__ void __launch_bounds__(256)
 fsf_pass_a(const T* __restrict__ V, float2* __restrict__ scr, const float2* __restrict__ W,
-           int N, int D, int H, int bh0) {
+           int N, int D, int H, int bh0, int nb) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if constexpr (N2 == 32) {
-    const int n1 = (blockIdx.x % (kFastN1 / 8)) * 8 + warp;
-    const int bhl = blockIdx.x / (kFastN1 / 8);
+    const int n1 = (blockIdx.x / nb) * 8 + warp;
+    const int bhl = blockIdx.x % nb;
     const int bh = bh0 + bhl, b = bh / H, h = bh - b * H;
     const T* src = V + ((size_t)b * N + n1) * D + h * 64 + 2 * lane;
     const size_t rs = (size_t)kFastN1 * D;
@@ -81,8 +84,8 @@ fsf_pass_a(const T* __restrict__ V, float2* __restrict__ scr, const float2* __re
     extern __shared__ float4 smem4[];
     float2* buf = reinterpret_cast<float2*>(smem4);
     const int j = warp;
-    const int n1 = blockIdx.x % kFastN1;
-    const int bhl = blockIdx.x / kFastN1;
+    const int n1 = blockIdx.x / nb;
+    const int bhl = blockIdx.x % nb;
     const int bh = bh0 + bhl, b = bh / H, h = bh - b * H;
     const T* src = V + ((size_t)b * N + n1) * D + h * 64 + 2 * lane;
     const size_t rs = (size_t)kFastN1 * D;
@@ -121,11 +124,11 @@ fsf_pass_a(const T* __restrict__ V, float2* __restrict__ scr, const float2* __re
 template <typename T, int N2>
 __global__ void __launch_bounds__(256)
 fsf_pass_c(const float2* __restrict__ scr, T* __restrict__ O, const float2* __restrict__ W,
-           int N, int D, int H, int bh0) {
+           int N, int D, int H, int bh0, int nb) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if constexpr (N2 == 32) {
-    const int n1 = (blockIdx.x % (kFastN1 / 8)) * 8 + warp;
-    const int bhl = blockIdx.x / (kFastN1 / 8);
+    const int n1 = (blockIdx.x / nb) * 8 + warp;
+    const int bhl = blockIdx.x % nb;
     const int bh = bh0 + bhl, b = bh / H, h = bh - b * H;
     float2 a[32];
 #pragma unroll
@@ -143,8 +146,8 @@ fsf_pass_c(const float2* __restrict__ scr, T* __restrict__ O, const float2* __re
     extern __shared__ float4 smem4[];
     float2* buf = reinterpret_cast<float2*>(smem4);
     const int j = warp;
-    const int n1 = blockIdx.x % kFastN1;
-    const int bhl = blockIdx.x / kFastN1;
+    const int n1 = blockIdx.x / nb;
+    const int bhl = blockIdx.x % nb;
     const int bh = bh0 + bhl, b = bh / H, h = bh - b * H;
     float2 a[32];
 #pragma unroll
@@ -174,6 +177,133 @@ fsf_pass_c(const float2* __restrict__ scr, T* __restrict__ O, const float2* __re
   }
 }
 
+// Two storage elements (one packed pair) read from shared memory.
+__device__ __forceinline__ float2 sh_pair(const float* p) {
+  return *reinterpret_cast<const float2*>(p);
+}
+__device__ __forceinline__ float2 sh_pair(const __nv_bfloat16* p) {
+  unsigned int u = *reinterpret_cast<const unsigned int*>(p);
+  return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+}
+
+// ---------------------------------------------------------------------------
+// Pipelined passes A and C for N2 == 32.  Every warp runs its own pipeline
+// over work items (b, h, n1) — heads fastest — with STAGES shared-memory
+// stages: the tile of an item (32 rows n1 + 512·n2 of the head, or 32 scratch
+// rows) arrives by one tensor copy (TMA) completing on the stage's mbarrier,
+// so the next items' loads are in flight while the current item is
+// transformed.
+// ---------------------------------------------------------------------------
+constexpr int kPipeWarps = 8;
+
+template <typename T>
+struct PipeA {
+  static constexpr int kRowBytes = 64 * (int)sizeof(T);   // one head row of V
+  static constexpr int kStages = sizeof(T) == 2 ? 3 : 2;
+  static constexpr size_t kSmem = 2304 + (size_t)kPipeWarps * kStages * 32 * kRowBytes;
+};
+struct PipeC {
+  static constexpr int kRowBytes = kFastPairs * 8;         // one scratch row (32 pairs)
+  static constexpr int kWarps = 4;
+  static constexpr int kStages = 3;
+  static constexpr size_t kSmem = 256 + (size_t)kWarps * kStages * 32 * kRowBytes;
+};
+
+template <typename T>
+__global__ void __launch_bounds__(kPipeWarps * 32)
+fsf_pass_a32(const __grid_constant__ CUtensorMap tmV, float2* __restrict__ scr,
+             const float2* __restrict__ W, int N, int D, int H, int bh0, int nb,
+             unsigned int* status) {
+  using P = PipeA<T>;
+  extern __shared__ __align__(128) unsigned char sm[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm) + warp * P::kStages;
+  unsigned char* stage = sm + 2304 + (size_t)warp * P::kStages * 32 * P::kRowBytes;
+  float2* twrow = reinterpret_cast<float2*>(sm + 256) + warp * 32;   // 256 B per warp
+  if (lane == 0)
+    for (int s = 0; s < P::kStages; ++s) mbar_init(bar + s, 1);
+  mbar_fence_init();
+  __syncwarp();
+  const int gw = blockIdx.x * kPipeWarps + warp, G = gridDim.x * kPipeWarps;
+  const int items = nb * kFastN1;
+  auto issue = [&](int s, int item) {
+    if (lane == 0) {
+      const int bh = bh0 + item % nb, n1 = item / nb;
+      const int b = bh / H, h = bh - b * H;
+      mbar_expect_tx(bar + s, 32 * P::kRowBytes);
+      tma_load_4d(stage + s * 32 * P::kRowBytes, &tmV, h * 64, n1, 0, b, bar + s);
+    }
+  };
+#pragma unroll
+  for (int k = 0; k < P::kStages; ++k)
+    if (gw + k * G < items) issue(k, gw + k * G);
+  int it = 0;
+  for (int item = gw; item < items; item += G, ++it) {
+    const int s = it % P::kStages;
+    if (!mbar_wait(bar + s, (it / P::kStages) & 1, status, 0x501)) return;
+    const int bhl = item % nb, n1 = item / nb;
+    const float2 tw = __ldg(&W[(size_t)n1 * lane]);   // w_N^{n1·k2} for k2 = lane
+    const T* tile = reinterpret_cast<const T*>(stage + s * 32 * P::kRowBytes) + 2 * lane;
+    float2 a[32];
+#pragma unroll
+    for (int n2 = 0; n2 < 32; ++n2) a[n2] = sh_pair(tile + n2 * 64);
+    dft<32, false>(a);
+    __syncwarp();
+    const int next = item + P::kStages * G;
+    if (next < items) issue(s, next);
+    twrow[lane] = tw;
+    __syncwarp();
+#pragma unroll
+    for (int k2 = 0; k2 < 32; ++k2) scr[scr_idx(bhl, 32, k2, n1, lane)] = cmul(a[k2], twrow[k2]);
+    __syncwarp();
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(PipeC::kWarps * 32)
+fsf_pass_c32(const __grid_constant__ CUtensorMap tmC, T* __restrict__ O, int N, int D, int H,
+             int bh0, int nb, unsigned int* status) {
+  using P = PipeC;
+  extern __shared__ __align__(128) unsigned char sm[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm) + warp * P::kStages;
+  unsigned char* stage = sm + 256 + (size_t)warp * P::kStages * 32 * P::kRowBytes;
+  if (lane == 0)
+    for (int s = 0; s < P::kStages; ++s) mbar_init(bar + s, 1);
+  mbar_fence_init();
+  __syncwarp();
+  const int gw = blockIdx.x * P::kWarps + warp, G = gridDim.x * P::kWarps;
+  const int items = nb * kFastN1;
+  auto issue = [&](int s, int item) {
+    if (lane == 0) {
+      mbar_expect_tx(bar + s, 32 * P::kRowBytes);
+      tma_load_4d(stage + s * 32 * P::kRowBytes, &tmC, 0, item / nb, 0, item % nb, bar + s);
+    }
+  };
+#pragma unroll
+  for (int k = 0; k < P::kStages; ++k)
+    if (gw + k * G < items) issue(k, gw + k * G);
+  int it = 0;
+  for (int item = gw; item < items; item += G, ++it) {
+    const int s = it % P::kStages;
+    if (!mbar_wait(bar + s, (it / P::kStages) & 1, status, 0x502)) return;
+    const float2* tile = reinterpret_cast<const float2*>(stage + s * 32 * P::kRowBytes) + lane;
+    float2 a[32];
+#pragma unroll
+    for (int k2 = 0; k2 < 32; ++k2) a[k2] = tile[k2 * kFastPairs];
+    dft<32, true>(a);
+    __syncwarp();
+    const int next = item + P::kStages * G;
+    if (next < items) issue(s, next);
+    const int bh = bh0 + item % nb, n1 = item / nb;
+    const int b = bh / H, h = bh - b * H;
+    T* dst = O + ((size_t)b * N + n1) * D + h * 64 + 2 * lane;
+    const size_t rs = (size_t)kFastN1 * D;
+#pragma unroll
+    for (int n2 = 0; n2 < 32; ++n2) st_pair(dst + n2 * rs, a[n2]);
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Pass B: per (b, h, k2) and half of the head's pairs (16 signals of length
 // 512).  Forward: step F1 (radix 32, span 1; thread j task j), step F2
@@ -181,12 +311,21 @@ fsf_pass_c(const float2* __restrict__ scr, T* __restrict__ O, const float2* __re
 // Inverse: step I1 (radix 16, span 1; tasks 2j, 2j+1 — exactly the bins the
 // thread holds), step I2 (radix 32, span 16; task j), leaving n1 = j + 16s.
 // Lane l: pair (l & 15) of the half, j = 2·warp + (l >> 4).
+// Everything the compute steps read besides the exchange buffer — the
+// length-512 twiddles, the row w_N^{n1·k2} and the spectrum of z* at this
+// k2 — is loaded into shared memory at the start, together with the 32
+// scratch values, so no global load waits inside the transforms.
 // ---------------------------------------------------------------------------
+constexpr size_t kSmemB = (size_t)16 * kRowB * sizeof(float2) + 3 * kFastN1 * sizeof(float2);
+
 __global__ void __launch_bounds__(256, 2)
 fsf_pass_b(float2* __restrict__ scr, const float2* __restrict__ zft, const float2* __restrict__ W,
            int N, int N2, int bh0) {
   extern __shared__ float4 smem4[];
   float2* buf = reinterpret_cast<float2*>(smem4);
+  float2* tw512 = buf + 16 * kRowB;          // w_512^e, e < 512
+  float2* twk = tw512 + kFastN1;             // w_N^{n1·k2}, n1 < 512
+  float4* zsh = reinterpret_cast<float4*>(twk + kFastN1);   // FFT(z*)/N, pass-B order
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int pl = lane & 15;
   const int j = 2 * warp + (lane >> 4);
@@ -200,9 +339,20 @@ fsf_pass_b(float2* __restrict__ scr, const float2* __restrict__ zft, const float
   float2 a[32];
 #pragma unroll
   for (int u = 0; u < 32; ++u) a[u] = scr[scr_idx(bhl, N2, k2, j + 16 * u, pair)];
+  // Tables (each thread two entries of each; zft row is 256 float4).
+  const int t = threadIdx.x;
+  const float2 w0 = __ldg(&W[(size_t)t * wstep]), w1 = __ldg(&W[(size_t)(t + 256) * wstep]);
+  const float2 v0 = __ldg(&W[(size_t)t * k2]), v1 = __ldg(&W[(size_t)(t + 256) * k2]);
+  const float4 zq = __ldg(reinterpret_cast<const float4*>(zft) +
+                          ((size_t)(bh0 + bhl) * N2 + k2) * (kFastN1 / 2) + t);
   dft<32, false>(a);
 #pragma unroll
-  for (int s = 0; s < 32; s += 2) st_sh2(row + 32 * j + s, a[s], a[s + 1]);
+  for (int q = 0; q < 32; q += 2) st_sh2(row + 32 * j + q, a[q], a[q + 1]);
+  tw512[t] = w0;
+  tw512[t + 256] = w1;
+  twk[t] = v0;
+  twk[t + 256] = v1;
+  zsh[t] = zq;
   __syncthreads();
 
   float2 c[2][16];
@@ -212,99 +362,146 @@ fsf_pass_b(float2* __restrict__ scr, const float2* __restrict__ zft, const float
   for (int e = 0; e < 2; ++e) {
     const int k = 2 * j + e;
 #pragma unroll
-    for (int u = 1; u < 16; ++u) c[e][u] = cmul(c[e][u], __ldg(&W[(size_t)(u * k) * wstep]));
+    for (int u = 1; u < 16; ++u) c[e][u] = cmul(c[e][u], tw512[u * k]);
     dft<16, false>(c[e]);
   }
   // Product with FFT(z*)/N at bins k1 = 2j + e + 32s.
-  const float4* zrow = reinterpret_cast<const float4*>(zft) +
-                       (((size_t)(bh0 + bhl) * N2 + k2) * 16 + j) * 16;
 #pragma unroll
-  for (int s = 0; s < 16; ++s) {
-    float4 z = __ldg(zrow + s);
-    c[0][s] = cmul(c[0][s], make_float2(z.x, z.y));
-    c[1][s] = cmul(c[1][s], make_float2(z.z, z.w));
+  for (int q = 0; q < 16; ++q) {
+    float4 z = zsh[j * 16 + q];
+    c[0][q] = cmul(c[0][q], make_float2(z.x, z.y));
+    c[1][q] = cmul(c[1][q], make_float2(z.z, z.w));
   }
   __syncthreads();
 #pragma unroll
   for (int e = 0; e < 2; ++e) {
     dft<16, true>(c[e]);
 #pragma unroll
-    for (int s = 0; s < 16; s += 2) st_sh2(row + 32 * j + 16 * e + s, c[e][s], c[e][s + 1]);
+    for (int q = 0; q < 16; q += 2) st_sh2(row + 32 * j + 16 * e + q, c[e][q], c[e][q + 1]);
   }
   __syncthreads();
 #pragma unroll
   for (int u = 0; u < 32; ++u) a[u] = row[j + 16 * u];
 #pragma unroll
-  for (int u = 1; u < 32; ++u) a[u] = cmulc(a[u], __ldg(&W[(size_t)(u * j) * wstep]));
+  for (int u = 1; u < 32; ++u) a[u] = cmulc(a[u], tw512[u * j]);
   dft<32, true>(a);
 #pragma unroll
-  for (int s = 0; s < 32; ++s) {
-    const int n1 = j + 16 * s;
-    scr[scr_idx(bhl, N2, k2, n1, pair)] = cmulc(a[s], __ldg(&W[(size_t)n1 * k2]));
+  for (int q = 0; q < 32; ++q) {
+    const int n1 = j + 16 * q;
+    scr[scr_idx(bhl, N2, k2, n1, pair)] = cmulc(a[q], twk[n1]);
   }
 }
 
 // ---------------------------------------------------------------------------
-// Spectrum of z* in pass B's order (generic Stockham in shared memory).
-// spec_a: CTA per (b, h, tile of TZ n1 values): DFT over n2, twiddle into
-// zscr[bh][k2][n1].  spec_b: CTA per (b, h, k2): DFT over n1, /N, scatter.
+// Spectrum of z* in pass B's order, with the same register transforms.
+// zspec_a (per n1, over n2): lanes are consecutive n1 of one (b, h) row, so
+// the strided reads of z* are coalesced; z* enters as a complex signal with
+// zero imaginary part.  Result times w_N^{n1 k2} into zscr[row][k2][n1].
+// zspec_b (per k2, over n1): 8 consecutive k2 per CTA laid out like pass B's
+// signals (lane: signal l & 7, j = 4·warp + (l >> 3)); result /N stored
+// where pass B's thread j reads it.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(1024)
-fsf_spec_a(const float* __restrict__ zs, float2* __restrict__ zscr, const float2* __restrict__ W,
-           RadixPlan rp2, int N, int TZ, unsigned int* status) {
-  extern __shared__ float4 smem4[];
-  float2* buf = reinterpret_cast<float2*>(smem4);
-  const int N2 = rp2.L;
-  const int ntile = kFastN1 / TZ;
-  const int bh = blockIdx.x / ntile, n10 = (blockIdx.x % ntile) * TZ;
-  if (TZ * N2 > vals_capacity(rp2) * (int)blockDim.x) {
-    report(status, 0x401);
-    return;
-  }
-  const float* zrow = zs + (size_t)bh * N;
-  for (int idx = threadIdx.x; idx < TZ * N2; idx += blockDim.x) {
-    int t = idx % TZ, n2 = idx / TZ;
-    buf[t * N2 + n2] = make_float2(__ldg(zrow + n10 + t + kFastN1 * n2), 0.f);
-  }
-  __syncthreads();
-  block_fft<false>(buf, rp2, TZ, N2, W, kFastN1);
-  float2* out = zscr + (size_t)bh * N;
-  for (int idx = threadIdx.x; idx < TZ * N2; idx += blockDim.x) {
-    int t = idx % TZ, k2 = idx / TZ;
-    int n1 = n10 + t;
-    out[(size_t)k2 * kFastN1 + n1] = cmul(buf[t * N2 + k2], __ldg(&W[(size_t)n1 * k2]));
+template <int N2>
+__global__ void __launch_bounds__(256)
+fsf_zspec_a(const float* __restrict__ zs, float2* __restrict__ zscr, const float2* __restrict__ W,
+            int N) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if constexpr (N2 == 32) {
+    const int row = blockIdx.x >> 3;
+    const int n1 = (blockIdx.x & 7) * 64 + threadIdx.x;
+    const float* src = zs + (size_t)row * N + n1;
+    float2 a[32];
+#pragma unroll
+    for (int n2 = 0; n2 < 32; ++n2) a[n2] = make_float2(__ldg(src + kFastN1 * n2), 0.f);
+    dft<32, false>(a);
+    float2* dst = zscr + (size_t)row * N + n1;
+#pragma unroll
+    for (int k2 = 0; k2 < 32; ++k2)
+      dst[(size_t)k2 * kFastN1] = cmul(a[k2], __ldg(&W[(size_t)n1 * k2]));
+  } else {
+    constexpr int TS = N2 / 32;
+    constexpr int R2 = N2 / 32;
+    constexpr int PER = 32 / TS;
+    constexpr int RS = N2 + 2;
+    extern __shared__ float4 smem4[];
+    float2* buf = reinterpret_cast<float2*>(smem4);
+    const int j = warp;
+    const int row = blockIdx.x / (kFastN1 / 32);
+    const int n1 = (blockIdx.x % (kFastN1 / 32)) * 32 + lane;
+    const float* src = zs + (size_t)row * N + n1;
+    float2 a[32];
+#pragma unroll
+    for (int u = 0; u < 32; ++u) a[u] = make_float2(__ldg(src + (size_t)kFastN1 * (j + TS * u)), 0.f);
+    dft<32, false>(a);
+    float2* rb = buf + lane * RS;
+#pragma unroll
+    for (int s = 0; s < 32; s += 2) st_sh2(rb + 32 * j + s, a[s], a[s + 1]);
+    __syncthreads();
+    float2 c[PER][R2];
+#pragma unroll
+    for (int u = 0; u < R2; ++u)
+#pragma unroll
+      for (int e = 0; e < PER; e += 2) ld_sh2(rb + PER * j + e + 32 * u, c[e][u], c[e + 1][u]);
+    const int wstep = N / N2;
+    float2* dst = zscr + (size_t)row * N + n1;
+#pragma unroll
+    for (int e = 0; e < PER; ++e) {
+      const int k = PER * j + e;
+#pragma unroll
+      for (int u = 1; u < R2; ++u) c[e][u] = cmul(c[e][u], __ldg(&W[(size_t)(u * k) * wstep]));
+      dft<R2, false>(c[e]);
+#pragma unroll
+      for (int s = 0; s < R2; ++s) {
+        const int k2 = k + 32 * s;
+        dst[(size_t)k2 * kFastN1] = cmul(c[e][s], __ldg(&W[(size_t)n1 * k2]));
+      }
+    }
   }
 }
 
-__global__ void __launch_bounds__(1024)
-fsf_spec_b(const float2* __restrict__ zscr, float2* __restrict__ zft, const float2* __restrict__ W,
-           RadixPlan rp1, int N, int N2, unsigned int* status) {
+__global__ void __launch_bounds__(128)
+fsf_zspec_b(const float2* __restrict__ zscr, float2* __restrict__ zft, const float2* __restrict__ W,
+            int N, int N2) {
   extern __shared__ float4 smem4[];
   float2* buf = reinterpret_cast<float2*>(smem4);
-  const int bh = blockIdx.x / N2, k2 = blockIdx.x % N2;
-  if (kFastN1 > vals_capacity(rp1) * (int)blockDim.x) {
-    report(status, 0x402);
-    return;
-  }
-  const float2* in = zscr + (size_t)bh * N + (size_t)k2 * kFastN1;
-  for (int n1 = threadIdx.x; n1 < kFastN1; n1 += blockDim.x) buf[n1] = in[n1];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int pl = lane & 7;
+  const int j = 4 * warp + (lane >> 3);
+  const int per_row = N2 / 8;
+  const int row = blockIdx.x / per_row;
+  const int k2 = (blockIdx.x % per_row) * 8 + pl;
+  const int wstep = N / kFastN1;
+  float2* rb = buf + pl * kRowB;
+  const float2* src = zscr + (size_t)row * N + (size_t)k2 * kFastN1;
+  float2 a[32];
+#pragma unroll
+  for (int u = 0; u < 32; ++u) a[u] = src[j + 16 * u];
+  dft<32, false>(a);
+#pragma unroll
+  for (int s = 0; s < 32; s += 2) st_sh2(rb + 32 * j + s, a[s], a[s + 1]);
   __syncthreads();
-  block_fft<false>(buf, rp1, 1, kFastN1, W, N2);
+  float2 c[2][16];
+#pragma unroll
+  for (int u = 0; u < 16; ++u) ld_sh2(rb + 2 * j + 32 * u, c[0][u], c[1][u]);
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    const int k = 2 * j + e;
+#pragma unroll
+    for (int u = 1; u < 16; ++u) c[e][u] = cmul(c[e][u], __ldg(&W[(size_t)(u * k) * wstep]));
+    dft<16, false>(c[e]);
+  }
   const float invN = 1.0f / (float)N;
-  float2* out = zft + ((size_t)bh * N2 + k2) * kFastN1;
-  for (int k1 = threadIdx.x; k1 < kFastN1; k1 += blockDim.x) {
-    int jj = (k1 & 31) >> 1, e = k1 & 1, s = k1 >> 5;
-    out[(jj * 16 + s) * 2 + e] = cscale(buf[k1], invN);
-  }
+  float4* out = reinterpret_cast<float4*>(zft) + (((size_t)row * N2 + k2) * 16 + j) * 16;
+#pragma unroll
+  for (int s = 0; s < 16; ++s)
+    out[s] = make_float4(c[0][s].x * invN, c[0][s].y * invN, c[1][s].x * invN, c[1][s].y * invN);
 }
 
 // ---------------------------------------------------------------------------
 // Host side.
 // ---------------------------------------------------------------------------
-constexpr int kSpecTZ = 8;   // n1 values per spec_a CTA
-
 size_t fast_smem_a(int N2) { return N2 == 32 ? 0 : (size_t)kFastPairs * (N2 + 2) * sizeof(float2); }
-size_t fast_smem_b() { return (size_t)16 * kRowB * sizeof(float2); }
+size_t fast_smem_b() { return (size_t)16 * kRowB * sizeof(float2); }   // zspec_b
 
 template <typename T>
 static cudaError_t setup_t(int N2) {
@@ -314,19 +511,33 @@ static cudaError_t setup_t(int N2) {
   case n:                                                           \
     e = allow_max_smem(fsf_pass_a<T, n>);                           \
     if (e == cudaSuccess) e = allow_max_smem(fsf_pass_c<T, n>);     \
+    if (e == cudaSuccess) e = allow_max_smem(fsf_zspec_a<n>);       \
     break;
     CAT_N2(32) CAT_N2(64) CAT_N2(128) CAT_N2(256)
 #undef CAT_N2
     default: return cudaErrorInvalidValue;
   }
   if (e == cudaSuccess) e = allow_max_smem(fsf_pass_b);
-  if (e == cudaSuccess) e = allow_max_smem(fsf_spec_a);
-  if (e == cudaSuccess) e = allow_max_smem(fsf_spec_b);
+  if (e == cudaSuccess) e = allow_max_smem(fsf_pass_a32<T>);
+  if (e == cudaSuccess) e = allow_max_smem(fsf_pass_c32<T>);
+  if (e == cudaSuccess) e = allow_max_smem(fsf_zspec_b);
   return e;
 }
 
-cudaError_t setup_fast_kernels(const cat_plan_s* p) {
-  return p->dtype == 1 ? setup_t<__nv_bfloat16>(p->fs.N2) : setup_t<float>(p->fs.N2);
+cudaError_t setup_fast_kernels(cat_plan_s* p) {
+  cudaError_t e = p->dtype == 1 ? setup_t<__nv_bfloat16>(p->fs.N2) : setup_t<float>(p->fs.N2);
+  if (e != cudaSuccess) return e;
+  // Scratch viewed as fp32 [chunk_bh][N2 (k2)][512 (n1)][64 (32 pairs)].
+  const unsigned long long row = (unsigned long long)kFastPairs * sizeof(float2);
+  const unsigned long long dims[4] = {2ull * kFastPairs, (unsigned long long)kFastN1,
+                                      (unsigned long long)p->fs.N2,
+                                      (unsigned long long)p->fs.chunk_bh};
+  const unsigned long long strides[3] = {row, row * kFastN1, row * kFastN1 * p->fs.N2};
+  const unsigned int box_c[4] = {64, 1, 32, 1};      // 32 rows k2 of all pairs
+  if (p->fs.N2 == 32 &&
+      !encode_map_4d(&p->tm_c, p->scratch, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dims, strides, box_c))
+    return cudaErrorInvalidValue;
+  return cudaSuccess;
 }
 
 template <typename T, int N2>
@@ -335,9 +546,11 @@ static void launch_ac(const cat_plan_s* p, const T* V, T* O, int bh0, int nb, bo
   const int threads = N2 == 32 ? 256 : N2;
   const size_t smem = fast_smem_a(N2);
   if (pass_a)
-    fsf_pass_a<T, N2><<<grid, threads, smem, p->stream>>>(V, p->scratch, p->tw, p->N, p->D, p->H, bh0);
+    fsf_pass_a<T, N2><<<grid, threads, smem, p->stream>>>(V, p->scratch, p->tw, p->N, p->D, p->H,
+                                                         bh0, nb);
   else
-    fsf_pass_c<T, N2><<<grid, threads, smem, p->stream>>>(p->scratch, O, p->tw, p->N, p->D, p->H, bh0);
+    fsf_pass_c<T, N2><<<grid, threads, smem, p->stream>>>(p->scratch, O, p->tw, p->N, p->D, p->H,
+                                                         bh0, nb);
 }
 
 template <typename T>
@@ -345,25 +558,65 @@ static cudaError_t run_t(const cat_plan_s* p, const T* V, T* O) {
   const FourStepCfg& f = p->fs;
   const int rows = p->B * p->H;
   const int N2 = f.N2;
+  // V viewed as [B][N2 (n2)][512 (n1)][D]: the box is one head's 64 columns
+  // of the 32 rows n1 + 512·n2 (N2 == 32 passes).
+  CUtensorMap tmV;
+  if (N2 == 32) {
+    const unsigned long long es = sizeof(T);
+    const unsigned long long dims[4] = {(unsigned long long)p->D, (unsigned long long)kFastN1,
+                                        (unsigned long long)N2, (unsigned long long)p->B};
+    const unsigned long long strides[4 - 1] = {p->D * es, (unsigned long long)kFastN1 * p->D * es,
+                                               (unsigned long long)p->N * p->D * es};
+    const unsigned int box[4] = {64, 1, 32, 1};
+    if (!encode_map_4d(&tmV, V, sizeof(T) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                               : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                       dims, strides, box))
+      return cudaErrorInvalidValue;
+  }
   // Spectrum of z*, once per (b, h).
-  const int ga = rows * (kFastN1 / kSpecTZ);
-  fsf_spec_a<<<ga, 256, (size_t)kSpecTZ * N2 * sizeof(float2), p->stream>>>(
-      p->zs, p->zscr, p->tw, f.rp2, p->N, kSpecTZ, p->status);
-  fsf_spec_b<<<rows * N2, 64, (size_t)kFastN1 * sizeof(float2), p->stream>>>(
-      p->zscr, p->zf, p->tw, f.rp1, p->N, N2, p->status);
+  switch (N2) {
+    case 32:
+      fsf_zspec_a<32><<<rows * 8, 64, 0, p->stream>>>(p->zs, p->zscr, p->tw, p->N);
+      break;
+#define CAT_ZA(n)                                                                          \
+  case n:                                                                                  \
+    fsf_zspec_a<n><<<rows * (kFastN1 / 32), n, fast_smem_a(n), p->stream>>>(p->zs, p->zscr, \
+                                                                             p->tw, p->N); \
+    break;
+    CAT_ZA(64) CAT_ZA(128) CAT_ZA(256)
+#undef CAT_ZA
+    default: return cudaErrorInvalidValue;
+  }
+  fsf_zspec_b<<<rows * (N2 / 8), 128, fast_smem_b() / 2, p->stream>>>(p->zscr, p->zf, p->tw,
+                                                                      p->N, N2);
   for (int bh0 = 0; bh0 < rows; bh0 += f.chunk_bh) {
     const int nb = rows - bh0 < f.chunk_bh ? rows - bh0 : f.chunk_bh;
     auto ac = [&](bool pass_a) {
       switch (N2) {
-        case 32: launch_ac<T, 32>(p, V, O, bh0, nb, pass_a); break;
+        case 32: {
+          const int items = nb * kFastN1;
+          if (pass_a) {
+            // Resident CTAs per SM: two when two tiles' stages fit.
+            const int per_sm = PipeA<T>::kSmem <= (113u << 10) ? 2 : 1;
+            int grid = (items + kPipeWarps - 1) / kPipeWarps;
+            if (grid > per_sm * p->sms) grid = per_sm * p->sms;
+            fsf_pass_a32<T><<<grid, kPipeWarps * 32, PipeA<T>::kSmem, p->stream>>>(
+                tmV, p->scratch, p->tw, p->N, p->D, p->H, bh0, nb, p->status);
+          } else {
+            int grid = (items + PipeC::kWarps - 1) / PipeC::kWarps;
+            if (grid > 2 * p->sms) grid = 2 * p->sms;
+            fsf_pass_c32<T><<<grid, PipeC::kWarps * 32, PipeC::kSmem, p->stream>>>(
+                p->tm_c, O, p->N, p->D, p->H, bh0, nb, p->status);
+          }
+          break;
+        }
         case 64: launch_ac<T, 64>(p, V, O, bh0, nb, pass_a); break;
         case 128: launch_ac<T, 128>(p, V, O, bh0, nb, pass_a); break;
         default: launch_ac<T, 256>(p, V, O, bh0, nb, pass_a); break;
       }
     };
     ac(true);
-    fsf_pass_b<<<nb * N2 * 2, 256, fast_smem_b(), p->stream>>>(p->scratch, p->zf, p->tw, p->N,
-                                                                N2, bh0);
+    fsf_pass_b<<<nb * N2 * 2, 256, kSmemB, p->stream>>>(p->scratch, p->zf, p->tw, p->N, N2, bh0);
     ac(false);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;

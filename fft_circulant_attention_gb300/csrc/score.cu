@@ -7,6 +7,7 @@
 // acceleration" design) fused into the softmax kernel.
 #include <cuda_bf16.h>
 
+#include "bulk.cuh"
 #include "cat_internal.h"
 #include "elem.cuh"
 
@@ -155,6 +156,309 @@ score_kernel(const T* __restrict__ X, const T* __restrict__ WA, float2* __restri
   }
 }
 
+// ---------------------------------------------------------------------------
+// bf16 score on the tensor cores (mma.sync m16n8k16, bf16 in, fp32 out).
+// Products of two bf16 values are exact in fp32, so each MMA pair sums 32
+// exact products of one 32-wide slice of d into a fresh fp32 accumulator;
+// the slice sums are then added into a double-float (hi, lo) with TwoSum,
+// exactly as the CUDA-core kernel does with its 16-wide runs.
+//
+// The slice order inside an MMA is free (a dot product), so each lane feeds
+// the MMAs from one 16-byte load per token row: lane (r = lane/4, c = lane%4)
+// loads X[row][d0 + 8c .. d0 + 8c + 8) for rows r and r + 8 of a 16-token
+// tile; words 0-1 of that load feed MMA 1 and words 2-3 MMA 2, and W_A^T
+// rows in shared memory are read with the same map.  A warp owns two tiles
+// (32 tokens); heads go in n-tiles of 8 (NT = 1 or 2).
+// ---------------------------------------------------------------------------
+// W_A^T staging for the tensor-core kernels: wt[hh·ws + d] = W_A[d, h0 + hh]
+// for hh < rows (0 beyond HT).  Each thread copies whole rows d of W_A (the
+// HT contiguous heads), so a warp reads consecutive rows: one coalesced
+// stream instead of a head-strided gather.
+__device__ __forceinline__ void stage_wt(unsigned short* wt, int ws, const unsigned short* wa,
+                                         int D, int H, int h0, int HT, int rows = 16) {
+  for (int d = threadIdx.x; d < D; d += blockDim.x) {
+    const unsigned short* src = wa + (size_t)d * H + h0;
+    unsigned short v[16];
+#pragma unroll
+    for (int hh = 0; hh < 16; ++hh) v[hh] = hh < HT ? __ldg(src + hh) : (unsigned short)0;
+#pragma unroll
+    for (int hh = 0; hh < 16; ++hh)
+      if (hh < rows) wt[hh * ws + d] = v[hh];
+  }
+}
+
+constexpr int kMmaWarps = 4;
+constexpr int kMmaTilesPerWarp = 2;
+constexpr int kMmaTokPerCta = kMmaWarps * kMmaTilesPerWarp * 16;
+
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const unsigned (&a)[4], unsigned b0,
+                                         unsigned b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Row stride (bf16) of W_A^T in shared memory: D padded so that the eight
+// head rows a quarter-warp reads fall in distinct bank groups.
+__host__ __device__ inline int mma_wt_stride(int D) { return D + ((32 - D % 64) + 64) % 64; }
+
+template <int NT>
+__global__ void __launch_bounds__(kMmaWarps * 32)
+score_mma_kernel(const __nv_bfloat16* __restrict__ X, const __nv_bfloat16* __restrict__ WA,
+                 float2* __restrict__ z, int N, int D, int H, int h0, int HT) {
+  extern __shared__ uint4 wsh4[];
+  unsigned short* wt = reinterpret_cast<unsigned short*>(wsh4);
+  const int ws = mma_wt_stride(D);
+  const int b = blockIdx.y;
+  stage_wt(wt, ws, reinterpret_cast<const unsigned short*>(WA), D, H, h0, HT, NT * 8);
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int r = lane >> 2, c = lane & 3;
+  const int tok0 = blockIdx.x * kMmaTokPerCta + warp * kMmaTilesPerWarp * 16;
+  const uint4* xr[kMmaTilesPerWarp][2];
+#pragma unroll
+  for (int t = 0; t < kMmaTilesPerWarp; ++t)
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      int n = min(tok0 + t * 16 + r + 8 * q, N - 1);
+      xr[t][q] = reinterpret_cast<const uint4*>(X + ((size_t)b * N + n) * D + 8 * c);
+    }
+  const uint4* wrow[NT];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+    wrow[nt] = reinterpret_cast<const uint4*>(wt + (nt * 8 + r) * ws + 8 * c);
+
+  float hi[kMmaTilesPerWarp][NT][4], lo[kMmaTilesPerWarp][NT][4];
+#pragma unroll
+  for (int t = 0; t < kMmaTilesPerWarp; ++t)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) hi[t][nt][i] = lo[t][nt][i] = 0.f;
+
+#pragma unroll 2
+  for (int d0 = 0; d0 < D; d0 += 32) {
+    uint4 xa[kMmaTilesPerWarp][2];
+#pragma unroll
+    for (int t = 0; t < kMmaTilesPerWarp; ++t)
+#pragma unroll
+      for (int q = 0; q < 2; ++q) xa[t][q] = __ldg(xr[t][q] + d0 / 8);
+    uint4 wb[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) wb[nt] = wrow[nt][d0 / 8];
+#pragma unroll
+    for (int t = 0; t < kMmaTilesPerWarp; ++t) {
+      const unsigned a1[4] = {xa[t][0].x, xa[t][1].x, xa[t][0].y, xa[t][1].y};
+      const unsigned a2[4] = {xa[t][0].z, xa[t][1].z, xa[t][0].w, xa[t][1].w};
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_bf16(acc, a1, wb[nt].x, wb[nt].y);
+        mma_bf16(acc, a2, wb[nt].z, wb[nt].w);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) two_sum_acc(hi[t][nt][i], lo[t][nt][i], acc[i]);
+      }
+    }
+  }
+  // Accumulator i of a tile: token r + 8·(i >> 1), head 2c + (i & 1).
+#pragma unroll
+  for (int t = 0; t < kMmaTilesPerWarp; ++t)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int n = tok0 + t * 16 + r + 8 * (i >> 1);
+        const int hh = nt * 8 + 2 * c + (i & 1);
+        if (n < N && hh < HT)
+          z[((size_t)b * H + h0 + hh) * N + n] = make_float2(hi[t][nt][i], lo[t][nt][i]);
+      }
+}
+
+// ---------------------------------------------------------------------------
+// TMA-fed bf16 score (the long workloads).  A persistent CTA streams tiles of
+// 64 tokens × 64 d of X through an 8-stage shared-memory ring: one producer
+// warp issues a 2-D tensor copy (128-byte swizzle) per stage, four consumer
+// warps (16 tokens each) read their A fragments with ldmatrix and run the
+// same slice-wise MMA + TwoSum as score_mma_kernel.  Loads thus run up to
+// eight stages ahead of the math, independent of the consumer registers.
+// ---------------------------------------------------------------------------
+constexpr int kTsRows = 64, kTsCols = 64, kTsStages = 8, kTsConsumers = 4;
+constexpr int kTsThreads = (kTsConsumers + 1) * 32;
+constexpr int kTsStageBytes = kTsRows * kTsCols * 2;
+
+__host__ __device__ inline int ts_wt_stride(int D) { return D + 8; }
+static size_t score_tma_smem(int D) {
+  return (size_t)kTsStages * kTsStageBytes + (size_t)16 * ts_wt_stride(D) * 2 + 2 * kTsStages * 8 +
+         1024;
+}
+
+__device__ __forceinline__ void ldmatrix_x4(unsigned (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+template <int NT>
+__global__ void __launch_bounds__(kTsThreads)
+score_tma_kernel(const __grid_constant__ CUtensorMap tmX, const __nv_bfloat16* __restrict__ WA,
+                 float2* __restrict__ z, int N, int D, int H, int h0, int HT, int rows_total,
+                 unsigned int* status) {
+  extern __shared__ __align__(1024) unsigned char sm_raw[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~(uintptr_t)1023);
+  unsigned char* stages = sm;
+  const int ws = ts_wt_stride(D);
+  unsigned short* wt = reinterpret_cast<unsigned short*>(sm + kTsStages * kTsStageBytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(wt + 16 * ws);
+  uint64_t* empty = full + kTsStages;
+  stage_wt(wt, ws, reinterpret_cast<const unsigned short*>(WA), D, H, h0, HT);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kTsStages; ++s) {
+      mbar_init(full + s, 1);
+      mbar_init(empty + s, kTsConsumers);
+    }
+  }
+  mbar_fence_init();
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nkb = D / kTsCols;
+  const int ntiles = (rows_total + kTsRows - 1) / kTsRows;
+
+  if (warp == kTsConsumers) {   // producer
+    if (lane == 0) {
+      int it = 0;
+      for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x)
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int s = it % kTsStages, use = it / kTsStages;
+          if (use > 0 && !mbar_wait(empty + s, (use - 1) & 1, status, 0x601)) return;
+          mbar_expect_tx(full + s, kTsStageBytes);
+          tma_load_2d(stages + s * kTsStageBytes, &tmX, kb * kTsCols, tile * kTsRows, full + s);
+        }
+    }
+    return;
+  }
+
+  const int c = lane & 3, mrow = lane >> 2;
+  const int lm = lane >> 3, li = lane & 7;
+  const int arow = warp * 16 + (lm & 1) * 8 + li;   // ldmatrix row this lane addresses
+  int it = 0;
+  for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+    float hi[NT][4], lo[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) hi[nt][i] = lo[nt][i] = 0.f;
+    for (int kb = 0; kb < nkb; ++kb, ++it) {
+      const int s = it % kTsStages;
+      if (!mbar_wait(full + s, (it / kTsStages) & 1, status, 0x602)) return;
+      const uint32_t base = smem_addr(stages + s * kTsStageBytes) + arow * 128;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        float acc[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) acc[nt][i] = 0.f;
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const int t = 2 * half + q;            // 16-wide k step within the 64
+          const int chunk = 2 * t + (lm >> 1);
+          unsigned a[4];
+          ldmatrix_x4(a, base + ((chunk ^ (arow & 7)) << 4));
+          const int k0 = kb * kTsCols + 16 * t + 2 * c;
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            const unsigned short* wr = wt + (nt * 8 + mrow) * ws + k0;
+            const unsigned b0 = *reinterpret_cast<const unsigned*>(wr);
+            const unsigned b1 = *reinterpret_cast<const unsigned*>(wr + 8);
+            mma_bf16(acc[nt], a, b0, b1);
+          }
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) two_sum_acc(hi[nt][i], lo[nt][i], acc[nt][i]);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty + s);
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int r = tile * kTsRows + warp * 16 + mrow + 8 * (i >> 1);
+        const int hh = nt * 8 + 2 * c + (i & 1);
+        if (r < rows_total && hh < HT) {
+          const int b = r / N, n = r - b * N;
+          z[((size_t)b * H + h0 + hh) * N + n] = make_float2(hi[nt][i], lo[nt][i]);
+        }
+      }
+  }
+}
+
+static bool score_tma_ok(const cat_plan_s* p, const void* X) {
+  return p->dtype == 1 && p->D % 64 == 0 && ((uintptr_t)X % 16) == 0 &&
+         score_tma_smem(p->D) <= (226u << 10);
+}
+
+static cudaError_t score_tma(const cat_plan_s* p, const void* X, const void* WA, bool setup) {
+  if (setup) {
+    cudaError_t e = allow_max_smem(score_tma_kernel<1>);
+    return e == cudaSuccess ? allow_max_smem(score_tma_kernel<2>) : e;
+  }
+  CUtensorMap tm;
+  const unsigned long long rows = (unsigned long long)p->B * p->N;
+  if (!encode_map_2d_sw128(&tm, X, (unsigned long long)p->D, rows, (unsigned long long)p->D * 2,
+                           kTsCols, kTsRows))
+    return cudaErrorInvalidValue;
+  const int ntiles = (int)((rows + kTsRows - 1) / kTsRows);
+  const size_t smem = score_tma_smem(p->D);
+  const int per_sm = smem <= (113u << 10) ? 2 : 1;
+  const int grid = ntiles < per_sm * p->sms ? ntiles : per_sm * p->sms;
+  for (int h0 = 0; h0 < p->H; h0 += 16) {
+    const int ht = p->H - h0 < 16 ? p->H - h0 : 16;
+    if (ht > 8)
+      score_tma_kernel<2><<<grid, kTsThreads, smem, p->stream>>>(
+          tm, (const __nv_bfloat16*)WA, p->z2, p->N, p->D, p->H, h0, ht, (int)rows, p->status);
+    else
+      score_tma_kernel<1><<<grid, kTsThreads, smem, p->stream>>>(
+          tm, (const __nv_bfloat16*)WA, p->z2, p->N, p->D, p->H, h0, ht, (int)rows, p->status);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+static size_t score_mma_smem(int D) { return (size_t)16 * mma_wt_stride(D) * 2; }
+
+static bool score_mma_ok(const cat_plan_s* p, const void* X) {
+  return p->dtype == 1 && p->D % 32 == 0 && ((uintptr_t)X % 16) == 0 &&
+         score_mma_smem(p->D) <= (200u << 10);
+}
+
+static cudaError_t score_mma(const cat_plan_s* p, const void* X, const void* WA, bool setup) {
+  if (setup) {
+    cudaError_t e = allow_max_smem(score_mma_kernel<1>);
+    return e == cudaSuccess ? allow_max_smem(score_mma_kernel<2>) : e;
+  }
+  dim3 grid((p->N + kMmaTokPerCta - 1) / kMmaTokPerCta, p->B);
+  for (int h0 = 0; h0 < p->H; h0 += 16) {
+    const int ht = p->H - h0 < 16 ? p->H - h0 : 16;
+    const size_t smem = score_mma_smem(p->D);
+    if (ht > 8)
+      score_mma_kernel<2><<<grid, kMmaWarps * 32, smem, p->stream>>>(
+          (const __nv_bfloat16*)X, (const __nv_bfloat16*)WA, p->z2, p->N, p->D, p->H, h0, ht);
+    else
+      score_mma_kernel<1><<<grid, kMmaWarps * 32, smem, p->stream>>>(
+          (const __nv_bfloat16*)X, (const __nv_bfloat16*)WA, p->z2, p->N, p->D, p->H, h0, ht);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
 template <typename T>
 static bool score_vec_ok(const cat_plan_s* p, const void* X) {
   const int V = 16 / (int)sizeof(T);
@@ -203,6 +507,9 @@ static cudaError_t score_dispatch(const cat_plan_s* p, const T* X, const T* WA, 
 
 cudaError_t launch_score(const cat_plan_s* p, const void* X, const void* WA) {
   if (p->B == 0) return cudaSuccess;
+  if (!p->score_cuda_cores && p->score_path != 1 && score_tma_ok(p, X))
+    return score_tma(p, X, WA, false);
+  if (score_mma_ok(p, X) && !p->score_cuda_cores) return score_mma(p, X, WA, false);
   if (p->dtype == 1)
     return score_dispatch(p, (const __nv_bfloat16*)X, (const __nv_bfloat16*)WA, false);
   return score_dispatch(p, (const float*)X, (const float*)WA, false);
@@ -219,32 +526,91 @@ __device__ __forceinline__ float exp_shifted(float2 zhl, float m) {
   return fmaf(e, err + zhl.y, e);
 }
 
-// Softmax over the N tokens of each (b, h) row, one CTA per row, streaming
-// through global memory: m = max of the scores, S = sum of exp(z - m), then
-// z* = exp(z - m) / S written to zs.
-__global__ void __launch_bounds__(1024)
-softmax_kernel(const float2* __restrict__ z, float* __restrict__ zs, int N) {
-  __shared__ float red[32];
-  const float2* row = z + (size_t)blockIdx.x * N;
-  float* out = zs + (size_t)blockIdx.x * N;
-  float m = -INFINITY;
-  for (int n = threadIdx.x; n < N; n += blockDim.x) m = fmaxf(m, row[n].x);
-  m = block_reduce<true>(m, red);
-  float s = 0.f;
-  for (int n = threadIdx.x; n < N; n += blockDim.x) {
-    float e = exp_shifted(row[n], m);
-    out[n] = e;
-    s += e;
-  }
-  s = block_reduce<false>(s, red);
-  const float inv = 1.0f / s;
-  for (int n = threadIdx.x; n < N; n += blockDim.x) out[n] *= inv;
+// Softmax over the N tokens of each (b, h) row, split over P CTAs per row
+// (about 2048 tokens each).  softmax_partial: per chunk c, m_c = max of the
+// scores and s_c = sum of exp(z - m_c).  softmax_finish: every CTA combines
+// its row's partials into m = max m_c and S = sum s_c·exp(m_c - m), then
+// writes z* = exp(z - m) / S for its chunk.
+constexpr int kSoftmaxThreads = 256;
+
+__device__ __forceinline__ void chunk_range(int N, int P, int c, int& n0, int& n1) {
+  const int len = (N + P - 1) / P;
+  n0 = min(N, c * len);
+  n1 = min(N, n0 + len);
 }
 
+// Each thread owns at most 8 tokens of its chunk (chunks hold at most
+// 2048 = 256·8 tokens); its loads are all issued before any use.
+constexpr int kSoftmaxPer = 8;
+
+__global__ void __launch_bounds__(kSoftmaxThreads)
+softmax_partial(const float2* __restrict__ z, float2* __restrict__ part, int N, int P) {
+  __shared__ float red[32];
+  const int row = blockIdx.x / P, c = blockIdx.x % P;
+  int n0, n1;
+  chunk_range(N, P, c, n0, n1);
+  const float2* zr = z + (size_t)row * N;
+  float2 v[kSoftmaxPer];
+  float m = -INFINITY;
+#pragma unroll
+  for (int k = 0; k < kSoftmaxPer; ++k) {
+    const int n = n0 + threadIdx.x + k * kSoftmaxThreads;
+    v[k] = n < n1 ? zr[n] : make_float2(-INFINITY, 0.f);
+  }
+#pragma unroll
+  for (int k = 0; k < kSoftmaxPer; ++k) m = fmaxf(m, v[k].x);
+  m = block_reduce<true>(m, red);
+  float s = 0.f;
+  if (m > -INFINITY) {
+#pragma unroll
+    for (int k = 0; k < kSoftmaxPer; ++k)
+      if (n0 + threadIdx.x + k * kSoftmaxThreads < n1) s += exp_shifted(v[k], m);
+  }
+  s = block_reduce<false>(s, red);
+  if (threadIdx.x == 0) part[blockIdx.x] = make_float2(m, s);
+}
+
+__global__ void __launch_bounds__(kSoftmaxThreads)
+softmax_finish(const float2* __restrict__ z, const float2* __restrict__ part, float* __restrict__ zs,
+               int N, int P) {
+  __shared__ float red[32];
+  const int row = blockIdx.x / P, c = blockIdx.x % P;
+  int n0, n1;
+  chunk_range(N, P, c, n0, n1);
+  const float2* zr = z + (size_t)row * N;
+  float2 v[kSoftmaxPer];
+#pragma unroll
+  for (int k = 0; k < kSoftmaxPer; ++k) {
+    const int n = n0 + threadIdx.x + k * kSoftmaxThreads;
+    v[k] = n < n1 ? zr[n] : make_float2(0.f, 0.f);
+  }
+  const float2* pr = part + (size_t)row * P;
+  float m = -INFINITY;
+  for (int i = threadIdx.x; i < P; i += blockDim.x) m = fmaxf(m, pr[i].x);
+  m = block_reduce<true>(m, red);
+  float S = 0.f;
+  for (int i = threadIdx.x; i < P; i += blockDim.x) {
+    float2 q = pr[i];
+    if (q.y > 0.f) S += q.y * expf(q.x - m);
+  }
+  S = block_reduce<false>(S, red);
+  const float inv = 1.0f / S;
+  float* out = zs + (size_t)row * N;
+#pragma unroll
+  for (int k = 0; k < kSoftmaxPer; ++k) {
+    const int n = n0 + threadIdx.x + k * kSoftmaxThreads;
+    if (n < n1) out[n] = exp_shifted(v[k], m) * inv;
+  }
+}
+
+int softmax_parts(int N) { return (N + 2047) / 2048; }
+
 cudaError_t launch_softmax(const cat_plan_s* p) {
-  int rows = p->B * p->H;
+  const int rows = p->B * p->H;
   if (rows == 0) return cudaSuccess;
-  softmax_kernel<<<rows, 1024, 0, p->stream>>>(p->z2, p->zs, p->N);
+  const int P = softmax_parts(p->N);
+  softmax_partial<<<rows * P, kSoftmaxThreads, 0, p->stream>>>(p->z2, p->part, p->N, P);
+  softmax_finish<<<rows * P, kSoftmaxThreads, 0, p->stream>>>(p->z2, p->part, p->zs, p->N, P);
   return cudaGetLastError();
 }
 
@@ -292,6 +658,11 @@ softmax_spectrum_kernel(const float2* __restrict__ z, float* __restrict__ zs,
 }
 
 cudaError_t setup_score_kernels(const cat_plan_s* p) {
+  if (p->dtype == 1) {
+    cudaError_t e0 = score_mma(p, nullptr, nullptr, true);
+    if (e0 == cudaSuccess) e0 = score_tma(p, nullptr, nullptr, true);
+    if (e0 != cudaSuccess) return e0;
+  }
   cudaError_t e = p->dtype == 1
       ? score_dispatch<__nv_bfloat16>(p, nullptr, nullptr, true)
       : score_dispatch<float>(p, nullptr, nullptr, true);

@@ -289,3 +289,20 @@ def test_fast_path_chunks(monkeypatch):
             outs.append(p.forward(X, WA, V))
             p.sync()
     assert torch.equal(outs[0], outs[1])
+
+
+@pytest.mark.parametrize("score", ["tma", "mma", "cuda"])
+@pytest.mark.parametrize("cfg", [dict(B=4, N=1024, D=768, H=12, wa_scale=8.0),
+                                 dict(B=2, N=2048, D=1024, H=16, wa_scale=1.0),
+                                 dict(B=1, N=512, D=96, H=3, wa_scale=8.0),
+                                 dict(B=3, N=100, D=128, H=32, wa_scale=8.0)])
+def test_bf16_score_kernels(monkeypatch, score, cfg):
+    """All three bf16 score kernels (TMA-fed tensor-core slices, register-fed
+    tensor-core slices, CUDA-core runs; each with a double-float total) meet
+    the z* bound, peaked case and ragged token tiles included."""
+    if score == "tma":
+        monkeypatch.delenv("CAT_SCORE", raising=False)
+    else:
+        monkeypatch.setenv("CAT_SCORE", score)
+    errO, errZ = parity(dtype="bf16", seed=41, mode="fft", **cfg)
+    print("score=%s %s: dO %.2e, dz* %.2e" % (score, cfg, errO, errZ))
