@@ -128,6 +128,12 @@ void free_events(cat_plan_s* p) {
 void free_plan(cat_plan_s* p) {
   if (!p) return;
   free_events(p);
+  for (int k = 0; k < 2; ++k) {
+    if (p->side[k]) cudaStreamDestroy(p->side[k]);
+    if (p->ev_join[k]) cudaEventDestroy(p->ev_join[k]);
+    if (p->ev_front[k]) cudaEventDestroy(p->ev_front[k]);
+  }
+  if (p->ev_fork) cudaEventDestroy(p->ev_fork);
   cudaFree(p->z2);
   cudaFree(p->zs);
   cudaFree(p->part);
@@ -135,6 +141,7 @@ void free_plan(cat_plan_s* p) {
   cudaFree(p->tw);
   cudaFree(p->scratch);
   cudaFree(p->zscr);
+  cudaFree(p->tabs);
   cudaFree(p->status);
   cudaFree(p->hx);
   cudaFree(p->hwa);
@@ -171,15 +178,20 @@ int choose_path(cat_plan_s* p) {
       f.G = 32;
       f.groups = 1;
       f.P = 32;
+      // Chunks of (b, h) rows stay inside one batch; two scratch slots let
+      // two chunks be in flight on the plan's two internal streams.
+      // With two or more batches, whole batches alternate between the two
+      // streams (a chunk is a batch's heads, as far as the scratch budget
+      // allows); with one batch, single heads alternate.
       const size_t per_bh = (size_t)N * 32 * sizeof(float2);
-      long chunk = (long)(kFastScratchBudget / per_bh);
+      long chunk = p->B >= 2 ? (long)(kFastScratchBudget / per_bh) : 1;
       if (const char* env = std::getenv("CAT_CHUNK_BH")) chunk = std::atol(env);
       if (chunk < 1) chunk = 1;
-      const long rows = (long)p->B * p->H;
-      if (chunk > rows) chunk = rows > 0 ? rows : 1;
+      if (chunk > p->H) chunk = p->H;
       f.chunk_bh = (int)chunk;
-      p->scratch_bytes = (size_t)f.chunk_bh * per_bh;
-      p->launches = score_launches(p->H, p->D) + 4 + 3 * (int)((rows + chunk - 1) / chunk);
+      p->scratch_bytes = 2 * (size_t)f.chunk_bh * per_bh;
+      const int chunks_per_batch = (int)((p->H + chunk - 1) / chunk);
+      p->launches = p->B * (score_launches(p->H, p->D) + 4 + 3 * chunks_per_batch);
       return CAT_OK;
     }
   }
@@ -319,6 +331,47 @@ int validate(int B, int N, int D, int H, int dtype) { return validate_shape(B, N
 
 extern "C" {
 
+namespace {
+
+// Fast path, overlapped schedule on the plan's two internal streams: batch b
+// (score, softmax, spectrum of z*) goes to stream b mod 2, and the chunks of
+// its rows alternate between the streams, each stream using its own scratch
+// slot; a chunk on the other stream first waits for the batch's spectrum.
+// The streams fork from and join back into the plan's stream.
+cudaError_t run_fast_overlapped(cat_plan_s* p, const void* X, const void* WA, const void* V,
+                                void* O) {
+  cudaError_t e = cudaEventRecord(p->ev_fork, p->stream);
+  for (int k = 0; k < 2 && e == cudaSuccess; ++k) e = cudaStreamWaitEvent(p->side[k], p->ev_fork, 0);
+  int g = 0;
+  for (int b = 0; b < p->B && e == cudaSuccess; ++b) {
+    const int kb = b & 1;
+    cudaStream_t sb = p->side[kb];
+    cat::Span sp;
+    sp.b0 = b;
+    sp.nbat = 1;
+    sp.st = sb;
+    sp.own = true;
+    e = cat::launch_score(p, X, WA, sp);
+    if (e == cudaSuccess) e = cat::launch_softmax(p, sp);
+    if (e == cudaSuccess) e = cat::launch_fast_zspec(p, b * p->H, p->H, sb);
+    if (e == cudaSuccess) e = cudaEventRecord(p->ev_front[kb], sb);
+    for (int h0 = 0; h0 < p->H && e == cudaSuccess; h0 += p->fs.chunk_bh, ++g) {
+      const int nb = p->H - h0 < p->fs.chunk_bh ? p->H - h0 : p->fs.chunk_bh;
+      const int k = g & 1;
+      if (k != kb) e = cudaStreamWaitEvent(p->side[k], p->ev_front[kb], 0);
+      if (e == cudaSuccess) e = cat::launch_fast_chunk(p, V, O, b * p->H + h0, nb, k, p->side[k]);
+    }
+  }
+  for (int k = 0; k < 2; ++k) {
+    cudaError_t e2 = cudaEventRecord(p->ev_join[k], p->side[k]);
+    if (e2 == cudaSuccess) e2 = cudaStreamWaitEvent(p->stream, p->ev_join[k], 0);
+    if (e == cudaSuccess) e = e2;
+  }
+  return e;
+}
+
+}  // namespace
+
 int cat_plan_create(cat_plan_t* out, int B, int N, int D, int H, int dtype, void* stream) {
   if (!out) return CAT_ERR_INVALID_ARG;
   *out = nullptr;
@@ -355,11 +408,14 @@ int cat_plan_create(cat_plan_t* out, int B, int N, int D, int H, int dtype, void
   if (ok && (p->path == cat::PATH_SMEM || p->path == cat::PATH_FAST))
     ok = alloc((void**)&p->zf, rowsN * sizeof(float2));
   if (ok && p->path == cat::PATH_FAST) ok = alloc((void**)&p->zscr, rowsN * sizeof(float2));
+  if (ok && p->path == cat::PATH_FAST)
+    ok = alloc((void**)&p->tabs, cat::fast_tables_bytes(p->fs.N2));
   if (ok && p->path != cat::PATH_SMEM) ok = alloc((void**)&p->scratch, p->scratch_bytes);
   if (!ok) { cudaGetLastError(); free_plan(p); return CAT_ERR_ALLOC; }
   p->workspace_bytes = rowsN * (sizeof(float) + sizeof(float2)) + (size_t)N * sizeof(float2) +
                        (p->zf ? rowsN * sizeof(float2) : 0) +
-                       (p->zscr ? rowsN * sizeof(float2) : 0) + p->scratch_bytes;
+                       (p->zscr ? rowsN * sizeof(float2) : 0) + p->scratch_bytes +
+                       (p->tabs ? cat::fast_tables_bytes(p->fs.N2) : 0);
 
   // Twiddle table exp(-2πi j/N), evaluated in fp64 and rounded once.
   std::vector<float2> tw((size_t)N);
@@ -375,6 +431,14 @@ int cat_plan_create(cat_plan_t* out, int B, int N, int D, int H, int dtype, void
     e = p->path == cat::PATH_SMEM       ? cat::setup_smem_kernels(p)
         : p->path == cat::PATH_FOURSTEP ? cat::setup_fourstep_kernels(p)
                                         : cat::setup_fast_kernels(p);
+  if (e == cudaSuccess && p->path == cat::PATH_FAST) {
+    for (int k = 0; k < 2 && e == cudaSuccess; ++k) {
+      e = cudaStreamCreateWithFlags(&p->side[k], cudaStreamNonBlocking);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_join[k], cudaEventDisableTiming);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_front[k], cudaEventDisableTiming);
+    }
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_fork, cudaEventDisableTiming);
+  }
   if (e != cudaSuccess) { free_plan(p); return CAT_ERR_CUDA; }
   describe(p);
   if (std::getenv("CAT_LOG")) std::fprintf(stderr, "[cat] %s\n", p->desc);
@@ -414,6 +478,7 @@ int cat_forward(cat_plan_t p, const void* X, const void* WA, const void* V, void
     return CAT_ERR_ALIAS;
   cudaEvent_t* ev = nullptr;
   if (p->timing_n < p->timing_cap) ev = p->ev + 4 * p->timing_n++;
+  if (!ev && p->path == cat::PATH_FAST) return map_cuda(run_fast_overlapped(p, X, WA, V, O));
   if (ev) cudaEventRecord(ev[0], p->stream);
   cudaError_t e = cat::launch_score(p, X, WA);
   if (e != cudaSuccess) return CAT_ERR_CUDA;

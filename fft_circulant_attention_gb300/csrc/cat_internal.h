@@ -44,7 +44,7 @@ struct FourStepCfg {
 }  // namespace cat
 
 struct cat_plan_s {
-  CUtensorMap tm_c;         // fast path: scratch view for pass C (TMA)
+  CUtensorMap tm_c[2];      // fast path: scratch views for pass C (TMA), per slot
   int B, N, D, H, dtype;
   int dh, npair;            // head width, packed pairs per head = ceil(dh/2)
   int device;
@@ -63,8 +63,13 @@ struct cat_plan_s {
   float2* zf;               // [B, H, N] spectrum of z* divided by N (smem path)
   float2* tw;               // [N] exp(-2πi j/N)
   float2* zscr;             // [B, H, N] fast path: z* after its first DFT pass
-  float2* scratch;          // four-step scratch, chunk_bh·N·P complex
+  float2* tabs;             // fast path: pass-B twiddle tables
+  float2* scratch;          // four-step scratch, chunk_bh·N·P complex (fast path: 2 slots)
   size_t scratch_bytes;
+  // fast path: two internal streams that run alternate batches / chunks so
+  // that one's score and small kernels overlap the other's FFT passes
+  cudaStream_t side[2];
+  cudaEvent_t ev_fork, ev_join[2], ev_front[2];
   unsigned int* status;     // device status word
   size_t workspace_bytes;
   // device staging for host-buffer calls (allocated at the first such call)
@@ -87,6 +92,17 @@ int softmax_parts(int N);
 
 namespace cat {
 
+// A range of batches and the stream its work goes to (default: all batches,
+// the plan's stream).
+struct Span {
+  int b0 = 0;
+  int nbat = -1;                 // -1: through the last batch
+  cudaStream_t st = nullptr;
+  bool own = false;              // true: use st instead of the plan's stream
+  int nb(const cat_plan_s* p) const { return nbat < 0 ? p->B - b0 : nbat; }
+  cudaStream_t stream(const cat_plan_s* p) const { return own ? st : p->stream; }
+};
+
 // Let `kernel` use all the dynamic shared memory the current device allows
 // a block (its opt-in limit minus the kernel's static shared memory).  The
 // limit is a property of the kernel, shared by every plan in the process,
@@ -106,12 +122,19 @@ cudaError_t allow_max_smem(K kernel) {
 }
 
 // Launchers (enqueue on plan->stream).  Each returns cudaGetLastError().
-cudaError_t launch_score(const cat_plan_s* p, const void* X, const void* WA);
-cudaError_t launch_softmax(const cat_plan_s* p);
+cudaError_t launch_score(const cat_plan_s* p, const void* X, const void* WA,
+                         const Span& sp = Span{});
+cudaError_t launch_softmax(const cat_plan_s* p, const Span& sp = Span{});
 cudaError_t launch_softmax_spectrum(const cat_plan_s* p);
 cudaError_t launch_conv_smem(const cat_plan_s* p, const void* V, void* O);
 cudaError_t launch_fourstep_conv(const cat_plan_s* p, const void* V, void* O);
 cudaError_t launch_fast_conv(const cat_plan_s* p, const void* V, void* O);
+// Fast path pieces for the overlapped schedule: the spectrum of z* for
+// (b, h) rows [row0, row0 + nrows), and passes A, B, C of one chunk of rows
+// [bh0, bh0 + nb) with scratch buffer `slot`, all on stream st.
+cudaError_t launch_fast_zspec(const cat_plan_s* p, int row0, int nrows, cudaStream_t st);
+cudaError_t launch_fast_chunk(const cat_plan_s* p, const void* V, void* O, int bh0, int nb,
+                              int slot, cudaStream_t st);
 
 // Shape validation and shared-memory-path configuration without allocation.
 int validate(int B, int N, int D, int H, int dtype);
@@ -122,5 +145,6 @@ cudaError_t setup_score_kernels(const cat_plan_s* p);
 cudaError_t setup_smem_kernels(const cat_plan_s* p);
 cudaError_t setup_fourstep_kernels(const cat_plan_s* p);
 cudaError_t setup_fast_kernels(cat_plan_s* p);
+size_t fast_tables_bytes(int N2);
 
 }  // namespace cat

@@ -226,12 +226,13 @@ fsf_pass_a32(const __grid_constant__ CUtensorMap tmV, float2* __restrict__ scr,
   __syncwarp();
   const int gw = blockIdx.x * kPipeWarps + warp, G = gridDim.x * kPipeWarps;
   const int items = nb * kFastN1;
+  const uint64_t keep = policy_evict_last(), stream = policy_evict_first();
   auto issue = [&](int s, int item) {
     if (lane == 0) {
       const int bh = bh0 + item % nb, n1 = item / nb;
       const int b = bh / H, h = bh - b * H;
       mbar_expect_tx(bar + s, 32 * P::kRowBytes);
-      tma_load_4d(stage + s * 32 * P::kRowBytes, &tmV, h * 64, n1, 0, b, bar + s);
+      tma_load_4d_hint(stage + s * 32 * P::kRowBytes, &tmV, h * 64, n1, 0, b, bar + s, stream);
     }
   };
 #pragma unroll
@@ -254,15 +255,16 @@ fsf_pass_a32(const __grid_constant__ CUtensorMap tmV, float2* __restrict__ scr,
     twrow[lane] = tw;
     __syncwarp();
 #pragma unroll
-    for (int k2 = 0; k2 < 32; ++k2) scr[scr_idx(bhl, 32, k2, n1, lane)] = cmul(a[k2], twrow[k2]);
+    for (int k2 = 0; k2 < 32; ++k2)
+      st_hint(scr + scr_idx(bhl, 32, k2, n1, lane), cmul(a[k2], twrow[k2]), keep);
     __syncwarp();
   }
 }
 
 template <typename T>
 __global__ void __launch_bounds__(PipeC::kWarps * 32)
-fsf_pass_c32(const __grid_constant__ CUtensorMap tmC, T* __restrict__ O, int N, int D, int H,
-             int bh0, int nb, unsigned int* status) {
+fsf_pass_c32(const __grid_constant__ CUtensorMap tmC, const float2* __restrict__ scr,
+             T* __restrict__ O, int N, int D, int H, int bh0, int nb, unsigned int* status) {
   using P = PipeC;
   extern __shared__ __align__(128) unsigned char sm[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -295,6 +297,13 @@ fsf_pass_c32(const __grid_constant__ CUtensorMap tmC, T* __restrict__ O, int N, 
     __syncwarp();
     const int next = item + P::kStages * G;
     if (next < items) issue(s, next);
+    {
+      // The item's 32 scratch rows (256 B = two lines each) are dead now:
+      // drop them from L2 without a write-back.
+      const float2* r = scr + scr_idx(item % nb, 32, lane, item / nb, 0);
+      discard_l2(r);
+      discard_l2(r + 16);
+    }
     const int bh = bh0 + item % nb, n1 = item / nb;
     const int b = bh / H, h = bh - b * H;
     T* dst = O + ((size_t)b * N + n1) * D + h * 64 + 2 * lane;
@@ -305,54 +314,69 @@ fsf_pass_c32(const __grid_constant__ CUtensorMap tmC, T* __restrict__ O, int N, 
 }
 
 // ---------------------------------------------------------------------------
-// Pass B: per (b, h, k2) and half of the head's pairs (16 signals of length
-// 512).  Forward: step F1 (radix 32, span 1; thread j task j), step F2
+// Pass B: per (b, h, k2) and a group of kBPairs of the head's pairs (signals
+// of length 512, 16 threads each).  Forward: step F1 (radix 32, span 1; thread j task j), step F2
 // (radix 16, span 32; tasks 2j, 2j+1).  Product with the spectrum of z*.
 // Inverse: step I1 (radix 16, span 1; tasks 2j, 2j+1 — exactly the bins the
 // thread holds), step I2 (radix 32, span 16; task j), leaving n1 = j + 16s.
-// Lane l: pair (l & 15) of the half, j = 2·warp + (l >> 4).
+// Lane l: pair l mod kBPairs of the group, j = (32/kBPairs)·warp + l/kBPairs.
 // Everything the compute steps read besides the exchange buffer — the
 // length-512 twiddles, the row w_N^{n1·k2} and the spectrum of z* at this
 // k2 — is loaded into shared memory at the start, together with the 32
 // scratch values, so no global load waits inside the transforms.
 // ---------------------------------------------------------------------------
-constexpr size_t kSmemB = (size_t)16 * kRowB * sizeof(float2) + 3 * kFastN1 * sizeof(float2);
+constexpr int kBPairs = 16;  // pairs (signals) per pass-B CTA; 16 threads each
+// Shared tables of pass B, all in the order the threads read them (float2):
+//   tf[k][u]  = w_512^{u·k}           k < 32, u < 16   (step F2)
+//   ti[j][u]  = w_512^{u·j}           j < 16, u < 32   (step I2, conjugated)
+//   tx[j][q]  = w_N^{(j+16q)·k2}      j < 16, q < 32   (inter-pass, conjugated)
+//   zf[j][q][e] = FFT(z*)/N at k1 = 2j + e + 32q       (the product)
+// tf and ti are the same for every CTA and tx for every CTA of one k2; the
+// plan builds them once (fast_tables).  Each is 4 KB.
+constexpr int kTabB = 512;   // complex entries per table
+constexpr size_t kSmemB =
+    (size_t)kBPairs * kRowB * sizeof(float2) + 4 * kTabB * sizeof(float2);
 
-__global__ void __launch_bounds__(256, 2)
-fsf_pass_b(float2* __restrict__ scr, const float2* __restrict__ zft, const float2* __restrict__ W,
-           int N, int N2, int bh0) {
+__global__ void __launch_bounds__(kBPairs * 16, 2)
+fsf_pass_b(float2* __restrict__ scr, const float2* __restrict__ zft,
+           const float2* __restrict__ tabs, int N2, int bh0) {
+  constexpr int NT = kBPairs * 16;
   extern __shared__ float4 smem4[];
   float2* buf = reinterpret_cast<float2*>(smem4);
-  float2* tw512 = buf + 16 * kRowB;          // w_512^e, e < 512
-  float2* twk = tw512 + kFastN1;             // w_N^{n1·k2}, n1 < 512
-  float4* zsh = reinterpret_cast<float4*>(twk + kFastN1);   // FFT(z*)/N, pass-B order
+  float2* tf = buf + kBPairs * kRowB;
+  float2* ti = tf + kTabB;
+  float2* tx = ti + kTabB;
+  float2* zf = tx + kTabB;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int pl = lane & 15;
-  const int j = 2 * warp + (lane >> 4);
-  const int grp = blockIdx.x & 1;
-  const int k2 = (blockIdx.x >> 1) % N2;
-  const int bhl = (blockIdx.x >> 1) / N2;
-  const int pair = grp * 16 + pl;
-  const int wstep = N / kFastN1;
+  const int pl = lane & (kBPairs - 1);
+  const int j = (32 / kBPairs) * warp + lane / kBPairs;
+  constexpr int G = kFastPairs / kBPairs;     // CTAs per (b, h, k2)
+  const int grp = blockIdx.x % G;
+  const int k2 = (blockIdx.x / G) % N2;
+  const int bhl = (blockIdx.x / G) / N2;
+  const int pair = grp * kBPairs + pl;
   float2* row = buf + pl * kRowB;
 
+  const uint64_t keep = policy_evict_last();
   float2 a[32];
 #pragma unroll
-  for (int u = 0; u < 32; ++u) a[u] = scr[scr_idx(bhl, N2, k2, j + 16 * u, pair)];
-  // Tables (each thread two entries of each; zft row is 256 float4).
+  for (int u = 0; u < 32; ++u) a[u] = ld_hint(scr + scr_idx(bhl, N2, k2, j + 16 * u, pair), keep);
+  // Tables: 4 x 4 KB, one 16-byte load of each per thread (NT = 256).
   const int t = threadIdx.x;
-  const float2 w0 = __ldg(&W[(size_t)t * wstep]), w1 = __ldg(&W[(size_t)(t + 256) * wstep]);
-  const float2 v0 = __ldg(&W[(size_t)t * k2]), v1 = __ldg(&W[(size_t)(t + 256) * k2]);
-  const float4 zq = __ldg(reinterpret_cast<const float4*>(zft) +
+  const float4* g4 = reinterpret_cast<const float4*>(tabs);
+  const float4 q0 = __ldg(g4 + t);                                   // tf, ti
+  const float4 q1 = __ldg(g4 + 256 + t);
+  const float4 q2 = __ldg(g4 + 512 + (size_t)k2 * 256 + t);          // tx of this k2
+  const float4 q3 = __ldg(reinterpret_cast<const float4*>(zft) +
                           ((size_t)(bh0 + bhl) * N2 + k2) * (kFastN1 / 2) + t);
   dft<32, false>(a);
 #pragma unroll
   for (int q = 0; q < 32; q += 2) st_sh2(row + 32 * j + q, a[q], a[q + 1]);
-  tw512[t] = w0;
-  tw512[t + 256] = w1;
-  twk[t] = v0;
-  twk[t + 256] = v1;
-  zsh[t] = zq;
+  float4* tf4 = reinterpret_cast<float4*>(tf);
+  tf4[t] = q0;
+  tf4[256 + t] = q1;
+  tf4[512 + t] = q2;
+  tf4[768 + t] = q3;
   __syncthreads();
 
   float2 c[2][16];
@@ -360,35 +384,80 @@ fsf_pass_b(float2* __restrict__ scr, const float2* __restrict__ zft, const float
   for (int u = 0; u < 16; ++u) ld_sh2(row + 2 * j + 32 * u, c[0][u], c[1][u]);
 #pragma unroll
   for (int e = 0; e < 2; ++e) {
-    const int k = 2 * j + e;
+    const float2* tw = tf + (2 * j + e) * 16;
 #pragma unroll
-    for (int u = 1; u < 16; ++u) c[e][u] = cmul(c[e][u], tw512[u * k]);
+    for (int u = 2; u < 16; u += 2) {
+      float2 w0, w1;
+      ld_sh2(tw + u, w0, w1);
+      c[e][u] = cmul(c[e][u], w0);
+      c[e][u + 1] = cmul(c[e][u + 1], w1);
+    }
+    c[e][1] = cmul(c[e][1], tw[1]);
     dft<16, false>(c[e]);
   }
   // Product with FFT(z*)/N at bins k1 = 2j + e + 32s.
 #pragma unroll
   for (int q = 0; q < 16; ++q) {
-    float4 z = zsh[j * 16 + q];
-    c[0][q] = cmul(c[0][q], make_float2(z.x, z.y));
-    c[1][q] = cmul(c[1][q], make_float2(z.z, z.w));
+    float2 z0, z1;
+    ld_sh2(zf + (j * 16 + q) * 2, z0, z1);
+    c[0][q] = cmul(c[0][q], z0);
+    c[1][q] = cmul(c[1][q], z1);
   }
   __syncthreads();
+  // Inverse step I1 writes position p = 32j + 16e + s to storage
+  // 32·(p mod 16) + p / 16 = 32s + 2j + e, so that I2's 32 inputs
+  // (positions j + 16u) sit at 32j + u: both sides move 16-byte pairs.
 #pragma unroll
-  for (int e = 0; e < 2; ++e) {
-    dft<16, true>(c[e]);
+  for (int e = 0; e < 2; ++e) dft<16, true>(c[e]);
 #pragma unroll
-    for (int q = 0; q < 16; q += 2) st_sh2(row + 32 * j + 16 * e + q, c[e][q], c[e][q + 1]);
-  }
+  for (int q = 0; q < 16; ++q) st_sh2(row + 32 * q + 2 * j, c[0][q], c[1][q]);
   __syncthreads();
 #pragma unroll
-  for (int u = 0; u < 32; ++u) a[u] = row[j + 16 * u];
+  for (int u = 0; u < 32; u += 2) ld_sh2(row + 32 * j + u, a[u], a[u + 1]);
+  {
+    const float2* tw = ti + j * 32;
 #pragma unroll
-  for (int u = 1; u < 32; ++u) a[u] = cmulc(a[u], tw512[u * j]);
+    for (int u = 2; u < 32; u += 2) {
+      float2 w0, w1;
+      ld_sh2(tw + u, w0, w1);
+      a[u] = cmulc(a[u], w0);
+      a[u + 1] = cmulc(a[u + 1], w1);
+    }
+    a[1] = cmulc(a[1], tw[1]);
+  }
   dft<32, true>(a);
+  {
+    const float2* tw = tx + j * 32;
 #pragma unroll
-  for (int q = 0; q < 32; ++q) {
-    const int n1 = j + 16 * q;
-    scr[scr_idx(bhl, N2, k2, n1, pair)] = cmulc(a[q], twk[n1]);
+    for (int q = 0; q < 32; q += 2) {
+      float2 w0, w1;
+      ld_sh2(tw + q, w0, w1);
+      st_hint(scr + scr_idx(bhl, N2, k2, j + 16 * q, pair), cmulc(a[q], w0), keep);
+      st_hint(scr + scr_idx(bhl, N2, k2, j + 16 * (q + 1), pair), cmulc(a[q + 1], w1), keep);
+    }
+  }
+}
+
+// Builds pass B's twiddle tables: [tf | ti | tx for k2 = 0..N2-1], from the
+// plan's table W[e] = exp(-2πi e/N).
+__global__ void fsf_build_tables(float2* __restrict__ tabs, const float2* __restrict__ W, int N,
+                                 int N2) {
+  const int wstep = N / kFastN1;
+  const int total = 2 * kTabB + N2 * kTabB;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
+    float2 v;
+    if (i < kTabB) {                       // tf[k][u]
+      const int k = i / 16, u = i % 16;
+      v = W[(size_t)(u * k) * wstep];
+    } else if (i < 2 * kTabB) {            // ti[j][u]
+      const int r = i - kTabB, jj = r / 32, u = r % 32;
+      v = W[(size_t)(u * jj) * wstep];
+    } else {                               // tx[k2][j][q]
+      const int r = i - 2 * kTabB, kk = r / kTabB, r2 = r % kTabB;
+      const int jj = r2 / 32, q = r2 % 32;
+      v = W[(size_t)(jj + 16 * q) * kk];
+    }
+    tabs[i] = v;
   }
 }
 
@@ -524,104 +593,141 @@ static cudaError_t setup_t(int N2) {
   return e;
 }
 
+size_t fast_tables_bytes(int N2) { return (size_t)(2 + N2) * kTabB * sizeof(float2); }
+
 cudaError_t setup_fast_kernels(cat_plan_s* p) {
   cudaError_t e = p->dtype == 1 ? setup_t<__nv_bfloat16>(p->fs.N2) : setup_t<float>(p->fs.N2);
   if (e != cudaSuccess) return e;
-  // Scratch viewed as fp32 [chunk_bh][N2 (k2)][512 (n1)][64 (32 pairs)].
+  fsf_build_tables<<<64, 256, 0, p->stream>>>(p->tabs, p->tw, p->N, p->fs.N2);
+  e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaStreamSynchronize(p->stream);
+  if (e != cudaSuccess) return e;
+  // Each scratch slot viewed as fp32 [chunk_bh][N2 (k2)][512 (n1)][64 (32 pairs)].
   const unsigned long long row = (unsigned long long)kFastPairs * sizeof(float2);
   const unsigned long long dims[4] = {2ull * kFastPairs, (unsigned long long)kFastN1,
                                       (unsigned long long)p->fs.N2,
                                       (unsigned long long)p->fs.chunk_bh};
   const unsigned long long strides[3] = {row, row * kFastN1, row * kFastN1 * p->fs.N2};
   const unsigned int box_c[4] = {64, 1, 32, 1};      // 32 rows k2 of all pairs
-  if (p->fs.N2 == 32 &&
-      !encode_map_4d(&p->tm_c, p->scratch, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dims, strides, box_c))
-    return cudaErrorInvalidValue;
+  for (int slot = 0; slot < 2; ++slot) {
+    const float2* base = p->scratch + (size_t)slot * (p->scratch_bytes / 2 / sizeof(float2));
+    if (p->fs.N2 == 32 &&
+        !encode_map_4d(&p->tm_c[slot], base, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dims, strides, box_c))
+      return cudaErrorInvalidValue;
+  }
   return cudaSuccess;
 }
 
 template <typename T, int N2>
-static void launch_ac(const cat_plan_s* p, const T* V, T* O, int bh0, int nb, bool pass_a) {
+static void launch_ac(const cat_plan_s* p, const T* V, T* O, float2* scr, int bh0, int nb,
+                      bool pass_a, cudaStream_t st) {
   const int grid = N2 == 32 ? nb * (kFastN1 / 8) : nb * kFastN1;
   const int threads = N2 == 32 ? 256 : N2;
   const size_t smem = fast_smem_a(N2);
   if (pass_a)
-    fsf_pass_a<T, N2><<<grid, threads, smem, p->stream>>>(V, p->scratch, p->tw, p->N, p->D, p->H,
-                                                         bh0, nb);
+    fsf_pass_a<T, N2><<<grid, threads, smem, st>>>(V, scr, p->tw, p->N, p->D, p->H, bh0, nb);
   else
-    fsf_pass_c<T, N2><<<grid, threads, smem, p->stream>>>(p->scratch, O, p->tw, p->N, p->D, p->H,
-                                                         bh0, nb);
+    fsf_pass_c<T, N2><<<grid, threads, smem, st>>>(scr, O, p->tw, p->N, p->D, p->H, bh0, nb);
 }
 
+// V viewed as [B][N2 (n2)][512 (n1)][D]: the box is one head's 64 columns of
+// the 32 rows n1 + 512·n2 (N2 == 32 passes).
 template <typename T>
-static cudaError_t run_t(const cat_plan_s* p, const T* V, T* O) {
-  const FourStepCfg& f = p->fs;
-  const int rows = p->B * p->H;
-  const int N2 = f.N2;
-  // V viewed as [B][N2 (n2)][512 (n1)][D]: the box is one head's 64 columns
-  // of the 32 rows n1 + 512·n2 (N2 == 32 passes).
-  CUtensorMap tmV;
-  if (N2 == 32) {
-    const unsigned long long es = sizeof(T);
-    const unsigned long long dims[4] = {(unsigned long long)p->D, (unsigned long long)kFastN1,
-                                        (unsigned long long)N2, (unsigned long long)p->B};
-    const unsigned long long strides[4 - 1] = {p->D * es, (unsigned long long)kFastN1 * p->D * es,
-                                               (unsigned long long)p->N * p->D * es};
-    const unsigned int box[4] = {64, 1, 32, 1};
-    if (!encode_map_4d(&tmV, V, sizeof(T) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                               : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
-                       dims, strides, box))
-      return cudaErrorInvalidValue;
-  }
-  // Spectrum of z*, once per (b, h).
+static bool encode_v_map(const cat_plan_s* p, const T* V, CUtensorMap* tmV) {
+  const unsigned long long es = sizeof(T);
+  const unsigned long long dims[4] = {(unsigned long long)p->D, (unsigned long long)kFastN1,
+                                      (unsigned long long)p->fs.N2, (unsigned long long)p->B};
+  const unsigned long long strides[3] = {p->D * es, (unsigned long long)kFastN1 * p->D * es,
+                                         (unsigned long long)p->N * p->D * es};
+  const unsigned int box[4] = {64, 1, 32, 1};
+  return encode_map_4d(tmV, V, sizeof(T) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                              : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                       dims, strides, box);
+}
+
+cudaError_t launch_fast_zspec(const cat_plan_s* p, int row0, int nrows, cudaStream_t st) {
+  const int N2 = p->fs.N2;
+  const float* zs = p->zs + (size_t)row0 * p->N;
+  float2* zscr = p->zscr + (size_t)row0 * p->N;
+  float2* zf = p->zf + (size_t)row0 * p->N;
   switch (N2) {
     case 32:
-      fsf_zspec_a<32><<<rows * 8, 64, 0, p->stream>>>(p->zs, p->zscr, p->tw, p->N);
+      fsf_zspec_a<32><<<nrows * 8, 64, 0, st>>>(zs, zscr, p->tw, p->N);
       break;
-#define CAT_ZA(n)                                                                          \
-  case n:                                                                                  \
-    fsf_zspec_a<n><<<rows * (kFastN1 / 32), n, fast_smem_a(n), p->stream>>>(p->zs, p->zscr, \
-                                                                             p->tw, p->N); \
+#define CAT_ZA(n)                                                                      \
+  case n:                                                                              \
+    fsf_zspec_a<n><<<nrows * (kFastN1 / 32), n, fast_smem_a(n), st>>>(zs, zscr, p->tw, \
+                                                                      p->N);           \
     break;
     CAT_ZA(64) CAT_ZA(128) CAT_ZA(256)
 #undef CAT_ZA
     default: return cudaErrorInvalidValue;
   }
-  fsf_zspec_b<<<rows * (N2 / 8), 128, fast_smem_b() / 2, p->stream>>>(p->zscr, p->zf, p->tw,
-                                                                      p->N, N2);
-  for (int bh0 = 0; bh0 < rows; bh0 += f.chunk_bh) {
-    const int nb = rows - bh0 < f.chunk_bh ? rows - bh0 : f.chunk_bh;
-    auto ac = [&](bool pass_a) {
-      switch (N2) {
-        case 32: {
-          const int items = nb * kFastN1;
-          if (pass_a) {
-            // Resident CTAs per SM: two when two tiles' stages fit.
-            const int per_sm = PipeA<T>::kSmem <= (113u << 10) ? 2 : 1;
-            int grid = (items + kPipeWarps - 1) / kPipeWarps;
-            if (grid > per_sm * p->sms) grid = per_sm * p->sms;
-            fsf_pass_a32<T><<<grid, kPipeWarps * 32, PipeA<T>::kSmem, p->stream>>>(
-                tmV, p->scratch, p->tw, p->N, p->D, p->H, bh0, nb, p->status);
-          } else {
-            int grid = (items + PipeC::kWarps - 1) / PipeC::kWarps;
-            if (grid > 2 * p->sms) grid = 2 * p->sms;
-            fsf_pass_c32<T><<<grid, PipeC::kWarps * 32, PipeC::kSmem, p->stream>>>(
-                p->tm_c, O, p->N, p->D, p->H, bh0, nb, p->status);
-          }
-          break;
+  fsf_zspec_b<<<nrows * (N2 / 8), 128, fast_smem_b() / 2, st>>>(zscr, zf, p->tw, p->N, N2);
+  return cudaGetLastError();
+}
+
+template <typename T>
+static cudaError_t chunk_t(const cat_plan_s* p, const T* V, T* O, int bh0, int nb, int slot,
+                           cudaStream_t st, const CUtensorMap* tmV) {
+  const int N2 = p->fs.N2;
+  float2* scr = p->scratch + (size_t)slot * (p->scratch_bytes / 2 / sizeof(float2));
+  auto ac = [&](bool pass_a) {
+    switch (N2) {
+      case 32: {
+        const int items = nb * kFastN1;
+        if (pass_a) {
+          // Resident CTAs per SM: two when two tiles' stages fit.
+          const int per_sm = PipeA<T>::kSmem <= (113u << 10) ? 2 : 1;
+          int grid = (items + kPipeWarps - 1) / kPipeWarps;
+          if (grid > per_sm * p->sms) grid = per_sm * p->sms;
+          fsf_pass_a32<T><<<grid, kPipeWarps * 32, PipeA<T>::kSmem, st>>>(
+              *tmV, scr, p->tw, p->N, p->D, p->H, bh0, nb, p->status);
+        } else {
+          int grid = (items + PipeC::kWarps - 1) / PipeC::kWarps;
+          if (grid > 2 * p->sms) grid = 2 * p->sms;
+          fsf_pass_c32<T><<<grid, PipeC::kWarps * 32, PipeC::kSmem, st>>>(
+              p->tm_c[slot], scr, O, p->N, p->D, p->H, bh0, nb, p->status);
         }
-        case 64: launch_ac<T, 64>(p, V, O, bh0, nb, pass_a); break;
-        case 128: launch_ac<T, 128>(p, V, O, bh0, nb, pass_a); break;
-        default: launch_ac<T, 256>(p, V, O, bh0, nb, pass_a); break;
+        break;
       }
-    };
-    ac(true);
-    fsf_pass_b<<<nb * N2 * 2, 256, kSmemB, p->stream>>>(p->scratch, p->zf, p->tw, p->N, N2, bh0);
-    ac(false);
-    cudaError_t e = cudaGetLastError();
+      case 64: launch_ac<T, 64>(p, V, O, scr, bh0, nb, pass_a, st); break;
+      case 128: launch_ac<T, 128>(p, V, O, scr, bh0, nb, pass_a, st); break;
+      default: launch_ac<T, 256>(p, V, O, scr, bh0, nb, pass_a, st); break;
+    }
+  };
+  ac(true);
+  fsf_pass_b<<<nb * N2 * (kFastPairs / kBPairs), kBPairs * 16, kSmemB, st>>>(scr, p->zf, p->tabs,
+                                                                             N2, bh0);
+  ac(false);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fast_chunk(const cat_plan_s* p, const void* V, void* O, int bh0, int nb,
+                              int slot, cudaStream_t st) {
+  CUtensorMap tmV;
+  if (p->dtype == 1) {
+    if (p->fs.N2 == 32 && !encode_v_map(p, (const __nv_bfloat16*)V, &tmV))
+      return cudaErrorInvalidValue;
+    return chunk_t(p, (const __nv_bfloat16*)V, (__nv_bfloat16*)O, bh0, nb, slot, st, &tmV);
+  }
+  if (p->fs.N2 == 32 && !encode_v_map(p, (const float*)V, &tmV)) return cudaErrorInvalidValue;
+  return chunk_t(p, (const float*)V, (float*)O, bh0, nb, slot, st, &tmV);
+}
+
+// Serialised fast path on the plan's stream (used when stage timing is on):
+// spectrum of z* for all rows, then every chunk in turn on scratch slot 0.
+template <typename T>
+static cudaError_t run_t(const cat_plan_s* p, const T* V, T* O) {
+  const int rows = p->B * p->H;
+  cudaError_t e = launch_fast_zspec(p, 0, rows, p->stream);
+  if (e != cudaSuccess) return e;
+  for (int bh0 = 0; bh0 < rows; bh0 += p->fs.chunk_bh) {
+    const int nb = rows - bh0 < p->fs.chunk_bh ? rows - bh0 : p->fs.chunk_bh;
+    e = launch_fast_chunk(p, V, O, bh0, nb, 0, p->stream);
     if (e != cudaSuccess) return e;
   }
-  return cudaGetLastError();
+  return cudaSuccess;
 }
 
 cudaError_t launch_fast_conv(const cat_plan_s* p, const void* V, void* O) {

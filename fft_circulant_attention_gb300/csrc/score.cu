@@ -79,12 +79,12 @@ constexpr int kChunk = 16;
 template <typename T, int HT, bool VEC>
 __global__ void __launch_bounds__(kScoreThreads)
 score_kernel(const T* __restrict__ X, const T* __restrict__ WA, float2* __restrict__ z,
-             int N, int D, int H, int h0) {
+             int N, int D, int H, int h0, int b0) {
   constexpr int HP = (HT + 3) & ~3;
   constexpr int TP = kScoreTokPerThread;
   extern __shared__ float4 ws4[];
   float* ws = reinterpret_cast<float*>(ws4);
-  const int b = blockIdx.y;
+  const int b = b0 + blockIdx.y;
   for (int i = threadIdx.x; i < D * HP; i += blockDim.x) {
     int d = i / HP, h = i - d * HP;
     ws[i] = (h < HT) ? ld_elem(WA + (size_t)d * H + h0 + h) : 0.f;
@@ -207,11 +207,11 @@ __host__ __device__ inline int mma_wt_stride(int D) { return D + ((32 - D % 64) 
 template <int NT>
 __global__ void __launch_bounds__(kMmaWarps * 32)
 score_mma_kernel(const __nv_bfloat16* __restrict__ X, const __nv_bfloat16* __restrict__ WA,
-                 float2* __restrict__ z, int N, int D, int H, int h0, int HT) {
+                 float2* __restrict__ z, int N, int D, int H, int h0, int HT, int b0) {
   extern __shared__ uint4 wsh4[];
   unsigned short* wt = reinterpret_cast<unsigned short*>(wsh4);
   const int ws = mma_wt_stride(D);
-  const int b = blockIdx.y;
+  const int b = b0 + blockIdx.y;
   stage_wt(wt, ws, reinterpret_cast<const unsigned short*>(WA), D, H, h0, HT, NT * 8);
   __syncthreads();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -303,8 +303,8 @@ __device__ __forceinline__ void ldmatrix_x4(unsigned (&r)[4], uint32_t addr) {
 template <int NT>
 __global__ void __launch_bounds__(kTsThreads)
 score_tma_kernel(const __grid_constant__ CUtensorMap tmX, const __nv_bfloat16* __restrict__ WA,
-                 float2* __restrict__ z, int N, int D, int H, int h0, int HT, int rows_total,
-                 unsigned int* status) {
+                 float2* __restrict__ z, int N, int D, int H, int h0, int HT, int row0,
+                 int rows_total, unsigned int* status) {
   extern __shared__ __align__(1024) unsigned char sm_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~(uintptr_t)1023);
@@ -324,17 +324,19 @@ score_tma_kernel(const __grid_constant__ CUtensorMap tmX, const __nv_bfloat16* _
   __syncthreads();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nkb = D / kTsCols;
-  const int ntiles = (rows_total + kTsRows - 1) / kTsRows;
+  const int ntiles = (rows_total - row0 + kTsRows - 1) / kTsRows;
 
   if (warp == kTsConsumers) {   // producer
     if (lane == 0) {
+      const uint64_t stream = policy_evict_first();
       int it = 0;
       for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x)
         for (int kb = 0; kb < nkb; ++kb, ++it) {
           const int s = it % kTsStages, use = it / kTsStages;
           if (use > 0 && !mbar_wait(empty + s, (use - 1) & 1, status, 0x601)) return;
           mbar_expect_tx(full + s, kTsStageBytes);
-          tma_load_2d(stages + s * kTsStageBytes, &tmX, kb * kTsCols, tile * kTsRows, full + s);
+          tma_load_2d_hint(stages + s * kTsStageBytes, &tmX, kb * kTsCols, row0 + tile * kTsRows,
+                           full + s, stream);
         }
     }
     return;
@@ -388,7 +390,7 @@ score_tma_kernel(const __grid_constant__ CUtensorMap tmX, const __nv_bfloat16* _
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const int r = tile * kTsRows + warp * 16 + mrow + 8 * (i >> 1);
+        const int r = row0 + tile * kTsRows + warp * 16 + mrow + 8 * (i >> 1);
         const int hh = nt * 8 + 2 * c + (i & 1);
         if (r < rows_total && hh < HT) {
           const int b = r / N, n = r - b * N;
@@ -403,7 +405,8 @@ static bool score_tma_ok(const cat_plan_s* p, const void* X) {
          score_tma_smem(p->D) <= (226u << 10);
 }
 
-static cudaError_t score_tma(const cat_plan_s* p, const void* X, const void* WA, bool setup) {
+static cudaError_t score_tma(const cat_plan_s* p, const void* X, const void* WA, bool setup,
+                             const Span& sp = Span{}) {
   if (setup) {
     cudaError_t e = allow_max_smem(score_tma_kernel<1>);
     return e == cudaSuccess ? allow_max_smem(score_tma_kernel<2>) : e;
@@ -413,18 +416,21 @@ static cudaError_t score_tma(const cat_plan_s* p, const void* X, const void* WA,
   if (!encode_map_2d_sw128(&tm, X, (unsigned long long)p->D, rows, (unsigned long long)p->D * 2,
                            kTsCols, kTsRows))
     return cudaErrorInvalidValue;
-  const int ntiles = (int)((rows + kTsRows - 1) / kTsRows);
+  const int row0 = sp.b0 * p->N;
+  const int row_end = (sp.b0 + sp.nb(p)) * p->N;
+  const int ntiles = (row_end - row0 + kTsRows - 1) / kTsRows;
   const size_t smem = score_tma_smem(p->D);
   const int per_sm = smem <= (113u << 10) ? 2 : 1;
   const int grid = ntiles < per_sm * p->sms ? ntiles : per_sm * p->sms;
+  const cudaStream_t st = sp.stream(p);
   for (int h0 = 0; h0 < p->H; h0 += 16) {
     const int ht = p->H - h0 < 16 ? p->H - h0 : 16;
     if (ht > 8)
-      score_tma_kernel<2><<<grid, kTsThreads, smem, p->stream>>>(
-          tm, (const __nv_bfloat16*)WA, p->z2, p->N, p->D, p->H, h0, ht, (int)rows, p->status);
+      score_tma_kernel<2><<<grid, kTsThreads, smem, st>>>(
+          tm, (const __nv_bfloat16*)WA, p->z2, p->N, p->D, p->H, h0, ht, row0, row_end, p->status);
     else
-      score_tma_kernel<1><<<grid, kTsThreads, smem, p->stream>>>(
-          tm, (const __nv_bfloat16*)WA, p->z2, p->N, p->D, p->H, h0, ht, (int)rows, p->status);
+      score_tma_kernel<1><<<grid, kTsThreads, smem, st>>>(
+          tm, (const __nv_bfloat16*)WA, p->z2, p->N, p->D, p->H, h0, ht, row0, row_end, p->status);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -438,21 +444,25 @@ static bool score_mma_ok(const cat_plan_s* p, const void* X) {
          score_mma_smem(p->D) <= (200u << 10);
 }
 
-static cudaError_t score_mma(const cat_plan_s* p, const void* X, const void* WA, bool setup) {
+static cudaError_t score_mma(const cat_plan_s* p, const void* X, const void* WA, bool setup,
+                             const Span& sp = Span{}) {
   if (setup) {
     cudaError_t e = allow_max_smem(score_mma_kernel<1>);
     return e == cudaSuccess ? allow_max_smem(score_mma_kernel<2>) : e;
   }
-  dim3 grid((p->N + kMmaTokPerCta - 1) / kMmaTokPerCta, p->B);
+  dim3 grid((p->N + kMmaTokPerCta - 1) / kMmaTokPerCta, sp.nb(p));
+  const cudaStream_t st = sp.stream(p);
   for (int h0 = 0; h0 < p->H; h0 += 16) {
     const int ht = p->H - h0 < 16 ? p->H - h0 : 16;
     const size_t smem = score_mma_smem(p->D);
     if (ht > 8)
-      score_mma_kernel<2><<<grid, kMmaWarps * 32, smem, p->stream>>>(
-          (const __nv_bfloat16*)X, (const __nv_bfloat16*)WA, p->z2, p->N, p->D, p->H, h0, ht);
+      score_mma_kernel<2><<<grid, kMmaWarps * 32, smem, st>>>(
+          (const __nv_bfloat16*)X, (const __nv_bfloat16*)WA, p->z2, p->N, p->D, p->H, h0, ht,
+          sp.b0);
     else
-      score_mma_kernel<1><<<grid, kMmaWarps * 32, smem, p->stream>>>(
-          (const __nv_bfloat16*)X, (const __nv_bfloat16*)WA, p->z2, p->N, p->D, p->H, h0, ht);
+      score_mma_kernel<1><<<grid, kMmaWarps * 32, smem, st>>>(
+          (const __nv_bfloat16*)X, (const __nv_bfloat16*)WA, p->z2, p->N, p->D, p->H, h0, ht,
+          sp.b0);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -466,24 +476,26 @@ static bool score_vec_ok(const cat_plan_s* p, const void* X) {
 }
 
 template <typename T, int HT, bool VEC>
-static cudaError_t run_score(const cat_plan_s* p, const T* X, const T* WA, int h0, bool setup) {
+static cudaError_t run_score(const cat_plan_s* p, const T* X, const T* WA, int h0, bool setup,
+                            const Span& sp) {
   constexpr int HP = (HT + 3) & ~3;
   size_t smem = (size_t)HP * p->D * sizeof(float);
   auto k = score_kernel<T, HT, VEC>;
   if (setup) return allow_max_smem(k);
-  dim3 grid((p->N + kScoreTokPerCta - 1) / kScoreTokPerCta, p->B);
-  k<<<grid, kScoreThreads, smem, p->stream>>>(X, WA, p->z2, p->N, p->D, p->H, h0);
+  dim3 grid((p->N + kScoreTokPerCta - 1) / kScoreTokPerCta, sp.nb(p));
+  k<<<grid, kScoreThreads, smem, sp.stream(p)>>>(X, WA, p->z2, p->N, p->D, p->H, h0, sp.b0);
   return cudaGetLastError();
 }
 
 template <typename T, bool VEC>
-static cudaError_t score_heads(const cat_plan_s* p, const T* X, const T* WA, bool setup) {
+static cudaError_t score_heads(const cat_plan_s* p, const T* X, const T* WA, bool setup,
+                               const Span& sp = Span{}) {
   const int hpp = score_heads_per_pass(p->D);
   for (int h0 = 0; h0 < p->H; h0 += hpp) {
     int ht = p->H - h0 < hpp ? p->H - h0 : hpp;
     cudaError_t e;
     switch (ht) {
-#define CAT_HT(n) case n: e = run_score<T, n, VEC>(p, X, WA, h0, setup); break;
+#define CAT_HT(n) case n: e = run_score<T, n, VEC>(p, X, WA, h0, setup, sp); break;
       CAT_HT(1) CAT_HT(2) CAT_HT(3) CAT_HT(4) CAT_HT(5) CAT_HT(6) CAT_HT(7) CAT_HT(8)
       CAT_HT(9) CAT_HT(10) CAT_HT(11) CAT_HT(12) CAT_HT(13) CAT_HT(14) CAT_HT(15) CAT_HT(16)
 #undef CAT_HT
@@ -495,24 +507,25 @@ static cudaError_t score_heads(const cat_plan_s* p, const T* X, const T* WA, boo
 }
 
 template <typename T>
-static cudaError_t score_dispatch(const cat_plan_s* p, const T* X, const T* WA, bool setup) {
+static cudaError_t score_dispatch(const cat_plan_s* p, const T* X, const T* WA, bool setup,
+                                 const Span& sp = Span{}) {
   if (setup) {
     cudaError_t e = score_heads<T, true>(p, X, WA, true);
     if (e != cudaSuccess) return e;
     return score_heads<T, false>(p, X, WA, true);
   }
-  if (score_vec_ok<T>(p, X)) return score_heads<T, true>(p, X, WA, false);
-  return score_heads<T, false>(p, X, WA, false);
+  if (score_vec_ok<T>(p, X)) return score_heads<T, true>(p, X, WA, false, sp);
+  return score_heads<T, false>(p, X, WA, false, sp);
 }
 
-cudaError_t launch_score(const cat_plan_s* p, const void* X, const void* WA) {
-  if (p->B == 0) return cudaSuccess;
+cudaError_t launch_score(const cat_plan_s* p, const void* X, const void* WA, const Span& sp) {
+  if (sp.nb(p) == 0) return cudaSuccess;
   if (!p->score_cuda_cores && p->score_path != 1 && score_tma_ok(p, X))
-    return score_tma(p, X, WA, false);
-  if (score_mma_ok(p, X) && !p->score_cuda_cores) return score_mma(p, X, WA, false);
+    return score_tma(p, X, WA, false, sp);
+  if (score_mma_ok(p, X) && !p->score_cuda_cores) return score_mma(p, X, WA, false, sp);
   if (p->dtype == 1)
-    return score_dispatch(p, (const __nv_bfloat16*)X, (const __nv_bfloat16*)WA, false);
-  return score_dispatch(p, (const float*)X, (const float*)WA, false);
+    return score_dispatch(p, (const __nv_bfloat16*)X, (const __nv_bfloat16*)WA, false, sp);
+  return score_dispatch(p, (const float*)X, (const float*)WA, false, sp);
 }
 
 // exp(z - m) for a score held as the double-float (hi, lo): the difference
@@ -605,12 +618,16 @@ softmax_finish(const float2* __restrict__ z, const float2* __restrict__ part, fl
 
 int softmax_parts(int N) { return (N + 2047) / 2048; }
 
-cudaError_t launch_softmax(const cat_plan_s* p) {
-  const int rows = p->B * p->H;
+cudaError_t launch_softmax(const cat_plan_s* p, const Span& sp) {
+  const int rows = sp.nb(p) * p->H;
   if (rows == 0) return cudaSuccess;
   const int P = softmax_parts(p->N);
-  softmax_partial<<<rows * P, kSoftmaxThreads, 0, p->stream>>>(p->z2, p->part, p->N, P);
-  softmax_finish<<<rows * P, kSoftmaxThreads, 0, p->stream>>>(p->z2, p->part, p->zs, p->N, P);
+  const size_t r0 = (size_t)sp.b0 * p->H;
+  const cudaStream_t st = sp.stream(p);
+  softmax_partial<<<rows * P, kSoftmaxThreads, 0, st>>>(p->z2 + r0 * p->N, p->part + r0 * P, p->N,
+                                                        P);
+  softmax_finish<<<rows * P, kSoftmaxThreads, 0, st>>>(p->z2 + r0 * p->N, p->part + r0 * P,
+                                                       p->zs + r0 * p->N, p->N, P);
   return cudaGetLastError();
 }
 

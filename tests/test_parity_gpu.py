@@ -278,17 +278,23 @@ def test_fast_path_lengths(N, B, H, dtype):
 
 
 def test_fast_path_chunks(monkeypatch):
-    """Several (b, h) chunks of scratch in one forward (chunk of 3 rows for
-    B·H = 8) give the same result as one chunk."""
-    X, WA, V = to_dev(*synth.make_inputs(2, 16384, 256, 4, "bf16", seed=31))
+    """Chunks of 1, 3 (ragged: 3 + 1) and 4 heads per scratch slot, on the
+    overlapped two-stream schedule and on the serialised one (stage timing
+    on), all give the same result."""
+    X, WA, V = to_dev(*synth.make_inputs(3, 16384, 256, 4, "bf16", seed=31))
     outs = []
-    for chunk in ("3", "8"):
+    for chunk in ("1", "3", "4"):
         monkeypatch.setenv("CAT_CHUNK_BH", chunk)
-        with cat.Plan(2, 16384, 256, 4, "bf16") as p:
+        with cat.Plan(3, 16384, 256, 4, "bf16") as p:
             assert "chunk_bh=%s" % chunk in p.describe()
             outs.append(p.forward(X, WA, V))
+            p.timing(1)
+            outs.append(p.forward(X, WA, V))
             p.sync()
-    assert torch.equal(outs[0], outs[1])
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
+    O_ref, _ = oracle.forward(X.cpu(), WA.cpu(), V.cpu(), mode="fft")
+    assert float(np.abs(outs[0].cpu().double().numpy() - O_ref).max()) <= 8e-3 * float(V.abs().max())
 
 
 @pytest.mark.parametrize("score", ["tma", "mma", "cuda"])
