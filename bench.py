@@ -41,10 +41,26 @@ SMS, FP32_LANES, MAX_SM_MHZ = 152, 128, 2070.0
 FP32_PEAK_TFLOPS = SMS * FP32_LANES * 2 * MAX_SM_MHZ * 1e6 / 1e12
 FALLBACK_HBM_GBS = 6800.0
 
-# DRAM bytes per launch of the circulant-product stage, from an ncu capture
-# of the same source (profiles/).  Keyed by workload; None = not captured
-# for the current kernels.
-NCU_TRAFFIC = {}
+# DRAM bytes (read + write) of one circulant-product stage (passes A, B, C
+# and the z* spectrum, serialised), summed from an ncu launch list of the
+# same kernel sources (profiles/).  Keyed by (workload, hash of the kernel
+# sources): any change to those sources makes the figure stale, and the
+# bench then reports null.
+NCU_TRAFFIC = {
+    # profiles/launches_long16k.md: fsf_* kernels, warm launch list, per forward
+    ("long16k", "089fa1a37ef4"): 330126250,
+}
+KERNEL_SOURCES = ["fourstep_fast.cu", "fft_reg.cuh", "fft_device.cuh", "bulk.cuh", "elem.cuh"]
+
+
+def kernel_hash():
+    import hashlib
+    h = hashlib.sha1()
+    base = os.path.join(ROOT, "fft_circulant_attention_gb300", "csrc")
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(base, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:12]
 
 
 def load_peaks():
@@ -244,7 +260,6 @@ def measure_workload(name, steps, warmup, device, world, sampler=None):
     for _ in range(warmup):
         plan.forward(Xd, Wd, Vd, Od)
     plan.sync()
-    plan.timing(steps)
     barrier(world)
     torch.cuda.synchronize(device)
     if sampler:
@@ -259,10 +274,17 @@ def measure_workload(name, steps, warmup, device, world, sampler=None):
     clocks = sampler.stop() if sampler else None
     barrier(world)
     ms_total = e0.elapsed_time(e1)
-    stage_ms, ncalls = plan.stage_times()
     plan.sync()
     desc = plan.describe()
     launches = int(desc.split("launches=")[1].split()[0])
+    # Stage times: the library's CUDA events on the plan's stream around each
+    # stage; with timing armed the forward runs its stages one after another
+    # (no cross-stream overlap), so each stage is timed on its own.
+    stage_steps = max(3, min(steps, 50))
+    plan.timing(stage_steps)
+    for _ in range(stage_steps):
+        plan.forward(Xd, Wd, Vd, Od)
+    stage_ms, ncalls = plan.stage_times()
     plan.timing(0)
     ms_total = max_over_ranks(ms_total, world, device)
 
@@ -293,13 +315,14 @@ def measure_workload(name, steps, warmup, device, world, sampler=None):
     bound = "alu" if a["conv_flops"] / FP32_PEAK_TFLOPS / 1e12 >= a["conv_bytes"] / hbm / 1e9 \
         else "hbm"
     roof = {
-        "kernel": "circulant product (%s)" % desc.split()[0].replace("path=", ""),
+        "kernel": "circulant-product stage (%s path: z* spectrum + passes A, B, C), timed "
+                  "serialised on the plan's stream" % desc.split()[0].replace("path=", ""),
         "bound": bound,
         "achieved": conv_tflops if bound == "alu" else conv_gbs,
         "peak": FP32_PEAK_TFLOPS if bound == "alu" else hbm,
         "unit": "TFLOP/s" if bound == "alu" else "GB/s",
         "frac": (conv_tflops / FP32_PEAK_TFLOPS) if bound == "alu" else conv_gbs / hbm,
-        "traffic": NCU_TRAFFIC.get(name),
+        "traffic": NCU_TRAFFIC.get((name, kernel_hash())),
         "peak_source": ("FP32: 152 SMs x 128 lanes x 2 x 2070 MHz (derived); HBM: %s %.0f GB/s"
                         % (hbm_kind, hbm)),
         "hbm_gbs_achieved": conv_gbs,
@@ -361,8 +384,9 @@ def run_gb300(args, world, rank, local):
                    "plan": prim["desc"]},
         "roofline": prim["roofline"],
         "path_roofline_frac": prim["path_roofline_frac"],
-        "stage_ms": {"score": prim["stage_ms"][0], "softmax_spectrum": prim["stage_ms"][1],
-                     "circulant_product": prim["stage_ms"][2]},
+        "stage_ms_serialised": {"score": prim["stage_ms"][0],
+                                "softmax": prim["stage_ms"][1],
+                                "circulant_product": prim["stage_ms"][2]},
         "e2e": prim["e2e"],
         "gpu_launches": prim["launches"] * args.steps,
         "clocks": prim["clocks"],
@@ -374,14 +398,14 @@ def run_gb300(args, world, rank, local):
             "workload": SECONDARY, "B": sc["B"], "N": sc["N"], "D": sc["D"], "H": sc["H"],
             "value": sec["value"], "ms_per_step": sec["ms_per_step"],
             "path_roofline_frac": sec["path_roofline_frac"], "roofline": sec["roofline"],
-            "stage_ms": sec["stage_ms"], "e2e": sec["e2e"], "plan": sec["desc"]}
+            "stage_ms_serialised": sec["stage_ms"], "e2e": sec["e2e"], "plan": sec["desc"]}
     print(json.dumps(line), flush=True)
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--config", default=PRIMARY, choices=sorted(synth.CONFIGS))

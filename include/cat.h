@@ -96,8 +96,12 @@ int cat_plan_set_stream(cat_plan_t plan, void *stream);
  * X, W_A, V: device pointers, read only.  O: device pointer, written.
  * All four must be 16-byte aligned and O must not overlap the others.
  * B, N, D, H, dtype must equal the plan's (CAT_ERR_PLAN_MISMATCH).
- * Asynchronous on the plan's stream; the plan's workspace is reused, so two
- * calls on one plan must not run concurrently on different streams.
+ * Asynchronous on the plan's stream: work that the fast long-sequence path
+ * (head width 64, N = 512·N2 with N2 in 32..256) spreads over the plan's two
+ * internal streams forks from and joins back into the plan's stream, so the
+ * call is ordered like a single kernel on it.  The plan's workspace is
+ * reused, so two calls on one plan must not run concurrently on different
+ * streams.
  */
 int cat_forward(cat_plan_t plan, const void *X, const void *W_A, const void *V,
                 void *O, int B, int N, int D, int H, int dtype);
@@ -138,12 +142,15 @@ int cat_plan_describe(cat_plan_t plan, char *buf, int len);
 
 /*
  * cat_plan_timing — stage timing for profiling.  max_calls > 0 arms the plan
- * to record CUDA events around its three stages (score; softmax and, for
- * N <= 16384, the spectrum of z*; the circulant product) on its stream for
- * the next max_calls cat_forward calls, discarding earlier records;
- * max_calls = 0 turns recording off.  Synchronises the plan's stream.
- * The plan owns the events.  Errors: CAT_ERR_INVALID_ARG, CAT_ERR_ALLOC,
- * CAT_ERR_CUDA.
+ * to record CUDA events around its three stages (score; softmax and, on the
+ * shared-memory path, the spectrum of z*; the circulant product, which on
+ * the long-sequence paths includes the spectrum of z*) on its stream for the
+ * next max_calls cat_forward calls, discarding earlier records; max_calls = 0
+ * turns recording off.  While recording, a forward runs its stages one after
+ * another on the plan's stream (the fast long-sequence path otherwise
+ * overlaps batches or heads on two internal streams), so each stage's time
+ * is its own.  Synchronises the plan's stream.  The plan owns the events.
+ * Errors: CAT_ERR_INVALID_ARG, CAT_ERR_ALLOC, CAT_ERR_CUDA.
  */
 int cat_plan_timing(cat_plan_t plan, int max_calls);
 
