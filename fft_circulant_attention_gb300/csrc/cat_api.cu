@@ -180,18 +180,20 @@ int choose_path(cat_plan_s* p) {
       f.P = 32;
       // Chunks of (b, h) rows stay inside one batch; two scratch slots let
       // two chunks be in flight on the plan's two internal streams.
-      // With two or more batches, whole batches alternate between the two
-      // streams (a chunk is a batch's heads, as far as the scratch budget
-      // allows); with one batch, single heads alternate.
+      // Chunks of heads alternate between the plan's two streams: half the
+      // scratch budget per slot with two or more batches (8 heads at
+      // N = 16384), single heads with one batch.
       const size_t per_bh = (size_t)N * 32 * sizeof(float2);
-      long chunk = p->B >= 2 ? (long)(kFastScratchBudget / per_bh) : 1;
+      long chunk = p->B >= 2 ? (long)(kFastScratchBudget / 2 / per_bh) : 1;
       if (const char* env = std::getenv("CAT_CHUNK_BH")) chunk = std::atol(env);
       if (chunk < 1) chunk = 1;
       if (chunk > p->H) chunk = p->H;
       f.chunk_bh = (int)chunk;
       p->scratch_bytes = 2 * (size_t)f.chunk_bh * per_bh;
       const int chunks_per_batch = (int)((p->H + chunk - 1) / chunk);
-      p->launches = p->B * (score_launches(p->H, p->D) + 4 + 3 * chunks_per_batch);
+      // Front (score, softmax partials, spectrum: 3 + score passes) once,
+      // then passes A, B, C per chunk.
+      p->launches = score_launches(p->H, p->D) + 3 + 3 * p->B * chunks_per_batch;
       return CAT_OK;
     }
   }
@@ -333,13 +335,40 @@ extern "C" {
 
 namespace {
 
-// Fast path, overlapped schedule on the plan's two internal streams: batch b
-// (score, softmax, spectrum of z*) goes to stream b mod 2, and the chunks of
-// its rows alternate between the streams, each stream using its own scratch
-// slot; a chunk on the other stream first waits for the batch's spectrum.
-// The streams fork from and join back into the plan's stream.
+// Fast path, overlapped schedules on the plan's two internal streams, which
+// fork from and join back into the plan's stream.  Default (front_all):
+// score, softmax partials and spectrum of all batches first, then the
+// chunks alternate between the streams.  CAT_SCHEDULE=batch: batch b's
+// front goes to stream b mod 2 and the chunks of its rows alternate between
+// the streams, a chunk on the other stream first waiting for the batch's
+// spectrum.  Each stream uses its own scratch slot.
 cudaError_t run_fast_overlapped(cat_plan_s* p, const void* X, const void* WA, const void* V,
                                 void* O) {
+  if (p->front_all) {
+    // Score, softmax partials and spectrum of every batch as single launches
+    // on the plan's stream (each fills the GPU), then the chunks' passes
+    // alternate over the two internal streams, one scratch slot each.
+    cudaError_t e = cat::launch_score(p, X, WA);
+    if (e == cudaSuccess) e = cat::launch_softmax(p, cat::Span{}, false);
+    if (e == cudaSuccess) e = cat::launch_fast_zspec(p, 0, p->B * p->H, p->stream);
+    if (e == cudaSuccess) e = cudaEventRecord(p->ev_fork, p->stream);
+    for (int k = 0; k < 2 && e == cudaSuccess; ++k)
+      e = cudaStreamWaitEvent(p->side[k], p->ev_fork, 0);
+    const int rows = p->B * p->H;
+    int g = 0;
+    for (int b = 0; b < p->B && e == cudaSuccess; ++b)
+      for (int h0 = 0; h0 < p->H && e == cudaSuccess; h0 += p->fs.chunk_bh, ++g) {
+        const int nb = p->H - h0 < p->fs.chunk_bh ? p->H - h0 : p->fs.chunk_bh;
+        e = cat::launch_fast_chunk(p, V, O, b * p->H + h0, nb, g & 1, p->side[g & 1]);
+      }
+    (void)rows;
+    for (int k = 0; k < 2; ++k) {
+      cudaError_t e2 = cudaEventRecord(p->ev_join[k], p->side[k]);
+      if (e2 == cudaSuccess) e2 = cudaStreamWaitEvent(p->stream, p->ev_join[k], 0);
+      if (e == cudaSuccess) e = e2;
+    }
+    return e;
+  }
   cudaError_t e = cudaEventRecord(p->ev_fork, p->stream);
   for (int k = 0; k < 2 && e == cudaSuccess; ++k) e = cudaStreamWaitEvent(p->side[k], p->ev_fork, 0);
   int g = 0;
@@ -352,7 +381,7 @@ cudaError_t run_fast_overlapped(cat_plan_s* p, const void* X, const void* WA, co
     sp.st = sb;
     sp.own = true;
     e = cat::launch_score(p, X, WA, sp);
-    if (e == cudaSuccess) e = cat::launch_softmax(p, sp);
+    if (e == cudaSuccess) e = cat::launch_softmax(p, sp, false);
     if (e == cudaSuccess) e = cat::launch_fast_zspec(p, b * p->H, p->H, sb);
     if (e == cudaSuccess) e = cudaEventRecord(p->ev_front[kb], sb);
     for (int h0 = 0; h0 < p->H && e == cudaSuccess; h0 += p->fs.chunk_bh, ++g) {
@@ -383,6 +412,8 @@ int cat_plan_create(cat_plan_t* out, int B, int N, int D, int H, int dtype, void
   p->dh = D / H;
   p->npair = (p->dh + 1) / 2;
   p->stream = (cudaStream_t)stream;
+  p->front_all = 1;
+  if (const char* sc = std::getenv("CAT_SCHEDULE")) p->front_all = std::strcmp(sc, "batch") != 0;
   if (const char* sc = std::getenv("CAT_SCORE")) {
     p->score_cuda_cores = std::strcmp(sc, "cuda") == 0;
     p->score_path = std::strcmp(sc, "mma") == 0 ? 1 : 0;

@@ -56,6 +56,7 @@ struct cat_plan_s {
   cat::FourStepCfg fs;
   int score_cuda_cores;     // 1: bf16 scores on the CUDA-core kernel (testing)
   int score_path;           // 1: bf16 scores on the register-fed MMA kernel (testing)
+  int front_all;            // fast path: score/softmax/spectrum of all batches first
   // workspace (device)
   float2* z2;               // [B, H, N] scores as double-float (hi, lo)
   float* zs;                // [B, H, N] z* (softmax weights)
@@ -124,7 +125,9 @@ cudaError_t allow_max_smem(K kernel) {
 // Launchers (enqueue on plan->stream).  Each returns cudaGetLastError().
 cudaError_t launch_score(const cat_plan_s* p, const void* X, const void* WA,
                          const Span& sp = Span{});
-cudaError_t launch_softmax(const cat_plan_s* p, const Span& sp = Span{});
+// finish = false: only the chunk partials (the fast path's spectrum kernel
+// applies the softmax itself).
+cudaError_t launch_softmax(const cat_plan_s* p, const Span& sp = Span{}, bool finish = true);
 cudaError_t launch_softmax_spectrum(const cat_plan_s* p);
 cudaError_t launch_conv_smem(const cat_plan_s* p, const void* V, void* O);
 cudaError_t launch_fourstep_conv(const cat_plan_s* p, const void* V, void* O);

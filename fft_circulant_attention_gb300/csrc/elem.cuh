@@ -51,4 +51,40 @@ __device__ __forceinline__ float block_reduce(float v, float* red) {
   return r;
 }
 
+// exp(z - m) for a score held as the double-float (hi, lo): the difference
+// hi - m is split exactly (TwoSum) and its rounding error, plus lo, enters
+// as the first-order factor (1 + delta).
+__device__ __forceinline__ float exp_shifted(float2 zhl, float m) {
+  float s = zhl.x - m;
+  float bp = s - zhl.x;
+  float err = (zhl.x - (s - bp)) + (-m - bp);
+  float e = expf(s);
+  return fmaf(e, err + zhl.y, e);
+}
+
+// Softmax statistics of one (b, h) row from its P chunk partials (m_c, s_c):
+// sh[0] = m = max m_c, sh[1] = 1 / S with S = sum s_c·exp(m_c - m).  Warp 0
+// combines; every thread of the CTA must call it (it ends with
+// __syncthreads).
+__device__ __forceinline__ void row_softmax_stats(const float2* __restrict__ part, int P,
+                                                  float* sh) {
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    float m = -INFINITY;
+    for (int i = lane; i < P; i += 32) m = fmaxf(m, part[i].x);
+    m = warp_max(m);
+    float S = 0.f;
+    for (int i = lane; i < P; i += 32) {
+      const float2 q = part[i];
+      if (q.y > 0.f) S += q.y * expf(q.x - m);
+    }
+    S = warp_sum(S);
+    if (lane == 0) {
+      sh[0] = m;
+      sh[1] = 1.0f / S;
+    }
+  }
+  __syncthreads();
+}
+
 }  // namespace cat

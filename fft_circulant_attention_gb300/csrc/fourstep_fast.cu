@@ -463,25 +463,33 @@ __global__ void fsf_build_tables(float2* __restrict__ tabs, const float2* __rest
 
 // ---------------------------------------------------------------------------
 // Spectrum of z* in pass B's order, with the same register transforms.
-// zspec_a (per n1, over n2): lanes are consecutive n1 of one (b, h) row, so
-// the strided reads of z* are coalesced; z* enters as a complex signal with
-// zero imaginary part.  Result times w_N^{n1 k2} into zscr[row][k2][n1].
+// zspec_a (per n1, over n2): applies the softmax itself — z* = exp(z - m)/S
+// from the double-float scores and the row's chunk partials — then the DFT;
+// lanes are consecutive n1 of one (b, h) row, so the strided reads are
+// coalesced; z* enters as a complex signal with zero imaginary part.
+// Result times w_N^{n1 k2} into zscr[row][k2][n1].
 // zspec_b (per k2, over n1): 8 consecutive k2 per CTA laid out like pass B's
 // signals (lane: signal l & 7, j = 4·warp + (l >> 3)); result /N stored
 // where pass B's thread j reads it.
 // ---------------------------------------------------------------------------
 template <int N2>
 __global__ void __launch_bounds__(256)
-fsf_zspec_a(const float* __restrict__ zs, float2* __restrict__ zscr, const float2* __restrict__ W,
-            int N) {
+fsf_zspec_a(const float2* __restrict__ z2, const float2* __restrict__ part, int P,
+            float2* __restrict__ zscr, const float2* __restrict__ W, int N) {
+  __shared__ float stats[2];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if constexpr (N2 == 32) {
     const int row = blockIdx.x >> 3;
     const int n1 = (blockIdx.x & 7) * 64 + threadIdx.x;
-    const float* src = zs + (size_t)row * N + n1;
+    const float2* src = z2 + (size_t)row * N + n1;
+    float2 zv[32];
+#pragma unroll
+    for (int n2 = 0; n2 < 32; ++n2) zv[n2] = __ldg(src + kFastN1 * n2);
+    row_softmax_stats(part + (size_t)row * P, P, stats);
+    const float m = stats[0], inv = stats[1];
     float2 a[32];
 #pragma unroll
-    for (int n2 = 0; n2 < 32; ++n2) a[n2] = make_float2(__ldg(src + kFastN1 * n2), 0.f);
+    for (int n2 = 0; n2 < 32; ++n2) a[n2] = make_float2(exp_shifted(zv[n2], m) * inv, 0.f);
     dft<32, false>(a);
     float2* dst = zscr + (size_t)row * N + n1;
 #pragma unroll
@@ -497,10 +505,15 @@ fsf_zspec_a(const float* __restrict__ zs, float2* __restrict__ zscr, const float
     const int j = warp;
     const int row = blockIdx.x / (kFastN1 / 32);
     const int n1 = (blockIdx.x % (kFastN1 / 32)) * 32 + lane;
-    const float* src = zs + (size_t)row * N + n1;
+    const float2* src = z2 + (size_t)row * N + n1;
+    float2 zv[32];
+#pragma unroll
+    for (int u = 0; u < 32; ++u) zv[u] = __ldg(src + (size_t)kFastN1 * (j + TS * u));
+    row_softmax_stats(part + (size_t)row * P, P, stats);
+    const float m = stats[0], inv = stats[1];
     float2 a[32];
 #pragma unroll
-    for (int u = 0; u < 32; ++u) a[u] = make_float2(__ldg(src + (size_t)kFastN1 * (j + TS * u)), 0.f);
+    for (int u = 0; u < 32; ++u) a[u] = make_float2(exp_shifted(zv[u], m) * inv, 0.f);
     dft<32, false>(a);
     float2* rb = buf + lane * RS;
 #pragma unroll
@@ -647,17 +660,19 @@ static bool encode_v_map(const cat_plan_s* p, const T* V, CUtensorMap* tmV) {
 
 cudaError_t launch_fast_zspec(const cat_plan_s* p, int row0, int nrows, cudaStream_t st) {
   const int N2 = p->fs.N2;
-  const float* zs = p->zs + (size_t)row0 * p->N;
+  const int P = softmax_parts(p->N);
+  const float2* z2 = p->z2 + (size_t)row0 * p->N;
+  const float2* part = p->part + (size_t)row0 * P;
   float2* zscr = p->zscr + (size_t)row0 * p->N;
   float2* zf = p->zf + (size_t)row0 * p->N;
   switch (N2) {
     case 32:
-      fsf_zspec_a<32><<<nrows * 8, 64, 0, st>>>(zs, zscr, p->tw, p->N);
+      fsf_zspec_a<32><<<nrows * 8, 64, 0, st>>>(z2, part, P, zscr, p->tw, p->N);
       break;
 #define CAT_ZA(n)                                                                      \
   case n:                                                                              \
-    fsf_zspec_a<n><<<nrows * (kFastN1 / 32), n, fast_smem_a(n), st>>>(zs, zscr, p->tw, \
-                                                                      p->N);           \
+    fsf_zspec_a<n><<<nrows * (kFastN1 / 32), n, fast_smem_a(n), st>>>(z2, part, P, zscr, \
+                                                                      p->tw, p->N);    \
     break;
     CAT_ZA(64) CAT_ZA(128) CAT_ZA(256)
 #undef CAT_ZA

@@ -171,19 +171,41 @@ score_kernel(const T* __restrict__ X, const T* __restrict__ WA, float2* __restri
 // (32 tokens); heads go in n-tiles of 8 (NT = 1 or 2).
 // ---------------------------------------------------------------------------
 // W_A^T staging for the tensor-core kernels: wt[hh·ws + d] = W_A[d, h0 + hh]
-// for hh < rows (0 beyond HT).  Each thread copies whole rows d of W_A (the
-// HT contiguous heads), so a warp reads consecutive rows: one coalesced
-// stream instead of a head-strided gather.
+// for hh < rows (0 beyond HT), by threads tid, tid + nthr, ...  When W_A's
+// rows split into 16-byte vectors (H a multiple of 8, W_A 16-byte aligned)
+// the threads read consecutive vectors of W_A — one coalesced stream — and
+// scatter their 8 heads into the transposed layout; otherwise each thread
+// copies whole rows element by element.
 __device__ __forceinline__ void stage_wt(unsigned short* wt, int ws, const unsigned short* wa,
-                                         int D, int H, int h0, int HT, int rows = 16) {
-  for (int d = threadIdx.x; d < D; d += blockDim.x) {
-    const unsigned short* src = wa + (size_t)d * H + h0;
-    unsigned short v[16];
+                                         int D, int H, int h0, int HT, int rows, int tid,
+                                         int nthr) {
+  for (int hh = HT; hh < rows; ++hh)
+    for (int d = tid; d < D; d += nthr) wt[hh * ws + d] = 0;
+  if (H % 8 == 0 && ((uintptr_t)wa & 15) == 0) {
+    const int vpr = H / 8;                        // 16-byte vectors per row of W_A
+    const uint4* wv = reinterpret_cast<const uint4*>(wa);
+    for (int i = tid; i < D * vpr; i += nthr) {
+      const int d = i / vpr, hb = (i - d * vpr) * 8 - h0;   // head of the vector's element 0
+      if (hb + 8 <= 0 || hb >= HT) continue;
+      const uint4 v = __ldg(wv + i);
+      const unsigned w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int hh = 0; hh < 16; ++hh) v[hh] = hh < HT ? __ldg(src + hh) : (unsigned short)0;
+      for (int q = 0; q < 8; ++q) {
+        const int hh = hb + q;
+        if (hh >= 0 && hh < HT && hh < rows)
+          wt[hh * ws + d] = (unsigned short)((q & 1) ? (w[q >> 1] >> 16) : (w[q >> 1] & 0xffffu));
+      }
+    }
+  } else {
+    for (int d = tid; d < D; d += nthr) {
+      const unsigned short* src = wa + (size_t)d * H + h0;
+      unsigned short v[16];
 #pragma unroll
-    for (int hh = 0; hh < 16; ++hh)
-      if (hh < rows) wt[hh * ws + d] = v[hh];
+      for (int hh = 0; hh < 16; ++hh) v[hh] = hh < HT ? __ldg(src + hh) : (unsigned short)0;
+#pragma unroll
+      for (int hh = 0; hh < 16; ++hh)
+        if (hh < rows && hh < HT) wt[hh * ws + d] = v[hh];
+    }
   }
 }
 
@@ -212,7 +234,8 @@ score_mma_kernel(const __nv_bfloat16* __restrict__ X, const __nv_bfloat16* __res
   unsigned short* wt = reinterpret_cast<unsigned short*>(wsh4);
   const int ws = mma_wt_stride(D);
   const int b = b0 + blockIdx.y;
-  stage_wt(wt, ws, reinterpret_cast<const unsigned short*>(WA), D, H, h0, HT, NT * 8);
+  stage_wt(wt, ws, reinterpret_cast<const unsigned short*>(WA), D, H, h0, HT, NT * 8, threadIdx.x,
+           blockDim.x);
   __syncthreads();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int r = lane >> 2, c = lane & 3;
@@ -313,7 +336,6 @@ score_tma_kernel(const __grid_constant__ CUtensorMap tmX, const __nv_bfloat16* _
   unsigned short* wt = reinterpret_cast<unsigned short*>(sm + kTsStages * kTsStageBytes);
   uint64_t* full = reinterpret_cast<uint64_t*>(wt + 16 * ws);
   uint64_t* empty = full + kTsStages;
-  stage_wt(wt, ws, reinterpret_cast<const unsigned short*>(WA), D, H, h0, HT);
   if (threadIdx.x == 0) {
     for (int s = 0; s < kTsStages; ++s) {
       mbar_init(full + s, 1);
@@ -323,6 +345,13 @@ score_tma_kernel(const __grid_constant__ CUtensorMap tmX, const __nv_bfloat16* _
   mbar_fence_init();
   __syncthreads();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  // The producer starts streaming X at once; the consumer warps stage W_A^T
+  // meanwhile and sync among themselves (named barrier 1) before using it.
+  if (warp < kTsConsumers) {
+    stage_wt(wt, ws, reinterpret_cast<const unsigned short*>(WA), D, H, h0, HT, 16, threadIdx.x,
+             kTsConsumers * 32);
+    asm volatile("bar.sync 1, %0;" ::"n"(kTsConsumers * 32) : "memory");
+  }
   const int nkb = D / kTsCols;
   const int ntiles = (rows_total - row0 + kTsRows - 1) / kTsRows;
 
@@ -528,16 +557,6 @@ cudaError_t launch_score(const cat_plan_s* p, const void* X, const void* WA, con
   return score_dispatch(p, (const float*)X, (const float*)WA, false, sp);
 }
 
-// exp(z - m) for a score held as the double-float (hi, lo): the difference
-// hi - m is split exactly (TwoSum) and its rounding error, plus lo, enters
-// as the first-order factor (1 + delta).
-__device__ __forceinline__ float exp_shifted(float2 zhl, float m) {
-  float s = zhl.x - m;
-  float bp = s - zhl.x;
-  float err = (zhl.x - (s - bp)) + (-m - bp);
-  float e = expf(s);
-  return fmaf(e, err + zhl.y, e);
-}
 
 // Softmax over the N tokens of each (b, h) row, split over P CTAs per row
 // (about 2048 tokens each).  softmax_partial: per chunk c, m_c = max of the
@@ -618,7 +637,7 @@ softmax_finish(const float2* __restrict__ z, const float2* __restrict__ part, fl
 
 int softmax_parts(int N) { return (N + 2047) / 2048; }
 
-cudaError_t launch_softmax(const cat_plan_s* p, const Span& sp) {
+cudaError_t launch_softmax(const cat_plan_s* p, const Span& sp, bool finish) {
   const int rows = sp.nb(p) * p->H;
   if (rows == 0) return cudaSuccess;
   const int P = softmax_parts(p->N);
@@ -626,8 +645,9 @@ cudaError_t launch_softmax(const cat_plan_s* p, const Span& sp) {
   const cudaStream_t st = sp.stream(p);
   softmax_partial<<<rows * P, kSoftmaxThreads, 0, st>>>(p->z2 + r0 * p->N, p->part + r0 * P, p->N,
                                                         P);
-  softmax_finish<<<rows * P, kSoftmaxThreads, 0, st>>>(p->z2 + r0 * p->N, p->part + r0 * P,
-                                                       p->zs + r0 * p->N, p->N, P);
+  if (finish)
+    softmax_finish<<<rows * P, kSoftmaxThreads, 0, st>>>(p->z2 + r0 * p->N, p->part + r0 * P,
+                                                         p->zs + r0 * p->N, p->N, P);
   return cudaGetLastError();
 }
 
