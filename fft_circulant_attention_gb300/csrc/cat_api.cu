@@ -134,6 +134,8 @@ void free_plan(cat_plan_s* p) {
     if (p->ev_front[k]) cudaEventDestroy(p->ev_front[k]);
   }
   if (p->ev_fork) cudaEventDestroy(p->ev_fork);
+  if (p->gexec) cudaGraphExecDestroy(p->gexec);
+  if (p->cap) cudaStreamDestroy(p->cap);
   cudaFree(p->z2);
   cudaFree(p->zs);
   cudaFree(p->part);
@@ -271,9 +273,10 @@ void describe(cat_plan_s* p) {
                   p->sm.spec_threads, p->workspace_bytes, p->launches);
   } else if (p->path == cat::PATH_FAST) {
     std::snprintf(p->desc, sizeof(p->desc),
-                  "path=fast N=%d N1=%d N2=%d chunk_bh=%d scratch=%zu workspace=%zu launches=%d",
+                  "path=fast N=%d N1=%d N2=%d chunk_bh=%d scratch=%zu workspace=%zu graph=%d "
+                  "launches=%d",
                   p->N, p->fs.N1, p->fs.N2, p->fs.chunk_bh, p->scratch_bytes,
-                  p->workspace_bytes, p->launches);
+                  p->workspace_bytes, p->use_graph, p->launches);
   } else {
     char r1[64] = {0}, r2[64] = {0};
     radstr(p->fs.rp1, r1, sizeof(r1));
@@ -399,6 +402,44 @@ cudaError_t run_fast_overlapped(cat_plan_s* p, const void* X, const void* WA, co
   return e;
 }
 
+// The fast path through a CUDA graph: the overlapped schedule is captured
+// on the private stream (its fork and join events pull the two internal
+// streams into the capture), instantiated once, updated in place when the
+// call's pointers change, and launched on the plan's stream.  A graph launch
+// replaces the schedule's ~30 separate launches and event operations.
+cudaError_t launch_fast_graph(cat_plan_s* p, const void* X, const void* WA, const void* V,
+                              void* O) {
+  if (!p->gexec || X != p->gX || WA != p->gWA || V != p->gV || O != p->gO) {
+    cudaStream_t saved = p->stream;
+    p->stream = p->cap;
+    cudaGraph_t g = nullptr;
+    cudaError_t e = cudaStreamBeginCapture(p->cap, cudaStreamCaptureModeThreadLocal);
+    if (e == cudaSuccess) {
+      const cudaError_t e1 = run_fast_overlapped(p, X, WA, V, O);
+      const cudaError_t e2 = cudaStreamEndCapture(p->cap, &g);
+      e = e1 != cudaSuccess ? e1 : e2;
+    }
+    p->stream = saved;
+    if (e == cudaSuccess && p->gexec) {
+      cudaGraphExecUpdateResultInfo info;
+      if (cudaGraphExecUpdate(p->gexec, g, &info) != cudaSuccess) {
+        cudaGetLastError();
+        cudaGraphExecDestroy(p->gexec);
+        p->gexec = nullptr;
+      }
+    }
+    if (e == cudaSuccess && !p->gexec) e = cudaGraphInstantiate(&p->gexec, g, 0);
+    if (g) cudaGraphDestroy(g);
+    if (e != cudaSuccess) {
+      if (p->gexec) cudaGraphExecDestroy(p->gexec);
+      p->gexec = nullptr;
+      return e;
+    }
+    p->gX = X; p->gWA = WA; p->gV = V; p->gO = O;
+  }
+  return cudaGraphLaunch(p->gexec, p->stream);
+}
+
 }  // namespace
 
 int cat_plan_create(cat_plan_t* out, int B, int N, int D, int H, int dtype, void* stream) {
@@ -469,6 +510,10 @@ int cat_plan_create(cat_plan_t* out, int B, int N, int D, int H, int dtype, void
       if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_front[k], cudaEventDisableTiming);
     }
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_fork, cudaEventDisableTiming);
+    p->use_graph = 1;
+    if (const char* g = std::getenv("CAT_GRAPH")) p->use_graph = std::strcmp(g, "0") != 0;
+    if (e == cudaSuccess && p->use_graph)
+      e = cudaStreamCreateWithFlags(&p->cap, cudaStreamNonBlocking);
   }
   if (e != cudaSuccess) { free_plan(p); return CAT_ERR_CUDA; }
   describe(p);
@@ -509,7 +554,18 @@ int cat_forward(cat_plan_t p, const void* X, const void* WA, const void* V, void
     return CAT_ERR_ALIAS;
   cudaEvent_t* ev = nullptr;
   if (p->timing_n < p->timing_cap) ev = p->ev + 4 * p->timing_n++;
-  if (!ev && p->path == cat::PATH_FAST) return map_cuda(run_fast_overlapped(p, X, WA, V, O));
+  if (!ev && p->path == cat::PATH_FAST) {
+    if (p->use_graph) {
+      const cudaError_t e = launch_fast_graph(p, X, WA, V, O);
+      if (e == cudaSuccess) return CAT_OK;
+      // Capture or instantiation failed: clear the error and launch the same
+      // schedule directly from now on.
+      cudaGetLastError();
+      p->use_graph = 0;
+      describe(p);
+    }
+    return map_cuda(run_fast_overlapped(p, X, WA, V, O));
+  }
   if (ev) cudaEventRecord(ev[0], p->stream);
   cudaError_t e = cat::launch_score(p, X, WA);
   if (e != cudaSuccess) return CAT_ERR_CUDA;

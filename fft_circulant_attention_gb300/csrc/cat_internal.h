@@ -71,6 +71,12 @@ struct cat_plan_s {
   // that one's score and small kernels overlap the other's FFT passes
   cudaStream_t side[2];
   cudaEvent_t ev_fork, ev_join[2], ev_front[2];
+  // fast path: the overlapped schedule captured once as a CUDA graph (on the
+  // private stream cap) and replayed while the call's pointers stay the same
+  int use_graph;
+  cudaStream_t cap;
+  cudaGraphExec_t gexec;
+  const void* gX; const void* gWA; const void* gV; void* gO;
   unsigned int* status;     // device status word
   size_t workspace_bytes;
   // device staging for host-buffer calls (allocated at the first such call)

@@ -182,18 +182,33 @@ __device__ __forceinline__ void stage_wt(unsigned short* wt, int ws, const unsig
   for (int hh = HT; hh < rows; ++hh)
     for (int d = tid; d < D; d += nthr) wt[hh * ws + d] = 0;
   if (H % 8 == 0 && ((uintptr_t)wa & 15) == 0) {
+    // kBatch vectors per thread are loaded before any is stored, so their
+    // latencies overlap instead of adding up.
+    constexpr int kBatch = 8;
     const int vpr = H / 8;                        // 16-byte vectors per row of W_A
+    const int total = D * vpr;
     const uint4* wv = reinterpret_cast<const uint4*>(wa);
-    for (int i = tid; i < D * vpr; i += nthr) {
-      const int d = i / vpr, hb = (i - d * vpr) * 8 - h0;   // head of the vector's element 0
-      if (hb + 8 <= 0 || hb >= HT) continue;
-      const uint4 v = __ldg(wv + i);
-      const unsigned w[4] = {v.x, v.y, v.z, v.w};
+    for (int i0 = tid; i0 < total; i0 += kBatch * nthr) {
+      uint4 v[kBatch];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const int hh = hb + q;
-        if (hh >= 0 && hh < HT && hh < rows)
-          wt[hh * ws + d] = (unsigned short)((q & 1) ? (w[q >> 1] >> 16) : (w[q >> 1] & 0xffffu));
+      for (int j = 0; j < kBatch; ++j) {
+        const int i = i0 + j * nthr;
+        const int d = i / vpr, hb = (i - d * vpr) * 8 - h0;   // head of the vector's element 0
+        v[j] = (i < total && hb + 8 > 0 && hb < HT) ? __ldg(wv + i) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const int i = i0 + j * nthr;
+        const int d = i / vpr, hb = (i - d * vpr) * 8 - h0;
+        if (i >= total || hb + 8 <= 0 || hb >= HT) continue;
+        const unsigned w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int hh = hb + q;
+          if (hh >= 0 && hh < HT && hh < rows)
+            wt[hh * ws + d] =
+                (unsigned short)((q & 1) ? (w[q >> 1] >> 16) : (w[q >> 1] & 0xffffu));
+        }
       }
     }
   } else {
@@ -448,9 +463,14 @@ static cudaError_t score_tma(const cat_plan_s* p, const void* X, const void* WA,
   const int row0 = sp.b0 * p->N;
   const int row_end = (sp.b0 + sp.nb(p)) * p->N;
   const int ntiles = (row_end - row0 + kTsRows - 1) / kTsRows;
+  if (ntiles <= 0) return cudaSuccess;
   const size_t smem = score_tma_smem(p->D);
   const int per_sm = smem <= (113u << 10) ? 2 : 1;
-  const int grid = ntiles < per_sm * p->sms ? ntiles : per_sm * p->sms;
+  // Every CTA takes the same number of tiles (the last one possibly fewer),
+  // so no CTA runs a lone extra tile at the end.
+  const int max_grid = per_sm * p->sms;
+  const int per_cta = (ntiles + max_grid - 1) / max_grid;
+  const int grid = (ntiles + per_cta - 1) / per_cta;
   const cudaStream_t st = sp.stream(p);
   for (int h0 = 0; h0 < p->H; h0 += 16) {
     const int ht = p->H - h0 < 16 ? p->H - h0 : 16;
