@@ -130,6 +130,15 @@ __device__ __forceinline__ void discard_l2(const void* p) {
   asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
 }
 
+// Order this thread's view of earlier shared-memory accesses in the generic
+// proxy (loads by any thread that released the buffer to it through an
+// mbarrier, or its own) before its later async-proxy accesses.  Needed
+// before a tensor or bulk copy rewrites a stage that was read with ordinary
+// loads: without it the copy may land before those reads are performed.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Plain arrive (count 1) on an mbarrier.
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");

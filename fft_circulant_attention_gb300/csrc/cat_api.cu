@@ -193,9 +193,10 @@ int choose_path(cat_plan_s* p) {
       f.chunk_bh = (int)chunk;
       p->scratch_bytes = 2 * (size_t)f.chunk_bh * per_bh;
       const int chunks_per_batch = (int)((p->H + chunk - 1) / chunk);
-      // Front (score, softmax partials, spectrum: 3 + score passes) once,
-      // then passes A, B, C per chunk.
-      p->launches = score_launches(p->H, p->D) + 3 + 3 * p->B * chunks_per_batch;
+      // Front once — the score passes, then the spectrum of z* (one launch for
+      // N2 = 32; softmax partials and two launches for longer rows) — then
+      // passes A, B, C per chunk.
+      p->launches = score_launches(p->H, p->D) + (f.N2 == 32 ? 1 : 3) + 3 * p->B * chunks_per_batch;
       return CAT_OK;
     }
   }
@@ -338,62 +339,37 @@ extern "C" {
 
 namespace {
 
-// Fast path, overlapped schedules on the plan's two internal streams, which
-// fork from and join back into the plan's stream.  Default (front_all):
-// score, softmax partials and spectrum of all batches first, then the
-// chunks alternate between the streams.  CAT_SCHEDULE=batch: batch b's
-// front goes to stream b mod 2 and the chunks of its rows alternate between
-// the streams, a chunk on the other stream first waiting for the batch's
-// spectrum.  Each stream uses its own scratch slot.
+// Fast path, overlapped schedule: the score and the spectrum of z* (each a
+// single launch over all batches) on the plan's stream; the chunks' passes
+// alternate between the two internal streams, one scratch slot each.  The
+// internal streams fork from the plan's stream at p->fork_at; when that is
+// before the spectrum, each waits for it just before its first pass B, so
+// the first passes A run beside the score and the spectrum.  Both join back
+// into the plan's stream at the end.
 cudaError_t run_fast_overlapped(cat_plan_s* p, const void* X, const void* WA, const void* V,
                                 void* O) {
-  if (p->front_all) {
-    // Score, softmax partials and spectrum of every batch as single launches
-    // on the plan's stream (each fills the GPU), then the chunks' passes
-    // alternate over the two internal streams, one scratch slot each.
-    cudaError_t e = cat::launch_score(p, X, WA);
-    if (e == cudaSuccess) e = cat::launch_softmax(p, cat::Span{}, false);
-    if (e == cudaSuccess) e = cat::launch_fast_zspec(p, 0, p->B * p->H, p->stream);
+  cudaError_t e = cudaSuccess;
+  auto fork = [&]() {
     if (e == cudaSuccess) e = cudaEventRecord(p->ev_fork, p->stream);
     for (int k = 0; k < 2 && e == cudaSuccess; ++k)
       e = cudaStreamWaitEvent(p->side[k], p->ev_fork, 0);
-    const int rows = p->B * p->H;
-    int g = 0;
-    for (int b = 0; b < p->B && e == cudaSuccess; ++b)
-      for (int h0 = 0; h0 < p->H && e == cudaSuccess; h0 += p->fs.chunk_bh, ++g) {
-        const int nb = p->H - h0 < p->fs.chunk_bh ? p->H - h0 : p->fs.chunk_bh;
-        e = cat::launch_fast_chunk(p, V, O, b * p->H + h0, nb, g & 1, p->side[g & 1]);
-      }
-    (void)rows;
-    for (int k = 0; k < 2; ++k) {
-      cudaError_t e2 = cudaEventRecord(p->ev_join[k], p->side[k]);
-      if (e2 == cudaSuccess) e2 = cudaStreamWaitEvent(p->stream, p->ev_join[k], 0);
-      if (e == cudaSuccess) e = e2;
-    }
-    return e;
-  }
-  cudaError_t e = cudaEventRecord(p->ev_fork, p->stream);
-  for (int k = 0; k < 2 && e == cudaSuccess; ++k) e = cudaStreamWaitEvent(p->side[k], p->ev_fork, 0);
+  };
+  if (p->fork_at == cat::FORK_START) fork();
+  if (e == cudaSuccess) e = cat::launch_score(p, X, WA);
+  if (p->fork_at == cat::FORK_SCORE) fork();
+  if (e == cudaSuccess) e = cat::launch_fast_zspec(p, 0, p->B * p->H, p->stream);
+  if (p->fork_at == cat::FORK_SPECTRUM) fork();
+  else if (e == cudaSuccess) e = cudaEventRecord(p->ev_front[0], p->stream);
+  bool waited[2] = {p->fork_at == cat::FORK_SPECTRUM, p->fork_at == cat::FORK_SPECTRUM};
   int g = 0;
-  for (int b = 0; b < p->B && e == cudaSuccess; ++b) {
-    const int kb = b & 1;
-    cudaStream_t sb = p->side[kb];
-    cat::Span sp;
-    sp.b0 = b;
-    sp.nbat = 1;
-    sp.st = sb;
-    sp.own = true;
-    e = cat::launch_score(p, X, WA, sp);
-    if (e == cudaSuccess) e = cat::launch_softmax(p, sp, false);
-    if (e == cudaSuccess) e = cat::launch_fast_zspec(p, b * p->H, p->H, sb);
-    if (e == cudaSuccess) e = cudaEventRecord(p->ev_front[kb], sb);
+  for (int b = 0; b < p->B && e == cudaSuccess; ++b)
     for (int h0 = 0; h0 < p->H && e == cudaSuccess; h0 += p->fs.chunk_bh, ++g) {
       const int nb = p->H - h0 < p->fs.chunk_bh ? p->H - h0 : p->fs.chunk_bh;
       const int k = g & 1;
-      if (k != kb) e = cudaStreamWaitEvent(p->side[k], p->ev_front[kb], 0);
-      if (e == cudaSuccess) e = cat::launch_fast_chunk(p, V, O, b * p->H + h0, nb, k, p->side[k]);
+      e = cat::launch_fast_chunk(p, V, O, b * p->H + h0, nb, k, p->side[k],
+                                 waited[k] ? nullptr : p->ev_front[0]);
+      waited[k] = true;
     }
-  }
   for (int k = 0; k < 2; ++k) {
     cudaError_t e2 = cudaEventRecord(p->ev_join[k], p->side[k]);
     if (e2 == cudaSuccess) e2 = cudaStreamWaitEvent(p->stream, p->ev_join[k], 0);
@@ -453,14 +429,19 @@ int cat_plan_create(cat_plan_t* out, int B, int N, int D, int H, int dtype, void
   p->dh = D / H;
   p->npair = (p->dh + 1) / 2;
   p->stream = (cudaStream_t)stream;
-  p->front_all = 1;
-  if (const char* sc = std::getenv("CAT_SCHEDULE")) p->front_all = std::strcmp(sc, "batch") != 0;
+  st = choose_path(p);
+  if (st != CAT_OK) { delete p; return st; }
+  // Default fork point: after the score when the spectrum is one launch
+  // (N2 = 32, where the first passes A then overlap it), else after it.
+  p->fork_at = p->path == cat::PATH_FAST && p->fs.N2 == 32 ? cat::FORK_SCORE : cat::FORK_SPECTRUM;
+  if (const char* sc = std::getenv("CAT_FORK"))
+    p->fork_at = std::strcmp(sc, "start") == 0   ? cat::FORK_START
+                 : std::strcmp(sc, "score") == 0 ? cat::FORK_SCORE
+                                                 : cat::FORK_SPECTRUM;
   if (const char* sc = std::getenv("CAT_SCORE")) {
     p->score_cuda_cores = std::strcmp(sc, "cuda") == 0;
     p->score_path = std::strcmp(sc, "mma") == 0 ? 1 : 0;
   }
-  st = choose_path(p);
-  if (st != CAT_OK) { delete p; return st; }
 
   if (cudaGetDevice(&p->device) != cudaSuccess ||
       cudaDeviceGetAttribute(&p->sms, cudaDevAttrMultiProcessorCount, p->device) != cudaSuccess) {
@@ -570,7 +551,9 @@ int cat_forward(cat_plan_t p, const void* X, const void* WA, const void* V, void
   cudaError_t e = cat::launch_score(p, X, WA);
   if (e != cudaSuccess) return CAT_ERR_CUDA;
   if (ev) cudaEventRecord(ev[1], p->stream);
-  e = p->path == cat::PATH_SMEM ? cat::launch_softmax_spectrum(p) : cat::launch_softmax(p);
+  e = p->path == cat::PATH_SMEM   ? cat::launch_softmax_spectrum(p)
+      : p->path == cat::PATH_FAST ? cat::launch_fast_zspec(p, 0, p->B * p->H, p->stream)
+                                  : cat::launch_softmax(p);
   if (e != cudaSuccess) return CAT_ERR_CUDA;
   if (ev) cudaEventRecord(ev[2], p->stream);
   e = p->path == cat::PATH_SMEM       ? cat::launch_conv_smem(p, V, O)

@@ -56,7 +56,7 @@ struct cat_plan_s {
   cat::FourStepCfg fs;
   int score_cuda_cores;     // 1: bf16 scores on the CUDA-core kernel (testing)
   int score_path;           // 1: bf16 scores on the register-fed MMA kernel (testing)
-  int front_all;            // fast path: score/softmax/spectrum of all batches first
+  int fork_at;              // fast path: where the chunk streams fork (cat::FORK_*)
   // workspace (device)
   float2* z2;               // [B, H, N] scores as double-float (hi, lo)
   float* zs;                // [B, H, N] z* (softmax weights)
@@ -99,6 +99,11 @@ int softmax_parts(int N);
 
 namespace cat {
 
+// Fork points of the fast path's overlapped schedule: the chunk streams
+// start after the spectrum of z*, after the score, or at once (their passes
+// A need only V; passes B wait for the spectrum).
+enum { FORK_SPECTRUM = 0, FORK_SCORE = 1, FORK_START = 2 };
+
 // A range of batches and the stream its work goes to (default: all batches,
 // the plan's stream).
 struct Span {
@@ -140,10 +145,11 @@ cudaError_t launch_fourstep_conv(const cat_plan_s* p, const void* V, void* O);
 cudaError_t launch_fast_conv(const cat_plan_s* p, const void* V, void* O);
 // Fast path pieces for the overlapped schedule: the spectrum of z* for
 // (b, h) rows [row0, row0 + nrows), and passes A, B, C of one chunk of rows
-// [bh0, bh0 + nb) with scratch buffer `slot`, all on stream st.
+// [bh0, bh0 + nb) with scratch buffer `slot`, all on stream st.  If
+// before_b is given, pass B (the first to read the spectrum) waits for it.
 cudaError_t launch_fast_zspec(const cat_plan_s* p, int row0, int nrows, cudaStream_t st);
 cudaError_t launch_fast_chunk(const cat_plan_s* p, const void* V, void* O, int bh0, int nb,
-                              int slot, cudaStream_t st);
+                              int slot, cudaStream_t st, cudaEvent_t before_b = nullptr);
 
 // Shape validation and shared-memory-path configuration without allocation.
 int validate(int B, int N, int D, int H, int dtype);

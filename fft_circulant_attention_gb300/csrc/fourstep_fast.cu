@@ -22,8 +22,9 @@
 // holding exactly the bins the first inverse step needs, so pass B takes
 // the product and starts the inverse without touching shared memory.
 //
-// The spectrum of z* is computed once per (b, h) by zspec_a/zspec_b (the
-// same register transforms) and stored in the order pass B's threads hold
+// The spectrum of z* is computed once per (b, h) — by zspec_row, one CTA per
+// row, for N2 = 32; by zspec_a/zspec_b for longer rows — with the same
+// register transforms, and stored in the order pass B's threads hold
 // the bins: thread j of the CTA for k2 holds k1 = 2j + e + 32s (e < 2,
 // s < 16), stored at ((k2·16 + j)·16 + s)·2 + e.
 #include <cuda_bf16.h>
@@ -229,6 +230,7 @@ fsf_pass_a32(const __grid_constant__ CUtensorMap tmV, float2* __restrict__ scr,
   const uint64_t keep = policy_evict_last(), stream = policy_evict_first();
   auto issue = [&](int s, int item) {
     if (lane == 0) {
+      fence_proxy_async_smem();   // the warp's reads of this stage come first
       const int bh = bh0 + item % nb, n1 = item / nb;
       const int b = bh / H, h = bh - b * H;
       mbar_expect_tx(bar + s, 32 * P::kRowBytes);
@@ -278,6 +280,7 @@ fsf_pass_c32(const __grid_constant__ CUtensorMap tmC, const float2* __restrict__
   const int items = nb * kFastN1;
   auto issue = [&](int s, int item) {
     if (lane == 0) {
+      fence_proxy_async_smem();   // the warp's reads of this stage come first
       mbar_expect_tx(bar + s, 32 * P::kRowBytes);
       tma_load_4d(stage + s * 32 * P::kRowBytes, &tmC, 0, item / nb, 0, item % nb, bar + s);
     }
@@ -438,12 +441,13 @@ fsf_pass_b(float2* __restrict__ scr, const float2* __restrict__ zft,
   }
 }
 
-// Builds pass B's twiddle tables: [tf | ti | tx for k2 = 0..N2-1], from the
-// plan's table W[e] = exp(-2πi e/N).
+// Builds pass B's twiddle tables [tf | ti | tx for k2 = 0..N2-1] and, for
+// N2 = 32, the spectrum kernel's t1, from the plan's table
+// W[e] = exp(-2πi e/N).
 __global__ void fsf_build_tables(float2* __restrict__ tabs, const float2* __restrict__ W, int N,
                                  int N2) {
   const int wstep = N / kFastN1;
-  const int total = 2 * kTabB + N2 * kTabB;
+  const int total = 2 * kTabB + N2 * kTabB + (N2 == 32 ? 32 * kFastN1 : 0);
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
     float2 v;
     if (i < kTabB) {                       // tf[k][u]
@@ -452,17 +456,21 @@ __global__ void fsf_build_tables(float2* __restrict__ tabs, const float2* __rest
     } else if (i < 2 * kTabB) {            // ti[j][u]
       const int r = i - kTabB, jj = r / 32, u = r % 32;
       v = W[(size_t)(u * jj) * wstep];
-    } else {                               // tx[k2][j][q]
+    } else if (i < (2 + N2) * kTabB) {     // tx[k2][j][q]
       const int r = i - 2 * kTabB, kk = r / kTabB, r2 = r % kTabB;
       const int jj = r2 / 32, q = r2 % 32;
       v = W[(size_t)(jj + 16 * q) * kk];
+    } else {                               // t1[k2][n1] (N2 = 32)
+      const int r = i - (2 + N2) * kTabB, kk = r / kFastN1, n1 = r % kFastN1;
+      v = W[(size_t)n1 * kk];
     }
     tabs[i] = v;
   }
 }
 
 // ---------------------------------------------------------------------------
-// Spectrum of z* in pass B's order, with the same register transforms.
+// Spectrum of z* in pass B's order for N2 > 32 (rows longer than one CTA
+// holds), with the same register transforms.
 // zspec_a (per n1, over n2): applies the softmax itself — z* = exp(z - m)/S
 // from the double-float scores and the row's chunk partials — then the DFT;
 // lanes are consecutive n1 of one (b, h) row, so the strided reads are
@@ -477,25 +485,9 @@ __global__ void __launch_bounds__(256)
 fsf_zspec_a(const float2* __restrict__ z2, const float2* __restrict__ part, int P,
             float2* __restrict__ zscr, const float2* __restrict__ W, int N) {
   __shared__ float stats[2];
+  static_assert(N2 > 32, "N2 = 32 rows take fsf_zspec_row");
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if constexpr (N2 == 32) {
-    const int row = blockIdx.x >> 3;
-    const int n1 = (blockIdx.x & 7) * 64 + threadIdx.x;
-    const float2* src = z2 + (size_t)row * N + n1;
-    float2 zv[32];
-#pragma unroll
-    for (int n2 = 0; n2 < 32; ++n2) zv[n2] = __ldg(src + kFastN1 * n2);
-    row_softmax_stats(part + (size_t)row * P, P, stats);
-    const float m = stats[0], inv = stats[1];
-    float2 a[32];
-#pragma unroll
-    for (int n2 = 0; n2 < 32; ++n2) a[n2] = make_float2(exp_shifted(zv[n2], m) * inv, 0.f);
-    dft<32, false>(a);
-    float2* dst = zscr + (size_t)row * N + n1;
-#pragma unroll
-    for (int k2 = 0; k2 < 32; ++k2)
-      dst[(size_t)k2 * kFastN1] = cmul(a[k2], __ldg(&W[(size_t)n1 * k2]));
-  } else {
+  {
     constexpr int TS = N2 / 32;
     constexpr int R2 = N2 / 32;
     constexpr int PER = 32 / TS;
@@ -580,6 +572,110 @@ fsf_zspec_b(const float2* __restrict__ zscr, float2* __restrict__ zft, const flo
 }
 
 // ---------------------------------------------------------------------------
+// Spectrum of z* for N = 16384 (N2 = 32) in one CTA per (b, h) row: the
+// softmax and both DFT passes of the row without leaving the SM.  Thread t
+// (of 512) loads the scores z[t + 512·u], u < 32 — the length-32 signal of
+// n1 = t over n2 = u — so the row maximum and the sum of exp(z - m) are
+// block reductions over registers, and the first pass (DFT over n2, times
+// w_N^{n1 k2}) needs no exchange.  Its results go to shared memory as
+// [k2][n1]; the second pass (DFT over n1 per k2, 16 threads per k2 exactly
+// as pass B's forward steps) stores FFT(z*)/N in pass B's order.
+// ---------------------------------------------------------------------------
+constexpr int kZRowThreads = 512;
+constexpr int kZRowStride = kRowB;        // shared row of one k2 signal (float2)
+constexpr size_t kZRowBuf = (size_t)32 * kZRowStride * sizeof(float2);
+constexpr size_t kSmemZRow = kZRowBuf + kTabB * sizeof(float2) + 16;
+
+__global__ void __launch_bounds__(kZRowThreads, 1)
+fsf_zspec_row(const float2* __restrict__ z2, float2* __restrict__ zft,
+              const float2* __restrict__ tabs, int N, unsigned int* status) {
+  extern __shared__ float4 smem4[];
+  float2* buf = reinterpret_cast<float2*>(smem4);
+  float2* tfs = buf + 32 * kZRowStride;                        // tf[k][u] = w_512^{u·k}
+  uint64_t* bar = reinterpret_cast<uint64_t*>(tfs + kTabB);
+  __shared__ float red[32];
+  const int t = threadIdx.x;
+  const int row = blockIdx.x;
+  // The first-pass twiddles t1[k2][n1] land in the row buffer itself, each
+  // where the thread that multiplies by it will store its product; tf goes
+  // after it.  Bulk copies, in flight while the scores load.
+  if (t == 0) {
+    mbar_init(bar, 1);
+    mbar_fence_init();
+    const float2* t1 = tabs + (size_t)(2 + 32) * kTabB;
+    mbar_expect_tx(bar, (32 * kFastN1 + kTabB) * (uint32_t)sizeof(float2));
+    for (int k2 = 0; k2 < 32; ++k2)
+      bulk_g2s(buf + k2 * kZRowStride, t1 + k2 * kFastN1, kFastN1 * sizeof(float2), bar);
+    bulk_g2s(tfs, tabs, kTabB * sizeof(float2), bar);
+  }
+  const float2* src = z2 + (size_t)row * N;
+  float2 a[32];
+#pragma unroll
+  for (int u = 0; u < 32; ++u) a[u] = __ldg(src + t + kFastN1 * u);
+  float m = -INFINITY;
+#pragma unroll
+  for (int u = 0; u < 32; ++u) m = fmaxf(m, a[u].x);
+  m = block_reduce<true>(m, red);     // (its barriers also publish the mbarrier init)
+  float S = 0.f;
+#pragma unroll
+  for (int u = 0; u < 32; ++u) {
+    const float e = exp_shifted(a[u], m);
+    a[u] = make_float2(e, 0.f);
+    S += e;
+  }
+  S = block_reduce<false>(S, red);
+  const float inv = 1.0f / S;
+#pragma unroll
+  for (int u = 0; u < 32; ++u) a[u].x *= inv;
+  dft<32, false>(a);
+  const bool ok = __syncthreads_and(mbar_wait(bar, 0, status, 0x503));
+  // Twiddle w_N^{n1·k2} (n1 = t) and store [k2][n1].
+  if (ok) {
+#pragma unroll
+    for (int k2 = 0; k2 < 32; ++k2) {
+      float2* e = buf + k2 * kZRowStride + t;
+      *e = cmul(a[k2], *e);
+    }
+  }
+  __syncthreads();
+  if (!ok) return;
+
+  // Second pass, lanes laid out as in pass B: signal k2 = (lane mod 16) +
+  // 16·(warp mod 2), thread j = 2·(warp / 2) + lane / 16 of it.
+  const int lane = t & 31, warp = t >> 5;
+  const int k2 = (lane & 15) + 16 * (warp & 1), j = 2 * (warp >> 1) + (lane >> 4);
+  float2* rb = buf + k2 * kZRowStride;
+#pragma unroll
+  for (int u = 0; u < 32; ++u) a[u] = rb[j + 16 * u];
+  __syncthreads();
+  dft<32, false>(a);
+#pragma unroll
+  for (int q = 0; q < 32; q += 2) st_sh2(rb + 32 * j + q, a[q], a[q + 1]);
+  __syncthreads();
+  float2 c[2][16];
+#pragma unroll
+  for (int u = 0; u < 16; ++u) ld_sh2(rb + 2 * j + 32 * u, c[0][u], c[1][u]);
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    const float2* tw = tfs + (2 * j + e) * 16;
+#pragma unroll
+    for (int u = 2; u < 16; u += 2) {
+      float2 w0, w1;
+      ld_sh2(tw + u, w0, w1);
+      c[e][u] = cmul(c[e][u], w0);
+      c[e][u + 1] = cmul(c[e][u + 1], w1);
+    }
+    c[e][1] = cmul(c[e][1], tw[1]);
+    dft<16, false>(c[e]);
+  }
+  const float invN = 1.0f / (float)N;
+  float4* out = reinterpret_cast<float4*>(zft) + (((size_t)row * 32 + k2) * 16 + j) * 16;
+#pragma unroll
+  for (int q = 0; q < 16; ++q)
+    out[q] = make_float4(c[0][q].x * invN, c[0][q].y * invN, c[1][q].x * invN, c[1][q].y * invN);
+}
+
+// ---------------------------------------------------------------------------
 // Host side.
 // ---------------------------------------------------------------------------
 size_t fast_smem_a(int N2) { return N2 == 32 ? 0 : (size_t)kFastPairs * (N2 + 2) * sizeof(float2); }
@@ -593,7 +689,7 @@ static cudaError_t setup_t(int N2) {
   case n:                                                           \
     e = allow_max_smem(fsf_pass_a<T, n>);                           \
     if (e == cudaSuccess) e = allow_max_smem(fsf_pass_c<T, n>);     \
-    if (e == cudaSuccess) e = allow_max_smem(fsf_zspec_a<n>);       \
+    if (e == cudaSuccess && n > 32) e = allow_max_smem(fsf_zspec_a<(n > 32 ? n : 64)>); \
     break;
     CAT_N2(32) CAT_N2(64) CAT_N2(128) CAT_N2(256)
 #undef CAT_N2
@@ -603,10 +699,15 @@ static cudaError_t setup_t(int N2) {
   if (e == cudaSuccess) e = allow_max_smem(fsf_pass_a32<T>);
   if (e == cudaSuccess) e = allow_max_smem(fsf_pass_c32<T>);
   if (e == cudaSuccess) e = allow_max_smem(fsf_zspec_b);
+  if (e == cudaSuccess) e = allow_max_smem(fsf_zspec_row);
   return e;
 }
 
-size_t fast_tables_bytes(int N2) { return (size_t)(2 + N2) * kTabB * sizeof(float2); }
+// [tf | ti | tx for k2 < N2], then for N2 = 32 the spectrum kernel's
+// first-pass twiddles t1[k2][n1] = w_N^{n1·k2}.
+size_t fast_tables_bytes(int N2) {
+  return ((size_t)(2 + N2) * kTabB + (N2 == 32 ? (size_t)32 * kFastN1 : 0)) * sizeof(float2);
+}
 
 cudaError_t setup_fast_kernels(cat_plan_s* p) {
   cudaError_t e = p->dtype == 1 ? setup_t<__nv_bfloat16>(p->fs.N2) : setup_t<float>(p->fs.N2);
@@ -660,15 +761,27 @@ static bool encode_v_map(const cat_plan_s* p, const T* V, CUtensorMap* tmV) {
 
 cudaError_t launch_fast_zspec(const cat_plan_s* p, int row0, int nrows, cudaStream_t st) {
   const int N2 = p->fs.N2;
+  if (nrows <= 0) return cudaSuccess;
+  if (N2 == 32) {
+    fsf_zspec_row<<<nrows, kZRowThreads, kSmemZRow, st>>>(p->z2 + (size_t)row0 * p->N,
+                                                          p->zf + (size_t)row0 * p->N, p->tabs,
+                                                          p->N, p->status);
+    return cudaGetLastError();
+  }
+  // Longer rows: the multi-CTA softmax's chunk partials, then the two passes.
+  Span sp;
+  sp.b0 = row0 / p->H;
+  sp.nbat = nrows / p->H;
+  sp.st = st;
+  sp.own = true;
+  cudaError_t e0 = launch_softmax(p, sp, false);
+  if (e0 != cudaSuccess) return e0;
   const int P = softmax_parts(p->N);
   const float2* z2 = p->z2 + (size_t)row0 * p->N;
   const float2* part = p->part + (size_t)row0 * P;
   float2* zscr = p->zscr + (size_t)row0 * p->N;
   float2* zf = p->zf + (size_t)row0 * p->N;
   switch (N2) {
-    case 32:
-      fsf_zspec_a<32><<<nrows * 8, 64, 0, st>>>(z2, part, P, zscr, p->tw, p->N);
-      break;
 #define CAT_ZA(n)                                                                      \
   case n:                                                                              \
     fsf_zspec_a<n><<<nrows * (kFastN1 / 32), n, fast_smem_a(n), st>>>(z2, part, P, zscr, \
@@ -684,7 +797,7 @@ cudaError_t launch_fast_zspec(const cat_plan_s* p, int row0, int nrows, cudaStre
 
 template <typename T>
 static cudaError_t chunk_t(const cat_plan_s* p, const T* V, T* O, int bh0, int nb, int slot,
-                           cudaStream_t st, const CUtensorMap* tmV) {
+                           cudaStream_t st, const CUtensorMap* tmV, cudaEvent_t before_b) {
   const int N2 = p->fs.N2;
   float2* scr = p->scratch + (size_t)slot * (p->scratch_bytes / 2 / sizeof(float2));
   auto ac = [&](bool pass_a) {
@@ -712,6 +825,10 @@ static cudaError_t chunk_t(const cat_plan_s* p, const T* V, T* O, int bh0, int n
     }
   };
   ac(true);
+  if (before_b) {
+    const cudaError_t e = cudaStreamWaitEvent(st, before_b, 0);
+    if (e != cudaSuccess) return e;
+  }
   fsf_pass_b<<<nb * N2 * (kFastPairs / kBPairs), kBPairs * 16, kSmemB, st>>>(scr, p->zf, p->tabs,
                                                                              N2, bh0);
   ac(false);
@@ -719,24 +836,25 @@ static cudaError_t chunk_t(const cat_plan_s* p, const T* V, T* O, int bh0, int n
 }
 
 cudaError_t launch_fast_chunk(const cat_plan_s* p, const void* V, void* O, int bh0, int nb,
-                              int slot, cudaStream_t st) {
+                              int slot, cudaStream_t st, cudaEvent_t before_b) {
   CUtensorMap tmV;
   if (p->dtype == 1) {
     if (p->fs.N2 == 32 && !encode_v_map(p, (const __nv_bfloat16*)V, &tmV))
       return cudaErrorInvalidValue;
-    return chunk_t(p, (const __nv_bfloat16*)V, (__nv_bfloat16*)O, bh0, nb, slot, st, &tmV);
+    return chunk_t(p, (const __nv_bfloat16*)V, (__nv_bfloat16*)O, bh0, nb, slot, st, &tmV,
+                   before_b);
   }
   if (p->fs.N2 == 32 && !encode_v_map(p, (const float*)V, &tmV)) return cudaErrorInvalidValue;
-  return chunk_t(p, (const float*)V, (float*)O, bh0, nb, slot, st, &tmV);
+  return chunk_t(p, (const float*)V, (float*)O, bh0, nb, slot, st, &tmV, before_b);
 }
 
-// Serialised fast path on the plan's stream (used when stage timing is on):
-// spectrum of z* for all rows, then every chunk in turn on scratch slot 0.
+// Serialised fast path on the plan's stream (used when stage timing is on;
+// the spectrum of z* is already in place): every chunk in turn on scratch
+// slot 0.
 template <typename T>
 static cudaError_t run_t(const cat_plan_s* p, const T* V, T* O) {
   const int rows = p->B * p->H;
-  cudaError_t e = launch_fast_zspec(p, 0, rows, p->stream);
-  if (e != cudaSuccess) return e;
+  cudaError_t e = cudaSuccess;
   for (int bh0 = 0; bh0 < rows; bh0 += p->fs.chunk_bh) {
     const int nb = rows - bh0 < p->fs.chunk_bh ? rows - bh0 : p->fs.chunk_bh;
     e = launch_fast_chunk(p, V, O, bh0, nb, 0, p->stream);

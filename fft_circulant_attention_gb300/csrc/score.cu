@@ -377,7 +377,10 @@ score_tma_kernel(const __grid_constant__ CUtensorMap tmX, const __nv_bfloat16* _
       for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x)
         for (int kb = 0; kb < nkb; ++kb, ++it) {
           const int s = it % kTsStages, use = it / kTsStages;
-          if (use > 0 && !mbar_wait(empty + s, (use - 1) & 1, status, 0x601)) return;
+          if (use > 0) {
+            if (!mbar_wait(empty + s, (use - 1) & 1, status, 0x601)) return;
+            fence_proxy_async_smem();   // the consumers' ldmatrix reads come first
+          }
           mbar_expect_tx(full + s, kTsStageBytes);
           tma_load_2d_hint(stages + s * kTsStageBytes, &tmX, kb * kTsCols, row0 + tile * kTsRows,
                            full + s, stream);
