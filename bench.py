@@ -41,16 +41,15 @@ SMS, FP32_LANES, MAX_SM_MHZ = 152, 128, 2070.0
 FP32_PEAK_TFLOPS = SMS * FP32_LANES * 2 * MAX_SM_MHZ * 1e6 / 1e12
 FALLBACK_HBM_GBS = 6800.0
 
-# DRAM bytes (read + write) of one circulant-product stage (passes A, B, C
-# and the z* spectrum, serialised), summed from an ncu launch list of the
-# same kernel sources (profiles/).  Keyed by (workload, hash of the kernel
-# sources): any change to those sources makes the figure stale, and the
-# bench then reports null.
-NCU_TRAFFIC = {
-    # profiles/launches_long16k.md: fsf_* kernels, warm launch list, per forward
-    ("long16k", "089fa1a37ef4"): 330126250,
-}
+# DRAM bytes (read + write) per launch of the dominant kernel (pass B of the
+# fast path), from the committed ncu launch list of the same kernel sources
+# (profiles/).  Keyed by (workload, hash of the kernel sources): any change
+# to those sources makes the figure stale, and the bench then reports null.
+NCU_TRAFFIC = {}
 KERNEL_SOURCES = ["fourstep_fast.cu", "fft_reg.cuh", "fft_device.cuh", "bulk.cuh", "elem.cuh"]
+# Pass B's transforms: per (pair, k2) signal one forward and one inverse DFT
+# of length N1 = 512, counted as 5·N1·log2(N1) flops each.
+PASS_B_N1 = 512
 
 
 def kernel_hash():
@@ -285,6 +284,7 @@ def measure_workload(name, steps, warmup, device, world, sampler=None):
     for _ in range(stage_steps):
         plan.forward(Xd, Wd, Vd, Od)
     stage_ms, ncalls = plan.stage_times()
+    pass_ms, pass_launches = plan.pass_times() if "path=fast" in desc else ([0.0] * 3, 0)
     plan.timing(0)
     ms_total = max_over_ranks(ms_total, world, device)
 
@@ -307,35 +307,41 @@ def measure_workload(name, steps, warmup, device, world, sampler=None):
     ms_step = ms_total / steps
     a = algorithmic(c)
     hbm, hbm_kind = load_peaks()
-    conv_ms = stage_ms[2] / max(ncalls, 1)
-    t_conv = conv_ms * 1e-3
-    conv_tflops = a["conv_flops"] / t_conv / 1e12
-    conv_gbs = a["conv_bytes"] / t_conv / 1e9
-    t_roof_conv = max(a["conv_bytes"] / (hbm * 1e9), a["conv_flops"] / (FP32_PEAK_TFLOPS * 1e12))
-    bound = "alu" if a["conv_flops"] / FP32_PEAK_TFLOPS / 1e12 >= a["conv_bytes"] / hbm / 1e9 \
-        else "hbm"
+    # Roofline of the dominant kernel, pass B: its average launch duration
+    # from the library's CUDA events around every pass-B launch of the
+    # recorded (serialised) forwards, against its algorithmic flops per
+    # launch: chunk_bh·N2 (b, h, k2) columns × npair signals × two length-512
+    # transforms.
+    chunk = int(desc.split("chunk_bh=")[1].split()[0]) if "chunk_bh=" in desc else 0
+    n2 = c["N"] // PASS_B_N1
+    npair = (c["D"] // c["H"] + 1) // 2
+    b_ms = pass_ms[1] / max(pass_launches, 1)
+    b_flops = chunk * n2 * npair * 2 * fft_flops(PASS_B_N1)
+    b_tflops = b_flops / (b_ms * 1e-3) / 1e12 if b_ms > 0 else 0.0
     roof = {
-        "kernel": "circulant-product stage (%s path: z* spectrum + passes A, B, C), timed "
-                  "serialised on the plan's stream" % desc.split()[0].replace("path=", ""),
-        "bound": bound,
-        "achieved": conv_tflops if bound == "alu" else conv_gbs,
-        "peak": FP32_PEAK_TFLOPS if bound == "alu" else hbm,
-        "unit": "TFLOP/s" if bound == "alu" else "GB/s",
-        "frac": (conv_tflops / FP32_PEAK_TFLOPS) if bound == "alu" else conv_gbs / hbm,
+        "kernel": "fsf_pass_b: per (b, h, k2) and 16 column pairs, the length-512 DFT over n1, "
+                  "the product with FFT(z*)/N and the inverse DFT, on the L2-resident scratch; "
+                  "one launch = one chunk of %d (b, h) rows" % chunk,
+        "bound": "alu",
+        "achieved": b_tflops,
+        "peak": FP32_PEAK_TFLOPS,
+        "unit": "TFLOP/s",
+        "frac": b_tflops / FP32_PEAK_TFLOPS,
         "traffic": NCU_TRAFFIC.get((name, kernel_hash())),
-        "peak_source": ("FP32: 152 SMs x 128 lanes x 2 x 2070 MHz (derived); HBM: %s %.0f GB/s"
-                        % (hbm_kind, hbm)),
-        "hbm_gbs_achieved": conv_gbs,
-        "hbm_frac": conv_gbs / hbm,
-        "ms_per_launch": conv_ms,
-        "roofline_frac_of_stage": t_roof_conv / t_conv,
+        "peak_source": "FP32: 152 SMs x 128 lanes x 2 x 2070 MHz (derived from unit counts "
+                       "and the maximum SM clock)",
+        "flops_per_launch": b_flops,
+        "ms_per_launch": b_ms,
+        "launches_timed": pass_launches,
     }
+    pass_ms_launch = {k: v / max(pass_launches, 1) for k, v in zip("ABC", pass_ms)}
     t_roof = max(a["total_bytes"] / (hbm * 1e9), a["total_flops"] / (FP32_PEAK_TFLOPS * 1e12))
     e2e_val = world * units * e2e_steps / e2e_s
     es = c["es"]
     return {
         "name": name, "c": c, "value": world * units / (ms_step * 1e-3), "ms_per_step": ms_step,
         "stage_ms": [s / max(ncalls, 1) for s in stage_ms], "roofline": roof,
+        "pass_ms_per_launch": pass_ms_launch,
         "path_roofline_frac": t_roof / (ms_step * 1e-3), "t_roof_us": t_roof * 1e6,
         "launches": launches, "desc": desc, "clocks": clocks,
         "e2e": {"value": e2e_val, "unit": UNIT,
@@ -385,8 +391,9 @@ def run_gb300(args, world, rank, local):
         "roofline": prim["roofline"],
         "path_roofline_frac": prim["path_roofline_frac"],
         "stage_ms_serialised": {"score": prim["stage_ms"][0],
-                                "softmax": prim["stage_ms"][1],
+                                "softmax_spectrum": prim["stage_ms"][1],
                                 "circulant_product": prim["stage_ms"][2]},
+        "pass_ms_per_launch_serialised": prim["pass_ms_per_launch"],
         "e2e": prim["e2e"],
         "gpu_launches": prim["launches"] * args.steps,
         "clocks": prim["clocks"],
@@ -398,7 +405,9 @@ def run_gb300(args, world, rank, local):
             "workload": SECONDARY, "B": sc["B"], "N": sc["N"], "D": sc["D"], "H": sc["H"],
             "value": sec["value"], "ms_per_step": sec["ms_per_step"],
             "path_roofline_frac": sec["path_roofline_frac"], "roofline": sec["roofline"],
-            "stage_ms_serialised": sec["stage_ms"], "e2e": sec["e2e"], "plan": sec["desc"]}
+            "stage_ms_serialised": sec["stage_ms"],
+            "pass_ms_per_launch_serialised": sec["pass_ms_per_launch"],
+            "e2e": sec["e2e"], "plan": sec["desc"]}
     print(json.dumps(line), flush=True)
 
 

@@ -12,6 +12,7 @@ and importing it fails loudly when the library has not been built.
 
 The functions carry the C names: ``cat_plan_create``, ``cat_forward``,
 ``cat_forward_zstar``, ``cat_forward_host``, ``cat_plan_sync``,
+``cat_plan_timing``, ``cat_plan_stage_times``, ``cat_plan_pass_times``,
 ``cat_plan_describe``, ``cat_plan_set_stream``, ``cat_plan_destroy`` and
 ``cat_status_string``.  ``Plan`` wraps them for convenience.
 """
@@ -47,6 +48,8 @@ SIGNATURES = {
     "cat_plan_timing": (_I, [_P, _I]),
     "cat_plan_stage_times": (_I, [_P, ctypes.POINTER(ctypes.c_float), _I,
                                   ctypes.POINTER(_I)]),
+    "cat_plan_pass_times": (_I, [_P, ctypes.POINTER(ctypes.c_float), _I,
+                                 ctypes.POINTER(_I)]),
     "cat_forward_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "cat_status_string": (ctypes.c_char_p, [_I]),
 }
@@ -177,6 +180,14 @@ def cat_plan_stage_times(plan):
     return [float(v) for v in ms], n.value
 
 
+def cat_plan_pass_times(plan):
+    """(ms of passes A, B, C summed over recorded chunks, launches of each)."""
+    ms = (ctypes.c_float * 3)()
+    n = ctypes.c_int(0)
+    _check(lib().cat_plan_pass_times(plan, ms, 3, ctypes.byref(n)), "cat_plan_pass_times")
+    return [float(v) for v in ms], n.value
+
+
 def cat_plan_describe(plan):
     buf = ctypes.create_string_buffer(512)
     _check(lib().cat_plan_describe(plan, buf, 512), "cat_plan_describe")
@@ -236,6 +247,9 @@ class Plan:
     def stage_times(self):
         return cat_plan_stage_times(self.handle)
 
+    def pass_times(self):
+        return cat_plan_pass_times(self.handle)
+
     def close(self):
         if self.handle:
             cat_plan_destroy(self.handle)
@@ -257,6 +271,6 @@ class Plan:
 __all__ = ["CatError", "Plan", "lib", "dtype_code", "cat_plan_create", "cat_plan_destroy",
            "cat_plan_set_stream", "cat_forward", "cat_forward_zstar", "cat_forward_host",
            "cat_plan_sync", "cat_plan_describe", "cat_plan_timing", "cat_plan_stage_times",
-           "cat_forward_noalloc",
+           "cat_plan_pass_times", "cat_forward_noalloc",
            "cat_status_string", "CAT_F32", "CAT_BF16",
            "SIGNATURES", "LIB_PATH"]

@@ -117,7 +117,7 @@ bool split_fourstep(int N, int* N1, int* N2) {
 
 void free_events(cat_plan_s* p) {
   if (p->ev) {
-    for (int i = 0; i < 4 * p->timing_cap; ++i)
+    for (int i = 0; i < p->ev_per_call * p->timing_cap; ++i)
       if (p->ev[i]) cudaEventDestroy(p->ev[i]);
     delete[] p->ev;
   }
@@ -534,7 +534,7 @@ int cat_forward(cat_plan_t p, const void* X, const void* WA, const void* V, void
   if (ranges_overlap(O, nx, X, nx) || ranges_overlap(O, nx, WA, nw) || ranges_overlap(O, nx, V, nx))
     return CAT_ERR_ALIAS;
   cudaEvent_t* ev = nullptr;
-  if (p->timing_n < p->timing_cap) ev = p->ev + 4 * p->timing_n++;
+  if (p->timing_n < p->timing_cap) ev = p->ev + (size_t)p->ev_per_call * p->timing_n++;
   if (!ev && p->path == cat::PATH_FAST) {
     if (p->use_graph) {
       const cudaError_t e = launch_fast_graph(p, X, WA, V, O);
@@ -556,10 +556,14 @@ int cat_forward(cat_plan_t p, const void* X, const void* WA, const void* V, void
                                   : cat::launch_softmax(p);
   if (e != cudaSuccess) return CAT_ERR_CUDA;
   if (ev) cudaEventRecord(ev[2], p->stream);
-  e = p->path == cat::PATH_SMEM       ? cat::launch_conv_smem(p, V, O)
-      : p->path == cat::PATH_FOURSTEP ? cat::launch_fourstep_conv(p, V, O)
-                                      : cat::launch_fast_conv(p, V, O);
-  if (ev) cudaEventRecord(ev[3], p->stream);
+  if (p->path == cat::PATH_FAST) {
+    // Events after each pass of each chunk; the last one closes the stage.
+    e = cat::launch_fast_conv(p, V, O, ev ? ev + 3 : nullptr);
+  } else {
+    e = p->path == cat::PATH_SMEM ? cat::launch_conv_smem(p, V, O)
+                                  : cat::launch_fourstep_conv(p, V, O);
+    if (ev) cudaEventRecord(ev[3], p->stream);
+  }
   return map_cuda(e);
 }
 
@@ -626,10 +630,12 @@ int cat_plan_timing(cat_plan_t p, int max_calls) {
   if (cudaStreamSynchronize(p->stream) != cudaSuccess) return CAT_ERR_CUDA;
   free_events(p);
   if (max_calls == 0) return CAT_OK;
-  p->ev = new (std::nothrow) cudaEvent_t[4 * (size_t)max_calls]();
+  p->ev_per_call = p->path == cat::PATH_FAST ? 3 + 3 * cat::fast_chunks(p) : 4;
+  const size_t n = (size_t)p->ev_per_call * max_calls;
+  p->ev = new (std::nothrow) cudaEvent_t[n]();
   if (!p->ev) return CAT_ERR_ALLOC;
   p->timing_cap = max_calls;
-  for (int i = 0; i < 4 * max_calls; ++i) {
+  for (size_t i = 0; i < n; ++i) {
     if (cudaEventCreate(&p->ev[i]) != cudaSuccess) {
       free_events(p);
       return CAT_ERR_CUDA;
@@ -643,14 +649,35 @@ int cat_plan_stage_times(cat_plan_t p, float* ms, int cap, int* ncalls) {
   if (cudaStreamSynchronize(p->stream) != cudaSuccess) return CAT_ERR_CUDA;
   ms[0] = ms[1] = ms[2] = 0.f;
   for (int c = 0; c < p->timing_n; ++c) {
-    cudaEvent_t* ev = p->ev + 4 * c;
+    cudaEvent_t* ev = p->ev + (size_t)p->ev_per_call * c;
+    const int b[4] = {0, 1, 2, p->ev_per_call - 1};
     for (int s = 0; s < 3; ++s) {
       float t = 0.f;
-      if (cudaEventElapsedTime(&t, ev[s], ev[s + 1]) != cudaSuccess) return CAT_ERR_CUDA;
+      if (cudaEventElapsedTime(&t, ev[b[s]], ev[b[s + 1]]) != cudaSuccess) return CAT_ERR_CUDA;
       ms[s] += t;
     }
   }
   if (ncalls) *ncalls = p->timing_n;
+  return CAT_OK;
+}
+
+int cat_plan_pass_times(cat_plan_t p, float* ms, int cap, int* launches) {
+  if (!p || !ms || cap < 3) return CAT_ERR_INVALID_ARG;
+  if (p->path != cat::PATH_FAST) return CAT_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(p->stream) != cudaSuccess) return CAT_ERR_CUDA;
+  ms[0] = ms[1] = ms[2] = 0.f;
+  const int chunks = (p->ev_per_call - 3) / 3;
+  for (int c = 0; c < p->timing_n; ++c) {
+    cudaEvent_t* ev = p->ev + (size_t)p->ev_per_call * c;
+    for (int k = 0; k < chunks; ++k)
+      for (int s = 0; s < 3; ++s) {
+        float t = 0.f;
+        if (cudaEventElapsedTime(&t, ev[2 + 3 * k + s], ev[3 + 3 * k + s]) != cudaSuccess)
+          return CAT_ERR_CUDA;
+        ms[s] += t;
+      }
+  }
+  if (launches) *launches = p->timing_n * chunks;
   return CAT_OK;
 }
 

@@ -85,6 +85,7 @@ struct cat_plan_s {
   // after softmax/spectrum, after the circulant product)
   cudaEvent_t* ev;
   int timing_cap, timing_n;
+  int ev_per_call;          // events recorded per call (3 + conv pass boundaries)
   int launches;             // kernel launches per cat_forward
   char desc[512];
 };
@@ -142,14 +143,20 @@ cudaError_t launch_softmax(const cat_plan_s* p, const Span& sp = Span{}, bool fi
 cudaError_t launch_softmax_spectrum(const cat_plan_s* p);
 cudaError_t launch_conv_smem(const cat_plan_s* p, const void* V, void* O);
 cudaError_t launch_fourstep_conv(const cat_plan_s* p, const void* V, void* O);
-cudaError_t launch_fast_conv(const cat_plan_s* p, const void* V, void* O);
+// Serialised fast-path circulant product; if ev is given, an event is
+// recorded on the plan's stream after each pass (3 per chunk).
+cudaError_t launch_fast_conv(const cat_plan_s* p, const void* V, void* O,
+                             cudaEvent_t* ev = nullptr);
+// Chunks of the fast path (launches of each of passes A, B, C per forward).
+int fast_chunks(const cat_plan_s* p);
 // Fast path pieces for the overlapped schedule: the spectrum of z* for
 // (b, h) rows [row0, row0 + nrows), and passes A, B, C of one chunk of rows
 // [bh0, bh0 + nb) with scratch buffer `slot`, all on stream st.  If
 // before_b is given, pass B (the first to read the spectrum) waits for it.
 cudaError_t launch_fast_zspec(const cat_plan_s* p, int row0, int nrows, cudaStream_t st);
 cudaError_t launch_fast_chunk(const cat_plan_s* p, const void* V, void* O, int bh0, int nb,
-                              int slot, cudaStream_t st, cudaEvent_t before_b = nullptr);
+                              int slot, cudaStream_t st, cudaEvent_t before_b = nullptr,
+                              cudaEvent_t* after = nullptr);
 
 // Shape validation and shared-memory-path configuration without allocation.
 int validate(int B, int N, int D, int H, int dtype);

@@ -797,7 +797,8 @@ cudaError_t launch_fast_zspec(const cat_plan_s* p, int row0, int nrows, cudaStre
 
 template <typename T>
 static cudaError_t chunk_t(const cat_plan_s* p, const T* V, T* O, int bh0, int nb, int slot,
-                           cudaStream_t st, const CUtensorMap* tmV, cudaEvent_t before_b) {
+                           cudaStream_t st, const CUtensorMap* tmV, cudaEvent_t before_b,
+                           cudaEvent_t* after) {
   const int N2 = p->fs.N2;
   float2* scr = p->scratch + (size_t)slot * (p->scratch_bytes / 2 / sizeof(float2));
   auto ac = [&](bool pass_a) {
@@ -825,48 +826,50 @@ static cudaError_t chunk_t(const cat_plan_s* p, const T* V, T* O, int bh0, int n
     }
   };
   ac(true);
+  if (after) cudaEventRecord(after[0], st);
   if (before_b) {
     const cudaError_t e = cudaStreamWaitEvent(st, before_b, 0);
     if (e != cudaSuccess) return e;
   }
   fsf_pass_b<<<nb * N2 * (kFastPairs / kBPairs), kBPairs * 16, kSmemB, st>>>(scr, p->zf, p->tabs,
                                                                              N2, bh0);
+  if (after) cudaEventRecord(after[1], st);
   ac(false);
+  if (after) cudaEventRecord(after[2], st);
   return cudaGetLastError();
 }
 
 cudaError_t launch_fast_chunk(const cat_plan_s* p, const void* V, void* O, int bh0, int nb,
-                              int slot, cudaStream_t st, cudaEvent_t before_b) {
+                              int slot, cudaStream_t st, cudaEvent_t before_b,
+                              cudaEvent_t* after) {
   CUtensorMap tmV;
   if (p->dtype == 1) {
     if (p->fs.N2 == 32 && !encode_v_map(p, (const __nv_bfloat16*)V, &tmV))
       return cudaErrorInvalidValue;
     return chunk_t(p, (const __nv_bfloat16*)V, (__nv_bfloat16*)O, bh0, nb, slot, st, &tmV,
-                   before_b);
+                   before_b, after);
   }
   if (p->fs.N2 == 32 && !encode_v_map(p, (const float*)V, &tmV)) return cudaErrorInvalidValue;
-  return chunk_t(p, (const float*)V, (float*)O, bh0, nb, slot, st, &tmV, before_b);
+  return chunk_t(p, (const float*)V, (float*)O, bh0, nb, slot, st, &tmV, before_b, after);
+}
+
+int fast_chunks(const cat_plan_s* p) {
+  const int rows = p->B * p->H;
+  return (rows + p->fs.chunk_bh - 1) / p->fs.chunk_bh;
 }
 
 // Serialised fast path on the plan's stream (used when stage timing is on;
 // the spectrum of z* is already in place): every chunk in turn on scratch
 // slot 0.
-template <typename T>
-static cudaError_t run_t(const cat_plan_s* p, const T* V, T* O) {
+cudaError_t launch_fast_conv(const cat_plan_s* p, const void* V, void* O, cudaEvent_t* ev) {
   const int rows = p->B * p->H;
-  cudaError_t e = cudaSuccess;
-  for (int bh0 = 0; bh0 < rows; bh0 += p->fs.chunk_bh) {
+  for (int bh0 = 0, c = 0; bh0 < rows; bh0 += p->fs.chunk_bh, ++c) {
     const int nb = rows - bh0 < p->fs.chunk_bh ? rows - bh0 : p->fs.chunk_bh;
-    e = launch_fast_chunk(p, V, O, bh0, nb, 0, p->stream);
+    const cudaError_t e =
+        launch_fast_chunk(p, V, O, bh0, nb, 0, p->stream, nullptr, ev ? ev + 3 * c : nullptr);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
-}
-
-cudaError_t launch_fast_conv(const cat_plan_s* p, const void* V, void* O) {
-  if (p->B == 0) return cudaSuccess;
-  if (p->dtype == 1) return run_t(p, (const __nv_bfloat16*)V, (__nv_bfloat16*)O);
-  return run_t(p, (const float*)V, (float*)O);
 }
 
 }  // namespace cat

@@ -143,13 +143,15 @@ int cat_plan_describe(cat_plan_t plan, char *buf, int len);
 /*
  * cat_plan_timing — stage timing for profiling.  max_calls > 0 arms the plan
  * to record CUDA events around its three stages (score; softmax and, on the
- * shared-memory path, the spectrum of z*; the circulant product, which on
- * the long-sequence paths includes the spectrum of z*) on its stream for the
- * next max_calls cat_forward calls, discarding earlier records; max_calls = 0
- * turns recording off.  While recording, a forward runs its stages one after
- * another on the plan's stream (the fast long-sequence path otherwise
- * overlaps batches or heads on two internal streams), so each stage's time
- * is its own.  Synchronises the plan's stream.  The plan owns the events.
+ * shared-memory and fast paths, the spectrum of z*; the circulant product,
+ * which on the general long-sequence path includes the spectrum of z*) on
+ * its stream for the next max_calls cat_forward calls, discarding earlier
+ * records; max_calls = 0 turns recording off.  On the fast path an event is
+ * also recorded after each of passes A, B and C of every chunk.  While
+ * recording, a forward runs its kernels one after another on the plan's
+ * stream (the fast path otherwise replays a graph that overlaps chunks on
+ * two internal streams), so each stage's and each pass's time is its own.
+ * Synchronises the plan's stream.  The plan owns the events.
  * Errors: CAT_ERR_INVALID_ARG, CAT_ERR_ALLOC, CAT_ERR_CUDA.
  */
 int cat_plan_timing(cat_plan_t plan, int max_calls);
@@ -161,6 +163,17 @@ int cat_plan_timing(cat_plan_t plan, int max_calls);
  * many calls that was.  Errors: CAT_ERR_INVALID_ARG, CAT_ERR_CUDA.
  */
 int cat_plan_stage_times(cat_plan_t plan, float *ms, int cap, int *ncalls);
+
+/*
+ * cat_plan_pass_times — fast path only: wait for the plan's stream and write
+ * into ms[0..2] (host array, cap >= 3) the milliseconds that passes A, B and
+ * C took, each summed over all chunks of the calls recorded since
+ * cat_plan_timing; *launches (may be NULL) receives how many launches of
+ * each pass that was (chunks per call times calls), so ms[i] / *launches is
+ * one launch's average duration.  Errors: CAT_ERR_INVALID_ARG (no plan, cap
+ * < 3, or not the fast path), CAT_ERR_CUDA.
+ */
+int cat_plan_pass_times(cat_plan_t plan, float *ms, int cap, int *launches);
 
 /* Limits of cat_forward_noalloc's fixed device workspace. */
 #define CAT_NOALLOC_MAX_ROWS (1 << 18) /* B·H·N                                 */

@@ -88,6 +88,9 @@ def test_null_plan_calls(lib):
     assert lib.cat_plan_set_stream(None, None) == cat.CAT_ERR_INVALID_ARG
     buf = ctypes.create_string_buffer(16)
     assert lib.cat_plan_describe(None, buf, 16) == cat.CAT_ERR_INVALID_ARG
+    ms = (ctypes.c_float * 3)()
+    assert lib.cat_plan_stage_times(None, ms, 3, None) == cat.CAT_ERR_INVALID_ARG
+    assert lib.cat_plan_pass_times(None, ms, 3, None) == cat.CAT_ERR_INVALID_ARG
 
 
 def test_python_raises_caterror(lib):

@@ -358,3 +358,24 @@ def test_repeated_forwards_are_bit_identical(monkeypatch, fork):
             p.forward(X, WA, V, O)
             p.sync()
             assert torch.equal(O, first)
+
+
+def test_pass_times_cover_the_circulant_product():
+    """With timing armed, the fast path records an event after each pass of
+    each chunk: one launch of each pass per chunk and call, and the three
+    passes' times add up to the circulant-product stage."""
+    B, N, D, H = 2, 16384, 256, 4
+    X, WA, V = to_dev(*synth.make_inputs(B, N, D, H, "bf16", seed=71))
+    with cat.Plan(B, N, D, H, "bf16") as p:
+        desc = p.describe()
+        chunks = -(-B * H // int(desc.split("chunk_bh=")[1].split()[0]))
+        p.timing(3)
+        for _ in range(3):
+            p.forward(X, WA, V)
+        stage, calls = p.stage_times()
+        passes, launches = p.pass_times()
+        p.timing(0)
+    assert calls == 3 and launches == 3 * chunks
+    assert all(t > 0 for t in stage) and all(t > 0 for t in passes)
+    assert sum(passes) <= stage[2] * 1.001 + 1e-3
+    assert sum(passes) >= 0.5 * stage[2]
