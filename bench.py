@@ -45,7 +45,11 @@ FALLBACK_HBM_GBS = 6800.0
 # fast path), from the committed ncu launch list of the same kernel sources
 # (profiles/).  Keyed by (workload, hash of the kernel sources): any change
 # to those sources makes the figure stale, and the bench then reports null.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # profiles/launches_long16k.md: fsf_pass_b, 16 launches, DRAM read + write
+    # per launch (cold: ncu flushes L2 before each launch).
+    ("long16k", "bffb773dccfe"): 34781008,
+}
 KERNEL_SOURCES = ["fourstep_fast.cu", "fft_reg.cuh", "fft_device.cuh", "bulk.cuh", "elem.cuh"]
 # Pass B's transforms: per (pair, k2) signal one forward and one inverse DFT
 # of length N1 = 512, counted as 5·N1·log2(N1) flops each.
