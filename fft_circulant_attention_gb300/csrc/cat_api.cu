@@ -200,23 +200,7 @@ int choose_path(cat_plan_s* p) {
       return CAT_OK;
     }
   }
-  if (N <= kSmemMaxN && !force_fs) {
-    p->path = cat::PATH_SMEM;
-    if (!make_radix_plan(N, &p->rpN)) return CAT_ERR_UNSUPPORTED_N;
-    cat::SmemCfg& s = p->sm;
-    size_t per = (size_t)N * sizeof(float2);
-    int gmax = (int)(kConvSmemBudget / per);
-    split_pairs(p->npair, gmax, &s.G, &s.groups);
-    s.tstride = N;
-    s.smem = (size_t)s.G * s.tstride * sizeof(float2);
-    s.threads = fft_threads(s.G, N);
-    s.spec_threads = fft_threads(1, N);
-    s.spec_smem = per;
-    if ((long)s.G * N > (long)cat::vals_capacity(p->rpN) * s.threads) return CAT_ERR_UNSUPPORTED_N;
-    if ((long)N > (long)cat::vals_capacity(p->rpN) * s.spec_threads) return CAT_ERR_UNSUPPORTED_N;
-    p->launches = score_launches(p->H, p->D) + 2;
-    return CAT_OK;
-  }
+  if (N <= kSmemMaxN && !force_fs) return cat::configure_smem_path(p);
   p->path = cat::PATH_FOURSTEP;
   cat::FourStepCfg& f = p->fs;
   if (!split_fourstep(N, &f.N1, &f.N2)) return CAT_ERR_UNSUPPORTED_N;
@@ -268,9 +252,9 @@ void describe(cat_plan_s* p) {
   if (p->path == cat::PATH_SMEM) {
     radstr(p->rpN, rad, sizeof(rad));
     std::snprintf(p->desc, sizeof(p->desc),
-                  "path=smem N=%d radices=%s G=%d groups=%d threads=%d smem=%zu "
+                  "path=smem N=%d radices=%s reg_m=%d G=%d groups=%d threads=%d smem=%zu "
                   "spec_threads=%d workspace=%zu launches=%d",
-                  p->N, rad, p->sm.G, p->sm.groups, p->sm.threads, p->sm.smem,
+                  p->N, rad, p->sm.reg_m, p->sm.G, p->sm.groups, p->sm.threads, p->sm.smem,
                   p->sm.spec_threads, p->workspace_bytes, p->launches);
   } else if (p->path == cat::PATH_FAST) {
     std::snprintf(p->desc, sizeof(p->desc),
@@ -326,6 +310,20 @@ int configure_smem_path(cat_plan_s* p) {
   s.spec_smem = per;
   if ((long)s.G * N > (long)cat::vals_capacity(p->rpN) * s.threads) return CAT_ERR_UNSUPPORTED_N;
   if ((long)N > (long)cat::vals_capacity(p->rpN) * s.spec_threads) return CAT_ERR_UNSUPPORTED_N;
+  // Square lengths with a register transform of the side take the two-step
+  // register kernel for the circulant product (CAT_SMEM_REG=0: block FFT).
+  s.reg_m = 0;
+  const char* env = std::getenv("CAT_SMEM_REG");
+  if (!(env && std::strcmp(env, "0") == 0)) {
+    for (int m : {8, 14, 16, 32})
+      if (m * m == N) s.reg_m = m;
+  }
+  if (s.reg_m) {
+    s.G = cat::conv_reg_pairs(s.reg_m);
+    s.groups = (p->npair + s.G - 1) / s.G;
+    s.smem = cat::conv_reg_smem(s.reg_m, s.G);
+    s.threads = s.reg_m * s.G;
+  }
   p->launches = score_launches(p->H, p->D) + 2;
   return CAT_OK;
 }

@@ -20,6 +20,7 @@ struct SmemCfg {
   size_t smem;       // dynamic shared memory of the conv kernel (bytes)
   int spec_threads;  // CTA size of the softmax+spectrum kernel
   size_t spec_smem;
+  int reg_m;         // N = reg_m² transformed in registers (conv_reg), else 0
 };
 
 // Four-step decomposition N = N1·N2 with row n = n1 + N1·n2 and bin
@@ -142,6 +143,11 @@ cudaError_t launch_score(const cat_plan_s* p, const void* X, const void* WA,
 cudaError_t launch_softmax(const cat_plan_s* p, const Span& sp = Span{}, bool finish = true);
 cudaError_t launch_softmax_spectrum(const cat_plan_s* p);
 cudaError_t launch_conv_smem(const cat_plan_s* p, const void* V, void* O);
+// Register two-step circulant product for N = M² (M in {8, 14, 16, 32}).
+cudaError_t setup_conv_reg(const cat_plan_s* p);
+cudaError_t launch_conv_reg(const cat_plan_s* p, const void* V, void* O);
+int conv_reg_pairs(int M);
+size_t conv_reg_smem(int M, int P);
 cudaError_t launch_fourstep_conv(const cat_plan_s* p, const void* V, void* O);
 // Serialised fast-path circulant product; if ev is given, an event is
 // recorded on the plan's stream after each pass (3 per chunk).

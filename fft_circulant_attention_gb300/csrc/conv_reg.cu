@@ -1,0 +1,147 @@
+// Circulant product for square lengths N = M·M (M in {8, 14, 16, 32}, i.e.
+// N = 64, 196, 256, 1024) with the whole transform in registers and one
+// shared-memory exchange per direction — the "FFT acceleration" design of
+// the notes page "CAT: Circular-Convolutional Attention for Sub-Quadratic
+// Transformers" (section 关键设计):
+//     O_h[:, c] = IFFT( FFT(z*_h) ⊙ FFT(V_h[:, c]) ),
+// for value column pairs packed as complex signals (see conv_smem.cu).
+//
+// With n = n1 + M·n2 and k = k2 + M·k1:
+//     FFT(v)[k2 + M k1] = sum_n1 w_M^{n1 k1} · w_N^{n1 k2} · sum_n2 w_M^{n2 k2} v[n1 + M n2].
+// A CTA owns P pairs of one (b, h); thread (i, p) (p fastest) is pair p and
+//   step 1: n1 = i — loads its M rows n1 + M·n2, DFT over n2, twiddle
+//           w_N^{n1·k2}, stores [k2][n1][p];
+//   step 2: k2 = i — DFT over n1 (bins k2 + M·k1), product with FFT(z*)/N,
+//           inverse DFT over k1, conjugate twiddle, stores back in place;
+//   step 3: n1 = i — inverse DFT over k2, stores the output rows.
+// Every shared-memory access has the pair index fastest, so it is free of
+// bank conflicts; the twiddles w_N^{n1·k2} sit in shared memory.
+#include <cuda_bf16.h>
+
+#include "cat_internal.h"
+#include "elem.cuh"
+#include "fft_reg.cuh"
+
+namespace cat {
+
+// A column pair (c, c+1), or the lone last column of an odd head width
+// (imaginary part zero).  Pairs at odd columns (odd head width, odd head)
+// move element by element.
+template <typename T>
+__device__ __forceinline__ float2 ld_col_pair(const T* p, bool pair, bool aligned) {
+  if (pair && aligned) return ld_pair(p);
+  return make_float2(ld_elem(p), pair ? ld_elem(p + 1) : 0.f);
+}
+
+template <typename T>
+__device__ __forceinline__ void st_col_pair(T* p, float2 v, bool pair, bool aligned) {
+  if (pair && aligned) {
+    st_pair(p, v);
+  } else {
+    st_elem(p, v.x);
+    if (pair) st_elem(p + 1, v.y);
+  }
+}
+
+template <typename T, int M>
+__global__ void __launch_bounds__(512)
+conv_reg_kernel(const T* __restrict__ V, T* __restrict__ O, const float2* __restrict__ zf,
+                const float2* __restrict__ W, int D, int H, int dh, int npair, int P,
+                int groups) {
+  constexpr int N = M * M;
+  extern __shared__ float4 smem4[];
+  float2* buf = reinterpret_cast<float2*>(smem4);   // [M][M][P]
+  float2* tw = buf + N * P;                          // tw[n1·M + k2] = w_N^{n1·k2}
+  const int bh = blockIdx.x / groups, grp = blockIdx.x - (blockIdx.x / groups) * groups;
+  const int b = bh / H, h = bh - b * H;
+  const int p = threadIdx.x % P, i = threadIdx.x / P;
+  for (int e = threadIdx.x; e < N; e += blockDim.x) tw[e] = __ldg(&W[(e / M) * (e % M)]);
+
+  const int g = grp * P + p;
+  const bool active = g < npair;
+  const bool pair = 2 * g + 1 < dh;
+  const int col = h * dh + 2 * (active ? g : 0);
+  // Pair accesses need the pair's first element at an even offset in every
+  // row: an even column and an even row length.
+  const bool aligned = (col & 1) == 0 && (D & 1) == 0;
+  const size_t base = (size_t)b * N * D + col;
+
+  float2 a[M];
+#pragma unroll
+  for (int n2 = 0; n2 < M; ++n2)
+    a[n2] = active ? ld_col_pair(V + base + (size_t)(i + M * n2) * D, pair, aligned)
+                   : make_float2(0.f, 0.f);
+  dft<M, false>(a);
+  __syncthreads();   // twiddle table ready
+#pragma unroll
+  for (int k2 = 0; k2 < M; ++k2) buf[(k2 * M + i) * P + p] = cmul(a[k2], tw[i * M + k2]);
+  __syncthreads();
+
+  // Step 2: k2 = i.  Each thread reads and rewrites only its own M slots.
+#pragma unroll
+  for (int n1 = 0; n1 < M; ++n1) a[n1] = buf[(i * M + n1) * P + p];
+  dft<M, false>(a);
+  const float2* zr = zf + (size_t)bh * N + i;
+#pragma unroll
+  for (int k1 = 0; k1 < M; ++k1) a[k1] = cmul(a[k1], __ldg(zr + M * k1));
+  dft<M, true>(a);
+#pragma unroll
+  for (int n1 = 0; n1 < M; ++n1) buf[(i * M + n1) * P + p] = cmulc(a[n1], tw[n1 * M + i]);
+  __syncthreads();
+
+  // Step 3: n1 = i.
+#pragma unroll
+  for (int k2 = 0; k2 < M; ++k2) a[k2] = buf[(k2 * M + i) * P + p];
+  dft<M, true>(a);
+  if (active) {
+#pragma unroll
+    for (int n2 = 0; n2 < M; ++n2)
+      st_col_pair(O + base + (size_t)(i + M * n2) * D, a[n2], pair, aligned);
+  }
+}
+
+// Pairs per CTA and the CTA shape for side M: 16 pairs (8 for M = 32, so
+// that a CTA of 256 threads and 74 KB of shared memory leaves room for more).
+int conv_reg_pairs(int M) { return M == 32 ? 8 : 16; }
+
+size_t conv_reg_smem(int M, int P) { return (size_t)M * M * (P + 1) * sizeof(float2); }
+
+template <typename T>
+static cudaError_t setup_t() {
+  cudaError_t e = allow_max_smem(conv_reg_kernel<T, 8>);
+  if (e == cudaSuccess) e = allow_max_smem(conv_reg_kernel<T, 14>);
+  if (e == cudaSuccess) e = allow_max_smem(conv_reg_kernel<T, 16>);
+  if (e == cudaSuccess) e = allow_max_smem(conv_reg_kernel<T, 32>);
+  return e;
+}
+
+cudaError_t setup_conv_reg(const cat_plan_s* p) {
+  return p->dtype == 1 ? setup_t<__nv_bfloat16>() : setup_t<float>();
+}
+
+template <typename T>
+static cudaError_t launch_t(const cat_plan_s* p, const T* V, T* O) {
+  const int M = p->sm.reg_m, P = p->sm.G, groups = p->sm.groups;
+  const int ctas = p->B * p->H * groups;
+  const dim3 block(M * P);
+  const size_t smem = p->sm.smem;
+  switch (M) {
+#define CAT_M(m)                                                                           \
+  case m:                                                                                  \
+    conv_reg_kernel<T, m><<<ctas, block, smem, p->stream>>>(V, O, p->zf, p->tw, p->D, p->H, \
+                                                            p->dh, p->npair, P, groups);   \
+    break;
+    CAT_M(8) CAT_M(14) CAT_M(16) CAT_M(32)
+#undef CAT_M
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_conv_reg(const cat_plan_s* p, const void* V, void* O) {
+  if (p->B == 0) return cudaSuccess;
+  if (p->dtype == 1) return launch_t(p, (const __nv_bfloat16*)V, (__nv_bfloat16*)O);
+  return launch_t(p, (const float*)V, (float*)O);
+}
+
+}  // namespace cat

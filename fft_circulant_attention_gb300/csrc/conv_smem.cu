@@ -38,7 +38,9 @@ conv_smem_kernel(const T* __restrict__ V, T* __restrict__ O, const float2* __res
   }
   const int col0 = h * dh + 2 * g0;                 // first column of this CTA
   const bool full_pairs = (2 * (g0 + gc) <= dh);    // no half pair at the end
-  const bool aligned = ((col0 & 1) == 0);           // pair loads 2·sizeof(T)-aligned
+  // Pair loads need 2·sizeof(T) alignment in every row: an even column and
+  // an even row length.
+  const bool aligned = ((col0 & 1) == 0) && ((D & 1) == 0);
   const T* Vb = V + (size_t)b * N * D;
   T* Ob = O + (size_t)b * N * D;
 
@@ -83,11 +85,13 @@ conv_smem_kernel(const T* __restrict__ V, T* __restrict__ O, const float2* __res
 }
 
 cudaError_t setup_smem_kernels(const cat_plan_s* p) {
+  if (p->sm.reg_m) return setup_conv_reg(p);
   if (p->dtype == 1) return allow_max_smem(conv_smem_kernel<__nv_bfloat16>);
   return allow_max_smem(conv_smem_kernel<float>);
 }
 
 cudaError_t launch_conv_smem(const cat_plan_s* p, const void* V, void* O) {
+  if (p->sm.reg_m) return launch_conv_reg(p, V, O);
   const int ctas = p->B * p->H * p->sm.groups;
   if (ctas == 0) return cudaSuccess;
   if (p->dtype == 1)

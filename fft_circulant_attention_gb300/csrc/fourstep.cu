@@ -54,7 +54,7 @@ fs_pass_a(const T* __restrict__ V, const float* __restrict__ zs, float2* __restr
   const int n1_0 = tile * TA;
   const int col0 = h * dh + 2 * g0;
   const bool full_pairs = (2 * (g0 + gc) <= dh);
-  const bool aligned = ((col0 & 1) == 0);
+  const bool aligned = ((col0 & 1) == 0) && ((D & 1) == 0);   // even column, even row length
   const T* Vb = V + (size_t)b * N * D;
   const float* zrow = zs + (size_t)bh * N;
 
@@ -183,7 +183,7 @@ fs_pass_c(const float2* __restrict__ scr, T* __restrict__ O, const float2* __res
   const int n1_0 = tile * TA;
   const int col0 = h * dh + 2 * g0;
   const bool full_pairs = (2 * (g0 + gc) <= dh);
-  const bool aligned = ((col0 & 1) == 0);
+  const bool aligned = ((col0 & 1) == 0) && ((D & 1) == 0);   // even column, even row length
   const float2* srow = scr + (size_t)bhl * N * P;
 
   const int total = count * N2;

@@ -379,3 +379,28 @@ def test_pass_times_cover_the_circulant_product():
     assert all(t > 0 for t in stage) and all(t > 0 for t in passes)
     assert sum(passes) <= stage[2] * 1.001 + 1e-3
     assert sum(passes) >= 0.5 * stage[2]
+
+
+@pytest.mark.parametrize("N", [64, 196, 256, 1024])
+@pytest.mark.parametrize("B,D,H,dtype", [(3, 128, 2, "f32"), (2, 384, 6, "bf16"),
+                                         (2, 75, 5, "f32"), (1, 63, 3, "bf16")])
+def test_square_lengths_register_kernel(monkeypatch, N, B, D, H, dtype):
+    """Square lengths N = M² (M = 8, 14, 16, 32) take the two-step register
+    kernel for the circulant product.  Odd head widths (15, 21) put pairs at
+    odd columns and a lone last column in every head.  Checked against the
+    oracle, and against the block-FFT kernel the lengths otherwise take."""
+    with cat.Plan(B, N, D, H, dtype) as p:
+        assert "reg_m=%d" % int(round(N ** 0.5)) in p.describe()
+    parity(B, N, D, H, dtype, seed=N + D)
+    X, WA, V = to_dev(*synth.make_inputs(B, N, D, H, dtype, seed=N + D))
+    with cat.Plan(B, N, D, H, dtype) as p:
+        O_reg = p.forward(X, WA, V)
+        p.sync()
+    monkeypatch.setenv("CAT_SMEM_REG", "0")
+    with cat.Plan(B, N, D, H, dtype) as p:
+        assert "reg_m=0" in p.describe()
+        O_blk = p.forward(X, WA, V)
+        p.sync()
+    scale = float(V.abs().max())
+    tol = (8e-3 if dtype == "bf16" else 2e-5) * scale
+    assert float((O_reg.float() - O_blk.float()).abs().max()) <= tol
