@@ -15,7 +15,8 @@
 //           inverse DFT over k1, conjugate twiddle, stores back in place;
 //   step 3: n1 = i — inverse DFT over k2, stores the output rows.
 // Every shared-memory access has the pair index fastest, so it is free of
-// bank conflicts; the twiddles w_N^{n1·k2} sit in shared memory.
+// bank conflicts; the twiddles w_N^{n1·k2} and the (b, h) row of FFT(z*)/N
+// sit in shared memory.
 #include <cuda_bf16.h>
 
 #include "cat_internal.h"
@@ -52,10 +53,14 @@ conv_reg_kernel(const T* __restrict__ V, T* __restrict__ O, const float2* __rest
   extern __shared__ float4 smem4[];
   float2* buf = reinterpret_cast<float2*>(smem4);   // [M][M][P]
   float2* tw = buf + N * P;                          // tw[n1·M + k2] = w_N^{n1·k2}
+  float2* zs = tw + N;                               // FFT(z*)/N of this (b, h)
   const int bh = blockIdx.x / groups, grp = blockIdx.x - (blockIdx.x / groups) * groups;
   const int b = bh / H, h = bh - b * H;
   const int p = threadIdx.x % P, i = threadIdx.x / P;
-  for (int e = threadIdx.x; e < N; e += blockDim.x) tw[e] = __ldg(&W[(e / M) * (e % M)]);
+  for (int e = threadIdx.x; e < N; e += blockDim.x) {
+    tw[e] = __ldg(&W[(e / M) * (e % M)]);
+    zs[e] = __ldg(&zf[(size_t)bh * N + e]);
+  }
 
   const int g = grp * P + p;
   const bool active = g < npair;
@@ -72,7 +77,7 @@ conv_reg_kernel(const T* __restrict__ V, T* __restrict__ O, const float2* __rest
     a[n2] = active ? ld_col_pair(V + base + (size_t)(i + M * n2) * D, pair, aligned)
                    : make_float2(0.f, 0.f);
   dft<M, false>(a);
-  __syncthreads();   // twiddle table ready
+  __syncthreads();   // twiddles and spectrum ready
 #pragma unroll
   for (int k2 = 0; k2 < M; ++k2) buf[(k2 * M + i) * P + p] = cmul(a[k2], tw[i * M + k2]);
   __syncthreads();
@@ -81,9 +86,8 @@ conv_reg_kernel(const T* __restrict__ V, T* __restrict__ O, const float2* __rest
 #pragma unroll
   for (int n1 = 0; n1 < M; ++n1) a[n1] = buf[(i * M + n1) * P + p];
   dft<M, false>(a);
-  const float2* zr = zf + (size_t)bh * N + i;
 #pragma unroll
-  for (int k1 = 0; k1 < M; ++k1) a[k1] = cmul(a[k1], __ldg(zr + M * k1));
+  for (int k1 = 0; k1 < M; ++k1) a[k1] = cmul(a[k1], zs[i + M * k1]);
   dft<M, true>(a);
 #pragma unroll
   for (int n1 = 0; n1 < M; ++n1) buf[(i * M + n1) * P + p] = cmulc(a[n1], tw[n1 * M + i]);
@@ -104,7 +108,7 @@ conv_reg_kernel(const T* __restrict__ V, T* __restrict__ O, const float2* __rest
 // that a CTA of 256 threads and 74 KB of shared memory leaves room for more).
 int conv_reg_pairs(int M) { return M == 32 ? 8 : 16; }
 
-size_t conv_reg_smem(int M, int P) { return (size_t)M * M * (P + 1) * sizeof(float2); }
+size_t conv_reg_smem(int M, int P) { return (size_t)M * M * (P + 2) * sizeof(float2); }
 
 template <typename T>
 static cudaError_t setup_t() {

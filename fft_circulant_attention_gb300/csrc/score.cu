@@ -64,6 +64,30 @@ __device__ __forceinline__ void two_sum_acc(float& hi, float& lo, float p) {
   lo += err;
 }
 
+// W_A's columns [h0, h0 + HT) as fp32 [D][HP] in shared memory (columns HT
+// to HP zero).  Eight loads per thread are in flight before any is stored,
+// so the staging costs a few latencies rather than D·HP / blockDim of them.
+template <typename T>
+__device__ __forceinline__ void stage_w_f32(float* ws, const T* __restrict__ WA, int D, int H,
+                                            int h0, int HT, int HP) {
+  constexpr int kBatch = 8;
+  const int total = D * HP;
+  for (int i0 = threadIdx.x; i0 < total; i0 += kBatch * blockDim.x) {
+    float v[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int i = i0 + j * blockDim.x;
+      const int d = i / HP, h = i - d * HP;
+      v[j] = (i < total && h < HT) ? ld_elem(WA + (size_t)d * H + h0 + h) : 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int i = i0 + j * blockDim.x;
+      if (i < total) ws[i] = v[j];
+    }
+  }
+}
+
 // One pass over X computes HT heads [h0, h0 + HT) for kScoreTokPerCta
 // tokens of one batch.  W_A's HT columns sit in shared memory as fp32
 // [D][HP] (HP = HT rounded up to 4); every lane of a warp reads the same
@@ -85,10 +109,7 @@ score_kernel(const T* __restrict__ X, const T* __restrict__ WA, float2* __restri
   extern __shared__ float4 ws4[];
   float* ws = reinterpret_cast<float*>(ws4);
   const int b = b0 + blockIdx.y;
-  for (int i = threadIdx.x; i < D * HP; i += blockDim.x) {
-    int d = i / HP, h = i - d * HP;
-    ws[i] = (h < HT) ? ld_elem(WA + (size_t)d * H + h0 + h) : 0.f;
-  }
+  stage_w_f32(ws, WA, D, H, h0, HT, HP);
   __syncthreads();
   const int nbase = blockIdx.x * kScoreTokPerCta + threadIdx.x;
   int nn[TP];
@@ -153,6 +174,81 @@ score_kernel(const T* __restrict__ X, const T* __restrict__ WA, float2* __restri
       for (int h = 0; h < HT; ++h)
         z[((size_t)b * H + h0 + h) * N + nn[t]] = make_float2(hi[t][h], lo[t][h]);
     }
+  }
+}
+
+// The same score with kSplit threads per token: thread q of a token takes
+// the 16-byte vectors q, q + kSplit, q + 2·kSplit, … of the token's row, so
+// a warp reads 32/kSplit rows in contiguous kSplit·16-byte runs and a CTA
+// covers only kScoreSplitTok tokens — four times the CTAs of score_kernel.
+// Each run of kChunk products per head is summed in a fresh fp32 register
+// and added into the thread's double-float (hi, lo) by TwoSum; the kSplit
+// partial double-floats of a token are then combined by TwoSum across the
+// lanes.  Requires 16-byte vectors and D a multiple of kSplit vectors.
+constexpr int kSplit = 4;
+constexpr int kScoreSplitTok = kScoreThreads / kSplit;
+
+template <typename T, int HT>
+__global__ void __launch_bounds__(kScoreThreads)
+score_split_kernel(const T* __restrict__ X, const T* __restrict__ WA, float2* __restrict__ z,
+                   int N, int D, int H, int h0, int b0) {
+  constexpr int HP = (HT + 3) & ~3;
+  constexpr int V = Vec16<T>::n;
+  constexpr int RUN = kChunk / V;   // vectors per fresh run
+  extern __shared__ float4 ws4[];
+  float* ws = reinterpret_cast<float*>(ws4);
+  const int b = b0 + blockIdx.y;
+  stage_w_f32(ws, WA, D, H, h0, HT, HP);
+  __syncthreads();
+  const int q = threadIdx.x % kSplit;
+  const int n = blockIdx.x * kScoreSplitTok + threadIdx.x / kSplit;
+  const bool ok = n < N;
+  const T* xr = X + ((size_t)b * N + (ok ? n : 0)) * D;
+  float hi[HT], lo[HT];
+#pragma unroll
+  for (int h = 0; h < HT; ++h) hi[h] = lo[h] = 0.f;
+  const int nvec = D / V;   // vectors per row; a multiple of kSplit
+  for (int v0 = q; v0 < nvec; v0 += kSplit * RUN) {
+    float part[HT];
+#pragma unroll
+    for (int h = 0; h < HT; ++h) part[h] = 0.f;
+#pragma unroll
+    for (int r = 0; r < RUN; ++r) {
+      const int v = v0 + r * kSplit;
+      if (v < nvec) {
+        float xv[V];
+        Vec16<T>::load(xr + v * V, xv);
+#pragma unroll
+        for (int j = 0; j < V; ++j) {
+          const float4* wrow = ws4 + (size_t)(v * V + j) * (HP / 4);
+#pragma unroll
+          for (int c = 0; c < HP / 4; ++c) {
+            const float4 w = wrow[c];
+            const float wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              if (c * 4 + e < HT) part[c * 4 + e] = fmaf(xv[j], wv[e], part[c * 4 + e]);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < HT; ++h) two_sum_acc(hi[h], lo[h], part[h]);
+  }
+  // Combine the token's kSplit lanes (adjacent lanes of one warp).
+#pragma unroll
+  for (int o = 1; o < kSplit; o <<= 1) {
+#pragma unroll
+    for (int h = 0; h < HT; ++h) {
+      const float oh = __shfl_xor_sync(0xffffffffu, hi[h], o);
+      const float ol = __shfl_xor_sync(0xffffffffu, lo[h], o);
+      two_sum_acc(hi[h], lo[h], oh);
+      lo[h] += ol;
+    }
+  }
+  if (ok && q == 0) {
+#pragma unroll
+    for (int h = 0; h < HT; ++h) z[((size_t)b * H + h0 + h) * N + n] = make_float2(hi[h], lo[h]);
   }
 }
 
@@ -533,7 +629,17 @@ static cudaError_t run_score(const cat_plan_s* p, const T* X, const T* WA, int h
   constexpr int HP = (HT + 3) & ~3;
   size_t smem = (size_t)HP * p->D * sizeof(float);
   auto k = score_kernel<T, HT, VEC>;
-  if (setup) return allow_max_smem(k);
+  auto ks = score_split_kernel<T, HT>;
+  if (setup) {
+    cudaError_t e = allow_max_smem(k);
+    return (e == cudaSuccess && VEC) ? allow_max_smem(ks) : e;
+  }
+  // Rows of whole kSplit-vector groups take the split kernel.
+  if (VEC && p->D % (kSplit * Vec16<T>::n) == 0) {
+    dim3 grid((p->N + kScoreSplitTok - 1) / kScoreSplitTok, sp.nb(p));
+    ks<<<grid, kScoreThreads, smem, sp.stream(p)>>>(X, WA, p->z2, p->N, p->D, p->H, h0, sp.b0);
+    return cudaGetLastError();
+  }
   dim3 grid((p->N + kScoreTokPerCta - 1) / kScoreTokPerCta, sp.nb(p));
   k<<<grid, kScoreThreads, smem, sp.stream(p)>>>(X, WA, p->z2, p->N, p->D, p->H, h0, sp.b0);
   return cudaGetLastError();
