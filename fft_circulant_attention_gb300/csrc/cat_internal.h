@@ -146,6 +146,7 @@ cudaError_t launch_conv_smem(const cat_plan_s* p, const void* V, void* O);
 // Register two-step circulant product for N = M² (M in {8, 14, 16, 32}).
 cudaError_t setup_conv_reg(const cat_plan_s* p);
 cudaError_t launch_conv_reg(const cat_plan_s* p, const void* V, void* O);
+cudaError_t launch_softmax_spectrum_reg(const cat_plan_s* p);
 int conv_reg_pairs(int M);
 size_t conv_reg_smem(int M, int P);
 cudaError_t launch_fourstep_conv(const cat_plan_s* p, const void* V, void* O);

@@ -104,6 +104,104 @@ conv_reg_kernel(const T* __restrict__ V, T* __restrict__ O, const float2* __rest
   }
 }
 
+// Softmax and spectrum of z* for N = M² in registers: a group of GL lanes
+// (M rounded up to a power of two; lanes >= M idle) owns one (b, h) row, so
+// the row maximum and Σ exp(z - m) are lane-group shuffles.  Lane i holds
+// z[i + M·n2] (n1 = i); it writes z* there, takes the DFT over n2, the
+// twiddle w_N^{n1·k2}, and exchanges through the row's shared-memory block
+// (row stride M + 1); then lane i (k2 = i) takes the DFT over n1 and writes
+// FFT(z*)/N at the natural bins k2 + M·k1.  The exact difference z - m comes
+// from the double-float score (exp_shifted), as in the block kernel.
+constexpr int kSpecRegThreads = 256;
+
+template <int M>
+__global__ void __launch_bounds__(kSpecRegThreads)
+softmax_spectrum_reg(const float2* __restrict__ z, float* __restrict__ zs,
+                     float2* __restrict__ zf, const float2* __restrict__ W, int rows) {
+  constexpr int N = M * M;
+  constexpr int GL = M <= 8 ? 8 : (M <= 16 ? 16 : 32);
+  constexpr int ROWS = kSpecRegThreads / GL;
+  constexpr int RS = M + 1;                  // shared row of one k2 (complex)
+  extern __shared__ float4 smem4[];
+  float2* tw = reinterpret_cast<float2*>(smem4);   // tw[n1·M + k2] = w_N^{n1·k2}
+  float2* xb = tw + N;                              // ROWS blocks of M·RS
+  for (int e = threadIdx.x; e < N; e += blockDim.x) tw[e] = __ldg(&W[(e / M) * (e % M)]);
+  const int i = threadIdx.x % GL, r = threadIdx.x / GL;
+  const int row = blockIdx.x * ROWS + r;
+  const bool act = i < M && row < rows;
+  const float2* src = z + (size_t)(row < rows ? row : 0) * N;
+  float2 v[M];
+#pragma unroll
+  for (int n2 = 0; n2 < M; ++n2) v[n2] = act ? src[i + M * n2] : make_float2(-INFINITY, 0.f);
+  float m = -INFINITY;
+#pragma unroll
+  for (int n2 = 0; n2 < M; ++n2) m = fmaxf(m, v[n2].x);
+#pragma unroll
+  for (int o = GL / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  float sum = 0.f;
+  float2 a[M];
+#pragma unroll
+  for (int n2 = 0; n2 < M; ++n2) {
+    const float e = act ? exp_shifted(v[n2], m) : 0.f;
+    a[n2] = make_float2(e, 0.f);
+    sum += e;
+  }
+#pragma unroll
+  for (int o = GL / 2; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  const float inv = 1.0f / sum;
+  float* out = zs + (size_t)row * N;
+#pragma unroll
+  for (int n2 = 0; n2 < M; ++n2) {
+    a[n2].x *= inv;
+    if (act) out[i + M * n2] = a[n2].x;
+  }
+  dft<M, false>(a);
+  __syncthreads();   // twiddle table ready
+  float2* xr = xb + r * M * RS;
+  if (i < M) {
+#pragma unroll
+    for (int k2 = 0; k2 < M; ++k2) xr[k2 * RS + i] = cmul(a[k2], tw[i * M + k2]);
+  }
+  __syncwarp();      // a row's lanes are one warp's
+  if (i < M) {
+#pragma unroll
+    for (int n1 = 0; n1 < M; ++n1) a[n1] = xr[i * RS + n1];
+  }
+  dft<M, false>(a);
+  if (act) {
+    const float invN = 1.0f / (float)N;
+    float2* spec = zf + (size_t)row * N + i;
+#pragma unroll
+    for (int k1 = 0; k1 < M; ++k1) spec[M * k1] = cscale(a[k1], invN);
+  }
+}
+
+size_t spectrum_reg_smem(int M) {
+  const int GL = M <= 8 ? 8 : (M <= 16 ? 16 : 32);
+  return ((size_t)M * M + (size_t)(kSpecRegThreads / GL) * M * (M + 1)) * sizeof(float2);
+}
+
+cudaError_t launch_softmax_spectrum_reg(const cat_plan_s* p) {
+  const int rows = p->B * p->H;
+  if (rows == 0) return cudaSuccess;
+  const int M = p->sm.reg_m;
+  const int GL = M <= 8 ? 8 : (M <= 16 ? 16 : 32);
+  const int per = kSpecRegThreads / GL;
+  const int ctas = (rows + per - 1) / per;
+  const size_t smem = spectrum_reg_smem(M);
+  switch (M) {
+#define CAT_M(m)                                                                            \
+  case m:                                                                                   \
+    softmax_spectrum_reg<m><<<ctas, kSpecRegThreads, smem, p->stream>>>(p->z2, p->zs, p->zf, \
+                                                                        p->tw, rows);       \
+    break;
+    CAT_M(8) CAT_M(14) CAT_M(16) CAT_M(32)
+#undef CAT_M
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
 // Pairs per CTA and the CTA shape for side M: 16 pairs (8 for M = 32, so
 // that a CTA of 256 threads and 74 KB of shared memory leaves room for more).
 int conv_reg_pairs(int M) { return M == 32 ? 8 : 16; }
@@ -112,7 +210,11 @@ size_t conv_reg_smem(int M, int P) { return (size_t)M * M * (P + 2) * sizeof(flo
 
 template <typename T>
 static cudaError_t setup_t() {
-  cudaError_t e = allow_max_smem(conv_reg_kernel<T, 8>);
+  cudaError_t e = allow_max_smem(softmax_spectrum_reg<8>);
+  if (e == cudaSuccess) e = allow_max_smem(softmax_spectrum_reg<14>);
+  if (e == cudaSuccess) e = allow_max_smem(softmax_spectrum_reg<16>);
+  if (e == cudaSuccess) e = allow_max_smem(softmax_spectrum_reg<32>);
+  if (e == cudaSuccess) e = allow_max_smem(conv_reg_kernel<T, 8>);
   if (e == cudaSuccess) e = allow_max_smem(conv_reg_kernel<T, 14>);
   if (e == cudaSuccess) e = allow_max_smem(conv_reg_kernel<T, 16>);
   if (e == cudaSuccess) e = allow_max_smem(conv_reg_kernel<T, 32>);

@@ -838,6 +838,7 @@ cudaError_t setup_score_kernels(const cat_plan_s* p) {
 }
 
 cudaError_t launch_softmax_spectrum(const cat_plan_s* p) {
+  if (p->sm.reg_m) return launch_softmax_spectrum_reg(p);
   int rows = p->B * p->H;
   if (rows == 0) return cudaSuccess;
   softmax_spectrum_kernel<<<rows, p->sm.spec_threads, p->sm.spec_smem, p->stream>>>(
