@@ -8,7 +8,7 @@ resident in HBM; X + V + O are larger than L2, so no flush is needed
 between steps.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
-                    [--config long16k] [--no-secondary]
+                    [--config long16k] [--no-secondary] [--no-short]
 
 Prints ONE JSON line (rank 0).  With --impl reference the fp64 CPU oracle
 is timed instead, on a bounded sample of the same workload.
@@ -355,6 +355,42 @@ def measure_workload(name, steps, warmup, device, world, sampler=None):
     }
 
 
+# The short-sequence configurations of the workload table (parity cases of
+# the tests; timed here so that every path has a measured figure).
+SHORT = ["tiny", "vit196", "gpt2_f32", "gpt2_bf16"]
+
+
+def measure_short(name, device, reps=200, warmup=20):
+    """ms per forward of one short configuration (resident inputs, plan's
+    stream, CUDA events) with its whole-step roofline fraction."""
+    import fft_circulant_attention_gb300 as cat
+    c = cfg_of(name)
+    X, WA, V = (t.to(device) for t in synth.make_inputs(c["B"], c["N"], c["D"], c["H"],
+                                                         c["dtype"], seed=0))
+    O = torch.empty_like(V)
+    stream = torch.cuda.current_stream(device)
+    with cat.Plan(c["B"], c["N"], c["D"], c["H"], c["dtype"], stream=stream) as plan:
+        for _ in range(warmup):
+            plan.forward(X, WA, V, O)
+        torch.cuda.synchronize(device)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            plan.forward(X, WA, V, O)
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        desc = plan.describe()
+    ms = e0.elapsed_time(e1) / reps
+    a = algorithmic(c)
+    hbm, _ = load_peaks()
+    t_roof = max(a["total_bytes"] / (hbm * 1e9), a["total_flops"] / (FP32_PEAK_TFLOPS * 1e12))
+    return {"workload": name, "B": c["B"], "N": c["N"], "D": c["D"], "H": c["H"],
+            "storage": c["dtype"], "ms_per_step": ms,
+            "value": c["B"] * c["N"] * c["H"] / (ms * 1e-3),
+            "path_roofline_frac": t_roof / (ms * 1e-3), "plan": desc}
+
+
 def run_gb300(args, world, rank, local):
     import fft_circulant_attention_gb300 as cat
     from fft_circulant_attention_gb300 import build
@@ -367,6 +403,7 @@ def run_gb300(args, world, rank, local):
     sec = None
     if not args.no_secondary and args.config != SECONDARY:
         sec = measure_workload(SECONDARY, max(3, args.steps // 4), args.warmup, device, world)
+    short = [] if args.no_short else [measure_short(n, device) for n in SHORT]
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -412,6 +449,8 @@ def run_gb300(args, world, rank, local):
             "stage_ms_serialised": sec["stage_ms"],
             "pass_ms_per_launch_serialised": sec["pass_ms_per_launch"],
             "e2e": sec["e2e"], "plan": sec["desc"]}
+    if short:
+        line["short_configs"] = short
     print(json.dumps(line), flush=True)
 
 
@@ -424,6 +463,7 @@ def main():
     ap.add_argument("--config", default=PRIMARY, choices=sorted(synth.CONFIGS))
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-short", action="store_true")
     ap.add_argument("--sample-heads", type=int, default=0)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)

@@ -179,14 +179,16 @@ score_kernel(const T* __restrict__ X, const T* __restrict__ WA, float2* __restri
 
 // The same score with kSplit threads per token: thread q of a token takes
 // the 16-byte vectors q, q + kSplit, q + 2·kSplit, … of the token's row, so
-// a warp reads 32/kSplit rows in contiguous kSplit·16-byte runs and a CTA
-// covers only kScoreSplitTok tokens — four times the CTAs of score_kernel.
+// a warp reads rows in contiguous kSplit·16-byte runs.  Each thread serves
+// kSplitTok tokens (the W_A row it reads from shared memory feeds all of
+// them) and loads a run's vectors for all of them before the first FMA.
 // Each run of kChunk products per head is summed in a fresh fp32 register
 // and added into the thread's double-float (hi, lo) by TwoSum; the kSplit
 // partial double-floats of a token are then combined by TwoSum across the
 // lanes.  Requires 16-byte vectors and D a multiple of kSplit vectors.
 constexpr int kSplit = 4;
-constexpr int kScoreSplitTok = kScoreThreads / kSplit;
+constexpr int kSplitTok = 2;
+constexpr int kScoreSplitTok = kScoreThreads / kSplit * kSplitTok;
 
 template <typename T, int HT>
 __global__ void __launch_bounds__(kScoreThreads)
@@ -195,29 +197,46 @@ score_split_kernel(const T* __restrict__ X, const T* __restrict__ WA, float2* __
   constexpr int HP = (HT + 3) & ~3;
   constexpr int V = Vec16<T>::n;
   constexpr int RUN = kChunk / V;   // vectors per fresh run
+  constexpr int TT = kSplitTok;
   extern __shared__ float4 ws4[];
   float* ws = reinterpret_cast<float*>(ws4);
   const int b = b0 + blockIdx.y;
   stage_w_f32(ws, WA, D, H, h0, HT, HP);
   __syncthreads();
   const int q = threadIdx.x % kSplit;
-  const int n = blockIdx.x * kScoreSplitTok + threadIdx.x / kSplit;
-  const bool ok = n < N;
-  const T* xr = X + ((size_t)b * N + (ok ? n : 0)) * D;
-  float hi[HT], lo[HT];
+  const int slot = threadIdx.x / kSplit;              // 0 .. kScoreThreads/kSplit - 1
+  int n[TT];
+  bool ok[TT];
+  const T* xr[TT];
 #pragma unroll
-  for (int h = 0; h < HT; ++h) hi[h] = lo[h] = 0.f;
+  for (int t = 0; t < TT; ++t) {
+    n[t] = blockIdx.x * kScoreSplitTok + slot + t * (kScoreThreads / kSplit);
+    ok[t] = n[t] < N;
+    xr[t] = X + ((size_t)b * N + (ok[t] ? n[t] : 0)) * D;
+  }
+  float hi[TT][HT], lo[TT][HT];
+#pragma unroll
+  for (int t = 0; t < TT; ++t)
+#pragma unroll
+    for (int h = 0; h < HT; ++h) hi[t][h] = lo[t][h] = 0.f;
   const int nvec = D / V;   // vectors per row; a multiple of kSplit
   for (int v0 = q; v0 < nvec; v0 += kSplit * RUN) {
-    float part[HT];
+    float xv[TT][RUN][V];
 #pragma unroll
-    for (int h = 0; h < HT; ++h) part[h] = 0.f;
+    for (int r = 0; r < RUN; ++r) {
+      const int v = min(v0 + r * kSplit, nvec - 1);   // loads stay in the row
+#pragma unroll
+      for (int t = 0; t < TT; ++t) Vec16<T>::load(xr[t] + v * V, xv[t][r]);
+    }
+    float part[TT][HT];
+#pragma unroll
+    for (int t = 0; t < TT; ++t)
+#pragma unroll
+      for (int h = 0; h < HT; ++h) part[t][h] = 0.f;
 #pragma unroll
     for (int r = 0; r < RUN; ++r) {
       const int v = v0 + r * kSplit;
       if (v < nvec) {
-        float xv[V];
-        Vec16<T>::load(xr + v * V, xv);
 #pragma unroll
         for (int j = 0; j < V; ++j) {
           const float4* wrow = ws4 + (size_t)(v * V + j) * (HP / 4);
@@ -227,28 +246,41 @@ score_split_kernel(const T* __restrict__ X, const T* __restrict__ WA, float2* __
             const float wv[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e)
-              if (c * 4 + e < HT) part[c * 4 + e] = fmaf(xv[j], wv[e], part[c * 4 + e]);
+              if (c * 4 + e < HT) {
+#pragma unroll
+                for (int t = 0; t < TT; ++t)
+                  part[t][c * 4 + e] = fmaf(xv[t][r][j], wv[e], part[t][c * 4 + e]);
+              }
           }
         }
       }
     }
 #pragma unroll
-    for (int h = 0; h < HT; ++h) two_sum_acc(hi[h], lo[h], part[h]);
+    for (int t = 0; t < TT; ++t)
+#pragma unroll
+      for (int h = 0; h < HT; ++h) two_sum_acc(hi[t][h], lo[t][h], part[t][h]);
   }
-  // Combine the token's kSplit lanes (adjacent lanes of one warp).
+  // Combine each token's kSplit lanes (adjacent lanes of one warp).
 #pragma unroll
   for (int o = 1; o < kSplit; o <<= 1) {
 #pragma unroll
-    for (int h = 0; h < HT; ++h) {
-      const float oh = __shfl_xor_sync(0xffffffffu, hi[h], o);
-      const float ol = __shfl_xor_sync(0xffffffffu, lo[h], o);
-      two_sum_acc(hi[h], lo[h], oh);
-      lo[h] += ol;
-    }
-  }
-  if (ok && q == 0) {
+    for (int t = 0; t < TT; ++t)
 #pragma unroll
-    for (int h = 0; h < HT; ++h) z[((size_t)b * H + h0 + h) * N + n] = make_float2(hi[h], lo[h]);
+      for (int h = 0; h < HT; ++h) {
+        const float oh = __shfl_xor_sync(0xffffffffu, hi[t][h], o);
+        const float ol = __shfl_xor_sync(0xffffffffu, lo[t][h], o);
+        two_sum_acc(hi[t][h], lo[t][h], oh);
+        lo[t][h] += ol;
+      }
+  }
+  if (q == 0) {
+#pragma unroll
+    for (int t = 0; t < TT; ++t)
+      if (ok[t]) {
+#pragma unroll
+        for (int h = 0; h < HT; ++h)
+          z[((size_t)b * H + h0 + h) * N + n[t]] = make_float2(hi[t][h], lo[t][h]);
+      }
   }
 }
 
