@@ -54,30 +54,17 @@ __device__ __forceinline__ void ld_sh2(const float2* p, float2& a, float2& b) {
 }
 
 // ---------------------------------------------------------------------------
-// Pass A.  N2 == 32: a warp per n1 (8 per CTA), one thread per pair holds the
-// whole length-32 transform.  N2 > 32: a CTA per n1, T = N2/32 warps; step 1
-// (radix 32, span 1) then step 2 (radix N2/32, span 32) with thread j taking
-// the tasks per·j + e, per = 32/T.
+// Pass A for N2 > 32 (N2 = 32 takes the pipelined fsf_pass_a32 below): a
+// CTA per n1, T = N2/32 warps; step 1 (radix 32, span 1) then step 2 (radix
+// N2/32, span 32) with thread j taking the tasks per·j + e, per = 32/T.
 // ---------------------------------------------------------------------------
 template <typename T, int N2>
 __global__ void __launch_bounds__(256)
 fsf_pass_a(const T* __restrict__ V, float2* __restrict__ scr, const float2* __restrict__ W,
            int N, int D, int H, int bh0, int nb) {
+  static_assert(N2 > 32, "N2 = 32 takes fsf_pass_a32");
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if constexpr (N2 == 32) {
-    const int n1 = (blockIdx.x / nb) * 8 + warp;
-    const int bhl = blockIdx.x % nb;
-    const int bh = bh0 + bhl, b = bh / H, h = bh - b * H;
-    const T* src = V + ((size_t)b * N + n1) * D + h * 64 + 2 * lane;
-    const size_t rs = (size_t)kFastN1 * D;
-    float2 a[32];
-#pragma unroll
-    for (int n2 = 0; n2 < 32; ++n2) a[n2] = ld_pair(src + n2 * rs);
-    dft<32, false>(a);
-#pragma unroll
-    for (int k2 = 0; k2 < 32; ++k2)
-      scr[scr_idx(bhl, 32, k2, n1, lane)] = cmul(a[k2], __ldg(&W[(size_t)n1 * k2]));
-  } else {
+  {
     constexpr int TS = N2 / 32;        // threads per signal
     constexpr int R2 = N2 / 32;        // radix of step 2
     constexpr int PER = 32 / TS;       // step-2 tasks per thread
@@ -126,20 +113,9 @@ template <typename T, int N2>
 __global__ void __launch_bounds__(256)
 fsf_pass_c(const float2* __restrict__ scr, T* __restrict__ O, const float2* __restrict__ W,
            int N, int D, int H, int bh0, int nb) {
+  static_assert(N2 > 32, "N2 = 32 takes fsf_pass_c32");
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if constexpr (N2 == 32) {
-    const int n1 = (blockIdx.x / nb) * 8 + warp;
-    const int bhl = blockIdx.x % nb;
-    const int bh = bh0 + bhl, b = bh / H, h = bh - b * H;
-    float2 a[32];
-#pragma unroll
-    for (int k2 = 0; k2 < 32; ++k2) a[k2] = scr[scr_idx(bhl, 32, k2, n1, lane)];
-    dft<32, true>(a);
-    T* dst = O + ((size_t)b * N + n1) * D + h * 64 + 2 * lane;
-    const size_t rs = (size_t)kFastN1 * D;
-#pragma unroll
-    for (int n2 = 0; n2 < 32; ++n2) st_pair(dst + n2 * rs, a[n2]);
-  } else {
+  {
     constexpr int TS = N2 / 32;
     constexpr int R2 = N2 / 32;
     constexpr int PER = 32 / TS;
@@ -685,13 +661,14 @@ template <typename T>
 static cudaError_t setup_t(int N2) {
   cudaError_t e = cudaSuccess;
   switch (N2) {
+    case 32: break;   // the pipelined passes and the row spectrum kernel, set below
 #define CAT_N2(n)                                                   \
   case n:                                                           \
     e = allow_max_smem(fsf_pass_a<T, n>);                           \
     if (e == cudaSuccess) e = allow_max_smem(fsf_pass_c<T, n>);     \
-    if (e == cudaSuccess && n > 32) e = allow_max_smem(fsf_zspec_a<(n > 32 ? n : 64)>); \
+    if (e == cudaSuccess) e = allow_max_smem(fsf_zspec_a<n>);       \
     break;
-    CAT_N2(32) CAT_N2(64) CAT_N2(128) CAT_N2(256)
+    CAT_N2(64) CAT_N2(128) CAT_N2(256)
 #undef CAT_N2
     default: return cudaErrorInvalidValue;
   }
@@ -732,11 +709,13 @@ cudaError_t setup_fast_kernels(cat_plan_s* p) {
   return cudaSuccess;
 }
 
+// Generic passes A and C (N2 > 32): a CTA of N2 threads per (b, h, n1).
 template <typename T, int N2>
 static void launch_ac(const cat_plan_s* p, const T* V, T* O, float2* scr, int bh0, int nb,
                       bool pass_a, cudaStream_t st) {
-  const int grid = N2 == 32 ? nb * (kFastN1 / 8) : nb * kFastN1;
-  const int threads = N2 == 32 ? 256 : N2;
+  static_assert(N2 > 32, "N2 = 32 takes the pipelined passes");
+  const int grid = nb * kFastN1;
+  const int threads = N2;
   const size_t smem = fast_smem_a(N2);
   if (pass_a)
     fsf_pass_a<T, N2><<<grid, threads, smem, st>>>(V, scr, p->tw, p->N, p->D, p->H, bh0, nb);
