@@ -404,3 +404,25 @@ def test_square_lengths_register_kernel(monkeypatch, N, B, D, H, dtype):
     scale = float(V.abs().max())
     tol = (8e-3 if dtype == "bf16" else 2e-5) * scale
     assert float((O_reg.float() - O_blk.float()).abs().max()) <= tol
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_longest_sequence(dtype):
+    """The longest sequence the ABI accepts (CAT_MAX_N = 2²² tokens) on the
+    general four-step path: all of z* against the oracle, O at sampled rows
+    against the per-element definition, and the column sums a circulant
+    with unit column sums keeps."""
+    B, N, D, H = 1, 1 << 22, 4, 2
+    X, WA, V = synth.make_inputs(B, N, D, H, dtype, seed=81)
+    with cat.Plan(B, N, D, H, dtype) as p:
+        assert "path=fourstep" in p.describe()
+    O, zs = run_gpu(X, WA, V, dtype)
+    zs_ref = oracle.zstar(X, WA)
+    check_zstar(zs, zs_ref)
+    rows = _sampled_rows(N, 12, 2)
+    O_ref = oracle.circ_direct_rows(zs_ref, V, rows)
+    check_out(O[:, rows], O_ref, V, dtype)
+    Vs = V.double().sum(1).numpy()
+    Os = O.double().sum(1).numpy()
+    tol = (8e-3 if dtype == "bf16" else 2e-5) * np.abs(V.double().numpy()).max() * np.sqrt(N)
+    assert np.abs(Os - Vs).max() <= tol
