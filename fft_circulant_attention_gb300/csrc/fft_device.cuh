@@ -37,6 +37,21 @@ __device__ __forceinline__ float2 rot90(float2 a) {
   return INV ? make_float2(-a.y, a.x) : make_float2(a.y, -a.x);
 }
 
+// Complex add and subtract for the register transforms: ordinary fp32
+// component pairs, or the paired fp32 instructions of sm_100 and later (one
+// instruction per complex add or subtract, the same rounding per component;
+// a - b is b·(-1) + a, exact).
+struct CxScalar {
+  static __device__ __forceinline__ float2 add(float2 a, float2 b) { return cadd(a, b); }
+  static __device__ __forceinline__ float2 sub(float2 a, float2 b) { return csub(a, b); }
+};
+struct CxPaired {
+  static __device__ __forceinline__ float2 add(float2 a, float2 b) { return __fadd2_rn(a, b); }
+  static __device__ __forceinline__ float2 sub(float2 a, float2 b) {
+    return __ffma2_rn(b, make_float2(-1.f, -1.f), a);
+  }
+};
+
 // Twiddle w or its conjugate.
 template <bool INV>
 __device__ __forceinline__ float2 twmul(float2 a, float2 w) {
@@ -47,11 +62,11 @@ __device__ __forceinline__ float2 twmul(float2 a, float2 w) {
 // Small DFTs on registers: b[s] = sum_u a[u] w_R^{±u s}, in place.
 // Constants are cos/sin of 2πk/R.
 // ---------------------------------------------------------------------------
-template <bool INV>
+template <bool INV, class Ops = CxScalar>
 __device__ __forceinline__ void dft2(float2* a) {
   float2 t = a[0];
-  a[0] = cadd(t, a[1]);
-  a[1] = csub(t, a[1]);
+  a[0] = Ops::add(t, a[1]);
+  a[1] = Ops::sub(t, a[1]);
 }
 
 template <bool INV>
@@ -66,14 +81,14 @@ __device__ __forceinline__ void dft3(float2* a) {
   a[2] = csub(m, r);
 }
 
-template <bool INV>
+template <bool INV, class Ops = CxScalar>
 __device__ __forceinline__ void dft4(float2* a) {
-  float2 t0 = cadd(a[0], a[2]), t1 = csub(a[0], a[2]);
-  float2 t2 = cadd(a[1], a[3]), t3 = rot90<INV>(csub(a[1], a[3]));
-  a[0] = cadd(t0, t2);
-  a[2] = csub(t0, t2);
-  a[1] = cadd(t1, t3);
-  a[3] = csub(t1, t3);
+  float2 t0 = Ops::add(a[0], a[2]), t1 = Ops::sub(a[0], a[2]);
+  float2 t2 = Ops::add(a[1], a[3]), t3 = rot90<INV>(Ops::sub(a[1], a[3]));
+  a[0] = Ops::add(t0, t2);
+  a[2] = Ops::sub(t0, t2);
+  a[1] = Ops::add(t1, t3);
+  a[3] = Ops::sub(t1, t3);
 }
 
 template <bool INV>
@@ -126,13 +141,13 @@ __device__ __forceinline__ void dft7(float2* a) {
   a[4] = csub(m3, r3);
 }
 
-template <bool INV>
+template <bool INV, class Ops = CxScalar>
 __device__ __forceinline__ void dft8(float2* a) {
   const float R2 = 0.7071067811865476f;  // cos(π/4)
   float2 e[4] = {a[0], a[2], a[4], a[6]};
   float2 o[4] = {a[1], a[3], a[5], a[7]};
-  dft4<INV>(e);
-  dft4<INV>(o);
+  dft4<INV, Ops>(e);
+  dft4<INV, Ops>(o);
   // o[k] *= w8^{±k}
   float2 o1 = o[1], o3 = o[3];
   if (!INV) {
@@ -145,8 +160,8 @@ __device__ __forceinline__ void dft8(float2* a) {
   o[2] = rot90<INV>(o[2]);
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    a[k] = cadd(e[k], o[k]);
-    a[k + 4] = csub(e[k], o[k]);
+    a[k] = Ops::add(e[k], o[k]);
+    a[k + 4] = Ops::sub(e[k], o[k]);
   }
 }
 

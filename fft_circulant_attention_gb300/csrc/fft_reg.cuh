@@ -93,11 +93,13 @@ __device__ __forceinline__ float2 twc(float2 a) {
   }
 }
 
-template <int R, bool INV>
+// Ops: the complex add/subtract policy (CxScalar, or CxPaired for the paired
+// fp32 instructions).
+template <int R, bool INV, class Ops = CxScalar>
 __device__ __forceinline__ void dft(float2* a);
 
 // R = P·Q split (see the file comment).
-template <int P, int Q, bool INV>
+template <int P, int Q, bool INV, class Ops>
 __device__ __forceinline__ void dft_pq(float2* a) {
   constexpr int R = P * Q;
   float2 y[P][Q];
@@ -106,7 +108,7 @@ __device__ __forceinline__ void dft_pq(float2* a) {
     float2 t[Q];
 #pragma unroll
     for (int n1 = 0; n1 < Q; ++n1) t[n1] = a[P * n1 + n2];
-    dft<Q, INV>(t);
+    dft<Q, INV, Ops>(t);
     static_for<0, Q>([&](auto k1c) {
       constexpr int k1 = decltype(k1c)::value;
       y[n2][k1] = twc<R, n2 * k1, INV>(t[k1]);
@@ -117,31 +119,31 @@ __device__ __forceinline__ void dft_pq(float2* a) {
     float2 t[P];
 #pragma unroll
     for (int n2 = 0; n2 < P; ++n2) t[n2] = y[n2][k1];
-    dft<P, INV>(t);
+    dft<P, INV, Ops>(t);
 #pragma unroll
     for (int k2 = 0; k2 < P; ++k2) a[Q * k2 + k1] = t[k2];
   }
 }
 
-template <int R, bool INV>
+template <int R, bool INV, class Ops>
 __device__ __forceinline__ void dft(float2* a) {
   if constexpr (R == 1) {
   } else if constexpr (R == 2) {
-    dft2<INV>(a);
+    dft2<INV, Ops>(a);
   } else if constexpr (R == 4) {
-    dft4<INV>(a);
+    dft4<INV, Ops>(a);
   } else if constexpr (R == 7) {
     dft7<INV>(a);
   } else if constexpr (R == 8) {
-    dft8<INV>(a);
+    dft8<INV, Ops>(a);
   } else if constexpr (R == 14) {
-    dft_pq<2, 7, INV>(a);
+    dft_pq<2, 7, INV, Ops>(a);
   } else if constexpr (R == 16) {
-    dft_pq<4, 4, INV>(a);
+    dft_pq<4, 4, INV, Ops>(a);
   } else if constexpr (R == 32) {
-    dft_pq<4, 8, INV>(a);
+    dft_pq<4, 8, INV, Ops>(a);
   } else if constexpr (R == 64) {
-    dft_pq<8, 8, INV>(a);
+    dft_pq<8, 8, INV, Ops>(a);
   } else {
     static_assert(R == 2, "dft: unsupported length");
   }

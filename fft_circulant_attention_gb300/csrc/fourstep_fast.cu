@@ -226,7 +226,7 @@ fsf_pass_a32(const __grid_constant__ CUtensorMap tmV, float2* __restrict__ scr,
     float2 a[32];
 #pragma unroll
     for (int n2 = 0; n2 < 32; ++n2) a[n2] = sh_pair(tile + n2 * 64);
-    dft<32, false>(a);
+    dft<32, false, CxPaired>(a);
     __syncwarp();
     const int next = item + P::kStages * G;
     if (next < items) issue(s, next);
@@ -272,7 +272,7 @@ fsf_pass_c32(const __grid_constant__ CUtensorMap tmC, const float2* __restrict__
     float2 a[32];
 #pragma unroll
     for (int k2 = 0; k2 < 32; ++k2) a[k2] = tile[k2 * kFastPairs];
-    dft<32, true>(a);
+    dft<32, true, CxPaired>(a);
     __syncwarp();
     const int next = item + P::kStages * G;
     if (next < items) issue(s, next);
@@ -348,7 +348,7 @@ fsf_pass_b(float2* __restrict__ scr, const float2* __restrict__ zft,
   const float4 q2 = __ldg(g4 + 512 + (size_t)k2 * 256 + t);          // tx of this k2
   const float4 q3 = __ldg(reinterpret_cast<const float4*>(zft) +
                           ((size_t)(bh0 + bhl) * N2 + k2) * (kFastN1 / 2) + t);
-  dft<32, false>(a);
+  dft<32, false, CxPaired>(a);
 #pragma unroll
   for (int q = 0; q < 32; q += 2) st_sh2(row + 32 * j + q, a[q], a[q + 1]);
   float4* tf4 = reinterpret_cast<float4*>(tf);
@@ -372,7 +372,7 @@ fsf_pass_b(float2* __restrict__ scr, const float2* __restrict__ zft,
       c[e][u + 1] = cmul(c[e][u + 1], w1);
     }
     c[e][1] = cmul(c[e][1], tw[1]);
-    dft<16, false>(c[e]);
+    dft<16, false, CxPaired>(c[e]);
   }
   // Product with FFT(z*)/N at bins k1 = 2j + e + 32s.
 #pragma unroll
@@ -387,7 +387,7 @@ fsf_pass_b(float2* __restrict__ scr, const float2* __restrict__ zft,
   // 32·(p mod 16) + p / 16 = 32s + 2j + e, so that I2's 32 inputs
   // (positions j + 16u) sit at 32j + u: both sides move 16-byte pairs.
 #pragma unroll
-  for (int e = 0; e < 2; ++e) dft<16, true>(c[e]);
+  for (int e = 0; e < 2; ++e) dft<16, true, CxPaired>(c[e]);
 #pragma unroll
   for (int q = 0; q < 16; ++q) st_sh2(row + 32 * q + 2 * j, c[0][q], c[1][q]);
   __syncthreads();
@@ -404,7 +404,7 @@ fsf_pass_b(float2* __restrict__ scr, const float2* __restrict__ zft,
     }
     a[1] = cmulc(a[1], tw[1]);
   }
-  dft<32, true>(a);
+  dft<32, true, CxPaired>(a);
   {
     const float2* tw = tx + j * 32;
 #pragma unroll
@@ -603,7 +603,7 @@ fsf_zspec_row(const float2* __restrict__ z2, float2* __restrict__ zft,
   const float inv = 1.0f / S;
 #pragma unroll
   for (int u = 0; u < 32; ++u) a[u].x *= inv;
-  dft<32, false>(a);
+  dft<32, false, CxPaired>(a);
   const bool ok = __syncthreads_and(mbar_wait(bar, 0, status, 0x503));
   // Twiddle w_N^{n1·k2} (n1 = t) and store [k2][n1].
   if (ok) {
@@ -624,7 +624,7 @@ fsf_zspec_row(const float2* __restrict__ z2, float2* __restrict__ zft,
 #pragma unroll
   for (int u = 0; u < 32; ++u) a[u] = rb[j + 16 * u];
   __syncthreads();
-  dft<32, false>(a);
+  dft<32, false, CxPaired>(a);
 #pragma unroll
   for (int q = 0; q < 32; q += 2) st_sh2(rb + 32 * j + q, a[q], a[q + 1]);
   __syncthreads();
@@ -642,7 +642,7 @@ fsf_zspec_row(const float2* __restrict__ z2, float2* __restrict__ zft,
       c[e][u + 1] = cmul(c[e][u + 1], w1);
     }
     c[e][1] = cmul(c[e][1], tw[1]);
-    dft<16, false>(c[e]);
+    dft<16, false, CxPaired>(c[e]);
   }
   const float invN = 1.0f / (float)N;
   float4* out = reinterpret_cast<float4*>(zft) + (((size_t)row * 32 + k2) * 16 + j) * 16;
