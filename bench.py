@@ -48,7 +48,7 @@ FALLBACK_HBM_GBS = 6800.0
 NCU_TRAFFIC = {
     # profiles/launches_long16k.md: fsf_pass_b, 16 launches, DRAM read + write
     # per launch (cold: ncu flushes L2 before each launch).
-    ("long16k", "20df85dd97fa"): 34781088,
+    ("long16k", "2463f22c18e9"): 34774016,
 }
 KERNEL_SOURCES = ["fourstep_fast.cu", "fft_reg.cuh", "fft_device.cuh", "bulk.cuh", "elem.cuh"]
 # Pass B's transforms: per (pair, k2) signal one forward and one inverse DFT
