@@ -64,6 +64,20 @@ __device__ __forceinline__ void two_sum_acc(float& hi, float& lo, float p) {
   lo += err;
 }
 
+// The same for two accumulators at once with the paired fp32 instructions
+// (each component rounds exactly as the scalar operation; x - y is formed as
+// y·(-1) + x, exact in the product).
+__device__ __forceinline__ float2 sub2(float2 x, float2 y) {
+  return __ffma2_rn(y, make_float2(-1.f, -1.f), x);
+}
+__device__ __forceinline__ void two_sum_acc2(float2& hi, float2& lo, float2 p) {
+  const float2 s = __fadd2_rn(hi, p);
+  const float2 bp = sub2(s, hi);
+  const float2 err = __fadd2_rn(sub2(hi, sub2(s, bp)), sub2(p, bp));
+  hi = s;
+  lo = __fadd2_rn(lo, err);
+}
+
 // W_A's columns [h0, h0 + HT) as fp32 [D][HP] in shared memory (columns HT
 // to HP zero).  Eight loads per thread are in flight before any is stored,
 // so the staging costs a few latencies rather than D·HP / blockDim of them.
@@ -522,11 +536,12 @@ score_tma_kernel(const __grid_constant__ CUtensorMap tmX, const __nv_bfloat16* _
   const int arow = warp * 16 + (lm & 1) * 8 + li;   // ldmatrix row this lane addresses
   int it = 0;
   for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-    float hi[NT][4], lo[NT][4];
+    // Accumulators in pairs: [nt][r] holds fragment elements 2r, 2r + 1.
+    float2 hi[NT][2], lo[NT][2];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int i = 0; i < 4; ++i) hi[nt][i] = lo[nt][i] = 0.f;
+      for (int r = 0; r < 2; ++r) hi[nt][r] = lo[nt][r] = make_float2(0.f, 0.f);
     for (int kb = 0; kb < nkb; ++kb, ++it) {
       const int s = it % kTsStages;
       if (!mbar_wait(full + s, (it / kTsStages) & 1, status, 0x602)) return;
@@ -556,7 +571,8 @@ score_tma_kernel(const __grid_constant__ CUtensorMap tmX, const __nv_bfloat16* _
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-          for (int i = 0; i < 4; ++i) two_sum_acc(hi[nt][i], lo[nt][i], acc[nt][i]);
+          for (int r = 0; r < 2; ++r)
+            two_sum_acc2(hi[nt][r], lo[nt][r], make_float2(acc[nt][2 * r], acc[nt][2 * r + 1]));
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(empty + s);
@@ -569,7 +585,9 @@ score_tma_kernel(const __grid_constant__ CUtensorMap tmX, const __nv_bfloat16* _
         const int hh = nt * 8 + 2 * c + (i & 1);
         if (r < rows_total && hh < HT) {
           const int b = r / N, n = r - b * N;
-          z[((size_t)b * H + h0 + hh) * N + n] = make_float2(hi[nt][i], lo[nt][i]);
+          const float2 hv = hi[nt][i >> 1], lv = lo[nt][i >> 1];
+          z[((size_t)b * H + h0 + hh) * N + n] =
+              (i & 1) ? make_float2(hv.y, lv.y) : make_float2(hv.x, lv.x);
         }
       }
   }
