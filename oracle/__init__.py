@@ -1,4 +1,4 @@
-"""fp64 CPU oracle for the CAT forward pass — TEST INFRASTRUCTURE.
+"""fp64 CPU oracle for the CAT forward and backward passes — TEST INFRASTRUCTURE.
 
 Only the tests, the smoke check and the benchmark's CPU-baseline leg may
 import this package.  The product path (the CUDA library and its binding)
@@ -13,6 +13,15 @@ matrix construction" and "FFT acceleration"):
     z* = softmax_n(z)         over the N tokens of each (b, h)
     O  = circ(z*) · V_h       circ(z*)[i, j] = z*[(i - j) mod N]
        = IFFT(FFT(z*) ⊙ FFT(V_h))   column by column
+
+The backward pass (gradients of a loss L given G = dL/dO) follows from
+these definitions by the chain rule; the page trains CAT layers with the
+usual losses (section 损失函数 / 训练策略) but prints no gradient formulas:
+
+    dV   = circ(z*)^T G                       dV[j, c] = sum_i z*[(i-j) mod N] G[i, c]
+    dz*  = sum_{c in h} corr(G[:, c], V[:, c])  dz*[k] = sum_c sum_i G[i, c] V[(i-k) mod N, c]
+    dz   = z* ⊙ (dz* - <z*, dz*>)             softmax Jacobian
+    dW_A = X^T dz,   dX = dz W_A^T
 
 All arithmetic is fp64 in ``cat_oracle.c``; this module only marshals numpy
 arrays.  ``brute_circulant`` builds the N x N matrix explicitly (tiny N only)
@@ -50,6 +59,22 @@ def _lib():
         lib.oracle_circ_fft.restype = ctypes.c_int
         lib.oracle_spectrum.argtypes = [dp, L, L, dp]
         lib.oracle_spectrum.restype = ctypes.c_int
+        lib.oracle_circ_transpose_direct.argtypes = [dp, dp, L, L, L, L, dp]
+        lib.oracle_circ_transpose_direct.restype = None
+        lib.oracle_circ_transpose_direct_rows.argtypes = [dp, dp, L, L, L, L, lp, L, dp]
+        lib.oracle_circ_transpose_direct_rows.restype = None
+        lib.oracle_corr_direct_bins.argtypes = [dp, dp, L, L, L, L, lp, L, dp]
+        lib.oracle_corr_direct_bins.restype = None
+        lib.oracle_softmax_backward.argtypes = [dp, dp, L, L, dp]
+        lib.oracle_softmax_backward.restype = None
+        lib.oracle_grad_wa.argtypes = [dp, dp, L, L, L, L, dp]
+        lib.oracle_grad_wa.restype = None
+        lib.oracle_grad_x.argtypes = [dp, dp, L, L, L, L, dp]
+        lib.oracle_grad_x.restype = None
+        lib.oracle_circ_transpose_fft.argtypes = [dp, dp, L, L, L, L, dp]
+        lib.oracle_circ_transpose_fft.restype = ctypes.c_int
+        lib.oracle_corr_fft.argtypes = [dp, dp, L, L, L, L, dp, dp]
+        lib.oracle_corr_fft.restype = ctypes.c_int
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = ctypes.c_int
         _LIB = lib
@@ -183,6 +208,132 @@ def forward(X, WA, V, mode="auto"):
     raise ValueError(mode)
 
 
+# --------------------------------------------------------------------------
+# Backward pass
+# --------------------------------------------------------------------------
+
+def _rows_arg(rows):
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).astype(np.int_))
+    return rows, rows.ctypes.data_as(ctypes.POINTER(ctypes.c_long))
+
+
+def circ_transpose_direct(zs, G):
+    """dV = circ(z*)^T G by the O(N^2) definition.  zs [B,H,N], G [B,N,D]."""
+    zs, G = _f64(zs), _f64(G)
+    B, N, D = G.shape
+    H = zs.shape[1]
+    dV = np.empty((B, N, D), np.float64)
+    _lib().oracle_circ_transpose_direct(_p(zs), _p(G), B, N, D, H, _p(dV))
+    return dV
+
+
+def circ_transpose_direct_rows(zs, G, rows):
+    """dV by the definition at the listed rows only: [B, len(rows), D]."""
+    zs, G = _f64(zs), _f64(G)
+    B, N, D = G.shape
+    H = zs.shape[1]
+    rows, rp = _rows_arg(rows)
+    out = np.empty((B, rows.size, D), np.float64)
+    _lib().oracle_circ_transpose_direct_rows(_p(zs), _p(G), B, N, D, H, rp, rows.size, _p(out))
+    return out
+
+
+def circ_transpose_fft(zs, G):
+    """dV = IFFT(conj(FFT(z*)) ⊙ FFT(G[:, c])) per column, fp64."""
+    zs, G = _f64(zs), _f64(G)
+    B, N, D = G.shape
+    H = zs.shape[1]
+    dV = np.empty((B, N, D), np.float64)
+    if _lib().oracle_circ_transpose_fft(_p(zs), _p(G), B, N, D, H, _p(dV)) != 0:
+        raise MemoryError("oracle_circ_transpose_fft")
+    return dV
+
+
+def corr_direct_bins(G, V, H, bins):
+    """dz*[b, h, k] = sum_{c in h} sum_i G[b,i,c] V[b,(i-k) mod N,c] by the
+    definition, at the listed bins k: [B, H, len(bins)]."""
+    G, V = _f64(G), _f64(V)
+    B, N, D = G.shape
+    bins, bp = _rows_arg(bins)
+    out = np.empty((B, H, bins.size), np.float64)
+    _lib().oracle_corr_direct_bins(_p(G), _p(V), B, N, D, H, bp, bins.size, _p(out))
+    return out
+
+
+def corr_direct(G, V, H):
+    """dz* at every bin by the definition, O(B·N^2·D): [B, H, N]."""
+    N = np.shape(G)[1]
+    return corr_direct_bins(G, V, H, np.arange(N))
+
+
+def corr_fft(G, V, H, return_max_imag=False):
+    """dz* = Re IFFT(sum_{c in h} FFT(G[:, c]) ⊙ conj(FFT(V[:, c]))), fp64."""
+    G, V = _f64(G), _f64(V)
+    B, N, D = G.shape
+    out = np.empty((B, H, N), np.float64)
+    mi = ctypes.c_double(0.0)
+    if _lib().oracle_corr_fft(_p(G), _p(V), B, N, D, H, _p(out), ctypes.pointer(mi)) != 0:
+        raise MemoryError("oracle_corr_fft")
+    return (out, mi.value) if return_max_imag else out
+
+
+def softmax_backward(zs, dzs):
+    """dz = z* ⊙ (dz* - sum_m z*[m] dz*[m]) over the last axis."""
+    zs, dzs = _f64(zs), _f64(dzs)
+    N = zs.shape[-1]
+    out = np.empty_like(zs)
+    _lib().oracle_softmax_backward(_p(zs), _p(dzs), zs.size // N if N else 0, N, _p(out))
+    return out
+
+
+def grad_wa(X, dz):
+    """dW_A[d, h] = sum_b sum_n X[b, n, d] dz[b, h, n]: [D, H]."""
+    X, dz = _f64(X), _f64(dz)
+    B, N, D = X.shape
+    H = dz.shape[1]
+    out = np.empty((D, H), np.float64)
+    _lib().oracle_grad_wa(_p(X), _p(dz), B, N, D, H, _p(out))
+    return out
+
+
+def grad_x(dz, WA):
+    """dX[b, n, d] = sum_h dz[b, h, n] W_A[d, h]: [B, N, D]."""
+    dz, WA = _f64(dz), _f64(WA)
+    B, H, N = dz.shape
+    D = WA.shape[0]
+    out = np.empty((B, N, D), np.float64)
+    _lib().oracle_grad_x(_p(dz), _p(WA), B, N, D, H, _p(out))
+    return out
+
+
+def backward(X, WA, V, G, mode="auto"):
+    """Whole backward for the upstream gradient G = dL/dO, fp64.
+
+    Returns a dict with dX [B,N,D], dWA [D,H], dV [B,N,D], and the
+    intermediates zs (z*), dzs (dL/dz*) and dz (dL/dz), each [B,H,N].
+    mode: "direct" (O(N^2) definitions), "fft" (convolution and correlation
+    theorems), or "auto" (direct while B·N²·D stays under ~2e9, else fft).
+    """
+    X, WA, V, G = _f64(X), _f64(WA), _f64(V), _f64(G)
+    B, N, D = V.shape
+    H = WA.shape[1]
+    zs = zstar(X, WA)
+    if mode == "auto":
+        mode = "direct" if B * N * N * D <= 2e9 else "fft"
+    if mode == "direct":
+        dV = circ_transpose_direct(zs, G)
+        dzs = corr_direct(G, V, H)
+    elif mode == "fft":
+        dV = circ_transpose_fft(zs, G)
+        dzs = corr_fft(G, V, H)
+    else:
+        raise ValueError(mode)
+    dz = softmax_backward(zs, dzs)
+    return dict(dX=grad_x(dz, WA), dWA=grad_wa(X, dz), dV=dV, zs=zs, dzs=dzs, dz=dz)
+
+
 __all__ = ["scores", "softmax", "zstar", "dft", "spectrum", "circ_direct",
            "circ_direct_rows", "circ_fft", "brute_circulant", "forward",
-           "num_threads"]
+           "num_threads", "circ_transpose_direct", "circ_transpose_direct_rows",
+           "circ_transpose_fft", "corr_direct", "corr_direct_bins", "corr_fft",
+           "softmax_backward", "grad_wa", "grad_x", "backward"]

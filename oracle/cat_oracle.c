@@ -1,5 +1,6 @@
 /*
- * fp64 CPU oracle for the CAT forward pass (circular-convolutional attention).
+ * fp64 CPU oracle for the CAT forward pass (circular-convolutional attention)
+ * and its backward pass (gradients by the chain rule, further below).
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may call, link or
  * load this file; only the tests, the smoke check and the benchmark's CPU
@@ -289,6 +290,239 @@ int oracle_spectrum(const double *zs, long rows, long N, double *zf) {
     }
     free(t);
   }
+  return fail ? -1 : 0;
+}
+
+/* ------------------------------------------------------------------------
+ * Backward pass.  The page trains CAT layers with the usual losses and
+ * optimisers (section 损失函数 / 训练策略, loss and training strategy) but
+ * prints no gradient formulas; these follow from the forward definitions
+ * above by the chain rule.  With G = dL/dO [B, N, D] the upstream gradient:
+ *
+ *   O[i, c] = sum_j z*[(i - j) mod N] V[j, c]           (forward, head h(c))
+ *   dV[j, c]   = sum_i z*[(i - j) mod N] G[i, c]        = (circ(z*)^T G)[j, c]
+ *   dz*[h, k]  = sum_{c in h} sum_i G[i, c] V[(i - k) mod N, c]
+ *   dz[h, n]   = z*[n] (dz*[n] - sum_m z*[m] dz*[m])     (softmax Jacobian)
+ *   dW_A[d, h] = sum_b sum_n X[b, n, d] dz[b, h, n]
+ *   dX[b, n, d] = sum_h dz[b, h, n] W_A[d, h]
+ *
+ * (∂O[i, c]/∂z*[k] = V[(i - k) mod N, c], because z*[k] multiplies V[j, c]
+ * exactly where (i - j) mod N = k.)
+ * ------------------------------------------------------------------------ */
+
+/* dV = circ(z*)^T · G by the definition, O(B·N²·D). */
+void oracle_circ_transpose_direct(const double *zs, const double *G, long B,
+                                  long N, long D, long H, double *dV) {
+  long b, j;
+#pragma omp parallel for collapse(2) schedule(static)
+  for (b = 0; b < B; ++b) {
+    for (j = 0; j < N; ++j) {
+      for (long c = 0; c < D; ++c) {
+        const double *w = zs + (b * H + head_of(c, D, H)) * N;
+        double acc = 0.0;
+        for (long i = 0; i < N; ++i) {
+          long s = i - j;
+          if (s < 0) s += N;
+          acc += w[s] * G[(b * N + i) * D + c];
+        }
+        dV[(b * N + j) * D + c] = acc;
+      }
+    }
+  }
+}
+
+/* The same at the listed rows j only: dVrows[b, r, c]. */
+void oracle_circ_transpose_direct_rows(const double *zs, const double *G,
+                                       long B, long N, long D, long H,
+                                       const long *rows, long nrows,
+                                       double *dVrows) {
+  long b, r;
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+  for (b = 0; b < B; ++b) {
+    for (r = 0; r < nrows; ++r) {
+      long j = rows[r];
+      for (long c = 0; c < D; ++c) {
+        const double *w = zs + (b * H + head_of(c, D, H)) * N;
+        double acc = 0.0;
+        for (long i = 0; i < N; ++i) {
+          long s = i - j;
+          if (s < 0) s += N;
+          acc += w[s] * G[(b * N + i) * D + c];
+        }
+        dVrows[(b * nrows + r) * D + c] = acc;
+      }
+    }
+  }
+}
+
+/* dz*[b, h, k] = sum_{c in head h} sum_i G[b, i, c] V[b, (i - k) mod N, c]
+ * by the definition, at the listed bins k only (nbins of them; pass every
+ * k for the whole row): out[b, h, r] for k = bins[r]. */
+void oracle_corr_direct_bins(const double *G, const double *V, long B, long N,
+                             long D, long H, const long *bins, long nbins,
+                             double *out) {
+  const long dh = D / H;
+  long b, h;
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+  for (b = 0; b < B; ++b) {
+    for (h = 0; h < H; ++h) {
+      for (long r = 0; r < nbins; ++r) {
+        long k = bins[r];
+        double acc = 0.0;
+        for (long c = h * dh; c < (h + 1) * dh; ++c) {
+          for (long i = 0; i < N; ++i) {
+            long s = i - k;
+            if (s < 0) s += N;
+            acc += G[(b * N + i) * D + c] * V[(b * N + s) * D + c];
+          }
+        }
+        out[(b * H + h) * nbins + r] = acc;
+      }
+    }
+  }
+}
+
+/* Softmax backward over each of `rows` rows of length N:
+ * dz[n] = z*[n] · (dz*[n] - sum_m z*[m] dz*[m]). */
+void oracle_softmax_backward(const double *zs, const double *dzs, long rows,
+                             long N, double *dz) {
+  long r;
+#pragma omp parallel for schedule(static)
+  for (r = 0; r < rows; ++r) {
+    const double *p = zs + r * N, *g = dzs + r * N;
+    double s = 0.0;
+    for (long m = 0; m < N; ++m) s += p[m] * g[m];
+    for (long n = 0; n < N; ++n) dz[r * N + n] = p[n] * (g[n] - s);
+  }
+}
+
+/* dW_A[d, h] = sum_b sum_n X[b, n, d] · dz[b, h, n]. */
+void oracle_grad_wa(const double *X, const double *dz, long B, long N, long D,
+                    long H, double *dWA) {
+  long d;
+#pragma omp parallel for schedule(static)
+  for (d = 0; d < D; ++d) {
+    for (long h = 0; h < H; ++h) {
+      double acc = 0.0;
+      for (long b = 0; b < B; ++b)
+        for (long n = 0; n < N; ++n)
+          acc += X[(b * N + n) * D + d] * dz[(b * H + h) * N + n];
+      dWA[d * H + h] = acc;
+    }
+  }
+}
+
+/* dX[b, n, d] = sum_h dz[b, h, n] · W_A[d, h]. */
+void oracle_grad_x(const double *dz, const double *WA, long B, long N, long D,
+                   long H, double *dX) {
+  long b, n;
+#pragma omp parallel for collapse(2) schedule(static)
+  for (b = 0; b < B; ++b) {
+    for (n = 0; n < N; ++n) {
+      for (long d = 0; d < D; ++d) {
+        double acc = 0.0;
+        for (long h = 0; h < H; ++h) acc += dz[(b * H + h) * N + n] * WA[d * H + h];
+        dX[(b * N + n) * D + d] = acc;
+      }
+    }
+  }
+}
+
+/* dV by the convolution theorem: circ(z*)^T has the spectrum conj(FFT(z*))
+ * (z* is real), so dV[:, c] = IFFT(conj(FFT(z*)) ⊙ FFT(G[:, c])), each
+ * column transformed on its own.  Returns 0 or -1 (memory). */
+int oracle_circ_transpose_fft(const double *zs, const double *G, long B, long N,
+                              long D, long H, double *dV) {
+  long rows = B * H;
+  double *zf = (double *)malloc(sizeof(double) * 2 * (size_t)(rows * N));
+  if (!zf) return -1;
+  int fail = 0;
+  long r;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (r = 0; r < rows; ++r) {
+    double *fr = zf + 2 * r * N, *fi = fr + N;
+    for (long n = 0; n < N; ++n) {
+      fr[n] = zs[r * N + n];
+      fi[n] = 0.0;
+    }
+    if (oracle_dft(fr, fi, N, 0) != 0) fail = 1;
+  }
+  long b, c;
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+  for (b = 0; b < B; ++b) {
+    for (c = 0; c < D; ++c) {
+      double *gr = (double *)malloc(sizeof(double) * 2 * (size_t)N);
+      if (!gr) {
+        fail = 1;
+        continue;
+      }
+      double *gi = gr + N;
+      for (long n = 0; n < N; ++n) {
+        gr[n] = G[(b * N + n) * D + c];
+        gi[n] = 0.0;
+      }
+      if (oracle_dft(gr, gi, N, 0) != 0) fail = 1;
+      const double *fr = zf + 2 * (b * H + head_of(c, D, H)) * N;
+      const double *fi = fr + N;
+      for (long k = 0; k < N; ++k) { /* conj(Zf) ⊙ Gf */
+        double pr = fr[k] * gr[k] + fi[k] * gi[k];
+        double pi = fr[k] * gi[k] - fi[k] * gr[k];
+        gr[k] = pr;
+        gi[k] = pi;
+      }
+      if (oracle_dft(gr, gi, N, 1) != 0) fail = 1;
+      for (long n = 0; n < N; ++n) dV[(b * N + n) * D + c] = gr[n];
+      free(gr);
+    }
+  }
+  free(zf);
+  return fail ? -1 : 0;
+}
+
+/* dz* by the correlation theorem: per (b, h),
+ * dz* = IFFT( sum_{c in h} FFT(G[:, c]) ⊙ conj(FFT(V[:, c])) ), real part.
+ * max_imag receives max |Im| of the inverse transforms (zero in exact
+ * arithmetic).  Returns 0 or -1 (memory). */
+int oracle_corr_fft(const double *G, const double *V, long B, long N, long D,
+                    long H, double *dzs, double *max_imag) {
+  const long dh = D / H;
+  int fail = 0;
+  double mi = 0.0;
+  long b, h;
+#pragma omp parallel for collapse(2) schedule(dynamic, 1) reduction(max : mi)
+  for (b = 0; b < B; ++b) {
+    for (h = 0; h < H; ++h) {
+      double *buf = (double *)malloc(sizeof(double) * 6 * (size_t)N);
+      if (!buf) {
+        fail = 1;
+        continue;
+      }
+      double *ar = buf, *ai = buf + N;          /* accumulated spectrum */
+      double *gr = buf + 2 * N, *gi = buf + 3 * N;
+      double *vr = buf + 4 * N, *vi = buf + 5 * N;
+      for (long k = 0; k < N; ++k) ar[k] = ai[k] = 0.0;
+      for (long c = h * dh; c < (h + 1) * dh; ++c) {
+        for (long n = 0; n < N; ++n) {
+          gr[n] = G[(b * N + n) * D + c];
+          gi[n] = 0.0;
+          vr[n] = V[(b * N + n) * D + c];
+          vi[n] = 0.0;
+        }
+        if (oracle_dft(gr, gi, N, 0) != 0 || oracle_dft(vr, vi, N, 0) != 0) fail = 1;
+        for (long k = 0; k < N; ++k) { /* Gf ⊙ conj(Vf) */
+          ar[k] += gr[k] * vr[k] + gi[k] * vi[k];
+          ai[k] += gi[k] * vr[k] - gr[k] * vi[k];
+        }
+      }
+      if (oracle_dft(ar, ai, N, 1) != 0) fail = 1;
+      for (long n = 0; n < N; ++n) {
+        dzs[(b * H + h) * N + n] = ar[n];
+        if (fabs(ai[n]) > mi) mi = fabs(ai[n]);
+      }
+      free(buf);
+    }
+  }
+  if (max_imag) *max_imag = mi;
   return fail ? -1 : 0;
 }
 

@@ -9,6 +9,8 @@ masked-LM tokens — have no public inputs here, so i.i.d. Gaussians stand in):
   * numpy ``Generator(PCG64(seed))``, draws in the order X, W_A, V, each drawn
     as float32 standard normals;
   * X, V ~ N(0, 1) of shape [B, N, D];  W_A ~ N(0, 1/D) · wa_scale, [D, H];
+  * the backward pass's upstream gradient dO ~ N(0, 1), [B, N, D], from a
+    second, independent stream (``make_grad``);
   * then rounded to the storage dtype (float32 as drawn; bfloat16 by torch's
     round-to-nearest-even conversion).
 """
@@ -40,6 +42,17 @@ def make_inputs(B, N, D, H, dtype="f32", seed=0, wa_scale=1.0):
     tdt = DTYPES[dtype]
     return (torch.from_numpy(X).to(tdt), torch.from_numpy(WA).to(tdt),
             torch.from_numpy(V).to(tdt))
+
+
+def make_grad(B, N, D, dtype="f32", seed=0):
+    """Upstream gradient dO [B, N, D] for the backward pass: float32 standard
+    normals from the stream ``PCG64([seed, 1])`` (independent of the stream
+    ``make_inputs`` draws X, W_A, V from), rounded to ``dtype``."""
+    if dtype not in DTYPES:
+        raise ValueError("dtype must be one of %s" % sorted(DTYPES))
+    rng = np.random.Generator(np.random.PCG64([seed, 1]))
+    G = rng.standard_normal((B, N, D), dtype=np.float32)
+    return torch.from_numpy(G).to(DTYPES[dtype])
 
 
 def make_config(name, seed=0, wa_scale=1.0):

@@ -35,9 +35,33 @@ MUTANTS = {
     "no_normalise": ("out[n] /= s;", "out[n] /= 1.0;"),
 }
 
+# Mistakes in the backward pass, caught by the backward pins.
+BACKWARD_MUTANTS = {
+    # correlation lag reversed (a convolution of G with V instead)
+    "corr_lag": ("long s = i - k;", "long s = k - i;"),
+    # softmax Jacobian without its mean term
+    "softmax_bw_no_mean": ("dz[r * N + n] = p[n] * (g[n] - s);", "dz[r * N + n] = p[n] * g[n];"),
+    # spectrum product without the conjugate on V (convolution theorem instead)
+    "corr_fft_no_conj": ("ar[k] += gr[k] * vr[k] + gi[k] * vi[k];\n"
+                         "          ai[k] += gi[k] * vr[k] - gr[k] * vi[k];",
+                         "ar[k] += gr[k] * vr[k] - gi[k] * vi[k];\n"
+                         "          ai[k] += gi[k] * vr[k] + gr[k] * vi[k];"),
+    # transposed circulant's spectrum not conjugated
+    "transpose_fft_no_conj": ("double pr = fr[k] * gr[k] + fi[k] * gi[k];\n"
+                              "        double pi = fr[k] * gi[k] - fi[k] * gr[k];",
+                              "double pr = fr[k] * gr[k] - fi[k] * gi[k];\n"
+                              "        double pi = fr[k] * gi[k] + fi[k] * gr[k];"),
+    # dX contracted with W_A read transposed
+    "grad_x_transposed_wa": ("acc += dz[(b * H + h) * N + n] * WA[d * H + h];",
+                             "acc += dz[(b * H + h) * N + n] * WA[h * D + d];"),
+    # dW_A summed against the wrong token of dz
+    "grad_wa_token": ("acc += X[(b * N + n) * D + d] * dz[(b * H + h) * N + n];",
+                      "acc += X[(b * N + n) * D + d] * dz[(b * H + h) * N + (N - 1 - n)];"),
+}
+
 
 def _build_mutant(tmp_path, name):
-    old, new = MUTANTS[name]
+    old, new = MUTANTS[name] if name in MUTANTS else BACKWARD_MUTANTS[name]
     src = open(SRC).read()
     assert src.count(old) >= 1, name
     d = tmp_path / name
@@ -86,6 +110,38 @@ def _pins_fail():
     return failed > 0
 
 
+def _backward_pins_fail():
+    import test_oracle_backward_pins as P
+    checks = [
+        lambda: P.test_gradients_match_finite_differences(1, 5, 6, 3, "direct"),
+        lambda: P.test_gradients_match_finite_differences(1, 5, 6, 3, "fft"),
+        lambda: P.test_dzstar_matches_finite_differences(5),
+        lambda: P.test_softmax_backward_matches_finite_differences(3),
+        lambda: P.test_transpose_brute_force(8),
+        lambda: P.test_correlation_by_roll(6),
+        P.test_dense_contractions_match_library_matmul,
+    ]
+    failed = 0
+    for c in checks:
+        try:
+            c()
+        except AssertionError:
+            failed += 1
+    return failed > 0
+
+
+@pytest.mark.parametrize("name", sorted(BACKWARD_MUTANTS))
+def test_backward_pins_catch_mutant(tmp_path, name):
+    if shutil.which("gcc") is None:
+        pytest.skip("gcc not available")
+    lib = _build_mutant(tmp_path, name)
+    saved = _with_lib(lib)
+    try:
+        assert _backward_pins_fail(), "mutant %s passed every backward pin" % name
+    finally:
+        oracle._LIB = saved
+
+
 @pytest.mark.parametrize("name", sorted(MUTANTS))
 def test_pins_catch_mutant(tmp_path, name):
     if shutil.which("gcc") is None:
@@ -109,5 +165,6 @@ def test_unmutated_copy_passes_pins(tmp_path):
     saved = _with_lib(str(lib))
     try:
         assert not _pins_fail()
+        assert not _backward_pins_fail()
     finally:
         oracle._LIB = saved
