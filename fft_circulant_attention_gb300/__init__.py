@@ -1,4 +1,5 @@
-"""Python binding of libcat, the GB300 CAT forward library (include/cat.h).
+"""Python binding of libcat, the GB300 CAT library (include/cat.h): the
+forward pass and its backward pass.
 
 CAT (circular-convolutional attention), from the notes page "CAT:
 Circular-Convolutional Attention for Sub-Quadratic Transformers", section
@@ -11,7 +12,8 @@ CUDA kernels of ``libcat.so``; there is no other implementation behind it,
 and importing it fails loudly when the library has not been built.
 
 The functions carry the C names: ``cat_plan_create``, ``cat_forward``,
-``cat_forward_zstar``, ``cat_forward_host``, ``cat_plan_sync``,
+``cat_forward_zstar``, ``cat_forward_host``, ``cat_backward``,
+``cat_backward_dz``, ``cat_plan_sync``,
 ``cat_plan_timing``, ``cat_plan_stage_times``, ``cat_plan_pass_times``,
 ``cat_plan_describe``, ``cat_plan_set_stream``, ``cat_plan_destroy`` and
 ``cat_status_string``.  ``Plan`` wraps them for convenience.
@@ -51,6 +53,8 @@ SIGNATURES = {
     "cat_plan_pass_times": (_I, [_P, ctypes.POINTER(ctypes.c_float), _I,
                                  ctypes.POINTER(_I)]),
     "cat_forward_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
+    "cat_backward": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I]),
+    "cat_backward_dz": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I]),
     "cat_status_string": (ctypes.c_char_p, [_I]),
 }
 
@@ -164,6 +168,16 @@ def cat_forward_noalloc(X, W_A, V, O, B, N, D, H, dtype, stream=None):
                                      dtype_code(dtype), _stream(stream)), "cat_forward_noalloc")
 
 
+def cat_backward(plan, X, W_A, V, dO, dX, dW_A, dV, B, N, D, H, dtype):
+    _check(lib().cat_backward(plan, _ptr(X), _ptr(W_A), _ptr(V), _ptr(dO), _ptr(dX), _ptr(dW_A),
+                              _ptr(dV), B, N, D, H, dtype_code(dtype)), "cat_backward")
+
+
+def cat_backward_dz(plan, X, W_A, V, dO, dzstar, dz, B, N, D, H, dtype):
+    _check(lib().cat_backward_dz(plan, _ptr(X), _ptr(W_A), _ptr(V), _ptr(dO), _ptr(dzstar),
+                                 _ptr(dz), B, N, D, H, dtype_code(dtype)), "cat_backward_dz")
+
+
 def cat_plan_sync(plan):
     _check(lib().cat_plan_sync(plan), "cat_plan_sync")
 
@@ -231,6 +245,27 @@ class Plan:
         cat_forward_zstar(self.handle, X, W_A, out, *self._shape())
         return out
 
+    def backward(self, X, W_A, V, dO, dX=None, dW_A=None, dV=None):
+        """Gradients (dX, dW_A, dV) for the upstream gradient dO = dL/dO."""
+        import torch
+        dX = torch.empty_like(X) if dX is None else dX
+        dW_A = torch.empty_like(W_A) if dW_A is None else dW_A
+        dV = torch.empty_like(V) if dV is None else dV
+        for t in (X, W_A, V, dO, dX, dW_A, dV):
+            if not t.is_contiguous() or t.dtype != self.torch_dtype:
+                raise ValueError("tensors must be contiguous %s" % self.torch_dtype)
+        cat_backward(self.handle, X, W_A, V, dO, dX, dW_A, dV, *self._shape())
+        return dX, dW_A, dV
+
+    def backward_dz(self, X, W_A, V, dO):
+        """(dL/dz*, dL/dz), each fp32 [B, H, N]."""
+        import torch
+        shape = (self.B, self.H, self.N)
+        dzs = torch.empty(shape, dtype=torch.float32, device=X.device)
+        dz = torch.empty(shape, dtype=torch.float32, device=X.device)
+        cat_backward_dz(self.handle, X, W_A, V, dO, dzs, dz, *self._shape())
+        return dzs, dz
+
     def forward_host(self, X, W_A, V, O):
         cat_forward_host(self.handle, X, W_A, V, O, *self._shape())
         return O
@@ -271,6 +306,6 @@ class Plan:
 __all__ = ["CatError", "Plan", "lib", "dtype_code", "cat_plan_create", "cat_plan_destroy",
            "cat_plan_set_stream", "cat_forward", "cat_forward_zstar", "cat_forward_host",
            "cat_plan_sync", "cat_plan_describe", "cat_plan_timing", "cat_plan_stage_times",
-           "cat_plan_pass_times", "cat_forward_noalloc",
+           "cat_plan_pass_times", "cat_forward_noalloc", "cat_backward", "cat_backward_dz",
            "cat_status_string", "CAT_F32", "CAT_BF16",
            "SIGNATURES", "LIB_PATH"]

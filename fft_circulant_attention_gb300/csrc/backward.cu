@@ -1,0 +1,532 @@
+// Backward pass of CAT.  The notes page "CAT: Circular-Convolutional
+// Attention for Sub-Quadratic Transformers" trains CAT layers with the usual
+// losses and optimisers (section 损失函数 / 训练策略) but gives no gradient
+// formulas; these follow from the forward definitions of section 方法详解
+// by the chain rule.  With G = dL/dO the upstream gradient:
+//
+//   dV   = circ(z*)^T G                  (the forward's circulant product with
+//                                         the scores reversed, see below)
+//   dz*[h, k] = sum_{c in h} sum_i G[i, c] V[(i - k) mod N, c]
+//             = Re IFFT( sum_{c in h} FFT(G[:, c]) ⊙ conj(FFT(V[:, c])) )
+//   dz   = z* ⊙ (dz* - <z*, dz*>)         (softmax Jacobian)
+//   dW_A = X^T dz,   dX = dz W_A^T
+//
+// Correlation.  Columns (c, c+1) are packed as complex signals g = G_c +
+// i G_{c+1} and v = V_c + i V_{c+1}.  Then FFT(g)·conj(FFT(v)) = Y_c + Y_{c+1}
+// + i (FFT(G_{c+1})conj(FFT(V_c)) - FFT(G_c)conj(FFT(V_{c+1}))), where Y_c is
+// the spectrum of column c's (real) correlation; the bracket is the spectrum
+// of a real signal too, so after the inverse transform the cross terms are
+// purely imaginary and the real part is the sum of both columns'
+// correlations.  The sum over a head's pairs is taken on the spectra, so each
+// (b, h) needs one inverse transform.
+//
+// The transforms use the four-step split N = N1·N2 (n = n1 + N1·n2,
+// k = N2·k1 + k2) of the long-sequence forward path, or N1 = N, N2 = 1 for
+// short rows:
+//   pass A (per n1): length-N2 DFTs of every G and V pair, twiddle
+//     w_N^{n1 k2}, into scratch [bh][k2][n1][q] (q < npair: G pairs,
+//     q >= npair: V pairs);
+//   pass B (per k2): length-N1 DFTs give both spectra at bins N2 k1 + k2;
+//     sum over pairs of FFT(g)·conj(FFT(v)); inverse DFT over k1; conjugate
+//     twiddle; into scratch signal 0;
+//   pass C (per n1): inverse DFT over k2; real part / N is dz*.
+#include <cuda_bf16.h>
+
+#include "cat_internal.h"
+#include "elem.cuh"
+
+namespace cat {
+
+// ---------------------------------------------------------------------------
+// dV: circ(z*)^T = circ(r) with r[n] = z*[(-n) mod N].  The softmax commutes
+// with any permutation of the tokens, so reversing the scores
+// z[n] -> z[(-n) mod N] makes the forward's spectrum and product kernels
+// compute circ(z*)^T·G.  In place: entries n and N - n swap, 1 <= n < N - n.
+// ---------------------------------------------------------------------------
+__global__ void reverse_scores_kernel(float2* __restrict__ z, int N, long long items) {
+  const int half = (N - 1) / 2;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < items;
+       i += (long long)gridDim.x * blockDim.x) {
+    const long long row = i / half;
+    const int n = 1 + (int)(i - row * half);
+    float2* r = z + row * (long long)N;
+    const float2 a = r[n], b = r[N - n];
+    r[n] = b;
+    r[N - n] = a;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Correlation pass A.  blockIdx.x = (bhl · (N1/TA) + tile) · groups + grp.
+// Shared layout: signal (t, s) at buf[(t·S + s)·N2], S = 2·gc; s < gc are
+// G pairs g0 + s, s >= gc the V pairs g0 + s - gc.
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(1024)
+corr_pass_a(const T* __restrict__ G, const T* __restrict__ V, float2* __restrict__ scr,
+            const float2* __restrict__ W, RadixPlan rp2, int N, int N1, int D, int H, int dh,
+            int npair, int GA, int groups, int TA, int Q, int bh0, unsigned int* status) {
+  extern __shared__ float2 buf[];
+  const int N2 = rp2.L;
+  const int ntile = N1 / TA;
+  int r = blockIdx.x;
+  const int grp = r % groups; r /= groups;
+  const int tile = r % ntile;
+  const int bhl = r / ntile;
+  const int bh = bh0 + bhl;
+  const int b = bh / H, h = bh - b * H;
+  const int g0 = grp * GA;
+  const int gc = min(GA, npair - g0);
+  if (gc <= 0) return;
+  const int S = 2 * gc;
+  const int count = TA * S;
+  if (count * N2 > vals_capacity(rp2) * (int)blockDim.x) {
+    report(status, 0x601);
+    return;
+  }
+  const int n1_0 = tile * TA;
+  const int col0 = h * dh + 2 * g0;
+  const bool full_pairs = (2 * (g0 + gc) <= dh);
+  const bool aligned = ((col0 & 1) == 0) && ((D & 1) == 0);   // even column, even row length
+  const size_t boff = (size_t)b * N * D;
+
+  // Load: s fastest (a row's G pairs, then its V pairs), then t, then n2.
+  const int total = count * N2;
+  for (int idx = threadIdx.x; idx < total; idx += blockDim.x) {
+    const int s = idx % S, q = idx / S;
+    const int t = q % TA, n2 = q / TA;
+    const int n = n1_0 + t + N1 * n2;
+    const bool isv = s >= gc;
+    const int g = isv ? s - gc : s;
+    const T* src = (isv ? V : G) + boff + (size_t)n * D + col0 + 2 * g;
+    float2 v;
+    if (full_pairs && aligned) {
+      v = ld_pair(src);
+    } else {
+      v.x = ld_elem(src);
+      v.y = (2 * (g0 + g) + 1 < dh) ? ld_elem(src + 1) : 0.f;
+    }
+    buf[(t * S + s) * N2 + n2] = v;
+  }
+  __syncthreads();
+  block_fft<false>(buf, rp2, count, N2, W, N1);
+
+  float2* srow = scr + (size_t)bhl * N * Q;
+  for (int idx = threadIdx.x; idx < total; idx += blockDim.x) {
+    const int s = idx % S, q = idx / S;
+    const int t = q % TA, k2 = q / TA;
+    const int n1 = n1_0 + t;
+    const float2 v = cmul(buf[(t * S + s) * N2 + k2], __ldg(&W[(size_t)n1 * k2]));
+    const int qi = s < gc ? g0 + s : npair + g0 + (s - gc);
+    srow[((size_t)k2 * N1 + n1) * Q + qi] = v;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Correlation pass B.  blockIdx.x = bhl · (N2/TB) + tile.  The head's pairs
+// go through in chunks of GB: signal (t, s) of a chunk at buf[(t·S + s)·N1]
+// (S = 2·gc: G pairs, then V pairs); the running sum of FFT(g)·conj(FFT(v))
+// for k2-slot t at acc[t·N1 + k1], after the chunk buffer.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(1024)
+corr_pass_b(float2* __restrict__ scr, const float2* __restrict__ W, RadixPlan rp1, int N,
+            int N2, int npair, int GB, int TB, int Q, unsigned int* status) {
+  extern __shared__ float2 buf[];
+  const int N1 = rp1.L;
+  const int ntile = N2 / TB;
+  const int tile = blockIdx.x % ntile;
+  const int bhl = blockIdx.x / ntile;
+  const int k2_0 = tile * TB;
+  if (TB * 2 * GB * N1 > vals_capacity(rp1) * (int)blockDim.x ||
+      TB * N1 > vals_capacity(rp1) * (int)blockDim.x) {
+    report(status, 0x602);
+    return;
+  }
+  float2* acc = buf + (size_t)TB * 2 * GB * N1;
+  float2* srow = scr + (size_t)bhl * N * Q;
+  const int npts = TB * N1;
+  for (int i = threadIdx.x; i < npts; i += blockDim.x) acc[i] = make_float2(0.f, 0.f);
+
+  for (int c0 = 0; c0 < npair; c0 += GB) {
+    const int gc = min(GB, npair - c0);
+    const int S = 2 * gc;
+    const int total = TB * S * N1;
+    __syncthreads();   // the previous chunk's reads of buf are done
+    for (int idx = threadIdx.x; idx < total; idx += blockDim.x) {
+      const int s = idx % S, q = idx / S;
+      const int n1 = q % N1, t = q / N1;
+      const int k2 = k2_0 + t;
+      const int qi = s < gc ? c0 + s : npair + c0 + (s - gc);
+      buf[(t * S + s) * N1 + n1] = srow[((size_t)k2 * N1 + n1) * Q + qi];
+    }
+    __syncthreads();
+    block_fft<false>(buf, rp1, TB * S, N1, W, N2);
+    for (int idx = threadIdx.x; idx < npts; idx += blockDim.x) {
+      const int k1 = idx % N1, t = idx / N1;
+      float2 a = acc[idx];
+      for (int s = 0; s < gc; ++s)
+        a = cadd(a, cmulc(buf[(t * S + s) * N1 + k1], buf[(t * S + gc + s) * N1 + k1]));
+      acc[idx] = a;
+    }
+  }
+  __syncthreads();
+  block_fft<true>(acc, rp1, TB, N1, W, N2);
+
+  // Conjugate twiddle w_N^{-n1 k2}; the result goes to scratch signal 0
+  // (this CTA's k2 slots have been read in full).
+  for (int idx = threadIdx.x; idx < npts; idx += blockDim.x) {
+    const int n1 = idx % N1, t = idx / N1;
+    const int k2 = k2_0 + t;
+    srow[((size_t)k2 * N1 + n1) * Q] = cmulc(acc[idx], __ldg(&W[(size_t)n1 * k2]));
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Correlation pass C.  blockIdx.x = bhl · (N1/TC) + tile.  Inverse DFT over
+// k2 of scratch signal 0 for TC values of n1; dz*[n1 + N1 n2] = Re / N.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(1024)
+corr_pass_c(const float2* __restrict__ scr, float* __restrict__ dzs,
+            const float2* __restrict__ W, RadixPlan rp2, int N, int N1, int TC, int Q, int bh0,
+            unsigned int* status) {
+  extern __shared__ float2 buf[];
+  const int N2 = rp2.L;
+  const int ntile = N1 / TC;
+  const int tile = blockIdx.x % ntile;
+  const int bhl = blockIdx.x / ntile;
+  if (TC * N2 > vals_capacity(rp2) * (int)blockDim.x) {
+    report(status, 0x603);
+    return;
+  }
+  const int n1_0 = tile * TC;
+  const float2* srow = scr + (size_t)bhl * N * Q;
+  const int total = TC * N2;
+  for (int idx = threadIdx.x; idx < total; idx += blockDim.x) {
+    const int t = idx % TC, k2 = idx / TC;
+    buf[t * N2 + k2] = srow[((size_t)k2 * N1 + n1_0 + t) * Q];
+  }
+  __syncthreads();
+  block_fft<true>(buf, rp2, TC, N2, W, N1);
+  const float invN = 1.0f / (float)N;
+  float* out = dzs + (size_t)(bh0 + bhl) * N;
+  for (int idx = threadIdx.x; idx < total; idx += blockDim.x) {
+    const int t = idx % TC, n2 = idx / TC;
+    out[n1_0 + t + (size_t)N1 * n2] = buf[t * N2 + n2].x * invN;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Softmax backward, one CTA per (b, h) row: s = sum_m z*[m] dz*[m] (fp32 per
+// thread, the threads' partial sums added in fp64 in a fixed order), then
+// dz[n] = z*[n] (dz*[n] - s).
+// ---------------------------------------------------------------------------
+constexpr int kSmBwThreads = 1024;
+
+__global__ void __launch_bounds__(kSmBwThreads)
+softmax_bw_kernel(const float* __restrict__ zs, const float* __restrict__ dzs,
+                  float* __restrict__ dz, int N) {
+  __shared__ double red[kSmBwThreads / 32];
+  const size_t off = (size_t)blockIdx.x * N;
+  float part = 0.f;
+  for (int n = threadIdx.x; n < N; n += blockDim.x) part = fmaf(zs[off + n], dzs[off + n], part);
+  double s = part;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nw = (blockDim.x + 31) >> 5;
+  if (lane == 0) red[warp] = s;
+  __syncthreads();
+  double tot = 0.0;
+  for (int w = 0; w < nw; ++w) tot += red[w];
+  const float sf = (float)tot;
+  for (int n = threadIdx.x; n < N; n += blockDim.x) dz[off + n] = zs[off + n] * (dzs[off + n] - sf);
+}
+
+// ---------------------------------------------------------------------------
+// dW_A[d, h] = sum over tokens of X[t, d] dz[h, t]: each CTA takes a range of
+// tokens (split), 1024 columns d (4 consecutive per thread) and 16 heads,
+// and writes its partial sums to part[split][h][d]; dwa_reduce adds the
+// splits in order.
+// ---------------------------------------------------------------------------
+constexpr int kDwThreads = 256, kDwDpt = 4, kDwH = 16, kDwTok = 32;
+
+// Four consecutive elements of a row starting at column d0 (d0 % 4 == 0);
+// `left` columns remain in the row.  vec: the row length is a multiple of 4,
+// so the four are one aligned vector.
+__device__ __forceinline__ void ld4(const float* p, int left, bool vec, float* x) {
+  if (vec) {
+    const float4 v = __ldg(reinterpret_cast<const float4*>(p));
+    x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+  } else {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) x[j] = j < left ? __ldg(p + j) : 0.f;
+  }
+}
+__device__ __forceinline__ void ld4(const __nv_bfloat16* p, int left, bool vec, float* x) {
+  if (vec) {
+    const uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
+    x[0] = __uint_as_float(u.x << 16);
+    x[1] = __uint_as_float(u.x & 0xffff0000u);
+    x[2] = __uint_as_float(u.y << 16);
+    x[3] = __uint_as_float(u.y & 0xffff0000u);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) x[j] = j < left ? ld_elem(p + j) : 0.f;
+  }
+}
+__device__ __forceinline__ void st4(float* p, int left, bool vec, const float* x) {
+  if (vec) {
+    *reinterpret_cast<float4*>(p) = make_float4(x[0], x[1], x[2], x[3]);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (j < left) p[j] = x[j];
+  }
+}
+__device__ __forceinline__ void st4(__nv_bfloat16* p, int left, bool vec, const float* x) {
+  if (vec) {
+    const __nv_bfloat162 a = __floats2bfloat162_rn(x[0], x[1]);
+    const __nv_bfloat162 b = __floats2bfloat162_rn(x[2], x[3]);
+    uint2 u;
+    u.x = *reinterpret_cast<const unsigned int*>(&a);
+    u.y = *reinterpret_cast<const unsigned int*>(&b);
+    *reinterpret_cast<uint2*>(p) = u;
+  } else {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (j < left) st_elem(p + j, x[j]);
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kDwThreads)
+dwa_partial_kernel(const T* __restrict__ X, const float* __restrict__ dz, float* __restrict__ part,
+                   int N, int D, int H, long long tokens, long long tps) {
+  __shared__ __align__(16) float dzs[kDwTok][kDwH];
+  const int split = blockIdx.x;
+  const int d0 = (blockIdx.y * kDwThreads + threadIdx.x) * kDwDpt;
+  const int h0 = blockIdx.z * kDwH;
+  const int hc = min(kDwH, H - h0);
+  const long long t_begin = (long long)split * tps;
+  const long long t_end = min(tokens, t_begin + tps);
+  const bool vec = (D & 3) == 0;
+  float acc[kDwDpt][kDwH];
+#pragma unroll
+  for (int j = 0; j < kDwDpt; ++j)
+#pragma unroll
+    for (int q = 0; q < kDwH; ++q) acc[j][q] = 0.f;
+
+  for (long long t0 = t_begin; t0 < t_end; t0 += kDwTok) {
+    __syncthreads();
+    for (int i = threadIdx.x; i < kDwTok * kDwH; i += kDwThreads) {
+      const int tl = i % kDwTok, hl = i / kDwTok;
+      const long long t = t0 + tl;
+      float v = 0.f;
+      if (t < t_end && hl < hc) {
+        const long long b = t / N, n = t - b * N;
+        v = dz[((size_t)b * H + h0 + hl) * N + n];
+      }
+      dzs[tl][hl] = v;
+    }
+    __syncthreads();
+    const int nt = (int)min((long long)kDwTok, t_end - t0);
+    if (d0 < D) {
+      for (int tl = 0; tl < nt; ++tl) {
+        float x[kDwDpt];
+        ld4(X + (size_t)(t0 + tl) * D + d0, D - d0, vec, x);
+        const float4* zr = reinterpret_cast<const float4*>(&dzs[tl][0]);
+#pragma unroll
+        for (int q = 0; q < kDwH / 4; ++q) {
+          const float4 z = zr[q];
+#pragma unroll
+          for (int j = 0; j < kDwDpt; ++j) {
+            acc[j][4 * q + 0] = fmaf(x[j], z.x, acc[j][4 * q + 0]);
+            acc[j][4 * q + 1] = fmaf(x[j], z.y, acc[j][4 * q + 1]);
+            acc[j][4 * q + 2] = fmaf(x[j], z.z, acc[j][4 * q + 2]);
+            acc[j][4 * q + 3] = fmaf(x[j], z.w, acc[j][4 * q + 3]);
+          }
+        }
+      }
+    }
+  }
+  if (d0 >= D) return;
+#pragma unroll
+  for (int q = 0; q < kDwH; ++q) {
+    if (q < hc) {
+      float v[kDwDpt];
+#pragma unroll
+      for (int j = 0; j < kDwDpt; ++j) v[j] = acc[j][q];
+      st4(part + ((size_t)split * H + h0 + q) * D + d0, D - d0, vec, v);
+    }
+  }
+}
+
+template <typename T>
+__global__ void dwa_reduce_kernel(const float* __restrict__ part, T* __restrict__ dWA, int nsplit,
+                                  int D, int H) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;   // i = h·D + d
+  if (i >= D * H) return;
+  float s = 0.f;
+  for (int k = 0; k < nsplit; ++k) s += part[(size_t)k * H * D + i];
+  const int h = i / D, d = i - h * D;
+  st_elem(dWA + (size_t)d * H + h, s);
+}
+
+// ---------------------------------------------------------------------------
+// dX[t, d] = sum_h dz[h, t] W_A[d, h]: each CTA takes 16 tokens and 1024
+// columns (4 consecutive per thread); heads go through 16 at a time with
+// W_A's slice in registers and dz's in shared memory.
+// ---------------------------------------------------------------------------
+constexpr int kDxThreads = 256, kDxDpt = 4, kDxTok = 16, kDxH = 16;
+
+template <typename T>
+__global__ void __launch_bounds__(kDxThreads)
+dx_kernel(const float* __restrict__ dz, const T* __restrict__ WA, T* __restrict__ dX, int N, int D,
+          int H, long long tokens) {
+  __shared__ __align__(16) float dzs[kDxTok][kDxH];
+  const long long t0 = (long long)blockIdx.x * kDxTok;
+  const int d0 = (blockIdx.y * kDxThreads + threadIdx.x) * kDxDpt;
+  const int nt = (int)min((long long)kDxTok, tokens - t0);
+  const bool vec = (D & 3) == 0;
+  float acc[kDxTok][kDxDpt];
+#pragma unroll
+  for (int t = 0; t < kDxTok; ++t)
+#pragma unroll
+    for (int j = 0; j < kDxDpt; ++j) acc[t][j] = 0.f;
+
+  for (int h0 = 0; h0 < H; h0 += kDxH) {
+    const int hc = min(kDxH, H - h0);
+    __syncthreads();
+    for (int i = threadIdx.x; i < kDxTok * kDxH; i += kDxThreads) {
+      const int tl = i % kDxTok, hl = i / kDxTok;
+      float v = 0.f;
+      if (tl < nt && hl < hc) {
+        const long long t = t0 + tl;
+        const long long b = t / N, n = t - b * N;
+        v = dz[((size_t)b * H + h0 + hl) * N + n];
+      }
+      dzs[tl][hl] = v;
+    }
+    __syncthreads();
+    if (d0 < D) {
+      float w[kDxDpt][kDxH];
+#pragma unroll
+      for (int j = 0; j < kDxDpt; ++j)
+#pragma unroll
+        for (int q = 0; q < kDxH; ++q)
+          w[j][q] = (d0 + j < D && q < hc) ? ld_elem(WA + (size_t)(d0 + j) * H + h0 + q) : 0.f;
+#pragma unroll
+      for (int tl = 0; tl < kDxTok; ++tl) {
+        const float4* zr = reinterpret_cast<const float4*>(&dzs[tl][0]);
+#pragma unroll
+        for (int q = 0; q < kDxH / 4; ++q) {
+          const float4 z = zr[q];
+#pragma unroll
+          for (int j = 0; j < kDxDpt; ++j) {
+            float a = acc[tl][j];
+            a = fmaf(w[j][4 * q + 0], z.x, a);
+            a = fmaf(w[j][4 * q + 1], z.y, a);
+            a = fmaf(w[j][4 * q + 2], z.z, a);
+            a = fmaf(w[j][4 * q + 3], z.w, a);
+            acc[tl][j] = a;
+          }
+        }
+      }
+    }
+  }
+  if (d0 >= D) return;
+#pragma unroll
+  for (int tl = 0; tl < kDxTok; ++tl)
+    if (tl < nt) st4(dX + (size_t)(t0 + tl) * D + d0, D - d0, vec, acc[tl]);
+}
+
+// ---------------------------------------------------------------------------
+// Host launchers (plan's stream).
+// ---------------------------------------------------------------------------
+cudaError_t setup_backward_kernels(const cat_plan_s* p) {
+  cudaError_t e = allow_max_smem(corr_pass_b);
+  if (e == cudaSuccess) e = allow_max_smem(corr_pass_c);
+  if (e == cudaSuccess)
+    e = p->dtype == 1 ? allow_max_smem(corr_pass_a<__nv_bfloat16>) : allow_max_smem(corr_pass_a<float>);
+  return e;
+}
+
+cudaError_t launch_reverse_scores(const cat_plan_s* p) {
+  const int half = (p->N - 1) / 2;
+  const long long items = (long long)p->B * p->H * half;
+  if (items == 0) return cudaSuccess;
+  long long blocks = (items + 255) / 256;
+  if (blocks > 8 * (long long)p->sms) blocks = 8 * (long long)p->sms;
+  reverse_scores_kernel<<<(int)blocks, 256, 0, p->stream>>>(p->z2, p->N, items);
+  return cudaGetLastError();
+}
+
+template <typename T>
+static cudaError_t corr_t(const cat_plan_s* p, const T* G, const T* V) {
+  const BwCfg& w = p->bw;
+  const int rows = p->B * p->H;
+  for (int bh0 = 0; bh0 < rows; bh0 += w.chunk_bh) {
+    const int nb = rows - bh0 < w.chunk_bh ? rows - bh0 : w.chunk_bh;
+    corr_pass_a<T><<<nb * (w.N1 / w.TA) * w.groupsA, w.threadsA, w.smemA, p->stream>>>(
+        G, V, p->bw_scr, p->tw, w.rp2, p->N, w.N1, p->D, p->H, p->dh, p->npair, w.GA, w.groupsA,
+        w.TA, w.Q, bh0, p->status);
+    corr_pass_b<<<nb * (w.N2 / w.TB), w.threadsB, w.smemB, p->stream>>>(
+        p->bw_scr, p->tw, w.rp1, p->N, w.N2, p->npair, w.GB, w.TB, w.Q, p->status);
+    corr_pass_c<<<nb * (w.N1 / w.TC), w.threadsC, w.smemC, p->stream>>>(
+        p->bw_scr, p->bw_dzs, p->tw, w.rp2, p->N, w.N1, w.TC, w.Q, bh0, p->status);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+cudaError_t launch_backward_dz(const cat_plan_s* p, const void* G, const void* V) {
+  const int rows = p->B * p->H;
+  if (rows == 0) return cudaSuccess;
+  const cudaError_t e = p->dtype == 1
+      ? corr_t(p, (const __nv_bfloat16*)G, (const __nv_bfloat16*)V)
+      : corr_t(p, (const float*)G, (const float*)V);
+  if (e != cudaSuccess) return e;
+  softmax_bw_kernel<<<rows, kSmBwThreads, 0, p->stream>>>(p->zs, p->bw_dzs, p->bw_dz, p->N);
+  return cudaGetLastError();
+}
+
+template <typename T>
+static cudaError_t dense_t(const cat_plan_s* p, const T* X, const T* WA, T* dX, T* dWA) {
+  const BwCfg& w = p->bw;
+  const long long tokens = (long long)p->B * p->N;
+  const int dchunks = (p->D + kDwThreads * kDwDpt - 1) / (kDwThreads * kDwDpt);
+  const int hchunks = (p->H + kDwH - 1) / kDwH;
+  const long long tps = (tokens + w.wsplit - 1) / w.wsplit;
+  dim3 gw(w.wsplit, dchunks, hchunks);
+  dwa_partial_kernel<T><<<gw, kDwThreads, 0, p->stream>>>(X, p->bw_dz, p->bw_wpart, p->N, p->D,
+                                                          p->H, tokens, tps);
+  const int dh_items = p->D * p->H;
+  dwa_reduce_kernel<T><<<(dh_items + 255) / 256, 256, 0, p->stream>>>(p->bw_wpart, dWA, w.wsplit,
+                                                                      p->D, p->H);
+  dim3 gx((unsigned)((tokens + kDxTok - 1) / kDxTok), (p->D + kDxThreads * kDxDpt - 1) /
+                                                          (kDxThreads * kDxDpt));
+  dx_kernel<T><<<gx, kDxThreads, 0, p->stream>>>(p->bw_dz, WA, dX, p->N, p->D, p->H, tokens);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_backward_dense(const cat_plan_s* p, const void* X, const void* WA, void* dX,
+                                  void* dWA) {
+  if (p->B == 0) return cudaSuccess;
+  if (p->dtype == 1)
+    return dense_t(p, (const __nv_bfloat16*)X, (const __nv_bfloat16*)WA, (__nv_bfloat16*)dX,
+                   (__nv_bfloat16*)dWA);
+  return dense_t(p, (const float*)X, (const float*)WA, (float*)dX, (float*)dWA);
+}
+
+int backward_wsplit(long long tokens, int D, int H, int sms) {
+  const int dchunks = (D + kDwThreads * kDwDpt - 1) / (kDwThreads * kDwDpt);
+  const int hchunks = (H + kDwH - 1) / kDwH;
+  long long s = 2ll * sms / ((long long)dchunks * hchunks);
+  const long long most = (tokens + kDwTok - 1) / kDwTok;
+  if (s > most) s = most;
+  if (s < 1) s = 1;
+  return (int)s;
+}
+
+}  // namespace cat

@@ -145,6 +145,10 @@ void free_plan(cat_plan_s* p) {
   cudaFree(p->zscr);
   cudaFree(p->tabs);
   cudaFree(p->status);
+  cudaFree(p->bw_scr);
+  cudaFree(p->bw_dzs);
+  cudaFree(p->bw_dz);
+  cudaFree(p->bw_wpart);
   cudaFree(p->hx);
   cudaFree(p->hwa);
   cudaFree(p->hv);
@@ -288,6 +292,102 @@ int run_front(cat_plan_s* p, const void* X, const void* WA) {
   return map_cuda(e);
 }
 
+
+// Launch shapes of the backward correlation (host only, no allocation).
+// Rows up to 4096 are transformed whole in pass B (N1 = N, N2 = 1); longer
+// ones use the four-step split of the long-sequence forward path.
+int configure_backward(cat_plan_s* p) {
+  cat::BwCfg& w = p->bw;
+  std::memset(&w, 0, sizeof(w));
+  const int N = p->N;
+  if (N <= 4096) {
+    w.N1 = N;
+    w.N2 = 1;
+  } else if (!split_fourstep(N, &w.N1, &w.N2)) {
+    return CAT_ERR_UNSUPPORTED_N;
+  }
+  if (!make_radix_plan(w.N1, &w.rp1) || !make_radix_plan(w.N2, &w.rp2))
+    return CAT_ERR_UNSUPPORTED_N;
+  const size_t c8 = sizeof(float2);
+  const int np = p->npair;
+  w.Q = 2 * np;
+  // Pass A: up to 16 pairs (32 signals) per CTA, then as many n1 as fit.
+  int gmax = (int)(kFsSmemBudget / (2 * (size_t)w.N2 * c8));
+  if (gmax > 16) gmax = 16;
+  if (gmax < 1) return CAT_ERR_UNSUPPORTED_N;
+  split_pairs(np, gmax, &w.GA, &w.groupsA);
+  w.TA = 1;
+  for (int t = 2; t <= 64; ++t)
+    if (w.N1 % t == 0 && (size_t)t * 2 * w.GA * w.N2 * c8 <= kFsSmemBudget) w.TA = t;
+  w.smemA = (size_t)w.TA * 2 * w.GA * w.N2 * c8;
+  w.threadsA = fft_threads((long)w.TA * 2 * w.GA, w.N2);
+  // Pass B: chunks of up to 8 pairs plus the accumulator, TB k2 per CTA.
+  w.GB = np < 8 ? np : 8;
+  w.TB = 0;
+  for (; w.GB >= 1 && !w.TB; --w.GB) {
+    for (int t = 1; t <= 64; ++t)
+      if (w.N2 % t == 0 && (size_t)t * (2 * w.GB + 1) * w.N1 * c8 <= kFsSmemBudget) w.TB = t;
+    if (w.TB) break;
+  }
+  if (w.GB < 1 || !w.TB) return CAT_ERR_UNSUPPORTED_N;
+  w.smemB = (size_t)w.TB * (2 * w.GB + 1) * w.N1 * c8;
+  w.threadsB = fft_threads((long)w.TB * 2 * w.GB, w.N1);
+  // Pass C: one signal per n1, TC n1 per CTA.
+  w.TC = 1;
+  for (int t = 2; t <= 64; ++t)
+    if (w.N1 % t == 0 && (size_t)t * w.N2 * c8 <= kFsSmemBudget) w.TC = t;
+  w.smemC = (size_t)w.TC * w.N2 * c8;
+  w.threadsC = fft_threads(w.TC, w.N2);
+  if ((long)w.TA * 2 * w.GA * w.N2 > (long)cat::vals_capacity(w.rp2) * w.threadsA ||
+      (long)w.TB * 2 * w.GB * w.N1 > (long)cat::vals_capacity(w.rp1) * w.threadsB ||
+      (long)w.TB * w.N1 > (long)cat::vals_capacity(w.rp1) * w.threadsB ||
+      (long)w.TC * w.N2 > (long)cat::vals_capacity(w.rp2) * w.threadsC)
+    return CAT_ERR_UNSUPPORTED_N;
+  const size_t per_bh = (size_t)N * w.Q * c8;
+  long chunk = (long)(kScratchBudget / per_bh);
+  if (chunk < 1) chunk = 1;
+  const long rows = (long)p->B * p->H;
+  if (chunk > rows) chunk = rows > 0 ? rows : 1;
+  w.chunk_bh = (int)chunk;
+  w.scratch_bytes = (size_t)w.chunk_bh * per_bh;
+  w.wsplit = cat::backward_wsplit((long long)p->B * N, p->D, p->H, p->sms > 0 ? p->sms : 148);
+  return CAT_OK;
+}
+
+// Configure and allocate the backward workspace at the first backward call.
+int ensure_backward(cat_plan_s* p) {
+  if (p->bw_ready) return CAT_OK;
+  int st = configure_backward(p);
+  if (st != CAT_OK) return st;
+  const size_t rowsN = (size_t)p->B * p->H * p->N;
+  auto alloc = [&](void** ptr, size_t bytes) {
+    if (bytes == 0) bytes = 16;
+    return cudaMalloc(ptr, bytes) == cudaSuccess;
+  };
+  bool ok = alloc((void**)&p->bw_scr, p->bw.scratch_bytes) &&
+            alloc((void**)&p->bw_dzs, rowsN * sizeof(float)) &&
+            alloc((void**)&p->bw_dz, rowsN * sizeof(float)) &&
+            alloc((void**)&p->bw_wpart, (size_t)p->bw.wsplit * p->H * p->D * sizeof(float));
+  if (!ok) {
+    cudaGetLastError();
+    cudaFree(p->bw_scr); cudaFree(p->bw_dzs); cudaFree(p->bw_dz); cudaFree(p->bw_wpart);
+    p->bw_scr = nullptr; p->bw_dzs = p->bw_dz = p->bw_wpart = nullptr;
+    return CAT_ERR_ALLOC;
+  }
+  if (cat::setup_backward_kernels(p) != cudaSuccess) return CAT_ERR_CUDA;
+  p->bw_ready = 1;
+  return CAT_OK;
+}
+
+// Score and softmax into the plan (z* in zs on every path), then the
+// correlation and the softmax backward (dz* and dz in the plan).
+int run_backward_front(cat_plan_s* p, const void* X, const void* WA, const void* V,
+                       const void* G) {
+  cudaError_t e = cat::launch_score(p, X, WA);
+  if (e == cudaSuccess) e = cat::launch_softmax(p);
+  if (e == cudaSuccess) e = cat::launch_backward_dz(p, G, V);
+  return map_cuda(e);
+}
 }  // namespace
 
 namespace cat {
@@ -606,6 +706,72 @@ int cat_forward_host(cat_plan_t p, const void* X, const void* WA, const void* V,
   if (st != CAT_OK) return st;
   e = cudaMemcpyAsync(O, p->ho, nx, cudaMemcpyDeviceToHost, p->stream);
   if (e == cudaSuccess) e = cudaStreamSynchronize(p->stream);
+  return map_cuda(e);
+}
+
+int cat_backward(cat_plan_t p, const void* X, const void* WA, const void* V, const void* dO,
+                 void* dX, void* dWA, void* dV, int B, int N, int D, int H, int dtype) {
+  if (!p) return CAT_ERR_INVALID_ARG;
+  int st = check_shape(p, B, N, D, H, dtype);
+  if (st != CAT_OK) return st;
+  if (B == 0) return CAT_OK;
+  if (!X || !WA || !V || !dO || !dX || !dWA || !dV) return CAT_ERR_INVALID_ARG;
+  if (((uintptr_t)X | (uintptr_t)WA | (uintptr_t)V | (uintptr_t)dO | (uintptr_t)dX |
+       (uintptr_t)dWA | (uintptr_t)dV) & 15)
+    return CAT_ERR_MISALIGNED;
+  const size_t es = dtype == CAT_BF16 ? 2 : 4;
+  const size_t nx = (size_t)B * N * D * es, nw = (size_t)D * H * es;
+  const void* in[4] = {X, WA, V, dO};
+  const size_t in_n[4] = {nx, nw, nx, nx};
+  const void* out[3] = {dX, dWA, dV};
+  const size_t out_n[3] = {nx, nw, nx};
+  for (int o = 0; o < 3; ++o) {
+    for (int i = 0; i < 4; ++i)
+      if (ranges_overlap(out[o], out_n[o], in[i], in_n[i])) return CAT_ERR_ALIAS;
+    for (int q = o + 1; q < 3; ++q)
+      if (ranges_overlap(out[o], out_n[o], out[q], out_n[q])) return CAT_ERR_ALIAS;
+  }
+  st = ensure_backward(p);
+  if (st != CAT_OK) return st;
+  st = run_backward_front(p, X, WA, V, dO);
+  if (st != CAT_OK) return st;
+  cudaError_t e = cat::launch_backward_dense(p, X, WA, dX, dWA);
+  // dV = circ(z*)^T dO: reverse the scores, then the forward's own spectrum
+  // and circulant product on dO.
+  if (e == cudaSuccess) e = cat::launch_reverse_scores(p);
+  if (e == cudaSuccess) {
+    if (p->path == cat::PATH_SMEM) {
+      e = cat::launch_softmax_spectrum(p);
+      if (e == cudaSuccess) e = cat::launch_conv_smem(p, dO, dV);
+    } else if (p->path == cat::PATH_FAST) {
+      e = cat::launch_fast_zspec(p, 0, p->B * p->H, p->stream);
+      if (e == cudaSuccess) e = cat::launch_fast_conv(p, dO, dV);
+    } else {
+      e = cat::launch_softmax(p);
+      if (e == cudaSuccess) e = cat::launch_fourstep_conv(p, dO, dV);
+    }
+  }
+  return map_cuda(e);
+}
+
+int cat_backward_dz(cat_plan_t p, const void* X, const void* WA, const void* V, const void* dO,
+                    float* dzstar, float* dz, int B, int N, int D, int H, int dtype) {
+  if (!p) return CAT_ERR_INVALID_ARG;
+  int st = check_shape(p, B, N, D, H, dtype);
+  if (st != CAT_OK) return st;
+  if (B == 0) return CAT_OK;
+  if (!X || !WA || !V || !dO || !dzstar || !dz) return CAT_ERR_INVALID_ARG;
+  if (((uintptr_t)X | (uintptr_t)WA | (uintptr_t)V | (uintptr_t)dO | (uintptr_t)dzstar |
+       (uintptr_t)dz) & 15)
+    return CAT_ERR_MISALIGNED;
+  st = ensure_backward(p);
+  if (st != CAT_OK) return st;
+  st = run_backward_front(p, X, WA, V, dO);
+  if (st != CAT_OK) return st;
+  const size_t bytes = (size_t)B * H * N * sizeof(float);
+  cudaError_t e = cudaMemcpyAsync(dzstar, p->bw_dzs, bytes, cudaMemcpyDeviceToDevice, p->stream);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(dz, p->bw_dz, bytes, cudaMemcpyDeviceToDevice, p->stream);
   return map_cuda(e);
 }
 

@@ -42,6 +42,25 @@ struct FourStepCfg {
   int chunk_bh;         // (b, h) rows whose scratch is live at once
 };
 
+// Backward correlation dz*[k] = sum_c sum_i G[i, c] V[(i - k) mod N, c] by
+// the four-step split N = N1·N2 (N1 = N, N2 = 1 for short rows).  Scratch
+// row layout per (b, h): [k2][n1][Q] complex, Q = 2·npair signals (G pairs,
+// then V pairs); signal 0 receives the correlation's partial inverse.
+struct BwCfg {
+  int N1, N2;
+  RadixPlan rp1, rp2;
+  int GA, groupsA, TA, threadsA;   // pass A: pairs per CTA, CTAs per (b, h), n1 per CTA
+  size_t smemA;
+  int GB, TB, threadsB;            // pass B: pairs per chunk, k2 per CTA
+  size_t smemB;
+  int TC, threadsC;                // pass C: n1 per CTA
+  size_t smemC;
+  int Q;                           // scratch signals per (b, h) = 2·npair
+  int chunk_bh;                    // (b, h) rows whose scratch is live at once
+  int wsplit;                      // token ranges of the dW_A partial sums
+  size_t scratch_bytes;
+};
+
 }  // namespace cat
 
 struct cat_plan_s {
@@ -88,6 +107,13 @@ struct cat_plan_s {
   int timing_cap, timing_n;
   int ev_per_call;          // events recorded per call (3 + conv pass boundaries)
   int launches;             // kernel launches per cat_forward
+  // backward workspace (configured and allocated at the first backward call)
+  int bw_ready;
+  cat::BwCfg bw;
+  float2* bw_scr;           // correlation scratch, chunk_bh·N·Q complex
+  float* bw_dzs;            // [B, H, N] dL/dz*
+  float* bw_dz;             // [B, H, N] dL/dz
+  float* bw_wpart;          // [wsplit, H, D] partial sums of dW_A
   char desc[512];
 };
 
@@ -175,5 +201,17 @@ cudaError_t setup_smem_kernels(const cat_plan_s* p);
 cudaError_t setup_fourstep_kernels(const cat_plan_s* p);
 cudaError_t setup_fast_kernels(cat_plan_s* p);
 size_t fast_tables_bytes(int N2);
+
+// Backward pass (backward.cu).  launch_backward_dz: correlation passes and
+// softmax backward into bw_dzs and bw_dz (needs z* in zs).
+// launch_backward_dense: dW_A and dX from bw_dz.  launch_reverse_scores:
+// z2[n] <-> z2[(-n) mod N] in every row, so that the forward's spectrum and
+// product kernels then give circ(z*)^T.
+cudaError_t setup_backward_kernels(const cat_plan_s* p);
+cudaError_t launch_backward_dz(const cat_plan_s* p, const void* G, const void* V);
+cudaError_t launch_backward_dense(const cat_plan_s* p, const void* X, const void* WA, void* dX,
+                                  void* dWA);
+cudaError_t launch_reverse_scores(const cat_plan_s* p);
+int backward_wsplit(long long tokens, int D, int H, int sms);
 
 }  // namespace cat

@@ -1,5 +1,6 @@
 /*
- * cat.h — C ABI of the GB300 CAT forward library (libcat.so).
+ * cat.h — C ABI of the GB300 CAT library (libcat.so): the forward pass and
+ * its backward pass.
  *
  * CAT (circular-convolutional attention), as defined on the notes page
  * "CAT: Circular-Convolutional Attention for Sub-Quadratic Transformers",
@@ -124,6 +125,47 @@ int cat_forward_zstar(cat_plan_t plan, const void *X, const void *W_A,
 int cat_forward_host(cat_plan_t plan, const void *X, const void *W_A,
                      const void *V, void *O, int B, int N, int D, int H,
                      int dtype);
+
+/*
+ * cat_backward — gradients of a loss L through the forward pass, given the
+ * upstream gradient dO = dL/dO.  The notes page cited above trains CAT
+ * layers with the usual losses and optimisers (section 损失函数 / 训练策略,
+ * loss and training strategy) but prints no gradients; these follow from
+ * the forward definitions by the chain rule, per (b, h):
+ *   dV   = circ(z*)^T dO          dV[j, c] = sum_i z*[(i - j) mod N] dO[i, c]
+ *   dz*[k] = sum_{c in h} sum_i dO[i, c] V[(i - k) mod N, c]
+ *          = Re IFFT( sum_c FFT(dO[:, c]) ⊙ conj(FFT(V[:, c])) )
+ *   dz   = z* ⊙ (dz* - <z*, dz*>)  (softmax Jacobian)
+ *   dW_A[d, h] = sum_{b, n} X[b, n, d] dz[b, h, n]
+ *   dX[b, n, d] = sum_h dz[b, h, n] W_A[d, h]
+ * z* is recomputed from X and W_A (nothing is kept from a forward call).
+ *
+ * X, W_A, V, dO: device pointers, read only ([B,N,D], [D,H], [B,N,D],
+ * [B,N,D]).  dX [B,N,D], dW_A [D,H], dV [B,N,D]: device pointers, written;
+ * dW_A is overwritten, not accumulated into.  All seven have the plan's
+ * dtype (bf16 gradients are rounded to nearest-even from fp32), must be
+ * 16-byte aligned (CAT_ERR_MISALIGNED), and no output may overlap an input
+ * or another output (CAT_ERR_ALIAS).  Shape arguments must equal the plan's.
+ * The first call configures and allocates the plan's backward workspace
+ * (correlation scratch, dz*, dz, dW_A partial sums), which the plan keeps;
+ * CAT_ERR_ALLOC if that fails.  Asynchronous on the plan's stream; the
+ * plan's forward workspace is reused, so a backward and a forward on one
+ * plan must not run concurrently on different streams.
+ */
+int cat_backward(cat_plan_t plan, const void *X, const void *W_A, const void *V,
+                 const void *dO, void *dX, void *dW_A, void *dV, int B, int N,
+                 int D, int H, int dtype);
+
+/*
+ * cat_backward_dz — only the score-side gradients of cat_backward: writes
+ * dz* = dL/dz* and dz = dL/dz (the softmax backward of dz*), each fp32
+ * [B, H, N], to the device pointers dzstar and dz (16-byte aligned, not
+ * overlapping the inputs or each other).  Inputs and errors as for
+ * cat_backward.
+ */
+int cat_backward_dz(cat_plan_t plan, const void *X, const void *W_A,
+                    const void *V, const void *dO, float *dzstar, float *dz,
+                    int B, int N, int D, int H, int dtype);
 
 /*
  * cat_plan_sync — wait for the plan's stream, then read the device status

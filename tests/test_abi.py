@@ -91,6 +91,10 @@ def test_null_plan_calls(lib):
     ms = (ctypes.c_float * 3)()
     assert lib.cat_plan_stage_times(None, ms, 3, None) == cat.CAT_ERR_INVALID_ARG
     assert lib.cat_plan_pass_times(None, ms, 3, None) == cat.CAT_ERR_INVALID_ARG
+    assert lib.cat_backward(None, None, None, None, None, None, None, None,
+                            1, 16, 64, 2, 0) == cat.CAT_ERR_INVALID_ARG
+    assert lib.cat_backward_dz(None, None, None, None, None, None, None,
+                               1, 16, 64, 2, 0) == cat.CAT_ERR_INVALID_ARG
 
 
 def test_python_raises_caterror(lib):
