@@ -8,7 +8,12 @@ resident in HBM; X + V + O are larger than L2, so no flush is needed
 between steps.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
-                    [--config long16k] [--no-secondary] [--no-short]
+                    [--config long16k] [--no-secondary] [--no-short] [--no-backward]
+                    [--backward-only]
+
+The line also carries the backward pass (cat_backward: dX, dW_A, dV for an
+upstream gradient) at both long-sequence workloads, with its roofline
+fraction; --backward-only times just that on --config.
 
 Prints ONE JSON line (rank 0).  With --impl reference the fp64 CPU oracle
 is timed instead, on a bounded sample of the same workload.
@@ -97,6 +102,20 @@ def algorithmic(c):
     total_bytes = 3 * B * N * D * es + D * H * es
     return dict(conv_flops=conv_flops, total_flops=total_flops, conv_bytes=conv_bytes,
                 total_bytes=total_bytes, score_flops=2.0 * B * N * D * H)
+
+
+def algorithmic_backward(c):
+    """Bytes and FFT flops of one backward: X, V, dO read, dX, dV written (W_A
+    read, dW_A written); transforms of length N: dV's circulant product (a
+    forward and an inverse per packed pair, plus the spectrum of z*) and the
+    correlation (a forward per packed pair of dO and of V, one inverse per
+    (b, h))."""
+    B, N, D, H, es = c["B"], c["N"], c["D"], c["H"], c["es"]
+    npair = (D // H + 1) // 2
+    transforms = 4 * B * H * npair + 2 * B * H
+    return dict(flops=transforms * fft_flops(N),
+                bytes=5 * B * N * D * es + 2 * D * H * es,
+                dense_flops=3 * 2.0 * B * N * D * H)
 
 
 class ClockSampler:
@@ -355,6 +374,42 @@ def measure_workload(name, steps, warmup, device, world, sampler=None):
     }
 
 
+def measure_backward(name, device, reps, warmup=3):
+    """ms per cat_backward (resident inputs and upstream gradient, plan's
+    stream, CUDA events) with its whole-pass roofline fraction."""
+    import fft_circulant_attention_gb300 as cat
+    c = cfg_of(name)
+    X, WA, V = (t.to(device) for t in synth.make_inputs(c["B"], c["N"], c["D"], c["H"],
+                                                         c["dtype"], seed=0))
+    G = synth.make_grad(c["B"], c["N"], c["D"], c["dtype"], seed=0).to(device)
+    dX, dWA, dV = torch.empty_like(X), torch.empty_like(WA), torch.empty_like(V)
+    stream = torch.cuda.current_stream(device)
+    with cat.Plan(c["B"], c["N"], c["D"], c["H"], c["dtype"], stream=stream) as plan:
+        for _ in range(warmup):
+            plan.backward(X, WA, V, G, dX, dWA, dV)
+        plan.sync()
+        torch.cuda.synchronize(device)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            plan.backward(X, WA, V, G, dX, dWA, dV)
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        plan.sync()
+    ms = e0.elapsed_time(e1) / reps
+    a = algorithmic_backward(c)
+    hbm, _ = load_peaks()
+    t_roof = max(a["bytes"] / (hbm * 1e9), a["flops"] / (FP32_PEAK_TFLOPS * 1e12))
+    del X, V, G, dX, dV
+    torch.cuda.empty_cache()
+    return {"workload": name, "B": c["B"], "N": c["N"], "D": c["D"], "H": c["H"],
+            "storage": c["dtype"], "ms_per_step": ms,
+            "value": c["B"] * c["N"] * c["H"] / (ms * 1e-3), "unit": UNIT,
+            "path_roofline_frac": t_roof / (ms * 1e-3), "t_roof_us": t_roof * 1e6,
+            "algorithmic_bytes": a["bytes"], "fft_flops": a["flops"], "reps": reps}
+
+
 # The short-sequence configurations of the workload table (parity cases of
 # the tests; timed here so that every path has a measured figure).
 SHORT = ["tiny", "vit196", "gpt2_f32", "gpt2_bf16"]
@@ -398,12 +453,19 @@ def run_gb300(args, world, rank, local):
     cat.lib()
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
+    if args.backward_only:
+        bw = measure_backward(args.config, device, max(args.steps, 1), args.warmup)
+        if rank == 0:
+            print(json.dumps({"backward": bw}), flush=True)
+        return
     sampler = ClockSampler(local) if rank == 0 else None
     prim = measure_workload(args.config, args.steps, args.warmup, device, world, sampler)
     sec = None
     if not args.no_secondary and args.config != SECONDARY:
         sec = measure_workload(SECONDARY, max(3, args.steps // 4), args.warmup, device, world)
     short = [] if args.no_short else [measure_short(n, device) for n in SHORT]
+    backward = [] if args.no_backward else [
+        measure_backward(n, device, r) for n, r in ((PRIMARY, 20), (SECONDARY, 5))]
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -451,6 +513,8 @@ def run_gb300(args, world, rank, local):
             "e2e": sec["e2e"], "plan": sec["desc"]}
     if short:
         line["short_configs"] = short
+    if backward:
+        line["backward"] = backward
     print(json.dumps(line), flush=True)
 
 
@@ -464,6 +528,9 @@ def main():
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-short", action="store_true")
+    ap.add_argument("--no-backward", action="store_true")
+    ap.add_argument("--backward-only", action="store_true",
+                    help="time only cat_backward on --config (--steps calls) and print it")
     ap.add_argument("--sample-heads", type=int, default=0)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)

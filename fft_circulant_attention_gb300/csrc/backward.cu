@@ -22,7 +22,9 @@
 //
 // The transforms use the four-step split N = N1·N2 (n = n1 + N1·n2,
 // k = N2·k1 + k2) of the long-sequence forward path, or N1 = N, N2 = 1 for
-// short rows:
+// short rows (on the fast path's shapes, its own pass A and the register
+// kernel fsf_corr_b take passes A and B, and pass C below runs on their
+// one-signal result):
 //   pass A (per n1): length-N2 DFTs of every G and V pair, twiddle
 //     w_N^{n1 k2}, into scratch [bh][k2][n1][q] (q < npair: G pairs,
 //     q >= npair: V pairs);
@@ -248,7 +250,8 @@ softmax_bw_kernel(const float* __restrict__ zs, const float* __restrict__ dzs,
 // and writes its partial sums to part[split][h][d]; dwa_reduce adds the
 // splits in order.
 // ---------------------------------------------------------------------------
-constexpr int kDwThreads = 256, kDwDpt = 4, kDwH = 16, kDwTok = 32;
+constexpr int kDwThreads = 256, kDwDpt = 4, kDwH = 16, kDwTok = 32, kDwPre = 8;
+static_assert(kDwTok % kDwPre == 0, "token tile is whole groups of preloads");
 
 // Four consecutive elements of a row starting at column d0 (d0 % 4 == 0);
 // `left` columns remain in the row.  vec: the row length is a multiple of 4,
@@ -331,19 +334,32 @@ dwa_partial_kernel(const T* __restrict__ X, const float* __restrict__ dz, float*
     __syncthreads();
     const int nt = (int)min((long long)kDwTok, t_end - t0);
     if (d0 < D) {
-      for (int tl = 0; tl < nt; ++tl) {
-        float x[kDwDpt];
-        ld4(X + (size_t)(t0 + tl) * D + d0, D - d0, vec, x);
-        const float4* zr = reinterpret_cast<const float4*>(&dzs[tl][0]);
+      // Eight tokens' loads in flight before their products (tokens past
+      // nt read as zero rows and add nothing: dzs is zero there too).
+      for (int tb = 0; tb < nt; tb += kDwPre) {
+        float x[kDwPre][kDwDpt];
 #pragma unroll
-        for (int q = 0; q < kDwH / 4; ++q) {
-          const float4 z = zr[q];
+        for (int u = 0; u < kDwPre; ++u) {
+          if (tb + u < nt) {
+            ld4(X + (size_t)(t0 + tb + u) * D + d0, D - d0, vec, x[u]);
+          } else {
 #pragma unroll
-          for (int j = 0; j < kDwDpt; ++j) {
-            acc[j][4 * q + 0] = fmaf(x[j], z.x, acc[j][4 * q + 0]);
-            acc[j][4 * q + 1] = fmaf(x[j], z.y, acc[j][4 * q + 1]);
-            acc[j][4 * q + 2] = fmaf(x[j], z.z, acc[j][4 * q + 2]);
-            acc[j][4 * q + 3] = fmaf(x[j], z.w, acc[j][4 * q + 3]);
+            for (int j = 0; j < kDwDpt; ++j) x[u][j] = 0.f;
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kDwPre; ++u) {
+          const float4* zr = reinterpret_cast<const float4*>(&dzs[(tb + u) & (kDwTok - 1)][0]);
+#pragma unroll
+          for (int q = 0; q < kDwH / 4; ++q) {
+            const float4 z = zr[q];
+#pragma unroll
+            for (int j = 0; j < kDwDpt; ++j) {
+              acc[j][4 * q + 0] = fmaf(x[u][j], z.x, acc[j][4 * q + 0]);
+              acc[j][4 * q + 1] = fmaf(x[u][j], z.y, acc[j][4 * q + 1]);
+              acc[j][4 * q + 2] = fmaf(x[u][j], z.z, acc[j][4 * q + 2]);
+              acc[j][4 * q + 3] = fmaf(x[u][j], z.w, acc[j][4 * q + 3]);
+            }
           }
         }
       }
@@ -373,78 +389,106 @@ __global__ void dwa_reduce_kernel(const float* __restrict__ part, T* __restrict_
 }
 
 // ---------------------------------------------------------------------------
-// dX[t, d] = sum_h dz[h, t] W_A[d, h]: each CTA takes 16 tokens and 1024
-// columns (4 consecutive per thread); heads go through 16 at a time with
-// W_A's slice in registers and dz's in shared memory.
+// dX[t, d] = sum_h dz[h, t] W_A[d, h]: a CTA owns 1024 columns (4
+// consecutive per thread) and walks tiles of 16 tokens; heads go 16 at a
+// time, W_A's slice staged once in shared memory as fp32 [h][d] and held in
+// registers (re-staged per tile only when there are more than 16 heads),
+// dz's slice of the tile in shared memory.
 // ---------------------------------------------------------------------------
 constexpr int kDxThreads = 256, kDxDpt = 4, kDxTok = 16, kDxH = 16;
+constexpr int kDxCols = kDxThreads * kDxDpt;
+constexpr size_t kDxSmem = (size_t)(kDxH * kDxCols + kDxTok * kDxH) * sizeof(float);
 
 template <typename T>
 __global__ void __launch_bounds__(kDxThreads)
 dx_kernel(const float* __restrict__ dz, const T* __restrict__ WA, T* __restrict__ dX, int N, int D,
-          int H, long long tokens) {
-  __shared__ __align__(16) float dzs[kDxTok][kDxH];
-  const long long t0 = (long long)blockIdx.x * kDxTok;
-  const int d0 = (blockIdx.y * kDxThreads + threadIdx.x) * kDxDpt;
-  const int nt = (int)min((long long)kDxTok, tokens - t0);
+          int H, long long tokens, long long ntiles) {
+  extern __shared__ float4 dxsm[];
+  float* Ws = reinterpret_cast<float*>(dxsm);     // [kDxH][kDxCols]
+  float* dzs = Ws + kDxH * kDxCols;                // [kDxTok][kDxH]
+  const int dbase = blockIdx.y * kDxCols;
+  const int d0 = dbase + threadIdx.x * kDxDpt;
   const bool vec = (D & 3) == 0;
-  float acc[kDxTok][kDxDpt];
-#pragma unroll
-  for (int t = 0; t < kDxTok; ++t)
-#pragma unroll
-    for (int j = 0; j < kDxDpt; ++j) acc[t][j] = 0.f;
-
-  for (int h0 = 0; h0 < H; h0 += kDxH) {
+  const int nchunks = (H + kDxH - 1) / kDxH;
+  float w[kDxDpt][kDxH];
+  auto stage_w = [&](int h0) {
     const int hc = min(kDxH, H - h0);
-    __syncthreads();
-    for (int i = threadIdx.x; i < kDxTok * kDxH; i += kDxThreads) {
-      const int tl = i % kDxTok, hl = i / kDxTok;
-      float v = 0.f;
-      if (tl < nt && hl < hc) {
-        const long long t = t0 + tl;
-        const long long b = t / N, n = t - b * N;
-        v = dz[((size_t)b * H + h0 + hl) * N + n];
-      }
-      dzs[tl][hl] = v;
+    for (int i = threadIdx.x; i < kDxH * kDxCols; i += kDxThreads) {
+      const int hl = i / kDxCols, d = dbase + (i - hl * kDxCols);
+      Ws[i] = (hl < hc && d < D) ? ld_elem(WA + (size_t)d * H + h0 + hl) : 0.f;
     }
+  };
+  auto load_w = [&]() {
+#pragma unroll
+    for (int q = 0; q < kDxH; ++q) {
+      const float4 v = *reinterpret_cast<const float4*>(Ws + q * kDxCols + threadIdx.x * kDxDpt);
+      w[0][q] = v.x; w[1][q] = v.y; w[2][q] = v.z; w[3][q] = v.w;
+    }
+  };
+  if (nchunks == 1) {
+    stage_w(0);
     __syncthreads();
-    if (d0 < D) {
-      float w[kDxDpt][kDxH];
+    load_w();
+  }
+  for (long long tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+    const long long t0 = tile * kDxTok;
+    const int nt = (int)min((long long)kDxTok, tokens - t0);
+    float acc[kDxTok][kDxDpt];
 #pragma unroll
-      for (int j = 0; j < kDxDpt; ++j)
+    for (int t = 0; t < kDxTok; ++t)
 #pragma unroll
-        for (int q = 0; q < kDxH; ++q)
-          w[j][q] = (d0 + j < D && q < hc) ? ld_elem(WA + (size_t)(d0 + j) * H + h0 + q) : 0.f;
+      for (int j = 0; j < kDxDpt; ++j) acc[t][j] = 0.f;
+    for (int c = 0; c < nchunks; ++c) {
+      const int h0 = c * kDxH, hc = min(kDxH, H - h0);
+      __syncthreads();   // the previous tile's (or chunk's) reads are done
+      if (nchunks > 1) stage_w(h0);
+      for (int i = threadIdx.x; i < kDxTok * kDxH; i += kDxThreads) {
+        const int tl = i % kDxTok, hl = i / kDxTok;
+        float v = 0.f;
+        if (tl < nt && hl < hc) {
+          const long long t = t0 + tl;
+          const long long b = t / N, n = t - b * N;
+          v = dz[((size_t)b * H + h0 + hl) * N + n];
+        }
+        dzs[tl * kDxH + hl] = v;
+      }
+      __syncthreads();
+      if (nchunks > 1) load_w();
+      if (d0 < D) {
 #pragma unroll
-      for (int tl = 0; tl < kDxTok; ++tl) {
-        const float4* zr = reinterpret_cast<const float4*>(&dzs[tl][0]);
+        for (int tl = 0; tl < kDxTok; ++tl) {
+          const float4* zr = reinterpret_cast<const float4*>(dzs + tl * kDxH);
 #pragma unroll
-        for (int q = 0; q < kDxH / 4; ++q) {
-          const float4 z = zr[q];
+          for (int q = 0; q < kDxH / 4; ++q) {
+            const float4 z = zr[q];
 #pragma unroll
-          for (int j = 0; j < kDxDpt; ++j) {
-            float a = acc[tl][j];
-            a = fmaf(w[j][4 * q + 0], z.x, a);
-            a = fmaf(w[j][4 * q + 1], z.y, a);
-            a = fmaf(w[j][4 * q + 2], z.z, a);
-            a = fmaf(w[j][4 * q + 3], z.w, a);
-            acc[tl][j] = a;
+            for (int j = 0; j < kDxDpt; ++j) {
+              float a = acc[tl][j];
+              a = fmaf(w[j][4 * q + 0], z.x, a);
+              a = fmaf(w[j][4 * q + 1], z.y, a);
+              a = fmaf(w[j][4 * q + 2], z.z, a);
+              a = fmaf(w[j][4 * q + 3], z.w, a);
+              acc[tl][j] = a;
+            }
           }
         }
       }
     }
-  }
-  if (d0 >= D) return;
+    if (d0 < D) {
 #pragma unroll
-  for (int tl = 0; tl < kDxTok; ++tl)
-    if (tl < nt) st4(dX + (size_t)(t0 + tl) * D + d0, D - d0, vec, acc[tl]);
+      for (int tl = 0; tl < kDxTok; ++tl)
+        if (tl < nt) st4(dX + (size_t)(t0 + tl) * D + d0, D - d0, vec, acc[tl]);
+    }
+  }
 }
 
 // ---------------------------------------------------------------------------
 // Host launchers (plan's stream).
 // ---------------------------------------------------------------------------
 cudaError_t setup_backward_kernels(const cat_plan_s* p) {
-  cudaError_t e = allow_max_smem(corr_pass_b);
+  cudaError_t e = p->dtype == 1 ? allow_max_smem(dx_kernel<__nv_bfloat16>)
+                                : allow_max_smem(dx_kernel<float>);
+  if (e == cudaSuccess) e = allow_max_smem(corr_pass_b);
   if (e == cudaSuccess) e = allow_max_smem(corr_pass_c);
   if (e == cudaSuccess)
     e = p->dtype == 1 ? allow_max_smem(corr_pass_a<__nv_bfloat16>) : allow_max_smem(corr_pass_a<float>);
@@ -480,12 +524,29 @@ static cudaError_t corr_t(const cat_plan_s* p, const T* G, const T* V) {
   return cudaSuccess;
 }
 
+// Fast path: its own pass A on dO and on V, fsf_corr_b into the one-signal
+// buffer bw_scr ([bhl][k2][n1]), then pass C above with Q = 1.
+static cudaError_t corr_fast(const cat_plan_s* p, const void* G, const void* V) {
+  const BwCfg& w = p->bw;
+  const int rows = p->B * p->H;
+  for (int bh0 = 0; bh0 < rows; bh0 += w.chunk_bh) {
+    const int nb = rows - bh0 < w.chunk_bh ? rows - bh0 : w.chunk_bh;
+    cudaError_t e = launch_fast_corr(p, G, V, p->bw_scr, bh0, nb, p->stream);
+    if (e != cudaSuccess) return e;
+    corr_pass_c<<<nb * (w.N1 / w.TC), w.threadsC, w.smemC, p->stream>>>(
+        p->bw_scr, p->bw_dzs, p->tw, w.rp2, p->N, w.N1, w.TC, 1, bh0, p->status);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
 cudaError_t launch_backward_dz(const cat_plan_s* p, const void* G, const void* V) {
   const int rows = p->B * p->H;
   if (rows == 0) return cudaSuccess;
-  const cudaError_t e = p->dtype == 1
-      ? corr_t(p, (const __nv_bfloat16*)G, (const __nv_bfloat16*)V)
-      : corr_t(p, (const float*)G, (const float*)V);
+  const cudaError_t e = p->bw.fast ? corr_fast(p, G, V)
+      : p->dtype == 1 ? corr_t(p, (const __nv_bfloat16*)G, (const __nv_bfloat16*)V)
+                      : corr_t(p, (const float*)G, (const float*)V);
   if (e != cudaSuccess) return e;
   softmax_bw_kernel<<<rows, kSmBwThreads, 0, p->stream>>>(p->zs, p->bw_dzs, p->bw_dz, p->N);
   return cudaGetLastError();
@@ -504,9 +565,14 @@ static cudaError_t dense_t(const cat_plan_s* p, const T* X, const T* WA, T* dX, 
   const int dh_items = p->D * p->H;
   dwa_reduce_kernel<T><<<(dh_items + 255) / 256, 256, 0, p->stream>>>(p->bw_wpart, dWA, w.wsplit,
                                                                       p->D, p->H);
-  dim3 gx((unsigned)((tokens + kDxTok - 1) / kDxTok), (p->D + kDxThreads * kDxDpt - 1) /
-                                                          (kDxThreads * kDxDpt));
-  dx_kernel<T><<<gx, kDxThreads, 0, p->stream>>>(p->bw_dz, WA, dX, p->N, p->D, p->H, tokens);
+  const long long ntiles = (tokens + kDxTok - 1) / kDxTok;
+  const int dxc = (p->D + kDxCols - 1) / kDxCols;
+  long long gxx = (long long)p->sms / dxc;
+  if (gxx < 1) gxx = 1;
+  if (gxx > ntiles) gxx = ntiles;
+  dim3 gx((unsigned)gxx, dxc);
+  dx_kernel<T><<<gx, kDxThreads, kDxSmem, p->stream>>>(p->bw_dz, WA, dX, p->N, p->D, p->H, tokens,
+                                                       ntiles);
   return cudaGetLastError();
 }
 

@@ -300,6 +300,28 @@ int configure_backward(cat_plan_s* p) {
   cat::BwCfg& w = p->bw;
   std::memset(&w, 0, sizeof(w));
   const int N = p->N;
+  const size_t c8 = sizeof(float2);
+  if (p->path == cat::PATH_FAST) {
+    // The fast path's pass A and the register kernel fsf_corr_b (both in
+    // its scratch slots and chunks), then pass C on one signal per row.
+    w.fast = 1;
+    w.N1 = p->fs.N1;
+    w.N2 = p->fs.N2;
+    w.rp1 = p->fs.rp1;
+    w.rp2 = p->fs.rp2;
+    w.Q = 1;
+    w.TC = 1;
+    for (int t = 2; t <= 64; ++t)
+      if (w.N1 % t == 0 && (size_t)t * w.N2 * c8 <= kFsSmemBudget) w.TC = t;
+    w.smemC = (size_t)w.TC * w.N2 * c8;
+    w.threadsC = fft_threads(w.TC, w.N2);
+    if ((long)w.TC * w.N2 > (long)cat::vals_capacity(w.rp2) * w.threadsC)
+      return CAT_ERR_UNSUPPORTED_N;
+    w.chunk_bh = p->fs.chunk_bh;
+    w.scratch_bytes = (size_t)w.chunk_bh * N * c8;
+    w.wsplit = cat::backward_wsplit((long long)p->B * N, p->D, p->H, p->sms > 0 ? p->sms : 148);
+    return CAT_OK;
+  }
   if (N <= 4096) {
     w.N1 = N;
     w.N2 = 1;
@@ -308,7 +330,6 @@ int configure_backward(cat_plan_s* p) {
   }
   if (!make_radix_plan(w.N1, &w.rp1) || !make_radix_plan(w.N2, &w.rp2))
     return CAT_ERR_UNSUPPORTED_N;
-  const size_t c8 = sizeof(float2);
   const int np = p->npair;
   w.Q = 2 * np;
   // Pass A: up to 16 pairs (32 signals) per CTA, then as many n1 as fit.

@@ -55,7 +55,8 @@ struct BwCfg {
   size_t smemB;
   int TC, threadsC;                // pass C: n1 per CTA
   size_t smemC;
-  int Q;                           // scratch signals per (b, h) = 2·npair
+  int fast;                        // 1: the fast path's passes A and fsf_corr_b
+  int Q;                           // scratch signals per (b, h) = 2·npair (fast: 1)
   int chunk_bh;                    // (b, h) rows whose scratch is live at once
   int wsplit;                      // token ranges of the dW_A partial sums
   size_t scratch_bytes;
@@ -213,5 +214,10 @@ cudaError_t launch_backward_dense(const cat_plan_s* p, const void* X, const void
                                   void* dWA);
 cudaError_t launch_reverse_scores(const cat_plan_s* p);
 int backward_wsplit(long long tokens, int D, int H, int sms);
+// Fast path (head width 64, N = 512·N2): the correlation's pass A on dO
+// (scratch slot 0) and on V (slot 1), then its pass B into y[bhl][k2][n1]
+// for rows [bh0, bh0 + nb), on stream st.
+cudaError_t launch_fast_corr(const cat_plan_s* p, const void* G, const void* V, float2* y,
+                             int bh0, int nb, cudaStream_t st);
 
 }  // namespace cat

@@ -417,6 +417,145 @@ fsf_pass_b(float2* __restrict__ scr, const float2* __restrict__ zft,
   }
 }
 
+
+// ---------------------------------------------------------------------------
+// Backward correlation, pass B (the fast path's layout; see backward.cu for
+// the method): per (b, h, k2), the length-512 DFTs over n1 of the head's 32
+// dO pairs (scratch slot 0) and 32 V pairs (slot 1), both after pass A; the
+// sum over pairs of FFT(g)·conj(FFT(v)) at every bin k1; the inverse DFT over
+// k1 of that one signal; the conjugate twiddle w_N^{-n1 k2}; into
+// y[bhl][k2][n1].  256 threads: signal sig = lane mod 16 (0..7 dO, 8..15 V;
+// pairs sig mod 8 + 8r in round r), j = 2·warp + lane / 16, with pass B's
+// forward steps F1, F2 (thread j then holds bins k1 = 2j + e + 32q).  The V
+// threads hand their bins over through shared memory, the dO threads keep
+// running sums; the 8 sums are added in a fixed order and 16 threads run
+// pass B's inverse steps I1, I2 on the result.
+// ---------------------------------------------------------------------------
+constexpr size_t kSmemCorrB = (size_t)16 * kRowB * sizeof(float2) + 3 * kTabB * sizeof(float2);
+
+__global__ void __launch_bounds__(256, 1)
+fsf_corr_b(const float2* __restrict__ scrG, const float2* __restrict__ scrV,
+           float2* __restrict__ y, const float2* __restrict__ tabs, int N2) {
+  extern __shared__ float4 smem4[];
+  float2* buf = reinterpret_cast<float2*>(smem4);
+  float2* tf = buf + 16 * kRowB;
+  float2* ti = tf + kTabB;
+  float2* tx = ti + kTabB;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int sig = lane & 15;
+  const int j = 2 * warp + (lane >> 4);
+  const int k2 = blockIdx.x % N2;
+  const int bhl = blockIdx.x / N2;
+  const float2* src = sig < 8 ? scrG : scrV;
+  float2* row = buf + sig * kRowB;
+  {
+    const int t = threadIdx.x;
+    const float4* g4 = reinterpret_cast<const float4*>(tabs);
+    float4* tf4 = reinterpret_cast<float4*>(tf);
+    tf4[t] = __ldg(g4 + t);
+    tf4[256 + t] = __ldg(g4 + 256 + t);
+    tf4[512 + t] = __ldg(g4 + 512 + (size_t)k2 * 256 + t);
+  }
+  float2 acc[2][16];
+#pragma unroll
+  for (int q = 0; q < 16; ++q) acc[0][q] = acc[1][q] = make_float2(0.f, 0.f);
+
+  for (int r = 0; r < kFastPairs / 8; ++r) {
+    const int pair = 8 * r + (sig & 7);
+    float2 a[32];
+#pragma unroll
+    for (int u = 0; u < 32; ++u) a[u] = src[scr_idx(bhl, N2, k2, j + 16 * u, pair)];
+    dft<32, false, CxPaired>(a);
+    __syncthreads();   // the previous round's reads of the rows are done
+#pragma unroll
+    for (int q = 0; q < 32; q += 2) st_sh2(row + 32 * j + q, a[q], a[q + 1]);
+    __syncthreads();
+    float2 c[2][16];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) ld_sh2(row + 2 * j + 32 * u, c[0][u], c[1][u]);
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const float2* tw = tf + (2 * j + e) * 16;
+#pragma unroll
+      for (int u = 2; u < 16; u += 2) {
+        float2 w0, w1;
+        ld_sh2(tw + u, w0, w1);
+        c[e][u] = cmul(c[e][u], w0);
+        c[e][u + 1] = cmul(c[e][u + 1], w1);
+      }
+      c[e][1] = cmul(c[e][1], tw[1]);
+      dft<16, false, CxPaired>(c[e]);
+    }
+    __syncthreads();   // every thread has read its row
+    if (sig >= 8) {
+#pragma unroll
+      for (int q = 0; q < 16; ++q) st_sh2(row + (j * 16 + q) * 2, c[0][q], c[1][q]);
+    }
+    __syncthreads();
+    if (sig < 8) {
+      const float2* vrow = buf + (sig + 8) * kRowB;
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        float2 v0, v1;
+        ld_sh2(vrow + (j * 16 + q) * 2, v0, v1);
+        acc[0][q] = cadd(acc[0][q], cmulc(c[0][q], v0));
+        acc[1][q] = cadd(acc[1][q], cmulc(c[1][q], v1));
+      }
+    }
+  }
+  __syncthreads();
+  if (sig < 8) {
+#pragma unroll
+    for (int q = 0; q < 16; ++q) st_sh2(row + (j * 16 + q) * 2, acc[0][q], acc[1][q]);
+  }
+  __syncthreads();
+  // Sum of the 8 partial spectra (rows 0..7) into row 8, two bins a thread.
+  float2* yrow = buf + 8 * kRowB;
+  float2* xrow = buf + 9 * kRowB;
+  {
+    const int t = threadIdx.x;
+    float2 s0 = make_float2(0.f, 0.f), s1 = s0;
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+      float2 v0, v1;
+      ld_sh2(buf + g * kRowB + 2 * t, v0, v1);
+      s0 = cadd(s0, v0);
+      s1 = cadd(s1, v1);
+    }
+    st_sh2(yrow + 2 * t, s0, s1);
+  }
+  __syncthreads();
+  if (sig == 0) {
+    float2 c[2][16];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) ld_sh2(yrow + (j * 16 + q) * 2, c[0][q], c[1][q]);
+#pragma unroll
+    for (int e = 0; e < 2; ++e) dft<16, true, CxPaired>(c[e]);
+#pragma unroll
+    for (int q = 0; q < 16; ++q) st_sh2(xrow + 32 * q + 2 * j, c[0][q], c[1][q]);
+  }
+  __syncthreads();
+  if (sig == 0) {
+    float2 a[32];
+#pragma unroll
+    for (int u = 0; u < 32; u += 2) ld_sh2(xrow + 32 * j + u, a[u], a[u + 1]);
+    const float2* tw = ti + j * 32;
+#pragma unroll
+    for (int u = 2; u < 32; u += 2) {
+      float2 w0, w1;
+      ld_sh2(tw + u, w0, w1);
+      a[u] = cmulc(a[u], w0);
+      a[u + 1] = cmulc(a[u + 1], w1);
+    }
+    a[1] = cmulc(a[1], tw[1]);
+    dft<32, true, CxPaired>(a);
+    const float2* tz = tx + j * 32;
+    float2* out = y + ((size_t)bhl * N2 + k2) * kFastN1;
+#pragma unroll
+    for (int q = 0; q < 32; ++q) out[j + 16 * q] = cmulc(a[q], tz[q]);
+  }
+}
+
 // Builds pass B's twiddle tables [tf | ti | tx for k2 = 0..N2-1] and, for
 // N2 = 32, the spectrum kernel's t1, from the plan's table
 // W[e] = exp(-2πi e/N).
@@ -677,6 +816,7 @@ static cudaError_t setup_t(int N2) {
   if (e == cudaSuccess) e = allow_max_smem(fsf_pass_c32<T>);
   if (e == cudaSuccess) e = allow_max_smem(fsf_zspec_b);
   if (e == cudaSuccess) e = allow_max_smem(fsf_zspec_row);
+  if (e == cudaSuccess) e = allow_max_smem(fsf_corr_b);
   return e;
 }
 
@@ -849,6 +989,46 @@ cudaError_t launch_fast_conv(const cat_plan_s* p, const void* V, void* O, cudaEv
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
+}
+
+
+// Pass A alone (the backward correlation transforms dO and V with it): rows
+// [bh0, bh0 + nb) of V into scratch slot `slot`, on stream st.
+template <typename T>
+static cudaError_t pass_a_t(const cat_plan_s* p, const T* V, int bh0, int nb, int slot,
+                            cudaStream_t st) {
+  float2* scr = p->scratch + (size_t)slot * (p->scratch_bytes / 2 / sizeof(float2));
+  switch (p->fs.N2) {
+    case 32: {
+      CUtensorMap tmV;
+      if (!encode_v_map(p, V, &tmV)) return cudaErrorInvalidValue;
+      const int per_sm = PipeA<T>::kSmem <= (113u << 10) ? 2 : 1;
+      int grid = (nb * kFastN1 + kPipeWarps - 1) / kPipeWarps;
+      if (grid > per_sm * p->sms) grid = per_sm * p->sms;
+      fsf_pass_a32<T><<<grid, kPipeWarps * 32, PipeA<T>::kSmem, st>>>(
+          tmV, scr, p->tw, p->N, p->D, p->H, bh0, nb, p->status);
+      break;
+    }
+    case 64: launch_ac<T, 64>(p, V, nullptr, scr, bh0, nb, true, st); break;
+    case 128: launch_ac<T, 128>(p, V, nullptr, scr, bh0, nb, true, st); break;
+    default: launch_ac<T, 256>(p, V, nullptr, scr, bh0, nb, true, st); break;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fast_corr(const cat_plan_s* p, const void* G, const void* V, float2* y,
+                             int bh0, int nb, cudaStream_t st) {
+  cudaError_t e = p->dtype == 1
+      ? pass_a_t(p, (const __nv_bfloat16*)G, bh0, nb, 0, st)
+      : pass_a_t(p, (const float*)G, bh0, nb, 0, st);
+  if (e == cudaSuccess)
+    e = p->dtype == 1 ? pass_a_t(p, (const __nv_bfloat16*)V, bh0, nb, 1, st)
+                      : pass_a_t(p, (const float*)V, bh0, nb, 1, st);
+  if (e != cudaSuccess) return e;
+  const float2* s0 = p->scratch;
+  const float2* s1 = p->scratch + p->scratch_bytes / 2 / sizeof(float2);
+  fsf_corr_b<<<nb * p->fs.N2, 256, kSmemCorrB, st>>>(s0, s1, y, p->tabs, p->fs.N2);
+  return cudaGetLastError();
 }
 
 }  // namespace cat
