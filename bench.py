@@ -51,9 +51,12 @@ FALLBACK_HBM_GBS = 6800.0
 # (profiles/).  Keyed by (workload, hash of the kernel sources): any change
 # to those sources makes the figure stale, and the bench then reports null.
 NCU_TRAFFIC = {
-    # profiles/launches_long16k.md: fsf_pass_b, 16 launches, DRAM read + write
-    # per launch (cold: ncu flushes L2 before each launch).
-    ("long16k", "2463f22c18e9"): 34774016,
+    # profiles/backward_long16k.md: fsf_pass_b, 32 launches (the backward's
+    # dV product runs the forward's pass B on the same chunks of 8 rows),
+    # median DRAM read + write per launch (cold: ncu flushes L2 before each
+    # launch).  The earlier forward-only list (profiles/launches_long16k.md)
+    # gave 34774016 for the same kernel.
+    ("long16k", "45cff3383846"): 34773248,
 }
 KERNEL_SOURCES = ["fourstep_fast.cu", "fft_reg.cuh", "fft_device.cuh", "bulk.cuh", "elem.cuh"]
 # Pass B's transforms: per (pair, k2) signal one forward and one inverse DFT

@@ -246,63 +246,52 @@ softmax_bw_kernel(const float* __restrict__ zs, const float* __restrict__ dzs,
 
 // ---------------------------------------------------------------------------
 // dW_A[d, h] = sum over tokens of X[t, d] dz[h, t]: each CTA takes a range of
-// tokens (split), 1024 columns d (4 consecutive per thread) and 16 heads,
+// tokens (split), 512 columns d (2 consecutive per thread) and 16 heads,
 // and writes its partial sums to part[split][h][d]; dwa_reduce adds the
 // splits in order.
 // ---------------------------------------------------------------------------
-constexpr int kDwThreads = 256, kDwDpt = 4, kDwH = 16, kDwTok = 32, kDwPre = 8;
+constexpr int kDwThreads = 256, kDwDpt = 2, kDwH = 16, kDwTok = 32, kDwPre = 16;
 static_assert(kDwTok % kDwPre == 0, "token tile is whole groups of preloads");
 
-// Four consecutive elements of a row starting at column d0 (d0 % 4 == 0);
-// `left` columns remain in the row.  vec: the row length is a multiple of 4,
-// so the four are one aligned vector.
-__device__ __forceinline__ void ld4(const float* p, int left, bool vec, float* x) {
+// Two consecutive elements from column d0 (d0 even); `left` columns remain;
+// vec: the row length is even, so the two are one aligned pair.
+__device__ __forceinline__ void ld2(const float* p, int left, bool vec, float* x) {
   if (vec) {
-    const float4 v = __ldg(reinterpret_cast<const float4*>(p));
-    x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+    const float2 v = __ldg(reinterpret_cast<const float2*>(p));
+    x[0] = v.x; x[1] = v.y;
   } else {
-#pragma unroll
-    for (int j = 0; j < 4; ++j) x[j] = j < left ? __ldg(p + j) : 0.f;
+    x[0] = __ldg(p);
+    x[1] = left > 1 ? __ldg(p + 1) : 0.f;
   }
 }
-__device__ __forceinline__ void ld4(const __nv_bfloat16* p, int left, bool vec, float* x) {
+__device__ __forceinline__ void ld2(const __nv_bfloat16* p, int left, bool vec, float* x) {
   if (vec) {
-    const uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
-    x[0] = __uint_as_float(u.x << 16);
-    x[1] = __uint_as_float(u.x & 0xffff0000u);
-    x[2] = __uint_as_float(u.y << 16);
-    x[3] = __uint_as_float(u.y & 0xffff0000u);
+    const float2 v = ld_pair(p);
+    x[0] = v.x; x[1] = v.y;
   } else {
-#pragma unroll
-    for (int j = 0; j < 4; ++j) x[j] = j < left ? ld_elem(p + j) : 0.f;
+    x[0] = ld_elem(p);
+    x[1] = left > 1 ? ld_elem(p + 1) : 0.f;
   }
 }
-__device__ __forceinline__ void st4(float* p, int left, bool vec, const float* x) {
+__device__ __forceinline__ void st2(float* p, int left, bool vec, const float* x) {
   if (vec) {
-    *reinterpret_cast<float4*>(p) = make_float4(x[0], x[1], x[2], x[3]);
+    *reinterpret_cast<float2*>(p) = make_float2(x[0], x[1]);
   } else {
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      if (j < left) p[j] = x[j];
+    p[0] = x[0];
+    if (left > 1) p[1] = x[1];
   }
 }
-__device__ __forceinline__ void st4(__nv_bfloat16* p, int left, bool vec, const float* x) {
+__device__ __forceinline__ void st2(__nv_bfloat16* p, int left, bool vec, const float* x) {
   if (vec) {
-    const __nv_bfloat162 a = __floats2bfloat162_rn(x[0], x[1]);
-    const __nv_bfloat162 b = __floats2bfloat162_rn(x[2], x[3]);
-    uint2 u;
-    u.x = *reinterpret_cast<const unsigned int*>(&a);
-    u.y = *reinterpret_cast<const unsigned int*>(&b);
-    *reinterpret_cast<uint2*>(p) = u;
+    st_pair(p, make_float2(x[0], x[1]));
   } else {
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      if (j < left) st_elem(p + j, x[j]);
+    st_elem(p, x[0]);
+    if (left > 1) st_elem(p + 1, x[1]);
   }
 }
 
-template <typename T>
-__global__ void __launch_bounds__(kDwThreads)
+template <typename T, bool VEC>
+__global__ void __launch_bounds__(kDwThreads, 2)
 dwa_partial_kernel(const T* __restrict__ X, const float* __restrict__ dz, float* __restrict__ part,
                    int N, int D, int H, long long tokens, long long tps) {
   __shared__ __align__(16) float dzs[kDwTok][kDwH];
@@ -312,7 +301,7 @@ dwa_partial_kernel(const T* __restrict__ X, const float* __restrict__ dz, float*
   const int hc = min(kDwH, H - h0);
   const long long t_begin = (long long)split * tps;
   const long long t_end = min(tokens, t_begin + tps);
-  const bool vec = (D & 3) == 0;
+  constexpr bool vec = VEC;   // even row length: column pairs are aligned
   float acc[kDwDpt][kDwH];
 #pragma unroll
   for (int j = 0; j < kDwDpt; ++j)
@@ -334,18 +323,15 @@ dwa_partial_kernel(const T* __restrict__ X, const float* __restrict__ dz, float*
     __syncthreads();
     const int nt = (int)min((long long)kDwTok, t_end - t0);
     if (d0 < D) {
-      // Eight tokens' loads in flight before their products (tokens past
-      // nt read as zero rows and add nothing: dzs is zero there too).
+      // Sixteen tokens' loads in flight before their products.
+      // The loads take no branch: a token past the tile reads the last
+      // valid row instead (its dzs entry is zero, so it adds nothing).
       for (int tb = 0; tb < nt; tb += kDwPre) {
         float x[kDwPre][kDwDpt];
 #pragma unroll
         for (int u = 0; u < kDwPre; ++u) {
-          if (tb + u < nt) {
-            ld4(X + (size_t)(t0 + tb + u) * D + d0, D - d0, vec, x[u]);
-          } else {
-#pragma unroll
-            for (int j = 0; j < kDwDpt; ++j) x[u][j] = 0.f;
-          }
+          const long long t = min(t0 + tb + u, tokens - 1);
+          ld2(X + (size_t)t * D + d0, D - d0, vec, x[u]);
         }
 #pragma unroll
         for (int u = 0; u < kDwPre; ++u) {
@@ -372,7 +358,7 @@ dwa_partial_kernel(const T* __restrict__ X, const float* __restrict__ dz, float*
       float v[kDwDpt];
 #pragma unroll
       for (int j = 0; j < kDwDpt; ++j) v[j] = acc[j][q];
-      st4(part + ((size_t)split * H + h0 + q) * D + d0, D - d0, vec, v);
+      st2(part + ((size_t)split * H + h0 + q) * D + d0, D - d0, vec, v);
     }
   }
 }
@@ -383,24 +369,25 @@ __global__ void dwa_reduce_kernel(const float* __restrict__ part, T* __restrict_
   const int i = blockIdx.x * blockDim.x + threadIdx.x;   // i = h·D + d
   if (i >= D * H) return;
   float s = 0.f;
+#pragma unroll 8
   for (int k = 0; k < nsplit; ++k) s += part[(size_t)k * H * D + i];
   const int h = i / D, d = i - h * D;
   st_elem(dWA + (size_t)d * H + h, s);
 }
 
 // ---------------------------------------------------------------------------
-// dX[t, d] = sum_h dz[h, t] W_A[d, h]: a CTA owns 1024 columns (4
+// dX[t, d] = sum_h dz[h, t] W_A[d, h]: a CTA owns 512 columns (2
 // consecutive per thread) and walks tiles of 16 tokens; heads go 16 at a
 // time, W_A's slice staged once in shared memory as fp32 [h][d] and held in
 // registers (re-staged per tile only when there are more than 16 heads),
 // dz's slice of the tile in shared memory.
 // ---------------------------------------------------------------------------
-constexpr int kDxThreads = 256, kDxDpt = 4, kDxTok = 16, kDxH = 16;
+constexpr int kDxThreads = 256, kDxDpt = 2, kDxTok = 16, kDxH = 16;
 constexpr int kDxCols = kDxThreads * kDxDpt;
 constexpr size_t kDxSmem = (size_t)(kDxH * kDxCols + kDxTok * kDxH) * sizeof(float);
 
 template <typename T>
-__global__ void __launch_bounds__(kDxThreads)
+__global__ void __launch_bounds__(kDxThreads, 2)
 dx_kernel(const float* __restrict__ dz, const T* __restrict__ WA, T* __restrict__ dX, int N, int D,
           int H, long long tokens, long long ntiles) {
   extern __shared__ float4 dxsm[];
@@ -408,7 +395,7 @@ dx_kernel(const float* __restrict__ dz, const T* __restrict__ WA, T* __restrict_
   float* dzs = Ws + kDxH * kDxCols;                // [kDxTok][kDxH]
   const int dbase = blockIdx.y * kDxCols;
   const int d0 = dbase + threadIdx.x * kDxDpt;
-  const bool vec = (D & 3) == 0;
+  const bool vec = (D & 1) == 0;
   const int nchunks = (H + kDxH - 1) / kDxH;
   float w[kDxDpt][kDxH];
   auto stage_w = [&](int h0) {
@@ -421,14 +408,26 @@ dx_kernel(const float* __restrict__ dz, const T* __restrict__ WA, T* __restrict_
   auto load_w = [&]() {
 #pragma unroll
     for (int q = 0; q < kDxH; ++q) {
-      const float4 v = *reinterpret_cast<const float4*>(Ws + q * kDxCols + threadIdx.x * kDxDpt);
-      w[0][q] = v.x; w[1][q] = v.y; w[2][q] = v.z; w[3][q] = v.w;
+      const float2 v = *reinterpret_cast<const float2*>(Ws + q * kDxCols + threadIdx.x * kDxDpt);
+      w[0][q] = v.x; w[1][q] = v.y;
     }
   };
+  // dz element (token tl, head h0 + hl) of a tile, zero outside the tile.
+  auto ld_dz = [&](long long t0, int h0, int i) {
+    const int tl = i % kDxTok, hl = i / kDxTok;
+    const int hc = min(kDxH, H - h0);
+    const long long t = t0 + tl;
+    if (t >= tokens || hl >= hc) return 0.f;
+    const long long b = t / N, n = t - b * N;
+    return dz[((size_t)b * H + h0 + hl) * N + n];
+  };
+  static_assert(kDxTok * kDxH == kDxThreads, "one dz element per thread and tile");
+  float pre = 0.f;   // the next tile's element (one head chunk only)
   if (nchunks == 1) {
     stage_w(0);
     __syncthreads();
     load_w();
+    if (blockIdx.x < ntiles) pre = ld_dz((long long)blockIdx.x * kDxTok, 0, threadIdx.x);
   }
   for (long long tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
     const long long t0 = tile * kDxTok;
@@ -439,20 +438,20 @@ dx_kernel(const float* __restrict__ dz, const T* __restrict__ WA, T* __restrict_
 #pragma unroll
       for (int j = 0; j < kDxDpt; ++j) acc[t][j] = 0.f;
     for (int c = 0; c < nchunks; ++c) {
-      const int h0 = c * kDxH, hc = min(kDxH, H - h0);
+      const int h0 = c * kDxH;
       __syncthreads();   // the previous tile's (or chunk's) reads are done
-      if (nchunks > 1) stage_w(h0);
-      for (int i = threadIdx.x; i < kDxTok * kDxH; i += kDxThreads) {
-        const int tl = i % kDxTok, hl = i / kDxTok;
-        float v = 0.f;
-        if (tl < nt && hl < hc) {
-          const long long t = t0 + tl;
-          const long long b = t / N, n = t - b * N;
-          v = dz[((size_t)b * H + h0 + hl) * N + n];
-        }
-        dzs[tl * kDxH + hl] = v;
+      // Thread i holds token i mod 16, head i / 16 of the tile (ld_dz).
+      float* slot = dzs + (threadIdx.x % kDxTok) * kDxH + threadIdx.x / kDxTok;
+      if (nchunks > 1) {
+        stage_w(h0);
+        *slot = ld_dz(t0, h0, threadIdx.x);
+      } else {
+        *slot = pre;
       }
       __syncthreads();
+      // Issue the next tile's load now; it completes during the products.
+      if (nchunks == 1 && tile + gridDim.x < ntiles)
+        pre = ld_dz((tile + gridDim.x) * kDxTok, 0, threadIdx.x);
       if (nchunks > 1) load_w();
       if (d0 < D) {
 #pragma unroll
@@ -477,7 +476,7 @@ dx_kernel(const float* __restrict__ dz, const T* __restrict__ WA, T* __restrict_
     if (d0 < D) {
 #pragma unroll
       for (int tl = 0; tl < kDxTok; ++tl)
-        if (tl < nt) st4(dX + (size_t)(t0 + tl) * D + d0, D - d0, vec, acc[tl]);
+        if (tl < nt) st2(dX + (size_t)(t0 + tl) * D + d0, D - d0, vec, acc[tl]);
     }
   }
 }
@@ -525,7 +524,8 @@ static cudaError_t corr_t(const cat_plan_s* p, const T* G, const T* V) {
 }
 
 // Fast path: its own pass A on dO and on V, fsf_corr_b into the one-signal
-// buffer bw_scr ([bhl][k2][n1]), then pass C above with Q = 1.
+// buffer bw_scr ([bhl][k2][n1]), then pass C (in registers for N2 = 32, else
+// pass C above with Q = 1).
 static cudaError_t corr_fast(const cat_plan_s* p, const void* G, const void* V) {
   const BwCfg& w = p->bw;
   const int rows = p->B * p->H;
@@ -533,9 +533,13 @@ static cudaError_t corr_fast(const cat_plan_s* p, const void* G, const void* V) 
     const int nb = rows - bh0 < w.chunk_bh ? rows - bh0 : w.chunk_bh;
     cudaError_t e = launch_fast_corr(p, G, V, p->bw_scr, bh0, nb, p->stream);
     if (e != cudaSuccess) return e;
-    corr_pass_c<<<nb * (w.N1 / w.TC), w.threadsC, w.smemC, p->stream>>>(
-        p->bw_scr, p->bw_dzs, p->tw, w.rp2, p->N, w.N1, w.TC, 1, bh0, p->status);
-    e = cudaGetLastError();
+    if (w.N2 == 32) {
+      e = launch_fast_corr_c32(p, p->bw_scr, p->bw_dzs, bh0, nb, p->stream);
+    } else {
+      corr_pass_c<<<nb * (w.N1 / w.TC), w.threadsC, w.smemC, p->stream>>>(
+          p->bw_scr, p->bw_dzs, p->tw, w.rp2, p->N, w.N1, w.TC, 1, bh0, p->status);
+      e = cudaGetLastError();
+    }
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
@@ -560,14 +564,18 @@ static cudaError_t dense_t(const cat_plan_s* p, const T* X, const T* WA, T* dX, 
   const int hchunks = (p->H + kDwH - 1) / kDwH;
   const long long tps = (tokens + w.wsplit - 1) / w.wsplit;
   dim3 gw(w.wsplit, dchunks, hchunks);
-  dwa_partial_kernel<T><<<gw, kDwThreads, 0, p->stream>>>(X, p->bw_dz, p->bw_wpart, p->N, p->D,
-                                                          p->H, tokens, tps);
+  if ((p->D & 1) == 0)
+    dwa_partial_kernel<T, true><<<gw, kDwThreads, 0, p->stream>>>(X, p->bw_dz, p->bw_wpart, p->N,
+                                                                  p->D, p->H, tokens, tps);
+  else
+    dwa_partial_kernel<T, false><<<gw, kDwThreads, 0, p->stream>>>(X, p->bw_dz, p->bw_wpart, p->N,
+                                                                   p->D, p->H, tokens, tps);
   const int dh_items = p->D * p->H;
   dwa_reduce_kernel<T><<<(dh_items + 255) / 256, 256, 0, p->stream>>>(p->bw_wpart, dWA, w.wsplit,
                                                                       p->D, p->H);
   const long long ntiles = (tokens + kDxTok - 1) / kDxTok;
   const int dxc = (p->D + kDxCols - 1) / kDxCols;
-  long long gxx = (long long)p->sms / dxc;
+  long long gxx = 2ll * p->sms / dxc;
   if (gxx < 1) gxx = 1;
   if (gxx > ntiles) gxx = ntiles;
   dim3 gx((unsigned)gxx, dxc);

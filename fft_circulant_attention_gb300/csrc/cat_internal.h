@@ -219,5 +219,8 @@ int backward_wsplit(long long tokens, int D, int H, int sms);
 // for rows [bh0, bh0 + nb), on stream st.
 cudaError_t launch_fast_corr(const cat_plan_s* p, const void* G, const void* V, float2* y,
                              int bh0, int nb, cudaStream_t st);
+// Its pass C for N2 = 32: dz* rows [bh0, bh0 + nb) from y.
+cudaError_t launch_fast_corr_c32(const cat_plan_s* p, const float2* y, float* dzs, int bh0,
+                                 int nb, cudaStream_t st);
 
 }  // namespace cat

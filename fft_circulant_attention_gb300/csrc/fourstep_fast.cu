@@ -429,11 +429,14 @@ fsf_pass_b(float2* __restrict__ scr, const float2* __restrict__ zft,
 // forward steps F1, F2 (thread j then holds bins k1 = 2j + e + 32q).  The V
 // threads hand their bins over through shared memory, the dO threads keep
 // running sums; the 8 sums are added in a fixed order and 16 threads run
-// pass B's inverse steps I1, I2 on the result.
+// pass B's inverse steps I1, I2 on the result.  The running sums live in
+// shared memory (rows of kRowB per signal, at the position the thread's bins
+// take in the exchange rows), so that two CTAs fit an SM.
 // ---------------------------------------------------------------------------
-constexpr size_t kSmemCorrB = (size_t)16 * kRowB * sizeof(float2) + 3 * kTabB * sizeof(float2);
+constexpr size_t kSmemCorrB =
+    (size_t)16 * kRowB * sizeof(float2) + 3 * kTabB * sizeof(float2) + 8 * (size_t)kRowB * sizeof(float2);
 
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(256, 2)
 fsf_corr_b(const float2* __restrict__ scrG, const float2* __restrict__ scrV,
            float2* __restrict__ y, const float2* __restrict__ tabs, int N2) {
   extern __shared__ float4 smem4[];
@@ -441,6 +444,7 @@ fsf_corr_b(const float2* __restrict__ scrG, const float2* __restrict__ scrV,
   float2* tf = buf + 16 * kRowB;
   float2* ti = tf + kTabB;
   float2* tx = ti + kTabB;
+  float2* accs = tx + kTabB;           // [8][kRowB] running sums of the dO threads
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int sig = lane & 15;
   const int j = 2 * warp + (lane >> 4);
@@ -448,6 +452,9 @@ fsf_corr_b(const float2* __restrict__ scrG, const float2* __restrict__ scrV,
   const int bhl = blockIdx.x / N2;
   const float2* src = sig < 8 ? scrG : scrV;
   float2* row = buf + sig * kRowB;
+  // This thread's 32 bins; rows kRowB apart put the 8 signals of a quarter
+  // warp in distinct 16-byte bank groups.
+  float2* acc = accs + (sig & 7) * kRowB + j * 32;
   {
     const int t = threadIdx.x;
     const float4* g4 = reinterpret_cast<const float4*>(tabs);
@@ -455,10 +462,9 @@ fsf_corr_b(const float2* __restrict__ scrG, const float2* __restrict__ scrV,
     tf4[t] = __ldg(g4 + t);
     tf4[256 + t] = __ldg(g4 + 256 + t);
     tf4[512 + t] = __ldg(g4 + 512 + (size_t)k2 * 256 + t);
+    float4* a4 = reinterpret_cast<float4*>(accs);
+    for (int i = t; i < 8 * kRowB / 2; i += 256) a4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  float2 acc[2][16];
-#pragma unroll
-  for (int q = 0; q < 16; ++q) acc[0][q] = acc[1][q] = make_float2(0.f, 0.f);
 
   for (int r = 0; r < kFastPairs / 8; ++r) {
     const int pair = 8 * r + (sig & 7);
@@ -496,20 +502,15 @@ fsf_corr_b(const float2* __restrict__ scrG, const float2* __restrict__ scrV,
       const float2* vrow = buf + (sig + 8) * kRowB;
 #pragma unroll
       for (int q = 0; q < 16; ++q) {
-        float2 v0, v1;
+        float2 v0, v1, s0, s1;
         ld_sh2(vrow + (j * 16 + q) * 2, v0, v1);
-        acc[0][q] = cadd(acc[0][q], cmulc(c[0][q], v0));
-        acc[1][q] = cadd(acc[1][q], cmulc(c[1][q], v1));
+        ld_sh2(acc + 2 * q, s0, s1);
+        st_sh2(acc + 2 * q, cadd(s0, cmulc(c[0][q], v0)), cadd(s1, cmulc(c[1][q], v1)));
       }
     }
   }
   __syncthreads();
-  if (sig < 8) {
-#pragma unroll
-    for (int q = 0; q < 16; ++q) st_sh2(row + (j * 16 + q) * 2, acc[0][q], acc[1][q]);
-  }
-  __syncthreads();
-  // Sum of the 8 partial spectra (rows 0..7) into row 8, two bins a thread.
+  // Sum of the 8 partial spectra into row 8, two bins a thread.
   float2* yrow = buf + 8 * kRowB;
   float2* xrow = buf + 9 * kRowB;
   {
@@ -518,7 +519,7 @@ fsf_corr_b(const float2* __restrict__ scrG, const float2* __restrict__ scrV,
 #pragma unroll
     for (int g = 0; g < 8; ++g) {
       float2 v0, v1;
-      ld_sh2(buf + g * kRowB + 2 * t, v0, v1);
+      ld_sh2(accs + g * kRowB + 2 * t, v0, v1);
       s0 = cadd(s0, v0);
       s1 = cadd(s1, v1);
     }
@@ -554,6 +555,27 @@ fsf_corr_b(const float2* __restrict__ scrG, const float2* __restrict__ scrV,
 #pragma unroll
     for (int q = 0; q < 32; ++q) out[j + 16 * q] = cmulc(a[q], tz[q]);
   }
+}
+
+
+// Backward correlation, pass C for N2 = 32: one thread per (b, h, n1), the
+// inverse DFT over k2 of y[bhl][k2][n1] in registers; dz*[n1 + 512·n2] =
+// Re / N.  Consecutive threads take consecutive n1, so loads and stores are
+// contiguous runs.
+__global__ void __launch_bounds__(128)
+fsf_corr_c32(const float2* __restrict__ y, float* __restrict__ dzs, int N, int bh0, int nb) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= nb * kFastN1) return;
+  const int bhl = i / kFastN1, n1 = i - bhl * kFastN1;
+  const float2* src = y + (size_t)bhl * 32 * kFastN1 + n1;
+  float2 a[32];
+#pragma unroll
+  for (int k2 = 0; k2 < 32; ++k2) a[k2] = src[(size_t)k2 * kFastN1];
+  dft<32, true, CxPaired>(a);
+  const float invN = 1.0f / (float)N;
+  float* out = dzs + (size_t)(bh0 + bhl) * N + n1;
+#pragma unroll
+  for (int n2 = 0; n2 < 32; ++n2) out[(size_t)n2 * kFastN1] = a[n2].x * invN;
 }
 
 // Builds pass B's twiddle tables [tf | ti | tx for k2 = 0..N2-1] and, for
@@ -1028,6 +1050,13 @@ cudaError_t launch_fast_corr(const cat_plan_s* p, const void* G, const void* V, 
   const float2* s0 = p->scratch;
   const float2* s1 = p->scratch + p->scratch_bytes / 2 / sizeof(float2);
   fsf_corr_b<<<nb * p->fs.N2, 256, kSmemCorrB, st>>>(s0, s1, y, p->tabs, p->fs.N2);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fast_corr_c32(const cat_plan_s* p, const float2* y, float* dzs, int bh0,
+                                 int nb, cudaStream_t st) {
+  const int items = nb * kFastN1;
+  fsf_corr_c32<<<(items + 127) / 128, 128, 0, st>>>(y, dzs, p->N, bh0, nb);
   return cudaGetLastError();
 }
 
