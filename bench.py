@@ -12,8 +12,8 @@ between steps.
                     [--backward-only]
 
 The line also carries the backward pass (cat_backward: dX, dW_A, dV for an
-upstream gradient) at both long-sequence workloads, with its roofline
-fraction; --backward-only times just that on --config.
+upstream gradient) at the long-sequence and the short workloads, with its
+roofline fraction; --backward-only times just that on --config.
 
 Prints ONE JSON line (rank 0).  With --impl reference the fp64 CPU oracle
 is timed instead, on a bounded sample of the same workload.
@@ -467,8 +467,16 @@ def run_gb300(args, world, rank, local):
     if not args.no_secondary and args.config != SECONDARY:
         sec = measure_workload(SECONDARY, max(3, args.steps // 4), args.warmup, device, world)
     short = [] if args.no_short else [measure_short(n, device) for n in SHORT]
-    backward = [] if args.no_backward else [
-        measure_backward(n, device, r) for n, r in ((PRIMARY, 20), (SECONDARY, 5))]
+    backward = []
+    if not args.no_backward:
+        # The backward pass at the two long workloads and the short ones; a
+        # failure is recorded in its entry instead of losing the line.
+        for n, r in ((PRIMARY, 20), (SECONDARY, 5), ("tiny", 50), ("vit196", 20),
+                     ("gpt2_f32", 20), ("gpt2_bf16", 20)):
+            try:
+                backward.append(measure_backward(n, device, r))
+            except Exception as exc:   # reported, not fatal to the forward's line
+                backward.append({"workload": n, "error": "%s: %s" % (type(exc).__name__, exc)})
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
