@@ -75,6 +75,10 @@ def _lib():
         lib.oracle_circ_transpose_fft.restype = ctypes.c_int
         lib.oracle_corr_fft.argtypes = [dp, dp, L, L, L, L, dp, dp]
         lib.oracle_corr_fft.restype = ctypes.c_int
+        lib.oracle_corr2d_direct.argtypes = [dp, dp, L, L, L, L, L, ctypes.c_double, dp]
+        lib.oracle_corr2d_direct.restype = None
+        lib.oracle_circ2d_direct.argtypes = [dp, dp, L, L, L, L, L, dp]
+        lib.oracle_circ2d_direct.restype = None
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = ctypes.c_int
         _LIB = lib
@@ -332,8 +336,95 @@ def backward(X, WA, V, G, mode="auto"):
     return dict(dX=grad_x(dz, WA), dWA=grad_wa(X, dz), dV=dV, zs=zs, dzs=dzs, dz=dz)
 
 
+# --------------------------------------------------------------------------
+# 2-D circulant attention (page "Vision Transformers are Circulant Attention
+# Learners"): tokens on an h x w grid (n = y·w + x), attention map a BCCB
+# matrix with generator σ(a), O = σ(a) ⊛ V (2-D circular convolution).
+# Reading for a (the page gives none): the channel-averaged 2-D circular
+# cross-correlation of Q and K, a[k] = (1/dh) Σ_c Σ_i Q[i, c] K[i ⊖ k, c].
+# --------------------------------------------------------------------------
+
+def corr2d_direct(Q, K, H, h, w, scale=None):
+    """a[b, hd, k] = scale · Σ_{c in hd} Σ_i Q[b,i,c] K[b, i ⊖ k, c] by the
+    definition (scale defaults to 1/dh): [B, H, h·w]."""
+    Q, K = _f64(Q), _f64(K)
+    B, N, D = Q.shape
+    assert N == h * w
+    if scale is None:
+        scale = 1.0 / (D // H)
+    a = np.empty((B, H, N), np.float64)
+    _lib().oracle_corr2d_direct(_p(Q), _p(K), B, h, w, D, H, float(scale), _p(a))
+    return a
+
+
+def corr2d_fft(Q, K, H, h, w, scale=None):
+    """The same by the correlation theorem with numpy's 2-D FFT:
+    a = scale · Re IFFT2( Σ_c FFT2(Q_c) ⊙ conj(FFT2(K_c)) )."""
+    Q, K = _f64(Q), _f64(K)
+    B, N, D = Q.shape
+    dh = D // H
+    if scale is None:
+        scale = 1.0 / dh
+    q = Q.reshape(B, h, w, H, dh)
+    k = K.reshape(B, h, w, H, dh)
+    spec = (np.fft.fft2(q, axes=(1, 2)) * np.conj(np.fft.fft2(k, axes=(1, 2)))).sum(axis=4)
+    a = np.real(np.fft.ifft2(spec, axes=(1, 2)))          # [B, h, w, H]
+    return scale * np.ascontiguousarray(a.transpose(0, 3, 1, 2).reshape(B, H, N))
+
+
+def circ2d_direct(g, V, h, w):
+    """O = BCCB(g) V by the definition: O[b,i,c] = Σ_j g[b,head(c), i ⊖ j] V[b,j,c]."""
+    g, V = _f64(g), _f64(V)
+    B, N, D = V.shape
+    H = g.shape[1]
+    assert N == h * w
+    O = np.empty((B, N, D), np.float64)
+    _lib().oracle_circ2d_direct(_p(g), _p(V), B, h, w, D, H, _p(O))
+    return O
+
+
+def circ2d_fft(g, V, h, w):
+    """The same by the 2-D convolution theorem (numpy's 2-D FFT)."""
+    g, V = _f64(g), _f64(V)
+    B, N, D = V.shape
+    H = g.shape[1]
+    dh = D // H
+    gf = np.fft.fft2(g.reshape(B, H, h, w), axes=(2, 3))            # [B, H, h, w]
+    vf = np.fft.fft2(V.reshape(B, h, w, H, dh), axes=(1, 2))        # [B, h, w, H, dh]
+    o = np.real(np.fft.ifft2(vf * gf.transpose(0, 2, 3, 1)[..., None], axes=(1, 2)))
+    return np.ascontiguousarray(o.reshape(B, N, D))
+
+
+def bccb_matrix(g2d):
+    """The explicit N x N BCCB matrix of a generator g2d [h, w]."""
+    g2d = np.asarray(g2d, dtype=np.float64)
+    h, w = g2d.shape
+    n = np.arange(h * w)
+    yi, xi = (n // w)[:, None], (n % w)[:, None]
+    yj, xj = (n // w)[None, :], (n % w)[None, :]
+    return g2d[(yi - yj) % h, (xi - xj) % w]
+
+
+def forward2d(Q, K, V, H, h, w, mode="auto"):
+    """2-D circulant attention: returns (O [B,N,D], a [B,H,N], σ(a) [B,H,N])."""
+    Q, K, V = _f64(Q), _f64(K), _f64(V)
+    B, N, D = V.shape
+    if mode == "auto":
+        mode = "direct" if B * N * N * D <= 2e9 else "fft"
+    if mode == "direct":
+        a = corr2d_direct(Q, K, H, h, w)
+        zs = softmax(a)
+        return circ2d_direct(zs, V, h, w), a, zs
+    if mode == "fft":
+        a = corr2d_fft(Q, K, H, h, w)
+        zs = softmax(a)
+        return circ2d_fft(zs, V, h, w), a, zs
+    raise ValueError(mode)
+
+
 __all__ = ["scores", "softmax", "zstar", "dft", "spectrum", "circ_direct",
            "circ_direct_rows", "circ_fft", "brute_circulant", "forward",
            "num_threads", "circ_transpose_direct", "circ_transpose_direct_rows",
            "circ_transpose_fft", "corr_direct", "corr_direct_bins", "corr_fft",
-           "softmax_backward", "grad_wa", "grad_x", "backward"]
+           "softmax_backward", "grad_wa", "grad_x", "backward", "corr2d_direct",
+           "corr2d_fft", "circ2d_direct", "circ2d_fft", "bccb_matrix", "forward2d"]

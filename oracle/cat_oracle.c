@@ -526,6 +526,68 @@ int oracle_corr_fft(const double *G, const double *V, long B, long N, long D,
   return fail ? -1 : 0;
 }
 
+/* ------------------------------------------------------------------------
+ * 2-D circulant attention (the page "Vision Transformers are Circulant
+ * Attention Learners", sections on the BCCB structure and "Circulant
+ * Attention: 用FFT重构注意力"): tokens on an h x w grid, token n = y·w + x.
+ * The attention map is a BCCB matrix (block circulant with circulant
+ * blocks) with generator g over the grid,
+ *     M[i, j] = g[(y_i - y_j) mod h, (x_i - x_j) mod w],
+ * so M·v is the 2-D circular convolution of g with v: O = σ(a) ⊛ V.
+ * Reading (the page prints no formula for a): a is the channel-averaged
+ * 2-D circular cross-correlation of Q and K, the sum along each wrapped
+ * 2-D diagonal of Q·K^T,
+ *     a[b, hd, k] = scale · Σ_{c in head hd} Σ_i Q[b, i, c] · K[b, i ⊖ k, c],
+ * with i ⊖ k the grid-wise difference mod (h, w) and scale = 1/dh.
+ * ------------------------------------------------------------------------ */
+
+/* Grid index of (y_i - y_k) mod h, (x_i - x_k) mod w for token indices. */
+static long grid_sub(long i, long k, long h, long w) {
+  long yi = i / w, xi = i % w, yk = k / w, xk = k % w;
+  long y = yi - yk, x = xi - xk;
+  if (y < 0) y += h;
+  if (x < 0) x += w;
+  return y * w + x;
+}
+
+/* a = scale · Σ_{c in head} Σ_i Q[i, c] K[i ⊖ k, c], every lag k. */
+void oracle_corr2d_direct(const double *Q, const double *K, long B, long h,
+                          long w, long D, long H, double scale, double *a) {
+  const long N = h * w, dh = D / H;
+  long b, hd;
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+  for (b = 0; b < B; ++b) {
+    for (hd = 0; hd < H; ++hd) {
+      for (long k = 0; k < N; ++k) {
+        double acc = 0.0;
+        for (long c = hd * dh; c < (hd + 1) * dh; ++c)
+          for (long i = 0; i < N; ++i)
+            acc += Q[(b * N + i) * D + c] * K[(b * N + grid_sub(i, k, h, w)) * D + c];
+        a[(b * H + hd) * N + k] = scale * acc;
+      }
+    }
+  }
+}
+
+/* O = BCCB(g) · V: O[b, i, c] = Σ_j g[b, head(c), i ⊖ j] · V[b, j, c]. */
+void oracle_circ2d_direct(const double *g, const double *V, long B, long h,
+                          long w, long D, long H, double *O) {
+  const long N = h * w;
+  long b, i;
+#pragma omp parallel for collapse(2) schedule(static)
+  for (b = 0; b < B; ++b) {
+    for (i = 0; i < N; ++i) {
+      for (long c = 0; c < D; ++c) {
+        const double *gr = g + (b * H + head_of(c, D, H)) * N;
+        double acc = 0.0;
+        for (long j = 0; j < N; ++j)
+          acc += gr[grid_sub(i, j, h, w)] * V[(b * N + j) * D + c];
+        O[(b * N + i) * D + c] = acc;
+      }
+    }
+  }
+}
+
 /* Number of OpenMP threads the oracle will use (1 without OpenMP). */
 int oracle_num_threads(void) {
 #ifdef _OPENMP

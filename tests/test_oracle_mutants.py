@@ -59,9 +59,24 @@ BACKWARD_MUTANTS = {
                       "acc += X[(b * N + n) * D + d] * dz[(b * H + h) * N + (N - 1 - n)];"),
 }
 
+# Mistakes in the 2-D circulant attention, caught by the 2-D pins.
+TWOD_MUTANTS = {
+    # x offsets wrapped with the wrong period
+    "wrap_period": ("if (x < 0) x += w;", "if (x < 0) x += h;"),
+    # grid difference reversed along x only
+    "x_direction": ("long y = yi - yk, x = xi - xk;", "long y = yi - yk, x = xk - xi;"),
+    # correlation lag reversed (K[i ⊕ k] instead of K[i ⊖ k])
+    "corr2d_lag": ("K[(b * N + grid_sub(i, k, h, w)) * D + c]",
+                   "K[(b * N + grid_sub(k, i, h, w)) * D + c]"),
+    # BCCB generator read transposed
+    "bccb_transposed": ("acc += gr[grid_sub(i, j, h, w)] * V[(b * N + j) * D + c];",
+                        "acc += gr[grid_sub(j, i, h, w)] * V[(b * N + j) * D + c];"),
+}
+
 
 def _build_mutant(tmp_path, name):
-    old, new = MUTANTS[name] if name in MUTANTS else BACKWARD_MUTANTS[name]
+    table = {**MUTANTS, **BACKWARD_MUTANTS, **TWOD_MUTANTS}
+    old, new = table[name]
     src = open(SRC).read()
     assert src.count(old) >= 1, name
     d = tmp_path / name
@@ -130,6 +145,37 @@ def _backward_pins_fail():
     return failed > 0
 
 
+def _twod_pins_fail():
+    import test_oracle_2d_pins as P
+    checks = [
+        lambda: P.test_one_row_grid_is_1d_cat(1, 9),
+        lambda: P.test_bccb_matrix_brute_force(3, 4),
+        lambda: P.test_scores_are_diagonal_sums_of_qkt(3, 5),
+        lambda: P.test_one_hot_generator_is_2d_shift(1, 2),
+        P.test_separable_generator,
+        lambda: P.test_direct_equals_fft(7, 12),
+    ]
+    failed = 0
+    for c in checks:
+        try:
+            c()
+        except AssertionError:
+            failed += 1
+    return failed > 0
+
+
+@pytest.mark.parametrize("name", sorted(TWOD_MUTANTS))
+def test_twod_pins_catch_mutant(tmp_path, name):
+    if shutil.which("gcc") is None:
+        pytest.skip("gcc not available")
+    lib = _build_mutant(tmp_path, name)
+    saved = _with_lib(lib)
+    try:
+        assert _twod_pins_fail(), "mutant %s passed every 2-D pin" % name
+    finally:
+        oracle._LIB = saved
+
+
 @pytest.mark.parametrize("name", sorted(BACKWARD_MUTANTS))
 def test_backward_pins_catch_mutant(tmp_path, name):
     if shutil.which("gcc") is None:
@@ -166,5 +212,6 @@ def test_unmutated_copy_passes_pins(tmp_path):
     try:
         assert not _pins_fail()
         assert not _backward_pins_fail()
+        assert not _twod_pins_fail()
     finally:
         oracle._LIB = saved
