@@ -13,7 +13,9 @@ between steps.
 
 The line also carries the backward pass (cat_backward: dX, dW_A, dV for an
 upstream gradient) at the long-sequence and the short workloads, with its
-roofline fraction; --backward-only times just that on --config.
+roofline fraction; --backward-only times just that on --config.  It also
+carries the 2-D (BCCB) circulant attention of a second page on its token-grid
+workloads (--no-grid2d leaves them out).
 
 Prints ONE JSON line (rank 0).  With --impl reference the fp64 CPU oracle
 is timed instead, on a bounded sample of the same workload.
@@ -413,6 +415,46 @@ def measure_backward(name, device, reps, warmup=3):
             "algorithmic_bytes": a["bytes"], "fft_flops": a["flops"], "reps": reps}
 
 
+def measure_grid2d(name, device, reps=20, warmup=3):
+    """ms per cat2d_forward (2-D circulant attention on a token grid;
+    resident inputs, plan's stream, CUDA events)."""
+    import fft_circulant_attention_gb300 as cat
+    c = dict(synth.GRID_CONFIGS[name])
+    B, h, w, D, H = c["B"], c["h"], c["w"], c["D"], c["H"]
+    Q, K, V = (t.to(device) for t in synth.make_qkv(B, h * w, D, c["dtype"], seed=0))
+    O = torch.empty_like(V)
+    stream = torch.cuda.current_stream(device)
+    with cat.Plan2D(B, h, w, D, H, c["dtype"], stream=stream) as plan:
+        for _ in range(warmup):
+            plan.forward(Q, K, V, O)
+        plan.sync()
+        torch.cuda.synchronize(device)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            plan.forward(Q, K, V, O)
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        plan.sync()
+        desc = plan.describe()
+    ms = e0.elapsed_time(e1) / reps
+    N = h * w
+    es = 2 if c["dtype"] == "bf16" else 4
+    npair = (D // H + 1) // 2
+    # Q, K, V read and O written; transforms: a forward per Q and K pair, one
+    # inverse per (b, h) for the scores, then the product (a forward and an
+    # inverse per V pair, one forward of σ(a)), each 5·N·log2(N) flops.
+    nbytes = 4 * B * N * D * es
+    flops = (4 * B * H * npair + 2 * B * H) * fft_flops(N)
+    hbm, _ = load_peaks()
+    t_roof = max(nbytes / (hbm * 1e9), flops / (FP32_PEAK_TFLOPS * 1e12))
+    return {"workload": name, "B": B, "grid": [h, w], "D": D, "H": H, "storage": c["dtype"],
+            "ms_per_step": ms, "value": B * N * H / (ms * 1e-3), "unit": UNIT,
+            "path_roofline_frac": t_roof / (ms * 1e-3), "t_roof_us": t_roof * 1e6,
+            "plan": desc, "reps": reps}
+
+
 # The short-sequence configurations of the workload table (parity cases of
 # the tests; timed here so that every path has a measured figure).
 SHORT = ["tiny", "vit196", "gpt2_f32", "gpt2_bf16"]
@@ -467,6 +509,15 @@ def run_gb300(args, world, rank, local):
     if not args.no_secondary and args.config != SECONDARY:
         sec = measure_workload(SECONDARY, max(3, args.steps // 4), args.warmup, device, world)
     short = [] if args.no_short else [measure_short(n, device) for n in SHORT]
+    grid2d = []
+    if not args.no_grid2d:
+        # The 2-D (BCCB) circulant attention of the token-grid workloads; a
+        # failure is recorded in its entry.
+        for n in synth.GRID_CONFIGS:
+            try:
+                grid2d.append(measure_grid2d(n, device))
+            except Exception as exc:
+                grid2d.append({"workload": n, "error": "%s: %s" % (type(exc).__name__, exc)})
     backward = []
     if not args.no_backward:
         # The backward pass at the two long workloads and the short ones; a
@@ -526,6 +577,8 @@ def run_gb300(args, world, rank, local):
         line["short_configs"] = short
     if backward:
         line["backward"] = backward
+    if grid2d:
+        line["grid2d"] = grid2d
     print(json.dumps(line), flush=True)
 
 
@@ -540,6 +593,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-short", action="store_true")
     ap.add_argument("--no-backward", action="store_true")
+    ap.add_argument("--no-grid2d", action="store_true")
     ap.add_argument("--backward-only", action="store_true",
                     help="time only cat_backward on --config (--steps calls) and print it")
     ap.add_argument("--sample-heads", type=int, default=0)

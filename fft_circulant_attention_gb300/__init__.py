@@ -13,10 +13,12 @@ and importing it fails loudly when the library has not been built.
 
 The functions carry the C names: ``cat_plan_create``, ``cat_forward``,
 ``cat_forward_zstar``, ``cat_forward_host``, ``cat_backward``,
-``cat_backward_dz``, ``cat_plan_sync``,
+``cat_backward_dz``, ``cat_plan_create_2d``, ``cat2d_forward``, ``cat2d_scores``,
+``cat_plan_sync``,
 ``cat_plan_timing``, ``cat_plan_stage_times``, ``cat_plan_pass_times``,
 ``cat_plan_describe``, ``cat_plan_set_stream``, ``cat_plan_destroy`` and
-``cat_status_string``.  ``Plan`` wraps them for convenience.
+``cat_status_string``.  ``Plan`` (1-D) and ``Plan2D`` (token grid) wrap them
+for convenience.
 """
 import ctypes
 import os
@@ -55,6 +57,9 @@ SIGNATURES = {
     "cat_forward_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "cat_backward": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I]),
     "cat_backward_dz": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I]),
+    "cat_plan_create_2d": (_I, [ctypes.POINTER(_P), _I, _I, _I, _I, _I, _I, _P]),
+    "cat2d_forward": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I]),
+    "cat2d_scores": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I]),
     "cat_status_string": (ctypes.c_char_p, [_I]),
 }
 
@@ -176,6 +181,24 @@ def cat_backward(plan, X, W_A, V, dO, dX, dW_A, dV, B, N, D, H, dtype):
 def cat_backward_dz(plan, X, W_A, V, dO, dzstar, dz, B, N, D, H, dtype):
     _check(lib().cat_backward_dz(plan, _ptr(X), _ptr(W_A), _ptr(V), _ptr(dO), _ptr(dzstar),
                                  _ptr(dz), B, N, D, H, dtype_code(dtype)), "cat_backward_dz")
+
+
+def cat_plan_create_2d(B, h, w, D, H, dtype, stream=None):
+    """Create a 2-D (h x w token grid) plan; returns its handle."""
+    hd = ctypes.c_void_p()
+    _check(lib().cat_plan_create_2d(ctypes.byref(hd), B, h, w, D, H, dtype_code(dtype),
+                                    _stream(stream)), "cat_plan_create_2d")
+    return hd.value
+
+
+def cat2d_forward(plan, Q, K, V, O, B, h, w, D, H, dtype):
+    _check(lib().cat2d_forward(plan, _ptr(Q), _ptr(K), _ptr(V), _ptr(O), B, h, w, D, H,
+                               dtype_code(dtype)), "cat2d_forward")
+
+
+def cat2d_scores(plan, Q, K, a, B, h, w, D, H, dtype):
+    _check(lib().cat2d_scores(plan, _ptr(Q), _ptr(K), _ptr(a), B, h, w, D, H,
+                              dtype_code(dtype)), "cat2d_scores")
 
 
 def cat_plan_sync(plan):
@@ -303,9 +326,67 @@ class Plan:
             pass
 
 
-__all__ = ["CatError", "Plan", "lib", "dtype_code", "cat_plan_create", "cat_plan_destroy",
+class Plan2D:
+    """Owns one 2-D circulant-attention plan for a fixed (B, h, w, D, H, dtype):
+    ``forward(Q, K, V, O=None)`` with CUDA tensors [B, h·w, D] of the plan's
+    dtype; ``scores(Q, K)`` returns the fp32 scores a [B, H, h·w]."""
+
+    def __init__(self, B, h, w, D, H, dtype, stream=None):
+        import torch
+        self.B, self.h, self.w, self.D, self.H = B, h, w, D, H
+        self.dtype = dtype_code(dtype)
+        self.torch_dtype = torch.bfloat16 if self.dtype == CAT_BF16 else torch.float32
+        if stream is None and torch.cuda.is_available():
+            stream = torch.cuda.current_stream()
+        self.handle = cat_plan_create_2d(B, h, w, D, H, self.dtype, stream)
+
+    def _shape(self):
+        return (self.B, self.h, self.w, self.D, self.H, self.dtype)
+
+    def forward(self, Q, K, V, O=None):
+        import torch
+        if O is None:
+            O = torch.empty_like(V)
+        for t in (Q, K, V, O):
+            if not t.is_contiguous() or t.dtype != self.torch_dtype:
+                raise ValueError("tensors must be contiguous %s" % self.torch_dtype)
+        cat2d_forward(self.handle, Q, K, V, O, *self._shape())
+        return O
+
+    def scores(self, Q, K):
+        import torch
+        a = torch.empty((self.B, self.H, self.h * self.w), dtype=torch.float32, device=Q.device)
+        cat2d_scores(self.handle, Q, K, a, *self._shape())
+        return a
+
+    def sync(self):
+        cat_plan_sync(self.handle)
+
+    def describe(self):
+        return cat_plan_describe(self.handle)
+
+    def close(self):
+        if self.handle:
+            cat_plan_destroy(self.handle)
+            self.handle = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+__all__ = ["CatError", "Plan", "Plan2D", "lib", "dtype_code", "cat_plan_create", "cat_plan_destroy",
            "cat_plan_set_stream", "cat_forward", "cat_forward_zstar", "cat_forward_host",
            "cat_plan_sync", "cat_plan_describe", "cat_plan_timing", "cat_plan_stage_times",
            "cat_plan_pass_times", "cat_forward_noalloc", "cat_backward", "cat_backward_dz",
+           "cat_plan_create_2d", "cat2d_forward", "cat2d_scores",
            "cat_status_string", "CAT_F32", "CAT_BF16",
            "SIGNATURES", "LIB_PATH"]

@@ -63,7 +63,7 @@ __global__ void reverse_scores_kernel(float2* __restrict__ z, int N, long long i
 // Shared layout: signal (t, s) at buf[(t·S + s)·N2], S = 2·gc; s < gc are
 // G pairs g0 + s, s >= gc the V pairs g0 + s - gc.
 // ---------------------------------------------------------------------------
-template <typename T>
+template <typename T, bool TW>
 __global__ void __launch_bounds__(1024)
 corr_pass_a(const T* __restrict__ G, const T* __restrict__ V, float2* __restrict__ scr,
             const float2* __restrict__ W, RadixPlan rp2, int N, int N1, int D, int H, int dh,
@@ -118,7 +118,8 @@ corr_pass_a(const T* __restrict__ G, const T* __restrict__ V, float2* __restrict
     const int s = idx % S, q = idx / S;
     const int t = q % TA, k2 = q / TA;
     const int n1 = n1_0 + t;
-    const float2 v = cmul(buf[(t * S + s) * N2 + k2], __ldg(&W[(size_t)n1 * k2]));
+    float2 v = buf[(t * S + s) * N2 + k2];
+    if (TW) v = cmul(v, __ldg(&W[(size_t)n1 * k2]));
     const int qi = s < gc ? g0 + s : npair + g0 + (s - gc);
     srow[((size_t)k2 * N1 + n1) * Q + qi] = v;
   }
@@ -130,6 +131,7 @@ corr_pass_a(const T* __restrict__ G, const T* __restrict__ V, float2* __restrict
 // (S = 2·gc: G pairs, then V pairs); the running sum of FFT(g)·conj(FFT(v))
 // for k2-slot t at acc[t·N1 + k1], after the chunk buffer.
 // ---------------------------------------------------------------------------
+template <bool TW>
 __global__ void __launch_bounds__(1024)
 corr_pass_b(float2* __restrict__ scr, const float2* __restrict__ W, RadixPlan rp1, int N,
             int N2, int npair, int GB, int TB, int Q, unsigned int* status) {
@@ -179,7 +181,7 @@ corr_pass_b(float2* __restrict__ scr, const float2* __restrict__ W, RadixPlan rp
   for (int idx = threadIdx.x; idx < npts; idx += blockDim.x) {
     const int n1 = idx % N1, t = idx / N1;
     const int k2 = k2_0 + t;
-    srow[((size_t)k2 * N1 + n1) * Q] = cmulc(acc[idx], __ldg(&W[(size_t)n1 * k2]));
+    srow[((size_t)k2 * N1 + n1) * Q] = TW ? cmulc(acc[idx], __ldg(&W[(size_t)n1 * k2])) : acc[idx];
   }
 }
 
@@ -487,10 +489,14 @@ dx_kernel(const float* __restrict__ dz, const T* __restrict__ WA, T* __restrict_
 cudaError_t setup_backward_kernels(const cat_plan_s* p) {
   cudaError_t e = p->dtype == 1 ? allow_max_smem(dx_kernel<__nv_bfloat16>)
                                 : allow_max_smem(dx_kernel<float>);
-  if (e == cudaSuccess) e = allow_max_smem(corr_pass_b);
+  const bool tw = !p->twod;
+  if (e == cudaSuccess) e = tw ? allow_max_smem(corr_pass_b<true>) : allow_max_smem(corr_pass_b<false>);
   if (e == cudaSuccess) e = allow_max_smem(corr_pass_c);
   if (e == cudaSuccess)
-    e = p->dtype == 1 ? allow_max_smem(corr_pass_a<__nv_bfloat16>) : allow_max_smem(corr_pass_a<float>);
+    e = p->dtype == 1 ? (tw ? allow_max_smem(corr_pass_a<__nv_bfloat16, true>)
+                            : allow_max_smem(corr_pass_a<__nv_bfloat16, false>))
+                      : (tw ? allow_max_smem(corr_pass_a<float, true>)
+                            : allow_max_smem(corr_pass_a<float, false>));
   return e;
 }
 
@@ -504,16 +510,16 @@ cudaError_t launch_reverse_scores(const cat_plan_s* p) {
   return cudaGetLastError();
 }
 
-template <typename T>
+template <typename T, bool TW>
 static cudaError_t corr_t(const cat_plan_s* p, const T* G, const T* V) {
   const BwCfg& w = p->bw;
   const int rows = p->B * p->H;
   for (int bh0 = 0; bh0 < rows; bh0 += w.chunk_bh) {
     const int nb = rows - bh0 < w.chunk_bh ? rows - bh0 : w.chunk_bh;
-    corr_pass_a<T><<<nb * (w.N1 / w.TA) * w.groupsA, w.threadsA, w.smemA, p->stream>>>(
+    corr_pass_a<T, TW><<<nb * (w.N1 / w.TA) * w.groupsA, w.threadsA, w.smemA, p->stream>>>(
         G, V, p->bw_scr, p->tw, w.rp2, p->N, w.N1, p->D, p->H, p->dh, p->npair, w.GA, w.groupsA,
         w.TA, w.Q, bh0, p->status);
-    corr_pass_b<<<nb * (w.N2 / w.TB), w.threadsB, w.smemB, p->stream>>>(
+    corr_pass_b<TW><<<nb * (w.N2 / w.TB), w.threadsB, w.smemB, p->stream>>>(
         p->bw_scr, p->tw, w.rp1, p->N, w.N2, p->npair, w.GB, w.TB, w.Q, p->status);
     corr_pass_c<<<nb * (w.N1 / w.TC), w.threadsC, w.smemC, p->stream>>>(
         p->bw_scr, p->bw_dzs, p->tw, w.rp2, p->N, w.N1, w.TC, w.Q, bh0, p->status);
@@ -549,10 +555,42 @@ cudaError_t launch_backward_dz(const cat_plan_s* p, const void* G, const void* V
   const int rows = p->B * p->H;
   if (rows == 0) return cudaSuccess;
   const cudaError_t e = p->bw.fast ? corr_fast(p, G, V)
-      : p->dtype == 1 ? corr_t(p, (const __nv_bfloat16*)G, (const __nv_bfloat16*)V)
-                      : corr_t(p, (const float*)G, (const float*)V);
+      : p->dtype == 1 ? corr_t<__nv_bfloat16, true>(p, (const __nv_bfloat16*)G, (const __nv_bfloat16*)V)
+                      : corr_t<float, true>(p, (const float*)G, (const float*)V);
   if (e != cudaSuccess) return e;
   softmax_bw_kernel<<<rows, kSmBwThreads, 0, p->stream>>>(p->zs, p->bw_dzs, p->bw_dz, p->N);
+  return cudaGetLastError();
+}
+
+
+// ---------------------------------------------------------------------------
+// 2-D circulant attention scores (page "Vision Transformers are Circulant
+// Attention Learners"): a = scale · Σ_{c in head} corr2d(Q_c, K_c), the
+// correlation passes above without their twiddles over the h x w grid
+// (N1 = w, N2 = h), then a stored as the softmax's scores (hi = a, lo = 0).
+// ---------------------------------------------------------------------------
+__global__ void scores_from_corr_kernel(const float* __restrict__ a, float2* __restrict__ z2,
+                                        float* __restrict__ out, float scale, long long count) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < count;
+       i += (long long)gridDim.x * blockDim.x) {
+    const float v = a[i] * scale;
+    z2[i] = make_float2(v, 0.f);
+    if (out) out[i] = v;
+  }
+}
+
+cudaError_t launch_scores2d(const cat_plan_s* p, const void* Q, const void* K, float* out) {
+  const int rows = p->B * p->H;
+  if (rows == 0) return cudaSuccess;
+  cudaError_t e = p->dtype == 1
+      ? corr_t<__nv_bfloat16, false>(p, (const __nv_bfloat16*)Q, (const __nv_bfloat16*)K)
+      : corr_t<float, false>(p, (const float*)Q, (const float*)K);
+  if (e != cudaSuccess) return e;
+  const long long count = (long long)rows * p->N;
+  long long blocks = (count + 255) / 256;
+  if (blocks > 8ll * p->sms) blocks = 8ll * p->sms;
+  scores_from_corr_kernel<<<(int)blocks, 256, 0, p->stream>>>(p->bw_dzs, p->z2, out,
+                                                              1.0f / (float)p->dh, count);
   return cudaGetLastError();
 }
 

@@ -161,6 +161,8 @@ int score_launches(int H, int D) {
   return (H + hpp - 1) / hpp;
 }
 
+int configure_fourstep(cat_plan_s* p, int N1, int N2);
+
 int choose_path(cat_plan_s* p) {
   const int N = p->N;
   // CAT_FORCE_PATH=fourstep sends short sequences down the multi-pass path
@@ -205,9 +207,18 @@ int choose_path(cat_plan_s* p) {
     }
   }
   if (N <= kSmemMaxN && !force_fs) return cat::configure_smem_path(p);
+  if (!split_fourstep(N, &n1, &n2)) return CAT_ERR_UNSUPPORTED_N;
+  return configure_fourstep(p, n1, n2);
+}
+
+// The generic four-step path for the split N = N1·N2 (both 7-smooth, at
+// most 16384; a 2-D plan passes N1 = w, N2 = h).
+int configure_fourstep(cat_plan_s* p, int N1, int N2) {
+  const int N = p->N;
   p->path = cat::PATH_FOURSTEP;
   cat::FourStepCfg& f = p->fs;
-  if (!split_fourstep(N, &f.N1, &f.N2)) return CAT_ERR_UNSUPPORTED_N;
+  f.N1 = N1;
+  f.N2 = N2;
   if (!make_radix_plan(f.N1, &f.rp1) || !make_radix_plan(f.N2, &f.rp2))
     return CAT_ERR_UNSUPPORTED_N;
   if (!make_radix_plan(N, &p->rpN)) return CAT_ERR_UNSUPPORTED_N;
@@ -271,10 +282,11 @@ void describe(cat_plan_s* p) {
     radstr(p->fs.rp1, r1, sizeof(r1));
     radstr(p->fs.rp2, r2, sizeof(r2));
     std::snprintf(p->desc, sizeof(p->desc),
-                  "path=fourstep N=%d N1=%d(%s) N2=%d(%s) G=%d groups=%d TA=%d TB=%d "
+                  "path=%s N=%d N1=%d(%s) N2=%d(%s) G=%d groups=%d TA=%d TB=%d "
                   "threads=%d/%d/%d smem=%zu/%zu/%zu chunk_bh=%d scratch=%zu workspace=%zu "
                   "launches=%d",
-                  p->N, p->fs.N1, r1, p->fs.N2, r2, p->fs.G, p->fs.groups, p->fs.TA, p->fs.TB,
+                  p->twod ? "grid2d" : "fourstep", p->N, p->fs.N1, r1, p->fs.N2, r2, p->fs.G,
+                  p->fs.groups, p->fs.TA, p->fs.TB,
                   p->fs.threadsA, p->fs.threadsB, p->fs.threadsC, p->fs.smemA, p->fs.smemB,
                   p->fs.smemC, p->fs.chunk_bh, p->scratch_bytes, p->workspace_bytes,
                   p->launches);
@@ -292,6 +304,8 @@ int run_front(cat_plan_s* p, const void* X, const void* WA) {
   return map_cuda(e);
 }
 
+
+int configure_corr(cat_plan_s* p, int N1, int N2);
 
 // Launch shapes of the backward correlation (host only, no allocation).
 // Rows up to 4096 are transformed whole in pass B (N1 = N, N2 = 1); longer
@@ -322,12 +336,23 @@ int configure_backward(cat_plan_s* p) {
     w.wsplit = cat::backward_wsplit((long long)p->B * N, p->D, p->H, p->sms > 0 ? p->sms : 148);
     return CAT_OK;
   }
-  if (N <= 4096) {
-    w.N1 = N;
-    w.N2 = 1;
-  } else if (!split_fourstep(N, &w.N1, &w.N2)) {
+  int n1 = N, n2 = 1;
+  if (p->twod) {
+    n1 = p->grid_w;
+    n2 = p->grid_h;
+  } else if (N > 4096 && !split_fourstep(N, &n1, &n2)) {
     return CAT_ERR_UNSUPPORTED_N;
   }
+  return configure_corr(p, n1, n2);
+}
+
+// Launch shapes of the generic correlation passes for the split N = N1·N2.
+int configure_corr(cat_plan_s* p, int N1, int N2) {
+  cat::BwCfg& w = p->bw;
+  const int N = p->N;
+  const size_t c8 = sizeof(float2);
+  w.N1 = N1;
+  w.N2 = N2;
   if (!make_radix_plan(w.N1, &w.rp1) || !make_radix_plan(w.N2, &w.rp2))
     return CAT_ERR_UNSUPPORTED_N;
   const int np = p->npair;
@@ -537,7 +562,29 @@ cudaError_t launch_fast_graph(cat_plan_s* p, const void* X, const void* WA, cons
 
 }  // namespace
 
+namespace {
+int create_plan(cat_plan_t* out, int B, int N, int D, int H, int dtype, void* stream, int gh,
+                int gw);
+}
+
 int cat_plan_create(cat_plan_t* out, int B, int N, int D, int H, int dtype, void* stream) {
+  return create_plan(out, B, N, D, H, dtype, stream, 0, 0);
+}
+
+int cat_plan_create_2d(cat_plan_t* out, int B, int h, int w, int D, int H, int dtype,
+                       void* stream) {
+  if (!out) return CAT_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (h < 1 || w < 1) return CAT_ERR_INVALID_ARG;
+  if (h > kSmemMaxN || w > kSmemMaxN || !seven_smooth(h) || !seven_smooth(w))
+    return CAT_ERR_UNSUPPORTED_N;
+  if ((long long)h * w > CAT_MAX_N) return CAT_ERR_UNSUPPORTED_N;
+  return create_plan(out, B, h * w, D, H, dtype, stream, h, w);
+}
+
+namespace {
+int create_plan(cat_plan_t* out, int B, int N, int D, int H, int dtype, void* stream, int gh,
+                int gw) {
   if (!out) return CAT_ERR_INVALID_ARG;
   *out = nullptr;
   int st = validate_shape(B, N, D, H, dtype);
@@ -548,7 +595,16 @@ int cat_plan_create(cat_plan_t* out, int B, int N, int D, int H, int dtype, void
   p->dh = D / H;
   p->npair = (p->dh + 1) / 2;
   p->stream = (cudaStream_t)stream;
-  st = choose_path(p);
+  if (gh > 0) {
+    // 2-D plan: the generic four-step passes over the grid (N1 = w, N2 = h)
+    // without twiddles; the scores come from the correlation passes.
+    p->twod = 1;
+    p->grid_h = gh;
+    p->grid_w = gw;
+    st = configure_fourstep(p, gw, gh);
+  } else {
+    st = choose_path(p);
+  }
   if (st != CAT_OK) { delete p; return st; }
   // Default fork point: after the score when the spectrum is one launch
   // (N2 = 32, where the first passes A then overlap it), else after it.
@@ -616,11 +672,16 @@ int cat_plan_create(cat_plan_t* out, int B, int N, int D, int H, int dtype, void
       e = cudaStreamCreateWithFlags(&p->cap, cudaStreamNonBlocking);
   }
   if (e != cudaSuccess) { free_plan(p); return CAT_ERR_CUDA; }
+  if (p->twod) {
+    st = ensure_backward(p);
+    if (st != CAT_OK) { free_plan(p); return st; }
+  }
   describe(p);
   if (std::getenv("CAT_LOG")) std::fprintf(stderr, "[cat] %s\n", p->desc);
   *out = p;
   return CAT_OK;
 }
+}  // namespace
 
 int cat_plan_destroy(cat_plan_t plan) {
   if (!plan) return CAT_OK;
@@ -643,6 +704,7 @@ int cat_plan_set_stream(cat_plan_t plan, void* stream) {
 int cat_forward(cat_plan_t p, const void* X, const void* WA, const void* V, void* O, int B, int N,
                 int D, int H, int dtype) {
   if (!p) return CAT_ERR_INVALID_ARG;
+  if (p->twod) return CAT_ERR_PLAN_MISMATCH;
   int st = check_shape(p, B, N, D, H, dtype);
   if (st != CAT_OK) return st;
   if (B == 0) return CAT_OK;
@@ -689,6 +751,7 @@ int cat_forward(cat_plan_t p, const void* X, const void* WA, const void* V, void
 int cat_forward_zstar(cat_plan_t p, const void* X, const void* WA, float* zstar, int B, int N,
                       int D, int H, int dtype) {
   if (!p) return CAT_ERR_INVALID_ARG;
+  if (p->twod) return CAT_ERR_PLAN_MISMATCH;
   int st = check_shape(p, B, N, D, H, dtype);
   if (st != CAT_OK) return st;
   if (B == 0) return CAT_OK;
@@ -703,6 +766,7 @@ int cat_forward_zstar(cat_plan_t p, const void* X, const void* WA, float* zstar,
 int cat_forward_host(cat_plan_t p, const void* X, const void* WA, const void* V, void* O, int B,
                      int N, int D, int H, int dtype) {
   if (!p) return CAT_ERR_INVALID_ARG;
+  if (p->twod) return CAT_ERR_PLAN_MISMATCH;
   int st = check_shape(p, B, N, D, H, dtype);
   if (st != CAT_OK) return st;
   if (B == 0) return CAT_OK;
@@ -733,6 +797,7 @@ int cat_forward_host(cat_plan_t p, const void* X, const void* WA, const void* V,
 int cat_backward(cat_plan_t p, const void* X, const void* WA, const void* V, const void* dO,
                  void* dX, void* dWA, void* dV, int B, int N, int D, int H, int dtype) {
   if (!p) return CAT_ERR_INVALID_ARG;
+  if (p->twod) return CAT_ERR_PLAN_MISMATCH;
   int st = check_shape(p, B, N, D, H, dtype);
   if (st != CAT_OK) return st;
   if (B == 0) return CAT_OK;
@@ -778,6 +843,7 @@ int cat_backward(cat_plan_t p, const void* X, const void* WA, const void* V, con
 int cat_backward_dz(cat_plan_t p, const void* X, const void* WA, const void* V, const void* dO,
                     float* dzstar, float* dz, int B, int N, int D, int H, int dtype) {
   if (!p) return CAT_ERR_INVALID_ARG;
+  if (p->twod) return CAT_ERR_PLAN_MISMATCH;
   int st = check_shape(p, B, N, D, H, dtype);
   if (st != CAT_OK) return st;
   if (B == 0) return CAT_OK;
@@ -793,6 +859,37 @@ int cat_backward_dz(cat_plan_t p, const void* X, const void* WA, const void* V, 
   cudaError_t e = cudaMemcpyAsync(dzstar, p->bw_dzs, bytes, cudaMemcpyDeviceToDevice, p->stream);
   if (e == cudaSuccess)
     e = cudaMemcpyAsync(dz, p->bw_dz, bytes, cudaMemcpyDeviceToDevice, p->stream);
+  return map_cuda(e);
+}
+
+int cat2d_scores(cat_plan_t p, const void* Q, const void* K, float* a, int B, int h, int w, int D,
+                 int H, int dtype) {
+  if (!p) return CAT_ERR_INVALID_ARG;
+  if (!p->twod || h != p->grid_h || w != p->grid_w) return CAT_ERR_PLAN_MISMATCH;
+  int st = check_shape(p, B, h * w, D, H, dtype);
+  if (st != CAT_OK) return st;
+  if (B == 0) return CAT_OK;
+  if (!Q || !K || !a) return CAT_ERR_INVALID_ARG;
+  if (((uintptr_t)Q | (uintptr_t)K | (uintptr_t)a) & 15) return CAT_ERR_MISALIGNED;
+  return map_cuda(cat::launch_scores2d(p, Q, K, a));
+}
+
+int cat2d_forward(cat_plan_t p, const void* Q, const void* K, const void* V, void* O, int B,
+                  int h, int w, int D, int H, int dtype) {
+  if (!p) return CAT_ERR_INVALID_ARG;
+  if (!p->twod || h != p->grid_h || w != p->grid_w) return CAT_ERR_PLAN_MISMATCH;
+  int st = check_shape(p, B, h * w, D, H, dtype);
+  if (st != CAT_OK) return st;
+  if (B == 0) return CAT_OK;
+  if (!Q || !K || !V || !O) return CAT_ERR_INVALID_ARG;
+  if (((uintptr_t)Q | (uintptr_t)K | (uintptr_t)V | (uintptr_t)O) & 15) return CAT_ERR_MISALIGNED;
+  const size_t es = dtype == CAT_BF16 ? 2 : 4;
+  const size_t nx = (size_t)B * p->N * D * es;
+  if (ranges_overlap(O, nx, Q, nx) || ranges_overlap(O, nx, K, nx) || ranges_overlap(O, nx, V, nx))
+    return CAT_ERR_ALIAS;
+  cudaError_t e = cat::launch_scores2d(p, Q, K);
+  if (e == cudaSuccess) e = cat::launch_softmax(p);
+  if (e == cudaSuccess) e = cat::launch_fourstep_conv(p, V, O);
   return map_cuda(e);
 }
 

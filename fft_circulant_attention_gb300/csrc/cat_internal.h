@@ -108,6 +108,9 @@ struct cat_plan_s {
   int timing_cap, timing_n;
   int ev_per_call;          // events recorded per call (3 + conv pass boundaries)
   int launches;             // kernel launches per cat_forward
+  // 2-D plan (cat_plan_create_2d): tokens on a grid_h x grid_w grid, the
+  // generic four-step passes without twiddles (N1 = grid_w, N2 = grid_h)
+  int twod, grid_h, grid_w;
   // backward workspace (configured and allocated at the first backward call)
   int bw_ready;
   cat::BwCfg bw;
@@ -214,6 +217,10 @@ cudaError_t launch_backward_dense(const cat_plan_s* p, const void* X, const void
                                   void* dWA);
 cudaError_t launch_reverse_scores(const cat_plan_s* p);
 int backward_wsplit(long long tokens, int D, int H, int sms);
+// 2-D plan: the channel-averaged 2-D correlation of Q and K into the
+// plan's scores z2 (ready for launch_softmax), and into out if given.
+cudaError_t launch_scores2d(const cat_plan_s* p, const void* Q, const void* K,
+                            float* out = nullptr);
 // Fast path (head width 64, N = 512·N2): the correlation's pass A on dO
 // (scratch slot 0) and on V (slot 1), then its pass B into y[bhl][k2][n1]
 // for rows [bh0, bh0 + nb), on stream st.

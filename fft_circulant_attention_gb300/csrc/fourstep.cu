@@ -17,6 +17,10 @@
 // Column pairs (c, c+1) are packed as one complex signal, exactly as in the
 // shared-memory path: the kernel z* is real, so the real and imaginary parts
 // stay separate through the whole product.
+// Without the twiddles (template flag TW = false) the same passes compute
+// the 2-D DFT over an h x w token grid (N1 = w, N2 = h, n = x + w·y): the
+// BCCB product of the page "Vision Transformers are Circulant Attention
+// Learners", O = σ(a) ⊛ V, a 2-D circular convolution.
 #include <cuda_bf16.h>
 
 #include "cat_internal.h"
@@ -27,7 +31,7 @@ namespace cat {
 // Pass A.  blockIdx.x = (bhl · (N1/TA) + tile) · groups + grp.
 // Shared layout: signal (t, s) at buf[(t·S + s)·N2]; s < gc are the CTA's
 // pairs, s = gc is z* (only in group 0).
-template <typename T>
+template <typename T, bool TW>
 __global__ void __launch_bounds__(1024)
 fs_pass_a(const T* __restrict__ V, const float* __restrict__ zs, float2* __restrict__ scr,
           const float2* __restrict__ W, RadixPlan rp2, int N, int N1, int D, int H, int dh,
@@ -87,7 +91,8 @@ fs_pass_a(const T* __restrict__ V, const float* __restrict__ zs, float2* __restr
     int s = idx % S, q = idx / S;
     int t = q % TA, k2 = q / TA;
     int n1 = n1_0 + t;
-    float2 v = cmul(buf[(t * S + s) * N2 + k2], __ldg(&W[(size_t)n1 * k2]));
+    float2 v = buf[(t * S + s) * N2 + k2];
+    if (TW) v = cmul(v, __ldg(&W[(size_t)n1 * k2]));
     int pidx = (s < gc) ? g0 + s : npair;
     srow[((size_t)k2 * N1 + n1) * P + pidx] = v;
   }
@@ -96,6 +101,7 @@ fs_pass_a(const T* __restrict__ V, const float* __restrict__ zs, float2* __restr
 // Pass B.  blockIdx.x = (bhl · (N2/TB) + tile) · groups + grp.
 // Shared layout: pair signal (t, s) at buf[(t·gc + s)·N1], z* of k2-slot t
 // at buf[(TB·gc + t)·N1].
+template <bool TW>
 __global__ void __launch_bounds__(1024)
 fs_pass_b(float2* __restrict__ scr, const float2* __restrict__ W, RadixPlan rp1, int N,
           int N2, int npair, int G, int groups, int TB, int P, unsigned int* status) {
@@ -151,7 +157,8 @@ fs_pass_b(float2* __restrict__ scr, const float2* __restrict__ W, RadixPlan rp1,
     int s = idx % gc, q = idx / gc;
     int n1 = q % N1, t = q / N1;
     int k2 = k2_0 + t;
-    float2 v = cmulc(buf[(t * gc + s) * N1 + n1], __ldg(&W[(size_t)n1 * k2]));
+    float2 v = buf[(t * gc + s) * N1 + n1];
+    if (TW) v = cmulc(v, __ldg(&W[(size_t)n1 * k2]));
     srow[((size_t)k2 * N1 + n1) * P + g0 + s] = v;
   }
 }
@@ -213,10 +220,9 @@ fs_pass_c(const float2* __restrict__ scr, T* __restrict__ O, const float2* __res
 
 template <typename T>
 static cudaError_t setup_t(const cat_plan_s* p) {
-  (void)p;
-  cudaError_t e = allow_max_smem(fs_pass_a<T>);
+  cudaError_t e = p->twod ? allow_max_smem(fs_pass_a<T, false>) : allow_max_smem(fs_pass_a<T, true>);
   if (e == cudaSuccess) e = allow_max_smem(fs_pass_c<T>);
-  if (e == cudaSuccess) e = allow_max_smem(fs_pass_b);
+  if (e == cudaSuccess) e = p->twod ? allow_max_smem(fs_pass_b<false>) : allow_max_smem(fs_pass_b<true>);
   return e;
 }
 
@@ -224,20 +230,20 @@ cudaError_t setup_fourstep_kernels(const cat_plan_s* p) {
   return p->dtype == 1 ? setup_t<__nv_bfloat16>(p) : setup_t<float>(p);
 }
 
-template <typename T>
+template <typename T, bool TW>
 static cudaError_t run_t(const cat_plan_s* p, const T* V, T* O) {
   const FourStepCfg& f = p->fs;
   const int rows = p->B * p->H;
   for (int bh0 = 0; bh0 < rows; bh0 += f.chunk_bh) {
     int nb = rows - bh0 < f.chunk_bh ? rows - bh0 : f.chunk_bh;
     int ga = nb * (f.N1 / f.TA) * f.groups;
-    fs_pass_a<T><<<ga, f.threadsA, f.smemA, p->stream>>>(
+    fs_pass_a<T, TW><<<ga, f.threadsA, f.smemA, p->stream>>>(
         V, p->zs, p->scratch, p->tw, f.rp2, p->N, f.N1, p->D, p->H, p->dh, p->npair, f.G,
         f.groups, f.TA, f.P, bh0, p->status);
     int gb = nb * (f.N2 / f.TB) * f.groups;
-    fs_pass_b<<<gb, f.threadsB, f.smemB, p->stream>>>(p->scratch, p->tw, f.rp1, p->N, f.N2,
-                                                       p->npair, f.G, f.groups, f.TB, f.P,
-                                                       p->status);
+    fs_pass_b<TW><<<gb, f.threadsB, f.smemB, p->stream>>>(p->scratch, p->tw, f.rp1, p->N, f.N2,
+                                                           p->npair, f.G, f.groups, f.TB, f.P,
+                                                           p->status);
     fs_pass_c<T><<<ga, f.threadsC, f.smemC, p->stream>>>(
         p->scratch, O, p->tw, f.rp2, p->N, f.N1, p->D, p->H, p->dh, p->npair, f.G, f.groups,
         f.TA, f.P, bh0, p->status);
@@ -249,8 +255,14 @@ static cudaError_t run_t(const cat_plan_s* p, const T* V, T* O) {
 
 cudaError_t launch_fourstep_conv(const cat_plan_s* p, const void* V, void* O) {
   if (p->B == 0) return cudaSuccess;
-  if (p->dtype == 1) return run_t(p, (const __nv_bfloat16*)V, (__nv_bfloat16*)O);
-  return run_t(p, (const float*)V, (float*)O);
+  // A 2-D plan (N1 = w, N2 = h) takes the passes without the inter-pass
+  // twiddle: their two DFTs are then the 2-D DFT over the token grid.
+  if (p->twod) {
+    if (p->dtype == 1) return run_t<__nv_bfloat16, false>(p, (const __nv_bfloat16*)V, (__nv_bfloat16*)O);
+    return run_t<float, false>(p, (const float*)V, (float*)O);
+  }
+  if (p->dtype == 1) return run_t<__nv_bfloat16, true>(p, (const __nv_bfloat16*)V, (__nv_bfloat16*)O);
+  return run_t<float, true>(p, (const float*)V, (float*)O);
 }
 
 }  // namespace cat

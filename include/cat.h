@@ -1,6 +1,6 @@
 /*
- * cat.h — C ABI of the GB300 CAT library (libcat.so): the forward pass and
- * its backward pass.
+ * cat.h — C ABI of the GB300 CAT library (libcat.so): the forward pass, its
+ * backward pass, and the 2-D (BCCB) circulant attention of a second page.
  *
  * CAT (circular-convolutional attention), as defined on the notes page
  * "CAT: Circular-Convolutional Attention for Sub-Quadratic Transformers",
@@ -166,6 +166,43 @@ int cat_backward(cat_plan_t plan, const void *X, const void *W_A, const void *V,
 int cat_backward_dz(cat_plan_t plan, const void *X, const void *W_A,
                     const void *V, const void *dO, float *dzstar, float *dz,
                     int B, int N, int D, int H, int dtype);
+
+/*
+ * 2-D circulant attention — the page "Vision Transformers are Circulant
+ * Attention Learners": for tokens on an h x w grid (token n = y·w + x) the
+ * attention map is modelled as a BCCB matrix (block circulant with
+ * circulant blocks) with generator σ(a), so that O = σ(a) ⊛ V, a 2-D
+ * circular convolution, computed with 2-D FFTs; a comes from Q and K by
+ * FFTs and an element-wise product.  The page prints no formula for a; the
+ * reading taken is the channel-averaged 2-D circular cross-correlation
+ *     a[b, hd, k] = (1/dh) Σ_{c in head hd} Σ_i Q[b, i, c] · K[b, i ⊖ k, c]
+ * (i ⊖ k: grid-wise difference mod (h, w)), σ the softmax over the N = h·w
+ * lags, and O[b, i, c] = Σ_j σ(a)[b, hd(c), i ⊖ j] · V[b, j, c].
+ *
+ * cat_plan_create_2d — a plan for B batches on an h x w grid (1 <= h, w <=
+ * 16384, each 7-smooth, h·w <= CAT_MAX_N), model width D, H heads, dtype,
+ * stream; errors as cat_plan_create.  A 2-D plan serves only the cat2d_*
+ * calls (the 1-D calls return CAT_ERR_PLAN_MISMATCH), and the cat2d_* calls
+ * take only 2-D plans.  It allocates its whole workspace at creation.
+ */
+int cat_plan_create_2d(cat_plan_t *out, int B, int h, int w, int D, int H,
+                       int dtype, void *stream);
+
+/*
+ * cat2d_forward — O = σ(a) ⊛ V for every batch and head.  Q, K, V: device
+ * pointers [B, h·w, D], read only; O: device pointer [B, h·w, D], written;
+ * all in the plan's dtype, 16-byte aligned, O not overlapping Q, K or V.
+ * Asynchronous on the plan's stream.
+ */
+int cat2d_forward(cat_plan_t plan, const void *Q, const void *K, const void *V,
+                  void *O, int B, int h, int w, int D, int H, int dtype);
+
+/*
+ * cat2d_scores — only the scores a (before the softmax), fp32 [B, H, h·w],
+ * to the device pointer a (16-byte aligned).
+ */
+int cat2d_scores(cat_plan_t plan, const void *Q, const void *K, float *a,
+                 int B, int h, int w, int D, int H, int dtype);
 
 /*
  * cat_plan_sync — wait for the plan's stream, then read the device status

@@ -11,6 +11,8 @@ masked-LM tokens — have no public inputs here, so i.i.d. Gaussians stand in):
   * X, V ~ N(0, 1) of shape [B, N, D];  W_A ~ N(0, 1/D) · wa_scale, [D, H];
   * the backward pass's upstream gradient dO ~ N(0, 1), [B, N, D], from a
     second, independent stream (``make_grad``);
+  * the 2-D circulant attention's Q, K, V ~ N(0, 1), [B, h·w, D], from a
+    third stream (``make_qkv``);
   * then rounded to the storage dtype (float32 as drawn; bfloat16 by torch's
     round-to-nearest-even conversion).
 """
@@ -53,6 +55,26 @@ def make_grad(B, N, D, dtype="f32", seed=0):
     rng = np.random.Generator(np.random.PCG64([seed, 1]))
     G = rng.standard_normal((B, N, D), dtype=np.float32)
     return torch.from_numpy(G).to(DTYPES[dtype])
+
+
+# 2-D circulant attention workloads (token grids): ViT-S/16 at 224 px (14 x 14
+# patches) and at 1536 px (96 x 96 patches, the page's high-resolution
+# comparison), DeiT-S width 384 with 6 heads.
+GRID_CONFIGS = {
+    "ca_vit196": dict(B=64, h=14, w=14, D=384, H=6, dtype="f32"),
+    "ca_deit1536": dict(B=1, h=96, w=96, D=384, H=6, dtype="bf16"),
+}
+
+
+def make_qkv(B, N, D, dtype="f32", seed=0):
+    """Q, K, V [B, N, D] for the 2-D circulant attention: float32 standard
+    normals from the stream ``PCG64([seed, 2])``, drawn Q, K, V, rounded to
+    ``dtype``."""
+    if dtype not in DTYPES:
+        raise ValueError("dtype must be one of %s" % sorted(DTYPES))
+    rng = np.random.Generator(np.random.PCG64([seed, 2]))
+    out = [rng.standard_normal((B, N, D), dtype=np.float32) for _ in range(3)]
+    return tuple(torch.from_numpy(a).to(DTYPES[dtype]) for a in out)
 
 
 def make_config(name, seed=0, wa_scale=1.0):

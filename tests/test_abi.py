@@ -18,7 +18,7 @@ HEADER = os.path.join(ROOT, "include", "cat.h")
 def _declared():
     src = open(HEADER).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    names = re.findall(r"^\s*(?:const\s+)?\w+\s*\**\s*(cat_\w+)\s*\(", src, flags=re.M)
+    names = re.findall(r"^\s*(?:const\s+)?\w+\s*\**\s*(cat\w+)\s*\(", src, flags=re.M)
     return sorted(set(names))
 
 
@@ -75,6 +75,21 @@ def test_create_rejects_bad_shapes(lib, args, code):
     assert not h
 
 
+@pytest.mark.parametrize("args,code", [
+    ((1, 0, 4, 64, 2, 0, None), cat.CAT_ERR_INVALID_ARG),       # h = 0
+    ((1, 4, -1, 64, 2, 0, None), cat.CAT_ERR_INVALID_ARG),      # w < 0
+    ((1, 11, 4, 64, 2, 0, None), cat.CAT_ERR_UNSUPPORTED_N),    # prime factor 11
+    ((1, 4, 20000, 64, 2, 0, None), cat.CAT_ERR_UNSUPPORTED_N), # side above 16384
+    ((1, 4, 4, 64, 3, 0, None), cat.CAT_ERR_INVALID_ARG),       # D % H != 0
+    ((1, 4, 4, 64, 2, 9, None), cat.CAT_ERR_INVALID_ARG),       # bad dtype
+])
+def test_create_2d_rejects_bad_shapes(lib, args, code):
+    h = ctypes.c_void_p()
+    assert lib.cat_plan_create_2d(ctypes.byref(h), *args) == code
+    assert not h.value
+    assert lib.cat_plan_create_2d(None, *args) == cat.CAT_ERR_INVALID_ARG
+
+
 def test_null_out_pointer(lib):
     assert lib.cat_plan_create(None, 1, 16, 64, 2, 0, None) == cat.CAT_ERR_INVALID_ARG
 
@@ -95,6 +110,8 @@ def test_null_plan_calls(lib):
                             1, 16, 64, 2, 0) == cat.CAT_ERR_INVALID_ARG
     assert lib.cat_backward_dz(None, None, None, None, None, None, None,
                                1, 16, 64, 2, 0) == cat.CAT_ERR_INVALID_ARG
+    assert lib.cat2d_forward(None, None, None, None, None, 1, 4, 4, 64, 2, 0) == cat.CAT_ERR_INVALID_ARG
+    assert lib.cat2d_scores(None, None, None, None, 1, 4, 4, 64, 2, 0) == cat.CAT_ERR_INVALID_ARG
 
 
 def test_python_raises_caterror(lib):
