@@ -8,9 +8,10 @@ the backward is the chain rule through the forward definitions of section
 方法详解 (designs "circulant attention matrix construction" and "FFT
 acceleration").  The pins tie it to things other than its own formulas:
 
-* central finite differences of the (separately pinned) forward oracle for
-  the loss L = sum(O ⊙ G): every gradient, and dL/dz* with z* perturbed
-  directly;
+* exact symbolic derivatives (sympy) of the forward definition for tiny
+  shapes, and central finite differences of the (separately pinned) forward
+  oracle for the loss L = sum(O ⊙ G): every gradient, and dL/dz* with z*
+  perturbed directly;
 * the adjoint (dot-product) identity <circ(z*) V, G> = <V, circ(z*)^T G>;
 * brute force: the explicit N x N circulant transposed, and numpy's roll;
 * closed forms: the 2-token softmax, uniform and one-hot z*;
@@ -216,3 +217,39 @@ def test_sampled_rows_and_bins_match_full():
                           oracle.circ_transpose_direct(zs, G)[:, rows])
     assert np.array_equal(oracle.corr_direct_bins(G, V, H, rows),
                           oracle.corr_direct(G, V, H)[:, :, rows])
+
+
+@pytest.mark.parametrize("N,D,H", [(3, 2, 1), (3, 2, 2), (4, 2, 1)])
+def test_gradients_match_symbolic_differentiation(N, D, H):
+    """Exact gradients: sympy differentiates the forward definition (scores,
+    softmax over tokens, circulant product) of L = Σ O ⊙ G symbolically; the
+    oracle's chain rule must agree to rounding."""
+    sp = pytest.importorskip("sympy")
+    rng = np.random.default_rng(N * 10 + D + H)
+    dh = D // H
+    Xn = np.round(rng.standard_normal((N, D)), 2)
+    Wn = np.round(rng.standard_normal((D, H)), 2)
+    Vn = np.round(rng.standard_normal((N, D)), 2)
+    Gn = np.round(rng.standard_normal((N, D)), 2)
+    X = sp.Matrix(N, D, lambda i, j: sp.Symbol("x_%d_%d" % (i, j)))
+    W = sp.Matrix(D, H, lambda i, j: sp.Symbol("w_%d_%d" % (i, j)))
+    V = sp.Matrix(N, D, lambda i, j: sp.Symbol("v_%d_%d" % (i, j)))
+    L = 0
+    for h in range(H):
+        z = [sum(X[n, d] * W[d, h] for d in range(D)) for n in range(N)]
+        e = [sp.exp(t) for t in z]
+        s = sum(e)
+        zs = [t / s for t in e]
+        for i in range(N):
+            for c in range(h * dh, (h + 1) * dh):
+                O = sum(zs[(i - j) % N] * V[j, c] for j in range(N))
+                L += O * sp.Rational(str(Gn[i, c]))
+    subs = {X[i, j]: sp.Rational(str(Xn[i, j])) for i in range(N) for j in range(D)}
+    subs.update({W[i, j]: sp.Rational(str(Wn[i, j])) for i in range(D) for j in range(H)})
+    subs.update({V[i, j]: sp.Rational(str(Vn[i, j])) for i in range(N) for j in range(D)})
+    g = oracle.backward(Xn[None], Wn, Vn[None], Gn[None], "direct")
+    for name, M, shape in (("dX", X, (N, D)), ("dWA", W, (D, H)), ("dV", V, (N, D))):
+        ref = np.array([[float(sp.N(sp.diff(L, M[i, j]).subs(subs), 30))
+                         for j in range(shape[1])] for i in range(shape[0])])
+        got = g[name][0] if name != "dWA" else g[name]
+        assert np.abs(got - ref).max() <= 1e-12 * (1 + np.abs(ref).max()), name
