@@ -14,6 +14,7 @@ and importing it fails loudly when the library has not been built.
 The functions carry the C names: ``cat_plan_create``, ``cat_forward``,
 ``cat_forward_zstar``, ``cat_forward_host``, ``cat_backward``,
 ``cat_backward_dz``, ``cat_plan_create_2d``, ``cat2d_forward``, ``cat2d_scores``,
+``cat_plan_query``,
 ``cat_plan_sync``,
 ``cat_plan_timing``, ``cat_plan_stage_times``, ``cat_plan_pass_times``,
 ``cat_plan_describe``, ``cat_plan_set_stream``, ``cat_plan_destroy`` and
@@ -58,6 +59,8 @@ SIGNATURES = {
     "cat_backward": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I]),
     "cat_backward_dz": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I]),
     "cat_plan_create_2d": (_I, [ctypes.POINTER(_P), _I, _I, _I, _I, _I, _I, _P]),
+    "cat_plan_query": (_I, [_I, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_size_t), ctypes.c_char_p,
+                            _I]),
     "cat2d_forward": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I]),
     "cat2d_scores": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I]),
     "cat_status_string": (ctypes.c_char_p, [_I]),
@@ -140,6 +143,16 @@ def cat_plan_create(B, N, D, H, dtype, stream=None):
     _check(lib().cat_plan_create(ctypes.byref(h), B, N, D, H, dtype_code(dtype),
                                  _stream(stream)), "cat_plan_create")
     return h.value
+
+
+def cat_plan_query(B, N, D, H, dtype):
+    """(device workspace bytes, description) of the plan cat_plan_create would
+    build for this shape, computed on the host without a device."""
+    nbytes = ctypes.c_size_t(0)
+    buf = ctypes.create_string_buffer(512)
+    _check(lib().cat_plan_query(B, N, D, H, dtype_code(dtype), ctypes.byref(nbytes), buf, 512),
+           "cat_plan_query")
+    return nbytes.value, buf.value.decode()
 
 
 def cat_plan_destroy(plan):
@@ -387,6 +400,6 @@ __all__ = ["CatError", "Plan", "Plan2D", "lib", "dtype_code", "cat_plan_create",
            "cat_plan_set_stream", "cat_forward", "cat_forward_zstar", "cat_forward_host",
            "cat_plan_sync", "cat_plan_describe", "cat_plan_timing", "cat_plan_stage_times",
            "cat_plan_pass_times", "cat_forward_noalloc", "cat_backward", "cat_backward_dz",
-           "cat_plan_create_2d", "cat2d_forward", "cat2d_scores",
+           "cat_plan_create_2d", "cat2d_forward", "cat2d_scores", "cat_plan_query",
            "cat_status_string", "CAT_F32", "CAT_BF16",
            "SIGNATURES", "LIB_PATH"]

@@ -305,6 +305,20 @@ int run_front(cat_plan_s* p, const void* X, const void* WA) {
 }
 
 
+// Device workspace a configured plan allocates at creation: scores (fp32
+// pairs) and z*, the twiddle table, the spectrum of z* (shared-memory and
+// fast paths), the fast path's first-pass spectrum and tables, and the
+// multi-pass scratch.
+size_t planned_workspace(const cat_plan_s* p) {
+  const size_t rowsN = (size_t)p->B * p->H * p->N;
+  const bool fast = p->path == cat::PATH_FAST;
+  return rowsN * (sizeof(float) + sizeof(float2)) + (size_t)p->N * sizeof(float2) +
+         ((p->path == cat::PATH_SMEM || fast) ? rowsN * sizeof(float2) : 0) +
+         (fast ? rowsN * sizeof(float2) : 0) +
+         (p->path != cat::PATH_SMEM ? p->scratch_bytes : 0) +
+         (fast ? cat::fast_tables_bytes(p->fs.N2) : 0);
+}
+
 int configure_corr(cat_plan_s* p, int N1, int N2);
 
 // Launch shapes of the backward correlation (host only, no allocation).
@@ -640,10 +654,7 @@ int create_plan(cat_plan_t* out, int B, int N, int D, int H, int dtype, void* st
     ok = alloc((void**)&p->tabs, cat::fast_tables_bytes(p->fs.N2));
   if (ok && p->path != cat::PATH_SMEM) ok = alloc((void**)&p->scratch, p->scratch_bytes);
   if (!ok) { cudaGetLastError(); free_plan(p); return CAT_ERR_ALLOC; }
-  p->workspace_bytes = rowsN * (sizeof(float) + sizeof(float2)) + (size_t)N * sizeof(float2) +
-                       (p->zf ? rowsN * sizeof(float2) : 0) +
-                       (p->zscr ? rowsN * sizeof(float2) : 0) + p->scratch_bytes +
-                       (p->tabs ? cat::fast_tables_bytes(p->fs.N2) : 0);
+  p->workspace_bytes = planned_workspace(p);
 
   // Twiddle table exp(-2πi j/N), evaluated in fp64 and rounded once.
   std::vector<float2> tw((size_t)N);
@@ -682,6 +693,29 @@ int create_plan(cat_plan_t* out, int B, int N, int D, int H, int dtype, void* st
   return CAT_OK;
 }
 }  // namespace
+
+int cat_plan_query(int B, int N, int D, int H, int dtype, size_t* workspace_bytes, char* desc,
+                   int len) {
+  int st = validate_shape(B, N, D, H, dtype);
+  if (st != CAT_OK) return st;
+  cat_plan_s q{};
+  q.B = B; q.N = N; q.D = D; q.H = H; q.dtype = dtype;
+  q.dh = D / H;
+  q.npair = (q.dh + 1) / 2;
+  st = choose_path(&q);
+  if (st != CAT_OK) return st;
+  if (q.path == cat::PATH_FAST) {
+    q.use_graph = 1;
+    if (const char* g = std::getenv("CAT_GRAPH")) q.use_graph = std::strcmp(g, "0") != 0;
+  }
+  q.workspace_bytes = planned_workspace(&q);
+  if (workspace_bytes) *workspace_bytes = q.workspace_bytes;
+  if (desc && len > 0) {
+    describe(&q);
+    std::snprintf(desc, (size_t)len, "%s", q.desc);
+  }
+  return CAT_OK;
+}
 
 int cat_plan_destroy(cat_plan_t plan) {
   if (!plan) return CAT_OK;

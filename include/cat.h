@@ -32,6 +32,8 @@
 #ifndef CAT_H_
 #define CAT_H_
 
+#include <stddef.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -81,6 +83,19 @@ enum {
  */
 int cat_plan_create(cat_plan_t *out, int B, int N, int D, int H, int dtype,
                     void *stream);
+
+/*
+ * cat_plan_query — the plan cat_plan_create would build for this shape,
+ * without touching the device or allocating: *workspace_bytes (may be
+ * NULL) receives the device workspace it would allocate, and desc (may be
+ * NULL; capacity len bytes, NUL-terminated, truncated if needed) the same
+ * one-line description cat_plan_describe gives (path, factorisation,
+ * launch shapes).  The backward workspace, allocated at a plan's first
+ * backward call, is not included.  Errors: those of cat_plan_create's
+ * shape validation (CAT_ERR_INVALID_ARG, CAT_ERR_UNSUPPORTED_N).
+ */
+int cat_plan_query(int B, int N, int D, int H, int dtype,
+                   size_t *workspace_bytes, char *desc, int len);
 
 /* Release a plan and its device memory.  NULL is accepted (no-op).
  * Synchronises the plan's stream first.  Destroying twice is undefined. */

@@ -127,3 +127,49 @@ def test_dtype_codes():
     assert cat.dtype_code("bf16") == cat.CAT_BF16
     with pytest.raises(ValueError):
         cat.dtype_code(torch.float16)
+
+
+# --------------------------------------------------------- host path choice
+# cat_plan_query runs the plan constructor's shape validation and path
+# selection on the host without a device, so the choice for every workload
+# shape is checked here.
+
+@pytest.mark.parametrize("shape,expect", [
+    ((1, 256, 64, 2, "f32"), ["path=smem", "reg_m=16", "radices=8x8x4"]),
+    ((64, 196, 384, 6, "f32"), ["path=smem", "reg_m=14", "radices=4x7x7"]),
+    ((16, 1024, 768, 12, "bf16"), ["path=smem", "reg_m=32"]),
+    ((1, 1000, 10, 2, "f32"), ["path=smem", "reg_m=0", "radices=8x5x5x5"]),
+    ((1, 16384, 8, 2, "f32"), ["path=smem", "reg_m=0"]),            # head width 4: not fast
+    ((4, 16384, 1024, 16, "bf16"), ["path=fast", "N2=32", "chunk_bh=8", "launches=26"]),
+    ((1, 131072, 1024, 16, "bf16"), ["path=fast", "N2=256", "chunk_bh=1"]),
+    ((2, 32768, 128, 2, "f32"), ["path=fast", "N2=64"]),
+    ((1, 20000, 4, 2, "f32"), ["path=fourstep", "N1=160(8x4x5)", "N2=125(5x5x5)"]),
+    ((1, 1 << 22, 64, 1, "f32"), ["path=fourstep", "N1=2048", "N2=2048"]),   # 2^22 > 512·256
+])
+def test_query_path_choice(lib, shape, expect):
+    nbytes, desc = cat.cat_plan_query(*shape)
+    for e in expect:
+        assert e in desc, (e, desc)
+    B, N, D, H, dt = shape
+    rows = B * H * N
+    assert nbytes >= rows * 12 + N * 8           # scores, z*, twiddles at least
+    assert ("workspace=%d" % nbytes) in desc
+
+
+def test_query_matches_between_calls_and_env(lib, monkeypatch):
+    a = cat.cat_plan_query(1, 4096, 8, 2, "f32")
+    assert a == cat.cat_plan_query(1, 4096, 8, 2, "f32")
+    monkeypatch.setenv("CAT_FORCE_PATH", "fourstep")
+    assert "path=fourstep" in cat.cat_plan_query(1, 4096, 8, 2, "f32")[1]
+    monkeypatch.delenv("CAT_FORCE_PATH")
+    monkeypatch.setenv("CAT_SMEM_REG", "0")
+    assert "reg_m=0" in cat.cat_plan_query(1, 256, 64, 2, "f32")[1]
+
+
+@pytest.mark.parametrize("shape,code", [
+    ((1, 11, 64, 2, 0), cat.CAT_ERR_UNSUPPORTED_N),
+    ((1, 16, 64, 3, 0), cat.CAT_ERR_INVALID_ARG),
+    ((1, 16, 64, 2, 5), cat.CAT_ERR_INVALID_ARG),
+])
+def test_query_rejects_bad_shapes(lib, shape, code):
+    assert lib.cat_plan_query(*shape, None, None, 0) == code
