@@ -173,3 +173,17 @@ def test_query_matches_between_calls_and_env(lib, monkeypatch):
 ])
 def test_query_rejects_bad_shapes(lib, shape, code):
     assert lib.cat_plan_query(*shape, None, None, 0) == code
+
+
+def test_no_device_fails_loudly(lib):
+    """Without a CUDA device the library has no other way to compute: plan
+    creation (1-D and 2-D) reports CAT_ERR_CUDA instead of falling back."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a CUDA device is present")
+    with pytest.raises(cat.CatError) as e:
+        cat.cat_plan_create(1, 256, 64, 2, "f32")
+    assert e.value.status == cat.CAT_ERR_CUDA
+    with pytest.raises(cat.CatError) as e:
+        cat.cat_plan_create_2d(1, 14, 14, 64, 2, "f32")
+    assert e.value.status == cat.CAT_ERR_CUDA
