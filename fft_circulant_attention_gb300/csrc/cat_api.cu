@@ -434,7 +434,12 @@ int ensure_backward(cat_plan_s* p) {
     p->bw_scr = nullptr; p->bw_dzs = p->bw_dz = p->bw_wpart = nullptr;
     return CAT_ERR_ALLOC;
   }
-  if (cat::setup_backward_kernels(p) != cudaSuccess) return CAT_ERR_CUDA;
+  if (cat::setup_backward_kernels(p) != cudaSuccess) {
+    cudaGetLastError();
+    cudaFree(p->bw_scr); cudaFree(p->bw_dzs); cudaFree(p->bw_dz); cudaFree(p->bw_wpart);
+    p->bw_scr = nullptr; p->bw_dzs = p->bw_dz = p->bw_wpart = nullptr;
+    return CAT_ERR_CUDA;
+  }
   p->bw_ready = 1;
   return CAT_OK;
 }
@@ -885,6 +890,17 @@ int cat_backward_dz(cat_plan_t p, const void* X, const void* WA, const void* V, 
   if (((uintptr_t)X | (uintptr_t)WA | (uintptr_t)V | (uintptr_t)dO | (uintptr_t)dzstar |
        (uintptr_t)dz) & 15)
     return CAT_ERR_MISALIGNED;
+  {
+    const size_t es = dtype == CAT_BF16 ? 2 : 4;
+    const size_t nx = (size_t)B * N * D * es, nw = (size_t)D * H * es;
+    const size_t nz = (size_t)B * H * N * sizeof(float);
+    const void* in[4] = {X, WA, V, dO};
+    const size_t in_n[4] = {nx, nw, nx, nx};
+    for (int i = 0; i < 4; ++i)
+      if (ranges_overlap(dzstar, nz, in[i], in_n[i]) || ranges_overlap(dz, nz, in[i], in_n[i]))
+        return CAT_ERR_ALIAS;
+    if (ranges_overlap(dzstar, nz, dz, nz)) return CAT_ERR_ALIAS;
+  }
   st = ensure_backward(p);
   if (st != CAT_OK) return st;
   st = run_backward_front(p, X, WA, V, dO);
@@ -905,6 +921,9 @@ int cat2d_scores(cat_plan_t p, const void* Q, const void* K, float* a, int B, in
   if (B == 0) return CAT_OK;
   if (!Q || !K || !a) return CAT_ERR_INVALID_ARG;
   if (((uintptr_t)Q | (uintptr_t)K | (uintptr_t)a) & 15) return CAT_ERR_MISALIGNED;
+  const size_t nx = (size_t)B * p->N * D * (dtype == CAT_BF16 ? 2 : 4);
+  const size_t na = (size_t)B * H * p->N * sizeof(float);
+  if (ranges_overlap(a, na, Q, nx) || ranges_overlap(a, na, K, nx)) return CAT_ERR_ALIAS;
   return map_cuda(cat::launch_scores2d(p, Q, K, a));
 }
 

@@ -175,8 +175,8 @@ int cat_backward(cat_plan_t plan, const void *X, const void *W_A, const void *V,
  * cat_backward_dz — only the score-side gradients of cat_backward: writes
  * dz* = dL/dz* and dz = dL/dz (the softmax backward of dz*), each fp32
  * [B, H, N], to the device pointers dzstar and dz (16-byte aligned, not
- * overlapping the inputs or each other).  Inputs and errors as for
- * cat_backward.
+ * overlapping the inputs or each other: CAT_ERR_ALIAS).  Inputs and errors
+ * as for cat_backward.
  */
 int cat_backward_dz(cat_plan_t plan, const void *X, const void *W_A,
                     const void *V, const void *dO, float *dzstar, float *dz,
@@ -214,7 +214,8 @@ int cat2d_forward(cat_plan_t plan, const void *Q, const void *K, const void *V,
 
 /*
  * cat2d_scores — only the scores a (before the softmax), fp32 [B, H, h·w],
- * to the device pointer a (16-byte aligned).
+ * to the device pointer a (16-byte aligned, not overlapping Q or K:
+ * CAT_ERR_ALIAS).
  */
 int cat2d_scores(cat_plan_t plan, const void *Q, const void *K, float *a,
                  int B, int h, int w, int D, int H, int dtype);
