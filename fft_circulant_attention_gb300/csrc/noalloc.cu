@@ -37,7 +37,8 @@ static __device__ __align__(256) unsigned char g_noalloc_ws[kBytes];
 constexpr int kMaxDevices = 64;
 struct DeviceState {
   unsigned char* base = nullptr;  // device address of g_noalloc_ws
-  int tw_n = 0;                   // length the twiddle region currently holds
+  int sms = 0;                    // multiprocessors (launch shapes of the score kernels)
+  int tw_n = 0;                   // length the twiddle region holds; 0 = none or refilling
 };
 DeviceState g_state[kMaxDevices];
 std::mutex g_mutex;
@@ -92,17 +93,26 @@ extern "C" int cat_forward_noalloc(const void* X, const void* WA, const void* V,
     DeviceState& ds = g_state[dev];
     if (!ds.base) {
       // One-time set-up on this device (it is current): the array's device
-      // address.
+      // address and the multiprocessor count the score kernels size their
+      // grids by.
       void* ptr = nullptr;
-      if (cudaGetSymbolAddress(&ptr, g_noalloc_ws) != cudaSuccess || !ptr) {
+      int sms = 0;
+      if (cudaGetSymbolAddress(&ptr, g_noalloc_ws) != cudaSuccess || !ptr ||
+          cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+          sms <= 0) {
         cudaGetLastError();
         return CAT_ERR_CUDA;
       }
       ds.base = (unsigned char*)ptr;
+      ds.sms = sms;
     }
     base = ds.base;
+    p.sms = ds.sms;
     refill = ds.tw_n != N;
-    ds.tw_n = N;
+    // While the region is being refilled it holds no valid length: a call
+    // that fails before the fill is enqueued leaves it marked empty, so the
+    // next call refills it.
+    if (refill) ds.tw_n = 0;
   }
   p.z2 = (float2*)(base + kOffZ2);
   p.zs = (float*)(base + kOffZs);
@@ -116,6 +126,8 @@ extern "C" int cat_forward_noalloc(const void* X, const void* WA, const void* V,
   if (refill) {
     fill_twiddles<<<(N + 255) / 256, 256, 0, p.stream>>>(p.tw, N);
     if (cudaGetLastError() != cudaSuccess) return CAT_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    g_state[dev].tw_n = N;
   }
   // The status word keeps the previous call's value: clear it.
   if (cudaMemsetAsync(p.status, 0, sizeof(unsigned int), p.stream) != cudaSuccess)

@@ -289,8 +289,11 @@ int cat_plan_pass_times(cat_plan_t plan, float *ms, int cap, int *launches);
  * is one fixed array in the library's device image, which every GPU that
  * loads the library holds until the process exits.  Its size bounds the
  * problem: B·H·N <= CAT_NOALLOC_MAX_ROWS and N <= CAT_NOALLOC_MAX_N, else
- * CAT_ERR_TOO_LARGE.  Other shape rules and errors are those of
- * cat_plan_create and cat_forward.
+ * CAT_ERR_TOO_LARGE.  Other shape rules and host-side errors are those of
+ * cat_plan_create and cat_forward.  The kernels' own status word (a failed
+ * internal check, which cat_plan_sync reports for plan calls) has no reader
+ * here: it is cleared at every call and not reported, so only the returned
+ * status (argument and launch errors) tells the caller of a failure.
  *
  * X, W_A, V (read) and O (written): device pointers as for cat_forward.
  * stream: cudaStream_t to enqueue on (NULL = legacy default stream).

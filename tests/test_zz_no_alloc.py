@@ -5,12 +5,18 @@ allocator, or they cannot absorb the synchronisation cudaMalloc implies).
 Its output must match the plan entry point cat_forward, through the C ABI,
 within the parity tolerances (2e-5·max|V| for fp32 storage, 8e-3·max|V| for
 bf16), on two calls in a row — the second call finds the fixed workspace
-holding the first call's data.  This file is collected last on purpose.
+holding the first call's data — and the fp64 oracle within the same bounds.
+The bf16 cases cover all three score kernels the entry point can take: the
+tensor-copy (TMA) kernel (D a multiple of 64), the register-fed MMA kernel
+(D a multiple of 32) and the CUDA-core kernel.  This file is collected last
+on purpose.
 """
+import numpy as np
 import pytest
 import torch
 
 import fft_circulant_attention_gb300 as cat
+import oracle
 import synth
 
 pytestmark = pytest.mark.gpu
@@ -41,21 +47,30 @@ def _plan_forward(X, WA, V, dtype):
 
 @pytest.mark.parametrize("B,N,D,H,dtype", [
     (2, 1024, 64, 4, "f32"),
-    (3, 196, 48, 6, "bf16"),
+    (3, 196, 48, 6, "bf16"),        # CUDA-core score
     (1, 16384, 16, 1, "f32"),
-    (4, 100, 18, 3, "bf16"),
+    (4, 100, 18, 3, "bf16"),        # CUDA-core score, ragged D
+    (2, 256, 64, 1, "bf16"),        # TMA score (D % 64 == 0)
+    (2, 1024, 128, 2, "bf16"),      # TMA score, head width 64
+    (2, 512, 96, 3, "bf16"),        # register-fed MMA score (D % 32 == 0)
+    (1, 1024, 768, 12, "bf16"),     # GPT-2-small width, TMA score
+    (16, 1024, 768, 12, "bf16"),    # the whole GPT-2-small bf16 workload
 ])
 def test_noalloc_matches_plan_entry(B, N, D, H, dtype):
-    X, WA, V = _dev(*synth.make_inputs(B, N, D, H, dtype, seed=N + D))
-    ref = _plan_forward(X, WA, V, dtype)
+    X, WA, V = synth.make_inputs(B, N, D, H, dtype, seed=N + D)
+    Xd, Wd, Vd = _dev(X, WA, V)
+    ref = _plan_forward(Xd, Wd, Vd, dtype)
     bound = TOL[dtype] * float(V.double().abs().max())
+    O_or, _ = oracle.forward(X, WA, V, mode="direct" if B * N * N * D <= 2e9 else "fft")
     stream = torch.cuda.current_stream()
     for _ in range(2):
-        O = torch.full_like(V, float("nan"))
-        cat.cat_forward_noalloc(X, WA, V, O, B, N, D, H, dtype, stream)
+        O = torch.full_like(Vd, float("nan"))
+        cat.cat_forward_noalloc(Xd, Wd, Vd, O, B, N, D, H, dtype, stream)
         torch.cuda.synchronize()
         err = float((O.double() - ref.double()).abs().max())
         assert err <= bound, (err, bound)
+        err_or = float(np.abs(O.double().cpu().numpy() - O_or).max())
+        assert err_or <= bound, (err_or, bound)
 
 
 def test_noalloc_alternating_lengths():
@@ -69,6 +84,24 @@ def test_noalloc_alternating_lengths():
         cat.cat_forward_noalloc(X, WA, V, O, B, N, D, H, dtype, stream)
         torch.cuda.synchronize()
         assert float((O - ref).abs().max()) <= TOL[dtype] * float(V.abs().max())
+
+
+def test_noalloc_rejected_call_does_not_poison_the_next():
+    """A call refused by the host checks leaves the shared workspace (its
+    twiddle length in particular) as it was: the next call is correct."""
+    stream = torch.cuda.current_stream()
+    B, N, D, H, dtype = 2, 1000, 32, 2, "f32"
+    X, WA, V = _dev(*synth.make_inputs(B, N, D, H, dtype, seed=7))
+    ref = _plan_forward(X, WA, V, dtype)
+    X5, V5 = X[:, :500].contiguous(), V[:, :500].contiguous()
+    bad = torch.empty(V5.numel() + 4, device="cuda:0")[1:1 + V5.numel()].view_as(V5)
+    with pytest.raises(cat.CatError) as e:      # misaligned output, other length
+        cat.cat_forward_noalloc(X5, WA, V5, bad, B, 500, D, H, dtype, stream)
+    assert e.value.status == cat.CAT_ERR_MISALIGNED
+    O = torch.empty_like(V)
+    cat.cat_forward_noalloc(X, WA, V, O, B, N, D, H, dtype, stream)
+    torch.cuda.synchronize()
+    assert float((O - ref).abs().max()) <= TOL[dtype] * float(V.abs().max())
 
 
 def test_noalloc_rejects_sizes_beyond_its_workspace():
