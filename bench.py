@@ -43,27 +43,43 @@ UNIT = "tokens·heads/s"
 PRIMARY = "long16k"
 SECONDARY = "long128k"
 
-# GB300: 152 SMs x 128 FP32 lanes x 2 flops (FMA) x 2070 MHz maximum SM clock.
-SMS, FP32_LANES, MAX_SM_MHZ = 152, 128, 2070.0
-FP32_PEAK_TFLOPS = SMS * FP32_LANES * 2 * MAX_SM_MHZ * 1e6 / 1e12
+# FP32 peak = SMs x 128 FP32 lanes x 2 flops (FMA) x maximum SM clock.  The
+# SM count is read from the device and the clock from the measured-peaks
+# file (else the GB300's 2070 MHz) when the GPU arm starts; 152 SMs until then.
+FP32_LANES, DEFAULT_MAX_SM_MHZ = 128, 2070.0
+FP32_PEAK_TFLOPS = 152 * FP32_LANES * 2 * DEFAULT_MAX_SM_MHZ * 1e6 / 1e12
+FP32_PEAK_SOURCE = "FP32: 152 SMs x 128 lanes x 2 x 2070 MHz"
 FALLBACK_HBM_GBS = 6800.0
 
 # DRAM bytes (read + write) per launch of the dominant kernel (pass B of the
-# fast path), from the committed ncu launch list of the same kernel sources
-# (profiles/).  Keyed by (workload, hash of the kernel sources): any change
-# to those sources makes the figure stale, and the bench then reports null.
+# fast path), from an ncu capture of the same kernel sources, committed with
+# its command under profiles/.  Keyed by (workload, hash of the kernel
+# sources): any change to those sources makes the figure stale, and the
+# bench then reports null.  ncu flushes L2 before each captured launch, so
+# the figure is cold-cache traffic (the scratch refilled from DRAM), an upper
+# bound on the traffic of a launch inside the overlapped schedule.
 NCU_TRAFFIC = {
-    # profiles/backward_long16k.md: fsf_pass_b, 32 launches (the backward's
-    # dV product runs the forward's pass B on the same chunks of 8 rows),
-    # median DRAM read + write per launch (cold: ncu flushes L2 before each
-    # launch).  The earlier forward-only list (profiles/launches_long16k.md)
-    # gave 34774016 for the same kernel.
     ("long16k", "45cff3383846"): 34773248,
 }
 KERNEL_SOURCES = ["fourstep_fast.cu", "fft_reg.cuh", "fft_device.cuh", "bulk.cuh", "elem.cuh"]
 # Pass B's transforms: per (pair, k2) signal one forward and one inverse DFT
 # of length N1 = 512, counted as 5·N1·log2(N1) flops each.
 PASS_B_N1 = 512
+
+
+def set_fp32_peak(device):
+    """FP32 peak of `device` from its SM count and the maximum SM clock."""
+    global FP32_PEAK_TFLOPS, FP32_PEAK_SOURCE
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    mhz, src = DEFAULT_MAX_SM_MHZ, "GB300 maximum"
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            mhz, src = float(json.load(f)["sm_max_mhz"]), "measured-peaks file"
+    except Exception:
+        pass
+    FP32_PEAK_TFLOPS = sms * FP32_LANES * 2 * mhz * 1e6 / 1e12
+    FP32_PEAK_SOURCE = ("FP32: %d SMs (device) x %d lanes x 2 x %.0f MHz (%s); derived "
+                        "from unit counts and the maximum SM clock" % (sms, FP32_LANES, mhz, src))
 
 
 def kernel_hash():
@@ -241,6 +257,81 @@ def sample_heads(c):
     return c["H"]
 
 
+def host_cores():
+    """Cores of the host and the CPU affinity of this process."""
+    try:
+        aff = sorted(os.sched_getaffinity(0))
+    except Exception:
+        aff = list(range(os.cpu_count() or 1))
+    # Compress the mask into ranges: [0, 1, 2, 5] -> "0-2,5".
+    parts, i = [], 0
+    while i < len(aff):
+        j = i
+        while j + 1 < len(aff) and aff[j + 1] == aff[j] + 1:
+            j += 1
+        parts.append(str(aff[i]) if i == j else "%d-%d" % (aff[i], aff[j]))
+        i = j + 1
+    return {"nproc": os.cpu_count(), "affinity": ",".join(parts), "affinity_cores": len(aff)}
+
+
+def time_slice_131072(heads=(0, 15)):
+    """The 131072-token workload's O(N^2) definition on its 4096-row slice
+    (rows 32·r) for the value columns of `heads`, all host cores: the
+    oracle's direct-product check of that workload, timed on its own."""
+    import oracle
+    c = cfg_of("long128k")
+    X, WA, V = synth.make_inputs(c["B"], c["N"], c["D"], c["H"], c["dtype"], seed=0)
+    dh = c["D"] // c["H"]
+    cols = np.concatenate([np.arange(h * dh, (h + 1) * dh) for h in heads])
+    t0 = time.perf_counter()
+    zs = oracle.zstar(X, WA)
+    t1 = time.perf_counter()
+    Vs = np.ascontiguousarray(V.double().numpy()[:, :, cols])
+    zss = np.ascontiguousarray(zs[:, list(heads)])
+    rows = list(range(0, c["N"], 32))
+    t2 = time.perf_counter()
+    oracle.circ_direct_rows(zss, Vs, rows)
+    t3 = time.perf_counter()
+    outputs = len(rows) * cols.size
+    return {"workload": "long128k", "rows": len(rows), "columns": int(cols.size),
+            "heads": list(heads), "zstar_s": t1 - t0, "direct_s": t3 - t2,
+            "multiply_adds": float(outputs) * c["N"],
+            "outputs_per_s": outputs / (t3 - t2), "threads": oracle.num_threads()}
+
+
+def cpu_baseline_leg(c, heads):
+    """The fp64 oracle on the host cores: FFT mode on batch 0 of the workload
+    with all cores (the reported value) and with one thread, and the
+    131072-token row slice of the direct product."""
+    import oracle
+    cores_all = oracle.num_threads()
+    units, times, cores = time_oracle(c, heads)
+    oracle.set_num_threads(1)
+    try:
+        units1, times1, _ = time_oracle(c, heads)
+    finally:
+        oracle.set_num_threads(cores_all)
+    sl = time_slice_131072()
+    return {"value": units / times[0], "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": "batch 0, head%s 0..%d of %s: z* from the full rows and the fp64 "
+                      "FFT-mode circulant product of those heads' columns"
+                      % ("s" if heads > 1 else "", heads - 1, c["name"]),
+            "seconds": times[0],
+            "single_thread": {"value": units1 / times1[0], "unit": UNIT, "cores": 1,
+                              "seconds": times1[0]},
+            "host": host_cores(),
+            "slice_131072_direct": sl}
+
+
+def workload_config(c, name, world):
+    """The `config` object of the JSON line; the same in both arms."""
+    return {"workload": name, "B": c["B"], "N": c["N"], "D": c["D"], "H": c["H"],
+            "storage": c["dtype"],
+            "l2": "inputs larger than L2 (X+V+O %.0f MB), no flush"
+                  % (3 * c["B"] * c["N"] * c["D"] * c["es"] / 1e6),
+            "parallelism": "replicas" if world > 1 else "single GPU"}
+
+
 def run_reference(args, world, rank):
     if rank != 0:
         return
@@ -264,10 +355,10 @@ def run_reference(args, world, rank):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * tot / len(times), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": args.config, "B": c["B"], "N": c["N"], "D": c["D"], "H": c["H"],
-                   "storage": c["dtype"]},
+        "config": workload_config(c, args.config, world),
+        "timed_sample": sample,
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": sample},
+                         "sample": sample, "host": host_cores()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
@@ -356,8 +447,11 @@ def measure_workload(name, steps, warmup, device, world, sampler=None):
         "unit": "TFLOP/s",
         "frac": b_tflops / FP32_PEAK_TFLOPS,
         "traffic": NCU_TRAFFIC.get((name, kernel_hash())),
-        "peak_source": "FP32: 152 SMs x 128 lanes x 2 x 2070 MHz (derived from unit counts "
-                       "and the maximum SM clock)",
+        "peak_source": FP32_PEAK_SOURCE,
+        "traffic_note": "ncu DRAM read+write per launch, cold cache (L2 flushed before the "
+                        "captured launch): the scratch refilled from DRAM, an upper bound "
+                        "on a launch inside the overlapped schedule; null when the kernel "
+                        "sources changed since the capture",
         "flops_per_launch": b_flops,
         "ms_per_launch": b_ms,
         "launches_timed": pass_launches,
@@ -491,6 +585,35 @@ def measure_short(name, device, reps=200, warmup=20):
             "path_roofline_frac": t_roof / (ms * 1e-3), "plan": desc}
 
 
+def profile_range(args, device):
+    """Steady-state forwards of --config bracketed by cudaProfilerStart/Stop
+    (after --warmup untimed ones), for a range capture of the whole forward:
+        ncu --profile-from-start off --replay-mode app-range --clock-control none \
+            --metrics dram__bytes_read.sum,dram__bytes_write.sum \
+            python bench.py --config long16k --profile-range 4
+    DRAM bytes per forward = the range's totals / --profile-range."""
+    import fft_circulant_attention_gb300 as cat
+    c = cfg_of(args.config)
+    X, WA, V = (t.to(device) for t in synth.make_inputs(c["B"], c["N"], c["D"], c["H"],
+                                                         c["dtype"], seed=0))
+    O = torch.empty_like(V)
+    stream = torch.cuda.current_stream(device)
+    with cat.Plan(c["B"], c["N"], c["D"], c["H"], c["dtype"], stream=stream) as plan:
+        for _ in range(args.warmup):
+            plan.forward(X, WA, V, O)
+        plan.sync()
+        torch.cuda.synchronize(device)
+        torch.cuda.profiler.start()
+        for _ in range(args.profile_range):
+            plan.forward(X, WA, V, O)
+        torch.cuda.synchronize(device)
+        torch.cuda.profiler.stop()
+        plan.sync()
+        desc = plan.describe()
+    print(json.dumps({"profile_range": args.profile_range, "workload": args.config,
+                      "plan": desc}), flush=True)
+
+
 def run_gb300(args, world, rank, local):
     import fft_circulant_attention_gb300 as cat
     from fft_circulant_attention_gb300 import build
@@ -498,6 +621,10 @@ def run_gb300(args, world, rank, local):
     cat.lib()
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
+    set_fp32_peak(device)
+    if args.profile_range:
+        profile_range(args, device)
+        return
     if args.backward_only:
         bw = measure_backward(args.config, device, max(args.steps, 1), args.warmup)
         if rank == 0:
@@ -533,13 +660,7 @@ def run_gb300(args, world, rank, local):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         c = cfg_of(args.config)
         c["name"] = args.config
-        heads = args.sample_heads or sample_heads(c)
-        units, times, cores = time_oracle(c, heads)
-        cpu = {"value": units / times[0], "unit": UNIT, "cores": cores, "kind": "oracle",
-               "sample": "batch 0, head%s 0..%d of %s: z* from the full rows and the fp64 "
-                         "FFT-mode circulant product of those heads' columns"
-                         % ("s" if heads > 1 else "", heads - 1, args.config),
-               "seconds": times[0]}
+        cpu = cpu_baseline_leg(c, args.sample_heads or sample_heads(c))
     if rank != 0:
         return
     c = prim["c"]
@@ -548,11 +669,8 @@ def run_gb300(args, world, rank, local):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": prim["ms_per_step"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": args.config, "B": c["B"], "N": c["N"], "D": c["D"], "H": c["H"],
-                   "storage": c["dtype"], "l2": "inputs larger than L2 (X+V+O %.0f MB)"
-                   % (3 * c["B"] * c["N"] * c["D"] * c["es"] / 1e6),
-                   "parallelism": "replicas" if world > 1 else "single GPU",
-                   "plan": prim["desc"]},
+        "config": workload_config(c, args.config, world),
+        "plan": prim["desc"],
         "roofline": prim["roofline"],
         "path_roofline_frac": prim["path_roofline_frac"],
         "stage_ms_serialised": {"score": prim["stage_ms"][0],
@@ -597,6 +715,9 @@ def main():
     ap.add_argument("--backward-only", action="store_true",
                     help="time only cat_backward on --config (--steps calls) and print it")
     ap.add_argument("--sample-heads", type=int, default=0)
+    ap.add_argument("--profile-range", type=int, default=0,
+                    help="run this many forwards of --config between cudaProfilerStart and "
+                         "cudaProfilerStop (for an ncu range capture) and exit")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world, rank, local = dist_init(args)

@@ -81,6 +81,8 @@ def _lib():
         lib.oracle_circ2d_direct.restype = None
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = ctypes.c_int
+        lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
+        lib.oracle_set_num_threads.restype = None
         _LIB = lib
     return _LIB
 
@@ -99,6 +101,11 @@ def _p(a):
 def num_threads() -> int:
     """OpenMP threads the oracle uses."""
     return int(_lib().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Set the OpenMP threads later oracle calls use."""
+    _lib().oracle_set_num_threads(int(n))
 
 
 def scores(X, WA):

@@ -107,24 +107,38 @@ void oracle_circ_direct(const double *zs, const double *V, long B, long N,
 }
 
 /* The same definition evaluated only at the output rows listed in `rows`
- * (nrows of them) for every batch and column: Orows[b, r, c]. */
+ * (nrows of them, each in [0, N)) for every batch and column:
+ * Orows[b, r, c] = sum_j z*[b, h(c), (rows[r] - j) mod N] * V[b, j, c].
+ * Every output is the same sum as in oracle_circ_direct, started at 0 and
+ * taken over j in ascending order, so the two agree bit for bit.  Only the
+ * order in which different outputs advance differs: the loop over j runs
+ * outside the loops over a block of listed rows and the columns, so each
+ * row V[b, j, :] is read once per block instead of once per output. */
 void oracle_circ_direct_rows(const double *zs, const double *V, long B, long N,
                              long D, long H, const long *rows, long nrows,
                              double *Orows) {
-  long b, r;
+  const long RB = 32; /* listed rows per block */
+  const long dh = D / H;
+  const long nblk = (nrows + RB - 1) / RB;
+  long b, blk;
 #pragma omp parallel for collapse(2) schedule(dynamic, 1)
   for (b = 0; b < B; ++b) {
-    for (r = 0; r < nrows; ++r) {
-      long i = rows[r];
-      for (long c = 0; c < D; ++c) {
-        const double *w = zs + (b * H + head_of(c, D, H)) * N;
-        double acc = 0.0;
-        for (long j = 0; j < N; ++j) {
-          long s = i - j;
+    for (blk = 0; blk < nblk; ++blk) {
+      const long r0 = blk * RB;
+      const long r1 = r0 + RB < nrows ? r0 + RB : nrows;
+      double *acc = Orows + (b * nrows + r0) * D;
+      for (long q = 0; q < (r1 - r0) * D; ++q) acc[q] = 0.0;
+      for (long j = 0; j < N; ++j) {
+        const double *v = V + (b * N + j) * D;
+        for (long r = r0; r < r1; ++r) {
+          long s = rows[r] - j;
           if (s < 0) s += N;
-          acc += w[s] * V[(b * N + j) * D + c];
+          double *o = acc + (r - r0) * D;
+          for (long h = 0; h < H; ++h) {
+            const double w = zs[(b * H + h) * N + s];
+            for (long c = h * dh; c < (h + 1) * dh; ++c) o[c] += w * v[c];
+          }
         }
-        Orows[(b * nrows + r) * D + c] = acc;
       }
     }
   }
@@ -595,5 +609,16 @@ int oracle_num_threads(void) {
   return omp_get_max_threads();
 #else
   return 1;
+#endif
+}
+
+/* Set the number of OpenMP threads later calls use (no effect without
+ * OpenMP); n < 1 is taken as 1. */
+void oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+  extern void omp_set_num_threads(int);
+  omp_set_num_threads(n < 1 ? 1 : n);
+#else
+  (void)n;
 #endif
 }
