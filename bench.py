@@ -593,19 +593,29 @@ def profile_range(args, device):
             python bench.py --config long16k --profile-range 4
     DRAM bytes per forward = the range's totals / --profile-range."""
     import fft_circulant_attention_gb300 as cat
-    c = cfg_of(args.config)
-    X, WA, V = (t.to(device) for t in synth.make_inputs(c["B"], c["N"], c["D"], c["H"],
-                                                         c["dtype"], seed=0))
-    O = torch.empty_like(V)
     stream = torch.cuda.current_stream(device)
-    with cat.Plan(c["B"], c["N"], c["D"], c["H"], c["dtype"], stream=stream) as plan:
+    if args.config in synth.GRID_CONFIGS:
+        # A 2-D (token-grid) workload: cat2d_forward on Q, K, V.
+        c = dict(synth.GRID_CONFIGS[args.config])
+        B, h, w = c["B"], c["h"], c["w"]
+        A, K, V = (t.to(device) for t in synth.make_qkv(B, h * w, c["D"], c["dtype"], seed=0))
+        plan = cat.Plan2D(B, h, w, c["D"], c["H"], c["dtype"], stream=stream)
+        run = lambda: plan.forward(A, K, V, O)   # noqa: E731
+    else:
+        c = cfg_of(args.config)
+        A, K, V = (t.to(device) for t in synth.make_inputs(c["B"], c["N"], c["D"], c["H"],
+                                                            c["dtype"], seed=0))
+        plan = cat.Plan(c["B"], c["N"], c["D"], c["H"], c["dtype"], stream=stream)
+        run = lambda: plan.forward(A, K, V, O)   # noqa: E731
+    O = torch.empty_like(V)
+    with plan:
         for _ in range(args.warmup):
-            plan.forward(X, WA, V, O)
+            run()
         plan.sync()
         torch.cuda.synchronize(device)
         torch.cuda.profiler.start()
         for _ in range(args.profile_range):
-            plan.forward(X, WA, V, O)
+            run()
         torch.cuda.synchronize(device)
         torch.cuda.profiler.stop()
         plan.sync()
@@ -706,7 +716,9 @@ def main():
     ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
-    ap.add_argument("--config", default=PRIMARY, choices=sorted(synth.CONFIGS))
+    ap.add_argument("--config", default=PRIMARY,
+                    choices=sorted(synth.CONFIGS) + sorted(synth.GRID_CONFIGS),
+                    help="workload (the 2-D grid ones only with --profile-range)")
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-short", action="store_true")
@@ -720,6 +732,9 @@ def main():
                          "cudaProfilerStop (for an ncu range capture) and exit")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.config in synth.GRID_CONFIGS and not args.profile_range:
+        ap.error("the 2-D grid workloads are timed in the grid2d entries; "
+                 "--config takes them only with --profile-range")
     world, rank, local = dist_init(args)
     if args.impl == "reference":
         run_reference(args, world, rank)

@@ -22,6 +22,7 @@ constexpr size_t kConvSmemBudget = 64 << 10;  // preferred per-CTA tile (bytes)
 constexpr size_t kFsSmemBudget = 100 << 10;
 constexpr size_t kScratchBudget = 80ull << 20;  // live four-step scratch (L2-sized)
 constexpr size_t kFastScratchBudget = 64ull << 20;
+constexpr int kDirectMaxN = 1024;              // longest direct (O(N²)) product
 
 bool seven_smooth(long n) {
   if (n < 1) return false;
@@ -149,10 +150,17 @@ void free_plan(cat_plan_s* p) {
   cudaFree(p->bw_dzs);
   cudaFree(p->bw_dz);
   cudaFree(p->bw_wpart);
-  cudaFree(p->hx);
+  for (int k = 0; k < 2; ++k) {
+    cudaFree(p->hx[k]);
+    cudaFree(p->hv[k]);
+    cudaFree(p->ho[k]);
+    if (p->hsub[k]) free_plan(p->hsub[k]);
+    if (p->hcp[k]) cudaStreamDestroy(p->hcp[k]);
+    if (p->hev_in[k]) cudaEventDestroy(p->hev_in[k]);
+    if (p->hev_done[k]) cudaEventDestroy(p->hev_done[k]);
+    if (p->hev_out[k]) cudaEventDestroy(p->hev_out[k]);
+  }
   cudaFree(p->hwa);
-  cudaFree(p->hv);
-  cudaFree(p->ho);
   delete p;
 }
 
@@ -163,11 +171,90 @@ int score_launches(int H, int D) {
 
 int configure_fourstep(cat_plan_s* p, int N1, int N2);
 
+// Whether the direct product can serve a shape: head width a multiple of 4
+// (four columns a thread), at most 128, N <= kDirectMaxN, and a CTA of whole
+// warps within 512 threads (dh/4 column threads times a row-group count
+// that makes a multiple of 32).
+bool direct_supported(const cat_plan_s* p) {
+  if (p->dh % 4 != 0 || p->dh > 128 || p->N > kDirectMaxN) return false;
+  const int ncg = p->dh / 4;
+  int a = ncg, b = 32;
+  while (b) { const int t = a % b; a = b; b = t; }
+  return ncg * (32 / a) <= 512;
+}
+
+// Whether the direct product is the faster path for a supported shape.
+// Measured on GB300 (forward, resident inputs): the register FFT kernels of
+// the square lengths 8², 14², 16², 32² beat it (N = 196: 39 µs against
+// 96 µs for B=64, D=384, H=6; N = 1024: 86 against 570 µs for GPT-2 small),
+// while for other lengths up to 512 the block-FFT path is the slower one
+// (N = 128: 92 against 35 µs for B=32, D=768, H=12 bf16; N = 512: 108
+// against 90 µs for B=8).
+constexpr int kDirectPreferMaxN = 512;
+bool direct_preferred(const cat_plan_s* p) {
+  const int N = p->N;
+  for (int m : {8, 14, 16, 32})
+    if (m * m == N) return false;
+  return N <= kDirectPreferMaxN;
+}
+
+// Launch shape of the direct path (host only, no allocation).  TR, the rows
+// a thread owns, is the largest of 8, 4, 2 that still gives a full wave of
+// 256-thread CTAs.  A CTA covers as many rows as 512 threads allow (the
+// whole row when it fits, so that the per-CTA softmax of the row is paid
+// once); the row tile shrinks (down to 64-thread CTAs) until there are two
+// CTAs per SM.  The scores are fused into the kernel when the row's X block
+// is small enough that every CTA of the row may read it.
+int configure_direct(cat_plan_s* p) {
+  if (!direct_supported(p)) return CAT_ERR_UNSUPPORTED_N;
+  p->path = cat::PATH_DIRECT;
+  cat::DirectCfg& c = p->dir;
+  const int N = p->N, ncg = p->dh / 4;
+  const long bh = (long)p->B * p->H;
+  const long sms = 152;
+  c.TR = 2;
+  for (int tr : {8, 4})
+    if (bh * ((N + tr - 1) / tr) * ncg >= sms * 256) {
+      c.TR = tr;
+      break;
+    }
+  const int groups = (N + c.TR - 1) / c.TR;
+  // Row groups per CTA: a multiple of `unit`, so that the CTA is a whole
+  // number of warps (its block reductions shuffle over full warps).
+  int g32 = ncg;
+  for (int b2 = 32; b2;) { const int t = g32 % b2; g32 = b2; b2 = t; }
+  const int unit = 32 / g32;
+  auto ru = [&](int x) { return (x + unit - 1) / unit * unit; };
+  const int nrg_cap = (512 / ncg) / unit * unit;
+  int nrg = ru(groups) < nrg_cap ? ru(groups) : nrg_cap;
+  const int nrg_min = ru((64 + ncg - 1) / ncg);
+  auto ctas = [&](int g) { return bh * ((N + c.TR * g - 1) / (c.TR * g)); };
+  for (;;) {
+    const int nx = ru(nrg / 2);
+    if (nx >= nrg || nx < nrg_min || ctas(nrg) >= 2 * sms) break;
+    nrg = nx;
+  }
+  c.nrg = nrg;
+  c.R = c.TR * nrg;
+  c.threads = ncg * nrg;
+  const size_t es = p->dtype == CAT_BF16 ? 2 : 4;
+  const double fused_bytes = (double)ctas(nrg) * N * p->D * es;
+  c.fused = (long)N * p->D <= (1L << 17) && fused_bytes <= 64e6;
+  if (const char* f = std::getenv("CAT_DIRECT_FUSED")) c.fused = std::strcmp(f, "0") != 0;
+  c.smem = cat::direct_smem(N, p->D, p->dh, c.R, c.fused != 0);
+  p->launches = c.fused ? 1 : score_launches(p->H, p->D) + 1;
+  return CAT_OK;
+}
+
 int choose_path(cat_plan_s* p) {
   const int N = p->N;
   // CAT_FORCE_PATH=fourstep sends short sequences down the multi-pass path
-  // too (debugging and testing of that path at small sizes).
+  // too (debugging and testing of that path at small sizes); =direct takes
+  // the direct product wherever it is supported; =smem never takes it.
   const char* force = std::getenv("CAT_FORCE_PATH");
+  if (direct_supported(p) &&
+      (force ? std::strcmp(force, "direct") == 0 : direct_preferred(p)))
+    return configure_direct(p);
   int n1 = 0, n2 = 0;
   const bool force_fs = force && std::strcmp(force, "fourstep") == 0 && split_fourstep(N, &n1, &n2);
   const bool allow_fast = !(force && (std::strcmp(force, "fourstep") == 0 ||
@@ -187,12 +274,12 @@ int choose_path(cat_plan_s* p) {
       f.groups = 1;
       f.P = 32;
       // Chunks of (b, h) rows stay inside one batch; two scratch slots let
-      // two chunks be in flight on the plan's two internal streams.
-      // Chunks of heads alternate between the plan's two streams: half the
-      // scratch budget per slot with two or more batches (8 heads at
-      // N = 16384), single heads with one batch.
+      // two chunks be in flight on the plan's two internal streams.  A slot
+      // takes half the scratch budget: 8 heads at N = 16384 (one batch of
+      // 16 heads runs in 68 µs with chunks of 8, 127 µs with single heads),
+      // one head at N = 131072.
       const size_t per_bh = (size_t)N * 32 * sizeof(float2);
-      long chunk = p->B >= 2 ? (long)(kFastScratchBudget / 2 / per_bh) : 1;
+      long chunk = (long)(kFastScratchBudget / 2 / per_bh);
       if (const char* env = std::getenv("CAT_CHUNK_BH")) chunk = std::atol(env);
       if (chunk < 1) chunk = 1;
       if (chunk > p->H) chunk = p->H;
@@ -264,7 +351,13 @@ void describe(cat_plan_s* p) {
     for (int i = 0; i < rp.npass && o + 4 < len; ++i)
       o += (size_t)std::snprintf(out + o, len - o, i ? "x%d" : "%d", rp.radix[i]);
   };
-  if (p->path == cat::PATH_SMEM) {
+  if (p->path == cat::PATH_DIRECT) {
+    std::snprintf(p->desc, sizeof(p->desc),
+                  "path=direct N=%d TR=%d R=%d threads=%d fused=%d smem=%zu workspace=%zu "
+                  "launches=%d",
+                  p->N, p->dir.TR, p->dir.R, p->dir.threads, p->dir.fused, p->dir.smem,
+                  p->workspace_bytes, p->launches);
+  } else if (p->path == cat::PATH_SMEM) {
     radstr(p->rpN, rad, sizeof(rad));
     std::snprintf(p->desc, sizeof(p->desc),
                   "path=smem N=%d radices=%s reg_m=%d G=%d groups=%d threads=%d smem=%zu "
@@ -674,6 +767,7 @@ int create_plan(cat_plan_t* out, int B, int N, int D, int H, int dtype, void* st
   if (e == cudaSuccess)
     e = p->path == cat::PATH_SMEM       ? cat::setup_smem_kernels(p)
         : p->path == cat::PATH_FOURSTEP ? cat::setup_fourstep_kernels(p)
+        : p->path == cat::PATH_DIRECT   ? cat::setup_direct_kernels(p)
                                         : cat::setup_fast_kernels(p);
   if (e == cudaSuccess && p->path == cat::PATH_FAST) {
     for (int k = 0; k < 2 && e == cudaSuccess; ++k) {
@@ -768,6 +862,15 @@ int cat_forward(cat_plan_t p, const void* X, const void* WA, const void* V, void
     return map_cuda(run_fast_overlapped(p, X, WA, V, O));
   }
   if (ev) cudaEventRecord(ev[0], p->stream);
+  if (p->path == cat::PATH_DIRECT) {
+    // Scores (in the kernel when fused), softmax and the direct product.
+    cudaError_t e = p->dir.fused ? cudaSuccess : cat::launch_score(p, X, WA);
+    if (ev) cudaEventRecord(ev[1], p->stream);
+    if (ev) cudaEventRecord(ev[2], p->stream);
+    if (e == cudaSuccess) e = cat::launch_direct(p, X, WA, V, O, p->dir.fused != 0);
+    if (ev) cudaEventRecord(ev[3], p->stream);
+    return map_cuda(e);
+  }
   cudaError_t e = cat::launch_score(p, X, WA);
   if (e != cudaSuccess) return CAT_ERR_CUDA;
   if (ev) cudaEventRecord(ev[1], p->stream);
@@ -802,6 +905,65 @@ int cat_forward_zstar(cat_plan_t p, const void* X, const void* WA, float* zstar,
                                   cudaMemcpyDeviceToDevice, p->stream));
 }
 
+namespace {
+
+// Set-up of the host-buffer path at its first call (see cat_plan_s).
+int ensure_host(cat_plan_s* p) {
+  if (p->hready) return CAT_OK;
+  const size_t es = p->dtype == CAT_BF16 ? 2 : 4;
+  // CAT_HOST_PIPELINE=0: the serial copy, compute, copy (for comparison).
+  const char* pipe = std::getenv("CAT_HOST_PIPELINE");
+  const bool steps = p->B >= 2 && !(pipe && std::strcmp(pipe, "0") == 0);
+  const size_t nx = (size_t)(steps ? 1 : p->B) * p->N * p->D * es;
+  const size_t nw = (size_t)p->D * p->H * es;
+  bool ok = cudaMalloc(&p->hwa, nw) == cudaSuccess;
+  for (int k = 0; k < (steps ? 2 : 1) && ok; ++k)
+    ok = cudaMalloc(&p->hx[k], nx) == cudaSuccess && cudaMalloc(&p->hv[k], nx) == cudaSuccess &&
+         cudaMalloc(&p->ho[k], nx) == cudaSuccess;
+  int st = ok ? CAT_OK : CAT_ERR_ALLOC;
+  if (st == CAT_OK && steps) {
+    for (int k = 0; k < 2 && st == CAT_OK; ++k) {
+      st = create_plan(&p->hsub[k], 1, p->N, p->D, p->H, p->dtype, p->stream, 0, 0);
+      if (st == CAT_OK &&
+          (cudaStreamCreateWithFlags(&p->hcp[k], cudaStreamNonBlocking) != cudaSuccess ||
+           cudaEventCreateWithFlags(&p->hev_in[k], cudaEventDisableTiming) != cudaSuccess ||
+           cudaEventCreateWithFlags(&p->hev_done[k], cudaEventDisableTiming) != cudaSuccess ||
+           cudaEventCreateWithFlags(&p->hev_out[k], cudaEventDisableTiming) != cudaSuccess))
+        st = CAT_ERR_CUDA;
+    }
+  }
+  if (st != CAT_OK) {
+    cudaGetLastError();
+    for (int k = 0; k < 2; ++k) {
+      cudaFree(p->hx[k]); cudaFree(p->hv[k]); cudaFree(p->ho[k]);
+      p->hx[k] = p->hv[k] = p->ho[k] = nullptr;
+      if (p->hsub[k]) free_plan(p->hsub[k]);
+      p->hsub[k] = nullptr;
+      if (p->hcp[k]) cudaStreamDestroy(p->hcp[k]);
+      if (p->hev_in[k]) cudaEventDestroy(p->hev_in[k]);
+      if (p->hev_done[k]) cudaEventDestroy(p->hev_done[k]);
+      if (p->hev_out[k]) cudaEventDestroy(p->hev_out[k]);
+      p->hcp[k] = nullptr;
+      p->hev_in[k] = p->hev_done[k] = p->hev_out[k] = nullptr;
+    }
+    cudaFree(p->hwa);
+    p->hwa = nullptr;
+    return st;
+  }
+  p->hready = 1;
+  return CAT_OK;
+}
+
+}  // namespace
+
+// With two or more batches the call runs one batch per step: the inputs of
+// step b go in on the first copy stream while step b - 1 computes on the
+// plan's stream and step b - 2's output comes back on the second, so the
+// host-to-device and device-to-host copies overlap each other and the
+// compute.  Step b uses staging slot b mod 2 and that slot's one-batch
+// sub-plan; events make a slot's input copy wait for the compute two steps
+// back, and its compute wait for its inputs and for the output copy two
+// steps back.
 int cat_forward_host(cat_plan_t p, const void* X, const void* WA, const void* V, void* O, int B,
                      int N, int D, int H, int dtype) {
   if (!p) return CAT_ERR_INVALID_ARG;
@@ -812,24 +974,48 @@ int cat_forward_host(cat_plan_t p, const void* X, const void* WA, const void* V,
   if (!X || !WA || !V || !O) return CAT_ERR_INVALID_ARG;
   const size_t es = dtype == CAT_BF16 ? 2 : 4;
   const size_t nx = (size_t)B * N * D * es, nw = (size_t)D * H * es;
-  if (!p->hx) {
-    bool ok = cudaMalloc(&p->hx, nx) == cudaSuccess && cudaMalloc(&p->hwa, nw) == cudaSuccess &&
-              cudaMalloc(&p->hv, nx) == cudaSuccess && cudaMalloc(&p->ho, nx) == cudaSuccess;
-    if (!ok) {
-      cudaGetLastError();
-      cudaFree(p->hx); cudaFree(p->hwa); cudaFree(p->hv); cudaFree(p->ho);
-      p->hx = p->hwa = p->hv = p->ho = nullptr;
-      return CAT_ERR_ALLOC;
-    }
-  }
-  cudaError_t e = cudaMemcpyAsync(p->hx, X, nx, cudaMemcpyHostToDevice, p->stream);
-  if (e == cudaSuccess) e = cudaMemcpyAsync(p->hwa, WA, nw, cudaMemcpyHostToDevice, p->stream);
-  if (e == cudaSuccess) e = cudaMemcpyAsync(p->hv, V, nx, cudaMemcpyHostToDevice, p->stream);
-  if (e != cudaSuccess) return CAT_ERR_CUDA;
-  st = cat_forward(p, p->hx, p->hwa, p->hv, p->ho, B, N, D, H, dtype);
+  st = ensure_host(p);
   if (st != CAT_OK) return st;
-  e = cudaMemcpyAsync(O, p->ho, nx, cudaMemcpyDeviceToHost, p->stream);
-  if (e == cudaSuccess) e = cudaStreamSynchronize(p->stream);
+  if (!p->hsub[0]) {
+    cudaError_t e = cudaMemcpyAsync(p->hx[0], X, nx, cudaMemcpyHostToDevice, p->stream);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(p->hwa, WA, nw, cudaMemcpyHostToDevice, p->stream);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(p->hv[0], V, nx, cudaMemcpyHostToDevice, p->stream);
+    if (e != cudaSuccess) return CAT_ERR_CUDA;
+    st = cat_forward(p, p->hx[0], p->hwa, p->hv[0], p->ho[0], B, N, D, H, dtype);
+    if (st != CAT_OK) return st;
+    e = cudaMemcpyAsync(O, p->ho[0], nx, cudaMemcpyDeviceToHost, p->stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(p->stream);
+    return map_cuda(e);
+  }
+  const size_t nb = (size_t)N * D * es;
+  const char* xs = static_cast<const char*>(X);
+  const char* vs = static_cast<const char*>(V);
+  char* os = static_cast<char*>(O);
+  cudaStream_t in = p->hcp[0], out = p->hcp[1];
+  // W_A first on the input stream: every step's compute waits for an event
+  // recorded after it there.
+  cudaError_t e = cudaStreamWaitEvent(in, p->hev_done[0], 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(in, p->hev_done[1], 0);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(p->hwa, WA, nw, cudaMemcpyHostToDevice, in);
+  for (int b = 0; b < B && e == cudaSuccess; ++b) {
+    const int s = b & 1;
+    cat_plan_s* sub = p->hsub[s];
+    sub->stream = p->stream;
+    e = cudaStreamWaitEvent(in, p->hev_done[s], 0);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(p->hx[s], xs + b * nb, nb, cudaMemcpyHostToDevice, in);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(p->hv[s], vs + b * nb, nb, cudaMemcpyHostToDevice, in);
+    if (e == cudaSuccess) e = cudaEventRecord(p->hev_in[s], in);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(p->stream, p->hev_in[s], 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(p->stream, p->hev_out[s], 0);
+    if (e != cudaSuccess) break;
+    st = cat_forward(sub, p->hx[s], p->hwa, p->hv[s], p->ho[s], 1, N, D, H, dtype);
+    if (st != CAT_OK) return st;
+    e = cudaEventRecord(p->hev_done[s], p->stream);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(out, p->hev_done[s], 0);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(os + b * nb, p->ho[s], nb, cudaMemcpyDeviceToHost, out);
+    if (e == cudaSuccess) e = cudaEventRecord(p->hev_out[s], out);
+  }
+  if (e == cudaSuccess) e = cudaStreamSynchronize(out);
   return map_cuda(e);
 }
 
@@ -871,6 +1057,8 @@ int cat_backward(cat_plan_t p, const void* X, const void* WA, const void* V, con
     } else if (p->path == cat::PATH_FAST) {
       e = cat::launch_fast_zspec(p, 0, p->B * p->H, p->stream);
       if (e == cudaSuccess) e = cat::launch_fast_conv(p, dO, dV);
+    } else if (p->path == cat::PATH_DIRECT) {
+      e = cat::launch_direct(p, nullptr, nullptr, dO, dV, false);
     } else {
       e = cat::launch_softmax(p);
       if (e == cudaSuccess) e = cat::launch_fourstep_conv(p, dO, dV);
@@ -949,15 +1137,20 @@ int cat2d_forward(cat_plan_t p, const void* Q, const void* K, const void* V, voi
 int cat_plan_sync(cat_plan_t p) {
   if (!p) return CAT_ERR_INVALID_ARG;
   if (cudaStreamSynchronize(p->stream) != cudaSuccess) return CAT_ERR_CUDA;
-  unsigned int word = 0;
-  if (cudaMemcpy(&word, p->status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
-    return CAT_ERR_CUDA;
-  if (word != 0) {
-    if (std::getenv("CAT_LOG")) std::fprintf(stderr, "[cat] device status 0x%x\n", word);
-    cudaMemset(p->status, 0, sizeof(unsigned int));
-    return CAT_ERR_DEVICE_STATUS;
+  // The plan's own status word and those of its host-buffer sub-plans.
+  int st = CAT_OK;
+  for (cat_plan_s* q : {p, p->hsub[0], p->hsub[1]}) {
+    if (!q) continue;
+    unsigned int word = 0;
+    if (cudaMemcpy(&word, q->status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+      return CAT_ERR_CUDA;
+    if (word != 0) {
+      if (std::getenv("CAT_LOG")) std::fprintf(stderr, "[cat] device status 0x%x\n", word);
+      cudaMemset(q->status, 0, sizeof(unsigned int));
+      st = CAT_ERR_DEVICE_STATUS;
+    }
   }
-  return CAT_OK;
+  return st;
 }
 
 int cat_plan_timing(cat_plan_t p, int max_calls) {

@@ -8,7 +8,7 @@
 
 namespace cat {
 
-enum Path { PATH_SMEM = 0, PATH_FOURSTEP = 1, PATH_FAST = 2 };
+enum Path { PATH_SMEM = 0, PATH_FOURSTEP = 1, PATH_FAST = 2, PATH_DIRECT = 3 };
 
 // Launch shape of the single-CTA shared-memory path (N up to 16384): one CTA
 // transforms G packed column pairs of one (b, h).
@@ -21,6 +21,15 @@ struct SmemCfg {
   int spec_threads;  // CTA size of the softmax+spectrum kernel
   size_t spec_smem;
   int reg_m;         // N = reg_m² transformed in registers (conv_reg), else 0
+};
+
+// Launch shape of the direct (O(N²·dh), no transform) path for short
+// sequences: one CTA of threads = (dh/4)·nrg per (R-row tile, b, h); thread
+// (rg, cg) owns TR rows and 4 columns.  fused: the CTA computes its row's
+// scores from X and W_A itself (the whole forward is one launch).
+struct DirectCfg {
+  int TR, nrg, R, threads, fused;
+  size_t smem;
 };
 
 // Four-step decomposition N = N1·N2 with row n = n1 + N1·n2 and bin
@@ -75,6 +84,7 @@ struct cat_plan_s {
   cat::RadixPlan rpN;       // radices of N (shared-memory path)
   cat::SmemCfg sm;
   cat::FourStepCfg fs;
+  cat::DirectCfg dir;
   int score_cuda_cores;     // 1: bf16 scores on the CUDA-core kernel (testing)
   int score_path;           // 1: bf16 scores on the register-fed MMA kernel (testing)
   int fork_at;              // fast path: where the chunk streams fork (cat::FORK_*)
@@ -100,8 +110,16 @@ struct cat_plan_s {
   const void* gX; const void* gWA; const void* gV; void* gO;
   unsigned int* status;     // device status word
   size_t workspace_bytes;
-  // device staging for host-buffer calls (allocated at the first such call)
-  void* hx; void* hwa; void* hv; void* ho;
+  // host-buffer calls (cat_forward_host), set up at the first such call:
+  // device staging (two slots of one batch each when B >= 2, else one slot
+  // of the whole problem), two one-batch sub-plans that alternate between the
+  // slots, the copy streams (0: host to device, 1: device to host) and the
+  // events that order a slot's copies and compute
+  int hready;
+  void* hx[2]; void* hv[2]; void* ho[2]; void* hwa;
+  cat_plan_s* hsub[2];
+  cudaStream_t hcp[2];
+  cudaEvent_t hev_in[2], hev_done[2], hev_out[2];
   // stage timing: 4 events per recorded call (before score, after score,
   // after softmax/spectrum, after the circulant product)
   cudaEvent_t* ev;
@@ -194,6 +212,14 @@ cudaError_t launch_fast_zspec(const cat_plan_s* p, int row0, int nrows, cudaStre
 cudaError_t launch_fast_chunk(const cat_plan_s* p, const void* V, void* O, int bh0, int nb,
                               int slot, cudaStream_t st, cudaEvent_t before_b = nullptr,
                               cudaEvent_t* after = nullptr);
+
+// Direct path (direct.cu): dynamic shared memory of a CTA, one-time
+// attribute set-up, and the launch (fused: scores computed in the kernel;
+// else from z2, which launch_score filled).
+size_t direct_smem(int N, int D, int dh, int R, bool fused);
+cudaError_t setup_direct_kernels(const cat_plan_s* p);
+cudaError_t launch_direct(const cat_plan_s* p, const void* X, const void* WA, const void* V,
+                          void* O, bool fused);
 
 // Shape validation and shared-memory-path configuration without allocation.
 int validate(int B, int N, int D, int H, int dtype);

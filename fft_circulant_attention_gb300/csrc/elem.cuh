@@ -25,6 +25,17 @@ __device__ __forceinline__ void st_pair(__nv_bfloat16* p, float2 v) {
   *reinterpret_cast<__nv_bfloat162*>(p) = __floats2bfloat162_rn(v.x, v.y);
 }
 
+// Adds p to the double-float accumulator (hi, lo): hi + p is split exactly
+// into its rounded sum and rounding error (Knuth's TwoSum), the error joins
+// lo.
+__device__ __forceinline__ void two_sum_acc(float& hi, float& lo, float p) {
+  float s = hi + p;
+  float bp = s - hi;
+  float err = (hi - (s - bp)) + (p - bp);
+  hi = s;
+  lo += err;
+}
+
 // Warp and block reductions.
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll

@@ -91,6 +91,8 @@ fsf_pass_a(const T* __restrict__ V, float2* __restrict__ scr, const float2* __re
 #pragma unroll
       for (int e = 0; e < PER; e += 2) ld_sh2(row + PER * j + e + 32 * u, c[e][u], c[e + 1][u]);
     const int wstep = N / N2;
+    // The scratch is read again by passes B and C: keep it in L2.
+    const uint64_t keep = policy_evict_last();
 #pragma unroll
     for (int e = 0; e < PER; ++e) {
       const int k = PER * j + e;
@@ -100,7 +102,8 @@ fsf_pass_a(const T* __restrict__ V, float2* __restrict__ scr, const float2* __re
 #pragma unroll
       for (int s = 0; s < R2; ++s) {
         const int k2 = k + 32 * s;
-        scr[scr_idx(bhl, N2, k2, n1, lane)] = cmul(c[e][s], __ldg(&W[(size_t)n1 * k2]));
+        st_hint(scr + scr_idx(bhl, N2, k2, n1, lane), cmul(c[e][s], __ldg(&W[(size_t)n1 * k2])),
+                keep);
       }
     }
   }
@@ -134,6 +137,14 @@ fsf_pass_c(const float2* __restrict__ scr, T* __restrict__ O, const float2* __re
 #pragma unroll
     for (int s = 0; s < 32; s += 2) st_sh2(row + 32 * j + s, a[s], a[s + 1]);
     __syncthreads();
+    {
+      // Every thread has its values: the CTA's N2 scratch rows (k2, n1) are
+      // dead, so their two 128-byte lines each leave L2 without a
+      // write-back (the next chunk's pass A rewrites them first).
+      const float2* r = scr + scr_idx(bhl, N2, threadIdx.x, n1, 0);
+      discard_l2(r);
+      discard_l2(r + 16);
+    }
     float2 c[PER][R2];
 #pragma unroll
     for (int u = 0; u < R2; ++u)

@@ -53,17 +53,6 @@ template <> struct Vec16<__nv_bfloat16> {
   }
 };
 
-// Adds p to the double-float accumulator (hi, lo): hi + p is split exactly
-// into its rounded sum and rounding error (Knuth's TwoSum), the error joins
-// lo.
-__device__ __forceinline__ void two_sum_acc(float& hi, float& lo, float p) {
-  float s = hi + p;
-  float bp = s - hi;
-  float err = (hi - (s - bp)) + (p - bp);
-  hi = s;
-  lo += err;
-}
-
 // The same for two accumulators at once with the paired fp32 instructions
 // (each component rounds exactly as the scalar operation; x - y is formed as
 // y·(-1) + x, exact in the product).

@@ -131,11 +131,17 @@ int cat_forward_zstar(cat_plan_t plan, const void *X, const void *W_A,
                       float *zstar, int B, int N, int D, int H, int dtype);
 
 /*
- * cat_forward_host — the same forward on HOST buffers: copies X, W_A, V to
- * plan-owned device buffers (allocated at the first call and kept by the
- * plan), runs cat_forward, copies O back, and synchronises the stream before
- * returning.  Pinned (page-locked) host memory gives asynchronous copies;
- * pageable memory works but is slower.  X, W_A, V are read, O is written.
+ * cat_forward_host — the same forward on HOST buffers, copies included: X,
+ * W_A, V are read from host memory and O is written to host memory before
+ * the call returns (it synchronises).  With B >= 2 the call runs one batch
+ * per step and overlaps the copies with the compute: batch b's inputs copy
+ * in on one internal stream while batch b - 1 computes on the plan's stream
+ * and batch b - 2's output copies out on another.  The first call sets up
+ * plan-owned device staging (two batches' worth, or the whole problem when
+ * B = 1), two internal one-batch plans and the copy streams, which the plan
+ * keeps; CAT_ERR_ALLOC if that fails.  Pinned (page-locked) host memory is
+ * needed for the copies to overlap; pageable memory works but serialises.
+ * Kernel status of the internal plans is reported by cat_plan_sync.
  */
 int cat_forward_host(cat_plan_t plan, const void *X, const void *W_A,
                      const void *V, void *O, int B, int N, int D, int H,

@@ -145,6 +145,12 @@ def test_dtype_codes():
     ((2, 32768, 128, 2, "f32"), ["path=fast", "N2=64"]),
     ((1, 20000, 4, 2, "f32"), ["path=fourstep", "N1=160(8x4x5)", "N2=125(5x5x5)"]),
     ((1, 1 << 22, 64, 1, "f32"), ["path=fourstep", "N1=2048", "N2=2048"]),   # 2^22 > 512·256
+    # Short lengths without a register FFT kernel take the direct product.
+    ((32, 128, 768, 12, "bf16"), ["path=direct", "TR=8", "fused=0", "launches=2"]),
+    ((8, 512, 768, 12, "bf16"), ["path=direct", "fused=0"]),
+    ((3, 100, 48, 3, "f32"), ["path=direct", "fused=1", "launches=1"]),
+    ((1, 1000, 16, 2, "f32"), ["path=smem", "reg_m=0"]),            # N > 512: transforms
+    ((4, 64, 384, 6, "f32"), ["path=smem", "reg_m=8"]),             # 8²: register FFT
 ])
 def test_query_path_choice(lib, shape, expect):
     nbytes, desc = cat.cat_plan_query(*shape)
@@ -164,6 +170,16 @@ def test_query_matches_between_calls_and_env(lib, monkeypatch):
     monkeypatch.delenv("CAT_FORCE_PATH")
     monkeypatch.setenv("CAT_SMEM_REG", "0")
     assert "reg_m=0" in cat.cat_plan_query(1, 256, 64, 2, "f32")[1]
+    monkeypatch.delenv("CAT_SMEM_REG")
+    # CAT_FORCE_PATH=direct wherever the direct product is supported (head
+    # width a multiple of 4, at most 128; N <= 1024), =smem never.
+    monkeypatch.setenv("CAT_FORCE_PATH", "direct")
+    assert "path=direct" in cat.cat_plan_query(1, 256, 64, 2, "f32")[1]
+    assert "path=direct" in cat.cat_plan_query(16, 1024, 768, 12, "f32")[1]
+    assert "path=smem" in cat.cat_plan_query(1, 256, 10, 2, "f32")[1]      # head width 5
+    assert "path=smem" in cat.cat_plan_query(1, 2048, 64, 2, "f32")[1]     # N > 1024
+    monkeypatch.setenv("CAT_FORCE_PATH", "smem")
+    assert "path=smem" in cat.cat_plan_query(32, 128, 768, 12, "bf16")[1]
 
 
 @pytest.mark.parametrize("shape,code", [

@@ -205,15 +205,24 @@ def test_uniform_gives_column_mean(N, dtype):
 
 # ------------------------------------------------------- API behaviour
 
-def test_host_buffer_entry_matches_device_entry():
-    B, N, D, H = 2, 1024, 64, 4
-    X, WA, V = synth.make_inputs(B, N, D, H, "bf16", seed=5)
-    Od, _ = run_gpu(X, WA, V, "bf16", want_zstar=False)
+@pytest.mark.parametrize("B,N,D,H,dtype", [
+    (2, 1024, 64, 4, "bf16"),      # two one-batch steps
+    (5, 196, 384, 6, "f32"),       # odd step count: both staging slots, last one alone
+    (3, 16384, 128, 2, "bf16"),    # the fast path in one-batch sub-plans
+    (1, 1000, 16, 2, "f32"),       # one batch: the serial copy, compute, copy
+])
+def test_host_buffer_entry_matches_device_entry(B, N, D, H, dtype):
+    """The host-buffer entry (copies inside the call, overlapped with the
+    compute one batch per step) gives the device entry's output bit for bit:
+    every (b, h) is computed by the same kernels on the same values."""
+    X, WA, V = synth.make_inputs(B, N, D, H, dtype, seed=5)
+    Od, _ = run_gpu(X, WA, V, dtype, want_zstar=False)
     Xp, Wp, Vp = (t.pin_memory() for t in (X, WA, V))
     Oh = torch.empty_like(Vp).pin_memory()
-    with cat.Plan(B, N, D, H, "bf16") as p:
+    with cat.Plan(B, N, D, H, dtype) as p:
         p.forward_host(Xp, Wp, Vp, Oh)
-        p.forward_host(Xp, Wp, Vp, Oh)   # staging buffers are reused
+        Oh.fill_(float("nan"))
+        p.forward_host(Xp, Wp, Vp, Oh)   # staging buffers and sub-plans are reused
         p.sync()
     assert torch.equal(Oh, Od)
 
