@@ -12,7 +12,8 @@ CUDA kernels of ``libcat.so``; there is no other implementation behind it,
 and importing it fails loudly when the library has not been built.
 
 The functions carry the C names: ``cat_plan_create``, ``cat_forward``,
-``cat_forward_zstar``, ``cat_forward_host``, ``cat_backward``,
+``cat_forward_zstar``, ``cat_forward_host``, ``cat_forward_fused``,
+``cat_project``, ``cat_forward_noalloc``, ``cat_backward``,
 ``cat_backward_dz``, ``cat_plan_create_2d``, ``cat2d_forward``, ``cat2d_scores``,
 ``cat_plan_query``,
 ``cat_plan_sync``,
@@ -47,6 +48,8 @@ SIGNATURES = {
     "cat_plan_set_stream": (_I, [_P, _P]),
     "cat_forward": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I]),
     "cat_forward_zstar": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I]),
+    "cat_forward_fused": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I]),
+    "cat_project": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I]),
     "cat_forward_host": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I]),
     "cat_plan_sync": (_I, [_P]),
     "cat_plan_describe": (_I, [_P, ctypes.c_char_p, _I]),
@@ -178,6 +181,16 @@ def cat_forward_host(plan, X, W_A, V, O, B, N, D, H, dtype):
                                   dtype_code(dtype)), "cat_forward_host")
 
 
+def cat_forward_fused(plan, X, W_V, W_A, V, O, B, N, D, H, dtype):
+    _check(lib().cat_forward_fused(plan, _ptr(X), _ptr(W_V), _ptr(W_A), _ptr(V), _ptr(O), B, N, D,
+                                   H, dtype_code(dtype)), "cat_forward_fused")
+
+
+def cat_project(plan, X, W_V, W_A, V, zstar, B, N, D, H, dtype):
+    _check(lib().cat_project(plan, _ptr(X), _ptr(W_V), _ptr(W_A), _ptr(V), _ptr(zstar), B, N, D,
+                             H, dtype_code(dtype)), "cat_project")
+
+
 def cat_forward_noalloc(X, W_A, V, O, B, N, D, H, dtype, stream=None):
     """The forward without a plan or any allocation (fixed device workspace;
     B·H·N and N bounded).  Enqueued on `stream` (default: the legacy default
@@ -273,6 +286,26 @@ class Plan:
                 raise ValueError("tensors must be contiguous %s" % self.torch_dtype)
         cat_forward(self.handle, X, W_A, V, O, *self._shape())
         return O
+
+    def forward_fused(self, X, W_V, W_A, V=None, O=None):
+        """V = X·W_V and the scores from one pass over X (tensor cores), then
+        the forward; returns (V, O)."""
+        import torch
+        V = torch.empty_like(X) if V is None else V
+        O = torch.empty_like(X) if O is None else O
+        for t in (X, W_V, W_A, V, O):
+            if not t.is_contiguous() or t.dtype != self.torch_dtype:
+                raise ValueError("tensors must be contiguous %s" % self.torch_dtype)
+        cat_forward_fused(self.handle, X, W_V, W_A, V, O, *self._shape())
+        return V, O
+
+    def project(self, X, W_V, W_A):
+        """The fused projection alone: returns (V, z*)."""
+        import torch
+        V = torch.empty_like(X)
+        zs = torch.empty((self.B, self.H, self.N), dtype=torch.float32, device=X.device)
+        cat_project(self.handle, X, W_V, W_A, V, zs, *self._shape())
+        return V, zs
 
     def zstar(self, X, W_A, out=None):
         import torch

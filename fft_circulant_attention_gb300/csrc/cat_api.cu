@@ -161,6 +161,7 @@ void free_plan(cat_plan_s* p) {
     if (p->hev_out[k]) cudaEventDestroy(p->hev_out[k]);
   }
   cudaFree(p->hwa);
+  cudaFree(p->pj_wt);
   delete p;
 }
 
@@ -603,7 +604,7 @@ namespace {
 // the first passes A run beside the score and the spectrum.  Both join back
 // into the plan's stream at the end.
 cudaError_t run_fast_overlapped(cat_plan_s* p, const void* X, const void* WA, const void* V,
-                                void* O) {
+                                void* O, bool score = true) {
   cudaError_t e = cudaSuccess;
   auto fork = [&]() {
     if (e == cudaSuccess) e = cudaEventRecord(p->ev_fork, p->stream);
@@ -611,7 +612,7 @@ cudaError_t run_fast_overlapped(cat_plan_s* p, const void* X, const void* WA, co
       e = cudaStreamWaitEvent(p->side[k], p->ev_fork, 0);
   };
   if (p->fork_at == cat::FORK_START) fork();
-  if (e == cudaSuccess) e = cat::launch_score(p, X, WA);
+  if (e == cudaSuccess && score) e = cat::launch_score(p, X, WA);
   if (p->fork_at == cat::FORK_SCORE) fork();
   if (e == cudaSuccess) e = cat::launch_fast_zspec(p, 0, p->B * p->H, p->stream);
   if (p->fork_at == cat::FORK_SPECTRUM) fork();
@@ -887,6 +888,94 @@ int cat_forward(cat_plan_t p, const void* X, const void* WA, const void* V, void
                                   : cat::launch_fourstep_conv(p, V, O);
     if (ev) cudaEventRecord(ev[3], p->stream);
   }
+  return map_cuda(e);
+}
+
+namespace {
+
+// Argument checks of the fused projection (bf16, D % 64 == 0, H <= 16,
+// 16-byte alignment, V not overlapping the inputs) and the first call's
+// workspace for the transposed weights.
+int project_prepare(cat_plan_s* p, const void* X, const void* WV, const void* WA, const void* V,
+                    int B, int N, int D, int H, int dtype) {
+  if (!p) return CAT_ERR_INVALID_ARG;
+  if (p->twod) return CAT_ERR_PLAN_MISMATCH;
+  int st = check_shape(p, B, N, D, H, dtype);
+  if (st != CAT_OK) return st;
+  if (dtype != CAT_BF16 || D % 64 != 0 || H > 16) return CAT_ERR_INVALID_ARG;
+  if (B == 0) return CAT_OK;
+  if (!X || !WV || !WA || !V) return CAT_ERR_INVALID_ARG;
+  if (((uintptr_t)X | (uintptr_t)WV | (uintptr_t)WA | (uintptr_t)V) & 15) return CAT_ERR_MISALIGNED;
+  const size_t nx = (size_t)B * N * D * 2;
+  if (ranges_overlap(V, nx, X, nx) || ranges_overlap(V, nx, WV, (size_t)D * D * 2) ||
+      ranges_overlap(V, nx, WA, (size_t)D * H * 2))
+    return CAT_ERR_ALIAS;
+  if (!p->pj_wt) {
+    if (cudaMalloc(&p->pj_wt, cat::project_workspace_bytes(D)) != cudaSuccess) {
+      cudaGetLastError();
+      p->pj_wt = nullptr;
+      return CAT_ERR_ALLOC;
+    }
+    if (cat::setup_project_kernels() != cudaSuccess) {
+      cudaGetLastError();
+      return CAT_ERR_CUDA;
+    }
+  }
+  return CAT_OK;
+}
+
+}  // namespace
+
+// The fused-projection forward: V = X·W_V and the scores in one pass over X
+// on the tensor cores, then the plan's own softmax, spectrum and circulant
+// product on that V (the fast path's overlapped schedule runs without a
+// graph here).
+int cat_forward_fused(cat_plan_t p, const void* X, const void* WV, const void* WA, void* V,
+                      void* O, int B, int N, int D, int H, int dtype) {
+  int st = project_prepare(p, X, WV, WA, V, B, N, D, H, dtype);
+  if (st != CAT_OK || B == 0) return st;
+  if (!O) return CAT_ERR_INVALID_ARG;
+  if ((uintptr_t)O & 15) return CAT_ERR_MISALIGNED;
+  const size_t nx = (size_t)B * N * D * 2;
+  if (ranges_overlap(O, nx, X, nx) || ranges_overlap(O, nx, WV, (size_t)D * D * 2) ||
+      ranges_overlap(O, nx, WA, (size_t)D * H * 2) || ranges_overlap(O, nx, V, nx))
+    return CAT_ERR_ALIAS;
+  cudaError_t e = cat::launch_project(p, X, WV, WA, V, p->pj_wt);
+  if (e != cudaSuccess) return CAT_ERR_CUDA;
+  switch (p->path) {
+    case cat::PATH_FAST:
+      e = run_fast_overlapped(p, X, WA, V, O, false);
+      break;
+    case cat::PATH_SMEM:
+      e = cat::launch_softmax_spectrum(p);
+      if (e == cudaSuccess) e = cat::launch_conv_smem(p, V, O);
+      break;
+    case cat::PATH_DIRECT:
+      e = cat::launch_direct(p, X, WA, V, O, false);
+      break;
+    default:
+      e = cat::launch_softmax(p);
+      if (e == cudaSuccess) e = cat::launch_fourstep_conv(p, V, O);
+      break;
+  }
+  return map_cuda(e);
+}
+
+// The fused projection alone: V and, after the softmax, z* (fp32 [B, H, N]).
+int cat_project(cat_plan_t p, const void* X, const void* WV, const void* WA, void* V,
+                float* zstar, int B, int N, int D, int H, int dtype) {
+  int st = project_prepare(p, X, WV, WA, V, B, N, D, H, dtype);
+  if (st != CAT_OK || B == 0) return st;
+  if (!zstar) return CAT_ERR_INVALID_ARG;
+  if ((uintptr_t)zstar & 15) return CAT_ERR_MISALIGNED;
+  const size_t nx = (size_t)B * N * D * 2, nz = (size_t)B * H * N * sizeof(float);
+  if (ranges_overlap(zstar, nz, X, nx) || ranges_overlap(zstar, nz, V, nx))
+    return CAT_ERR_ALIAS;
+  cudaError_t e = cat::launch_project(p, X, WV, WA, V, p->pj_wt);
+  if (e == cudaSuccess)
+    e = p->path == cat::PATH_SMEM ? cat::launch_softmax_spectrum(p) : cat::launch_softmax(p);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(zstar, p->zs, nz, cudaMemcpyDeviceToDevice, p->stream);
   return map_cuda(e);
 }
 

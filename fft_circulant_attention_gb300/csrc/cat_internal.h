@@ -120,6 +120,9 @@ struct cat_plan_s {
   cat_plan_s* hsub[2];
   cudaStream_t hcp[2];
   cudaEvent_t hev_in[2], hev_done[2], hev_out[2];
+  // fused projection (cat_forward_fused): the K-major B operands W_V^T and
+  // W_A^T, allocated at the first such call
+  void* pj_wt;
   // stage timing: 4 events per recorded call (before score, after score,
   // after softmax/spectrum, after the circulant product)
   cudaEvent_t* ev;
@@ -220,6 +223,15 @@ size_t direct_smem(int N, int D, int dh, int R, bool fused);
 cudaError_t setup_direct_kernels(const cat_plan_s* p);
 cudaError_t launch_direct(const cat_plan_s* p, const void* X, const void* WA, const void* V,
                           void* O, bool fused);
+
+// Fused projection on the tensor cores (proj_tc.cu): V = X·W_V into V and
+// the scores X·W_A into the plan's z2 in one pass over X (bf16, D % 64 == 0,
+// H <= 16).  wt: project_workspace_bytes(D) of device memory for the
+// transposed weights.
+size_t project_workspace_bytes(int D);
+cudaError_t setup_project_kernels();
+cudaError_t launch_project(const cat_plan_s* p, const void* X, const void* WV, const void* WA,
+                           void* V, void* wt);
 
 // Shape validation and shared-memory-path configuration without allocation.
 int validate(int B, int N, int D, int H, int dtype);

@@ -1,0 +1,96 @@
+// Fifth-generation tensor core (tcgen05) building blocks for sm_103a:
+// tensor-memory allocation, shared-memory matrix descriptors, the
+// single-thread MMA issue and its completion on an mbarrier, and the
+// tensor-memory loads of the epilogue.  Inline PTX, one instruction each.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "bulk.cuh"
+
+namespace cat {
+
+// Tensor memory: one warp allocates `ncols` columns (a power of two, >= 32)
+// for all 128 lanes and writes the base address to shared memory; the same
+// warp frees them.  The permit is given up right after so that other CTAs
+// on the SM can allocate.
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_addr(slot)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+// Ordering of tcgen05 operations across a thread barrier.
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major tile stored with the
+// 128-byte swizzle (rows of 64 bf16 = 128 bytes, 8-row atoms of 1024 bytes,
+// the layout a 128-byte-swizzled tensor copy writes): start address,
+// stride between 8-row atoms 1024 bytes, descriptor version 1, swizzle
+// mode 128 bytes.  The tile must start on a 1024-byte boundary; a start
+// advanced by 32·k bytes selects the k-th 16-element slice of the 64.
+__device__ __forceinline__ uint64_t sdesc_k128(const void* p) {
+  const uint32_t a = smem_addr(p);
+  uint64_t d = (uint64_t)((a & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;                 // leading-dimension offset (unused here)
+  d |= (uint64_t)(1024 >> 4) << 32;       // stride-dimension offset
+  d |= (uint64_t)1 << 46;                 // descriptor version
+  d |= (uint64_t)2 << 61;                 // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor of kind::f16 with bf16 A and B (both K-major) and
+// an fp32 accumulator, shape M x N (M = 128: N a multiple of 16, <= 256).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
+
+// D[tmem] (+)= A[smem] · B[smem]^T, issued by one thread.
+__device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on `bar` once every MMA this thread issued before has completed.
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_addr(bar))
+      : "memory");
+}
+
+// 16 consecutive fp32 columns of this thread's lane (32x32b shape: warp w
+// of a warpgroup reads lanes 32·(w % 4) ..), waited for.
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+}  // namespace cat

@@ -123,6 +123,38 @@ int cat_forward(cat_plan_t plan, const void *X, const void *W_A, const void *V,
                 void *O, int B, int N, int D, int H, int dtype);
 
 /*
+ * cat_forward_fused — the value projection and the scores from one pass
+ * over X, then the forward: V = X·W_V (written to V) and z = X·W_A from the
+ * same tensor-core GEMM [V | z] = X·[W_V | W_A] (the notes page cited
+ * above, 整体框架 overall framework: a CAT layer projects X with W_V for
+ * the values and W_A for the scores), then O = CAT(X, W_A, V) exactly as
+ * cat_forward computes it from those V and z.
+ *
+ * X [B, N, D], W_V [D, D] (row-major, V[b, n, :] = X[b, n, :]·W_V) and
+ * W_A [D, H]: device pointers, read only.  V and O [B, N, D]: device
+ * pointers, written.  bf16 only (CAT_ERR_INVALID_ARG otherwise), D a
+ * multiple of 64, H <= 16; products of bf16 values are exact, accumulation
+ * fp32; V is rounded to bf16 (nearest even); the scores are kept as
+ * double-float sums of 64-wide fp32 slices.  All pointers 16-byte aligned;
+ * V and O must not overlap the inputs or each other (CAT_ERR_ALIAS).  The
+ * first call allocates the plan's transposed-weight workspace (2·D·(D+16)
+ * bytes; CAT_ERR_ALLOC).  Asynchronous on the plan's stream.
+ */
+int cat_forward_fused(cat_plan_t plan, const void *X, const void *W_V,
+                      const void *W_A, void *V, void *O, int B, int N, int D,
+                      int H, int dtype);
+
+/*
+ * cat_project — the fused projection alone: V = X·W_V (written to V) and
+ * z* = softmax over the tokens of X·W_A (fp32 [B, H, N], written to the
+ * device pointer zstar), from the same one-pass tensor-core GEMM as
+ * cat_forward_fused.  Arguments, limits and errors as cat_forward_fused;
+ * zstar must not overlap X or V (CAT_ERR_ALIAS).
+ */
+int cat_project(cat_plan_t plan, const void *X, const void *W_V, const void *W_A,
+                void *V, float *zstar, int B, int N, int D, int H, int dtype);
+
+/*
  * cat_forward_zstar — only the first two steps (score projection and
  * softmax over the N tokens, "circulant attention matrix construction"):
  * writes z* as fp32 [B, H, N] to the device pointer zstar (16-byte aligned).

@@ -128,6 +128,13 @@ def softmax(z):
     return out
 
 
+def project(X, W):
+    """V = X · W per token (the value projection of a CAT layer), fp64:
+    V[b, n, e] = sum_d X[b, n, d] W[d, e].  numpy's matmul is the step."""
+    X, W = _f64(X), _f64(W)
+    return X @ W
+
+
 def zstar(X, WA):
     """z* = softmax_n(X · W_A), shape [B, H, N]."""
     return softmax(scores(X, WA))

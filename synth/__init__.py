@@ -13,6 +13,8 @@ masked-LM tokens — have no public inputs here, so i.i.d. Gaussians stand in):
     second, independent stream (``make_grad``);
   * the 2-D circulant attention's Q, K, V ~ N(0, 1), [B, h·w, D], from a
     third stream (``make_qkv``);
+  * the value projection's W_V ~ N(0, 1/D), [D, D], from a fourth stream
+    (``make_wv``);
   * then rounded to the storage dtype (float32 as drawn; bfloat16 by torch's
     round-to-nearest-even conversion).
 """
@@ -75,6 +77,18 @@ def make_qkv(B, N, D, dtype="f32", seed=0):
     rng = np.random.Generator(np.random.PCG64([seed, 2]))
     out = [rng.standard_normal((B, N, D), dtype=np.float32) for _ in range(3)]
     return tuple(torch.from_numpy(a).to(DTYPES[dtype]) for a in out)
+
+
+def make_wv(D, dtype="f32", seed=0):
+    """Value-projection weights W_V [D, D] ~ N(0, 1/D): float32 normals from
+    the stream ``PCG64([seed, 3])`` (independent of the other draws), scaled,
+    rounded to ``dtype``."""
+    if dtype not in DTYPES:
+        raise ValueError("dtype must be one of %s" % sorted(DTYPES))
+    rng = np.random.Generator(np.random.PCG64([seed, 3]))
+    W = rng.standard_normal((D, D), dtype=np.float32)
+    W *= np.float32(1.0 / np.sqrt(D)) if D > 0 else np.float32(0)
+    return torch.from_numpy(W).to(DTYPES[dtype])
 
 
 def make_config(name, seed=0, wa_scale=1.0):

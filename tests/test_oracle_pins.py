@@ -348,3 +348,27 @@ def test_peaked_softmax_is_finite_and_normalised():
     assert np.isfinite(zs).all() and (zs >= 0).all()
     np.testing.assert_allclose(zs.sum(-1), 1.0, atol=1e-13)
     assert zs.max() > 0.5      # peaked
+
+
+# --------------------------------------------------------------------------
+# Value projection V = X · W_V (the fused-projection entry's first product)
+# --------------------------------------------------------------------------
+
+def test_projection_against_explicit_sums():
+    """oracle.project against the sum written out term by term, and the
+    identity and linearity it must have (section 整体框架: V = X·W_V)."""
+    rng = np.random.default_rng(31)
+    X = rng.standard_normal((2, 5, 6))
+    W = rng.standard_normal((6, 4))
+    V = oracle.project(X, W)
+    for b in range(2):
+        for n in range(5):
+            for e in range(4):
+                s = 0.0
+                for d in range(6):
+                    s += X[b, n, d] * W[d, e]
+                assert abs(V[b, n, e] - s) <= 1e-13 * (1 + abs(s))
+    np.testing.assert_array_equal(oracle.project(X, np.eye(6)), X)
+    W2 = rng.standard_normal((6, 4))
+    np.testing.assert_allclose(oracle.project(X, 2 * W - W2), 2 * V - oracle.project(X, W2),
+                               atol=1e-12)
