@@ -376,10 +376,11 @@ void describe(cat_plan_s* p) {
     radstr(p->fs.rp1, r1, sizeof(r1));
     radstr(p->fs.rp2, r2, sizeof(r2));
     std::snprintf(p->desc, sizeof(p->desc),
-                  "path=%s N=%d N1=%d(%s) N2=%d(%s) G=%d groups=%d TA=%d TB=%d "
+                  "path=%s%s N=%d N1=%d(%s) N2=%d(%s) G=%d groups=%d TA=%d TB=%d "
                   "threads=%d/%d/%d smem=%zu/%zu/%zu chunk_bh=%d scratch=%zu workspace=%zu "
                   "launches=%d",
-                  p->twod ? "grid2d" : "fourstep", p->N, p->fs.N1, r1, p->fs.N2, r2, p->fs.G,
+                  p->twod ? "grid2d" : "fourstep", p->reg2d ? " reg2d=1" : "", p->N,
+                  p->fs.N1, r1, p->fs.N2, r2, p->fs.G,
                   p->fs.groups, p->fs.TA, p->fs.TB,
                   p->fs.threadsA, p->fs.threadsB, p->fs.threadsC, p->fs.smemA, p->fs.smemB,
                   p->fs.smemC, p->fs.chunk_bh, p->scratch_bytes, p->workspace_bytes,
@@ -407,7 +408,7 @@ size_t planned_workspace(const cat_plan_s* p) {
   const size_t rowsN = (size_t)p->B * p->H * p->N;
   const bool fast = p->path == cat::PATH_FAST;
   return rowsN * (sizeof(float) + sizeof(float2)) + (size_t)p->N * sizeof(float2) +
-         ((p->path == cat::PATH_SMEM || fast) ? rowsN * sizeof(float2) : 0) +
+         ((p->path == cat::PATH_SMEM || fast || p->reg2d) ? rowsN * sizeof(float2) : 0) +
          (fast ? rowsN * sizeof(float2) : 0) +
          (p->path != cat::PATH_SMEM ? p->scratch_bytes : 0) +
          (fast ? cat::fast_tables_bytes(p->fs.N2) : 0);
@@ -715,6 +716,20 @@ int create_plan(cat_plan_t* out, int B, int N, int D, int H, int dtype, void* st
     p->grid_h = gh;
     p->grid_w = gw;
     st = configure_fourstep(p, gw, gh);
+    // Square grids of a register-DFT side take the register kernels
+    // (CAT_2D_REG=0: the generic passes).
+    const char* r2 = std::getenv("CAT_2D_REG");
+    if (st == CAT_OK && gh == gw && (gh == 8 || gh == 14 || gh == 16 || gh == 32) &&
+        !(r2 && std::strcmp(r2, "0") == 0)) {
+      p->reg2d = 1;
+      cat::SmemCfg& sc = p->sm;
+      sc.reg_m = gh;
+      sc.G = cat::conv_reg_pairs(gh);
+      sc.groups = (p->npair + sc.G - 1) / sc.G;
+      sc.smem = cat::conv_reg_smem(gh, sc.G);
+      sc.threads = gh * sc.G;
+      p->launches = 3;
+    }
   } else {
     st = choose_path(p);
   }
@@ -746,7 +761,7 @@ int create_plan(cat_plan_t* out, int B, int N, int D, int H, int dtype, void* st
             alloc((void**)&p->part, (size_t)B * H * cat::softmax_parts(N) * sizeof(float2)) &&
             alloc((void**)&p->tw, (size_t)N * sizeof(float2)) &&
             alloc((void**)&p->status, sizeof(unsigned int));
-  if (ok && (p->path == cat::PATH_SMEM || p->path == cat::PATH_FAST))
+  if (ok && (p->path == cat::PATH_SMEM || p->path == cat::PATH_FAST || p->reg2d))
     ok = alloc((void**)&p->zf, rowsN * sizeof(float2));
   if (ok && p->path == cat::PATH_FAST) ok = alloc((void**)&p->zscr, rowsN * sizeof(float2));
   if (ok && p->path == cat::PATH_FAST)
@@ -770,6 +785,7 @@ int create_plan(cat_plan_t* out, int B, int N, int D, int H, int dtype, void* st
         : p->path == cat::PATH_FOURSTEP ? cat::setup_fourstep_kernels(p)
         : p->path == cat::PATH_DIRECT   ? cat::setup_direct_kernels(p)
                                         : cat::setup_fast_kernels(p);
+  if (e == cudaSuccess && p->reg2d) e = cat::setup_conv_reg(p);
   if (e == cudaSuccess && p->path == cat::PATH_FAST) {
     for (int k = 0; k < 2 && e == cudaSuccess; ++k) {
       e = cudaStreamCreateWithFlags(&p->side[k], cudaStreamNonBlocking);
@@ -1201,7 +1217,7 @@ int cat2d_scores(cat_plan_t p, const void* Q, const void* K, float* a, int B, in
   const size_t nx = (size_t)B * p->N * D * (dtype == CAT_BF16 ? 2 : 4);
   const size_t na = (size_t)B * H * p->N * sizeof(float);
   if (ranges_overlap(a, na, Q, nx) || ranges_overlap(a, na, K, nx)) return CAT_ERR_ALIAS;
-  return map_cuda(cat::launch_scores2d(p, Q, K, a));
+  return map_cuda(p->reg2d ? cat::launch_scores2d_reg(p, Q, K, a) : cat::launch_scores2d(p, Q, K, a));
 }
 
 int cat2d_forward(cat_plan_t p, const void* Q, const void* K, const void* V, void* O, int B,
@@ -1217,6 +1233,13 @@ int cat2d_forward(cat_plan_t p, const void* Q, const void* K, const void* V, voi
   const size_t nx = (size_t)B * p->N * D * es;
   if (ranges_overlap(O, nx, Q, nx) || ranges_overlap(O, nx, K, nx) || ranges_overlap(O, nx, V, nx))
     return CAT_ERR_ALIAS;
+  if (p->reg2d) {
+    // Register kernels: scores, softmax with the 2-D spectrum, product.
+    cudaError_t e = cat::launch_scores2d_reg(p, Q, K, nullptr);
+    if (e == cudaSuccess) e = cat::launch_softmax_spectrum_reg(p);
+    if (e == cudaSuccess) e = cat::launch_conv_reg(p, V, O);
+    return map_cuda(e);
+  }
   cudaError_t e = cat::launch_scores2d(p, Q, K);
   if (e == cudaSuccess) e = cat::launch_softmax(p);
   if (e == cudaSuccess) e = cat::launch_fourstep_conv(p, V, O);

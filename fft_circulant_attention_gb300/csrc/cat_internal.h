@@ -132,6 +132,9 @@ struct cat_plan_s {
   // 2-D plan (cat_plan_create_2d): tokens on a grid_h x grid_w grid, the
   // generic four-step passes without twiddles (N1 = grid_w, N2 = grid_h)
   int twod, grid_h, grid_w;
+  // 2-D plan on a square grid of side 8, 14, 16 or 32: the register kernels
+  // without twiddles (scores, spectrum, product) instead of the generic passes
+  int reg2d;
   // backward workspace (configured and allocated at the first backward call)
   int bw_ready;
   cat::BwCfg bw;
@@ -198,6 +201,9 @@ cudaError_t launch_conv_smem(const cat_plan_s* p, const void* V, void* O);
 cudaError_t setup_conv_reg(const cat_plan_s* p);
 cudaError_t launch_conv_reg(const cat_plan_s* p, const void* V, void* O);
 cudaError_t launch_softmax_spectrum_reg(const cat_plan_s* p);
+// 2-D plan with reg2d: the scores a (channel-averaged 2-D correlation of Q
+// and K) into z2 as (a, 0), and into out if given.
+cudaError_t launch_scores2d_reg(const cat_plan_s* p, const void* Q, const void* K, float* out);
 int conv_reg_pairs(int M);
 size_t conv_reg_smem(int M, int P);
 cudaError_t launch_fourstep_conv(const cat_plan_s* p, const void* V, void* O);

@@ -44,7 +44,10 @@ __device__ __forceinline__ void st_col_pair(T* p, float2 v, bool pair, bool alig
   }
 }
 
-template <typename T, int M>
+// TW = false: no twiddle between the two steps, i.e. the 2-D DFT of an
+// M x M token grid (n1 = x, n2 = y): the 2-D circular convolution of the
+// second page's circulant attention.
+template <typename T, int M, bool TW = true>
 __global__ void __launch_bounds__(512)
 conv_reg_kernel(const T* __restrict__ V, T* __restrict__ O, const float2* __restrict__ zf,
                 const float2* __restrict__ W, int D, int H, int dh, int npair, int P,
@@ -58,7 +61,7 @@ conv_reg_kernel(const T* __restrict__ V, T* __restrict__ O, const float2* __rest
   const int b = bh / H, h = bh - b * H;
   const int p = threadIdx.x % P, i = threadIdx.x / P;
   for (int e = threadIdx.x; e < N; e += blockDim.x) {
-    tw[e] = __ldg(&W[(e / M) * (e % M)]);
+    if (TW) tw[e] = __ldg(&W[(e / M) * (e % M)]);
     zs[e] = __ldg(&zf[(size_t)bh * N + e]);
   }
 
@@ -79,7 +82,7 @@ conv_reg_kernel(const T* __restrict__ V, T* __restrict__ O, const float2* __rest
   dft<M, false>(a);
   __syncthreads();   // twiddles and spectrum ready
 #pragma unroll
-  for (int k2 = 0; k2 < M; ++k2) buf[(k2 * M + i) * P + p] = cmul(a[k2], tw[i * M + k2]);
+  for (int k2 = 0; k2 < M; ++k2) buf[(k2 * M + i) * P + p] = TW ? cmul(a[k2], tw[i * M + k2]) : a[k2];
   __syncthreads();
 
   // Step 2: k2 = i.  Each thread reads and rewrites only its own M slots.
@@ -90,7 +93,7 @@ conv_reg_kernel(const T* __restrict__ V, T* __restrict__ O, const float2* __rest
   for (int k1 = 0; k1 < M; ++k1) a[k1] = cmul(a[k1], zs[i + M * k1]);
   dft<M, true>(a);
 #pragma unroll
-  for (int n1 = 0; n1 < M; ++n1) buf[(i * M + n1) * P + p] = cmulc(a[n1], tw[n1 * M + i]);
+  for (int n1 = 0; n1 < M; ++n1) buf[(i * M + n1) * P + p] = TW ? cmulc(a[n1], tw[n1 * M + i]) : a[n1];
   __syncthreads();
 
   // Step 3: n1 = i.
@@ -104,6 +107,128 @@ conv_reg_kernel(const T* __restrict__ V, T* __restrict__ O, const float2* __rest
   }
 }
 
+// Scores of the 2-D circulant attention on an M x M grid (token n = x + M·y,
+// the second page's "Vision Transformers are Circulant Attention Learners"
+// design: a from Q and K by FFTs and an element-wise product), read as the
+// channel-averaged 2-D circular cross-correlation
+//     a[b, h, k] = (1/dh) Σ_{c in head h} Σ_i Q[b, i, c] · K[b, i ⊖ k, c]
+//                = (1/dh) Re IFFT2( Σ_pairs FFT2(q) · conj(FFT2(kk)) ),
+// with q = Q[:, c] + i·Q[:, c+1] and kk likewise for K (the imaginary parts
+// of the pair products transform to purely imaginary signals, so the real
+// part of the inverse is the two columns' sum).  One CTA per (b, h): thread
+// (i, p) transforms pair p of Q and of K in registers as the circulant
+// product's first two steps do (no twiddle: a 2-D DFT), the pair products
+// are summed over the head's pairs in a fixed order, and M threads run the
+// inverse of the sum.  Writes z2 = (a, 0) and, if out is given, a.
+template <typename T, int M>
+__global__ void __launch_bounds__(512)
+corr_reg_kernel(const T* __restrict__ Q, const T* __restrict__ K, float2* __restrict__ z2,
+                float* __restrict__ out, int D, int H, int dh, int npair, int P, float scale) {
+  constexpr int N = M * M;
+  extern __shared__ float4 smem4[];
+  float2* bq = reinterpret_cast<float2*>(smem4);   // [M][M][P] Q pairs, then products
+  float2* bk = bq + N * P;                          // [M][M][P] K pairs
+  float2* S = bk + N * P;                           // [k2][k1] running sum
+  const int bh = blockIdx.x, b = bh / H, h = bh - b * H;
+  const int p = threadIdx.x % P, i = threadIdx.x / P;
+  for (int e = threadIdx.x; e < N; e += blockDim.x) S[e] = make_float2(0.f, 0.f);
+  for (int g0 = 0; g0 < npair; g0 += P) {
+    const int g = g0 + p;
+    const bool active = g < npair;
+    const bool pair = 2 * g + 1 < dh;
+    const int col = h * dh + 2 * (active ? g : 0);
+    const bool aligned = (col & 1) == 0 && (D & 1) == 0;
+    const size_t base = (size_t)b * N * D + col;
+    // One signal's M values in registers at a time: Q's transforms go back
+    // to shared memory and K's product reads them there.
+    float2 a[M];
+#pragma unroll
+    for (int n2 = 0; n2 < M; ++n2)
+      a[n2] = active ? ld_col_pair(Q + base + (size_t)(i + M * n2) * D, pair, aligned)
+                     : make_float2(0.f, 0.f);
+    dft<M, false>(a);
+    __syncthreads();   // the previous pass's sums have read bq
+#pragma unroll
+    for (int k2 = 0; k2 < M; ++k2) bq[(k2 * M + i) * P + p] = a[k2];
+#pragma unroll
+    for (int n2 = 0; n2 < M; ++n2)
+      a[n2] = active ? ld_col_pair(K + base + (size_t)(i + M * n2) * D, pair, aligned)
+                     : make_float2(0.f, 0.f);
+    dft<M, false>(a);
+#pragma unroll
+    for (int k2 = 0; k2 < M; ++k2) bk[(k2 * M + i) * P + p] = a[k2];
+    __syncthreads();
+    // Step 2 (k2 = i): each thread reads and rewrites only its own slots.
+#pragma unroll
+    for (int n1 = 0; n1 < M; ++n1) a[n1] = bq[(i * M + n1) * P + p];
+    dft<M, false>(a);
+#pragma unroll
+    for (int k1 = 0; k1 < M; ++k1) bq[(i * M + k1) * P + p] = a[k1];
+#pragma unroll
+    for (int n1 = 0; n1 < M; ++n1) a[n1] = bk[(i * M + n1) * P + p];
+    dft<M, false>(a);
+#pragma unroll
+    for (int k1 = 0; k1 < M; ++k1)
+      bq[(i * M + k1) * P + p] = cmulc(bq[(i * M + k1) * P + p], a[k1]);
+    __syncthreads();
+    for (int e = threadIdx.x; e < N; e += blockDim.x) {
+      float2 s = S[e];
+      for (int q = 0; q < P; ++q) s = cadd(s, bq[e * P + q]);
+      S[e] = s;
+    }
+  }
+  __syncthreads();
+  // The inverse of the one summed signal, on threads t < M.
+  const int t = threadIdx.x;
+  float2 a[M];
+  if (t < M) {   // k2 = t: inverse over k1, to [n1][k2]
+#pragma unroll
+    for (int k1 = 0; k1 < M; ++k1) a[k1] = S[t * M + k1];
+    dft<M, true>(a);
+#pragma unroll
+    for (int n1 = 0; n1 < M; ++n1) bk[n1 * M + t] = a[n1];
+  }
+  __syncthreads();
+  if (t < M) {   // n1 = t: inverse over k2
+#pragma unroll
+    for (int k2 = 0; k2 < M; ++k2) a[k2] = bk[t * M + k2];
+    dft<M, true>(a);
+#pragma unroll
+    for (int n2 = 0; n2 < M; ++n2) {
+      const float v = a[n2].x * scale;
+      z2[(size_t)bh * N + t + M * n2] = make_float2(v, 0.f);
+      if (out) out[(size_t)bh * N + t + M * n2] = v;
+    }
+  }
+}
+
+size_t corr_reg_smem(int M, int P) { return ((size_t)2 * M * M * P + (size_t)M * M) * sizeof(float2); }
+
+template <typename T>
+static cudaError_t corr_t(const cat_plan_s* p, const T* Q, const T* K, float* out) {
+  const int M = p->sm.reg_m, P = p->sm.G;
+  const float scale = 1.0f / ((float)p->dh * (float)p->N);
+  const size_t smem = corr_reg_smem(M, P);
+  switch (M) {
+#define CAT_M(m)                                                                              \
+  case m:                                                                                     \
+    corr_reg_kernel<T, m><<<p->B * p->H, m * P, smem, p->stream>>>(Q, K, p->z2, out, p->D,     \
+                                                                   p->H, p->dh, p->npair, P, \
+                                                                   scale);                   \
+    break;
+    CAT_M(8) CAT_M(14) CAT_M(16) CAT_M(32)
+#undef CAT_M
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scores2d_reg(const cat_plan_s* p, const void* Q, const void* K, float* out) {
+  if (p->B * p->H == 0) return cudaSuccess;
+  if (p->dtype == 1) return corr_t(p, (const __nv_bfloat16*)Q, (const __nv_bfloat16*)K, out);
+  return corr_t(p, (const float*)Q, (const float*)K, out);
+}
+
 // Softmax and spectrum of z* for N = M² in registers: a group of GL lanes
 // (M rounded up to a power of two; lanes >= M idle) owns one (b, h) row, so
 // the row maximum and Σ exp(z - m) are lane-group shuffles.  Lane i holds
@@ -114,7 +239,7 @@ conv_reg_kernel(const T* __restrict__ V, T* __restrict__ O, const float2* __rest
 // from the double-float score (exp_shifted), as in the block kernel.
 constexpr int kSpecRegThreads = 256;
 
-template <int M>
+template <int M, bool TW = true>
 __global__ void __launch_bounds__(kSpecRegThreads)
 softmax_spectrum_reg(const float2* __restrict__ z, float* __restrict__ zs,
                      float2* __restrict__ zf, const float2* __restrict__ W, int rows) {
@@ -125,7 +250,8 @@ softmax_spectrum_reg(const float2* __restrict__ z, float* __restrict__ zs,
   extern __shared__ float4 smem4[];
   float2* tw = reinterpret_cast<float2*>(smem4);   // tw[n1·M + k2] = w_N^{n1·k2}
   float2* xb = tw + N;                              // ROWS blocks of M·RS
-  for (int e = threadIdx.x; e < N; e += blockDim.x) tw[e] = __ldg(&W[(e / M) * (e % M)]);
+  if (TW)
+    for (int e = threadIdx.x; e < N; e += blockDim.x) tw[e] = __ldg(&W[(e / M) * (e % M)]);
   const int i = threadIdx.x % GL, r = threadIdx.x / GL;
   const int row = blockIdx.x * ROWS + r;
   const bool act = i < M && row < rows;
@@ -160,7 +286,7 @@ softmax_spectrum_reg(const float2* __restrict__ z, float* __restrict__ zs,
   float2* xr = xb + r * M * RS;
   if (i < M) {
 #pragma unroll
-    for (int k2 = 0; k2 < M; ++k2) xr[k2 * RS + i] = cmul(a[k2], tw[i * M + k2]);
+    for (int k2 = 0; k2 < M; ++k2) xr[k2 * RS + i] = TW ? cmul(a[k2], tw[i * M + k2]) : a[k2];
   }
   __syncwarp();      // a row's lanes are one warp's
   if (i < M) {
@@ -181,7 +307,8 @@ size_t spectrum_reg_smem(int M) {
   return ((size_t)M * M + (size_t)(kSpecRegThreads / GL) * M * (M + 1)) * sizeof(float2);
 }
 
-cudaError_t launch_softmax_spectrum_reg(const cat_plan_s* p) {
+template <bool TW>
+static cudaError_t spectrum_reg_t(const cat_plan_s* p) {
   const int rows = p->B * p->H;
   if (rows == 0) return cudaSuccess;
   const int M = p->sm.reg_m;
@@ -192,14 +319,18 @@ cudaError_t launch_softmax_spectrum_reg(const cat_plan_s* p) {
   switch (M) {
 #define CAT_M(m)                                                                            \
   case m:                                                                                   \
-    softmax_spectrum_reg<m><<<ctas, kSpecRegThreads, smem, p->stream>>>(p->z2, p->zs, p->zf, \
-                                                                        p->tw, rows);       \
+    softmax_spectrum_reg<m, TW><<<ctas, kSpecRegThreads, smem, p->stream>>>(p->z2, p->zs,    \
+                                                                            p->zf, p->tw, rows); \
     break;
     CAT_M(8) CAT_M(14) CAT_M(16) CAT_M(32)
 #undef CAT_M
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
+}
+
+cudaError_t launch_softmax_spectrum_reg(const cat_plan_s* p) {
+  return p->twod ? spectrum_reg_t<false>(p) : spectrum_reg_t<true>(p);
 }
 
 // Pairs per CTA and the CTA shape for side M: 16 pairs (8 for M = 32, so
@@ -208,16 +339,27 @@ int conv_reg_pairs(int M) { return M == 32 ? 8 : 16; }
 
 size_t conv_reg_smem(int M, int P) { return (size_t)M * M * (P + 2) * sizeof(float2); }
 
+template <typename T, bool TW>
+static cudaError_t setup_tw() {
+  cudaError_t e = allow_max_smem(softmax_spectrum_reg<8, TW>);
+  if (e == cudaSuccess) e = allow_max_smem(softmax_spectrum_reg<14, TW>);
+  if (e == cudaSuccess) e = allow_max_smem(softmax_spectrum_reg<16, TW>);
+  if (e == cudaSuccess) e = allow_max_smem(softmax_spectrum_reg<32, TW>);
+  if (e == cudaSuccess) e = allow_max_smem(conv_reg_kernel<T, 8, TW>);
+  if (e == cudaSuccess) e = allow_max_smem(conv_reg_kernel<T, 14, TW>);
+  if (e == cudaSuccess) e = allow_max_smem(conv_reg_kernel<T, 16, TW>);
+  if (e == cudaSuccess) e = allow_max_smem(conv_reg_kernel<T, 32, TW>);
+  return e;
+}
+
 template <typename T>
 static cudaError_t setup_t() {
-  cudaError_t e = allow_max_smem(softmax_spectrum_reg<8>);
-  if (e == cudaSuccess) e = allow_max_smem(softmax_spectrum_reg<14>);
-  if (e == cudaSuccess) e = allow_max_smem(softmax_spectrum_reg<16>);
-  if (e == cudaSuccess) e = allow_max_smem(softmax_spectrum_reg<32>);
-  if (e == cudaSuccess) e = allow_max_smem(conv_reg_kernel<T, 8>);
-  if (e == cudaSuccess) e = allow_max_smem(conv_reg_kernel<T, 14>);
-  if (e == cudaSuccess) e = allow_max_smem(conv_reg_kernel<T, 16>);
-  if (e == cudaSuccess) e = allow_max_smem(conv_reg_kernel<T, 32>);
+  cudaError_t e = setup_tw<T, true>();
+  if (e == cudaSuccess) e = setup_tw<T, false>();
+  if (e == cudaSuccess) e = allow_max_smem(corr_reg_kernel<T, 8>);
+  if (e == cudaSuccess) e = allow_max_smem(corr_reg_kernel<T, 14>);
+  if (e == cudaSuccess) e = allow_max_smem(corr_reg_kernel<T, 16>);
+  if (e == cudaSuccess) e = allow_max_smem(corr_reg_kernel<T, 32>);
   return e;
 }
 
@@ -225,23 +367,28 @@ cudaError_t setup_conv_reg(const cat_plan_s* p) {
   return p->dtype == 1 ? setup_t<__nv_bfloat16>() : setup_t<float>();
 }
 
-template <typename T>
-static cudaError_t launch_t(const cat_plan_s* p, const T* V, T* O) {
+template <typename T, bool TW>
+static cudaError_t launch_tw(const cat_plan_s* p, const T* V, T* O) {
   const int M = p->sm.reg_m, P = p->sm.G, groups = p->sm.groups;
   const int ctas = p->B * p->H * groups;
   const dim3 block(M * P);
   const size_t smem = p->sm.smem;
   switch (M) {
-#define CAT_M(m)                                                                           \
-  case m:                                                                                  \
-    conv_reg_kernel<T, m><<<ctas, block, smem, p->stream>>>(V, O, p->zf, p->tw, p->D, p->H, \
-                                                            p->dh, p->npair, P, groups);   \
+#define CAT_M(m)                                                                               \
+  case m:                                                                                      \
+    conv_reg_kernel<T, m, TW><<<ctas, block, smem, p->stream>>>(V, O, p->zf, p->tw, p->D, p->H, \
+                                                                p->dh, p->npair, P, groups);   \
     break;
     CAT_M(8) CAT_M(14) CAT_M(16) CAT_M(32)
 #undef CAT_M
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
+}
+
+template <typename T>
+static cudaError_t launch_t(const cat_plan_s* p, const T* V, T* O) {
+  return p->twod ? launch_tw<T, false>(p, V, O) : launch_tw<T, true>(p, V, O);
 }
 
 cudaError_t launch_conv_reg(const cat_plan_s* p, const void* V, void* O) {

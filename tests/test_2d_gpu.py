@@ -74,6 +74,41 @@ def test_grid_shapes(B, h, w, D, H, dtype):
     print("B%d %dx%d D%d H%d %s: max|dO|/max|V| = %.2e [%s]" % (B, h, w, D, H, dtype, err, desc))
 
 
+# Square grids of side 8, 14, 16 or 32 take the register kernels (the 2-D
+# DFT as the register transform's two steps without the twiddle); both paths
+# are held to the oracle, and to each other.
+@pytest.mark.parametrize("B,side,D,H,dtype", [
+    (2, 8, 64, 1, "f32"),
+    (3, 14, 96, 2, "f32"),
+    (2, 14, 30, 2, "bf16"),        # head width 15: a half pair
+    (1, 16, 64, 4, "f32"),
+    (1, 32, 128, 2, "f32"),
+    (2, 32, 64, 2, "bf16"),
+    (4, 14, 384, 6, "f32"),        # ViT-S widths
+])
+@pytest.mark.parametrize("reg", ["1", "0"])
+def test_square_grids_register_and_generic(B, side, D, H, dtype, reg, monkeypatch):
+    monkeypatch.setenv("CAT_2D_REG", reg)
+    err, desc = check2d(B, side, side, D, H, dtype, seed=side + D)
+    assert ("reg2d=1" in desc) == (reg == "1"), desc
+    print("B%d %dx%d D%d H%d %s reg=%s: max|dO|/max|V| = %.2e" % (B, side, side, D, H, dtype,
+                                                                  reg, err))
+
+
+def test_register_and_generic_2d_agree(monkeypatch):
+    B, side, D, H = 2, 14, 384, 6
+    Q, K, V = to_dev(*synth.make_qkv(B, side * side, D, "f32", 4))
+    outs = []
+    for reg in ("1", "0"):
+        monkeypatch.setenv("CAT_2D_REG", reg)
+        with cat.Plan2D(B, side, side, D, H, "f32") as plan:
+            outs.append((plan.forward(Q, K, V), plan.scores(Q, K)))
+            plan.sync()
+    (O1, a1), (O0, a0) = outs
+    assert float((a1 - a0).abs().max()) <= 2e-5 * float(a0.abs().max())
+    assert float((O1 - O0).abs().max()) <= 4e-5 * float(V.abs().max())
+
+
 @pytest.mark.parametrize("name", list(synth.GRID_CONFIGS))
 def test_grid_workloads(name):
     c = synth.GRID_CONFIGS[name]
