@@ -34,6 +34,9 @@
 //   pass C (per n1): inverse DFT over k2; real part / N is dz*.
 #include <cuda_bf16.h>
 
+#include <cstdlib>
+#include <cstring>
+
 #include "cat_internal.h"
 #include "elem.cuh"
 
@@ -554,7 +557,13 @@ static cudaError_t corr_fast(const cat_plan_s* p, const void* G, const void* V) 
 cudaError_t launch_backward_dz(const cat_plan_s* p, const void* G, const void* V) {
   const int rows = p->B * p->H;
   if (rows == 0) return cudaSuccess;
+  // Square lengths with a register transform (N = 8², 14², 16², 32²) take
+  // the register correlation kernel; CAT_BW_REG=0 keeps the block passes.
+  const char* env = std::getenv("CAT_BW_REG");
+  const bool reg = !p->bw.fast && !p->twod && p->path == PATH_SMEM && p->sm.reg_m > 0 &&
+                   !(env && std::strcmp(env, "0") == 0);
   const cudaError_t e = p->bw.fast ? corr_fast(p, G, V)
+      : reg           ? launch_corr_reg(p, G, V, p->bw_dzs)
       : p->dtype == 1 ? corr_t<__nv_bfloat16, true>(p, (const __nv_bfloat16*)G, (const __nv_bfloat16*)V)
                       : corr_t<float, true>(p, (const float*)G, (const float*)V);
   if (e != cudaSuccess) return e;

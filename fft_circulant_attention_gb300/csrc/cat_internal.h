@@ -204,6 +204,9 @@ cudaError_t launch_softmax_spectrum_reg(const cat_plan_s* p);
 // 2-D plan with reg2d: the scores a (channel-averaged 2-D correlation of Q
 // and K) into z2 as (a, 0), and into out if given.
 cudaError_t launch_scores2d_reg(const cat_plan_s* p, const void* Q, const void* K, float* out);
+// Backward correlation dz*[b, h, k] = Σ_c Σ_i G[i, c] V[(i - k) mod N, c] into
+// dzs by the register transform, for N = reg_m² on the shared-memory path.
+cudaError_t launch_corr_reg(const cat_plan_s* p, const void* G, const void* V, float* dzs);
 int conv_reg_pairs(int M);
 size_t conv_reg_smem(int M, int P);
 cudaError_t launch_fourstep_conv(const cat_plan_s* p, const void* V, void* O);

@@ -107,31 +107,42 @@ conv_reg_kernel(const T* __restrict__ V, T* __restrict__ O, const float2* __rest
   }
 }
 
-// Scores of the 2-D circulant attention on an M x M grid (token n = x + M·y,
-// the second page's "Vision Transformers are Circulant Attention Learners"
-// design: a from Q and K by FFTs and an element-wise product), read as the
-// channel-averaged 2-D circular cross-correlation
-//     a[b, h, k] = (1/dh) Σ_{c in head h} Σ_i Q[b, i, c] · K[b, i ⊖ k, c]
-//                = (1/dh) Re IFFT2( Σ_pairs FFT2(q) · conj(FFT2(kk)) ),
-// with q = Q[:, c] + i·Q[:, c+1] and kk likewise for K (the imaginary parts
-// of the pair products transform to purely imaginary signals, so the real
-// part of the inverse is the two columns' sum).  One CTA per (b, h): thread
-// (i, p) transforms pair p of Q and of K in registers as the circulant
-// product's first two steps do (no twiddle: a 2-D DFT), the pair products
-// are summed over the head's pairs in a fixed order, and M threads run the
-// inverse of the sum.  Writes z2 = (a, 0) and, if out is given, a.
-template <typename T, int M>
+// Correlation of pair-packed column signals summed over a head, by the
+// register transform of N = M·M (n = n1 + M·n2, k = k2 + M·k1), for two
+// uses:
+//  - TW = false, the 2-D scores of the second page's circulant attention
+//    ("Vision Transformers are Circulant Attention Learners": a from Q and K
+//    by FFTs and an element-wise product) on an M x M grid (n1 = x, n2 = y),
+//    read as the channel-averaged 2-D circular cross-correlation
+//        a[b, h, k] = (1/dh) Σ_{c in head h} Σ_i Q[b, i, c] · K[b, i ⊖ k, c];
+//  - TW = true, the backward pass's dz*[b, h, k] = Σ_{c in h} Σ_i dO[b, i, c]
+//    · V[b, (i - k) mod N, c] (the derivative of the CAT output with respect
+//    to z*), a 1-D correlation of length N.
+// Both are Re IFFT( Σ_pairs FFT(q) · conj(FFT(kk)) ) times `scale`, with
+// q = A[:, c] + i·A[:, c+1] and kk likewise from B (the imaginary parts of
+// the pair products transform to purely imaginary signals, so the real part
+// of the inverse is the two columns' sum).  One CTA per (b, h): thread
+// (i, p) transforms pair p of A and of B as the circulant product's first
+// two steps do, the products are summed over the head's pairs in a fixed
+// order, and M threads run the inverse of the sum.  Writes out (fp32) and,
+// if z2 is given, (value, 0) into it.
+template <typename T, int M, bool TW>
 __global__ void __launch_bounds__(512)
 corr_reg_kernel(const T* __restrict__ Q, const T* __restrict__ K, float2* __restrict__ z2,
-                float* __restrict__ out, int D, int H, int dh, int npair, int P, float scale) {
+                float* __restrict__ out, const float2* __restrict__ W, int D, int H, int dh,
+                int npair, int P, float scale) {
   constexpr int N = M * M;
   extern __shared__ float4 smem4[];
   float2* bq = reinterpret_cast<float2*>(smem4);   // [M][M][P] Q pairs, then products
   float2* bk = bq + N * P;                          // [M][M][P] K pairs
   float2* S = bk + N * P;                           // [k2][k1] running sum
+  float2* tw = S + N;                               // TW: tw[n1·M + k2] = w_N^{n1·k2}
   const int bh = blockIdx.x, b = bh / H, h = bh - b * H;
   const int p = threadIdx.x % P, i = threadIdx.x / P;
-  for (int e = threadIdx.x; e < N; e += blockDim.x) S[e] = make_float2(0.f, 0.f);
+  for (int e = threadIdx.x; e < N; e += blockDim.x) {
+    S[e] = make_float2(0.f, 0.f);
+    if (TW) tw[e] = __ldg(&W[(e / M) * (e % M)]);
+  }
   for (int g0 = 0; g0 < npair; g0 += P) {
     const int g = g0 + p;
     const bool active = g < npair;
@@ -147,16 +158,16 @@ corr_reg_kernel(const T* __restrict__ Q, const T* __restrict__ K, float2* __rest
       a[n2] = active ? ld_col_pair(Q + base + (size_t)(i + M * n2) * D, pair, aligned)
                      : make_float2(0.f, 0.f);
     dft<M, false>(a);
-    __syncthreads();   // the previous pass's sums have read bq
+    __syncthreads();   // the previous pass's sums have read bq; twiddles ready
 #pragma unroll
-    for (int k2 = 0; k2 < M; ++k2) bq[(k2 * M + i) * P + p] = a[k2];
+    for (int k2 = 0; k2 < M; ++k2) bq[(k2 * M + i) * P + p] = TW ? cmul(a[k2], tw[i * M + k2]) : a[k2];
 #pragma unroll
     for (int n2 = 0; n2 < M; ++n2)
       a[n2] = active ? ld_col_pair(K + base + (size_t)(i + M * n2) * D, pair, aligned)
                      : make_float2(0.f, 0.f);
     dft<M, false>(a);
 #pragma unroll
-    for (int k2 = 0; k2 < M; ++k2) bk[(k2 * M + i) * P + p] = a[k2];
+    for (int k2 = 0; k2 < M; ++k2) bk[(k2 * M + i) * P + p] = TW ? cmul(a[k2], tw[i * M + k2]) : a[k2];
     __syncthreads();
     // Step 2 (k2 = i): each thread reads and rewrites only its own slots.
 #pragma unroll
@@ -186,7 +197,7 @@ corr_reg_kernel(const T* __restrict__ Q, const T* __restrict__ K, float2* __rest
     for (int k1 = 0; k1 < M; ++k1) a[k1] = S[t * M + k1];
     dft<M, true>(a);
 #pragma unroll
-    for (int n1 = 0; n1 < M; ++n1) bk[n1 * M + t] = a[n1];
+    for (int n1 = 0; n1 < M; ++n1) bk[n1 * M + t] = TW ? cmulc(a[n1], tw[n1 * M + t]) : a[n1];
   }
   __syncthreads();
   if (t < M) {   // n1 = t: inverse over k2
@@ -196,25 +207,26 @@ corr_reg_kernel(const T* __restrict__ Q, const T* __restrict__ K, float2* __rest
 #pragma unroll
     for (int n2 = 0; n2 < M; ++n2) {
       const float v = a[n2].x * scale;
-      z2[(size_t)bh * N + t + M * n2] = make_float2(v, 0.f);
+      if (z2) z2[(size_t)bh * N + t + M * n2] = make_float2(v, 0.f);
       if (out) out[(size_t)bh * N + t + M * n2] = v;
     }
   }
 }
 
-size_t corr_reg_smem(int M, int P) { return ((size_t)2 * M * M * P + (size_t)M * M) * sizeof(float2); }
+size_t corr_reg_smem(int M, int P) {
+  return ((size_t)2 * M * M * P + 2 * (size_t)M * M) * sizeof(float2);
+}
 
-template <typename T>
-static cudaError_t corr_t(const cat_plan_s* p, const T* Q, const T* K, float* out) {
+template <typename T, bool TW>
+static cudaError_t corr_t(const cat_plan_s* p, const T* A, const T* Bm, float2* z2, float* out,
+                          float scale) {
   const int M = p->sm.reg_m, P = p->sm.G;
-  const float scale = 1.0f / ((float)p->dh * (float)p->N);
   const size_t smem = corr_reg_smem(M, P);
   switch (M) {
 #define CAT_M(m)                                                                              \
   case m:                                                                                     \
-    corr_reg_kernel<T, m><<<p->B * p->H, m * P, smem, p->stream>>>(Q, K, p->z2, out, p->D,     \
-                                                                   p->H, p->dh, p->npair, P, \
-                                                                   scale);                   \
+    corr_reg_kernel<T, m, TW><<<p->B * p->H, m * P, smem, p->stream>>>(                        \
+        A, Bm, z2, out, p->tw, p->D, p->H, p->dh, p->npair, P, scale);                        \
     break;
     CAT_M(8) CAT_M(14) CAT_M(16) CAT_M(32)
 #undef CAT_M
@@ -225,8 +237,20 @@ static cudaError_t corr_t(const cat_plan_s* p, const T* Q, const T* K, float* ou
 
 cudaError_t launch_scores2d_reg(const cat_plan_s* p, const void* Q, const void* K, float* out) {
   if (p->B * p->H == 0) return cudaSuccess;
-  if (p->dtype == 1) return corr_t(p, (const __nv_bfloat16*)Q, (const __nv_bfloat16*)K, out);
-  return corr_t(p, (const float*)Q, (const float*)K, out);
+  const float scale = 1.0f / ((float)p->dh * (float)p->N);
+  if (p->dtype == 1)
+    return corr_t<__nv_bfloat16, false>(p, (const __nv_bfloat16*)Q, (const __nv_bfloat16*)K,
+                                        p->z2, out, scale);
+  return corr_t<float, false>(p, (const float*)Q, (const float*)K, p->z2, out, scale);
+}
+
+cudaError_t launch_corr_reg(const cat_plan_s* p, const void* G, const void* V, float* dzs) {
+  if (p->B * p->H == 0) return cudaSuccess;
+  const float scale = 1.0f / (float)p->N;
+  if (p->dtype == 1)
+    return corr_t<__nv_bfloat16, true>(p, (const __nv_bfloat16*)G, (const __nv_bfloat16*)V,
+                                       nullptr, dzs, scale);
+  return corr_t<float, true>(p, (const float*)G, (const float*)V, nullptr, dzs, scale);
 }
 
 // Softmax and spectrum of z* for N = M² in registers: a group of GL lanes
@@ -356,10 +380,14 @@ template <typename T>
 static cudaError_t setup_t() {
   cudaError_t e = setup_tw<T, true>();
   if (e == cudaSuccess) e = setup_tw<T, false>();
-  if (e == cudaSuccess) e = allow_max_smem(corr_reg_kernel<T, 8>);
-  if (e == cudaSuccess) e = allow_max_smem(corr_reg_kernel<T, 14>);
-  if (e == cudaSuccess) e = allow_max_smem(corr_reg_kernel<T, 16>);
-  if (e == cudaSuccess) e = allow_max_smem(corr_reg_kernel<T, 32>);
+  if (e == cudaSuccess) e = allow_max_smem(corr_reg_kernel<T, 8, false>);
+  if (e == cudaSuccess) e = allow_max_smem(corr_reg_kernel<T, 14, false>);
+  if (e == cudaSuccess) e = allow_max_smem(corr_reg_kernel<T, 16, false>);
+  if (e == cudaSuccess) e = allow_max_smem(corr_reg_kernel<T, 32, false>);
+  if (e == cudaSuccess) e = allow_max_smem(corr_reg_kernel<T, 8, true>);
+  if (e == cudaSuccess) e = allow_max_smem(corr_reg_kernel<T, 14, true>);
+  if (e == cudaSuccess) e = allow_max_smem(corr_reg_kernel<T, 16, true>);
+  if (e == cudaSuccess) e = allow_max_smem(corr_reg_kernel<T, 32, true>);
   return e;
 }
 
