@@ -15,7 +15,8 @@ The line also carries the backward pass (cat_backward: dX, dW_A, dV for an
 upstream gradient) at the long-sequence and the short workloads, with its
 roofline fraction; --backward-only times just that on --config.  It also
 carries the 2-D (BCCB) circulant attention of a second page on its token-grid
-workloads (--no-grid2d leaves them out).
+workloads (--no-grid2d leaves them out) and the fused value-and-score
+projection (cat_forward_fused, --no-fused leaves it out).
 
 Prints ONE JSON line (rank 0).  With --impl reference the fp64 CPU oracle
 is timed instead, on a bounded sample of the same workload.
@@ -549,6 +550,51 @@ def measure_grid2d(name, device, reps=20, warmup=3):
             "plan": desc, "reps": reps}
 
 
+def measure_fused(name, device, reps=20, warmup=3):
+    """ms per cat_forward_fused (V = X·W_V and the scores from one pass over
+    X on the tensor cores, then the forward), with the projection alone
+    (cat_project) and, as context, a library GEMM for V (torch.matmul, i.e.
+    cuBLAS) followed by cat_forward.  Resident bf16 inputs, CUDA events."""
+    import fft_circulant_attention_gb300 as cat
+    c = cfg_of(name)
+    B, N, D, H = c["B"], c["N"], c["D"], c["H"]
+    X, WA, _ = synth.make_inputs(B, N, D, H, "bf16", seed=0)
+    WV = synth.make_wv(D, "bf16", seed=0)
+    Xd, WAd, WVd = X.to(device), WA.to(device), WV.to(device)
+    V = torch.empty_like(Xd)
+    O = torch.empty_like(Xd)
+    zs = torch.empty((B, H, N), dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def timed(fn):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize(device)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        return e0.elapsed_time(e1) / reps
+
+    with cat.Plan(B, N, D, H, "bf16", stream=stream) as plan:
+        t_fused = timed(lambda: plan.forward_fused(Xd, WVd, WAd, V, O))
+        t_proj = timed(lambda: cat.cat_project(plan.handle, Xd, WVd, WAd, V, zs, B, N, D, H,
+                                               "bf16"))
+        t_lib = timed(lambda: (torch.matmul(Xd, WVd, out=V), plan.forward(Xd, WAd, V, O)))
+        plan.sync()
+    gemm_flops = 2.0 * B * N * D * (D + H)
+    del Xd, V, O
+    torch.cuda.empty_cache()
+    return {"workload": name, "B": B, "N": N, "D": D, "H": H, "storage": "bf16",
+            "ms_fused_forward": t_fused, "ms_projection": t_proj,
+            "projection_tflops": gemm_flops / (t_proj * 1e-3) / 1e12,
+            "ms_library_gemm_then_forward": t_lib,
+            "value": B * N * H / (t_fused * 1e-3), "unit": UNIT, "reps": reps}
+
+
 # The short-sequence configurations of the workload table (parity cases of
 # the tests; timed here so that every path has a measured figure).
 SHORT = ["tiny", "vit196", "gpt2_f32", "gpt2_bf16"]
@@ -624,6 +670,42 @@ def profile_range(args, device):
                       "plan": desc}), flush=True)
 
 
+def dft_probe(args, device):
+    """One length-32 DFT stage on the FP32 pipe against the same stage as a
+    dense contraction on the tensor cores (cat_probe_dft32): time per stage
+    per signal with CUDA events, and the error of one stage against an fp64
+    DFT (numpy), for 2 and 3 bf16 terms.
+        python bench.py --dft-probe"""
+    import fft_circulant_attention_gb300 as cat
+    nsig, rounds = 152 * 128 * 8, 64
+    rng = np.random.default_rng(0)
+    xh = rng.standard_normal((nsig, 32, 2)).astype(np.float32)
+    x = torch.from_numpy(xh).to(device)
+    y = torch.empty_like(x)
+    stream = torch.cuda.current_stream(device)
+    ref = np.fft.fft(xh[..., 0].astype(np.float64) + 1j * xh[..., 1], axis=1) / np.sqrt(32)
+    out = {"signals": nsig, "rounds": rounds}
+    for mode, name in ((0, "fp32_pipe"), (1, "tensor_2terms"), (2, "tensor_3terms")):
+        cat.cat_probe_dft32(x, y, nsig, mode, 1, stream)
+        torch.cuda.synchronize(device)
+        g = y.cpu().double().numpy()
+        err = np.abs(g[..., 0] + 1j * g[..., 1] - ref).max() / np.abs(ref).max()
+        for _ in range(3):
+            cat.cat_probe_dft32(x, y, nsig, mode, rounds, stream)
+        torch.cuda.synchronize(device)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        cat.cat_probe_dft32(x, y, nsig, mode, rounds, stream)
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        ms = e0.elapsed_time(e1)
+        out[name] = {"ms": ms, "ns_per_stage_per_signal": ms * 1e6 / (nsig * rounds),
+                     "stages_per_s": nsig * rounds / (ms * 1e-3),
+                     "max_rel_error_one_stage": float(err)}
+    print(json.dumps({"dft32_stage_probe": out}), flush=True)
+
+
 def run_gb300(args, world, rank, local):
     import fft_circulant_attention_gb300 as cat
     from fft_circulant_attention_gb300 import build
@@ -634,6 +716,9 @@ def run_gb300(args, world, rank, local):
     set_fp32_peak(device)
     if args.profile_range:
         profile_range(args, device)
+        return
+    if args.dft_probe:
+        dft_probe(args, device)
         return
     if args.backward_only:
         bw = measure_backward(args.config, device, max(args.steps, 1), args.warmup)
@@ -655,6 +740,13 @@ def run_gb300(args, world, rank, local):
                 grid2d.append(measure_grid2d(n, device))
             except Exception as exc:
                 grid2d.append({"workload": n, "error": "%s: %s" % (type(exc).__name__, exc)})
+    fused = []
+    if not args.no_fused:
+        for n in (PRIMARY, "gpt2_bf16"):
+            try:
+                fused.append(measure_fused(n, device))
+            except Exception as exc:
+                fused.append({"workload": n, "error": "%s: %s" % (type(exc).__name__, exc)})
     backward = []
     if not args.no_backward:
         # The backward pass at the two long workloads and the short ones; a
@@ -707,6 +799,8 @@ def run_gb300(args, world, rank, local):
         line["backward"] = backward
     if grid2d:
         line["grid2d"] = grid2d
+    if fused:
+        line["fused_projection"] = fused
     print(json.dumps(line), flush=True)
 
 
@@ -724,6 +818,10 @@ def main():
     ap.add_argument("--no-short", action="store_true")
     ap.add_argument("--no-backward", action="store_true")
     ap.add_argument("--no-grid2d", action="store_true")
+    ap.add_argument("--no-fused", action="store_true")
+    ap.add_argument("--dft-probe", action="store_true",
+                    help="time one DFT-32 stage on the FP32 pipe and on the tensor cores, "
+                         "print it and exit")
     ap.add_argument("--backward-only", action="store_true",
                     help="time only cat_backward on --config (--steps calls) and print it")
     ap.add_argument("--sample-heads", type=int, default=0)

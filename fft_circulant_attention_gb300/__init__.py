@@ -66,6 +66,7 @@ SIGNATURES = {
                             _I]),
     "cat2d_forward": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I]),
     "cat2d_scores": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I]),
+    "cat_probe_dft32": (_I, [_P, _P, _I, _I, _I, _P]),
     "cat_status_string": (ctypes.c_char_p, [_I]),
 }
 
@@ -134,6 +135,13 @@ def dtype_code(dtype):
     if name in ("bfloat16", "bf16"):
         return CAT_BF16
     raise ValueError("unsupported dtype %r" % (dtype,))
+
+
+def cat_probe_dft32(x, y, nsig, mode, rounds, stream=None):
+    """Measurement probe: one DFT-32 stage `rounds` times on `nsig` signals
+    (mode 0 FP32 pipe, 1 / 2 tensor cores with 2 / 3 bf16 terms)."""
+    _check(lib().cat_probe_dft32(_ptr(x), _ptr(y), nsig, mode, rounds, _stream(stream)),
+           "cat_probe_dft32")
 
 
 def cat_status_string(status):

@@ -346,6 +346,22 @@ int cat_plan_pass_times(cat_plan_t plan, float *ms, int cap, int *launches);
 int cat_forward_noalloc(const void *X, const void *W_A, const void *V, void *O, int B,
                         int N, int D, int H, int dtype, void *stream);
 
+/*
+ * cat_probe_dft32 — measurement only, not part of the forward or backward:
+ * applies one length-32 DFT stage `rounds` times (each scaled by
+ * 1/sqrt(32)) to `nsig` complex fp32 signals (device pointers x, y,
+ * [nsig][32] interleaved re/im), keeping each signal on chip, so that the
+ * time is the stage's own cost.  mode 0: the register DFT-32 on the FP32
+ * pipe (one signal per thread); mode 1 / 2: the stage as a dense 64 x 64 real
+ * contraction on the tensor cores (tcgen05, 128 signals per CTA) with the
+ * operands split into 2 / 3 bf16 terms (about 16 / 24 significant bits).
+ * For the choice of where the small-DFT stages of the circulant product
+ * run (the notes page's "FFT acceleration" design fixes the transform, not
+ * the unit).  Asynchronous on `stream`.  Errors: CAT_ERR_INVALID_ARG,
+ * CAT_ERR_ALLOC, CAT_ERR_CUDA.
+ */
+int cat_probe_dft32(const void *x, void *y, int nsig, int mode, int rounds, void *stream);
+
 /* Static string for a status code ("CAT_OK", "CAT_ERR_INVALID_ARG", ...). */
 const char *cat_status_string(int status);
 
