@@ -535,9 +535,39 @@ static cudaError_t corr_t(const cat_plan_s* p, const T* G, const T* V) {
 // Fast path: its own pass A on dO and on V, fsf_corr_b into the one-signal
 // buffer bw_scr ([bhl][k2][n1]), then pass C (in registers for N2 = 32, else
 // pass C above with Q = 1).
+// With the forward's chunks of 8 rows (N2 = 32) the correlation runs chunks
+// of 4 rows alternately on the plan's two internal streams: chunk c uses the
+// half c mod 2 of both scratch slots (dO's and V's spectra) and of the
+// one-signal buffer y, so two chunks are in flight in the same 64 MB.
+static cudaError_t corr_fast_overlapped(const cat_plan_s* p, const void* G, const void* V) {
+  const int rows = p->B * p->H;
+  const int cb = p->fs.chunk_bh / 2;
+  const size_t half = p->scratch_bytes / 4 / sizeof(float2);   // a half slot
+  const size_t yhalf = (size_t)cb * p->N;
+  cudaError_t e = cudaEventRecord(p->ev_fork, p->stream);
+  for (int k = 0; k < 2 && e == cudaSuccess; ++k) e = cudaStreamWaitEvent(p->side[k], p->ev_fork, 0);
+  for (int bh0 = 0, c = 0; bh0 < rows && e == cudaSuccess; bh0 += cb, ++c) {
+    const int nb = rows - bh0 < cb ? rows - bh0 : cb;
+    const int k = c & 1;
+    float2* s0 = p->scratch + (size_t)k * half;
+    float2* s1 = p->scratch + 2 * half + (size_t)k * half;
+    float2* y = p->bw_scr + (size_t)k * yhalf;
+    e = launch_fast_corr(p, G, V, y, bh0, nb, p->side[k], s0, s1);
+    if (e == cudaSuccess) e = launch_fast_corr_c32(p, y, p->bw_dzs, bh0, nb, p->side[k]);
+  }
+  for (int k = 0; k < 2; ++k) {
+    cudaError_t e2 = cudaEventRecord(p->ev_join[k], p->side[k]);
+    if (e2 == cudaSuccess) e2 = cudaStreamWaitEvent(p->stream, p->ev_join[k], 0);
+    if (e == cudaSuccess) e = e2;
+  }
+  return e;
+}
+
 static cudaError_t corr_fast(const cat_plan_s* p, const void* G, const void* V) {
   const BwCfg& w = p->bw;
   const int rows = p->B * p->H;
+  if (w.N2 == 32 && p->fs.chunk_bh >= 2 && p->fs.chunk_bh % 2 == 0)
+    return corr_fast_overlapped(p, G, V);
   for (int bh0 = 0; bh0 < rows; bh0 += w.chunk_bh) {
     const int nb = rows - bh0 < w.chunk_bh ? rows - bh0 : w.chunk_bh;
     cudaError_t e = launch_fast_corr(p, G, V, p->bw_scr, bh0, nb, p->stream);

@@ -8,6 +8,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <functional>
 #include <vector>
 
 #include "../../include/cat.h"
@@ -604,8 +605,12 @@ namespace {
 // before the spectrum, each waits for it just before its first pass B, so
 // the first passes A run beside the score and the spectrum.  Both join back
 // into the plan's stream at the end.
+// `between`, if given, enqueues further work on the plan's stream after the
+// spectrum and the chunks are enqueued and before the join, so that it runs
+// beside the chunks (the backward's dense gradients beside its dV).
 cudaError_t run_fast_overlapped(cat_plan_s* p, const void* X, const void* WA, const void* V,
-                                void* O, bool score = true) {
+                                void* O, bool score = true,
+                                const std::function<cudaError_t()>* between = nullptr) {
   cudaError_t e = cudaSuccess;
   auto fork = [&]() {
     if (e == cudaSuccess) e = cudaEventRecord(p->ev_fork, p->stream);
@@ -628,6 +633,7 @@ cudaError_t run_fast_overlapped(cat_plan_s* p, const void* X, const void* WA, co
                                  waited[k] ? nullptr : p->ev_front[0]);
       waited[k] = true;
     }
+  if (e == cudaSuccess && between) e = (*between)();
   for (int k = 0; k < 2; ++k) {
     cudaError_t e2 = cudaEventRecord(p->ev_join[k], p->side[k]);
     if (e2 == cudaSuccess) e2 = cudaStreamWaitEvent(p->stream, p->ev_join[k], 0);
@@ -1151,6 +1157,17 @@ int cat_backward(cat_plan_t p, const void* X, const void* WA, const void* V, con
   if (st != CAT_OK) return st;
   st = run_backward_front(p, X, WA, V, dO);
   if (st != CAT_OK) return st;
+  if (p->path == cat::PATH_FAST) {
+    // dV = circ(z*)^T dO by the forward's overlapped schedule on the scores
+    // reversed; dW_A and dX (which need only dz) run on the plan's stream
+    // beside its chunks.
+    cudaError_t e = cat::launch_reverse_scores(p);
+    const std::function<cudaError_t()> dense = [&]() {
+      return cat::launch_backward_dense(p, X, WA, dX, dWA);
+    };
+    if (e == cudaSuccess) e = run_fast_overlapped(p, nullptr, nullptr, dO, dV, false, &dense);
+    return map_cuda(e);
+  }
   cudaError_t e = cat::launch_backward_dense(p, X, WA, dX, dWA);
   // dV = circ(z*)^T dO: reverse the scores, then the forward's own spectrum
   // and circulant product on dO.

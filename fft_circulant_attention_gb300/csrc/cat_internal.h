@@ -269,10 +269,11 @@ int backward_wsplit(long long tokens, int D, int H, int sms);
 cudaError_t launch_scores2d(const cat_plan_s* p, const void* Q, const void* K,
                             float* out = nullptr);
 // Fast path (head width 64, N = 512·N2): the correlation's pass A on dO
-// (scratch slot 0) and on V (slot 1), then its pass B into y[bhl][k2][n1]
-// for rows [bh0, bh0 + nb), on stream st.
+// (into s0, default scratch slot 0) and on V (s1, default slot 1), then its
+// pass B into y[bhl][k2][n1] for rows [bh0, bh0 + nb), on stream st.
 cudaError_t launch_fast_corr(const cat_plan_s* p, const void* G, const void* V, float2* y,
-                             int bh0, int nb, cudaStream_t st);
+                             int bh0, int nb, cudaStream_t st, float2* s0 = nullptr,
+                             float2* s1 = nullptr);
 // Its pass C for N2 = 32: dz* rows [bh0, bh0 + nb) from y.
 cudaError_t launch_fast_corr_c32(const cat_plan_s* p, const float2* y, float* dzs, int bh0,
                                  int nb, cudaStream_t st);

@@ -1028,9 +1028,8 @@ cudaError_t launch_fast_conv(const cat_plan_s* p, const void* V, void* O, cudaEv
 // Pass A alone (the backward correlation transforms dO and V with it): rows
 // [bh0, bh0 + nb) of V into scratch slot `slot`, on stream st.
 template <typename T>
-static cudaError_t pass_a_t(const cat_plan_s* p, const T* V, int bh0, int nb, int slot,
+static cudaError_t pass_a_t(const cat_plan_s* p, const T* V, int bh0, int nb, float2* scr,
                             cudaStream_t st) {
-  float2* scr = p->scratch + (size_t)slot * (p->scratch_bytes / 2 / sizeof(float2));
   switch (p->fs.N2) {
     case 32: {
       CUtensorMap tmV;
@@ -1050,16 +1049,16 @@ static cudaError_t pass_a_t(const cat_plan_s* p, const T* V, int bh0, int nb, in
 }
 
 cudaError_t launch_fast_corr(const cat_plan_s* p, const void* G, const void* V, float2* y,
-                             int bh0, int nb, cudaStream_t st) {
+                             int bh0, int nb, cudaStream_t st, float2* s0, float2* s1) {
+  if (!s0) s0 = p->scratch;
+  if (!s1) s1 = p->scratch + p->scratch_bytes / 2 / sizeof(float2);
   cudaError_t e = p->dtype == 1
-      ? pass_a_t(p, (const __nv_bfloat16*)G, bh0, nb, 0, st)
-      : pass_a_t(p, (const float*)G, bh0, nb, 0, st);
+      ? pass_a_t(p, (const __nv_bfloat16*)G, bh0, nb, s0, st)
+      : pass_a_t(p, (const float*)G, bh0, nb, s0, st);
   if (e == cudaSuccess)
-    e = p->dtype == 1 ? pass_a_t(p, (const __nv_bfloat16*)V, bh0, nb, 1, st)
-                      : pass_a_t(p, (const float*)V, bh0, nb, 1, st);
+    e = p->dtype == 1 ? pass_a_t(p, (const __nv_bfloat16*)V, bh0, nb, s1, st)
+                      : pass_a_t(p, (const float*)V, bh0, nb, s1, st);
   if (e != cudaSuccess) return e;
-  const float2* s0 = p->scratch;
-  const float2* s1 = p->scratch + p->scratch_bytes / 2 / sizeof(float2);
   fsf_corr_b<<<nb * p->fs.N2, 256, kSmemCorrB, st>>>(s0, s1, y, p->tabs, p->fs.N2);
   return cudaGetLastError();
 }
