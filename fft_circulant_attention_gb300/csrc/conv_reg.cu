@@ -34,6 +34,32 @@ __device__ __forceinline__ float2 ld_col_pair(const T* p, bool pair, bool aligne
   return make_float2(ld_elem(p), pair ? ld_elem(p + 1) : 0.f);
 }
 
+// The M rows r0 + step·n2 (n2 < M) of a column pair.  On the common path
+// (whole pair, aligned) every load is issued before any value is widened,
+// so all M are in flight at once.
+template <typename T, int M>
+__device__ __forceinline__ void ld_rows(float2* a, const T* base, size_t step, size_t r0,
+                                        bool active, bool pair, bool aligned) {
+  if (active && pair && aligned) {
+    if constexpr (sizeof(T) == 2) {
+      unsigned int raw[M];
+#pragma unroll
+      for (int n2 = 0; n2 < M; ++n2)
+        raw[n2] = __ldg(reinterpret_cast<const unsigned int*>(base + r0 + step * n2));
+#pragma unroll
+      for (int n2 = 0; n2 < M; ++n2)
+        a[n2] = make_float2(__uint_as_float(raw[n2] << 16), __uint_as_float(raw[n2] & 0xffff0000u));
+    } else {
+#pragma unroll
+      for (int n2 = 0; n2 < M; ++n2) a[n2] = ld_pair(base + r0 + step * n2);
+    }
+  } else {
+#pragma unroll
+    for (int n2 = 0; n2 < M; ++n2)
+      a[n2] = active ? ld_col_pair(base + r0 + step * n2, pair, aligned) : make_float2(0.f, 0.f);
+  }
+}
+
 template <typename T>
 __device__ __forceinline__ void st_col_pair(T* p, float2 v, bool pair, bool aligned) {
   if (pair && aligned) {
@@ -75,10 +101,7 @@ conv_reg_kernel(const T* __restrict__ V, T* __restrict__ O, const float2* __rest
   const size_t base = (size_t)b * N * D + col;
 
   float2 a[M];
-#pragma unroll
-  for (int n2 = 0; n2 < M; ++n2)
-    a[n2] = active ? ld_col_pair(V + base + (size_t)(i + M * n2) * D, pair, aligned)
-                   : make_float2(0.f, 0.f);
+  ld_rows<T, M>(a, V + base, (size_t)M * D, (size_t)i * D, active, pair, aligned);
   dft<M, false>(a);
   __syncthreads();   // twiddles and spectrum ready
 #pragma unroll
