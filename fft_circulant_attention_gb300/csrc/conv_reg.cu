@@ -86,9 +86,27 @@ conv_reg_kernel(const T* __restrict__ V, T* __restrict__ O, const float2* __rest
   const int bh = blockIdx.x / groups, grp = blockIdx.x - (blockIdx.x / groups) * groups;
   const int b = bh / H, h = bh - b * H;
   const int p = threadIdx.x % P, i = threadIdx.x / P;
-  for (int e = threadIdx.x; e < N; e += blockDim.x) {
-    if (TW) tw[e] = __ldg(&W[(e / M) * (e % M)]);
-    zs[e] = __ldg(&zf[(size_t)bh * N + e]);
+  // Twiddles and spectrum to shared memory, four loads of each in flight
+  // per thread (one round trip for N = 32² with 256 threads).
+  constexpr int kPro = 4;
+  for (int e0 = threadIdx.x; e0 < N; e0 += kPro * blockDim.x) {
+    float2 tv[kPro], zv[kPro];
+#pragma unroll
+    for (int u = 0; u < kPro; ++u) {
+      const int e = e0 + u * blockDim.x;
+      if (e < N) {
+        if (TW) tv[u] = __ldg(&W[(e / M) * (e % M)]);
+        zv[u] = __ldg(&zf[(size_t)bh * N + e]);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kPro; ++u) {
+      const int e = e0 + u * blockDim.x;
+      if (e < N) {
+        if (TW) tw[e] = tv[u];
+        zs[e] = zv[u];
+      }
+    }
   }
 
   const int g = grp * P + p;
@@ -292,15 +310,14 @@ softmax_spectrum_reg(const float2* __restrict__ z, float* __restrict__ zs,
                      float2* __restrict__ zf, const float2* __restrict__ W, int rows) {
   constexpr int N = M * M;
   constexpr int GL = M <= 8 ? 8 : (M <= 16 ? 16 : 32);
-  constexpr int ROWS = kSpecRegThreads / GL;
   constexpr int RS = M + 1;                  // shared row of one k2 (complex)
   extern __shared__ float4 smem4[];
-  float2* tw = reinterpret_cast<float2*>(smem4);   // tw[n1·M + k2] = w_N^{n1·k2}
-  float2* xb = tw + N;                              // ROWS blocks of M·RS
-  if (TW)
-    for (int e = threadIdx.x; e < N; e += blockDim.x) tw[e] = __ldg(&W[(e / M) * (e % M)]);
+  float2* xb = reinterpret_cast<float2*>(smem4);   // one block of M·RS per row
+  // Rows are independent (a row's lanes are one warp's): the CTA holds
+  // blockDim.x / GL of them, whole warps, sized by the launch to the row
+  // count.  Lane i reads its twiddles w_N^{i·k2} straight from the table.
   const int i = threadIdx.x % GL, r = threadIdx.x / GL;
-  const int row = blockIdx.x * ROWS + r;
+  const int row = blockIdx.x * (blockDim.x / GL) + r;
   const bool act = i < M && row < rows;
   const float2* src = z + (size_t)(row < rows ? row : 0) * N;
   float2 v[M];
@@ -329,11 +346,10 @@ softmax_spectrum_reg(const float2* __restrict__ z, float* __restrict__ zs,
     if (act) out[i + M * n2] = a[n2].x;
   }
   dft<M, false>(a);
-  __syncthreads();   // twiddle table ready
   float2* xr = xb + r * M * RS;
   if (i < M) {
 #pragma unroll
-    for (int k2 = 0; k2 < M; ++k2) xr[k2 * RS + i] = TW ? cmul(a[k2], tw[i * M + k2]) : a[k2];
+    for (int k2 = 0; k2 < M; ++k2) xr[k2 * RS + i] = TW ? cmul(a[k2], __ldg(&W[i * k2])) : a[k2];
   }
   __syncwarp();      // a row's lanes are one warp's
   if (i < M) {
@@ -349,9 +365,19 @@ softmax_spectrum_reg(const float2* __restrict__ z, float* __restrict__ zs,
   }
 }
 
+// Rows per CTA: whole warps, at most kSpecRegThreads threads, and no more
+// rows than keep two CTAs on every SM when the row count is small.
+static int spectrum_reg_rows(int M, int rows, int sms) {
+  const int GL = M <= 8 ? 8 : (M <= 16 ? 16 : 32);
+  const int unit = 32 / GL, most = kSpecRegThreads / GL;
+  int per = rows / (2 * (sms > 0 ? sms : 1));
+  per = per < unit ? unit : (per > most ? most : per);
+  return per / unit * unit;
+}
+
 size_t spectrum_reg_smem(int M) {
   const int GL = M <= 8 ? 8 : (M <= 16 ? 16 : 32);
-  return ((size_t)M * M + (size_t)(kSpecRegThreads / GL) * M * (M + 1)) * sizeof(float2);
+  return (size_t)(kSpecRegThreads / GL) * M * (M + 1) * sizeof(float2);
 }
 
 template <bool TW>
@@ -360,13 +386,13 @@ static cudaError_t spectrum_reg_t(const cat_plan_s* p) {
   if (rows == 0) return cudaSuccess;
   const int M = p->sm.reg_m;
   const int GL = M <= 8 ? 8 : (M <= 16 ? 16 : 32);
-  const int per = kSpecRegThreads / GL;
+  const int per = spectrum_reg_rows(M, rows, p->sms);
   const int ctas = (rows + per - 1) / per;
-  const size_t smem = spectrum_reg_smem(M);
+  const size_t smem = (size_t)per * M * (M + 1) * sizeof(float2);
   switch (M) {
 #define CAT_M(m)                                                                            \
   case m:                                                                                   \
-    softmax_spectrum_reg<m, TW><<<ctas, kSpecRegThreads, smem, p->stream>>>(p->z2, p->zs,    \
+    softmax_spectrum_reg<m, TW><<<ctas, per * GL, smem, p->stream>>>(p->z2, p->zs,    \
                                                                             p->zf, p->tw, rows); \
     break;
     CAT_M(8) CAT_M(14) CAT_M(16) CAT_M(32)

@@ -7,6 +7,8 @@
 // acceleration" design) fused into the softmax kernel.
 #include <cuda_bf16.h>
 
+#include <type_traits>
+
 #include "bulk.cuh"
 #include "cat_internal.h"
 #include "elem.cuh"
@@ -70,9 +72,39 @@ __device__ __forceinline__ void two_sum_acc2(float2& hi, float2& lo, float2 p) {
 // W_A's columns [h0, h0 + HT) as fp32 [D][HP] in shared memory (columns HT
 // to HP zero).  Eight loads per thread are in flight before any is stored,
 // so the staging costs a few latencies rather than D·HP / blockDim of them.
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 template <typename T>
 __device__ __forceinline__ void stage_w_f32(float* ws, const T* __restrict__ WA, int D, int H,
-                                            int h0, int HT, int HP) {
+                                            int h0, int HT, int HP, bool wait = true) {
+  if constexpr (std::is_same<T, float>::value) {
+    // fp32 W_A needs no conversion: every element goes by an asynchronous
+    // copy (all of a thread's copies in flight at once, no registers held),
+    // 16 bytes at a time when the staged block is W_A itself (all heads,
+    // H a multiple of 4, 16-byte aligned), else 4; padding columns are zeroed.
+    if (h0 == 0 && HT == H && HP == H && ((uintptr_t)WA % 16) == 0) {
+      for (int i = threadIdx.x; i < D * H / 4; i += blockDim.x)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(ws + 4 * i)),
+                     "l"(__cvta_generic_to_global(WA + 4 * i))
+                     : "memory");
+    } else {
+      for (int i = threadIdx.x; i < D * HP; i += blockDim.x) {
+        const int d = i / HP, h = i - d * HP;
+        if (h < HT)
+          asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(ws + i)),
+                       "l"(__cvta_generic_to_global(WA + (size_t)d * H + h0 + h))
+                       : "memory");
+        else
+          ws[i] = 0.f;
+      }
+    }
+    // Without `wait` the caller waits (cp_async_wait_all) before the
+    // barrier that publishes the block.
+    if (wait) cp_async_wait_all();
+    return;
+  }
   constexpr int kBatch = 8;
   const int total = D * HP;
   for (int i0 = threadIdx.x; i0 < total; i0 += kBatch * blockDim.x) {
@@ -189,11 +221,12 @@ score_kernel(const T* __restrict__ X, const T* __restrict__ WA, float2* __restri
 // and added into the thread's double-float (hi, lo) by TwoSum; the kSplit
 // partial double-floats of a token are then combined by TwoSum across the
 // lanes.  Requires 16-byte vectors and D a multiple of kSplit vectors.
-constexpr int kSplit = 4;
 constexpr int kSplitTok = 2;
-constexpr int kScoreSplitTok = kScoreThreads / kSplit * kSplitTok;
+// Tokens per CTA with KS threads per token.
+template <int KS>
+constexpr int split_tokens() { return kScoreThreads / KS * kSplitTok; }
 
-template <typename T, int HT>
+template <typename T, int HT, int kSplit>
 __global__ void __launch_bounds__(kScoreThreads)
 score_split_kernel(const T* __restrict__ X, const T* __restrict__ WA, float2* __restrict__ z,
                    int N, int D, int H, int h0, int b0) {
@@ -201,11 +234,13 @@ score_split_kernel(const T* __restrict__ X, const T* __restrict__ WA, float2* __
   constexpr int V = Vec16<T>::n;
   constexpr int RUN = kChunk / V;   // vectors per fresh run
   constexpr int TT = kSplitTok;
+  constexpr int kScoreSplitTok = split_tokens<kSplit>();
   extern __shared__ float4 ws4[];
   float* ws = reinterpret_cast<float*>(ws4);
   const int b = b0 + blockIdx.y;
-  stage_w_f32(ws, WA, D, H, h0, HT, HP);
-  __syncthreads();
+  // W_A's copies are issued first and waited for after the first X loads,
+  // so the two latencies overlap.
+  stage_w_f32(ws, WA, D, H, h0, HT, HP, false);
   const int q = threadIdx.x % kSplit;
   const int slot = threadIdx.x / kSplit;              // 0 .. kScoreThreads/kSplit - 1
   int n[TT];
@@ -223,14 +258,18 @@ score_split_kernel(const T* __restrict__ X, const T* __restrict__ WA, float2* __
 #pragma unroll
     for (int h = 0; h < HT; ++h) hi[t][h] = lo[t][h] = 0.f;
   const int nvec = D / V;   // vectors per row; a multiple of kSplit
-  for (int v0 = q; v0 < nvec; v0 += kSplit * RUN) {
-    float xv[TT][RUN][V];
+  constexpr int kStep = kSplit * RUN;   // vectors a run advances
+  // One run: RUN vectors of each token, loaded before any FMA (two buffers,
+  // the next run's loads in flight while this one is summed).
+  auto load_run = [&](float (&xv)[TT][RUN][V], int v0) {
 #pragma unroll
     for (int r = 0; r < RUN; ++r) {
       const int v = min(v0 + r * kSplit, nvec - 1);   // loads stay in the row
 #pragma unroll
       for (int t = 0; t < TT; ++t) Vec16<T>::load(xr[t] + v * V, xv[t][r]);
     }
+  };
+  auto sum_run = [&](const float (&xv)[TT][RUN][V], int v0) {
     float part[TT][HT];
 #pragma unroll
     for (int t = 0; t < TT; ++t)
@@ -262,6 +301,17 @@ score_split_kernel(const T* __restrict__ X, const T* __restrict__ WA, float2* __
     for (int t = 0; t < TT; ++t)
 #pragma unroll
       for (int h = 0; h < HT; ++h) two_sum_acc(hi[t][h], lo[t][h], part[t][h]);
+  };
+  float xa[TT][RUN][V], xb[TT][RUN][V];
+  load_run(xa, q);
+  cp_async_wait_all();
+  __syncthreads();
+  for (int v0 = q; v0 < nvec; v0 += 2 * kStep) {
+    if (v0 + kStep < nvec) load_run(xb, v0 + kStep);
+    sum_run(xa, v0);
+    if (v0 + kStep >= nvec) break;
+    if (v0 + 2 * kStep < nvec) load_run(xa, v0 + 2 * kStep);
+    sum_run(xb, v0 + kStep);
   }
   // Combine each token's kSplit lanes (adjacent lanes of one warp).
 #pragma unroll
@@ -668,15 +718,16 @@ static cudaError_t run_score(const cat_plan_s* p, const T* X, const T* WA, int h
   constexpr int HP = (HT + 3) & ~3;
   size_t smem = (size_t)HP * p->D * sizeof(float);
   auto k = score_kernel<T, HT, VEC>;
-  auto ks = score_split_kernel<T, HT>;
+  auto ks4 = score_split_kernel<T, HT, 4>;
   if (setup) {
     cudaError_t e = allow_max_smem(k);
-    return (e == cudaSuccess && VEC) ? allow_max_smem(ks) : e;
+    return (e == cudaSuccess && VEC) ? allow_max_smem(ks4) : e;
   }
-  // Rows of whole kSplit-vector groups take the split kernel.
-  if (VEC && p->D % (kSplit * Vec16<T>::n) == 0) {
-    dim3 grid((p->N + kScoreSplitTok - 1) / kScoreSplitTok, sp.nb(p));
-    ks<<<grid, kScoreThreads, smem, sp.stream(p)>>>(X, WA, p->z2, p->N, p->D, p->H, h0, sp.b0);
+  // Rows of whole 4-thread vector groups take the split kernel.
+  if (VEC && p->D % (4 * Vec16<T>::n) == 0) {
+    constexpr int tok = split_tokens<4>();
+    dim3 grid((p->N + tok - 1) / tok, sp.nb(p));
+    ks4<<<grid, kScoreThreads, smem, sp.stream(p)>>>(X, WA, p->z2, p->N, p->D, p->H, h0, sp.b0);
     return cudaGetLastError();
   }
   dim3 grid((p->N + kScoreTokPerCta - 1) / kScoreTokPerCta, sp.nb(p));
