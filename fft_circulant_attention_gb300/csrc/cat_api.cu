@@ -372,6 +372,12 @@ void describe(cat_plan_s* p) {
                   "launches=%d",
                   p->N, p->fs.N1, p->fs.N2, p->fs.chunk_bh, p->scratch_bytes,
                   p->workspace_bytes, p->use_graph, p->launches);
+  } else if (p->gp2d) {
+    std::snprintf(p->desc, sizeof(p->desc),
+                  "path=grid2d gp=1 N=%d M=%d(32x%d) chunk_bh=%d scratch=%zu workspace=%zu "
+                  "launches=%d",
+                  p->N, p->gp.M, p->gp.R, p->gp.chunk, p->scratch_bytes, p->workspace_bytes,
+                  p->launches);
   } else {
     char r1[64] = {0}, r2[64] = {0};
     radstr(p->fs.rp1, r1, sizeof(r1));
@@ -735,6 +741,14 @@ int create_plan(cat_plan_t* out, int B, int N, int D, int H, int dtype, void* st
       sc.smem = cat::conv_reg_smem(gh, sc.G);
       sc.threads = gh * sc.G;
       p->launches = 3;
+    } else if (st == CAT_OK && cat::grid_pass_supported(gh, gw, p->dh) &&
+               !(r2 && std::strcmp(r2, "0") == 0)) {
+      // Square grids of side 64, 96 or 128: the row/column passes.
+      p->gp2d = 1;
+      st = cat::configure_grid_pass(p);
+      p->scratch_bytes = p->gp.scratch_bytes;
+      const int rows = B * H;
+      p->launches = 5 * ((rows + p->gp.chunk - 1) / p->gp.chunk);
     }
   } else {
     st = choose_path(p);
@@ -792,6 +806,7 @@ int create_plan(cat_plan_t* out, int B, int N, int D, int H, int dtype, void* st
         : p->path == cat::PATH_DIRECT   ? cat::setup_direct_kernels(p)
                                         : cat::setup_fast_kernels(p);
   if (e == cudaSuccess && p->reg2d) e = cat::setup_conv_reg(p);
+  if (e == cudaSuccess && p->gp2d) e = cat::setup_grid_pass(p);
   if (e == cudaSuccess && p->path == cat::PATH_FAST) {
     for (int k = 0; k < 2 && e == cudaSuccess; ++k) {
       e = cudaStreamCreateWithFlags(&p->side[k], cudaStreamNonBlocking);
@@ -1234,6 +1249,7 @@ int cat2d_scores(cat_plan_t p, const void* Q, const void* K, float* a, int B, in
   const size_t nx = (size_t)B * p->N * D * (dtype == CAT_BF16 ? 2 : 4);
   const size_t na = (size_t)B * H * p->N * sizeof(float);
   if (ranges_overlap(a, na, Q, nx) || ranges_overlap(a, na, K, nx)) return CAT_ERR_ALIAS;
+  if (p->gp2d) return map_cuda(cat::launch_grid_pass(p, Q, K, nullptr, nullptr, a));
   return map_cuda(p->reg2d ? cat::launch_scores2d_reg(p, Q, K, a) : cat::launch_scores2d(p, Q, K, a));
 }
 
@@ -1250,6 +1266,7 @@ int cat2d_forward(cat_plan_t p, const void* Q, const void* K, const void* V, voi
   const size_t nx = (size_t)B * p->N * D * es;
   if (ranges_overlap(O, nx, Q, nx) || ranges_overlap(O, nx, K, nx) || ranges_overlap(O, nx, V, nx))
     return CAT_ERR_ALIAS;
+  if (p->gp2d) return map_cuda(cat::launch_grid_pass(p, Q, K, V, O, nullptr));
   if (p->reg2d) {
     // Register kernels: scores, softmax with the 2-D spectrum, product.
     cudaError_t e = cat::launch_scores2d_reg(p, Q, K, nullptr);

@@ -32,6 +32,13 @@ struct DirectCfg {
   size_t smem;
 };
 
+// 2-D plan on a square grid of side M = 32·R (64, 96, 128): the five-pass
+// row/column transform of grid_pass.cu over chunks of `chunk` (b, h) rows.
+struct GridPassCfg {
+  int M, R, chunk;
+  size_t scratch_bytes;
+};
+
 // Four-step decomposition N = N1·N2 with row n = n1 + N1·n2 and bin
 // k = N2·k1 + k2.  Column pass A: per n1, DFT over n2 (length N2), then the
 // twiddle exp(-2πi n1·k2/N).  Row pass B: per k2, DFT over n1 (length N1),
@@ -135,6 +142,10 @@ struct cat_plan_s {
   // 2-D plan on a square grid of side 8, 14, 16 or 32: the register kernels
   // without twiddles (scores, spectrum, product) instead of the generic passes
   int reg2d;
+  // 2-D plan on a square grid of side 64, 96 or 128: the row/column passes
+  // of grid_pass.cu (scratch: p->scratch)
+  int gp2d;
+  cat::GridPassCfg gp;
   // backward workspace (configured and allocated at the first backward call)
   int bw_ready;
   cat::BwCfg bw;
@@ -232,6 +243,16 @@ size_t direct_smem(int N, int D, int dh, int R, bool fused);
 cudaError_t setup_direct_kernels(const cat_plan_s* p);
 cudaError_t launch_direct(const cat_plan_s* p, const void* X, const void* WA, const void* V,
                           void* O, bool fused);
+
+// 2-D plans on square grids of side 64, 96 or 128 (grid_pass.cu): whether
+// the shape fits, the chunking and scratch size (no allocation), one-time
+// attribute set-up, and the launch (V and O null: the scores only, into
+// aout; else the forward, aout null).
+bool grid_pass_supported(int h, int w, int dh);
+int configure_grid_pass(cat_plan_s* p);
+cudaError_t setup_grid_pass(const cat_plan_s* p);
+cudaError_t launch_grid_pass(const cat_plan_s* p, const void* Q, const void* K, const void* V,
+                             void* O, float* aout);
 
 // Fused projection on the tensor cores (proj_tc.cu): V = X·W_V into V and
 // the scores X·W_A into the plan's z2 in one pass over X (bf16, D % 64 == 0,

@@ -109,6 +109,43 @@ def test_register_and_generic_2d_agree(monkeypatch):
     assert float((O1 - O0).abs().max()) <= 4e-5 * float(V.abs().max())
 
 
+# Square grids of side 64, 96 or 128 take the row/column passes (length-M
+# DFTs as a register DFT-32 and a DFT-M/32 in shared memory, five passes over
+# grid rows and columns); both they and the generic passes are held to the
+# oracle.  The 128 x 128 case at head width 64 needs two chunks of (b, h)
+# rows, and head width 5 leaves a half pair.
+@pytest.mark.parametrize("B,side,D,H,dtype", [
+    (1, 64, 64, 2, "f32"),
+    (2, 64, 15, 3, "f32"),         # head width 5: a half pair
+    (1, 96, 96, 2, "bf16"),
+    (1, 128, 48, 2, "f32"),
+    (1, 128, 384, 6, "bf16"),      # two chunks of (b, h) rows
+])
+@pytest.mark.parametrize("gp", ["1", "0"])
+def test_square_grids_row_column_passes(B, side, D, H, dtype, gp, monkeypatch):
+    monkeypatch.setenv("CAT_2D_REG", gp)
+    err, desc = check2d(B, side, side, D, H, dtype, seed=side + D)
+    assert ("gp=1" in desc) == (gp == "1"), desc
+    if gp == "1" and side == 128 and D == 384:
+        assert "launches=10" in desc, desc
+    print("B%d %dx%d D%d H%d %s gp=%s: max|dO|/max|V| = %.2e" % (B, side, side, D, H, dtype,
+                                                                 gp, err))
+
+
+def test_row_column_passes_and_generic_2d_agree(monkeypatch):
+    B, side, D, H = 1, 96, 384, 6
+    Q, K, V = to_dev(*synth.make_qkv(B, side * side, D, "f32", 5))
+    outs = []
+    for gp in ("1", "0"):
+        monkeypatch.setenv("CAT_2D_REG", gp)
+        with cat.Plan2D(B, side, side, D, H, "f32") as plan:
+            outs.append((plan.forward(Q, K, V), plan.scores(Q, K)))
+            plan.sync()
+    (O1, a1), (O0, a0) = outs
+    assert float((a1 - a0).abs().max()) <= 2e-5 * float(a0.abs().max())
+    assert float((O1 - O0).abs().max()) <= 4e-5 * float(V.abs().max())
+
+
 @pytest.mark.parametrize("name", list(synth.GRID_CONFIGS))
 def test_grid_workloads(name):
     c = synth.GRID_CONFIGS[name]
