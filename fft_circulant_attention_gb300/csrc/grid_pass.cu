@@ -25,10 +25,12 @@
 // correlation Re(IDFT(X̂·conj(Ŷ))) of two such signals is the sum of the two
 // channels' real correlations.
 //
-// Inside a CTA, a length-M DFT of S signals held in shared memory (stride
-// M + 1, odd, so that column accesses hit distinct banks) is two in-place
-// stages: a register DFT-32 over each stride-R subsequence, times
-// w_M^{e1·k2}, then a DFT-R over adjacent slots.  With n = e1 + R·e2 and
+// Inside a CTA, a length-M DFT of S signals is two stages: a register
+// DFT-32 over each stride-R subsequence, times w_M^{e1·k2}, then a DFT-R
+// over adjacent slots, with the signals in shared memory (stride M + 1, odd,
+// so that column accesses hit distinct banks) between them.  The first
+// stage of a pass reads its input straight from global memory and the last
+// writes its output there, a warp's lanes on consecutive channel pairs.  With n = e1 + R·e2 and
 // k = k2 + 32·k1,
 //     X[k2 + 32·k1] = Σ_e1 w_R^{e1·k1} · w_M^{e1·k2} · Σ_e2 w_32^{e2·k2} x[e1 + R·e2],
 // so the spectrum lands in the slot order k ↦ k1 + R·k2.  The inverse runs
@@ -54,31 +56,6 @@ constexpr int kGpRowsPerCta = 8;          // pass 3: one warp per grid row
 // the error of the float product, so the truncation is exact.
 __device__ __forceinline__ int fdiv(int i, float r) { return (int)(((float)i + 0.5f) * r); }
 
-// The M twiddles w_M^m of a CTA (blocks of at least 64 threads, M <= 128:
-// at most two a thread), fetched into registers at the start and put in
-// shared memory after the CTA's main loads, so that no thread waits on them
-// before issuing those.  The plan's table holds w_N^j for N = M², and
-// w_M^m = w_N^{M·m}.
-template <int R>
-struct Twm {
-  static constexpr int M = 32 * R;
-  float2 v[2];
-  __device__ __forceinline__ void fetch(const float2* __restrict__ tw) {
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const int m = threadIdx.x + u * blockDim.x;
-      if (m < M) v[u] = __ldg(&tw[(size_t)M * m]);
-    }
-  }
-  __device__ __forceinline__ void put(float2* twm) const {
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const int m = threadIdx.x + u * blockDim.x;
-      if (m < M) twm[m] = v[u];
-    }
-  }
-};
-
 // Elements i = 0 .. count-1 moved by the CTA's threads from ld(i) to st(i, ·),
 // U loads in flight a thread before the first store (a loop that stored each
 // value before the next load would wait a full memory latency per element).
@@ -99,89 +76,69 @@ __device__ __forceinline__ void batched(int count, Ld ld, St st) {
   }
 }
 
-// A 16-byte chunk of a token's channels as PV (channel 2j, 2j + 1) pairs.
-template <typename T> struct Chunk16;
-template <> struct Chunk16<float> {
-  static constexpr int PV = 2;
-  static __device__ __forceinline__ void unpack(uint4 u, float2* v) {
-    v[0] = make_float2(__uint_as_float(u.x), __uint_as_float(u.y));
-    v[1] = make_float2(__uint_as_float(u.z), __uint_as_float(u.w));
-  }
-  static __device__ __forceinline__ uint4 pack(const float2* v) {
-    return make_uint4(__float_as_uint(v[0].x), __float_as_uint(v[0].y), __float_as_uint(v[1].x),
-                      __float_as_uint(v[1].y));
-  }
-};
-template <> struct Chunk16<__nv_bfloat16> {
-  static constexpr int PV = 4;
-  static __device__ __forceinline__ float2 word(unsigned int w) {
-    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
-  }
-  static __device__ __forceinline__ unsigned int bits(float2 v) {
-    const __nv_bfloat162 b = __floats2bfloat162_rn(v.x, v.y);
-    return *reinterpret_cast<const unsigned int*>(&b);
-  }
-  static __device__ __forceinline__ void unpack(uint4 u, float2* v) {
-    v[0] = word(u.x);
-    v[1] = word(u.y);
-    v[2] = word(u.z);
-    v[3] = word(u.w);
-  }
-  static __device__ __forceinline__ uint4 pack(const float2* v) {
-    return make_uint4(bits(v[0]), bits(v[1]), bits(v[2]), bits(v[3]));
-  }
-};
-
-// Length-M DFT of S signals in shared memory (signal s at buf + s·(M + 1)),
-// in place, all threads of the CTA.  Forward: natural order in, slot order
-// k1 + R·k2 out.  Inverse (unscaled): slot order in, natural order out.
-// Callers synchronise before; the routine ends with a barrier.
-template <int R, bool INV>
-__device__ __forceinline__ void dft_m(float2* buf, int S, const float2* twm) {
-  constexpr int M = 32 * R, LS = M + 1;
+// The two stages of a length-M DFT of S signals, M = 32·R.  Element n of
+// signal sig comes from ld(sig, n) and goes to st(sig, n, value), so a stage
+// reads from or writes to global memory or shared memory as the pass needs.
+// Tasks run signal-fastest, so that the lanes of a warp touch consecutive
+// signals: consecutive channel pairs in global memory, rows M + 1 apart (an
+// odd stride: distinct banks) in shared memory.  twm: w_M^m, m < M.
+//
+// Stage A, forward: task (sig, e1) transforms x[e1 + R·e2] over e2 (a
+// register DFT-32) and writes slot e1 + R·k2 times w_M^{e1·k2}.
+template <int R, class Ld, class St>
+__device__ __forceinline__ void stage_a_fwd(int S, const float2* __restrict__ twm, Ld ld, St st) {
   const float rS = 1.0f / (float)S;
-  auto stage_a = [&]() {
-    for (int t = threadIdx.x; t < S * R; t += blockDim.x) {
-      const int e1 = fdiv(t, rS), sig = t - e1 * S;
-      float2* s = buf + sig * LS + e1;
-      float2 a[32];
-      if constexpr (!INV) {
+  for (int t = threadIdx.x; t < S * R; t += blockDim.x) {
+    const int e1 = fdiv(t, rS), sig = t - e1 * S;
+    float2 a[32];
 #pragma unroll
-        for (int e2 = 0; e2 < 32; ++e2) a[e2] = s[R * e2];
-        dft<32, false>(a);
+    for (int e2 = 0; e2 < 32; ++e2) a[e2] = ld(sig, e1 + R * e2);
+    dft<32, false>(a);
 #pragma unroll
-        for (int k2 = 0; k2 < 32; ++k2) s[R * k2] = cmul(a[k2], twm[e1 * k2]);
-      } else {
-#pragma unroll
-        for (int k2 = 0; k2 < 32; ++k2) a[k2] = cmulc(s[R * k2], twm[e1 * k2]);
-        dft<32, true>(a);
-#pragma unroll
-        for (int e2 = 0; e2 < 32; ++e2) s[R * e2] = a[e2];
-      }
-    }
-    __syncthreads();
-  };
-  auto stage_b = [&]() {
-    for (int t = threadIdx.x; t < S * 32; t += blockDim.x) {
-      const int k2 = fdiv(t, rS), sig = t - k2 * S;
-      float2* s = buf + sig * LS + R * k2;
-      float2 a[R];
-#pragma unroll
-      for (int j = 0; j < R; ++j) a[j] = s[j];
-      dft_small<R, INV>(a);
-#pragma unroll
-      for (int j = 0; j < R; ++j) s[j] = a[j];
-    }
-    __syncthreads();
-  };
-  if constexpr (!INV) {
-    stage_a();
-    stage_b();
-  } else {
-    stage_b();
-    stage_a();
+    for (int k2 = 0; k2 < 32; ++k2) st(sig, e1 + R * k2, cmul(a[k2], __ldg(&twm[e1 * k2])));
   }
 }
+// Stage A, inverse: slot e1 + R·k2 times conj w_M^{e1·k2}, the inverse
+// DFT-32 over k2, written to element e1 + R·e2.
+template <int R, class Ld, class St>
+__device__ __forceinline__ void stage_a_inv(int S, const float2* __restrict__ twm, Ld ld, St st) {
+  const float rS = 1.0f / (float)S;
+  for (int t = threadIdx.x; t < S * R; t += blockDim.x) {
+    const int e1 = fdiv(t, rS), sig = t - e1 * S;
+    float2 a[32];
+#pragma unroll
+    for (int k2 = 0; k2 < 32; ++k2) a[k2] = cmulc(ld(sig, e1 + R * k2), __ldg(&twm[e1 * k2]));
+    dft<32, true>(a);
+#pragma unroll
+    for (int e2 = 0; e2 < 32; ++e2) st(sig, e1 + R * e2, a[e2]);
+  }
+}
+// Stage B: task (sig, k2) applies the DFT-R (inverse: its conjugate) to the
+// R adjacent slots R·k2 .. R·k2 + R - 1.
+template <int R, bool INV, class Ld, class St>
+__device__ __forceinline__ void stage_b(int S, Ld ld, St st) {
+  const float rS = 1.0f / (float)S;
+  for (int t = threadIdx.x; t < S * 32; t += blockDim.x) {
+    const int k2 = fdiv(t, rS), sig = t - k2 * S;
+    float2 a[R];
+#pragma unroll
+    for (int j = 0; j < R; ++j) a[j] = ld(sig, R * k2 + j);
+    dft_small<R, INV>(a);
+#pragma unroll
+    for (int j = 0; j < R; ++j) st(sig, R * k2 + j, a[j]);
+  }
+}
+
+// Shared-memory signals: signal sig at buf + sig·(M + 1).
+template <int R>
+struct Smem {
+  static constexpr int LS = 32 * R + 1;
+  float2* buf;
+  __device__ __forceinline__ float2 operator()(int sig, int e) const { return buf[sig * LS + e]; }
+  __device__ __forceinline__ void operator()(int sig, int e, float2 v) const {
+    buf[sig * LS + e] = v;
+  }
+};
 
 // Channels (c, c + 1) of a row as one complex value; c + 1 past the head
 // width reads as 0.  `aligned`: c even in an even-width row (pair access).
@@ -200,140 +157,64 @@ __device__ __forceinline__ void st_chan_pair(T* p, float2 v, bool pair, bool ali
   }
 }
 
-// Scratch rows [y][slot][g] of npair complex values: the M·np values of
-// one grid row (or the strided column entries) to and from shared-memory
-// signals buf[g·LS + e].  Two pairs (16 bytes) an access when npair is even.
-// Load: element e of the signals from src + e·estride + g.
-template <int R>
-__device__ __forceinline__ void scr_load(float2* buf, int sigoff, const float2* __restrict__ src,
-                                         size_t estride, int np) {
-  constexpr int M = 32 * R, LS = M + 1;
-  if ((np & 1) == 0) {
-    const int h2 = np / 2;
-    const float r2 = 1.0f / (float)h2;
-    batched<8, float4>(
-        M * h2,
-        [&](int i) {
-          const int e = fdiv(i, r2), g2 = i - e * h2;
-          return __ldg(reinterpret_cast<const float4*>(src + (size_t)e * estride) + g2);
-        },
-        [&](int i, float4 v) {
-          const int e = fdiv(i, r2), g = 2 * (i - e * h2);
-          buf[(sigoff + g) * LS + e] = make_float2(v.x, v.y);
-          buf[(sigoff + g + 1) * LS + e] = make_float2(v.z, v.w);
-        });
-  } else {
-    const float r = 1.0f / (float)np;
-    batched<16, float2>(
-        M * np,
-        [&](int i) {
-          const int e = fdiv(i, r), g = i - e * np;
-          return src[(size_t)e * estride + g];
-        },
-        [&](int i, float2 v) {
-          const int e = fdiv(i, r), g = i - e * np;
-          buf[(sigoff + g) * LS + e] = v;
-        });
-  }
-}
-template <int R>
-__device__ __forceinline__ void scr_store(const float2* buf, float2* __restrict__ dst,
-                                          size_t estride, int np) {
-  constexpr int M = 32 * R, LS = M + 1;
-  if ((np & 1) == 0) {
-    const int h2 = np / 2;
-    const float r2 = 1.0f / (float)h2;
-    for (int i = threadIdx.x; i < M * h2; i += blockDim.x) {
-      const int e = fdiv(i, r2), g2 = i - e * h2;
-      const float2 a = buf[2 * g2 * LS + e], c = buf[(2 * g2 + 1) * LS + e];
-      reinterpret_cast<float4*>(dst + (size_t)e * estride)[g2] = make_float4(a.x, a.y, c.x, c.y);
-    }
-  } else {
-    const float r = 1.0f / (float)np;
-    for (int i = threadIdx.x; i < M * np; i += blockDim.x) {
-      const int e = fdiv(i, r), g = i - e * np;
-      dst[(size_t)e * estride + g] = buf[g * LS + e];
-    }
-  }
-}
-
 // Pass 1: grid row y of (b, h) = bh0 + blockIdx.y, tensor blockIdx.z (Q, K,
-// V): the x-DFT of its npair signals into xs[z][bhl][y][slot][g].  vec: the
-// head's channels come in whole 16-byte chunks (dh and D multiples of the
-// chunk), else pair by pair.
+// V): the x-DFT of its npair signals into xs[z][bhl][y][slot][g]; stage A
+// reads the row's channel pairs, stage B writes the scratch.
 template <typename T, int R>
 __global__ void __launch_bounds__(kGpMaxThreads)
 gp_rows_fwd(const T* __restrict__ X0, const T* __restrict__ X1, const T* __restrict__ X2,
-            float2* __restrict__ xs, size_t tstride, const float2* __restrict__ tw, int D, int H,
-            int dh, int np, int bh0, int vec) {
-  constexpr int M = 32 * R, LS = M + 1;
+            float2* __restrict__ xs, size_t tstride, const float2* __restrict__ twm, int D,
+            int H, int dh, int np, int bh0) {
+  constexpr int M = 32 * R;
   extern __shared__ float4 smem4[];
-  float2* twm = reinterpret_cast<float2*>(smem4);
-  float2* buf = twm + M;
+  const Smem<R> sm{reinterpret_cast<float2*>(smem4)};
   const int y = blockIdx.x, bhl = blockIdx.y, z = blockIdx.z;
   const int bh = bh0 + bhl, b = bh / H, h = bh - b * H;
   const T* X = z == 0 ? X0 : (z == 1 ? X1 : X2);
-  Twm<R> tv;
-  tv.fetch(tw);
+  const bool aligned = ((h * dh) % 2) == 0 && (D % 2) == 0;
   const T* row = X + ((size_t)b * M * M + (size_t)y * M) * D + (size_t)h * dh;
-  if (vec) {
-    constexpr int E = 16 / (int)sizeof(T), PV = E / 2;
-    const int vpr = dh / E;
-    const float rv = 1.0f / (float)vpr;
-    batched<8, uint4>(
-        M * vpr,
-        [&](int i) {
-          const int x = fdiv(i, rv), j = i - x * vpr;
-          return __ldg(reinterpret_cast<const uint4*>(row + (size_t)x * D + j * E));
-        },
-        [&](int i, uint4 u) {
-          const int x = fdiv(i, rv), j = i - x * vpr;
-          float2 v[PV];
-          Chunk16<T>::unpack(u, v);
-#pragma unroll
-          for (int k = 0; k < PV; ++k) buf[(j * PV + k) * LS + x] = v[k];
-        });
-  } else {
-    const bool aligned = ((h * dh) % 2) == 0 && (D % 2) == 0;
-    const float r = 1.0f / (float)np;
-    batched<16, float2>(
-        M * np,
-        [&](int i) {
-          const int x = fdiv(i, r), g = i - x * np;
+  // Whole pairs at even offsets (the common case) load without a branch, so
+  // that all of a task's loads issue before its transform.
+  if (aligned && (dh % 2) == 0)
+    stage_a_fwd<R>(np, twm, [&](int g, int x) { return ld_pair(row + (size_t)x * D + 2 * g); },
+                   sm);
+  else
+    stage_a_fwd<R>(
+        np, twm,
+        [&](int g, int x) {
           return ld_chan_pair(row + (size_t)x * D + 2 * g, 2 * g + 1 < dh, aligned);
         },
-        [&](int i, float2 v) {
-          const int x = fdiv(i, r), g = i - x * np;
-          buf[g * LS + x] = v;
-        });
-  }
-  tv.put(twm);
+        sm);
   __syncthreads();
-  dft_m<R, false>(buf, np, twm);
-  scr_store<R>(buf, xs + z * tstride + ((size_t)bhl * M + y) * M * np, np, np);
+  float2* dst = xs + z * tstride + ((size_t)bhl * M + y) * M * np;
+  stage_b<R, false>(np, sm, [&](int g, int s, float2 v) { dst[(size_t)s * np + g] = v; });
 }
 
 // Pass 2: column slot kx = blockIdx.x of (b, h) row bhl = blockIdx.y: the
-// y-DFT of Q's and K's npair signals, Σ_g Q̂_g·conj(K̂_g) in the order g = 0,
-// 1, …, and its inverse y-DFT into tsc[bhl][y][kx].
+// y-DFT of Q's and K's npair signals (stage A reads the scratch column),
+// Σ_g Q̂_g·conj(K̂_g) in the order g = 0, 1, …, and its inverse y-DFT into
+// tsc[bhl][y][kx].
 template <int R>
 __global__ void __launch_bounds__(kGpMaxThreads)
 gp_cols_scores(const float2* __restrict__ qs, const float2* __restrict__ ks,
-               float2* __restrict__ tsc, const float2* __restrict__ tw, int np) {
+               float2* __restrict__ tsc, const float2* __restrict__ twm, int np) {
   constexpr int M = 32 * R, LS = M + 1;
   extern __shared__ float4 smem4[];
-  float2* twm = reinterpret_cast<float2*>(smem4);
-  float2* buf = twm + M;               // Q's signals, then K's
-  float2* sum = buf + 2 * np * LS;
+  float2* buf = reinterpret_cast<float2*>(smem4);   // Q's signals, then K's
+  const Smem<R> sm{buf};
+  const Smem<R> sum{buf + 2 * np * LS};
   const int kx = blockIdx.x, bhl = blockIdx.y;
-  Twm<R> tv;
-  tv.fetch(tw);
   const size_t base = (size_t)bhl * M * M * np + (size_t)kx * np;
-  scr_load<R>(buf, 0, qs + base, (size_t)M * np, np);
-  scr_load<R>(buf, np, ks + base, (size_t)M * np, np);
-  tv.put(twm);
+  stage_a_fwd<R>(
+      2 * np, twm,
+      [&](int sig, int y) {
+        const int q = sig >= np;
+        return (q ? ks : qs)[base + (size_t)y * M * np + (sig - q * np)];
+      },
+      sm);
   __syncthreads();
-  dft_m<R, false>(buf, 2 * np, twm);
+  stage_b<R, false>(2 * np, sm, sm);
+  __syncthreads();
   for (int s = threadIdx.x; s < M; s += blockDim.x) {
     float2 acc = make_float2(0.f, 0.f);
     for (int g = 0; g < np; ++g) {
@@ -341,12 +222,13 @@ gp_cols_scores(const float2* __restrict__ qs, const float2* __restrict__ ks,
       acc.x = fmaf(q.x, k.x, fmaf(q.y, k.y, acc.x));
       acc.y = fmaf(q.y, k.x, fmaf(-q.x, k.y, acc.y));
     }
-    sum[s] = acc;
+    sum(0, s, acc);
   }
   __syncthreads();
-  dft_m<R, true>(sum, 1, twm);
+  stage_b<R, true>(1, sum, sum);
+  __syncthreads();
   float2* dst = tsc + (size_t)bhl * M * M + kx;
-  for (int y = threadIdx.x; y < M; y += blockDim.x) dst[(size_t)y * M] = sum[y];
+  stage_a_inv<R>(1, twm, sum, [&](int, int yy, float2 v) { dst[(size_t)yy * M] = v; });
 }
 
 // Pass 3: grid rows y0 .. y0 + 7 (one warp each) of (b, h) row bhl: the
@@ -357,24 +239,17 @@ template <int R>
 __global__ void __launch_bounds__(32 * kGpRowsPerCta)
 gp_rows_scores(const float2* __restrict__ tsc, float2* __restrict__ esp,
                float2* __restrict__ stats, float* __restrict__ aout,
-               const float2* __restrict__ tw, int bh0, float scale) {
+               const float2* __restrict__ twm, int bh0, float scale) {
   constexpr int M = 32 * R, LS = M + 1, RB = kGpRowsPerCta;
   extern __shared__ float4 smem4[];
-  float2* twm = reinterpret_cast<float2*>(smem4);
-  float2* buf = twm + M;
+  float2* buf = reinterpret_cast<float2*>(smem4);
+  const Smem<R> sm{buf};
   const int bhl = blockIdx.y, bh = bh0 + bhl, y0 = blockIdx.x * RB;
-  Twm<R> tv;
-  tv.fetch(tw);
-  const float rM = 1.0f / (float)M;
-  batched<4, float2>(
-      RB * M, [&](int i) { return tsc[((size_t)bhl * M + y0) * M + i]; },
-      [&](int i, float2 v) {
-        const int r = fdiv(i, rM), s = i - r * M;
-        buf[r * LS + s] = v;
-      });
-  tv.put(twm);
+  const float2* src = tsc + ((size_t)bhl * M + y0) * M;
+  stage_b<R, true>(RB, [&](int r, int s) { return src[r * M + s]; }, sm);
   __syncthreads();
-  dft_m<R, true>(buf, RB, twm);
+  stage_a_inv<R>(RB, twm, sm, sm);
+  __syncthreads();
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31, y = y0 + w;
   float v[R];
   float m = -INFINITY;
@@ -399,11 +274,10 @@ gp_rows_scores(const float2* __restrict__ tsc, float2* __restrict__ esp,
   s = warp_sum(s);
   if (lane == 0) stats[(size_t)bhl * M + y] = make_float2(m, s);
   __syncthreads();
-  dft_m<R, false>(buf, RB, twm);
-  for (int i = threadIdx.x; i < RB * M; i += blockDim.x) {
-    const int r = fdiv(i, rM), sl = i - r * M;
-    esp[((size_t)bhl * M + y0 + r) * M + sl] = buf[r * LS + sl];
-  }
+  stage_a_fwd<R>(RB, twm, sm, sm);
+  __syncthreads();
+  float2* dst = esp + ((size_t)bhl * M + y0) * M;
+  stage_b<R, false>(RB, sm, [&](int r, int sl, float2 val) { dst[r * M + sl] = val; });
 }
 
 // Pass 4: column slot kx of (b, h) row bhl.  The softmax's scale of grid
@@ -414,18 +288,16 @@ gp_rows_scores(const float2* __restrict__ tsc, float2* __restrict__ esp,
 template <int R>
 __global__ void __launch_bounds__(kGpMaxThreads)
 gp_cols_conv(float2* __restrict__ vs, const float2* __restrict__ esp,
-             const float2* __restrict__ stats, const float2* __restrict__ tw, int np,
+             const float2* __restrict__ stats, const float2* __restrict__ twm, int np,
              float invN) {
   constexpr int M = 32 * R, LS = M + 1;
   extern __shared__ float4 smem4[];
-  float2* twm = reinterpret_cast<float2*>(smem4);
-  float2* sig = twm + M;               // σ's column, then V's npair columns
-  float2* vb = sig + LS;
-  float* cy = reinterpret_cast<float*>(vb + np * LS);
+  float2* sbuf = reinterpret_cast<float2*>(smem4);   // σ's column, then V's npair columns
+  const Smem<R> all{sbuf};
+  const Smem<R> vb{sbuf + LS};
+  float* cy = reinterpret_cast<float*>(sbuf + (np + 1) * LS);
   const int kx = blockIdx.x, bhl = blockIdx.y;
-  Twm<R> tv;
-  tv.fetch(tw);
-  // σ's column and (warp 0) the row statistics, fetched with the rest.
+  // σ's column and (warp 0) the row statistics, fetched first.
   float2 ev[2], st[R];
 #pragma unroll
   for (int u = 0; u < 2; ++u) {
@@ -436,9 +308,10 @@ gp_cols_conv(float2* __restrict__ vs, const float2* __restrict__ esp,
 #pragma unroll
     for (int j = 0; j < R; ++j) st[j] = stats[(size_t)bhl * M + threadIdx.x + 32 * j];
   }
-  const size_t base = (size_t)bhl * M * M * np + (size_t)kx * np;
-  scr_load<R>(vb, 0, vs + base, (size_t)M * np, np);
-  tv.put(twm);
+  float2* col = vs + (size_t)bhl * M * M * np + (size_t)kx * np;
+  auto gcol_ld = [&](int g, int y) { return col[(size_t)y * M * np + g]; };
+  auto gcol_st = [&](int g, int y, float2 v) { col[(size_t)y * M * np + g] = v; };
+  stage_a_fwd<R>(np, twm, gcol_ld, vb);
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
     float mm = -INFINITY;
@@ -457,58 +330,48 @@ gp_cols_conv(float2* __restrict__ vs, const float2* __restrict__ esp,
 #pragma unroll
   for (int u = 0; u < 2; ++u) {
     const int y = threadIdx.x + u * blockDim.x;
-    if (y < M) sig[y] = cscale(ev[u], cy[y]);
+    if (y < M) sbuf[y] = cscale(ev[u], cy[y]);
   }
   __syncthreads();
-  dft_m<R, false>(sig, np + 1, twm);
+  stage_a_fwd<R>(1, twm, all, all);
+  __syncthreads();
+  stage_b<R, false>(np + 1, all, all);
+  __syncthreads();
   const float rM = 1.0f / (float)M;
   for (int i = threadIdx.x; i < M * np; i += blockDim.x) {
     const int g = fdiv(i, rM), s = i - g * M;
-    vb[g * LS + s] = cmul(vb[g * LS + s], sig[s]);
+    vb(g, s, cmul(vb(g, s), sbuf[s]));
   }
   __syncthreads();
-  dft_m<R, true>(vb, np, twm);
-  scr_store<R>(vb, vs + base, (size_t)M * np, np);
+  stage_b<R, true>(np, vb, vb);
+  __syncthreads();
+  stage_a_inv<R>(np, twm, vb, gcol_st);
 }
 
 // Pass 5: grid row y of (b, h) row bhl: the inverse x-DFT of V's npair
-// signals, stored as O's channels (2g, 2g + 1); vec as in pass 1.
+// signals (stage B reads the scratch row), stored as O's channels
+// (2g, 2g + 1) by stage A.
 template <typename T, int R>
 __global__ void __launch_bounds__(kGpMaxThreads)
-gp_rows_out(const float2* __restrict__ vs, T* __restrict__ O, const float2* __restrict__ tw,
-            int D, int H, int dh, int np, int bh0, int vec) {
-  constexpr int M = 32 * R, LS = M + 1;
+gp_rows_out(const float2* __restrict__ vs, T* __restrict__ O, const float2* __restrict__ twm,
+            int D, int H, int dh, int np, int bh0) {
+  constexpr int M = 32 * R;
   extern __shared__ float4 smem4[];
-  float2* twm = reinterpret_cast<float2*>(smem4);
-  float2* buf = twm + M;
+  const Smem<R> sm{reinterpret_cast<float2*>(smem4)};
   const int y = blockIdx.x, bhl = blockIdx.y;
   const int bh = bh0 + bhl, b = bh / H, h = bh - b * H;
-  Twm<R> tv;
-  tv.fetch(tw);
-  scr_load<R>(buf, 0, vs + ((size_t)bhl * M + y) * M * np, np, np);
-  tv.put(twm);
+  const float2* src = vs + ((size_t)bhl * M + y) * M * np;
+  stage_b<R, true>(np, [&](int g, int s) { return src[(size_t)s * np + g]; }, sm);
   __syncthreads();
-  dft_m<R, true>(buf, np, twm);
+  const bool aligned = ((h * dh) % 2) == 0 && (D % 2) == 0;
   T* row = O + ((size_t)b * M * M + (size_t)y * M) * D + (size_t)h * dh;
-  if (vec) {
-    constexpr int E = 16 / (int)sizeof(T), PV = E / 2;
-    const int vpr = dh / E;
-    const float rv = 1.0f / (float)vpr;
-    for (int i = threadIdx.x; i < M * vpr; i += blockDim.x) {
-      const int x = fdiv(i, rv), j = i - x * vpr;
-      float2 v[PV];
-#pragma unroll
-      for (int k = 0; k < PV; ++k) v[k] = buf[(j * PV + k) * LS + x];
-      *reinterpret_cast<uint4*>(row + (size_t)x * D + j * E) = Chunk16<T>::pack(v);
-    }
-  } else {
-    const bool aligned = ((h * dh) % 2) == 0 && (D % 2) == 0;
-    const float r = 1.0f / (float)np;
-    for (int i = threadIdx.x; i < M * np; i += blockDim.x) {
-      const int x = fdiv(i, r), g = i - x * np;
-      st_chan_pair(row + (size_t)x * D + 2 * g, buf[g * LS + x], 2 * g + 1 < dh, aligned);
-    }
-  }
+  if (aligned && (dh % 2) == 0)
+    stage_a_inv<R>(np, twm, sm,
+                   [&](int g, int x, float2 v) { st_pair(row + (size_t)x * D + 2 * g, v); });
+  else
+    stage_a_inv<R>(np, twm, sm, [&](int g, int x, float2 v) {
+      st_chan_pair(row + (size_t)x * D + 2 * g, v, 2 * g + 1 < dh, aligned);
+    });
 }
 
 // ---------------------------------------------------------------------------
@@ -516,21 +379,17 @@ gp_rows_out(const float2* __restrict__ vs, T* __restrict__ O, const float2* __re
 
 namespace {
 
+// Threads of a CTA whose stage A has `tasks` tasks: whole warps, 128 .. 512.
 int gp_threads(int tasks) {
   int t = (tasks + 31) / 32 * 32;
-  return t < 64 ? 64 : (t > kGpMaxThreads ? kGpMaxThreads : t);
+  return t < 128 ? 128 : (t > kGpMaxThreads ? kGpMaxThreads : t);
 }
 
-size_t smem_rows(int M, int np) { return ((size_t)M + (size_t)np * (M + 1)) * sizeof(float2); }
-size_t smem_cols_scores(int M, int np) {
-  return ((size_t)M + (size_t)(2 * np + 1) * (M + 1)) * sizeof(float2);
-}
-size_t smem_rows_scores(int M) {
-  return ((size_t)M + (size_t)kGpRowsPerCta * (M + 1)) * sizeof(float2);
-}
-size_t smem_cols_conv(int M, int np) {
-  return ((size_t)M + (size_t)(np + 1) * (M + 1)) * sizeof(float2) + (size_t)M * sizeof(float);
-}
+size_t sig_bytes(int M, int nsig) { return (size_t)nsig * (M + 1) * sizeof(float2); }
+size_t smem_rows(int M, int np) { return sig_bytes(M, np); }
+size_t smem_cols_scores(int M, int np) { return sig_bytes(M, 2 * np + 1); }
+size_t smem_rows_scores(int M) { return sig_bytes(M, kGpRowsPerCta); }
+size_t smem_cols_conv(int M, int np) { return sig_bytes(M, np + 1) + (size_t)M * sizeof(float); }
 
 // Complex values of scratch per (b, h) row: Q, K, V after pass 1 (M²·npair
 // each), the correlation after pass 2 and σ's x-spectrum (M² each), and the
@@ -549,7 +408,11 @@ cudaError_t setup_r() {
   return e;
 }
 
+// Scratch layout: the M twiddles w_M^m, then per chunk of (b, h) rows the
+// pass-1 spectra of Q, K, V, the correlation, σ's x-spectrum and the row
+// statistics.
 struct Bufs {
+  float2* twm;     // [M]
   float2* xs;      // [3][chunk][M][M][np]
   size_t tstride;  // chunk·M²·np
   float2* tsc;     // [chunk][M][M]
@@ -560,7 +423,8 @@ struct Bufs {
 Bufs bufs(const cat_plan_s* p) {
   const int M = p->gp.M, np = p->npair, c = p->gp.chunk;
   Bufs b;
-  b.xs = p->scratch;
+  b.twm = p->scratch;
+  b.xs = p->scratch + M;
   b.tstride = (size_t)c * M * M * np;
   b.tsc = b.xs + 3 * b.tstride;
   b.esp = b.tsc + (size_t)c * M * M;
@@ -579,26 +443,22 @@ cudaError_t run_chunk(const cat_plan_s* p, const T* Q, const T* K, const T* V, T
   cudaStream_t st = p->stream;
   const bool fwd = V != nullptr;
   const int ntens = fwd ? 3 : 2;
-  // Whole 16-byte chunks of channels per head (the API's 16-byte aligned
-  // tensors then give aligned chunks).
-  const int E = 16 / (int)sizeof(T);
-  const int vec = (p->dh % E == 0 && p->D % E == 0) ? 1 : 0;
   gp_rows_fwd<T, R><<<dim3(M, nb, ntens), gp_threads(np * R), smem_rows(M, np), st>>>(
-      Q, K, V, bf.xs, bf.tstride, p->tw, p->D, p->H, p->dh, np, bh0, vec);
+      Q, K, V, bf.xs, bf.tstride, bf.twm, p->D, p->H, p->dh, np, bh0);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   gp_cols_scores<R><<<dim3(M, nb), gp_threads(2 * np * R), smem_cols_scores(M, np), st>>>(
-      bf.xs, bf.xs + bf.tstride, bf.tsc, p->tw, np);
+      bf.xs, bf.xs + bf.tstride, bf.tsc, bf.twm, np);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const float scale = 1.0f / ((float)p->dh * (float)(M * M));
   gp_rows_scores<R><<<dim3(M / kGpRowsPerCta, nb), 32 * kGpRowsPerCta, smem_rows_scores(M), st>>>(
-      bf.tsc, fwd ? bf.esp : nullptr, bf.stats, aout, p->tw, bh0, scale);
+      bf.tsc, fwd ? bf.esp : nullptr, bf.stats, aout, bf.twm, bh0, scale);
   if ((e = cudaGetLastError()) != cudaSuccess || !fwd) return e;
-  gp_cols_conv<R><<<dim3(M, nb), gp_threads((np + 1) * R), smem_cols_conv(M, np), st>>>(
-      bf.xs + 2 * bf.tstride, bf.esp, bf.stats, p->tw, np, 1.0f / (float)(M * M));
+  gp_cols_conv<R><<<dim3(M, nb), gp_threads(np * R), smem_cols_conv(M, np), st>>>(
+      bf.xs + 2 * bf.tstride, bf.esp, bf.stats, bf.twm, np, 1.0f / (float)(M * M));
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   gp_rows_out<T, R><<<dim3(M, nb), gp_threads(np * R), smem_rows(M, np), st>>>(
-      bf.xs + 2 * bf.tstride, O, p->tw, p->D, p->H, p->dh, np, bh0, vec);
+      bf.xs + 2 * bf.tstride, O, bf.twm, p->D, p->H, p->dh, np, bh0);
   return cudaGetLastError();
 }
 
@@ -629,8 +489,9 @@ cudaError_t run_all(const cat_plan_s* p, const void* Q, const void* K, const voi
 bool grid_pass_supported(int h, int w, int dh) {
   if (h != w || (h != 64 && h != 96 && h != 128)) return false;
   const int np = (dh + 1) / 2;
-  // Pass 2 holds Q's and K's columns of one slot in shared memory.
-  return smem_cols_scores(h, np) <= (size_t)200 * 1024;
+  // Pass 2 holds Q's and K's columns of one slot in shared memory, and its
+  // stage A has 2·npair·M/32 tasks for at most 512 threads.
+  return smem_cols_scores(h, np) <= (size_t)200 * 1024 && 2 * np * (h / 32) <= kGpMaxThreads;
 }
 
 int configure_grid_pass(cat_plan_s* p) {
@@ -644,15 +505,25 @@ int configure_grid_pass(cat_plan_s* p) {
   if (c < 1) c = 1;
   if (c > rows) c = rows;
   g.chunk = rows > 0 ? (int)c : 1;
-  g.scratch_bytes = (size_t)g.chunk * one;
+  g.scratch_bytes = (size_t)M * sizeof(float2) + (size_t)g.chunk * one;
   return CAT_OK;
 }
 
+// Kernel attributes, and the M twiddles w_M^m = exp(-2πi m/M) (evaluated in
+// fp64, rounded once) at the start of the scratch.
 cudaError_t setup_grid_pass(const cat_plan_s* p) {
   cudaError_t e = p->dtype == 1 ? setup_r<__nv_bfloat16, 2>() : setup_r<float, 2>();
   if (e == cudaSuccess) e = p->dtype == 1 ? setup_r<__nv_bfloat16, 3>() : setup_r<float, 3>();
   if (e == cudaSuccess) e = p->dtype == 1 ? setup_r<__nv_bfloat16, 4>() : setup_r<float, 4>();
-  return e;
+  if (e != cudaSuccess) return e;
+  const int M = p->gp.M;
+  float2 host[128];
+  const double two_pi = 6.283185307179586476925286766559;
+  for (int m = 0; m < M; ++m) {
+    const double a = -two_pi * (double)m / (double)M;
+    host[m] = make_float2((float)std::cos(a), (float)std::sin(a));
+  }
+  return cudaMemcpy(p->scratch, host, (size_t)M * sizeof(float2), cudaMemcpyHostToDevice);
 }
 
 cudaError_t launch_grid_pass(const cat_plan_s* p, const void* Q, const void* K, const void* V,
