@@ -1,5 +1,6 @@
 // Internal plan structure and kernel launchers of libcat (not part of the ABI).
 #pragma once
+#include <cstdlib>
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
@@ -198,6 +199,27 @@ cudaError_t allow_max_smem(K kernel) {
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              optin - (int)a.sharedSizeBytes);
   return e;
+}
+
+// Launch `kernel` as the programmatic dependent of the kernel ahead of it
+// on `st` (it may start before that one finishes; it calls pdl_wait before
+// using that kernel's output).  Returns the launch's status.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  // CAT_PDL=0: ordinary launches (the waits are then no-ops).
+  if (const char* e = std::getenv("CAT_PDL")) cfg.numAttrs = e[0] == '0' ? 0 : 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
 // Launchers (enqueue on plan->stream).  Each returns cudaGetLastError().

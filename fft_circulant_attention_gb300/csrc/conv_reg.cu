@@ -75,7 +75,7 @@ __device__ __forceinline__ void st_col_pair(T* p, float2 v, bool pair, bool alig
 // second page's circulant attention.
 template <typename T, int M, bool TW = true>
 __global__ void __launch_bounds__(512)
-conv_reg_kernel(const T* __restrict__ V, T* __restrict__ O, const float2* __restrict__ zf,
+conv_reg_kernel(const T* __restrict__ V, T* __restrict__ O, const float2* zf,
                 const float2* __restrict__ W, int D, int H, int dh, int npair, int P,
                 int groups) {
   constexpr int N = M * M;
@@ -86,25 +86,22 @@ conv_reg_kernel(const T* __restrict__ V, T* __restrict__ O, const float2* __rest
   const int bh = blockIdx.x / groups, grp = blockIdx.x - (blockIdx.x / groups) * groups;
   const int b = bh / H, h = bh - b * H;
   const int p = threadIdx.x % P, i = threadIdx.x / P;
-  // Twiddles and spectrum to shared memory, four loads of each in flight
-  // per thread (one round trip for N = 32² with 256 threads).
+  // Twiddles to shared memory, four loads in flight per thread (one round
+  // trip for N = 32² with 256 threads).  The spectrum follows the first
+  // transform: it is the kernel ahead's output (see pdl_wait).
   constexpr int kPro = 4;
-  for (int e0 = threadIdx.x; e0 < N; e0 += kPro * blockDim.x) {
-    float2 tv[kPro], zv[kPro];
+  if (TW) {
+    for (int e0 = threadIdx.x; e0 < N; e0 += kPro * blockDim.x) {
+      float2 tv[kPro];
 #pragma unroll
-    for (int u = 0; u < kPro; ++u) {
-      const int e = e0 + u * blockDim.x;
-      if (e < N) {
-        if (TW) tv[u] = __ldg(&W[(e / M) * (e % M)]);
-        zv[u] = __ldg(&zf[(size_t)bh * N + e]);
+      for (int u = 0; u < kPro; ++u) {
+        const int e = e0 + u * blockDim.x;
+        if (e < N) tv[u] = __ldg(&W[(e / M) * (e % M)]);
       }
-    }
 #pragma unroll
-    for (int u = 0; u < kPro; ++u) {
-      const int e = e0 + u * blockDim.x;
-      if (e < N) {
-        if (TW) tw[e] = tv[u];
-        zs[e] = zv[u];
+      for (int u = 0; u < kPro; ++u) {
+        const int e = e0 + u * blockDim.x;
+        if (e < N) tw[e] = tv[u];
       }
     }
   }
@@ -121,6 +118,22 @@ conv_reg_kernel(const T* __restrict__ V, T* __restrict__ O, const float2* __rest
   float2 a[M];
   ld_rows<T, M>(a, V + base, (size_t)M * D, (size_t)i * D, active, pair, aligned);
   dft<M, false>(a);
+  // V's loads and first transform may overlap the spectrum kernel ahead
+  // (launched as its programmatic dependent); its output is read only now.
+  pdl_wait();
+  for (int e0 = threadIdx.x; e0 < N; e0 += kPro * blockDim.x) {
+    float2 zv[kPro];
+#pragma unroll
+    for (int u = 0; u < kPro; ++u) {
+      const int e = e0 + u * blockDim.x;
+      if (e < N) zv[u] = ld_dep(&zf[(size_t)bh * N + e]);
+    }
+#pragma unroll
+    for (int u = 0; u < kPro; ++u) {
+      const int e = e0 + u * blockDim.x;
+      if (e < N) zs[e] = zv[u];
+    }
+  }
   __syncthreads();   // twiddles and spectrum ready
 #pragma unroll
   for (int k2 = 0; k2 < M; ++k2) buf[(k2 * M + i) * P + p] = TW ? cmul(a[k2], tw[i * M + k2]) : a[k2];
@@ -306,7 +319,7 @@ constexpr int kSpecRegThreads = 256;
 
 template <int M, bool TW = true>
 __global__ void __launch_bounds__(kSpecRegThreads)
-softmax_spectrum_reg(const float2* __restrict__ z, float* __restrict__ zs,
+softmax_spectrum_reg(const float2* z, float* __restrict__ zs,
                      float2* __restrict__ zf, const float2* __restrict__ W, int rows) {
   constexpr int N = M * M;
   constexpr int GL = M <= 8 ? 8 : (M <= 16 ? 16 : 32);
@@ -318,11 +331,15 @@ softmax_spectrum_reg(const float2* __restrict__ z, float* __restrict__ zs,
   // count.  Lane i reads its twiddles w_N^{i·k2} straight from the table.
   const int i = threadIdx.x % GL, r = threadIdx.x / GL;
   const int row = blockIdx.x * (blockDim.x / GL) + r;
+  // Launched as the score's programmatic dependent: let the product kernel
+  // behind launch, then wait for the scores.
+  pdl_trigger();
+  pdl_wait();
   const bool act = i < M && row < rows;
   const float2* src = z + (size_t)(row < rows ? row : 0) * N;
   float2 v[M];
 #pragma unroll
-  for (int n2 = 0; n2 < M; ++n2) v[n2] = act ? src[i + M * n2] : make_float2(-INFINITY, 0.f);
+  for (int n2 = 0; n2 < M; ++n2) v[n2] = act ? ld_dep(src + i + M * n2) : make_float2(-INFINITY, 0.f);
   float m = -INFINITY;
 #pragma unroll
   for (int n2 = 0; n2 < M; ++n2) m = fmaxf(m, v[n2].x);
@@ -390,16 +407,15 @@ static cudaError_t spectrum_reg_t(const cat_plan_s* p) {
   const int ctas = (rows + per - 1) / per;
   const size_t smem = (size_t)per * M * (M + 1) * sizeof(float2);
   switch (M) {
-#define CAT_M(m)                                                                            \
-  case m:                                                                                   \
-    softmax_spectrum_reg<m, TW><<<ctas, per * GL, smem, p->stream>>>(p->z2, p->zs,    \
-                                                                            p->zf, p->tw, rows); \
-    break;
+#define CAT_M(m)                                                                         \
+  case m:                                                                                \
+    return launch_dependent(softmax_spectrum_reg<m, TW>, dim3(ctas), dim3(per * GL), smem, \
+                            p->stream, (const float2*)p->z2, p->zs, p->zf,                 \
+                            (const float2*)p->tw, rows);
     CAT_M(8) CAT_M(14) CAT_M(16) CAT_M(32)
 #undef CAT_M
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 cudaError_t launch_softmax_spectrum_reg(const cat_plan_s* p) {
@@ -451,16 +467,15 @@ static cudaError_t launch_tw(const cat_plan_s* p, const T* V, T* O) {
   const dim3 block(M * P);
   const size_t smem = p->sm.smem;
   switch (M) {
-#define CAT_M(m)                                                                               \
-  case m:                                                                                      \
-    conv_reg_kernel<T, m, TW><<<ctas, block, smem, p->stream>>>(V, O, p->zf, p->tw, p->D, p->H, \
-                                                                p->dh, p->npair, P, groups);   \
-    break;
+#define CAT_M(m)                                                                             \
+  case m:                                                                                    \
+    return launch_dependent(conv_reg_kernel<T, m, TW>, dim3(ctas), block, smem, p->stream, V, \
+                            O, (const float2*)p->zf, (const float2*)p->tw, p->D, p->H, p->dh, \
+                            p->npair, P, groups);
     CAT_M(8) CAT_M(14) CAT_M(16) CAT_M(32)
 #undef CAT_M
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 template <typename T>

@@ -6,6 +6,30 @@
 
 namespace cat {
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialisation may start before the kernel ahead of it in the stream has
+// finished (once every CTA of that kernel has run pdl_trigger or exited);
+// pdl_wait blocks until that kernel has completed and its memory is
+// visible.  Launched the ordinary way, both are no-ops.  A kernel that is
+// launched this way calls pdl_wait before it touches memory the kernels
+// ahead of it write, and before it exits, so that completion stays
+// transitive along the stream.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// A load of the kernel ahead's output after pdl_wait.  A load through a
+// const __restrict__ pointer may be compiled as an invariant (read-only
+// cache) load and moved above the wait; this one is ordered after it.
+__device__ __forceinline__ float2 ld_dep(const float2* p) {
+  float2 v;
+  asm volatile("ld.global.v2.f32 {%0, %1}, [%2];"
+               : "=f"(v.x), "=f"(v.y)
+               : "l"(__cvta_generic_to_global(p))
+               : "memory");
+  return v;
+}
+
 __device__ __forceinline__ float ld_elem(const float* p) { return __ldg(p); }
 __device__ __forceinline__ float ld_elem(const __nv_bfloat16* p) {
   unsigned short u = __ldg(reinterpret_cast<const unsigned short*>(p));

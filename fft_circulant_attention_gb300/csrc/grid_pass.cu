@@ -165,6 +165,7 @@ __global__ void __launch_bounds__(kGpMaxThreads)
 gp_rows_fwd(const T* __restrict__ X0, const T* __restrict__ X1, const T* __restrict__ X2,
             float2* __restrict__ xs, size_t tstride, const float2* __restrict__ twm, int D,
             int H, int dh, int np, int bh0) {
+  pdl_trigger();   // the next pass may launch; it waits for this one
   constexpr int M = 32 * R;
   extern __shared__ float4 smem4[];
   const Smem<R> sm{reinterpret_cast<float2*>(smem4)};
@@ -196,8 +197,10 @@ gp_rows_fwd(const T* __restrict__ X0, const T* __restrict__ X1, const T* __restr
 // tsc[bhl][y][kx].
 template <int R>
 __global__ void __launch_bounds__(kGpMaxThreads)
-gp_cols_scores(const float2* __restrict__ qs, const float2* __restrict__ ks,
+gp_cols_scores(const float2* qs, const float2* ks,
                float2* __restrict__ tsc, const float2* __restrict__ twm, int np) {
+  pdl_trigger();
+  pdl_wait();      // launched as the previous pass's programmatic dependent
   constexpr int M = 32 * R, LS = M + 1;
   extern __shared__ float4 smem4[];
   float2* buf = reinterpret_cast<float2*>(smem4);   // Q's signals, then K's
@@ -237,9 +240,11 @@ gp_cols_scores(const float2* __restrict__ qs, const float2* __restrict__ ks,
 // stats[bhl][y] and the x-DFT of exp(a − m) to esp[bhl][y][slot].
 template <int R>
 __global__ void __launch_bounds__(32 * kGpRowsPerCta)
-gp_rows_scores(const float2* __restrict__ tsc, float2* __restrict__ esp,
+gp_rows_scores(const float2* tsc, float2* __restrict__ esp,
                float2* __restrict__ stats, float* __restrict__ aout,
                const float2* __restrict__ twm, int bh0, float scale) {
+  pdl_trigger();
+  pdl_wait();      // launched as the previous pass's programmatic dependent
   constexpr int M = 32 * R, LS = M + 1, RB = kGpRowsPerCta;
   extern __shared__ float4 smem4[];
   float2* buf = reinterpret_cast<float2*>(smem4);
@@ -287,9 +292,11 @@ gp_rows_scores(const float2* __restrict__ tsc, float2* __restrict__ esp,
 // multiplied by it and inverse y-transformed back into vs.
 template <int R>
 __global__ void __launch_bounds__(kGpMaxThreads)
-gp_cols_conv(float2* __restrict__ vs, const float2* __restrict__ esp,
-             const float2* __restrict__ stats, const float2* __restrict__ twm, int np,
+gp_cols_conv(float2* vs, const float2* esp,
+             const float2* stats, const float2* __restrict__ twm, int np,
              float invN) {
+  pdl_trigger();
+  pdl_wait();      // launched as the previous pass's programmatic dependent
   constexpr int M = 32 * R, LS = M + 1;
   extern __shared__ float4 smem4[];
   float2* sbuf = reinterpret_cast<float2*>(smem4);   // σ's column, then V's npair columns
@@ -353,8 +360,10 @@ gp_cols_conv(float2* __restrict__ vs, const float2* __restrict__ esp,
 // (2g, 2g + 1) by stage A.
 template <typename T, int R>
 __global__ void __launch_bounds__(kGpMaxThreads)
-gp_rows_out(const float2* __restrict__ vs, T* __restrict__ O, const float2* __restrict__ twm,
+gp_rows_out(const float2* vs, T* __restrict__ O, const float2* __restrict__ twm,
             int D, int H, int dh, int np, int bh0) {
+  pdl_trigger();
+  pdl_wait();      // launched as the previous pass's programmatic dependent
   constexpr int M = 32 * R;
   extern __shared__ float4 smem4[];
   const Smem<R> sm{reinterpret_cast<float2*>(smem4)};
@@ -447,19 +456,26 @@ cudaError_t run_chunk(const cat_plan_s* p, const T* Q, const T* K, const T* V, T
       Q, K, V, bf.xs, bf.tstride, bf.twm, p->D, p->H, p->dh, np, bh0);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  gp_cols_scores<R><<<dim3(M, nb), gp_threads(2 * np * R), smem_cols_scores(M, np), st>>>(
-      bf.xs, bf.xs + bf.tstride, bf.tsc, bf.twm, np);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // Passes 2-5 launch as programmatic dependents (each waits for the pass
+  // ahead at its start), which hides the launch gaps.
+  e = launch_dependent(gp_cols_scores<R>, dim3(M, nb), dim3(gp_threads(2 * np * R)),
+                       smem_cols_scores(M, np), st, (const float2*)bf.xs,
+                       (const float2*)(bf.xs + bf.tstride), bf.tsc, (const float2*)bf.twm, np);
+  if (e != cudaSuccess) return e;
   const float scale = 1.0f / ((float)p->dh * (float)(M * M));
-  gp_rows_scores<R><<<dim3(M / kGpRowsPerCta, nb), 32 * kGpRowsPerCta, smem_rows_scores(M), st>>>(
-      bf.tsc, fwd ? bf.esp : nullptr, bf.stats, aout, bf.twm, bh0, scale);
-  if ((e = cudaGetLastError()) != cudaSuccess || !fwd) return e;
-  gp_cols_conv<R><<<dim3(M, nb), gp_threads(np * R), smem_cols_conv(M, np), st>>>(
-      bf.xs + 2 * bf.tstride, bf.esp, bf.stats, bf.twm, np, 1.0f / (float)(M * M));
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  gp_rows_out<T, R><<<dim3(M, nb), gp_threads(np * R), smem_rows(M, np), st>>>(
-      bf.xs + 2 * bf.tstride, O, bf.twm, p->D, p->H, p->dh, np, bh0);
-  return cudaGetLastError();
+  e = launch_dependent(gp_rows_scores<R>, dim3(M / kGpRowsPerCta, nb), dim3(32 * kGpRowsPerCta),
+                       smem_rows_scores(M), st, (const float2*)bf.tsc,
+                       fwd ? bf.esp : (float2*)nullptr, bf.stats, aout, (const float2*)bf.twm,
+                       bh0, scale);
+  if (e != cudaSuccess || !fwd) return e;
+  e = launch_dependent(gp_cols_conv<R>, dim3(M, nb), dim3(gp_threads(np * R)),
+                       smem_cols_conv(M, np), st, bf.xs + 2 * bf.tstride,
+                       (const float2*)bf.esp, (const float2*)bf.stats, (const float2*)bf.twm, np,
+                       1.0f / (float)(M * M));
+  if (e != cudaSuccess) return e;
+  return launch_dependent(gp_rows_out<T, R>, dim3(M, nb), dim3(gp_threads(np * R)),
+                          smem_rows(M, np), st, (const float2*)(bf.xs + 2 * bf.tstride), O,
+                          (const float2*)bf.twm, p->D, p->H, p->dh, np, bh0);
 }
 
 template <typename T>

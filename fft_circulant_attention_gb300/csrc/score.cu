@@ -139,6 +139,7 @@ template <typename T, int HT, bool VEC>
 __global__ void __launch_bounds__(kScoreThreads)
 score_kernel(const T* __restrict__ X, const T* __restrict__ WA, float2* __restrict__ z,
              int N, int D, int H, int h0, int b0) {
+  pdl_trigger();   // the softmax kernel behind may launch (it waits for the scores)
   constexpr int HP = (HT + 3) & ~3;
   constexpr int TP = kScoreTokPerThread;
   extern __shared__ float4 ws4[];
@@ -230,6 +231,7 @@ template <typename T, int HT, int kSplit>
 __global__ void __launch_bounds__(kScoreThreads)
 score_split_kernel(const T* __restrict__ X, const T* __restrict__ WA, float2* __restrict__ z,
                    int N, int D, int H, int h0, int b0) {
+  pdl_trigger();   // the softmax kernel behind may launch (it waits for the scores)
   constexpr int HP = (HT + 3) & ~3;
   constexpr int V = Vec16<T>::n;
   constexpr int RUN = kChunk / V;   // vectors per fresh run
@@ -426,6 +428,7 @@ template <int NT>
 __global__ void __launch_bounds__(kMmaWarps * 32)
 score_mma_kernel(const __nv_bfloat16* __restrict__ X, const __nv_bfloat16* __restrict__ WA,
                  float2* __restrict__ z, int N, int D, int H, int h0, int HT, int b0) {
+  pdl_trigger();   // the softmax kernel behind may launch (it waits for the scores)
   extern __shared__ uint4 wsh4[];
   unsigned short* wt = reinterpret_cast<unsigned short*>(wsh4);
   const int ws = mma_wt_stride(D);
@@ -524,6 +527,7 @@ __global__ void __launch_bounds__(kTsThreads)
 score_tma_kernel(const __grid_constant__ CUtensorMap tmX, const __nv_bfloat16* __restrict__ WA,
                  float2* __restrict__ z, int N, int D, int H, int h0, int HT, int row0,
                  int rows_total, unsigned int* status) {
+  pdl_trigger();   // the softmax kernel behind may launch (it waits for the scores)
   extern __shared__ __align__(1024) unsigned char sm_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~(uintptr_t)1023);
