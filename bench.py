@@ -649,6 +649,10 @@ def profile_range(args, device):
         run = lambda: plan.forward(A, K, V, O)   # noqa: E731
     else:
         c = cfg_of(args.config)
+        if args.batches:
+            # A smaller case of the same workload (its first batches), for
+            # captures that replay each kernel many times.
+            c["B"] = min(c["B"], args.batches)
         A, K, V = (t.to(device) for t in synth.make_inputs(c["B"], c["N"], c["D"], c["H"],
                                                             c["dtype"], seed=0))
         plan = cat.Plan(c["B"], c["N"], c["D"], c["H"], c["dtype"], stream=stream)
@@ -825,6 +829,8 @@ def main():
     ap.add_argument("--backward-only", action="store_true",
                     help="time only cat_backward on --config (--steps calls) and print it")
     ap.add_argument("--sample-heads", type=int, default=0)
+    ap.add_argument("--batches", type=int, default=0,
+                    help="with --profile-range: run only the first this-many batches of --config")
     ap.add_argument("--profile-range", type=int, default=0,
                     help="run this many forwards of --config between cudaProfilerStart and "
                          "cudaProfilerStop (for an ncu range capture) and exit")

@@ -1,5 +1,5 @@
-// Register-resident DFT building blocks for lengths 1, 2, 4, 7, 8, 14, 16,
-// 32 and 64.
+// Register-resident DFT building blocks for lengths 1, 2, 3, 4, 7, 8, 12, 14,
+// 16, 32 and 64.
 //
 // The method they serve is the "FFT acceleration" design of the notes page
 // "CAT: Circular-Convolutional Attention for Sub-Quadratic Transformers"
@@ -7,7 +7,7 @@
 // exp(-2πi kn/R), inverse exp(+2πi kn/R), neither scaled.
 //
 // dft<R, INV>(a) transforms R values held in registers, in place, natural
-// order in and out.  Lengths 14, 16, 32 and 64 are split R = P·Q with
+// order in and out.  Lengths 12, 14, 16, 32 and 64 are split R = P·Q with
 // n = P·n1 + n2 and k = Q·k2 + k1:
 //     X[Q k2 + k1] = sum_n2 w_P^{n2 k2} · w_R^{n2 k1} · sum_n1 a[P n1 + n2] w_Q^{n1 k1},
 // i.e. P DFTs of length Q, a twiddle per (n2, k1), Q DFTs of length P.
@@ -130,12 +130,16 @@ __device__ __forceinline__ void dft(float2* a) {
   if constexpr (R == 1) {
   } else if constexpr (R == 2) {
     dft2<INV, Ops>(a);
+  } else if constexpr (R == 3) {
+    dft3<INV>(a);
   } else if constexpr (R == 4) {
     dft4<INV, Ops>(a);
   } else if constexpr (R == 7) {
     dft7<INV>(a);
   } else if constexpr (R == 8) {
     dft8<INV, Ops>(a);
+  } else if constexpr (R == 12) {
+    dft_pq<4, 3, INV, Ops>(a);
   } else if constexpr (R == 14) {
     dft_pq<2, 7, INV, Ops>(a);
   } else if constexpr (R == 16) {

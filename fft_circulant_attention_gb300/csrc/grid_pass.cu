@@ -25,15 +25,16 @@
 // correlation Re(IDFT(X̂·conj(Ŷ))) of two such signals is the sum of the two
 // channels' real correlations.
 //
-// Inside a CTA, a length-M DFT of S signals is two stages: a register
-// DFT-32 over each stride-R subsequence, times w_M^{e1·k2}, then a DFT-R
-// over adjacent slots, with the signals in shared memory (stride M + 1, odd,
-// so that column accesses hit distinct banks) between them.  The first
-// stage of a pass reads its input straight from global memory and the last
-// writes its output there, a warp's lanes on consecutive channel pairs.  With n = e1 + R·e2 and
-// k = k2 + 32·k1,
-//     X[k2 + 32·k1] = Σ_e1 w_R^{e1·k1} · w_M^{e1·k2} · Σ_e2 w_32^{e2·k2} x[e1 + R·e2],
-// so the spectrum lands in the slot order k ↦ k1 + R·k2.  The inverse runs
+// Inside a CTA, a length-M DFT (M = P·Q: 64 = 8·8, 96 = 12·8, 128 = 16·8)
+// of S signals is two stages: a register DFT-P over each stride-Q
+// subsequence, times w_M^{e1·k2}, then a DFT-Q over adjacent slots, with the
+// signals in shared memory (stride M + 1, odd, so that column accesses hit
+// distinct banks) between them.  The first stage of a pass reads its input
+// straight from global memory and the last writes its output there, a
+// warp's lanes on consecutive channel pairs.  With n = e1 + Q·e2 and
+// k = k2 + P·k1,
+//     X[k2 + P·k1] = Σ_e1 w_Q^{e1·k1} · w_M^{e1·k2} · Σ_e2 w_P^{e2·k2} x[e1 + Q·e2],
+// so the spectrum lands in the slot order k ↦ k1 + Q·k2.  The inverse runs
 // the stages in reverse, from that order back to natural order.  Spectra
 // are only ever multiplied with spectra of the same order, or inverted.
 #include <cuda_bf16.h>
@@ -76,56 +77,69 @@ __device__ __forceinline__ void batched(int count, Ld ld, St st) {
   }
 }
 
-// The two stages of a length-M DFT of S signals, M = 32·R.  Element n of
-// signal sig comes from ld(sig, n) and goes to st(sig, n, value), so a stage
-// reads from or writes to global memory or shared memory as the pass needs.
-// Tasks run signal-fastest, so that the lanes of a warp touch consecutive
-// signals: consecutive channel pairs in global memory, rows M + 1 apart (an
-// odd stride: distinct banks) in shared memory.  twm: w_M^m, m < M.
+// The split of a grid side M = 32·R into the two stages of its DFT,
+// M = P·Q: a register DFT of length P over stride-Q subsequences, then a
+// DFT of length Q over adjacent slots.  Short register transforms (12 or
+// 16 points, not 32) keep a thread's registers near 60, so that more warps
+// fit an SM.
+template <int R> struct Split;
+template <> struct Split<2> { static constexpr int P = 8, Q = 8; };
+template <> struct Split<3> { static constexpr int P = 12, Q = 8; };
+template <> struct Split<4> { static constexpr int P = 16, Q = 8; };
+
+// The two stages of a length-M DFT of S signals.  Element n of signal sig
+// comes from ld(sig, n) and goes to st(sig, n, value), so a stage reads from
+// or writes to global memory or shared memory as the pass needs.  Tasks run
+// signal-fastest, so that the lanes of a warp touch consecutive signals:
+// consecutive channel pairs in global memory, rows M + 1 apart (an odd
+// stride: distinct banks) in shared memory.  twm: w_M^m, m < M.
 //
-// Stage A, forward: task (sig, e1) transforms x[e1 + R·e2] over e2 (a
-// register DFT-32) and writes slot e1 + R·k2 times w_M^{e1·k2}.
+// Stage A, forward: task (sig, e1), e1 < Q, transforms x[e1 + Q·e2] over
+// e2 < P (a register DFT-P) and writes slot e1 + Q·k2 times w_M^{e1·k2}.
 template <int R, class Ld, class St>
 __device__ __forceinline__ void stage_a_fwd(int S, const float2* __restrict__ twm, Ld ld, St st) {
+  constexpr int P = Split<R>::P, Q = Split<R>::Q;
   const float rS = 1.0f / (float)S;
-  for (int t = threadIdx.x; t < S * R; t += blockDim.x) {
+  for (int t = threadIdx.x; t < S * Q; t += blockDim.x) {
     const int e1 = fdiv(t, rS), sig = t - e1 * S;
-    float2 a[32];
+    float2 a[P];
 #pragma unroll
-    for (int e2 = 0; e2 < 32; ++e2) a[e2] = ld(sig, e1 + R * e2);
-    dft<32, false>(a);
+    for (int e2 = 0; e2 < P; ++e2) a[e2] = ld(sig, e1 + Q * e2);
+    dft<P, false>(a);
 #pragma unroll
-    for (int k2 = 0; k2 < 32; ++k2) st(sig, e1 + R * k2, cmul(a[k2], __ldg(&twm[e1 * k2])));
+    for (int k2 = 0; k2 < P; ++k2) st(sig, e1 + Q * k2, cmul(a[k2], __ldg(&twm[e1 * k2])));
   }
 }
-// Stage A, inverse: slot e1 + R·k2 times conj w_M^{e1·k2}, the inverse
-// DFT-32 over k2, written to element e1 + R·e2.
+// Stage A, inverse: slot e1 + Q·k2 times conj w_M^{e1·k2}, the inverse
+// DFT-P over k2, written to element e1 + Q·e2.
 template <int R, class Ld, class St>
 __device__ __forceinline__ void stage_a_inv(int S, const float2* __restrict__ twm, Ld ld, St st) {
+  constexpr int P = Split<R>::P, Q = Split<R>::Q;
   const float rS = 1.0f / (float)S;
-  for (int t = threadIdx.x; t < S * R; t += blockDim.x) {
+  for (int t = threadIdx.x; t < S * Q; t += blockDim.x) {
     const int e1 = fdiv(t, rS), sig = t - e1 * S;
-    float2 a[32];
+    float2 a[P];
 #pragma unroll
-    for (int k2 = 0; k2 < 32; ++k2) a[k2] = cmulc(ld(sig, e1 + R * k2), __ldg(&twm[e1 * k2]));
-    dft<32, true>(a);
+    for (int k2 = 0; k2 < P; ++k2) a[k2] = cmulc(ld(sig, e1 + Q * k2), __ldg(&twm[e1 * k2]));
+    dft<P, true>(a);
 #pragma unroll
-    for (int e2 = 0; e2 < 32; ++e2) st(sig, e1 + R * e2, a[e2]);
+    for (int e2 = 0; e2 < P; ++e2) st(sig, e1 + Q * e2, a[e2]);
   }
 }
-// Stage B: task (sig, k2) applies the DFT-R (inverse: its conjugate) to the
-// R adjacent slots R·k2 .. R·k2 + R - 1.
+// Stage B: task (sig, k2), k2 < P, applies the DFT-Q (inverse: its
+// conjugate) to the Q adjacent slots Q·k2 .. Q·k2 + Q - 1.
 template <int R, bool INV, class Ld, class St>
 __device__ __forceinline__ void stage_b(int S, Ld ld, St st) {
+  constexpr int P = Split<R>::P, Q = Split<R>::Q;
   const float rS = 1.0f / (float)S;
-  for (int t = threadIdx.x; t < S * 32; t += blockDim.x) {
+  for (int t = threadIdx.x; t < S * P; t += blockDim.x) {
     const int k2 = fdiv(t, rS), sig = t - k2 * S;
-    float2 a[R];
+    float2 a[Q];
 #pragma unroll
-    for (int j = 0; j < R; ++j) a[j] = ld(sig, R * k2 + j);
-    dft_small<R, INV>(a);
+    for (int j = 0; j < Q; ++j) a[j] = ld(sig, Q * k2 + j);
+    dft_small<Q, INV>(a);
 #pragma unroll
-    for (int j = 0; j < R; ++j) st(sig, R * k2 + j, a[j]);
+    for (int j = 0; j < Q; ++j) st(sig, Q * k2 + j, a[j]);
   }
 }
 
@@ -452,13 +466,13 @@ cudaError_t run_chunk(const cat_plan_s* p, const T* Q, const T* K, const T* V, T
   cudaStream_t st = p->stream;
   const bool fwd = V != nullptr;
   const int ntens = fwd ? 3 : 2;
-  gp_rows_fwd<T, R><<<dim3(M, nb, ntens), gp_threads(np * R), smem_rows(M, np), st>>>(
+  gp_rows_fwd<T, R><<<dim3(M, nb, ntens), gp_threads(np * Split<R>::Q), smem_rows(M, np), st>>>(
       Q, K, V, bf.xs, bf.tstride, bf.twm, p->D, p->H, p->dh, np, bh0);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // Passes 2-5 launch as programmatic dependents (each waits for the pass
   // ahead at its start), which hides the launch gaps.
-  e = launch_dependent(gp_cols_scores<R>, dim3(M, nb), dim3(gp_threads(2 * np * R)),
+  e = launch_dependent(gp_cols_scores<R>, dim3(M, nb), dim3(gp_threads(2 * np * Split<R>::Q)),
                        smem_cols_scores(M, np), st, (const float2*)bf.xs,
                        (const float2*)(bf.xs + bf.tstride), bf.tsc, (const float2*)bf.twm, np);
   if (e != cudaSuccess) return e;
@@ -468,12 +482,12 @@ cudaError_t run_chunk(const cat_plan_s* p, const T* Q, const T* K, const T* V, T
                        fwd ? bf.esp : (float2*)nullptr, bf.stats, aout, (const float2*)bf.twm,
                        bh0, scale);
   if (e != cudaSuccess || !fwd) return e;
-  e = launch_dependent(gp_cols_conv<R>, dim3(M, nb), dim3(gp_threads(np * R)),
+  e = launch_dependent(gp_cols_conv<R>, dim3(M, nb), dim3(gp_threads(np * Split<R>::Q)),
                        smem_cols_conv(M, np), st, bf.xs + 2 * bf.tstride,
                        (const float2*)bf.esp, (const float2*)bf.stats, (const float2*)bf.twm, np,
                        1.0f / (float)(M * M));
   if (e != cudaSuccess) return e;
-  return launch_dependent(gp_rows_out<T, R>, dim3(M, nb), dim3(gp_threads(np * R)),
+  return launch_dependent(gp_rows_out<T, R>, dim3(M, nb), dim3(gp_threads(np * Split<R>::Q)),
                           smem_rows(M, np), st, (const float2*)(bf.xs + 2 * bf.tstride), O,
                           (const float2*)bf.twm, p->D, p->H, p->dh, np, bh0);
 }
@@ -505,9 +519,8 @@ cudaError_t run_all(const cat_plan_s* p, const void* Q, const void* K, const voi
 bool grid_pass_supported(int h, int w, int dh) {
   if (h != w || (h != 64 && h != 96 && h != 128)) return false;
   const int np = (dh + 1) / 2;
-  // Pass 2 holds Q's and K's columns of one slot in shared memory, and its
-  // stage A has 2·npair·M/32 tasks for at most 512 threads.
-  return smem_cols_scores(h, np) <= (size_t)200 * 1024 && 2 * np * (h / 32) <= kGpMaxThreads;
+  // Pass 2 holds Q's and K's columns of one slot in shared memory.
+  return smem_cols_scores(h, np) <= (size_t)200 * 1024;
 }
 
 int configure_grid_pass(cat_plan_s* p) {
