@@ -397,11 +397,112 @@ size_t spectrum_reg_smem(int M) {
   return (size_t)(kSpecRegThreads / GL) * M * (M + 1) * sizeof(float2);
 }
 
+// The same softmax and spectrum for N = 32², one (b, h) row per CTA of 128
+// threads: each 32-point DFT of the two steps is split over 4 threads
+// (n2 = q + 4m, k2 = ka + 8kb: thread q takes the DFT-8 over m, times
+// w_32^{q·ka}; the DFT-4 over q runs after a hand-over through shared
+// memory, thread q taking ka = 2q, 2q + 1), so that a row's serial chain is
+// about a quarter of the one-warp kernel's.  The softmax is spread over the
+// 128 threads.  Output as softmax_spectrum_reg: z* in natural order, the
+// spectrum at index k2 + 32·k1.
+constexpr int kSpecQ4Threads = 128;
+
+template <bool TW>
+__device__ __forceinline__ void spec_q4_step(const float2* __restrict__ in, float2* ex,
+                                             const float2* __restrict__ W, int g, int q,
+                                             float2 (&out)[8]) {
+  constexpr int LD = 36;
+  float2 a[8];
+#pragma unroll
+  for (int m = 0; m < 8; ++m) a[m] = in[g * LD + q + 4 * m];
+  dft<8, false>(a);
+  float2* mine = ex + g * 33;
+#pragma unroll
+  for (int ka = 0; ka < 8; ++ka) mine[q * 8 + ka] = ka == 0 || q == 0 ? a[ka] : cmul(a[ka], W[32 * q * ka]);
+  __syncwarp();
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int ka = 2 * q + h;
+    float2 c[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) c[r] = mine[r * 8 + ka];
+    dft_small<4, false>(c);
+#pragma unroll
+    for (int kb = 0; kb < 4; ++kb) out[4 * h + kb] = c[kb];   // bin ka + 8·kb
+  }
+}
+
+template <bool TW>
+__global__ void __launch_bounds__(kSpecQ4Threads)
+softmax_spectrum_q4(const float2* z, float* __restrict__ zs, float2* __restrict__ zf,
+                    const float2* __restrict__ W) {
+  constexpr int N = 1024, LD = 36;
+  __shared__ float2 sa[32 * LD];   // σ as [n1][n2], then the spectrum
+  __shared__ float2 sb[32 * LD];   // step 1's output as [k2][n1]
+  __shared__ float2 ex[32 * 33];   // the 4-thread hand-over, one block per column
+  __shared__ float red[32];
+  pdl_trigger();
+  pdl_wait();
+  const int t = threadIdx.x, row = blockIdx.x;
+  const float2* src = z + (size_t)row * N;
+  float2 v[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) v[j] = ld_dep(src + t + kSpecQ4Threads * j);
+  float m = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) m = fmaxf(m, v[j].x);
+  m = block_reduce<true>(m, red);
+  float e[8], sum = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    e[j] = exp_shifted(v[j], m);
+    sum += e[j];
+  }
+  sum = block_reduce<false>(sum, red);
+  const float inv = 1.0f / sum;
+  float* out = zs + (size_t)row * N;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int n = t + kSpecQ4Threads * j;
+    const float sg = e[j] * inv;
+    out[n] = sg;
+    sa[(n & 31) * LD + (n >> 5)] = make_float2(sg, 0.f);
+  }
+  __syncthreads();
+  const int g = t >> 2, q = t & 3;
+  float2 y[8];
+  spec_q4_step<TW>(sa, ex, W, g, q, y);   // column n1 = g: bins k2 = 2q + h + 8kb
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+#pragma unroll
+    for (int kb = 0; kb < 4; ++kb) {
+      const int k2 = 2 * q + h + 8 * kb;
+      const float2 w = y[4 * h + kb];
+      sb[k2 * LD + g] = TW ? cmul(w, W[g * k2]) : w;
+    }
+  __syncthreads();
+  spec_q4_step<TW>(sb, ex, W, g, q, y);   // k2 = g: bins k1 = 2q + h + 8kb
+  const float invN = 1.0f / (float)N;
+  float2* so = sa;                         // step 1 is done with sa
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+#pragma unroll
+    for (int kb = 0; kb < 4; ++kb) so[g + 32 * (2 * q + h + 8 * kb)] = cscale(y[4 * h + kb], invN);
+  __syncthreads();
+  float2* spec = zf + (size_t)row * N;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) spec[t + kSpecQ4Threads * j] = so[t + kSpecQ4Threads * j];
+}
+
 template <bool TW>
 static cudaError_t spectrum_reg_t(const cat_plan_s* p) {
   const int rows = p->B * p->H;
   if (rows == 0) return cudaSuccess;
   const int M = p->sm.reg_m;
+  if (M == 32)
+    return launch_dependent(softmax_spectrum_q4<TW>, dim3(rows), dim3(kSpecQ4Threads), 0,
+                            p->stream, (const float2*)p->z2, p->zs, p->zf,
+                            (const float2*)p->tw);
   const int GL = M <= 8 ? 8 : (M <= 16 ? 16 : 32);
   const int per = spectrum_reg_rows(M, rows, p->sms);
   const int ctas = (rows + per - 1) / per;
