@@ -233,6 +233,7 @@ __global__ void __launch_bounds__(kSmBwThreads)
 softmax_bw_kernel(const float* __restrict__ zs, const float* __restrict__ dzs,
                   float* __restrict__ dz, int N) {
   __shared__ double red[kSmBwThreads / 32];
+  __shared__ float total;
   const size_t off = (size_t)blockIdx.x * N;
   float part = 0.f;
   for (int n = threadIdx.x; n < N; n += blockDim.x) part = fmaf(zs[off + n], dzs[off + n], part);
@@ -243,9 +244,15 @@ softmax_bw_kernel(const float* __restrict__ zs, const float* __restrict__ dzs,
   const int nw = (blockDim.x + 31) >> 5;
   if (lane == 0) red[warp] = s;
   __syncthreads();
-  double tot = 0.0;
-  for (int w = 0; w < nw; ++w) tot += red[w];
-  const float sf = (float)tot;
+  // One thread adds the warps' sums in order (fp64 is a slow pipe on this
+  // GPU: the sum is done once, not by every thread), then shares it.
+  if (threadIdx.x == 0) {
+    double tot = 0.0;
+    for (int w = 0; w < nw; ++w) tot += red[w];
+    total = (float)tot;
+  }
+  __syncthreads();
+  const float sf = total;
   for (int n = threadIdx.x; n < N; n += blockDim.x) dz[off + n] = zs[off + n] * (dzs[off + n] - sf);
 }
 

@@ -207,18 +207,12 @@ corr_reg_kernel(const T* __restrict__ Q, const T* __restrict__ K, float2* __rest
     // One signal's M values in registers at a time: Q's transforms go back
     // to shared memory and K's product reads them there.
     float2 a[M];
-#pragma unroll
-    for (int n2 = 0; n2 < M; ++n2)
-      a[n2] = active ? ld_col_pair(Q + base + (size_t)(i + M * n2) * D, pair, aligned)
-                     : make_float2(0.f, 0.f);
+    ld_rows<T, M>(a, Q + base, (size_t)M * D, (size_t)i * D, active, pair, aligned);
     dft<M, false>(a);
     __syncthreads();   // the previous pass's sums have read bq; twiddles ready
 #pragma unroll
     for (int k2 = 0; k2 < M; ++k2) bq[(k2 * M + i) * P + p] = TW ? cmul(a[k2], tw[i * M + k2]) : a[k2];
-#pragma unroll
-    for (int n2 = 0; n2 < M; ++n2)
-      a[n2] = active ? ld_col_pair(K + base + (size_t)(i + M * n2) * D, pair, aligned)
-                     : make_float2(0.f, 0.f);
+    ld_rows<T, M>(a, K + base, (size_t)M * D, (size_t)i * D, active, pair, aligned);
     dft<M, false>(a);
 #pragma unroll
     for (int k2 = 0; k2 < M; ++k2) bk[(k2 * M + i) * P + p] = TW ? cmul(a[k2], tw[i * M + k2]) : a[k2];
