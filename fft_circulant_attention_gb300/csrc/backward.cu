@@ -599,6 +599,7 @@ cudaError_t launch_backward_dz(const cat_plan_s* p, const void* G, const void* V
   const char* env = std::getenv("CAT_BW_REG");
   const bool reg = !p->bw.fast && !p->twod && p->path == PATH_SMEM && p->sm.reg_m > 0 &&
                    !(env && std::strcmp(env, "0") == 0);
+  if (reg && corr_reg_split_fits(p)) return launch_corr_reg_split(p, G, V);
   const cudaError_t e = p->bw.fast ? corr_fast(p, G, V)
       : reg           ? launch_corr_reg(p, G, V, p->bw_dzs)
       : p->dtype == 1 ? corr_t<__nv_bfloat16, true>(p, (const __nv_bfloat16*)G, (const __nv_bfloat16*)V)

@@ -240,6 +240,12 @@ cudaError_t launch_scores2d_reg(const cat_plan_s* p, const void* Q, const void* 
 // Backward correlation dz*[b, h, k] = Σ_c Σ_i G[i, c] V[(i - k) mod N, c] into
 // dzs by the register transform, for N = reg_m² on the shared-memory path.
 cudaError_t launch_corr_reg(const cat_plan_s* p, const void* G, const void* V, float* dzs);
+// At N = 32² (1-D) the correlation splits each row's pairs over 4 CTAs whose
+// partial spectra (in the backward scratch, when it holds them) a finishing
+// kernel adds, inverts and turns into dz* and dz (the softmax backward
+// included): whether that fits, and the launch.
+bool corr_reg_split_fits(const cat_plan_s* p);
+cudaError_t launch_corr_reg_split(const cat_plan_s* p, const void* G, const void* V);
 int conv_reg_pairs(int M);
 size_t conv_reg_smem(int M, int P);
 cudaError_t launch_fourstep_conv(const cat_plan_s* p, const void* V, void* O);

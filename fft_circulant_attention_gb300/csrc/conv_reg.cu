@@ -184,22 +184,28 @@ template <typename T, int M, bool TW>
 __global__ void __launch_bounds__(512)
 corr_reg_kernel(const T* __restrict__ Q, const T* __restrict__ K, float2* __restrict__ z2,
                 float* __restrict__ out, const float2* __restrict__ W, int D, int H, int dh,
-                int npair, int P, float scale) {
+                int npair, int P, float scale, float2* __restrict__ part, int G) {
   constexpr int N = M * M;
   extern __shared__ float4 smem4[];
   float2* bq = reinterpret_cast<float2*>(smem4);   // [M][M][P] Q pairs, then products
   float2* bk = bq + N * P;                          // [M][M][P] K pairs
   float2* S = bk + N * P;                           // [k2][k1] running sum
   float2* tw = S + N;                               // TW: tw[n1·M + k2] = w_N^{n1·k2}
-  const int bh = blockIdx.x, b = bh / H, h = bh - b * H;
+  // With part (G > 1), CTA gi of the (b, h) row takes its share of the
+  // pairs (whole groups of P) and leaves its partial sum S in part instead
+  // of inverting it; a finishing kernel adds the G partials in order.
+  const int bh = blockIdx.x / G, gi = blockIdx.x - bh * G;
+  const int b = bh / H, h = bh - b * H;
+  const int share = (npair + P * G - 1) / (P * G) * P;
+  const int pbeg = gi * share, pend = min(npair, pbeg + share);
   const int p = threadIdx.x % P, i = threadIdx.x / P;
   for (int e = threadIdx.x; e < N; e += blockDim.x) {
     S[e] = make_float2(0.f, 0.f);
     if (TW) tw[e] = __ldg(&W[(e / M) * (e % M)]);
   }
-  for (int g0 = 0; g0 < npair; g0 += P) {
+  for (int g0 = pbeg; g0 < pend; g0 += P) {
     const int g = g0 + p;
-    const bool active = g < npair;
+    const bool active = g < pend;
     const bool pair = 2 * g + 1 < dh;
     const int col = h * dh + 2 * (active ? g : 0);
     const bool aligned = (col & 1) == 0 && (D & 1) == 0;
@@ -237,6 +243,11 @@ corr_reg_kernel(const T* __restrict__ Q, const T* __restrict__ K, float2* __rest
     }
   }
   __syncthreads();
+  if (part) {
+    float2* dst = part + (size_t)blockIdx.x * N;   // [k2][k1], as S
+    for (int e = threadIdx.x; e < N; e += blockDim.x) dst[e] = S[e];
+    return;
+  }
   // The inverse of the one summed signal, on threads t < M.
   const int t = threadIdx.x;
   float2 a[M];
@@ -267,14 +278,14 @@ size_t corr_reg_smem(int M, int P) {
 
 template <typename T, bool TW>
 static cudaError_t corr_t(const cat_plan_s* p, const T* A, const T* Bm, float2* z2, float* out,
-                          float scale) {
+                          float scale, float2* part = nullptr, int G = 1) {
   const int M = p->sm.reg_m, P = p->sm.G;
   const size_t smem = corr_reg_smem(M, P);
   switch (M) {
 #define CAT_M(m)                                                                              \
   case m:                                                                                     \
-    corr_reg_kernel<T, m, TW><<<p->B * p->H, m * P, smem, p->stream>>>(                        \
-        A, Bm, z2, out, p->tw, p->D, p->H, p->dh, p->npair, P, scale);                        \
+    corr_reg_kernel<T, m, TW><<<p->B * p->H * G, m * P, smem, p->stream>>>(                    \
+        A, Bm, z2, out, p->tw, p->D, p->H, p->dh, p->npair, P, scale, part, G);               \
     break;
     CAT_M(8) CAT_M(14) CAT_M(16) CAT_M(32)
 #undef CAT_M
@@ -400,8 +411,13 @@ size_t spectrum_reg_smem(int M) {
 // 128 threads.  Output as softmax_spectrum_reg: z* in natural order, the
 // spectrum at index k2 + 32·k1.
 constexpr int kSpecQ4Threads = 128;
+// CTAs per (b, h) row of the split register correlation (N = 32²).
+constexpr int kCorrSplitG = 4;
 
-template <bool TW>
+// One 32-point DFT (INV: its unscaled inverse) of column g of `in` ([g][n]
+// with row stride 36), split over the 4 threads q of the column; thread q
+// ends with bins 2q + h + 8kb in out[4h + kb].  W: the length-1024 table.
+template <bool INV>
 __device__ __forceinline__ void spec_q4_step(const float2* __restrict__ in, float2* ex,
                                              const float2* __restrict__ W, int g, int q,
                                              float2 (&out)[8]) {
@@ -409,10 +425,11 @@ __device__ __forceinline__ void spec_q4_step(const float2* __restrict__ in, floa
   float2 a[8];
 #pragma unroll
   for (int m = 0; m < 8; ++m) a[m] = in[g * LD + q + 4 * m];
-  dft<8, false>(a);
+  dft<8, INV>(a);
   float2* mine = ex + g * 33;
 #pragma unroll
-  for (int ka = 0; ka < 8; ++ka) mine[q * 8 + ka] = ka == 0 || q == 0 ? a[ka] : cmul(a[ka], W[32 * q * ka]);
+  for (int ka = 0; ka < 8; ++ka)
+    mine[q * 8 + ka] = ka == 0 || q == 0 ? a[ka] : twr<INV>(a[ka], W[32 * q * ka]);
   __syncwarp();
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
@@ -420,7 +437,7 @@ __device__ __forceinline__ void spec_q4_step(const float2* __restrict__ in, floa
     float2 c[4];
 #pragma unroll
     for (int r = 0; r < 4; ++r) c[r] = mine[r * 8 + ka];
-    dft_small<4, false>(c);
+    dft_small<4, INV>(c);
 #pragma unroll
     for (int kb = 0; kb < 4; ++kb) out[4 * h + kb] = c[kb];   // bin ka + 8·kb
   }
@@ -465,7 +482,7 @@ softmax_spectrum_q4(const float2* z, float* __restrict__ zs, float2* __restrict_
   __syncthreads();
   const int g = t >> 2, q = t & 3;
   float2 y[8];
-  spec_q4_step<TW>(sa, ex, W, g, q, y);   // column n1 = g: bins k2 = 2q + h + 8kb
+  spec_q4_step<false>(sa, ex, W, g, q, y);   // column n1 = g: bins k2 = 2q + h + 8kb
 #pragma unroll
   for (int h = 0; h < 2; ++h)
 #pragma unroll
@@ -475,7 +492,7 @@ softmax_spectrum_q4(const float2* z, float* __restrict__ zs, float2* __restrict_
       sb[k2 * LD + g] = TW ? cmul(w, W[g * k2]) : w;
     }
   __syncthreads();
-  spec_q4_step<TW>(sb, ex, W, g, q, y);   // k2 = g: bins k1 = 2q + h + 8kb
+  spec_q4_step<false>(sb, ex, W, g, q, y);   // k2 = g: bins k1 = 2q + h + 8kb
   const float invN = 1.0f / (float)N;
   float2* so = sa;                         // step 1 is done with sa
 #pragma unroll
@@ -486,6 +503,104 @@ softmax_spectrum_q4(const float2* z, float* __restrict__ zs, float2* __restrict_
   float2* spec = zf + (size_t)row * N;
 #pragma unroll
   for (int j = 0; j < 8; ++j) spec[t + kSpecQ4Threads * j] = so[t + kSpecQ4Threads * j];
+}
+
+// The backward's correlation at N = 32², finished: the G partial spectra
+// of a (b, h) row (S[k2][k1], from corr_reg_kernel's partial mode) added in
+// the order g = 0, 1, …; the inverse DFT (over k1, conjugate twiddle
+// w_N^{-n1·k2}, over k2; each 32-point DFT split over 4 threads as in
+// softmax_spectrum_q4); dz* = Re/N; then the softmax backward
+// dz = z*⊙(dz* − ⟨z*, dz*⟩), the threads' fp32 partial sums added in fp64 in
+// a fixed order.  One row per CTA of 128 threads.
+__global__ void __launch_bounds__(kSpecQ4Threads)
+corr_finish_q4(const float2* __restrict__ part, int G, const float* __restrict__ zs,
+               float* __restrict__ dzs, float* __restrict__ dz,
+               const float2* __restrict__ W) {
+  constexpr int N = 1024, LD = 36;
+  __shared__ float2 sa[32 * LD];   // S as [k2][k1], then dz* in natural order
+  __shared__ float2 sb[32 * LD];   // step 1's output as [n1][k2]
+  __shared__ float2 ex[32 * 33];
+  __shared__ double red[kSpecQ4Threads / 32];
+  __shared__ float total;
+  const int t = threadIdx.x, row = blockIdx.x;
+  const float2* src = part + (size_t)row * G * N;
+  float2 acc[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) acc[j] = make_float2(0.f, 0.f);
+  for (int g = 0; g < G; ++g) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] = cadd(acc[j], src[(size_t)g * N + t + kSpecQ4Threads * j]);
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int e = t + kSpecQ4Threads * j;   // e = k2·32 + k1
+    sa[(e >> 5) * LD + (e & 31)] = acc[j];
+  }
+  __syncthreads();
+  const int g = t >> 2, q = t & 3;
+  float2 y[8];
+  spec_q4_step<true>(sa, ex, W, g, q, y);   // k2 = g: bins n1 = 2q + h + 8kb
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+#pragma unroll
+    for (int kb = 0; kb < 4; ++kb) {
+      const int n1 = 2 * q + h + 8 * kb;
+      sb[n1 * LD + g] = cmulc(y[4 * h + kb], W[n1 * g]);
+    }
+  __syncthreads();
+  spec_q4_step<true>(sb, ex, W, g, q, y);   // n1 = g: bins n2 = 2q + h + 8kb
+  float* flat = reinterpret_cast<float*>(sa);   // dz*[n1 + 32·n2]
+  const float invN = 1.0f / (float)N;
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+#pragma unroll
+    for (int kb = 0; kb < 4; ++kb) flat[g + 32 * (2 * q + h + 8 * kb)] = y[4 * h + kb].x * invN;
+  __syncthreads();
+  const size_t off = (size_t)row * N;
+  float d[8], zv[8], pt = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int n = t + kSpecQ4Threads * j;
+    d[j] = flat[n];
+    zv[j] = zs[off + n];
+    dzs[off + n] = d[j];
+    pt = fmaf(zv[j], d[j], pt);
+  }
+  double sd = pt;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sd += __shfl_xor_sync(0xffffffffu, sd, o);
+  if ((t & 31) == 0) red[t >> 5] = sd;
+  __syncthreads();
+  if (t == 0) {
+    double tot = 0.0;
+    for (int w = 0; w < kSpecQ4Threads / 32; ++w) tot += red[w];
+    total = (float)tot;
+  }
+  __syncthreads();
+  const float sf = total;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) dz[off + t + kSpecQ4Threads * j] = zv[j] * (d[j] - sf);
+}
+
+bool corr_reg_split_fits(const cat_plan_s* p) {
+  return p->sm.reg_m == 32 && !p->twod &&
+         (size_t)p->B * p->H * kCorrSplitG * p->N * sizeof(float2) <= p->bw.scratch_bytes;
+}
+
+cudaError_t launch_corr_reg_split(const cat_plan_s* p, const void* G, const void* V) {
+  const int rows = p->B * p->H;
+  if (rows == 0) return cudaSuccess;
+  const float scale = 1.0f / (float)p->N;
+  float2* part = p->bw_scr;
+  cudaError_t e = p->dtype == 1
+      ? corr_t<__nv_bfloat16, true>(p, (const __nv_bfloat16*)G, (const __nv_bfloat16*)V, nullptr,
+                                    nullptr, scale, part, kCorrSplitG)
+      : corr_t<float, true>(p, (const float*)G, (const float*)V, nullptr, nullptr, scale, part,
+                            kCorrSplitG);
+  if (e != cudaSuccess) return e;
+  corr_finish_q4<<<rows, kSpecQ4Threads, 0, p->stream>>>(part, kCorrSplitG, p->zs, p->bw_dzs,
+                                                         p->bw_dz, p->tw);
+  return cudaGetLastError();
 }
 
 template <bool TW>

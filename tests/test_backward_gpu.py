@@ -249,11 +249,13 @@ def test_backward_empty_batch():
 
 @pytest.mark.parametrize("B,N,D,H,dtype", [(2, 64, 32, 2, "f32"), (4, 196, 384, 6, "f32"),
                                            (1, 256, 64, 2, "f32"), (2, 1024, 768, 12, "bf16"),
-                                           (3, 196, 30, 2, "bf16")])
+                                           (3, 196, 30, 2, "bf16"), (1, 1024, 75, 5, "f32")])
 def test_register_correlation_matches_block_passes(B, N, D, H, dtype, monkeypatch):
-    """For N = M² the correlation dz* runs in the register kernel; it agrees
-    with the block-FFT passes (CAT_BW_REG=0) and the oracle within the dz*
-    bound."""
+    """For N = M² the correlation dz* runs in the register kernel (at
+    N = 1024 split over 4 CTAs a row, their partial spectra added, inverted
+    and turned into dz by a finishing kernel; head width 15 leaves three of
+    the four CTAs without pairs); it agrees with the block-FFT passes
+    (CAT_BW_REG=0) and the oracle within the dz* and dz bounds."""
     X, WA, V = synth.make_inputs(B, N, D, H, dtype, seed=N + 3)
     G = synth.make_grad(B, N, D, dtype, seed=N + 3)
     Xd, Wd, Vd, Gd = to_dev(X, WA, V, G)
@@ -263,8 +265,10 @@ def test_register_correlation_matches_block_passes(B, N, D, H, dtype, monkeypatc
         with cat.Plan(B, N, D, H, dtype) as plan:
             dzs, dz = plan.backward_dz(Xd, Wd, Vd, Gd)
             plan.sync()
-        got[reg] = dzs.double().cpu().numpy()
-    ref = oracle.backward(X, WA, V, G, mode="direct" if B * N * N * D <= 2e9 else "fft")["dzs"]
+        got[reg] = (dzs.double().cpu().numpy(), dz.double().cpu().numpy())
+    full = oracle.backward(X, WA, V, G, mode="direct" if B * N * N * D <= 2e9 else "fft")
+    ref = full["dzs"]
     tol = DZS_TOL * np.abs(ref).max(axis=-1, keepdims=True)
     for reg in ("1", "0"):
-        assert (np.abs(got[reg] - ref) <= tol).all(), reg
+        assert (np.abs(got[reg][0] - ref) <= tol).all(), reg
+        check_dz(got[reg][1], full["dz"], full["zs"], ref, tol)
