@@ -201,7 +201,11 @@ template <typename T>
 __global__ void __launch_bounds__(kPipeWarps * 32)
 fsf_pass_a32(const __grid_constant__ CUtensorMap tmV, float2* __restrict__ scr,
              const float2* __restrict__ W, int N, int D, int H, int bh0, int nb,
-             unsigned int* status) {
+             unsigned int* status, const __grid_constant__ CUtensorMap tmV2,
+             float2* __restrict__ scr2, int ntens) {
+  // ntens = 2: a second tensor (tmV2 into scr2) in the same launch, its
+  // items after the first's (the backward's correlation transforms dO and V
+  // together).
   using P = PipeA<T>;
   extern __shared__ __align__(128) unsigned char sm[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -213,15 +217,17 @@ fsf_pass_a32(const __grid_constant__ CUtensorMap tmV, float2* __restrict__ scr,
   mbar_fence_init();
   __syncwarp();
   const int gw = blockIdx.x * kPipeWarps + warp, G = gridDim.x * kPipeWarps;
-  const int items = nb * kFastN1;
+  const int items1 = nb * kFastN1, items = ntens * items1;
   const uint64_t keep = policy_evict_last(), stream = policy_evict_first();
   auto issue = [&](int s, int item) {
     if (lane == 0) {
       fence_proxy_async_smem();   // the warp's reads of this stage come first
-      const int bh = bh0 + item % nb, n1 = item / nb;
+      const int second = item >= items1, it1 = item - second * items1;
+      const int bh = bh0 + it1 % nb, n1 = it1 / nb;
       const int b = bh / H, h = bh - b * H;
       mbar_expect_tx(bar + s, 32 * P::kRowBytes);
-      tma_load_4d_hint(stage + s * 32 * P::kRowBytes, &tmV, h * 64, n1, 0, b, bar + s, stream);
+      tma_load_4d_hint(stage + s * 32 * P::kRowBytes, second ? &tmV2 : &tmV, h * 64, n1, 0, b,
+                       bar + s, stream);
     }
   };
 #pragma unroll
@@ -231,7 +237,9 @@ fsf_pass_a32(const __grid_constant__ CUtensorMap tmV, float2* __restrict__ scr,
   for (int item = gw; item < items; item += G, ++it) {
     const int s = it % P::kStages;
     if (!mbar_wait(bar + s, (it / P::kStages) & 1, status, 0x501)) return;
-    const int bhl = item % nb, n1 = item / nb;
+    const int second = item >= items1, it1 = item - second * items1;
+    float2* dst = second ? scr2 : scr;
+    const int bhl = it1 % nb, n1 = it1 / nb;
     const float2 tw = __ldg(&W[(size_t)n1 * lane]);   // w_N^{n1·k2} for k2 = lane
     const T* tile = reinterpret_cast<const T*>(stage + s * 32 * P::kRowBytes) + 2 * lane;
     float2 a[32];
@@ -245,7 +253,7 @@ fsf_pass_a32(const __grid_constant__ CUtensorMap tmV, float2* __restrict__ scr,
     __syncwarp();
 #pragma unroll
     for (int k2 = 0; k2 < 32; ++k2)
-      st_hint(scr + scr_idx(bhl, 32, k2, n1, lane), cmul(a[k2], twrow[k2]), keep);
+      st_hint(dst + scr_idx(bhl, 32, k2, n1, lane), cmul(a[k2], twrow[k2]), keep);
     __syncwarp();
   }
 }
@@ -963,7 +971,7 @@ static cudaError_t chunk_t(const cat_plan_s* p, const T* V, T* O, int bh0, int n
           int grid = (items + kPipeWarps - 1) / kPipeWarps;
           if (grid > per_sm * p->sms) grid = per_sm * p->sms;
           fsf_pass_a32<T><<<grid, kPipeWarps * 32, PipeA<T>::kSmem, st>>>(
-              *tmV, scr, p->tw, p->N, p->D, p->H, bh0, nb, p->status);
+              *tmV, scr, p->tw, p->N, p->D, p->H, bh0, nb, p->status, *tmV, scr, 1);
         } else {
           int grid = (items + PipeC::kWarps - 1) / PipeC::kWarps;
           if (grid > 2 * p->sms) grid = 2 * p->sms;
@@ -1038,7 +1046,7 @@ static cudaError_t pass_a_t(const cat_plan_s* p, const T* V, int bh0, int nb, fl
       int grid = (nb * kFastN1 + kPipeWarps - 1) / kPipeWarps;
       if (grid > per_sm * p->sms) grid = per_sm * p->sms;
       fsf_pass_a32<T><<<grid, kPipeWarps * 32, PipeA<T>::kSmem, st>>>(
-          tmV, scr, p->tw, p->N, p->D, p->H, bh0, nb, p->status);
+          tmV, scr, p->tw, p->N, p->D, p->H, bh0, nb, p->status, tmV, scr, 1);
       break;
     }
     case 64: launch_ac<T, 64>(p, V, nullptr, scr, bh0, nb, true, st); break;
@@ -1048,10 +1056,32 @@ static cudaError_t pass_a_t(const cat_plan_s* p, const T* V, int bh0, int nb, fl
   return cudaGetLastError();
 }
 
+template <typename T>
+static cudaError_t pass_a32_pair(const cat_plan_s* p, const T* A, const T* Bm, int bh0, int nb,
+                                 float2* s0, float2* s1, cudaStream_t st) {
+  CUtensorMap tmA, tmB;
+  if (!encode_v_map(p, A, &tmA) || !encode_v_map(p, Bm, &tmB)) return cudaErrorInvalidValue;
+  const int per_sm = PipeA<T>::kSmem <= (113u << 10) ? 2 : 1;
+  int grid = (2 * nb * kFastN1 + kPipeWarps - 1) / kPipeWarps;
+  if (grid > per_sm * p->sms) grid = per_sm * p->sms;
+  fsf_pass_a32<T><<<grid, kPipeWarps * 32, PipeA<T>::kSmem, st>>>(
+      tmA, s0, p->tw, p->N, p->D, p->H, bh0, nb, p->status, tmB, s1, 2);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_fast_corr(const cat_plan_s* p, const void* G, const void* V, float2* y,
                              int bh0, int nb, cudaStream_t st, float2* s0, float2* s1) {
   if (!s0) s0 = p->scratch;
   if (!s1) s1 = p->scratch + p->scratch_bytes / 2 / sizeof(float2);
+  if (p->fs.N2 == 32) {
+    // dO into s0 and V into s1 as one launch.
+    cudaError_t e = p->dtype == 1
+        ? pass_a32_pair(p, (const __nv_bfloat16*)G, (const __nv_bfloat16*)V, bh0, nb, s0, s1, st)
+        : pass_a32_pair(p, (const float*)G, (const float*)V, bh0, nb, s0, s1, st);
+    if (e != cudaSuccess) return e;
+    fsf_corr_b<<<nb * p->fs.N2, 256, kSmemCorrB, st>>>(s0, s1, y, p->tabs, p->fs.N2);
+    return cudaGetLastError();
+  }
   cudaError_t e = p->dtype == 1
       ? pass_a_t(p, (const __nv_bfloat16*)G, bh0, nb, s0, st)
       : pass_a_t(p, (const float*)G, bh0, nb, s0, st);
