@@ -137,6 +137,7 @@ void free_plan(cat_plan_s* p) {
   }
   if (p->ev_fork) cudaEventDestroy(p->ev_fork);
   if (p->gexec) cudaGraphExecDestroy(p->gexec);
+  if (p->bgexec) cudaGraphExecDestroy(p->bgexec);
   if (p->cap) cudaStreamDestroy(p->cap);
   cudaFree(p->z2);
   cudaFree(p->zs);
@@ -1145,6 +1146,63 @@ int cat_forward_host(cat_plan_t p, const void* X, const void* WA, const void* V,
   return map_cuda(e);
 }
 
+namespace {
+
+// The fast path's backward: score, softmax, the correlation and the softmax
+// backward, then dV = circ(z*)^T dO by the forward's overlapped schedule on
+// the scores reversed, with dW_A and dX (which need only dz) on the plan's
+// stream beside its chunks.
+cudaError_t backward_fast_schedule(cat_plan_s* p, const void* X, const void* WA, const void* V,
+                                   const void* dO, void* dX, void* dWA, void* dV) {
+  if (run_backward_front(p, X, WA, V, dO) != CAT_OK) return cudaErrorLaunchFailure;
+  cudaError_t e = cat::launch_reverse_scores(p);
+  const std::function<cudaError_t()> dense = [&]() {
+    return cat::launch_backward_dense(p, X, WA, dX, dWA);
+  };
+  if (e == cudaSuccess) e = run_fast_overlapped(p, nullptr, nullptr, dO, dV, false, &dense);
+  return e;
+}
+
+// The same schedule through a CUDA graph, captured on the private stream
+// as the forward's is, and replayed while the call's pointers stay the same.
+cudaError_t launch_backward_graph(cat_plan_s* p, const void* X, const void* WA, const void* V,
+                                  const void* dO, void* dX, void* dWA, void* dV) {
+  const void* ptrs[7] = {X, WA, V, dO, dX, dWA, dV};
+  bool same = p->bgexec != nullptr;
+  for (int k = 0; k < 7 && same; ++k) same = ptrs[k] == p->bgp[k];
+  if (!same) {
+    cudaStream_t saved = p->stream;
+    p->stream = p->cap;
+    cudaGraph_t g = nullptr;
+    cudaError_t e = cudaStreamBeginCapture(p->cap, cudaStreamCaptureModeThreadLocal);
+    if (e == cudaSuccess) {
+      const cudaError_t e1 = backward_fast_schedule(p, X, WA, V, dO, dX, dWA, dV);
+      const cudaError_t e2 = cudaStreamEndCapture(p->cap, &g);
+      e = e1 != cudaSuccess ? e1 : e2;
+    }
+    p->stream = saved;
+    if (e == cudaSuccess && p->bgexec) {
+      cudaGraphExecUpdateResultInfo info;
+      if (cudaGraphExecUpdate(p->bgexec, g, &info) != cudaSuccess) {
+        cudaGetLastError();
+        cudaGraphExecDestroy(p->bgexec);
+        p->bgexec = nullptr;
+      }
+    }
+    if (e == cudaSuccess && !p->bgexec) e = cudaGraphInstantiate(&p->bgexec, g, 0);
+    if (g) cudaGraphDestroy(g);
+    if (e != cudaSuccess) {
+      if (p->bgexec) cudaGraphExecDestroy(p->bgexec);
+      p->bgexec = nullptr;
+      return e;
+    }
+    for (int k = 0; k < 7; ++k) p->bgp[k] = ptrs[k];
+  }
+  return cudaGraphLaunch(p->bgexec, p->stream);
+}
+
+}  // namespace
+
 int cat_backward(cat_plan_t p, const void* X, const void* WA, const void* V, const void* dO,
                  void* dX, void* dWA, void* dV, int B, int N, int D, int H, int dtype) {
   if (!p) return CAT_ERR_INVALID_ARG;
@@ -1170,19 +1228,20 @@ int cat_backward(cat_plan_t p, const void* X, const void* WA, const void* V, con
   }
   st = ensure_backward(p);
   if (st != CAT_OK) return st;
+  if (p->path == cat::PATH_FAST) {
+    if (p->use_graph) {
+      const cudaError_t e = launch_backward_graph(p, X, WA, V, dO, dX, dWA, dV);
+      if (e == cudaSuccess) return CAT_OK;
+      // Capture or instantiation failed: clear the error and launch the
+      // schedule directly from now on.
+      cudaGetLastError();
+      p->use_graph = 0;
+      describe(p);
+    }
+    return map_cuda(backward_fast_schedule(p, X, WA, V, dO, dX, dWA, dV));
+  }
   st = run_backward_front(p, X, WA, V, dO);
   if (st != CAT_OK) return st;
-  if (p->path == cat::PATH_FAST) {
-    // dV = circ(z*)^T dO by the forward's overlapped schedule on the scores
-    // reversed; dW_A and dX (which need only dz) run on the plan's stream
-    // beside its chunks.
-    cudaError_t e = cat::launch_reverse_scores(p);
-    const std::function<cudaError_t()> dense = [&]() {
-      return cat::launch_backward_dense(p, X, WA, dX, dWA);
-    };
-    if (e == cudaSuccess) e = run_fast_overlapped(p, nullptr, nullptr, dO, dV, false, &dense);
-    return map_cuda(e);
-  }
   cudaError_t e = cat::launch_backward_dense(p, X, WA, dX, dWA);
   // dV = circ(z*)^T dO: reverse the scores, then the forward's own spectrum
   // and circulant product on dO.

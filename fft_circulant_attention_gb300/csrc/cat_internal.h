@@ -116,6 +116,10 @@ struct cat_plan_s {
   cudaStream_t cap;
   cudaGraphExec_t gexec;
   const void* gX; const void* gWA; const void* gV; void* gO;
+  // fast path: the backward's schedule captured the same way (its own graph;
+  // the pointers it was captured with)
+  cudaGraphExec_t bgexec;
+  const void* bgp[7];
   unsigned int* status;     // device status word
   size_t workspace_bytes;
   // host-buffer calls (cat_forward_host), set up at the first such call:

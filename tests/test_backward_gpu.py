@@ -213,6 +213,42 @@ def test_backward_repeatable_and_forward_unaffected():
     assert torch.equal(O1, O2)
 
 
+def test_backward_graph_follows_pointers(monkeypatch):
+    """The fast path replays its backward as a CUDA graph while the call's
+    pointers stay the same and re-captures it when they change: new output
+    buffers, then new inputs, give exactly what the schedule launched
+    directly (CAT_GRAPH=0) gives."""
+    B, N, D, H, dtype = 1, 16384, 128, 2, "bf16"
+    ins = []
+    for seed in (7, 8):
+        X, WA, V = synth.make_inputs(B, N, D, H, dtype, seed=seed)
+        G = synth.make_grad(B, N, D, dtype, seed=seed)
+        ins.append(to_dev(X, WA, V, G))
+    ref = []
+    monkeypatch.setenv("CAT_GRAPH", "0")
+    with cat.Plan(B, N, D, H, dtype) as plan:
+        assert "graph=0" in plan.describe()
+        for args in ins:
+            ref.append([t.clone() for t in plan.backward(*args)])
+        plan.sync()
+    monkeypatch.delenv("CAT_GRAPH")
+    with cat.Plan(B, N, D, H, dtype) as plan:
+        assert "graph=1" in plan.describe()
+        first = [t.clone() for t in plan.backward(*ins[0])]           # capture
+        again = [t.clone() for t in plan.backward(*ins[0])]           # new outputs: update
+        outs = plan.backward(*ins[1])                                  # new inputs and outputs
+        other = [t.clone() for t in outs]
+        replay = [t.clone() for t in plan.backward(*ins[1], *outs)]   # same pointers: replay
+        plan.sync()
+        assert "graph=1" in plan.describe()
+    for got in (first, again):
+        for x, y in zip(got, ref[0]):
+            assert torch.equal(x, y)
+    for got in (other, replay):
+        for x, y in zip(got, ref[1]):
+            assert torch.equal(x, y)
+
+
 def test_backward_argument_errors():
     B, N, D, H = 1, 64, 16, 2
     X, WA, V = to_dev(*synth.make_inputs(B, N, D, H, "f32"))
