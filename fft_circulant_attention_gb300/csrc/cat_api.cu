@@ -815,10 +815,13 @@ int create_plan(cat_plan_t* out, int B, int N, int D, int H, int dtype, void* st
       if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_front[k], cudaEventDisableTiming);
     }
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_fork, cudaEventDisableTiming);
+  }
+  // Graph replay (CAT_GRAPH=0: direct launches): the fast path's forward and
+  // every 1-D plan's backward, captured on a private stream.
+  if (e == cudaSuccess && !p->twod) {
     p->use_graph = 1;
     if (const char* g = std::getenv("CAT_GRAPH")) p->use_graph = std::strcmp(g, "0") != 0;
-    if (e == cudaSuccess && p->use_graph)
-      e = cudaStreamCreateWithFlags(&p->cap, cudaStreamNonBlocking);
+    if (p->use_graph) e = cudaStreamCreateWithFlags(&p->cap, cudaStreamNonBlocking);
   }
   if (e != cudaSuccess) { free_plan(p); return CAT_ERR_CUDA; }
   if (p->twod) {
@@ -1148,18 +1151,34 @@ int cat_forward_host(cat_plan_t p, const void* X, const void* WA, const void* V,
 
 namespace {
 
-// The fast path's backward: score, softmax, the correlation and the softmax
-// backward, then dV = circ(z*)^T dO by the forward's overlapped schedule on
-// the scores reversed, with dW_A and dX (which need only dz) on the plan's
-// stream beside its chunks.
-cudaError_t backward_fast_schedule(cat_plan_s* p, const void* X, const void* WA, const void* V,
-                                   const void* dO, void* dX, void* dWA, void* dV) {
+// The backward's schedule: score, softmax, the correlation and the softmax
+// backward (dz* and dz), then dW_A, dX and dV = circ(z*)^T dO, the forward's
+// own spectrum and product on the scores reversed.  On the fast path dV runs
+// the forward's overlapped schedule with dW_A and dX (which need only dz) on
+// the plan's stream beside its chunks.
+cudaError_t backward_schedule(cat_plan_s* p, const void* X, const void* WA, const void* V,
+                              const void* dO, void* dX, void* dWA, void* dV) {
   if (run_backward_front(p, X, WA, V, dO) != CAT_OK) return cudaErrorLaunchFailure;
-  cudaError_t e = cat::launch_reverse_scores(p);
-  const std::function<cudaError_t()> dense = [&]() {
-    return cat::launch_backward_dense(p, X, WA, dX, dWA);
-  };
-  if (e == cudaSuccess) e = run_fast_overlapped(p, nullptr, nullptr, dO, dV, false, &dense);
+  if (p->path == cat::PATH_FAST) {
+    cudaError_t e = cat::launch_reverse_scores(p);
+    const std::function<cudaError_t()> dense = [&]() {
+      return cat::launch_backward_dense(p, X, WA, dX, dWA);
+    };
+    if (e == cudaSuccess) e = run_fast_overlapped(p, nullptr, nullptr, dO, dV, false, &dense);
+    return e;
+  }
+  cudaError_t e = cat::launch_backward_dense(p, X, WA, dX, dWA);
+  if (e == cudaSuccess) e = cat::launch_reverse_scores(p);
+  if (e != cudaSuccess) return e;
+  if (p->path == cat::PATH_SMEM) {
+    e = cat::launch_softmax_spectrum(p);
+    if (e == cudaSuccess) e = cat::launch_conv_smem(p, dO, dV);
+  } else if (p->path == cat::PATH_DIRECT) {
+    e = cat::launch_direct(p, nullptr, nullptr, dO, dV, false);
+  } else {
+    e = cat::launch_softmax(p);
+    if (e == cudaSuccess) e = cat::launch_fourstep_conv(p, dO, dV);
+  }
   return e;
 }
 
@@ -1176,7 +1195,7 @@ cudaError_t launch_backward_graph(cat_plan_s* p, const void* X, const void* WA, 
     cudaGraph_t g = nullptr;
     cudaError_t e = cudaStreamBeginCapture(p->cap, cudaStreamCaptureModeThreadLocal);
     if (e == cudaSuccess) {
-      const cudaError_t e1 = backward_fast_schedule(p, X, WA, V, dO, dX, dWA, dV);
+      const cudaError_t e1 = backward_schedule(p, X, WA, V, dO, dX, dWA, dV);
       const cudaError_t e2 = cudaStreamEndCapture(p->cap, &g);
       e = e1 != cudaSuccess ? e1 : e2;
     }
@@ -1228,39 +1247,16 @@ int cat_backward(cat_plan_t p, const void* X, const void* WA, const void* V, con
   }
   st = ensure_backward(p);
   if (st != CAT_OK) return st;
-  if (p->path == cat::PATH_FAST) {
-    if (p->use_graph) {
-      const cudaError_t e = launch_backward_graph(p, X, WA, V, dO, dX, dWA, dV);
-      if (e == cudaSuccess) return CAT_OK;
-      // Capture or instantiation failed: clear the error and launch the
-      // schedule directly from now on.
-      cudaGetLastError();
-      p->use_graph = 0;
-      describe(p);
-    }
-    return map_cuda(backward_fast_schedule(p, X, WA, V, dO, dX, dWA, dV));
+  if (p->use_graph) {
+    const cudaError_t e = launch_backward_graph(p, X, WA, V, dO, dX, dWA, dV);
+    if (e == cudaSuccess) return CAT_OK;
+    // Capture or instantiation failed: clear the error and launch the
+    // schedule directly from now on.
+    cudaGetLastError();
+    p->use_graph = 0;
+    describe(p);
   }
-  st = run_backward_front(p, X, WA, V, dO);
-  if (st != CAT_OK) return st;
-  cudaError_t e = cat::launch_backward_dense(p, X, WA, dX, dWA);
-  // dV = circ(z*)^T dO: reverse the scores, then the forward's own spectrum
-  // and circulant product on dO.
-  if (e == cudaSuccess) e = cat::launch_reverse_scores(p);
-  if (e == cudaSuccess) {
-    if (p->path == cat::PATH_SMEM) {
-      e = cat::launch_softmax_spectrum(p);
-      if (e == cudaSuccess) e = cat::launch_conv_smem(p, dO, dV);
-    } else if (p->path == cat::PATH_FAST) {
-      e = cat::launch_fast_zspec(p, 0, p->B * p->H, p->stream);
-      if (e == cudaSuccess) e = cat::launch_fast_conv(p, dO, dV);
-    } else if (p->path == cat::PATH_DIRECT) {
-      e = cat::launch_direct(p, nullptr, nullptr, dO, dV, false);
-    } else {
-      e = cat::launch_softmax(p);
-      if (e == cudaSuccess) e = cat::launch_fourstep_conv(p, dO, dV);
-    }
-  }
-  return map_cuda(e);
+  return map_cuda(backward_schedule(p, X, WA, V, dO, dX, dWA, dV));
 }
 
 int cat_backward_dz(cat_plan_t p, const void* X, const void* WA, const void* V, const void* dO,
