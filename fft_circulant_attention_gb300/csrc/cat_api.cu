@@ -649,12 +649,32 @@ cudaError_t run_fast_overlapped(cat_plan_s* p, const void* X, const void* WA, co
   return e;
 }
 
-// The fast path through a CUDA graph: the overlapped schedule is captured
-// on the private stream (its fork and join events pull the two internal
+// The forward's schedule without stage events: the fast path's overlapped
+// schedule, else the score, the softmax (with the spectrum of z* on the
+// shared-memory path) and the circulant product, or the direct product.
+cudaError_t forward_schedule(cat_plan_s* p, const void* X, const void* WA, const void* V,
+                             void* O) {
+  if (p->path == cat::PATH_FAST) return run_fast_overlapped(p, X, WA, V, O);
+  if (p->path == cat::PATH_DIRECT) {
+    cudaError_t e = p->dir.fused ? cudaSuccess : cat::launch_score(p, X, WA);
+    if (e == cudaSuccess) e = cat::launch_direct(p, X, WA, V, O, p->dir.fused != 0);
+    return e;
+  }
+  cudaError_t e = cat::launch_score(p, X, WA);
+  if (e == cudaSuccess)
+    e = p->path == cat::PATH_SMEM ? cat::launch_softmax_spectrum(p) : cat::launch_softmax(p);
+  if (e == cudaSuccess)
+    e = p->path == cat::PATH_SMEM ? cat::launch_conv_smem(p, V, O)
+                                  : cat::launch_fourstep_conv(p, V, O);
+  return e;
+}
+
+// The forward through a CUDA graph: the schedule is captured on the private
+// stream (on the fast path its fork and join events pull the two internal
 // streams into the capture), instantiated once, updated in place when the
 // call's pointers change, and launched on the plan's stream.  A graph launch
-// replaces the schedule's ~30 separate launches and event operations.
-cudaError_t launch_fast_graph(cat_plan_s* p, const void* X, const void* WA, const void* V,
+// replaces the schedule's separate launches and event operations.
+cudaError_t launch_forward_graph(cat_plan_s* p, const void* X, const void* WA, const void* V,
                               void* O) {
   if (!p->gexec || X != p->gX || WA != p->gWA || V != p->gV || O != p->gO) {
     cudaStream_t saved = p->stream;
@@ -662,7 +682,7 @@ cudaError_t launch_fast_graph(cat_plan_s* p, const void* X, const void* WA, cons
     cudaGraph_t g = nullptr;
     cudaError_t e = cudaStreamBeginCapture(p->cap, cudaStreamCaptureModeThreadLocal);
     if (e == cudaSuccess) {
-      const cudaError_t e1 = run_fast_overlapped(p, X, WA, V, O);
+      const cudaError_t e1 = forward_schedule(p, X, WA, V, O);
       const cudaError_t e2 = cudaStreamEndCapture(p->cap, &g);
       e = e1 != cudaSuccess ? e1 : e2;
     }
@@ -816,8 +836,8 @@ int create_plan(cat_plan_t* out, int B, int N, int D, int H, int dtype, void* st
     }
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_fork, cudaEventDisableTiming);
   }
-  // Graph replay (CAT_GRAPH=0: direct launches): the fast path's forward and
-  // every 1-D plan's backward, captured on a private stream.
+  // Graph replay (CAT_GRAPH=0: direct launches) of every 1-D plan's forward
+  // and backward, captured on a private stream.
   if (e == cudaSuccess && !p->twod) {
     p->use_graph = 1;
     if (const char* g = std::getenv("CAT_GRAPH")) p->use_graph = std::strcmp(g, "0") != 0;
@@ -891,18 +911,16 @@ int cat_forward(cat_plan_t p, const void* X, const void* WA, const void* V, void
     return CAT_ERR_ALIAS;
   cudaEvent_t* ev = nullptr;
   if (p->timing_n < p->timing_cap) ev = p->ev + (size_t)p->ev_per_call * p->timing_n++;
-  if (!ev && p->path == cat::PATH_FAST) {
-    if (p->use_graph) {
-      const cudaError_t e = launch_fast_graph(p, X, WA, V, O);
-      if (e == cudaSuccess) return CAT_OK;
-      // Capture or instantiation failed: clear the error and launch the same
-      // schedule directly from now on.
-      cudaGetLastError();
-      p->use_graph = 0;
-      describe(p);
-    }
-    return map_cuda(run_fast_overlapped(p, X, WA, V, O));
+  if (!ev && p->use_graph) {
+    const cudaError_t e = launch_forward_graph(p, X, WA, V, O);
+    if (e == cudaSuccess) return CAT_OK;
+    // Capture or instantiation failed: clear the error and launch the same
+    // schedule directly from now on.
+    cudaGetLastError();
+    p->use_graph = 0;
+    describe(p);
   }
+  if (!ev && p->path == cat::PATH_FAST) return map_cuda(run_fast_overlapped(p, X, WA, V, O));
   if (ev) cudaEventRecord(ev[0], p->stream);
   if (p->path == cat::PATH_DIRECT) {
     // Scores (in the kernel when fused), softmax and the direct product.
