@@ -60,10 +60,18 @@ __device__ __forceinline__ void ld_sh2(const float2* p, float2& a, float2& b) {
 // ---------------------------------------------------------------------------
 template <typename T, int N2>
 __global__ void __launch_bounds__(256)
-fsf_pass_a(const T* __restrict__ V, float2* __restrict__ scr, const float2* __restrict__ W,
-           int N, int D, int H, int bh0, int nb) {
+fsf_pass_a(const T* __restrict__ V0, float2* __restrict__ scr0, const float2* __restrict__ W,
+           int N, int D, int H, int bh0, int nb, const T* __restrict__ V1 = nullptr,
+           float2* __restrict__ scr1 = nullptr) {
   static_assert(N2 > 32, "N2 = 32 takes fsf_pass_a32");
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  // With V1, the grid is doubled and its second half transforms V1 into scr1
+  // (the backward's correlation transforms dO and V in one launch).
+  const int half = nb * kFastN1;
+  const bool second = V1 != nullptr && (int)blockIdx.x >= half;
+  const int bid = (int)blockIdx.x - (second ? half : 0);
+  const T* V = second ? V1 : V0;
+  float2* scr = second ? scr1 : scr0;
   {
     constexpr int TS = N2 / 32;        // threads per signal
     constexpr int R2 = N2 / 32;        // radix of step 2
@@ -72,8 +80,8 @@ fsf_pass_a(const T* __restrict__ V, float2* __restrict__ scr, const float2* __re
     extern __shared__ float4 smem4[];
     float2* buf = reinterpret_cast<float2*>(smem4);
     const int j = warp;
-    const int n1 = blockIdx.x / nb;
-    const int bhl = blockIdx.x % nb;
+    const int n1 = bid / nb;
+    const int bhl = bid % nb;
     const int bh = bh0 + bhl, b = bh / H, h = bh - b * H;
     const T* src = V + ((size_t)b * N + n1) * D + h * 64 + 2 * lane;
     const size_t rs = (size_t)kFastN1 * D;
@@ -1036,27 +1044,6 @@ cudaError_t launch_fast_conv(const cat_plan_s* p, const void* V, void* O, cudaEv
 // Pass A alone (the backward correlation transforms dO and V with it): rows
 // [bh0, bh0 + nb) of V into scratch slot `slot`, on stream st.
 template <typename T>
-static cudaError_t pass_a_t(const cat_plan_s* p, const T* V, int bh0, int nb, float2* scr,
-                            cudaStream_t st) {
-  switch (p->fs.N2) {
-    case 32: {
-      CUtensorMap tmV;
-      if (!encode_v_map(p, V, &tmV)) return cudaErrorInvalidValue;
-      const int per_sm = PipeA<T>::kSmem <= (113u << 10) ? 2 : 1;
-      int grid = (nb * kFastN1 + kPipeWarps - 1) / kPipeWarps;
-      if (grid > per_sm * p->sms) grid = per_sm * p->sms;
-      fsf_pass_a32<T><<<grid, kPipeWarps * 32, PipeA<T>::kSmem, st>>>(
-          tmV, scr, p->tw, p->N, p->D, p->H, bh0, nb, p->status, tmV, scr, 1);
-      break;
-    }
-    case 64: launch_ac<T, 64>(p, V, nullptr, scr, bh0, nb, true, st); break;
-    case 128: launch_ac<T, 128>(p, V, nullptr, scr, bh0, nb, true, st); break;
-    default: launch_ac<T, 256>(p, V, nullptr, scr, bh0, nb, true, st); break;
-  }
-  return cudaGetLastError();
-}
-
-template <typename T>
 static cudaError_t pass_a32_pair(const cat_plan_s* p, const T* A, const T* Bm, int bh0, int nb,
                                  float2* s0, float2* s1, cudaStream_t st) {
   CUtensorMap tmA, tmB;
@@ -1073,21 +1060,33 @@ cudaError_t launch_fast_corr(const cat_plan_s* p, const void* G, const void* V, 
                              int bh0, int nb, cudaStream_t st, float2* s0, float2* s1) {
   if (!s0) s0 = p->scratch;
   if (!s1) s1 = p->scratch + p->scratch_bytes / 2 / sizeof(float2);
-  if (p->fs.N2 == 32) {
-    // dO into s0 and V into s1 as one launch.
-    cudaError_t e = p->dtype == 1
-        ? pass_a32_pair(p, (const __nv_bfloat16*)G, (const __nv_bfloat16*)V, bh0, nb, s0, s1, st)
-        : pass_a32_pair(p, (const float*)G, (const float*)V, bh0, nb, s0, s1, st);
+  if (p->fs.N2 != 32) {
+    // dO into s0 and V into s1 as one launch (a doubled grid).
+    const int grid = 2 * nb * kFastN1;
+    const size_t smem = fast_smem_a(p->fs.N2);
+    const int N2 = p->fs.N2;
+    if (p->dtype == 1) {
+      const __nv_bfloat16* g = (const __nv_bfloat16*)G;
+      const __nv_bfloat16* v = (const __nv_bfloat16*)V;
+      if (N2 == 64) fsf_pass_a<__nv_bfloat16, 64><<<grid, N2, smem, st>>>(g, s0, p->tw, p->N, p->D, p->H, bh0, nb, v, s1);
+      else if (N2 == 128) fsf_pass_a<__nv_bfloat16, 128><<<grid, N2, smem, st>>>(g, s0, p->tw, p->N, p->D, p->H, bh0, nb, v, s1);
+      else fsf_pass_a<__nv_bfloat16, 256><<<grid, N2, smem, st>>>(g, s0, p->tw, p->N, p->D, p->H, bh0, nb, v, s1);
+    } else {
+      const float* g = (const float*)G;
+      const float* v = (const float*)V;
+      if (N2 == 64) fsf_pass_a<float, 64><<<grid, N2, smem, st>>>(g, s0, p->tw, p->N, p->D, p->H, bh0, nb, v, s1);
+      else if (N2 == 128) fsf_pass_a<float, 128><<<grid, N2, smem, st>>>(g, s0, p->tw, p->N, p->D, p->H, bh0, nb, v, s1);
+      else fsf_pass_a<float, 256><<<grid, N2, smem, st>>>(g, s0, p->tw, p->N, p->D, p->H, bh0, nb, v, s1);
+    }
+    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    fsf_corr_b<<<nb * p->fs.N2, 256, kSmemCorrB, st>>>(s0, s1, y, p->tabs, p->fs.N2);
+    fsf_corr_b<<<nb * N2, 256, kSmemCorrB, st>>>(s0, s1, y, p->tabs, N2);
     return cudaGetLastError();
   }
+  // N2 = 32: dO into s0 and V into s1 as one launch.
   cudaError_t e = p->dtype == 1
-      ? pass_a_t(p, (const __nv_bfloat16*)G, bh0, nb, s0, st)
-      : pass_a_t(p, (const float*)G, bh0, nb, s0, st);
-  if (e == cudaSuccess)
-    e = p->dtype == 1 ? pass_a_t(p, (const __nv_bfloat16*)V, bh0, nb, s1, st)
-                      : pass_a_t(p, (const float*)V, bh0, nb, s1, st);
+      ? pass_a32_pair(p, (const __nv_bfloat16*)G, (const __nv_bfloat16*)V, bh0, nb, s0, s1, st)
+      : pass_a32_pair(p, (const float*)G, (const float*)V, bh0, nb, s0, s1, st);
   if (e != cudaSuccess) return e;
   fsf_corr_b<<<nb * p->fs.N2, 256, kSmemCorrB, st>>>(s0, s1, y, p->tabs, p->fs.N2);
   return cudaGetLastError();
