@@ -550,7 +550,6 @@ static cudaError_t corr_fast_overlapped(const cat_plan_s* p, const void* G, cons
   const int rows = p->B * p->H;
   const int cb = p->fs.chunk_bh / 2;
   const size_t half = p->scratch_bytes / 4 / sizeof(float2);   // a half slot
-  const size_t yhalf = (size_t)cb * p->N;
   cudaError_t e = cudaEventRecord(p->ev_fork, p->stream);
   for (int k = 0; k < 2 && e == cudaSuccess; ++k) e = cudaStreamWaitEvent(p->side[k], p->ev_fork, 0);
   for (int bh0 = 0, c = 0; bh0 < rows && e == cudaSuccess; bh0 += cb, ++c) {
@@ -558,15 +557,15 @@ static cudaError_t corr_fast_overlapped(const cat_plan_s* p, const void* G, cons
     const int k = c & 1;
     float2* s0 = p->scratch + (size_t)k * half;
     float2* s1 = p->scratch + 2 * half + (size_t)k * half;
-    float2* y = p->bw_scr + (size_t)k * yhalf;
-    e = launch_fast_corr(p, G, V, y, bh0, nb, p->side[k], s0, s1);
-    if (e == cudaSuccess) e = launch_fast_corr_c32(p, y, p->bw_dzs, bh0, nb, p->side[k]);
+    // Each chunk's y at its own rows: pass C runs once for all rows below.
+    e = launch_fast_corr(p, G, V, p->bw_scr + (size_t)bh0 * p->N, bh0, nb, p->side[k], s0, s1);
   }
   for (int k = 0; k < 2; ++k) {
     cudaError_t e2 = cudaEventRecord(p->ev_join[k], p->side[k]);
     if (e2 == cudaSuccess) e2 = cudaStreamWaitEvent(p->stream, p->ev_join[k], 0);
     if (e == cudaSuccess) e = e2;
   }
+  if (e == cudaSuccess) e = launch_fast_corr_c32(p, p->bw_scr, p->bw_dzs, 0, rows, p->stream);
   return e;
 }
 

@@ -449,7 +449,11 @@ int configure_backward(cat_plan_s* p) {
     if ((long)w.TC * w.N2 > (long)cat::vals_capacity(w.rp2) * w.threadsC)
       return CAT_ERR_UNSUPPORTED_N;
     w.chunk_bh = p->fs.chunk_bh;
-    w.scratch_bytes = (size_t)w.chunk_bh * N * c8;
+    // y, the correlation's one signal per row: every row's at N2 = 32 (the
+    // overlapped chunks leave theirs for one pass-C launch at the end), a
+    // chunk's otherwise.
+    const size_t yrows = w.N2 == 32 ? (size_t)p->B * p->H : (size_t)w.chunk_bh;
+    w.scratch_bytes = yrows * N * c8;
     w.wsplit = cat::backward_wsplit((long long)p->B * N, p->D, p->H, p->sms > 0 ? p->sms : 148);
     return CAT_OK;
   }

@@ -455,13 +455,13 @@ fsf_pass_b(float2* __restrict__ scr, const float2* __restrict__ zft,
 // pairs sig mod 8 + 8r in round r), j = 2·warp + lane / 16, with pass B's
 // forward steps F1, F2 (thread j then holds bins k1 = 2j + e + 32q).  The V
 // threads hand their bins over through shared memory, the dO threads keep
-// running sums; the 8 sums are added in a fixed order and 16 threads run
+// running sums; the 8 sums are added in a fixed order and one warp runs
 // pass B's inverse steps I1, I2 on the result.  The running sums live in
 // shared memory (rows of kRowB per signal, at the position the thread's bins
 // take in the exchange rows), so that two CTAs fit an SM.
 // ---------------------------------------------------------------------------
 constexpr size_t kSmemCorrB =
-    (size_t)16 * kRowB * sizeof(float2) + 3 * kTabB * sizeof(float2) + 8 * (size_t)kRowB * sizeof(float2);
+    (size_t)16 * kRowB * sizeof(float2) + kTabB * sizeof(float2) + 8 * (size_t)kRowB * sizeof(float2);
 
 __global__ void __launch_bounds__(256, 2)
 fsf_corr_b(const float2* __restrict__ scrG, const float2* __restrict__ scrV,
@@ -469,9 +469,7 @@ fsf_corr_b(const float2* __restrict__ scrG, const float2* __restrict__ scrV,
   extern __shared__ float4 smem4[];
   float2* buf = reinterpret_cast<float2*>(smem4);
   float2* tf = buf + 16 * kRowB;
-  float2* ti = tf + kTabB;
-  float2* tx = ti + kTabB;
-  float2* accs = tx + kTabB;           // [8][kRowB] running sums of the dO threads
+  float2* accs = tf + kTabB;           // [8][kRowB] running sums of the dO threads
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int sig = lane & 15;
   const int j = 2 * warp + (lane >> 4);
@@ -487,8 +485,6 @@ fsf_corr_b(const float2* __restrict__ scrG, const float2* __restrict__ scrV,
     const float4* g4 = reinterpret_cast<const float4*>(tabs);
     float4* tf4 = reinterpret_cast<float4*>(tf);
     tf4[t] = __ldg(g4 + t);
-    tf4[256 + t] = __ldg(g4 + 256 + t);
-    tf4[512 + t] = __ldg(g4 + 512 + (size_t)k2 * 256 + t);
     float4* a4 = reinterpret_cast<float4*>(accs);
     for (int i = t; i < 8 * kRowB / 2; i += 256) a4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
@@ -537,9 +533,11 @@ fsf_corr_b(const float2* __restrict__ scrG, const float2* __restrict__ scrV,
     }
   }
   __syncthreads();
-  // Sum of the 8 partial spectra into row 8, two bins a thread.
-  float2* yrow = buf + 8 * kRowB;
-  float2* xrow = buf + 9 * kRowB;
+  // Sum of the 8 partial spectra, two bins a thread, into Y[m][q] (row
+  // stride 17): bin k1 = m + 32q, m = 2j + e, sits at 32j + 2q + e in the
+  // sums' rows.
+  float2* ybuf = buf + 8 * kRowB;      // Y: 32 x 17
+  float2* zbuf = buf + 10 * kRowB;     // Z: 16 x 33
   {
     const int t = threadIdx.x;
     float2 s0 = make_float2(0.f, 0.f), s1 = s0;
@@ -550,37 +548,51 @@ fsf_corr_b(const float2* __restrict__ scrG, const float2* __restrict__ scrV,
       s0 = cadd(s0, v0);
       s1 = cadd(s1, v1);
     }
-    st_sh2(yrow + 2 * t, s0, s1);
+    const int m = 2 * (t >> 4), q = t & 15;
+    ybuf[m * 17 + q] = s0;
+    ybuf[(m + 1) * 17 + q] = s1;
   }
   __syncthreads();
-  if (sig == 0) {
-    float2 c[2][16];
+  if (warp != 0) return;
+  // The inverse 512-point DFT (pass B's steps I1, I2 with the same
+  // twiddles) on one warp.  I1: lane m, the 16-point inverse over q.
+  {
+    float2 c[16];
 #pragma unroll
-    for (int q = 0; q < 16; ++q) ld_sh2(yrow + (j * 16 + q) * 2, c[0][q], c[1][q]);
+    for (int q = 0; q < 16; ++q) c[q] = ybuf[lane * 17 + q];
+    dft<16, true, CxPaired>(c);
 #pragma unroll
-    for (int e = 0; e < 2; ++e) dft<16, true, CxPaired>(c[e]);
-#pragma unroll
-    for (int q = 0; q < 16; ++q) st_sh2(xrow + 32 * q + 2 * j, c[0][q], c[1][q]);
+    for (int r = 0; r < 16; ++r) zbuf[r * 33 + lane] = c[r];
   }
-  __syncthreads();
-  if (sig == 0) {
-    float2 a[32];
+  __syncwarp();
+  // I2: for each r the twiddle conj(w_512^{m r}), then the 32-point inverse
+  // over m, split in two halves: lane r + 16h transforms the m = 2i + h
+  // terms, h = 1 scales by w_32^{-n}, and the lane pair adds/subtracts
+  // through one shuffle per component.
+  // ti and the output twiddles tx are read from the global tables: a lane's
+  // entries are 32 apart, one bank in shared memory.
+  const int r = lane & 15, h = lane >> 4;
+  const float2* ti = tabs + kTabB;
+  float2 x[16];
 #pragma unroll
-    for (int u = 0; u < 32; u += 2) ld_sh2(xrow + 32 * j + u, a[u], a[u + 1]);
-    const float2* tw = ti + j * 32;
+  for (int i = 0; i < 16; ++i) {
+    const int m = 2 * i + h;
+    x[i] = cmulc(zbuf[r * 33 + m], __ldg(ti + r * 32 + m));
+  }
+  dft<16, true, CxPaired>(x);
+  if (h) {
 #pragma unroll
-    for (int u = 2; u < 32; u += 2) {
-      float2 w0, w1;
-      ld_sh2(tw + u, w0, w1);
-      a[u] = cmulc(a[u], w0);
-      a[u + 1] = cmulc(a[u + 1], w1);
-    }
-    a[1] = cmulc(a[1], tw[1]);
-    dft<32, true, CxPaired>(a);
-    const float2* tz = tx + j * 32;
-    float2* out = y + ((size_t)bhl * N2 + k2) * kFastN1;
+    for (int n = 1; n < 16; ++n) x[n] = cmulc(x[n], tf[16 * 16 + n]);
+  }
+  const float2* tz = tabs + (size_t)(2 + k2) * kTabB + r * 32 + 16 * h;
+  float2* out = y + ((size_t)bhl * N2 + k2) * kFastN1 + r + 256 * h;
 #pragma unroll
-    for (int q = 0; q < 32; ++q) out[j + 16 * q] = cmulc(a[q], tz[q]);
+  for (int n = 0; n < 16; ++n) {
+    float2 o;
+    o.x = __shfl_xor_sync(0xffffffffu, x[n].x, 16);
+    o.y = __shfl_xor_sync(0xffffffffu, x[n].y, 16);
+    const float2 v = h ? csub(o, x[n]) : cadd(x[n], o);
+    out[16 * n] = cmulc(v, __ldg(tz + n));
   }
 }
 
