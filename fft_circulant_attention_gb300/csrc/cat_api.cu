@@ -641,7 +641,7 @@ cudaError_t run_fast_overlapped(cat_plan_s* p, const void* X, const void* WA, co
       const int nb = p->H - h0 < p->fs.chunk_bh ? p->H - h0 : p->fs.chunk_bh;
       const int k = g & 1;
       e = cat::launch_fast_chunk(p, V, O, b * p->H + h0, nb, k, p->side[k],
-                                 waited[k] ? nullptr : p->ev_front[0]);
+                                 waited[k] ? nullptr : p->ev_front[0], nullptr, g >= 2);
       waited[k] = true;
     }
   if (e == cudaSuccess && between) e = (*between)();
@@ -786,6 +786,11 @@ int create_plan(cat_plan_t* out, int B, int N, int D, int H, int dtype, void* st
     p->fork_at = std::strcmp(sc, "start") == 0   ? cat::FORK_START
                  : std::strcmp(sc, "score") == 0 ? cat::FORK_SCORE
                                                  : cat::FORK_SPECTRUM;
+  // Fast-path passes as programmatic dependents of the pass ahead
+  // (CAT_PDL_FAST=0 off, "end": signal at each CTA's end, else at its start).
+  p->fast_pdl = 2;
+  if (const char* sc = std::getenv("CAT_PDL_FAST"))
+    p->fast_pdl = std::strcmp(sc, "0") == 0 ? 0 : std::strcmp(sc, "end") == 0 ? 1 : 2;
   if (const char* sc = std::getenv("CAT_SCORE")) {
     p->score_cuda_cores = std::strcmp(sc, "cuda") == 0;
     p->score_path = std::strcmp(sc, "mma") == 0 ? 1 : 0;

@@ -96,6 +96,9 @@ struct cat_plan_s {
   int score_cuda_cores;     // 1: bf16 scores on the CUDA-core kernel (testing)
   int score_path;           // 1: bf16 scores on the register-fed MMA kernel (testing)
   int fork_at;              // fast path: where the chunk streams fork (cat::FORK_*)
+  int fast_pdl;             // fast path: passes launched as programmatic dependents of
+                            // the pass ahead on their stream (0 no, 1 signal at the
+                            // end of each CTA, 2 at its start)
   // workspace (device)
   float2* z2;               // [B, H, N] scores as double-float (hi, lo)
   float* zs;                // [B, H, N] z* (softmax weights)
@@ -263,10 +266,12 @@ int fast_chunks(const cat_plan_s* p);
 // (b, h) rows [row0, row0 + nrows), and passes A, B, C of one chunk of rows
 // [bh0, bh0 + nb) with scratch buffer `slot`, all on stream st.  If
 // before_b is given, pass B (the first to read the spectrum) waits for it.
+// dep_a: the kernel ahead of this chunk's pass A on st is the previous
+// chunk's pass C (pass A may then launch as its programmatic dependent).
 cudaError_t launch_fast_zspec(const cat_plan_s* p, int row0, int nrows, cudaStream_t st);
 cudaError_t launch_fast_chunk(const cat_plan_s* p, const void* V, void* O, int bh0, int nb,
                               int slot, cudaStream_t st, cudaEvent_t before_b = nullptr,
-                              cudaEvent_t* after = nullptr);
+                              cudaEvent_t* after = nullptr, bool dep_a = false);
 
 // Direct path (direct.cu): dynamic shared memory of a CTA, one-time
 // attribute set-up, and the launch (fused: scores computed in the kernel;

@@ -62,8 +62,9 @@ template <typename T, int N2>
 __global__ void __launch_bounds__(256)
 fsf_pass_a(const T* __restrict__ V0, float2* __restrict__ scr0, const float2* __restrict__ W,
            int N, int D, int H, int bh0, int nb, const T* __restrict__ V1 = nullptr,
-           float2* __restrict__ scr1 = nullptr) {
+           float2* __restrict__ scr1 = nullptr, int early = 0) {
   static_assert(N2 > 32, "N2 = 32 takes fsf_pass_a32");
+  if (early) pdl_trigger();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   // With V1, the grid is doubled and its second half transforms V1 into scr1
   // (the backward's correlation transforms dO and V in one launch).
@@ -101,6 +102,9 @@ fsf_pass_a(const T* __restrict__ V0, float2* __restrict__ scr0, const float2* __
     const int wstep = N / N2;
     // The scratch is read again by passes B and C: keep it in L2.
     const uint64_t keep = policy_evict_last();
+    // Launched as a dependent of the previous chunk's pass C, which reads
+    // the scratch slot this pass overwrites.
+    pdl_wait();
 #pragma unroll
     for (int e = 0; e < PER; ++e) {
       const int k = PER * j + e;
@@ -115,6 +119,7 @@ fsf_pass_a(const T* __restrict__ V0, float2* __restrict__ scr0, const float2* __
       }
     }
   }
+  if (!early) pdl_trigger();
 }
 
 // ---------------------------------------------------------------------------
@@ -122,9 +127,10 @@ fsf_pass_a(const T* __restrict__ V0, float2* __restrict__ scr0, const float2* __
 // ---------------------------------------------------------------------------
 template <typename T, int N2>
 __global__ void __launch_bounds__(256)
-fsf_pass_c(const float2* __restrict__ scr, T* __restrict__ O, const float2* __restrict__ W,
-           int N, int D, int H, int bh0, int nb) {
+fsf_pass_c(const float2* scr, T* __restrict__ O, const float2* __restrict__ W, int N, int D,
+           int H, int bh0, int nb, int early = 0) {
   static_assert(N2 > 32, "N2 = 32 takes fsf_pass_c32");
+  if (early) pdl_trigger();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   {
     constexpr int TS = N2 / 32;
@@ -138,8 +144,9 @@ fsf_pass_c(const float2* __restrict__ scr, T* __restrict__ O, const float2* __re
     const int bhl = blockIdx.x % nb;
     const int bh = bh0 + bhl, b = bh / H, h = bh - b * H;
     float2 a[32];
+    pdl_wait();   // pass B ahead on the stream wrote the scratch
 #pragma unroll
-    for (int u = 0; u < 32; ++u) a[u] = scr[scr_idx(bhl, N2, j + TS * u, n1, lane)];
+    for (int u = 0; u < 32; ++u) a[u] = ld_dep(scr + scr_idx(bhl, N2, j + TS * u, n1, lane));
     dft<32, true>(a);
     float2* row = buf + lane * RS;
 #pragma unroll
@@ -171,6 +178,7 @@ fsf_pass_c(const float2* __restrict__ scr, T* __restrict__ O, const float2* __re
       for (int s = 0; s < R2; ++s) st_pair(dst + (size_t)(k + 32 * s) * rs, c[e][s]);
     }
   }
+  if (!early) pdl_trigger();
 }
 
 // Two storage elements (one packed pair) read from shared memory.
@@ -210,10 +218,11 @@ __global__ void __launch_bounds__(kPipeWarps * 32)
 fsf_pass_a32(const __grid_constant__ CUtensorMap tmV, float2* __restrict__ scr,
              const float2* __restrict__ W, int N, int D, int H, int bh0, int nb,
              unsigned int* status, const __grid_constant__ CUtensorMap tmV2,
-             float2* __restrict__ scr2, int ntens) {
+             float2* __restrict__ scr2, int ntens, int early) {
   // ntens = 2: a second tensor (tmV2 into scr2) in the same launch, its
   // items after the first's (the backward's correlation transforms dO and V
   // together).
+  if (early) pdl_trigger();
   using P = PipeA<T>;
   extern __shared__ __align__(128) unsigned char sm[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -241,6 +250,9 @@ fsf_pass_a32(const __grid_constant__ CUtensorMap tmV, float2* __restrict__ scr,
 #pragma unroll
   for (int k = 0; k < P::kStages; ++k)
     if (gw + k * G < items) issue(k, gw + k * G);
+  // Launched as a dependent of the previous chunk's pass C, which reads the
+  // scratch slot this pass overwrites: the first tiles load meanwhile.
+  pdl_wait();
   int it = 0;
   for (int item = gw; item < items; item += G, ++it) {
     const int s = it % P::kStages;
@@ -264,12 +276,15 @@ fsf_pass_a32(const __grid_constant__ CUtensorMap tmV, float2* __restrict__ scr,
       st_hint(dst + scr_idx(bhl, 32, k2, n1, lane), cmul(a[k2], twrow[k2]), keep);
     __syncwarp();
   }
+  if (!early) pdl_trigger();
 }
 
 template <typename T>
 __global__ void __launch_bounds__(PipeC::kWarps * 32)
 fsf_pass_c32(const __grid_constant__ CUtensorMap tmC, const float2* __restrict__ scr,
-             T* __restrict__ O, int N, int D, int H, int bh0, int nb, unsigned int* status) {
+             T* __restrict__ O, int N, int D, int H, int bh0, int nb, unsigned int* status,
+             int early) {
+  if (early) pdl_trigger();
   using P = PipeC;
   extern __shared__ __align__(128) unsigned char sm[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -288,6 +303,7 @@ fsf_pass_c32(const __grid_constant__ CUtensorMap tmC, const float2* __restrict__
       tma_load_4d(stage + s * 32 * P::kRowBytes, &tmC, 0, item / nb, 0, item % nb, bar + s);
     }
   };
+  pdl_wait();   // pass B ahead on the stream wrote the scratch
 #pragma unroll
   for (int k = 0; k < P::kStages; ++k)
     if (gw + k * G < items) issue(k, gw + k * G);
@@ -317,6 +333,7 @@ fsf_pass_c32(const __grid_constant__ CUtensorMap tmC, const float2* __restrict__
 #pragma unroll
     for (int n2 = 0; n2 < 32; ++n2) st_pair(dst + n2 * rs, a[n2]);
   }
+  if (!early) pdl_trigger();
 }
 
 // ---------------------------------------------------------------------------
@@ -345,8 +362,8 @@ constexpr size_t kSmemB =
 
 __global__ void __launch_bounds__(kBPairs * 16, 2)
 fsf_pass_b(float2* __restrict__ scr, const float2* __restrict__ zft,
-           const float2* __restrict__ tabs, int N2, int bh0) {
-  constexpr int NT = kBPairs * 16;
+           const float2* __restrict__ tabs, int N2, int bh0, int early) {
+  if (early) pdl_trigger();
   extern __shared__ float4 smem4[];
   float2* buf = reinterpret_cast<float2*>(smem4);
   float2* tf = buf + kBPairs * kRowB;
@@ -364,10 +381,10 @@ fsf_pass_b(float2* __restrict__ scr, const float2* __restrict__ zft,
   float2* row = buf + pl * kRowB;
 
   const uint64_t keep = policy_evict_last();
-  float2 a[32];
-#pragma unroll
-  for (int u = 0; u < 32; ++u) a[u] = ld_hint(scr + scr_idx(bhl, N2, k2, j + 16 * u, pair), keep);
-  // Tables: 4 x 4 KB, one 16-byte load of each per thread (NT = 256).
+  // Tables: 4 x 4 KB, one 16-byte load of each per thread (256 threads).
+  // The plan's tables are loaded before the wait for pass A (this launch may
+  // be its programmatic dependent); the spectrum of z* was complete before
+  // the stream's first pass B started.
   const int t = threadIdx.x;
   const float4* g4 = reinterpret_cast<const float4*>(tabs);
   const float4 q0 = __ldg(g4 + t);                                   // tf, ti
@@ -375,6 +392,10 @@ fsf_pass_b(float2* __restrict__ scr, const float2* __restrict__ zft,
   const float4 q2 = __ldg(g4 + 512 + (size_t)k2 * 256 + t);          // tx of this k2
   const float4 q3 = __ldg(reinterpret_cast<const float4*>(zft) +
                           ((size_t)(bh0 + bhl) * N2 + k2) * (kFastN1 / 2) + t);
+  pdl_wait();
+  float2 a[32];
+#pragma unroll
+  for (int u = 0; u < 32; ++u) a[u] = ld_hint(scr + scr_idx(bhl, N2, k2, j + 16 * u, pair), keep);
   dft<32, false, CxPaired>(a);
 #pragma unroll
   for (int q = 0; q < 32; q += 2) st_sh2(row + 32 * j + q, a[q], a[q + 1]);
@@ -442,6 +463,7 @@ fsf_pass_b(float2* __restrict__ scr, const float2* __restrict__ zft,
       st_hint(scr + scr_idx(bhl, N2, k2, j + 16 * (q + 1), pair), cmulc(a[q + 1], w1), keep);
     }
   }
+  if (!early) pdl_trigger();
 }
 
 
@@ -911,17 +933,29 @@ cudaError_t setup_fast_kernels(cat_plan_s* p) {
 }
 
 // Generic passes A and C (N2 > 32): a CTA of N2 threads per (b, h, n1).
+// An ordinary launch, or (dep) one as the programmatic dependent of the
+// kernel ahead on the stream.
+template <typename... KArgs, typename... Args>
+static cudaError_t fast_launch(bool dep, void (*kernel)(KArgs...), int grid, int block,
+                               size_t smem, cudaStream_t st, Args... args) {
+  if (dep) return launch_dependent(kernel, dim3(grid), dim3(block), smem, st, args...);
+  kernel<<<grid, block, smem, st>>>(args...);
+  return cudaGetLastError();
+}
+
 template <typename T, int N2>
-static void launch_ac(const cat_plan_s* p, const T* V, T* O, float2* scr, int bh0, int nb,
-                      bool pass_a, cudaStream_t st) {
+static cudaError_t launch_ac(const cat_plan_s* p, const T* V, T* O, float2* scr, int bh0,
+                             int nb, bool pass_a, cudaStream_t st, bool dep) {
   static_assert(N2 > 32, "N2 = 32 takes the pipelined passes");
   const int grid = nb * kFastN1;
   const int threads = N2;
   const size_t smem = fast_smem_a(N2);
+  const int early = p->fast_pdl == 2;
   if (pass_a)
-    fsf_pass_a<T, N2><<<grid, threads, smem, st>>>(V, scr, p->tw, p->N, p->D, p->H, bh0, nb);
-  else
-    fsf_pass_c<T, N2><<<grid, threads, smem, st>>>(scr, O, p->tw, p->N, p->D, p->H, bh0, nb);
+    return fast_launch(dep, fsf_pass_a<T, N2>, grid, threads, smem, st, V, scr, (const float2*)p->tw,
+                       p->N, p->D, p->H, bh0, nb, (const T*)nullptr, (float2*)nullptr, early);
+  return fast_launch(dep, fsf_pass_c<T, N2>, grid, threads, smem, st, (const float2*)scr, O,
+                     (const float2*)p->tw, p->N, p->D, p->H, bh0, nb, early);
 }
 
 // V viewed as [B][N2 (n2)][512 (n1)][D]: the box is one head's 64 columns of
@@ -975,13 +1009,21 @@ cudaError_t launch_fast_zspec(const cat_plan_s* p, int row0, int nrows, cudaStre
   return cudaGetLastError();
 }
 
+// A chunk's passes on stream st.  With p->fast_pdl set, each pass whose
+// stream predecessor is the pass before it (pass A after the previous
+// chunk's pass C when dep_a, pass B after pass A unless an event wait sits
+// between them, pass C after pass B) launches as that kernel's programmatic
+// dependent: its launch and the work before its wait overlap the end of the
+// pass ahead.  Stage timing (after != nullptr) keeps ordinary launches.
 template <typename T>
 static cudaError_t chunk_t(const cat_plan_s* p, const T* V, T* O, int bh0, int nb, int slot,
                            cudaStream_t st, const CUtensorMap* tmV, cudaEvent_t before_b,
-                           cudaEvent_t* after) {
+                           cudaEvent_t* after, bool dep_a) {
   const int N2 = p->fs.N2;
   float2* scr = p->scratch + (size_t)slot * (p->scratch_bytes / 2 / sizeof(float2));
-  auto ac = [&](bool pass_a) {
+  const bool pdl = p->fast_pdl != 0 && after == nullptr;
+  const int early = p->fast_pdl == 2;
+  auto ac = [&](bool pass_a, bool dep) -> cudaError_t {
     switch (N2) {
       case 32: {
         const int items = nb * kFastN1;
@@ -990,47 +1032,50 @@ static cudaError_t chunk_t(const cat_plan_s* p, const T* V, T* O, int bh0, int n
           const int per_sm = PipeA<T>::kSmem <= (113u << 10) ? 2 : 1;
           int grid = (items + kPipeWarps - 1) / kPipeWarps;
           if (grid > per_sm * p->sms) grid = per_sm * p->sms;
-          fsf_pass_a32<T><<<grid, kPipeWarps * 32, PipeA<T>::kSmem, st>>>(
-              *tmV, scr, p->tw, p->N, p->D, p->H, bh0, nb, p->status, *tmV, scr, 1);
-        } else {
-          int grid = (items + PipeC::kWarps - 1) / PipeC::kWarps;
-          if (grid > 2 * p->sms) grid = 2 * p->sms;
-          fsf_pass_c32<T><<<grid, PipeC::kWarps * 32, PipeC::kSmem, st>>>(
-              p->tm_c[slot], scr, O, p->N, p->D, p->H, bh0, nb, p->status);
+          return fast_launch(dep, fsf_pass_a32<T>, grid, kPipeWarps * 32, PipeA<T>::kSmem, st,
+                             *tmV, scr, (const float2*)p->tw, p->N, p->D, p->H, bh0, nb,
+                             p->status, *tmV, scr, 1, early);
         }
-        break;
+        int grid = (items + PipeC::kWarps - 1) / PipeC::kWarps;
+        if (grid > 2 * p->sms) grid = 2 * p->sms;
+        return fast_launch(dep, fsf_pass_c32<T>, grid, PipeC::kWarps * 32, PipeC::kSmem, st,
+                           p->tm_c[slot], (const float2*)scr, O, p->N, p->D, p->H, bh0, nb,
+                           p->status, early);
       }
-      case 64: launch_ac<T, 64>(p, V, O, scr, bh0, nb, pass_a, st); break;
-      case 128: launch_ac<T, 128>(p, V, O, scr, bh0, nb, pass_a, st); break;
-      default: launch_ac<T, 256>(p, V, O, scr, bh0, nb, pass_a, st); break;
+      case 64: return launch_ac<T, 64>(p, V, O, scr, bh0, nb, pass_a, st, dep);
+      case 128: return launch_ac<T, 128>(p, V, O, scr, bh0, nb, pass_a, st, dep);
+      default: return launch_ac<T, 256>(p, V, O, scr, bh0, nb, pass_a, st, dep);
     }
   };
-  ac(true);
+  cudaError_t e = ac(true, pdl && dep_a);
+  if (e != cudaSuccess) return e;
   if (after) cudaEventRecord(after[0], st);
   if (before_b) {
-    const cudaError_t e = cudaStreamWaitEvent(st, before_b, 0);
+    e = cudaStreamWaitEvent(st, before_b, 0);
     if (e != cudaSuccess) return e;
   }
-  fsf_pass_b<<<nb * N2 * (kFastPairs / kBPairs), kBPairs * 16, kSmemB, st>>>(scr, p->zf, p->tabs,
-                                                                             N2, bh0);
+  e = fast_launch(pdl && !before_b, fsf_pass_b, nb * N2 * (kFastPairs / kBPairs), kBPairs * 16,
+                  kSmemB, st, scr, (const float2*)p->zf, (const float2*)p->tabs, N2, bh0, early);
+  if (e != cudaSuccess) return e;
   if (after) cudaEventRecord(after[1], st);
-  ac(false);
+  e = ac(false, pdl);
+  if (e != cudaSuccess) return e;
   if (after) cudaEventRecord(after[2], st);
   return cudaGetLastError();
 }
 
 cudaError_t launch_fast_chunk(const cat_plan_s* p, const void* V, void* O, int bh0, int nb,
                               int slot, cudaStream_t st, cudaEvent_t before_b,
-                              cudaEvent_t* after) {
+                              cudaEvent_t* after, bool dep_a) {
   CUtensorMap tmV;
   if (p->dtype == 1) {
     if (p->fs.N2 == 32 && !encode_v_map(p, (const __nv_bfloat16*)V, &tmV))
       return cudaErrorInvalidValue;
     return chunk_t(p, (const __nv_bfloat16*)V, (__nv_bfloat16*)O, bh0, nb, slot, st, &tmV,
-                   before_b, after);
+                   before_b, after, dep_a);
   }
   if (p->fs.N2 == 32 && !encode_v_map(p, (const float*)V, &tmV)) return cudaErrorInvalidValue;
-  return chunk_t(p, (const float*)V, (float*)O, bh0, nb, slot, st, &tmV, before_b, after);
+  return chunk_t(p, (const float*)V, (float*)O, bh0, nb, slot, st, &tmV, before_b, after, dep_a);
 }
 
 int fast_chunks(const cat_plan_s* p) {
@@ -1064,7 +1109,7 @@ static cudaError_t pass_a32_pair(const cat_plan_s* p, const T* A, const T* Bm, i
   int grid = (2 * nb * kFastN1 + kPipeWarps - 1) / kPipeWarps;
   if (grid > per_sm * p->sms) grid = per_sm * p->sms;
   fsf_pass_a32<T><<<grid, kPipeWarps * 32, PipeA<T>::kSmem, st>>>(
-      tmA, s0, p->tw, p->N, p->D, p->H, bh0, nb, p->status, tmB, s1, 2);
+      tmA, s0, p->tw, p->N, p->D, p->H, bh0, nb, p->status, tmB, s1, 2, 0);
   return cudaGetLastError();
 }
 
