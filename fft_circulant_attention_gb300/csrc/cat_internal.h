@@ -57,6 +57,8 @@ struct FourStepCfg {
   int threadsA, threadsB, threadsC;
   size_t smemA, smemB, smemC;
   int chunk_bh;         // (b, h) rows whose scratch is live at once
+  int a_tma_per_sm;     // fast path, N2 > 32: resident CTAs per SM of the
+                        // tensor-copy pass A (0: the plain pass A)
 };
 
 // Backward correlation dz*[k] = sum_c sum_i G[i, c] V[(i - k) mod N, c] by

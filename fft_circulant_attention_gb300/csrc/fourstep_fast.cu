@@ -122,6 +122,117 @@ fsf_pass_a(const T* __restrict__ V0, float2* __restrict__ scr0, const float2* __
   if (!early) pdl_trigger();
 }
 
+// Two storage elements (one packed pair) read from shared memory.
+__device__ __forceinline__ float2 sh_pair(const float* p) {
+  return *reinterpret_cast<const float2*>(p);
+}
+__device__ __forceinline__ float2 sh_pair(const __nv_bfloat16* p) {
+  unsigned int u = *reinterpret_cast<const unsigned int*>(p);
+  return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+}
+
+// ---------------------------------------------------------------------------
+// Pass A for N2 > 32, persistent and fed by tensor copies: each CTA takes
+// items (b, h, n1) in turn (item, item + grid, ...).  An item's V tile — the
+// N2 rows n1 + 512·n2 of the head's 64 columns — arrives by one tensor copy
+// into shared memory; as soon as every thread holds its 32 values, the next
+// item's copy is issued into the same buffer, so it loads while this item
+// is transformed.  The transform is fsf_pass_a's (step 1 radix 32, step 2
+// radix N2/32), with the step-2 twiddles in a shared table and the row
+// w_N^{n1·k2} fetched once per item (one value a thread).  ntens = 2: a
+// second tensor (tmV2 into scr2), its items after the first's.
+// ---------------------------------------------------------------------------
+template <typename T, int N2>
+struct PipeAT {
+  static constexpr int kTile = N2 * 64 * (int)sizeof(T);            // one V tile
+  static constexpr int kOffTile = 1024;
+  static constexpr int kOffTw2 = kOffTile + kTile;                   // [R2][32]
+  static constexpr int kOffTwRow = kOffTw2 + (N2 / 32) * 32 * 8;     // [N2]
+  static constexpr int kOffBuf = kOffTwRow + N2 * 8;                 // [32][N2 + 2]
+  static constexpr size_t kSmem = (size_t)kOffBuf + (size_t)kFastPairs * (N2 + 2) * 8;
+};
+
+template <typename T, int N2>
+__global__ void __launch_bounds__(N2, 2)
+fsf_pass_a_tma(const __grid_constant__ CUtensorMap tmV, float2* __restrict__ scr,
+               const float2* __restrict__ W, int N, int D, int H, int bh0, int nb,
+               unsigned int* status, const __grid_constant__ CUtensorMap tmV2,
+               float2* __restrict__ scr2, int ntens, int early) {
+  static_assert(N2 > 32 && N2 <= 256, "N2 = 32 takes fsf_pass_a32");
+  using P = PipeAT<T, N2>;
+  constexpr int TS = N2 / 32;        // warps; threads per signal
+  constexpr int R2 = N2 / 32;        // radix of step 2
+  constexpr int PER = 32 / TS;       // step-2 tasks per thread
+  constexpr int RS = N2 + 2;         // shared row of one pair
+  if (early) pdl_trigger();
+  extern __shared__ __align__(128) unsigned char sm[];
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm);
+  const T* tile = reinterpret_cast<const T*>(sm + P::kOffTile);
+  float2* tw2 = reinterpret_cast<float2*>(sm + P::kOffTw2);
+  float2* twrow = reinterpret_cast<float2*>(sm + P::kOffTwRow);
+  float2* buf = reinterpret_cast<float2*>(sm + P::kOffBuf);
+  const int t = threadIdx.x, lane = t & 31, j = t >> 5;
+  const int items1 = nb * kFastN1, items = ntens * items1;
+  const uint64_t keep = policy_evict_last(), stream = policy_evict_first();
+  auto issue = [&](int item) {
+    fence_proxy_async_smem();   // the CTA's reads of the tile come first
+    const int second = item >= items1, it1 = item - second * items1;
+    const int bh = bh0 + it1 % nb, n1 = it1 / nb;
+    const int b = bh / H, h = bh - b * H;
+    mbar_expect_tx(bar, P::kTile);
+    tma_load_4d_hint(sm + P::kOffTile, second ? &tmV2 : &tmV, h * 64, n1, 0, b, bar, stream);
+  };
+  if (t == 0) mbar_init(bar, 1);
+  mbar_fence_init();
+  {
+    const int wstep = N / N2;
+    for (int i = t; i < R2 * 32; i += N2) tw2[i] = W[(size_t)((i / 32) * (i % 32)) * wstep];
+  }
+  __syncthreads();
+  if (t == 0 && (int)blockIdx.x < items) issue(blockIdx.x);
+  // Launched as a dependent of the previous chunk's pass C, which reads the
+  // scratch slot this pass overwrites: the first tile loads meanwhile.
+  pdl_wait();
+  float2* row = buf + lane * RS;
+  int it = 0;
+  for (int item = blockIdx.x; item < items; item += gridDim.x, ++it) {
+    const bool ok = mbar_wait(bar, it & 1, status, 0x503);
+    if (__syncthreads_or(!ok)) return;
+    const int second = item >= items1, it1 = item - second * items1;
+    float2* dst = second ? scr2 : scr;
+    const int bhl = it1 % nb, n1 = it1 / nb;
+    const float2 tw = __ldg(&W[(size_t)n1 * t]);   // w_N^{n1·k2}, k2 = t
+    float2 a[32];
+#pragma unroll
+    for (int u = 0; u < 32; ++u) a[u] = sh_pair(tile + (j + TS * u) * 64 + 2 * lane);
+    __syncthreads();   // the tile is read; the previous item's row reads are done
+    if (t == 0 && item + (int)gridDim.x < items) issue(item + gridDim.x);
+    dft<32, false, CxPaired>(a);
+#pragma unroll
+    for (int q = 0; q < 32; q += 2) st_sh2(row + 32 * j + q, a[q], a[q + 1]);
+    twrow[t] = tw;
+    __syncthreads();
+    float2 c[PER][R2];
+#pragma unroll
+    for (int u = 0; u < R2; ++u)
+#pragma unroll
+      for (int e = 0; e < PER; e += 2) ld_sh2(row + PER * j + e + 32 * u, c[e][u], c[e + 1][u]);
+#pragma unroll
+    for (int e = 0; e < PER; ++e) {
+      const int k = PER * j + e;
+#pragma unroll
+      for (int u = 1; u < R2; ++u) c[e][u] = cmul(c[e][u], tw2[u * 32 + k]);
+      dft<R2, false, CxPaired>(c[e]);
+#pragma unroll
+      for (int q = 0; q < R2; ++q) {
+        const int k2 = k + 32 * q;
+        st_hint(dst + scr_idx(bhl, N2, k2, n1, lane), cmul(c[e][q], twrow[k2]), keep);
+      }
+    }
+  }
+  if (!early) pdl_trigger();
+}
+
 // ---------------------------------------------------------------------------
 // Pass C: the inverse of pass A's transform over k2, then the output rows.
 // ---------------------------------------------------------------------------
@@ -181,14 +292,6 @@ fsf_pass_c(const float2* scr, T* __restrict__ O, const float2* __restrict__ W, i
   if (!early) pdl_trigger();
 }
 
-// Two storage elements (one packed pair) read from shared memory.
-__device__ __forceinline__ float2 sh_pair(const float* p) {
-  return *reinterpret_cast<const float2*>(p);
-}
-__device__ __forceinline__ float2 sh_pair(const __nv_bfloat16* p) {
-  unsigned int u = *reinterpret_cast<const unsigned int*>(p);
-  return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
-}
 
 // ---------------------------------------------------------------------------
 // Pipelined passes A and C for N2 == 32.  Every warp runs its own pipeline
@@ -887,6 +990,7 @@ static cudaError_t setup_t(int N2) {
 #define CAT_N2(n)                                                   \
   case n:                                                           \
     e = allow_max_smem(fsf_pass_a<T, n>);                           \
+    if (e == cudaSuccess) e = allow_max_smem(fsf_pass_a_tma<T, n>); \
     if (e == cudaSuccess) e = allow_max_smem(fsf_pass_c<T, n>);     \
     if (e == cudaSuccess) e = allow_max_smem(fsf_zspec_a<n>);       \
     break;
@@ -909,9 +1013,44 @@ size_t fast_tables_bytes(int N2) {
   return ((size_t)(2 + N2) * kTabB + (N2 == 32 ? (size_t)32 * kFastN1 : 0)) * sizeof(float2);
 }
 
+// Resident CTAs per SM of the tensor-copy pass A at N2 (0 if it cannot run).
+template <typename T>
+static int pass_a_tma_per_sm(int N2) {
+  int n = 0;
+  cudaError_t e = cudaErrorInvalidValue;
+  switch (N2) {
+    case 64:
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fsf_pass_a_tma<T, 64>, 64,
+                                                        PipeAT<T, 64>::kSmem);
+      break;
+    case 128:
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fsf_pass_a_tma<T, 128>, 128,
+                                                        PipeAT<T, 128>::kSmem);
+      break;
+    case 256:
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fsf_pass_a_tma<T, 256>, 256,
+                                                        PipeAT<T, 256>::kSmem);
+      break;
+    default: break;
+  }
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
 cudaError_t setup_fast_kernels(cat_plan_s* p) {
   cudaError_t e = p->dtype == 1 ? setup_t<__nv_bfloat16>(p->fs.N2) : setup_t<float>(p->fs.N2);
   if (e != cudaSuccess) return e;
+  // The tensor-copy pass A for N2 >= 128 (at N2 = 64 the plain one was
+  // faster); CAT_PASS_A_TMA=0 / 1 forces the plain / tensor-copy one.
+  p->fs.a_tma_per_sm = 0;
+  const char* ea = std::getenv("CAT_PASS_A_TMA");
+  const bool use_tma = ea ? ea[0] != '0' : p->fs.N2 >= 128;
+  if (p->fs.N2 > 32 && use_tma)
+    p->fs.a_tma_per_sm = p->dtype == 1 ? pass_a_tma_per_sm<__nv_bfloat16>(p->fs.N2)
+                                       : pass_a_tma_per_sm<float>(p->fs.N2);
   fsf_build_tables<<<64, 256, 0, p->stream>>>(p->tabs, p->tw, p->N, p->fs.N2);
   e = cudaGetLastError();
   if (e == cudaSuccess) e = cudaStreamSynchronize(p->stream);
@@ -943,6 +1082,30 @@ static cudaError_t fast_launch(bool dep, void (*kernel)(KArgs...), int grid, int
   return cudaGetLastError();
 }
 
+// V viewed as [B][N2 (n2)][512 (n1)][D]: the box is one head's 64 columns of
+// the N2 rows n1 + 512·n2.
+template <typename T>
+static bool encode_v_map(const cat_plan_s* p, const T* V, CUtensorMap* tmV) {
+  const unsigned long long es = sizeof(T);
+  const unsigned long long dims[4] = {(unsigned long long)p->D, (unsigned long long)kFastN1,
+                                      (unsigned long long)p->fs.N2, (unsigned long long)p->B};
+  const unsigned long long strides[3] = {p->D * es, (unsigned long long)kFastN1 * p->D * es,
+                                         (unsigned long long)p->N * p->D * es};
+  const unsigned int box[4] = {64, 1, (unsigned int)p->fs.N2, 1};
+  return encode_map_4d(tmV, V, sizeof(T) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                              : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                       dims, strides, box);
+}
+
+// Grid of the tensor-copy pass A over `items` items: every CTA takes the
+// same number of items (the last ones possibly one fewer), at most the
+// resident CTAs of all SMs.
+static int pass_a_tma_grid(const cat_plan_s* p, int items) {
+  const int slots = p->fs.a_tma_per_sm * p->sms;
+  const int per_cta = (items + slots - 1) / slots;
+  return (items + per_cta - 1) / per_cta;
+}
+
 template <typename T, int N2>
 static cudaError_t launch_ac(const cat_plan_s* p, const T* V, T* O, float2* scr, int bh0,
                              int nb, bool pass_a, cudaStream_t st, bool dep) {
@@ -951,26 +1114,18 @@ static cudaError_t launch_ac(const cat_plan_s* p, const T* V, T* O, float2* scr,
   const int threads = N2;
   const size_t smem = fast_smem_a(N2);
   const int early = p->fast_pdl == 2;
+  CUtensorMap tm;
+  if (pass_a && p->fs.a_tma_per_sm > 0 && encode_v_map(p, V, &tm)) {
+    const int g = pass_a_tma_grid(p, grid);
+    return fast_launch(dep, fsf_pass_a_tma<T, N2>, g, N2, PipeAT<T, N2>::kSmem, st, tm, scr,
+                       (const float2*)p->tw, p->N, p->D, p->H, bh0, nb, p->status, tm, scr, 1,
+                       early);
+  }
   if (pass_a)
     return fast_launch(dep, fsf_pass_a<T, N2>, grid, threads, smem, st, V, scr, (const float2*)p->tw,
                        p->N, p->D, p->H, bh0, nb, (const T*)nullptr, (float2*)nullptr, early);
   return fast_launch(dep, fsf_pass_c<T, N2>, grid, threads, smem, st, (const float2*)scr, O,
                      (const float2*)p->tw, p->N, p->D, p->H, bh0, nb, early);
-}
-
-// V viewed as [B][N2 (n2)][512 (n1)][D]: the box is one head's 64 columns of
-// the 32 rows n1 + 512·n2 (N2 == 32 passes).
-template <typename T>
-static bool encode_v_map(const cat_plan_s* p, const T* V, CUtensorMap* tmV) {
-  const unsigned long long es = sizeof(T);
-  const unsigned long long dims[4] = {(unsigned long long)p->D, (unsigned long long)kFastN1,
-                                      (unsigned long long)p->fs.N2, (unsigned long long)p->B};
-  const unsigned long long strides[3] = {p->D * es, (unsigned long long)kFastN1 * p->D * es,
-                                         (unsigned long long)p->N * p->D * es};
-  const unsigned int box[4] = {64, 1, 32, 1};
-  return encode_map_4d(tmV, V, sizeof(T) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                              : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
-                       dims, strides, box);
 }
 
 cudaError_t launch_fast_zspec(const cat_plan_s* p, int row0, int nrows, cudaStream_t st) {
@@ -1113,31 +1268,70 @@ static cudaError_t pass_a32_pair(const cat_plan_s* p, const T* A, const T* Bm, i
   return cudaGetLastError();
 }
 
+// The correlation's pass A for N2 > 32 on dO (into s0) and V (into s1) in
+// one launch: the plain kernel on a doubled grid ...
+template <typename T, int N2>
+static cudaError_t corr_a_plain_t(const cat_plan_s* p, const T* g, const T* v, float2* s0,
+                                  float2* s1, int bh0, int nb, cudaStream_t st) {
+  fsf_pass_a<T, N2><<<2 * nb * kFastN1, N2, fast_smem_a(N2), st>>>(g, s0, p->tw, p->N, p->D,
+                                                                   p->H, bh0, nb, v, s1);
+  return cudaGetLastError();
+}
+
+// ... or the tensor-copy kernel over both tensors' items
+// (cudaErrorNotSupported when it cannot run: off, or a map that does not
+// encode).
+template <typename T, int N2>
+static cudaError_t corr_a_tma_t(const cat_plan_s* p, const T* g, const T* v, float2* s0,
+                                float2* s1, int bh0, int nb, cudaStream_t st) {
+  CUtensorMap tmA, tmB;
+  if (p->fs.a_tma_per_sm <= 0 || !encode_v_map(p, g, &tmA) || !encode_v_map(p, v, &tmB))
+    return cudaErrorNotSupported;
+  const int grid = pass_a_tma_grid(p, 2 * nb * kFastN1);
+  fsf_pass_a_tma<T, N2><<<grid, N2, PipeAT<T, N2>::kSmem, st>>>(
+      tmA, s0, p->tw, p->N, p->D, p->H, bh0, nb, p->status, tmB, s1, 2, 0);
+  return cudaGetLastError();
+}
+
+template <bool TMA, typename T>
+static cudaError_t corr_a_t(const cat_plan_s* p, const T* g, const T* v, float2* s0, float2* s1,
+                            int bh0, int nb, cudaStream_t st) {
+  switch (p->fs.N2) {
+#define CAT_CA(n)                                                              \
+  case n:                                                                      \
+    return TMA ? corr_a_tma_t<T, n>(p, g, v, s0, s1, bh0, nb, st)              \
+               : corr_a_plain_t<T, n>(p, g, v, s0, s1, bh0, nb, st);
+    CAT_CA(64) CAT_CA(128) CAT_CA(256)
+#undef CAT_CA
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+static cudaError_t corr_pass_a_tma(const cat_plan_s* p, const void* G, const void* V, float2* s0,
+                                   float2* s1, int bh0, int nb, cudaStream_t st) {
+  return p->dtype == 1 ? corr_a_t<true>(p, (const __nv_bfloat16*)G, (const __nv_bfloat16*)V, s0,
+                                        s1, bh0, nb, st)
+                       : corr_a_t<true>(p, (const float*)G, (const float*)V, s0, s1, bh0, nb, st);
+}
+
+static cudaError_t corr_pass_a_plain(const cat_plan_s* p, const void* G, const void* V,
+                                     float2* s0, float2* s1, int bh0, int nb, cudaStream_t st) {
+  return p->dtype == 1 ? corr_a_t<false>(p, (const __nv_bfloat16*)G, (const __nv_bfloat16*)V, s0,
+                                         s1, bh0, nb, st)
+                       : corr_a_t<false>(p, (const float*)G, (const float*)V, s0, s1, bh0, nb, st);
+}
+
 cudaError_t launch_fast_corr(const cat_plan_s* p, const void* G, const void* V, float2* y,
                              int bh0, int nb, cudaStream_t st, float2* s0, float2* s1) {
   if (!s0) s0 = p->scratch;
   if (!s1) s1 = p->scratch + p->scratch_bytes / 2 / sizeof(float2);
   if (p->fs.N2 != 32) {
-    // dO into s0 and V into s1 as one launch (a doubled grid).
-    const int grid = 2 * nb * kFastN1;
-    const size_t smem = fast_smem_a(p->fs.N2);
-    const int N2 = p->fs.N2;
-    if (p->dtype == 1) {
-      const __nv_bfloat16* g = (const __nv_bfloat16*)G;
-      const __nv_bfloat16* v = (const __nv_bfloat16*)V;
-      if (N2 == 64) fsf_pass_a<__nv_bfloat16, 64><<<grid, N2, smem, st>>>(g, s0, p->tw, p->N, p->D, p->H, bh0, nb, v, s1);
-      else if (N2 == 128) fsf_pass_a<__nv_bfloat16, 128><<<grid, N2, smem, st>>>(g, s0, p->tw, p->N, p->D, p->H, bh0, nb, v, s1);
-      else fsf_pass_a<__nv_bfloat16, 256><<<grid, N2, smem, st>>>(g, s0, p->tw, p->N, p->D, p->H, bh0, nb, v, s1);
-    } else {
-      const float* g = (const float*)G;
-      const float* v = (const float*)V;
-      if (N2 == 64) fsf_pass_a<float, 64><<<grid, N2, smem, st>>>(g, s0, p->tw, p->N, p->D, p->H, bh0, nb, v, s1);
-      else if (N2 == 128) fsf_pass_a<float, 128><<<grid, N2, smem, st>>>(g, s0, p->tw, p->N, p->D, p->H, bh0, nb, v, s1);
-      else fsf_pass_a<float, 256><<<grid, N2, smem, st>>>(g, s0, p->tw, p->N, p->D, p->H, bh0, nb, v, s1);
-    }
-    cudaError_t e = cudaGetLastError();
+    // dO into s0 and V into s1 as one launch (a doubled grid, or the
+    // tensor-copy pass A over both tensors' items).
+    cudaError_t e = corr_pass_a_tma(p, G, V, s0, s1, bh0, nb, st);
+    if (e == cudaErrorNotSupported) e = corr_pass_a_plain(p, G, V, s0, s1, bh0, nb, st);
     if (e != cudaSuccess) return e;
-    fsf_corr_b<<<nb * N2, 256, kSmemCorrB, st>>>(s0, s1, y, p->tabs, N2);
+    fsf_corr_b<<<nb * p->fs.N2, 256, kSmemCorrB, st>>>(s0, s1, y, p->tabs, p->fs.N2);
     return cudaGetLastError();
   }
   // N2 = 32: dO into s0 and V into s1 as one launch.
