@@ -507,6 +507,7 @@ cudaError_t setup_backward_kernels(const cat_plan_s* p) {
                             : allow_max_smem(corr_pass_a<__nv_bfloat16, false>))
                       : (tw ? allow_max_smem(corr_pass_a<float, true>)
                             : allow_max_smem(corr_pass_a<float, false>));
+  if (e == cudaSuccess && p->dtype == 1) e = setup_dense_mma();
   return e;
 }
 
@@ -644,6 +645,15 @@ template <typename T>
 static cudaError_t dense_t(const cat_plan_s* p, const T* X, const T* WA, T* dX, T* dWA) {
   const BwCfg& w = p->bw;
   const long long tokens = (long long)p->B * p->N;
+  if (dense_mma_ok(p, X, dX)) {
+    const int ns = dwa_mma_splits(p, w.wsplit);
+    cudaError_t e = launch_dwa_mma(p, X, p->bw_wpart, ns);
+    if (e != cudaSuccess) return e;
+    dwa_reduce_kernel<T><<<(p->D * p->H + 255) / 256, 256, 0, p->stream>>>(p->bw_wpart, dWA, ns,
+                                                                          p->D, p->H);
+    e = cudaGetLastError();
+    return e == cudaSuccess ? launch_dx_mma(p, WA, dX) : e;
+  }
   const int dchunks = (p->D + kDwThreads * kDwDpt - 1) / (kDwThreads * kDwDpt);
   const int hchunks = (p->H + kDwH - 1) / kDwH;
   const long long tps = (tokens + w.wsplit - 1) / w.wsplit;

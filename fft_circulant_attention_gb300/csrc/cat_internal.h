@@ -335,6 +335,16 @@ cudaError_t launch_fast_corr(const cat_plan_s* p, const void* G, const void* V, 
                              int bh0, int nb, cudaStream_t st, float2* s0 = nullptr,
                              float2* s1 = nullptr);
 // Its pass C for N2 = 32: dz* rows [bh0, bh0 + nb) from y.
+// Tensor-core dW_A and dX for bf16 data (dense_mma.cu): whether they serve
+// this plan and these pointers, their one-time attribute set-up, the token
+// splits of dW_A's partial sums (at most `most`), and the launches (dW_A's
+// partial sums into part[nsplit][H][D], dX from the plan's dz).
+bool dense_mma_ok(const cat_plan_s* p, const void* X, const void* dX);
+cudaError_t setup_dense_mma();
+int dwa_mma_splits(const cat_plan_s* p, int most);
+cudaError_t launch_dwa_mma(const cat_plan_s* p, const void* X, float* part, int nsplit);
+cudaError_t launch_dx_mma(const cat_plan_s* p, const void* WA, void* dX);
+
 cudaError_t launch_fast_corr_c32(const cat_plan_s* p, const float2* y, float* dzs, int bh0,
                                  int nb, cudaStream_t st);
 

@@ -12,6 +12,7 @@
 #include "bulk.cuh"
 #include "cat_internal.h"
 #include "elem.cuh"
+#include "mma.cuh"
 
 namespace cat {
 
@@ -411,15 +412,6 @@ constexpr int kMmaWarps = 4;
 constexpr int kMmaTilesPerWarp = 2;
 constexpr int kMmaTokPerCta = kMmaWarps * kMmaTilesPerWarp * 16;
 
-__device__ __forceinline__ void mma_bf16(float (&d)[4], const unsigned (&a)[4], unsigned b0,
-                                         unsigned b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};\n"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
 // Row stride (bf16) of W_A^T in shared memory: D padded so that the eight
 // head rows a quarter-warp reads fall in distinct bank groups.
 __host__ __device__ inline int mma_wt_stride(int D) { return D + ((32 - D % 64) + 64) % 64; }
@@ -514,12 +506,6 @@ __host__ __device__ inline int ts_wt_stride(int D) { return D + 8; }
 static size_t score_tma_smem(int D) {
   return (size_t)kTsStages * kTsStageBytes + (size_t)16 * ts_wt_stride(D) * 2 + 2 * kTsStages * 8 +
          1024;
-}
-
-__device__ __forceinline__ void ldmatrix_x4(unsigned (&r)[4], uint32_t addr) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
 }
 
 template <int NT>

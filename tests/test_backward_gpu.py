@@ -114,7 +114,8 @@ def parity_bw(B, N, D, H, dtype, seed=0, wa_scale=1.0, mode="auto"):
 # Shapes covering every forward path the dV product takes (block FFT,
 # square-length register kernel, generic four-step, fast four-step with
 # N2 = 32 and 64) and both correlation layouts (whole rows up to 4096,
-# four-step split above), odd head widths, prime and tiny N.
+# four-step split above), odd head widths, prime and tiny N, and both
+# kernels of the dense gradients (FP32, tensor cores).
 SHAPES = [
     (1, 1, 4, 2, "f32"),
     (1, 2, 4, 1, "f32"),
@@ -132,6 +133,11 @@ SHAPES = [
     (1, 20000, 4, 2, "f32"),
     (1, 16384, 128, 2, "bf16"),
     (1, 32768, 64, 1, "f32"),
+    # bf16 with D a multiple of 64 (the tensor-core dW_A and dX): a column
+    # group past D, an odd head count, token tiles across batch rows and a
+    # ragged last tile.
+    (3, 1000, 192, 3, "bf16"),
+    (2, 4096, 320, 5, "bf16"),
 ]
 
 
