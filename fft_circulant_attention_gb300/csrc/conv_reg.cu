@@ -117,7 +117,7 @@ conv_reg_kernel(const T* __restrict__ V, T* __restrict__ O, const float2* zf,
 
   float2 a[M];
   ld_rows<T, M>(a, V + base, (size_t)M * D, (size_t)i * D, active, pair, aligned);
-  dft<M, false>(a);
+  dft<M, false, CxPaired>(a);
   // V's loads and first transform may overlap the spectrum kernel ahead
   // (launched as its programmatic dependent); its output is read only now.
   pdl_wait();
@@ -142,10 +142,10 @@ conv_reg_kernel(const T* __restrict__ V, T* __restrict__ O, const float2* zf,
   // Step 2: k2 = i.  Each thread reads and rewrites only its own M slots.
 #pragma unroll
   for (int n1 = 0; n1 < M; ++n1) a[n1] = buf[(i * M + n1) * P + p];
-  dft<M, false>(a);
+  dft<M, false, CxPaired>(a);
 #pragma unroll
   for (int k1 = 0; k1 < M; ++k1) a[k1] = cmul(a[k1], zs[i + M * k1]);
-  dft<M, true>(a);
+  dft<M, true, CxPaired>(a);
 #pragma unroll
   for (int n1 = 0; n1 < M; ++n1) buf[(i * M + n1) * P + p] = TW ? cmulc(a[n1], tw[n1 * M + i]) : a[n1];
   __syncthreads();
@@ -153,7 +153,7 @@ conv_reg_kernel(const T* __restrict__ V, T* __restrict__ O, const float2* zf,
   // Step 3: n1 = i.
 #pragma unroll
   for (int k2 = 0; k2 < M; ++k2) a[k2] = buf[(k2 * M + i) * P + p];
-  dft<M, true>(a);
+  dft<M, true, CxPaired>(a);
   if (active) {
 #pragma unroll
     for (int n2 = 0; n2 < M; ++n2)
@@ -214,24 +214,24 @@ corr_reg_kernel(const T* __restrict__ Q, const T* __restrict__ K, float2* __rest
     // to shared memory and K's product reads them there.
     float2 a[M];
     ld_rows<T, M>(a, Q + base, (size_t)M * D, (size_t)i * D, active, pair, aligned);
-    dft<M, false>(a);
+    dft<M, false, CxPaired>(a);
     __syncthreads();   // the previous pass's sums have read bq; twiddles ready
 #pragma unroll
     for (int k2 = 0; k2 < M; ++k2) bq[(k2 * M + i) * P + p] = TW ? cmul(a[k2], tw[i * M + k2]) : a[k2];
     ld_rows<T, M>(a, K + base, (size_t)M * D, (size_t)i * D, active, pair, aligned);
-    dft<M, false>(a);
+    dft<M, false, CxPaired>(a);
 #pragma unroll
     for (int k2 = 0; k2 < M; ++k2) bk[(k2 * M + i) * P + p] = TW ? cmul(a[k2], tw[i * M + k2]) : a[k2];
     __syncthreads();
     // Step 2 (k2 = i): each thread reads and rewrites only its own slots.
 #pragma unroll
     for (int n1 = 0; n1 < M; ++n1) a[n1] = bq[(i * M + n1) * P + p];
-    dft<M, false>(a);
+    dft<M, false, CxPaired>(a);
 #pragma unroll
     for (int k1 = 0; k1 < M; ++k1) bq[(i * M + k1) * P + p] = a[k1];
 #pragma unroll
     for (int n1 = 0; n1 < M; ++n1) a[n1] = bk[(i * M + n1) * P + p];
-    dft<M, false>(a);
+    dft<M, false, CxPaired>(a);
 #pragma unroll
     for (int k1 = 0; k1 < M; ++k1)
       bq[(i * M + k1) * P + p] = cmulc(bq[(i * M + k1) * P + p], a[k1]);
@@ -254,7 +254,7 @@ corr_reg_kernel(const T* __restrict__ Q, const T* __restrict__ K, float2* __rest
   if (t < M) {   // k2 = t: inverse over k1, to [n1][k2]
 #pragma unroll
     for (int k1 = 0; k1 < M; ++k1) a[k1] = S[t * M + k1];
-    dft<M, true>(a);
+    dft<M, true, CxPaired>(a);
 #pragma unroll
     for (int n1 = 0; n1 < M; ++n1) bk[n1 * M + t] = TW ? cmulc(a[n1], tw[n1 * M + t]) : a[n1];
   }
@@ -262,7 +262,7 @@ corr_reg_kernel(const T* __restrict__ Q, const T* __restrict__ K, float2* __rest
   if (t < M) {   // n1 = t: inverse over k2
 #pragma unroll
     for (int k2 = 0; k2 < M; ++k2) a[k2] = bk[t * M + k2];
-    dft<M, true>(a);
+    dft<M, true, CxPaired>(a);
 #pragma unroll
     for (int n2 = 0; n2 < M; ++n2) {
       const float v = a[n2].x * scale;
@@ -367,7 +367,7 @@ softmax_spectrum_reg(const float2* z, float* __restrict__ zs,
     a[n2].x *= inv;
     if (act) out[i + M * n2] = a[n2].x;
   }
-  dft<M, false>(a);
+  dft<M, false, CxPaired>(a);
   float2* xr = xb + r * M * RS;
   if (i < M) {
 #pragma unroll
@@ -378,7 +378,7 @@ softmax_spectrum_reg(const float2* z, float* __restrict__ zs,
 #pragma unroll
     for (int n1 = 0; n1 < M; ++n1) a[n1] = xr[i * RS + n1];
   }
-  dft<M, false>(a);
+  dft<M, false, CxPaired>(a);
   if (act) {
     const float invN = 1.0f / (float)N;
     float2* spec = zf + (size_t)row * N + i;
@@ -425,7 +425,7 @@ __device__ __forceinline__ void spec_q4_step(const float2* __restrict__ in, floa
   float2 a[8];
 #pragma unroll
   for (int m = 0; m < 8; ++m) a[m] = in[g * LD + q + 4 * m];
-  dft<8, INV>(a);
+  dft<8, INV, CxPaired>(a);
   float2* mine = ex + g * 33;
 #pragma unroll
   for (int ka = 0; ka < 8; ++ka)
