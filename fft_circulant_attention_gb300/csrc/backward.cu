@@ -547,7 +547,11 @@ static cudaError_t corr_t(const cat_plan_s* p, const T* G, const T* V) {
 // of 4 rows alternately on the plan's two internal streams: chunk c uses the
 // half c mod 2 of both scratch slots (dO's and V's spectra) and of the
 // one-signal buffer y, so two chunks are in flight in the same 64 MB.
-static cudaError_t corr_fast_overlapped(const cat_plan_s* p, const void* G, const void* V) {
+// With dV given, each chunk then runs the forward's passes B and C on dO's
+// transform, still in its half slot (the spectrum of the reversed scores
+// must be in zf): dV = circ(z*)^T dO without transforming dO a second time.
+static cudaError_t corr_fast_overlapped(const cat_plan_s* p, const void* G, const void* V,
+                                        void* dV) {
   const int rows = p->B * p->H;
   const int cb = p->fs.chunk_bh / 2;
   const size_t half = p->scratch_bytes / 4 / sizeof(float2);   // a half slot
@@ -560,6 +564,7 @@ static cudaError_t corr_fast_overlapped(const cat_plan_s* p, const void* G, cons
     float2* s1 = p->scratch + 2 * half + (size_t)k * half;
     // Each chunk's y at its own rows: pass C runs once for all rows below.
     e = launch_fast_corr(p, G, V, p->bw_scr + (size_t)bh0 * p->N, bh0, nb, p->side[k], s0, s1);
+    if (e == cudaSuccess && dV) e = launch_fast_bc32(p, s0, dV, bh0, nb, k * cb, p->side[k]);
   }
   for (int k = 0; k < 2; ++k) {
     cudaError_t e2 = cudaEventRecord(p->ev_join[k], p->side[k]);
@@ -570,11 +575,14 @@ static cudaError_t corr_fast_overlapped(const cat_plan_s* p, const void* G, cons
   return e;
 }
 
-static cudaError_t corr_fast(const cat_plan_s* p, const void* G, const void* V) {
+static bool corr_overlapped(const cat_plan_s* p) {
+  return p->bw.fast && p->bw.N2 == 32 && p->fs.chunk_bh >= 2 && p->fs.chunk_bh % 2 == 0;
+}
+
+static cudaError_t corr_fast(const cat_plan_s* p, const void* G, const void* V, void* dV) {
   const BwCfg& w = p->bw;
   const int rows = p->B * p->H;
-  if (w.N2 == 32 && p->fs.chunk_bh >= 2 && p->fs.chunk_bh % 2 == 0)
-    return corr_fast_overlapped(p, G, V);
+  if (corr_overlapped(p)) return corr_fast_overlapped(p, G, V, dV);
   for (int bh0 = 0; bh0 < rows; bh0 += w.chunk_bh) {
     const int nb = rows - bh0 < w.chunk_bh ? rows - bh0 : w.chunk_bh;
     cudaError_t e = launch_fast_corr(p, G, V, p->bw_scr, bh0, nb, p->stream);
@@ -591,16 +599,22 @@ static cudaError_t corr_fast(const cat_plan_s* p, const void* G, const void* V) 
   return cudaSuccess;
 }
 
-cudaError_t launch_backward_dz(const cat_plan_s* p, const void* G, const void* V) {
+bool backward_dv_in_corr(const cat_plan_s* p) {
+  const char* e = std::getenv("CAT_BW_DV_CORR");
+  return corr_overlapped(p) && !(e && e[0] == '0');
+}
+
+cudaError_t launch_backward_dz(const cat_plan_s* p, const void* G, const void* V, void* dV) {
   const int rows = p->B * p->H;
   if (rows == 0) return cudaSuccess;
+  if (dV && !backward_dv_in_corr(p)) return cudaErrorInvalidValue;
   // Square lengths with a register transform (N = 8², 14², 16², 32²) take
   // the register correlation kernel; CAT_BW_REG=0 keeps the block passes.
   const char* env = std::getenv("CAT_BW_REG");
   const bool reg = !p->bw.fast && !p->twod && p->path == PATH_SMEM && p->sm.reg_m > 0 &&
                    !(env && std::strcmp(env, "0") == 0);
   if (reg && corr_reg_split_fits(p)) return launch_corr_reg_split(p, G, V);
-  const cudaError_t e = p->bw.fast ? corr_fast(p, G, V)
+  const cudaError_t e = p->bw.fast ? corr_fast(p, G, V, dV)
       : reg           ? launch_corr_reg(p, G, V, p->bw_dzs)
       : p->dtype == 1 ? corr_t<__nv_bfloat16, true>(p, (const __nv_bfloat16*)G, (const __nv_bfloat16*)V)
                       : corr_t<float, true>(p, (const float*)G, (const float*)V);

@@ -1180,11 +1180,25 @@ namespace {
 
 // The backward's schedule: score, softmax, the correlation and the softmax
 // backward (dz* and dz), then dW_A, dX and dV = circ(z*)^T dO, the forward's
-// own spectrum and product on the scores reversed.  On the fast path dV runs
-// the forward's overlapped schedule with dW_A and dX (which need only dz) on
-// the plan's stream beside its chunks.
+// own spectrum and product on the scores reversed.  On the fast path with
+// N2 = 32 the reversed scores' spectrum comes first and every correlation
+// chunk finishes its rows of dV from its own transform of dO; on the other
+// fast shapes dV runs the forward's overlapped schedule with dW_A and dX
+// (which need only dz) on the plan's stream beside its chunks.
 cudaError_t backward_schedule(cat_plan_s* p, const void* X, const void* WA, const void* V,
                               const void* dO, void* dX, void* dWA, void* dV) {
+  if (p->path == cat::PATH_FAST && cat::backward_dv_in_corr(p)) {
+    // z* (zs) from the scores, then the scores reversed and their spectrum,
+    // so that the correlation's chunks give dV from their own transform of
+    // dO; dW_A and dX once dz is complete.
+    cudaError_t e = cat::launch_score(p, X, WA);
+    if (e == cudaSuccess) e = cat::launch_softmax(p);
+    if (e == cudaSuccess) e = cat::launch_reverse_scores(p);
+    if (e == cudaSuccess) e = cat::launch_fast_zspec(p, 0, p->B * p->H, p->stream);
+    if (e == cudaSuccess) e = cat::launch_backward_dz(p, dO, V, dV);
+    if (e == cudaSuccess) e = cat::launch_backward_dense(p, X, WA, dX, dWA);
+    return e;
+  }
   if (run_backward_front(p, X, WA, V, dO) != CAT_OK) return cudaErrorLaunchFailure;
   if (p->path == cat::PATH_FAST) {
     cudaError_t e = cat::launch_reverse_scores(p);

@@ -314,12 +314,16 @@ cudaError_t setup_fast_kernels(cat_plan_s* p);
 size_t fast_tables_bytes(int N2);
 
 // Backward pass (backward.cu).  launch_backward_dz: correlation passes and
-// softmax backward into bw_dzs and bw_dz (needs z* in zs).
+// softmax backward into bw_dzs and bw_dz (needs z* in zs); with dV, also
+// dV from the correlation's own transform of G (only where
+// backward_dv_in_corr holds, and with the reversed scores' spectrum in zf).
 // launch_backward_dense: dW_A and dX from bw_dz.  launch_reverse_scores:
 // z2[n] <-> z2[(-n) mod N] in every row, so that the forward's spectrum and
 // product kernels then give circ(z*)^T.
 cudaError_t setup_backward_kernels(const cat_plan_s* p);
-cudaError_t launch_backward_dz(const cat_plan_s* p, const void* G, const void* V);
+bool backward_dv_in_corr(const cat_plan_s* p);
+cudaError_t launch_backward_dz(const cat_plan_s* p, const void* G, const void* V,
+                               void* dV = nullptr);
 cudaError_t launch_backward_dense(const cat_plan_s* p, const void* X, const void* WA, void* dX,
                                   void* dWA);
 cudaError_t launch_reverse_scores(const cat_plan_s* p);
@@ -345,6 +349,11 @@ int dwa_mma_splits(const cat_plan_s* p, int most);
 cudaError_t launch_dwa_mma(const cat_plan_s* p, const void* X, float* part, int nsplit);
 cudaError_t launch_dx_mma(const cat_plan_s* p, const void* WA, void* dX);
 
+// Passes B and C (N2 = 32) on rows whose pass-A output already sits in
+// scratch slot 0 (rows row_off .. row_off + nb - 1 of its tensor map, at
+// scr), with the spectrum in p->zf, into O.
+cudaError_t launch_fast_bc32(const cat_plan_s* p, float2* scr, void* O, int bh0, int nb,
+                             int row_off, cudaStream_t st);
 cudaError_t launch_fast_corr_c32(const cat_plan_s* p, const float2* y, float* dzs, int bh0,
                                  int nb, cudaStream_t st);
 

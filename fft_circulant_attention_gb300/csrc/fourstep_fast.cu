@@ -386,7 +386,8 @@ template <typename T>
 __global__ void __launch_bounds__(PipeC::kWarps * 32)
 fsf_pass_c32(const __grid_constant__ CUtensorMap tmC, const float2* __restrict__ scr,
              T* __restrict__ O, int N, int D, int H, int bh0, int nb, unsigned int* status,
-             int early) {
+             int early, int row_off) {
+  // row_off: the chunk's first row in tmC (scr points at that row).
   if (early) pdl_trigger();
   using P = PipeC;
   extern __shared__ __align__(128) unsigned char sm[];
@@ -403,7 +404,8 @@ fsf_pass_c32(const __grid_constant__ CUtensorMap tmC, const float2* __restrict__
     if (lane == 0) {
       fence_proxy_async_smem();   // the warp's reads of this stage come first
       mbar_expect_tx(bar + s, 32 * P::kRowBytes);
-      tma_load_4d(stage + s * 32 * P::kRowBytes, &tmC, 0, item / nb, 0, item % nb, bar + s);
+      tma_load_4d(stage + s * 32 * P::kRowBytes, &tmC, 0, item / nb, 0, row_off + item % nb,
+                  bar + s);
     }
   };
   pdl_wait();   // pass B ahead on the stream wrote the scratch
@@ -1195,7 +1197,7 @@ static cudaError_t chunk_t(const cat_plan_s* p, const T* V, T* O, int bh0, int n
         if (grid > 2 * p->sms) grid = 2 * p->sms;
         return fast_launch(dep, fsf_pass_c32<T>, grid, PipeC::kWarps * 32, PipeC::kSmem, st,
                            p->tm_c[slot], (const float2*)scr, O, p->N, p->D, p->H, bh0, nb,
-                           p->status, early);
+                           p->status, early, 0);
       }
       case 64: return launch_ac<T, 64>(p, V, O, scr, bh0, nb, pass_a, st, dep);
       case 128: return launch_ac<T, 128>(p, V, O, scr, bh0, nb, pass_a, st, dep);
@@ -1231,6 +1233,32 @@ cudaError_t launch_fast_chunk(const cat_plan_s* p, const void* V, void* O, int b
   }
   if (p->fs.N2 == 32 && !encode_v_map(p, (const float*)V, &tmV)) return cudaErrorInvalidValue;
   return chunk_t(p, (const float*)V, (float*)O, bh0, nb, slot, st, &tmV, before_b, after, dep_a);
+}
+
+// Passes B and C (N2 = 32) of the product on rows [bh0, bh0 + nb) whose
+// pass-A output is already at scr: rows row_off .. row_off + nb - 1 of
+// scratch slot 0 (the backward's correlation leaves dO's transform there).
+// Pass B multiplies by the spectrum in p->zf; pass C writes O.
+template <typename T>
+static cudaError_t bc32_t(const cat_plan_s* p, float2* scr, T* O, int bh0, int nb, int row_off,
+                          cudaStream_t st) {
+  const int early = p->fast_pdl == 2;
+  fsf_pass_b<<<nb * 32 * (kFastPairs / kBPairs), kBPairs * 16, kSmemB, st>>>(
+      scr, p->zf, p->tabs, 32, bh0, early);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  int grid = (nb * kFastN1 + PipeC::kWarps - 1) / PipeC::kWarps;
+  if (grid > 2 * p->sms) grid = 2 * p->sms;
+  return fast_launch(p->fast_pdl != 0, fsf_pass_c32<T>, grid, PipeC::kWarps * 32, PipeC::kSmem,
+                     st, p->tm_c[0], (const float2*)scr, O, p->N, p->D, p->H, bh0, nb, p->status,
+                     early, row_off);
+}
+
+cudaError_t launch_fast_bc32(const cat_plan_s* p, float2* scr, void* O, int bh0, int nb,
+                             int row_off, cudaStream_t st) {
+  if (p->fs.N2 != 32 || row_off + nb > p->fs.chunk_bh) return cudaErrorInvalidValue;
+  return p->dtype == 1 ? bc32_t(p, scr, (__nv_bfloat16*)O, bh0, nb, row_off, st)
+                       : bc32_t(p, scr, (float*)O, bh0, nb, row_off, st);
 }
 
 int fast_chunks(const cat_plan_s* p) {
