@@ -61,8 +61,12 @@ __device__ __forceinline__ void ld_sh2(const float2* p, float2& a, float2& b) {
 template <typename T, int N2>
 __global__ void __launch_bounds__(256)
 fsf_pass_a(const T* __restrict__ V0, float2* __restrict__ scr0, const float2* __restrict__ W,
-           int N, int D, int H, int bh0, int nb, const T* __restrict__ V1 = nullptr,
-           float2* __restrict__ scr1 = nullptr, int early = 0) {
+           const float2* __restrict__ tf, int N, int D, int H, int bh0, int nb,
+           const T* __restrict__ V1 = nullptr, float2* __restrict__ scr1 = nullptr,
+           int early = 0) {
+  // W: w_N^m (the row twiddles w_N^{n1·k2}); tf[k][u] = w_512^{u·k}, whose
+  // entry (k, (16 / R2)·u) is the step-2 twiddle w_N2^{u·k} (a 4 KB table
+  // that stays in L1).
   static_assert(N2 > 32, "N2 = 32 takes fsf_pass_a32");
   if (early) pdl_trigger();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -99,7 +103,6 @@ fsf_pass_a(const T* __restrict__ V0, float2* __restrict__ scr0, const float2* __
     for (int u = 0; u < R2; ++u)
 #pragma unroll
       for (int e = 0; e < PER; e += 2) ld_sh2(row + PER * j + e + 32 * u, c[e][u], c[e + 1][u]);
-    const int wstep = N / N2;
     // The scratch is read again by passes B and C: keep it in L2.
     const uint64_t keep = policy_evict_last();
     // Launched as a dependent of the previous chunk's pass C, which reads
@@ -109,7 +112,7 @@ fsf_pass_a(const T* __restrict__ V0, float2* __restrict__ scr0, const float2* __
     for (int e = 0; e < PER; ++e) {
       const int k = PER * j + e;
 #pragma unroll
-      for (int u = 1; u < R2; ++u) c[e][u] = cmul(c[e][u], __ldg(&W[(size_t)(u * k) * wstep]));
+      for (int u = 1; u < R2; ++u) c[e][u] = cmul(c[e][u], __ldg(&tf[k * 16 + (16 / R2) * u]));
       dft<R2, false>(c[e]);
 #pragma unroll
       for (int s = 0; s < R2; ++s) {
@@ -238,8 +241,9 @@ fsf_pass_a_tma(const __grid_constant__ CUtensorMap tmV, float2* __restrict__ scr
 // ---------------------------------------------------------------------------
 template <typename T, int N2>
 __global__ void __launch_bounds__(256)
-fsf_pass_c(const float2* scr, T* __restrict__ O, const float2* __restrict__ W, int N, int D,
+fsf_pass_c(const float2* scr, T* __restrict__ O, const float2* __restrict__ tf, int N, int D,
            int H, int bh0, int nb, int early = 0) {
+  // tf[k][u] = w_512^{u·k}: entry (k, (16 / R2)·u) is the step-2 twiddle.
   static_assert(N2 > 32, "N2 = 32 takes fsf_pass_c32");
   if (early) pdl_trigger();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -276,14 +280,13 @@ fsf_pass_c(const float2* scr, T* __restrict__ O, const float2* __restrict__ W, i
     for (int u = 0; u < R2; ++u)
 #pragma unroll
       for (int e = 0; e < PER; e += 2) ld_sh2(row + PER * j + e + 32 * u, c[e][u], c[e + 1][u]);
-    const int wstep = N / N2;
     T* dst = O + ((size_t)b * N + n1) * D + h * 64 + 2 * lane;
     const size_t rs = (size_t)kFastN1 * D;
 #pragma unroll
     for (int e = 0; e < PER; ++e) {
       const int k = PER * j + e;
 #pragma unroll
-      for (int u = 1; u < R2; ++u) c[e][u] = cmulc(c[e][u], __ldg(&W[(size_t)(u * k) * wstep]));
+      for (int u = 1; u < R2; ++u) c[e][u] = cmulc(c[e][u], __ldg(&tf[k * 16 + (16 / R2) * u]));
       dft<R2, true>(c[e]);
 #pragma unroll
       for (int s = 0; s < R2; ++s) st_pair(dst + (size_t)(k + 32 * s) * rs, c[e][s]);
@@ -786,7 +789,11 @@ __global__ void fsf_build_tables(float2* __restrict__ tabs, const float2* __rest
 template <int N2>
 __global__ void __launch_bounds__(256)
 fsf_zspec_a(const float2* __restrict__ z2, const float2* __restrict__ part, int P,
-            float2* __restrict__ zscr, const float2* __restrict__ W, int N) {
+            float2* __restrict__ zscr, const float2* __restrict__ W, int N,
+            const float2* __restrict__ tf) {
+  // tf[k][u] = w_512^{u·k} (k < 32, u < 16), the plan's first table: the
+  // step-2 twiddle w_N2^{u·k} is tf[k][(16 / R2)·u], a 4 KB table that stays
+  // in L1 (the full table W is N entries).
   __shared__ float stats[2];
   static_assert(N2 > 32, "N2 = 32 rows take fsf_zspec_row");
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -819,13 +826,12 @@ fsf_zspec_a(const float2* __restrict__ z2, const float2* __restrict__ part, int 
     for (int u = 0; u < R2; ++u)
 #pragma unroll
       for (int e = 0; e < PER; e += 2) ld_sh2(rb + PER * j + e + 32 * u, c[e][u], c[e + 1][u]);
-    const int wstep = N / N2;
     float2* dst = zscr + (size_t)row * N + n1;
 #pragma unroll
     for (int e = 0; e < PER; ++e) {
       const int k = PER * j + e;
 #pragma unroll
-      for (int u = 1; u < R2; ++u) c[e][u] = cmul(c[e][u], __ldg(&W[(size_t)(u * k) * wstep]));
+      for (int u = 1; u < R2; ++u) c[e][u] = cmul(c[e][u], __ldg(&tf[k * 16 + (16 / R2) * u]));
       dft<R2, false>(c[e]);
 #pragma unroll
       for (int s = 0; s < R2; ++s) {
@@ -837,8 +843,9 @@ fsf_zspec_a(const float2* __restrict__ z2, const float2* __restrict__ part, int 
 }
 
 __global__ void __launch_bounds__(128)
-fsf_zspec_b(const float2* __restrict__ zscr, float2* __restrict__ zft, const float2* __restrict__ W,
+fsf_zspec_b(const float2* __restrict__ zscr, float2* __restrict__ zft, const float2* __restrict__ tf,
             int N, int N2) {
+  // tf[k][u] = w_512^{u·k}: the step-F2 twiddles, 16 a bin pair.
   extern __shared__ float4 smem4[];
   float2* buf = reinterpret_cast<float2*>(smem4);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -847,7 +854,6 @@ fsf_zspec_b(const float2* __restrict__ zscr, float2* __restrict__ zft, const flo
   const int per_row = N2 / 8;
   const int row = blockIdx.x / per_row;
   const int k2 = (blockIdx.x % per_row) * 8 + pl;
-  const int wstep = N / kFastN1;
   float2* rb = buf + pl * kRowB;
   const float2* src = zscr + (size_t)row * N + (size_t)k2 * kFastN1;
   float2 a[32];
@@ -862,9 +868,13 @@ fsf_zspec_b(const float2* __restrict__ zscr, float2* __restrict__ zft, const flo
   for (int u = 0; u < 16; ++u) ld_sh2(rb + 2 * j + 32 * u, c[0][u], c[1][u]);
 #pragma unroll
   for (int e = 0; e < 2; ++e) {
-    const int k = 2 * j + e;
+    const float4* tw = reinterpret_cast<const float4*>(tf + (2 * j + e) * 16);
 #pragma unroll
-    for (int u = 1; u < 16; ++u) c[e][u] = cmul(c[e][u], __ldg(&W[(size_t)(u * k) * wstep]));
+    for (int u = 0; u < 16; u += 2) {
+      const float4 w = __ldg(tw + u / 2);
+      if (u > 0) c[e][u] = cmul(c[e][u], make_float2(w.x, w.y));
+      c[e][u + 1] = cmul(c[e][u + 1], make_float2(w.z, w.w));
+    }
     dft<16, false>(c[e]);
   }
   const float invN = 1.0f / (float)N;
@@ -1125,9 +1135,10 @@ static cudaError_t launch_ac(const cat_plan_s* p, const T* V, T* O, float2* scr,
   }
   if (pass_a)
     return fast_launch(dep, fsf_pass_a<T, N2>, grid, threads, smem, st, V, scr, (const float2*)p->tw,
-                       p->N, p->D, p->H, bh0, nb, (const T*)nullptr, (float2*)nullptr, early);
+                       (const float2*)p->tabs, p->N, p->D, p->H, bh0, nb, (const T*)nullptr,
+                       (float2*)nullptr, early);
   return fast_launch(dep, fsf_pass_c<T, N2>, grid, threads, smem, st, (const float2*)scr, O,
-                     (const float2*)p->tw, p->N, p->D, p->H, bh0, nb, early);
+                     (const float2*)p->tabs, p->N, p->D, p->H, bh0, nb, early);
 }
 
 cudaError_t launch_fast_zspec(const cat_plan_s* p, int row0, int nrows, cudaStream_t st) {
@@ -1156,13 +1167,13 @@ cudaError_t launch_fast_zspec(const cat_plan_s* p, int row0, int nrows, cudaStre
 #define CAT_ZA(n)                                                                      \
   case n:                                                                              \
     fsf_zspec_a<n><<<nrows * (kFastN1 / 32), n, fast_smem_a(n), st>>>(z2, part, P, zscr, \
-                                                                      p->tw, p->N);    \
+                                                                      p->tw, p->N, p->tabs); \
     break;
     CAT_ZA(64) CAT_ZA(128) CAT_ZA(256)
 #undef CAT_ZA
     default: return cudaErrorInvalidValue;
   }
-  fsf_zspec_b<<<nrows * (N2 / 8), 128, fast_smem_b() / 2, st>>>(zscr, zf, p->tw, p->N, N2);
+  fsf_zspec_b<<<nrows * (N2 / 8), 128, fast_smem_b() / 2, st>>>(zscr, zf, p->tabs, p->N, N2);
   return cudaGetLastError();
 }
 
@@ -1301,7 +1312,7 @@ static cudaError_t pass_a32_pair(const cat_plan_s* p, const T* A, const T* Bm, i
 template <typename T, int N2>
 static cudaError_t corr_a_plain_t(const cat_plan_s* p, const T* g, const T* v, float2* s0,
                                   float2* s1, int bh0, int nb, cudaStream_t st) {
-  fsf_pass_a<T, N2><<<2 * nb * kFastN1, N2, fast_smem_a(N2), st>>>(g, s0, p->tw, p->N, p->D,
+  fsf_pass_a<T, N2><<<2 * nb * kFastN1, N2, fast_smem_a(N2), st>>>(g, s0, p->tw, p->tabs, p->N, p->D,
                                                                    p->H, bh0, nb, v, s1);
   return cudaGetLastError();
 }
