@@ -944,7 +944,7 @@ int cat_forward(cat_plan_t p, const void* X, const void* WA, const void* V, void
   if (e != cudaSuccess) return CAT_ERR_CUDA;
   if (ev) cudaEventRecord(ev[1], p->stream);
   e = p->path == cat::PATH_SMEM   ? cat::launch_softmax_spectrum(p)
-      : p->path == cat::PATH_FAST ? cat::launch_fast_zspec(p, 0, p->B * p->H, p->stream)
+      : p->path == cat::PATH_FAST ? cat::launch_fast_zspec(p, 0, p->B * p->H, p->stream, !ev)
                                   : cat::launch_softmax(p);
   if (e != cudaSuccess) return CAT_ERR_CUDA;
   if (ev) cudaEventRecord(ev[2], p->stream);

@@ -270,7 +270,11 @@ int fast_chunks(const cat_plan_s* p);
 // before_b is given, pass B (the first to read the spectrum) waits for it.
 // dep_a: the kernel ahead of this chunk's pass A on st is the previous
 // chunk's pass C (pass A may then launch as its programmatic dependent).
-cudaError_t launch_fast_zspec(const cat_plan_s* p, int row0, int nrows, cudaStream_t st);
+// dependent: at N2 = 32 the spectrum kernel launches as the programmatic
+// dependent of the kernel ahead (off for the stage-timed forward, whose
+// events sit between them).
+cudaError_t launch_fast_zspec(const cat_plan_s* p, int row0, int nrows, cudaStream_t st,
+                              bool dependent = true);
 cudaError_t launch_fast_chunk(const cat_plan_s* p, const void* V, void* O, int bh0, int nb,
                               int slot, cudaStream_t st, cudaEvent_t before_b = nullptr,
                               cudaEvent_t* after = nullptr, bool dep_a = false);

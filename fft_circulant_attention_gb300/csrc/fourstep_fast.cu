@@ -900,8 +900,8 @@ constexpr size_t kZRowBuf = (size_t)32 * kZRowStride * sizeof(float2);
 constexpr size_t kSmemZRow = kZRowBuf + kTabB * sizeof(float2) + 16;
 
 __global__ void __launch_bounds__(kZRowThreads, 1)
-fsf_zspec_row(const float2* __restrict__ z2, float2* __restrict__ zft,
-              const float2* __restrict__ tabs, int N, unsigned int* status) {
+fsf_zspec_row(const float2* z2, float2* __restrict__ zft, const float2* __restrict__ tabs, int N,
+              unsigned int* status) {
   extern __shared__ float4 smem4[];
   float2* buf = reinterpret_cast<float2*>(smem4);
   float2* tfs = buf + 32 * kZRowStride;                        // tf[k][u] = w_512^{u·k}
@@ -923,8 +923,11 @@ fsf_zspec_row(const float2* __restrict__ z2, float2* __restrict__ zft,
   }
   const float2* src = z2 + (size_t)row * N;
   float2 a[32];
+  // Launched as the dependent of the score: the table copies above are in
+  // flight while it finishes; the scores are read after the wait.
+  pdl_wait();
 #pragma unroll
-  for (int u = 0; u < 32; ++u) a[u] = __ldg(src + t + kFastN1 * u);
+  for (int u = 0; u < 32; ++u) a[u] = ld_dep(src + t + kFastN1 * u);
   float m = -INFINITY;
 #pragma unroll
   for (int u = 0; u < 32; ++u) m = fmaxf(m, a[u].x);
@@ -1141,16 +1144,17 @@ static cudaError_t launch_ac(const cat_plan_s* p, const T* V, T* O, float2* scr,
                      (const float2*)p->tabs, p->N, p->D, p->H, bh0, nb, early);
 }
 
-cudaError_t launch_fast_zspec(const cat_plan_s* p, int row0, int nrows, cudaStream_t st) {
+cudaError_t launch_fast_zspec(const cat_plan_s* p, int row0, int nrows, cudaStream_t st,
+                              bool dependent) {
   const int N2 = p->fs.N2;
   if (nrows <= 0) return cudaSuccess;
-  if (N2 == 32) {
-    fsf_zspec_row<<<nrows, kZRowThreads, kSmemZRow, st>>>(p->z2 + (size_t)row0 * p->N,
-                                                          p->zf + (size_t)row0 * p->N, p->tabs,
-                                                          p->N, p->status);
-    return cudaGetLastError();
-  }
-  // Longer rows: the multi-CTA softmax's chunk partials, then the two passes.
+  if (N2 == 32)
+    return fast_launch(dependent && p->fast_pdl != 0, fsf_zspec_row, nrows, kZRowThreads,
+                       kSmemZRow, st, (const float2*)(p->z2 + (size_t)row0 * p->N),
+                       p->zf + (size_t)row0 * p->N, (const float2*)p->tabs, p->N, p->status);
+  // Longer rows: the multi-CTA softmax's chunk partials, then the two passes
+  // (as programmatic dependents their early CTAs held SMs the kernel ahead
+  // still needed: long128k 541 against 552 us).
   Span sp;
   sp.b0 = row0 / p->H;
   sp.nbat = nrows / p->H;
