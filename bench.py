@@ -60,8 +60,10 @@ FALLBACK_HBM_GBS = 6800.0
 # the figure is cold-cache traffic (the scratch refilled from DRAM), an upper
 # bound on the traffic of a launch inside the overlapped schedule.
 NCU_TRAFFIC = {
-    # the long16k launch-list capture: the median of its 8 pass-B launches
-    ("long16k", "3aca664de5a5"): 34773248,
+    # the launch-list captures: the median of their pass-B launches (8 at
+    # long16k, 16 at long128k)
+    ("long16k", "86b1d648db80"): 34773888,
+    ("long128k", "86b1d648db80"): 35691008,
 }
 KERNEL_SOURCES = ["fourstep_fast.cu", "fft_reg.cuh", "fft_device.cuh", "bulk.cuh", "elem.cuh"]
 # Pass B's transforms: per (pair, k2) signal one forward and one inverse DFT
