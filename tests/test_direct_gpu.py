@@ -46,12 +46,16 @@ CASES = [
 ]
 
 
-@pytest.mark.parametrize("B,N,D,H,dtype,wa", CASES)
-@pytest.mark.parametrize("fused", ["auto", "0", "1"])
+# Every case with the plan's own choice, the scores forced separate ("0")
+# and forced fused ("1"); the fused kernel serves small N·D only, so the
+# forced-fused variant runs where N·D <= 2^17.
+PARITY_CASES = [c + (f,) for c in CASES for f in ("auto", "0", "1")
+                if f != "1" or c[1] * c[2] <= (1 << 17)]
+
+
+@pytest.mark.parametrize("B,N,D,H,dtype,wa,fused", PARITY_CASES)
 def test_direct_parity(B, N, D, H, dtype, wa, fused, monkeypatch):
     if fused != "auto":
-        if fused == "1" and N * D > (1 << 17):
-            pytest.skip("fused scores are for small N·D")
         monkeypatch.setenv("CAT_DIRECT_FUSED", fused)
     with cat.Plan(B, N, D, H, dtype) as p:
         assert "path=direct" in p.describe(), p.describe()
