@@ -9,13 +9,21 @@
 // memory.
 //
 // Tiles of 128 tokens (the MMA's M, one tensor-memory lane each) by 256
-// value columns, or by the 16 score columns (heads padded with zeros).  A
-// CTA runs three roles: warp 0 issues the tensor copies of the X and W
-// tiles (64-wide K slices, 128-byte swizzle) into a ring of kPjStages
-// stages; warp 1 allocates the tensor memory and one of its threads issues
-// the MMAs of each stage, releasing the stage through tcgen05.commit; warps
-// 2-5 read the accumulators back (tcgen05.ld) once the last MMA completes
-// and store V in bf16 (round to nearest even) or z as a double-float.
+// value columns, or by the 16 score columns (heads padded with zeros).  The
+// kernel is persistent, one CTA per SM: CTA c takes the tiles c, c + grid,
+// ... of the list ordered token block first, so the CTAs working at one time
+// share their token blocks of X through L2.  Three roles:
+//   - warp 0 issues the tensor copies of the X and W tiles (64-wide K
+//     slices, 128-byte swizzle) into a ring of kPjStages stages, running
+//     ahead across tiles;
+//   - warp 1 allocates the tensor memory (two accumulators of 256 columns)
+//     and one of its threads issues the MMAs of each stage, releasing the
+//     stage through tcgen05.commit; a tile's last commit marks its
+//     accumulator full;
+//   - warps 2-5 read a full accumulator back (tcgen05.ld), store V in bf16
+//     (round to nearest even) or z as a double-float, and mark it empty, so
+//     the MMAs of the next tile run into the other accumulator meanwhile.
+// Every mbarrier wait is bounded; a lost wait ends the role's loop.
 //
 // Scores: the peaked workloads need z to about 1e-6 absolute, so each
 // 64-wide K slice (a group of slices when D > 1024) accumulates into its own
@@ -33,14 +41,18 @@ constexpr int kPjM = 128;                        // tokens per tile (MMA M)
 constexpr int kPjK = 64;                         // K per stage: one 128-byte row
 constexpr int kPjNV = 256;                       // value columns per tile (MMA N)
 constexpr int kPjNZ = 16;                        // score columns per tile (MMA N)
-constexpr int kPjStages = 2;
+constexpr int kPjStages = 4;
 constexpr int kPjThreads = 192;                  // warp 0 copies, 1 MMA, 2-5 epilogue
 constexpr int kPjXBytes = kPjM * kPjK * 2;       // 16 KB
 constexpr int kPjWBytes = kPjNV * kPjK * 2;      // 32 KB
 constexpr int kPjStageBytes = kPjXBytes + kPjWBytes;
 constexpr int kPjMaxSlices = 16;                 // score accumulators
-constexpr int kPjTmemCols = 256;
-constexpr size_t kPjSmem = 1024 + (size_t)kPjStages * kPjStageBytes + 128;
+constexpr int kPjAccCols = 256;                  // one accumulator
+constexpr int kPjTmemCols = 2 * kPjAccCols;      // two, all of the SM's tensor memory
+constexpr size_t kPjSmem = 1024 + (size_t)kPjStages * kPjStageBytes + 256;
+// More than half of an SM's shared memory: one CTA per SM, so the 512
+// tensor-memory columns it allocates are always free.
+static_assert(kPjSmem > 114 * 1024, "one projection CTA per SM");
 
 __device__ __forceinline__ unsigned int pack_bf16x2(float a, float b) {
   __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
@@ -50,28 +62,31 @@ __device__ __forceinline__ unsigned int pack_bf16x2(float a, float b) {
 __global__ void __launch_bounds__(kPjThreads, 1)
 proj_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                const __grid_constant__ CUtensorMap tmA, __nv_bfloat16* __restrict__ V,
-               float2* __restrict__ z2, int Mtot, int N, int D, int H, unsigned int* status) {
+               float2* __restrict__ z2, int Mtot, int N, int D, int H, int ntiles,
+               unsigned int* status) {
   extern __shared__ unsigned char pj_raw[];
   const uint32_t raw = smem_addr(pj_raw);
   unsigned char* sm = pj_raw + (((raw + 1023u) & ~1023u) - raw);   // 1024-byte aligned
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + kPjStages * kPjStageBytes);
   uint64_t* empty = full + kPjStages;
-  uint64_t* done = empty + kPjStages;
+  uint64_t* tfull = empty + kPjStages;     // [2] accumulator b holds a finished tile
+  uint64_t* tempty = tfull + 2;            // [2] accumulator b has been read back
+  uint64_t* done = tempty + 2;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(done + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nvt = (D + kPjNV - 1) / kPjNV;
-  const bool ztile = (int)blockIdx.x == nvt;
-  const int n0 = blockIdx.x * kPjNV;
-  const int NT = ztile ? kPjNZ : min(kPjNV, D - n0);
-  const int m0 = blockIdx.y * kPjM;
+  const int nt = nvt + 1;                   // value tiles, then the score tile
   const int nks = D / kPjK;
   const int per_slice = (nks + kPjMaxSlices - 1) / kPjMaxSlices;   // K steps per score slice
-  const uint32_t wbytes = (ztile ? kPjNZ : kPjNV) * kPjK * 2;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kPjStages; ++s) {
       mbar_init(full + s, 1);
       mbar_init(empty + s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull + b, 1);
+      mbar_init(tempty + b, 4);
     }
     mbar_init(done, 1);
     mbar_fence_init();
@@ -83,40 +98,72 @@ proj_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
   const uint32_t tmem = *tslot;
 
   if (warp == 0) {
-    // Tensor copies: stage s % kPjStages once the MMAs of its previous use
-    // have completed.
+    // Tensor copies: stage g % kPjStages once the MMAs of its previous use
+    // have completed (g counts the K steps of all this CTA's tiles).
     if (lane == 0) {
-      for (int s = 0; s < nks; ++s) {
-        const int st = s % kPjStages;
-        if (s >= kPjStages &&
-            !mbar_wait(empty + st, ((s / kPjStages) - 1) & 1, status, 0x601))
-          break;
-        unsigned char* xs = sm + st * kPjStageBytes;
-        mbar_expect_tx(full + st, kPjXBytes + wbytes);
-        tma_load_2d(xs, &tmX, s * kPjK, m0, full + st);
-        if (ztile)
-          tma_load_2d(xs + kPjXBytes, &tmA, s * kPjK, 0, full + st);
-        else
-          tma_load_2d(xs + kPjXBytes, &tmW, s * kPjK, n0, full + st);
+      int g = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+        const int m0 = (t / nt) * kPjM, nti = t % nt;
+        const bool ztile = nti == nvt;
+        const uint32_t wbytes = (ztile ? kPjNZ : kPjNV) * kPjK * 2;
+        for (int s = 0; s < nks; ++s, ++g) {
+          const int st = g % kPjStages;
+          if (g >= kPjStages && !mbar_wait(empty + st, ((g / kPjStages) - 1) & 1, status, 0x601)) {
+            ok = false;
+            break;
+          }
+          unsigned char* xs = sm + st * kPjStageBytes;
+          mbar_expect_tx(full + st, kPjXBytes + wbytes);
+          tma_load_2d(xs, &tmX, s * kPjK, m0, full + st);
+          if (ztile)
+            tma_load_2d(xs + kPjXBytes, &tmA, s * kPjK, 0, full + st);
+          else
+            tma_load_2d(xs + kPjXBytes, &tmW, s * kPjK, nti * kPjNV, full + st);
+        }
       }
     }
   } else if (warp == 1) {
-    // MMA issue: four K = 16 MMAs per stage from one thread.
-    const uint32_t idesc = idesc_bf16_f32(kPjM, NT);
-    for (int s = 0; s < nks; ++s) {
-      const int st = s % kPjStages;
-      if (!mbar_wait(full + st, (s / kPjStages) & 1, status, 0x602)) break;
+    // MMA issue: four K = 16 MMAs per stage from one thread, into the
+    // accumulator of the tile's parity.
+    int g = 0, it = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++it) {
+      const int nti = t % nt;
+      const bool ztile = nti == nvt;
+      const int NT = ztile ? kPjNZ : min(kPjNV, D - nti * kPjNV);
+      const uint32_t idesc = idesc_bf16_f32(kPjM, NT);
+      const int b = it & 1;
+      // Lane 0 waits and issues; the warp follows its verdict, so that the
+      // whole warp leaves a loop together.
+      bool w = true;
+      if (it >= 2 && lane == 0) w = mbar_wait(tempty + b, ((it >> 1) - 1) & 1, status, 0x605);
+      if (!__shfl_sync(0xffffffffu, w, 0)) break;
       tc_fence_after();
-      if (lane == 0) {
-        const unsigned char* xs = sm + st * kPjStageBytes;
-        const uint32_t d = ztile ? tmem + kPjNZ * (uint32_t)(s / per_slice) : tmem;
-#pragma unroll
-        for (int k = 0; k < kPjK / 16; ++k) {
-          const uint32_t acc = ztile ? (k > 0 || s % per_slice != 0) : (k > 0 || s > 0);
-          tc_mma_bf16(d, sdesc_k128(xs + 32 * k), sdesc_k128(xs + kPjXBytes + 32 * k), idesc, acc);
+      const uint32_t acc0 = tmem + (uint32_t)(b * kPjAccCols);
+      for (int s = 0; s < nks; ++s, ++g) {
+        const int st = g % kPjStages;
+        w = true;
+        if (lane == 0) w = mbar_wait(full + st, (g / kPjStages) & 1, status, 0x602);
+        if (!__shfl_sync(0xffffffffu, w, 0)) {
+          ok = false;
+          break;
         }
-        tc_commit(empty + st);
+        tc_fence_after();
+        if (lane == 0) {
+          const unsigned char* xs = sm + st * kPjStageBytes;
+          const uint32_t d = ztile ? acc0 + kPjNZ * (uint32_t)(s / per_slice) : acc0;
+#pragma unroll
+          for (int k = 0; k < kPjK / 16; ++k) {
+            const uint32_t acc = ztile ? (k > 0 || s % per_slice != 0) : (k > 0 || s > 0);
+            tc_mma_bf16(d, sdesc_k128(xs + 32 * k), sdesc_k128(xs + kPjXBytes + 32 * k), idesc,
+                        acc);
+          }
+          tc_commit(empty + st);
+        }
+        __syncwarp();
       }
+      if (ok && lane == 0) tc_commit(tfull + b);
       __syncwarp();
     }
     if (lane == 0) tc_commit(done);
@@ -124,23 +171,32 @@ proj_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
   } else {
     // Epilogue: the four warps cover the 128 lanes by quadrant (warp % 4).
     const int q = warp & 3;
-    const int row = m0 + 32 * q + lane;
-    const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16);
-    if (mbar_wait(done, 0, status, 0x603)) {
+    int it = 0;
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
+      const int m0 = (t / nt) * kPjM, nti = t % nt;
+      const bool ztile = nti == nvt;
+      const int n0 = nti * kPjNV;
+      const int NT = ztile ? kPjNZ : min(kPjNV, D - n0);
+      const int b = it & 1;
+      // The tensor-memory loads are warp-wide: the warp goes on only if
+      // every lane saw the accumulator full.
+      if (!__all_sync(0xffffffffu, mbar_wait(tfull + b, (it >> 1) & 1, status, 0x603))) break;
       tc_fence_after();
+      const int row = m0 + 32 * q + lane;
+      const uint32_t taddr = tmem + (uint32_t)(b * kPjAccCols) + ((uint32_t)(32 * q) << 16);
       if (!ztile) {
         __nv_bfloat16* dst = V + (size_t)row * D + n0;
         for (int c0 = 0; c0 < NT; c0 += 16) {
           float v[16];
           tc_ld16(taddr + c0, v);
           if (row < Mtot) {
-            uint4 a, b;
+            uint4 a, c;
             a.x = pack_bf16x2(v[0], v[1]);   a.y = pack_bf16x2(v[2], v[3]);
             a.z = pack_bf16x2(v[4], v[5]);   a.w = pack_bf16x2(v[6], v[7]);
-            b.x = pack_bf16x2(v[8], v[9]);   b.y = pack_bf16x2(v[10], v[11]);
-            b.z = pack_bf16x2(v[12], v[13]); b.w = pack_bf16x2(v[14], v[15]);
+            c.x = pack_bf16x2(v[8], v[9]);   c.y = pack_bf16x2(v[10], v[11]);
+            c.z = pack_bf16x2(v[12], v[13]); c.w = pack_bf16x2(v[14], v[15]);
             reinterpret_cast<uint4*>(dst + c0)[0] = a;
-            reinterpret_cast<uint4*>(dst + c0)[1] = b;
+            reinterpret_cast<uint4*>(dst + c0)[1] = c;
           }
         }
       } else {
@@ -155,19 +211,23 @@ proj_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
           for (int h = 0; h < 16; ++h) two_sum_acc(hi[h], lo[h], v[h]);
         }
         if (row < Mtot) {
-          const int b = row / N, n = row - b * N;
+          const int bb = row / N, n = row - bb * N;
 #pragma unroll
           for (int h = 0; h < 16; ++h)
-            if (h < H) z2[((size_t)b * H + h) * N + n] = make_float2(hi[h], lo[h]);
+            if (h < H) z2[((size_t)bb * H + h) * N + n] = make_float2(hi[h], lo[h]);
         }
       }
+      // This warp's reads of the accumulator are complete (tc_ld16 waits):
+      // hand it back to the MMA warp.
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty + b);
     }
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
-    // The columns are freed only after every MMA has completed (the
-    // epilogue waited for `done`; check again, bounded, in case it gave up).
+    // The columns are freed only after every MMA has completed (bounded).
     mbar_wait(done, 0, status, 0x604);
     tc_fence_after();
     tmem_dealloc(tmem, kPjTmemCols);
@@ -228,9 +288,13 @@ cudaError_t launch_project(const cat_plan_s* p, const void* X, const void* WV, c
       !encode_map_2d_sw128(&tmW, Wt, D, D, (unsigned long long)D * 2, kPjK, kPjNV) ||
       !encode_map_2d_sw128(&tmA, At, D, kPjNZ, (unsigned long long)D * 2, kPjK, kPjNZ))
     return cudaErrorInvalidValue;
-  dim3 grid((D + kPjNV - 1) / kPjNV + 1, (unsigned)((Mtot + kPjM - 1) / kPjM));
+  // Tiles ordered token block first (value tiles, then the score tile of
+  // each block); one persistent CTA per SM, never more CTAs than tiles.
+  const long long ntiles = ((Mtot + kPjM - 1) / kPjM) * ((D + kPjNV - 1) / kPjNV + 1);
+  const int grid = (int)(ntiles < p->sms ? ntiles : p->sms);
   proj_tc_kernel<<<grid, kPjThreads, kPjSmem, p->stream>>>(
-      tmX, tmW, tmA, static_cast<__nv_bfloat16*>(V), p->z2, (int)Mtot, p->N, D, p->H, p->status);
+      tmX, tmW, tmA, static_cast<__nv_bfloat16*>(V), p->z2, (int)Mtot, p->N, D, p->H,
+      (int)ntiles, p->status);
   return cudaGetLastError();
 }
 
