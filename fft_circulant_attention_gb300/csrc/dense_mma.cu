@@ -220,10 +220,22 @@ dx_mma_kernel(const float* __restrict__ dz, const __nv_bfloat16* __restrict__ WA
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   unsigned short* os = reinterpret_cast<unsigned short*>(sm + (size_t)D * kDxmWs * 2) +
                        (size_t)warp * (kDxmOut / 2);
+  // W_A as bf16 [d][h], heads padded to 16 with zeros; eight loads a
+  // thread in flight before any is stored (one at a time, the CTA's start
+  // waited D·16 / threads memory latencies).
   const unsigned short* wg = reinterpret_cast<const unsigned short*>(WA);
-  for (int i = threadIdx.x; i < D * 16; i += blockDim.x) {
-    const int d = i >> 4, h = i & 15;
-    wa[d * kDxmWs + h] = h < H ? wg[(size_t)d * H + h] : (unsigned short)0;
+  for (int i0 = threadIdx.x; i0 < D * 16; i0 += 8 * blockDim.x) {
+    unsigned short v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + u * blockDim.x, d = i >> 4, h = i & 15;
+      v[u] = (i < D * 16 && h < H) ? wg[(size_t)d * H + h] : (unsigned short)0;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + u * blockDim.x;
+      if (i < D * 16) wa[(i >> 4) * kDxmWs + (i & 15)] = v[u];
+    }
   }
   __syncthreads();
   const int g = lane >> 2, c = lane & 3;
