@@ -235,8 +235,22 @@ softmax_bw_kernel(const float* __restrict__ zs, const float* __restrict__ dzs,
   __shared__ double red[kSmBwThreads / 32];
   __shared__ float total;
   const size_t off = (size_t)blockIdx.x * N;
+  const int bd = blockDim.x;
+  // Each thread's terms in order n = t, t + bd, ...; eight of each operand
+  // loaded before they are used.
   float part = 0.f;
-  for (int n = threadIdx.x; n < N; n += blockDim.x) part = fmaf(zs[off + n], dzs[off + n], part);
+  int n = threadIdx.x;
+  for (; n + 7 * bd < N; n += 8 * bd) {
+    float a[8], c[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      a[u] = zs[off + n + u * bd];
+      c[u] = dzs[off + n + u * bd];
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) part = fmaf(a[u], c[u], part);
+  }
+  for (; n < N; n += bd) part = fmaf(zs[off + n], dzs[off + n], part);
   double s = part;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
@@ -253,7 +267,18 @@ softmax_bw_kernel(const float* __restrict__ zs, const float* __restrict__ dzs,
   }
   __syncthreads();
   const float sf = total;
-  for (int n = threadIdx.x; n < N; n += blockDim.x) dz[off + n] = zs[off + n] * (dzs[off + n] - sf);
+  n = threadIdx.x;
+  for (; n + 7 * bd < N; n += 8 * bd) {
+    float a[8], c[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      a[u] = zs[off + n + u * bd];
+      c[u] = dzs[off + n + u * bd];
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) dz[off + n + u * bd] = a[u] * (c[u] - sf);
+  }
+  for (; n < N; n += bd) dz[off + n] = zs[off + n] * (dzs[off + n] - sf);
 }
 
 // ---------------------------------------------------------------------------
@@ -380,9 +405,17 @@ __global__ void dwa_reduce_kernel(const float* __restrict__ part, T* __restrict_
                                   int D, int H) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;   // i = h·D + d
   if (i >= D * H) return;
+  // Splits added in order k = 0, 1, ...; sixteen loads in flight at a time.
   float s = 0.f;
-#pragma unroll 8
-  for (int k = 0; k < nsplit; ++k) s += part[(size_t)k * H * D + i];
+  int k = 0;
+  for (; k + 16 <= nsplit; k += 16) {
+    float v[16];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) v[u] = part[(size_t)(k + u) * H * D + i];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) s += v[u];
+  }
+  for (; k < nsplit; ++k) s += part[(size_t)k * H * D + i];
   const int h = i / D, d = i - h * D;
   st_elem(dWA + (size_t)d * H + h, s);
 }
