@@ -138,6 +138,11 @@ SHAPES = [
     # ragged last tile.
     (3, 1000, 192, 3, "bf16"),
     (2, 4096, 320, 5, "bf16"),
+    # The fast path's correlation chunks with dV from their own transform of
+    # dO: chunks of 3 rows in half slots (6 heads), and 10 heads in chunks of
+    # 4 with a last chunk of 2.
+    (1, 16384, 384, 6, "bf16"),
+    (1, 16384, 640, 10, "bf16"),
 ]
 
 
