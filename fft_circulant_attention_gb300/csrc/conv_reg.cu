@@ -199,9 +199,22 @@ corr_reg_kernel(const T* __restrict__ Q, const T* __restrict__ K, float2* __rest
   const int share = (npair + P * G - 1) / (P * G) * P;
   const int pbeg = gi * share, pend = min(npair, pbeg + share);
   const int p = threadIdx.x % P, i = threadIdx.x / P;
-  for (int e = threadIdx.x; e < N; e += blockDim.x) {
-    S[e] = make_float2(0.f, 0.f);
-    if (TW) tw[e] = __ldg(&W[(e / M) * (e % M)]);
+  // Twiddles: eight loads a thread in flight before any is stored.
+  for (int e0 = threadIdx.x; e0 < N; e0 += 8 * blockDim.x) {
+    float2 w[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int e = e0 + u * blockDim.x;
+      if (TW && e < N) w[u] = __ldg(&W[(e / M) * (e % M)]);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int e = e0 + u * blockDim.x;
+      if (e < N) {
+        S[e] = make_float2(0.f, 0.f);
+        if (TW) tw[e] = w[u];
+      }
+    }
   }
   for (int g0 = pbeg; g0 < pend; g0 += P) {
     const int g = g0 + p;
