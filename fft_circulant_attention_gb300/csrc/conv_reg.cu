@@ -70,6 +70,15 @@ __device__ __forceinline__ void st_col_pair(T* p, float2 v, bool pair, bool alig
   }
 }
 
+// Shared layout of the product kernel: the [M][M][P] signal block with a
+// row (first index) stride of M·P + 8 when P = 8 (a warp then spans four
+// rows in step 2; rows M·P = 256 apart would share banks), and the twiddle
+// table with a row stride of M + 1 for M = 32 (step 1 reads a column).
+// (conv_reg_pairs gives P = 8 exactly when M = 32, so the product kernel
+// takes both strides as compile-time constants there.)
+__host__ __device__ inline int reg_rs(int M, int P) { return M * P + (P == 8 ? 8 : 0); }
+__host__ __device__ constexpr int reg_tws(int M) { return M == 32 ? M + 1 : M; }
+
 // TW = false: no twiddle between the two steps, i.e. the 2-D DFT of an
 // M x M token grid (n1 = x, n2 = y): the 2-D circular convolution of the
 // second page's circulant attention.
@@ -78,11 +87,13 @@ __global__ void __launch_bounds__(512)
 conv_reg_kernel(const T* __restrict__ V, T* __restrict__ O, const float2* zf,
                 const float2* __restrict__ W, int D, int H, int dh, int npair, int P,
                 int groups) {
-  constexpr int N = M * M;
+  constexpr int N = M * M, TWS = reg_tws(M);
+  if (M == 32) P = 8;
+  const int RS = reg_rs(M, P);
   extern __shared__ float4 smem4[];
-  float2* buf = reinterpret_cast<float2*>(smem4);   // [M][M][P]
-  float2* tw = buf + N * P;                          // tw[n1·M + k2] = w_N^{n1·k2}
-  float2* zs = tw + N;                               // FFT(z*)/N of this (b, h)
+  float2* buf = reinterpret_cast<float2*>(smem4);   // [M][M][P], rows RS apart
+  float2* tw = buf + M * RS;                         // tw[n1·TWS + k2] = w_N^{n1·k2}
+  float2* zs = tw + M * TWS;                         // FFT(z*)/N of this (b, h)
   const int bh = blockIdx.x / groups, grp = blockIdx.x - (blockIdx.x / groups) * groups;
   const int b = bh / H, h = bh - b * H;
   const int p = threadIdx.x % P, i = threadIdx.x / P;
@@ -101,7 +112,7 @@ conv_reg_kernel(const T* __restrict__ V, T* __restrict__ O, const float2* zf,
 #pragma unroll
       for (int u = 0; u < kPro; ++u) {
         const int e = e0 + u * blockDim.x;
-        if (e < N) tw[e] = tv[u];
+        if (e < N) tw[(e / M) * TWS + e % M] = tv[u];
       }
     }
   }
@@ -136,23 +147,23 @@ conv_reg_kernel(const T* __restrict__ V, T* __restrict__ O, const float2* zf,
   }
   __syncthreads();   // twiddles and spectrum ready
 #pragma unroll
-  for (int k2 = 0; k2 < M; ++k2) buf[(k2 * M + i) * P + p] = TW ? cmul(a[k2], tw[i * M + k2]) : a[k2];
+  for (int k2 = 0; k2 < M; ++k2) buf[k2 * RS + i * P + p] = TW ? cmul(a[k2], tw[i * TWS + k2]) : a[k2];
   __syncthreads();
 
   // Step 2: k2 = i.  Each thread reads and rewrites only its own M slots.
 #pragma unroll
-  for (int n1 = 0; n1 < M; ++n1) a[n1] = buf[(i * M + n1) * P + p];
+  for (int n1 = 0; n1 < M; ++n1) a[n1] = buf[i * RS + n1 * P + p];
   dft<M, false, CxPaired>(a);
 #pragma unroll
   for (int k1 = 0; k1 < M; ++k1) a[k1] = cmul(a[k1], zs[i + M * k1]);
   dft<M, true, CxPaired>(a);
 #pragma unroll
-  for (int n1 = 0; n1 < M; ++n1) buf[(i * M + n1) * P + p] = TW ? cmulc(a[n1], tw[n1 * M + i]) : a[n1];
+  for (int n1 = 0; n1 < M; ++n1) buf[i * RS + n1 * P + p] = TW ? cmulc(a[n1], tw[n1 * TWS + i]) : a[n1];
   __syncthreads();
 
   // Step 3: n1 = i.
 #pragma unroll
-  for (int k2 = 0; k2 < M; ++k2) a[k2] = buf[(k2 * M + i) * P + p];
+  for (int k2 = 0; k2 < M; ++k2) a[k2] = buf[k2 * RS + i * P + p];
   dft<M, true, CxPaired>(a);
   if (active) {
 #pragma unroll
@@ -185,12 +196,13 @@ __global__ void __launch_bounds__(512)
 corr_reg_kernel(const T* __restrict__ Q, const T* __restrict__ K, float2* __restrict__ z2,
                 float* __restrict__ out, const float2* __restrict__ W, int D, int H, int dh,
                 int npair, int P, float scale, float2* __restrict__ part, int G) {
-  constexpr int N = M * M;
+  constexpr int N = M * M, TWS = reg_tws(M);
+  const int RS = reg_rs(M, P);
   extern __shared__ float4 smem4[];
-  float2* bq = reinterpret_cast<float2*>(smem4);   // [M][M][P] Q pairs, then products
-  float2* bk = bq + N * P;                          // [M][M][P] K pairs
-  float2* S = bk + N * P;                           // [k2][k1] running sum
-  float2* tw = S + N;                               // TW: tw[n1·M + k2] = w_N^{n1·k2}
+  float2* bq = reinterpret_cast<float2*>(smem4);   // [M][M][P] Q pairs, then products (rows RS apart)
+  float2* bk = bq + M * RS;                         // [M][M][P] K pairs
+  float2* S = bk + M * RS;                          // [k2][k1] running sum
+  float2* tw = S + N;                               // TW: tw[n1·TWS + k2] = w_N^{n1·k2}
   // With part (G > 1), CTA gi of the (b, h) row takes its share of the
   // pairs (whole groups of P) and leaves its partial sum S in part instead
   // of inverting it; a finishing kernel adds the G partials in order.
@@ -212,7 +224,7 @@ corr_reg_kernel(const T* __restrict__ Q, const T* __restrict__ K, float2* __rest
       const int e = e0 + u * blockDim.x;
       if (e < N) {
         S[e] = make_float2(0.f, 0.f);
-        if (TW) tw[e] = w[u];
+        if (TW) tw[(e / M) * TWS + e % M] = w[u];
       }
     }
   }
@@ -230,28 +242,29 @@ corr_reg_kernel(const T* __restrict__ Q, const T* __restrict__ K, float2* __rest
     dft<M, false, CxPaired>(a);
     __syncthreads();   // the previous pass's sums have read bq; twiddles ready
 #pragma unroll
-    for (int k2 = 0; k2 < M; ++k2) bq[(k2 * M + i) * P + p] = TW ? cmul(a[k2], tw[i * M + k2]) : a[k2];
+    for (int k2 = 0; k2 < M; ++k2) bq[k2 * RS + i * P + p] = TW ? cmul(a[k2], tw[i * TWS + k2]) : a[k2];
     ld_rows<T, M>(a, K + base, (size_t)M * D, (size_t)i * D, active, pair, aligned);
     dft<M, false, CxPaired>(a);
 #pragma unroll
-    for (int k2 = 0; k2 < M; ++k2) bk[(k2 * M + i) * P + p] = TW ? cmul(a[k2], tw[i * M + k2]) : a[k2];
+    for (int k2 = 0; k2 < M; ++k2) bk[k2 * RS + i * P + p] = TW ? cmul(a[k2], tw[i * TWS + k2]) : a[k2];
     __syncthreads();
     // Step 2 (k2 = i): each thread reads and rewrites only its own slots.
 #pragma unroll
-    for (int n1 = 0; n1 < M; ++n1) a[n1] = bq[(i * M + n1) * P + p];
+    for (int n1 = 0; n1 < M; ++n1) a[n1] = bq[i * RS + n1 * P + p];
     dft<M, false, CxPaired>(a);
 #pragma unroll
-    for (int k1 = 0; k1 < M; ++k1) bq[(i * M + k1) * P + p] = a[k1];
+    for (int k1 = 0; k1 < M; ++k1) bq[i * RS + k1 * P + p] = a[k1];
 #pragma unroll
-    for (int n1 = 0; n1 < M; ++n1) a[n1] = bk[(i * M + n1) * P + p];
+    for (int n1 = 0; n1 < M; ++n1) a[n1] = bk[i * RS + n1 * P + p];
     dft<M, false, CxPaired>(a);
 #pragma unroll
     for (int k1 = 0; k1 < M; ++k1)
-      bq[(i * M + k1) * P + p] = cmulc(bq[(i * M + k1) * P + p], a[k1]);
+      bq[i * RS + k1 * P + p] = cmulc(bq[i * RS + k1 * P + p], a[k1]);
     __syncthreads();
     for (int e = threadIdx.x; e < N; e += blockDim.x) {
       float2 s = S[e];
-      for (int q = 0; q < P; ++q) s = cadd(s, bq[e * P + q]);
+      const float2* pr = bq + (e / M) * RS + (e % M) * P;   // S[k2][k1]: row k2, slot k1
+      for (int q = 0; q < P; ++q) s = cadd(s, pr[q]);
       S[e] = s;
     }
   }
@@ -269,7 +282,7 @@ corr_reg_kernel(const T* __restrict__ Q, const T* __restrict__ K, float2* __rest
     for (int k1 = 0; k1 < M; ++k1) a[k1] = S[t * M + k1];
     dft<M, true, CxPaired>(a);
 #pragma unroll
-    for (int n1 = 0; n1 < M; ++n1) bk[n1 * M + t] = TW ? cmulc(a[n1], tw[n1 * M + t]) : a[n1];
+    for (int n1 = 0; n1 < M; ++n1) bk[n1 * M + t] = TW ? cmulc(a[n1], tw[n1 * TWS + t]) : a[n1];
   }
   __syncthreads();
   if (t < M) {   // n1 = t: inverse over k2
@@ -286,7 +299,8 @@ corr_reg_kernel(const T* __restrict__ Q, const T* __restrict__ K, float2* __rest
 }
 
 size_t corr_reg_smem(int M, int P) {
-  return ((size_t)2 * M * M * P + 2 * (size_t)M * M) * sizeof(float2);
+  return ((size_t)2 * M * reg_rs(M, P) + (size_t)M * M + (size_t)M * reg_tws(M)) *
+         sizeof(float2);
 }
 
 template <typename T, bool TW>
@@ -649,7 +663,9 @@ cudaError_t launch_softmax_spectrum_reg(const cat_plan_s* p) {
 // that a CTA of 256 threads and 74 KB of shared memory leaves room for more).
 int conv_reg_pairs(int M) { return M == 32 ? 8 : 16; }
 
-size_t conv_reg_smem(int M, int P) { return (size_t)M * M * (P + 2) * sizeof(float2); }
+size_t conv_reg_smem(int M, int P) {
+  return ((size_t)M * reg_rs(M, P) + (size_t)M * reg_tws(M) + (size_t)M * M) * sizeof(float2);
+}
 
 template <typename T, bool TW>
 static cudaError_t setup_tw() {
