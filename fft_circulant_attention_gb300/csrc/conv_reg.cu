@@ -441,9 +441,17 @@ constexpr int kSpecQ4Threads = 128;
 // CTAs per (b, h) row of the split register correlation (N = 32²).
 constexpr int kCorrSplitG = 4;
 
+// Column of element (row, col) in the q4 kernels' [32][36] arrays: the low
+// two bits of col flipped by bits 2-3 of row, so that a warp writing one
+// column of 32 rows (the transposed store of σ) hits distinct banks, while
+// the step's reads (four rows a half-warp, four columns each) stay
+// conflict-free.
+__device__ __forceinline__ int q4_col(int row, int col) { return col ^ ((row >> 2) & 3); }
+
 // One 32-point DFT (INV: its unscaled inverse) of column g of `in` ([g][n]
-// with row stride 36), split over the 4 threads q of the column; thread q
-// ends with bins 2q + h + 8kb in out[4h + kb].  W: the length-1024 table.
+// with row stride 36, columns placed by q4_col), split over the 4 threads q
+// of the column; thread q ends with bins 2q + h + 8kb in out[4h + kb].
+// W: the length-1024 table.
 template <bool INV>
 __device__ __forceinline__ void spec_q4_step(const float2* __restrict__ in, float2* ex,
                                              const float2* __restrict__ W, int g, int q,
@@ -451,7 +459,7 @@ __device__ __forceinline__ void spec_q4_step(const float2* __restrict__ in, floa
   constexpr int LD = 36;
   float2 a[8];
 #pragma unroll
-  for (int m = 0; m < 8; ++m) a[m] = in[g * LD + q + 4 * m];
+  for (int m = 0; m < 8; ++m) a[m] = in[g * LD + q4_col(g, q + 4 * m)];
   dft<8, INV, CxPaired>(a);
   float2* mine = ex + g * 33;
 #pragma unroll
@@ -504,7 +512,7 @@ softmax_spectrum_q4(const float2* z, float* __restrict__ zs, float2* __restrict_
     const int n = t + kSpecQ4Threads * j;
     const float sg = e[j] * inv;
     out[n] = sg;
-    sa[(n & 31) * LD + (n >> 5)] = make_float2(sg, 0.f);
+    sa[(n & 31) * LD + q4_col(n & 31, n >> 5)] = make_float2(sg, 0.f);
   }
   __syncthreads();
   const int g = t >> 2, q = t & 3;
@@ -516,7 +524,7 @@ softmax_spectrum_q4(const float2* z, float* __restrict__ zs, float2* __restrict_
     for (int kb = 0; kb < 4; ++kb) {
       const int k2 = 2 * q + h + 8 * kb;
       const float2 w = y[4 * h + kb];
-      sb[k2 * LD + g] = TW ? cmul(w, W[g * k2]) : w;
+      sb[k2 * LD + q4_col(k2, g)] = TW ? cmul(w, W[g * k2]) : w;
     }
   __syncthreads();
   spec_q4_step<false>(sb, ex, W, g, q, y);   // k2 = g: bins k1 = 2q + h + 8kb
@@ -561,7 +569,7 @@ corr_finish_q4(const float2* __restrict__ part, int G, const float* __restrict__
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     const int e = t + kSpecQ4Threads * j;   // e = k2·32 + k1
-    sa[(e >> 5) * LD + (e & 31)] = acc[j];
+    sa[(e >> 5) * LD + q4_col(e >> 5, e & 31)] = acc[j];
   }
   __syncthreads();
   const int g = t >> 2, q = t & 3;
@@ -572,7 +580,7 @@ corr_finish_q4(const float2* __restrict__ part, int G, const float* __restrict__
 #pragma unroll
     for (int kb = 0; kb < 4; ++kb) {
       const int n1 = 2 * q + h + 8 * kb;
-      sb[n1 * LD + g] = cmulc(y[4 * h + kb], W[n1 * g]);
+      sb[n1 * LD + q4_col(n1, g)] = cmulc(y[4 * h + kb], W[n1 * g]);
     }
   __syncthreads();
   spec_q4_step<true>(sb, ex, W, g, q, y);   // n1 = g: bins n2 = 2q + h + 8kb
