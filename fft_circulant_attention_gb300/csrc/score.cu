@@ -77,28 +77,40 @@ __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
+// Row d of the staged block starts at float d·HP, or with `pad` at
+// d·HP + 4·(d / 4): one 16-byte slot after every fourth row, so that the
+// split kernel's four lanes of a token, which read rows 4 (fp32) or 8
+// (bf16) apart at the same time, fall in distinct bank groups.
+__host__ __device__ inline int w_row(int d, int HP, bool pad) { return d * HP + (pad ? 4 * (d >> 2) : 0); }
+
 template <typename T>
 __device__ __forceinline__ void stage_w_f32(float* ws, const T* __restrict__ WA, int D, int H,
-                                            int h0, int HT, int HP, bool wait = true) {
+                                            int h0, int HT, int HP, bool wait = true,
+                                            bool pad = false) {
   if constexpr (std::is_same<T, float>::value) {
     // fp32 W_A needs no conversion: every element goes by an asynchronous
     // copy (all of a thread's copies in flight at once, no registers held),
     // 16 bytes at a time when the staged block is W_A itself (all heads,
     // H a multiple of 4, 16-byte aligned), else 4; padding columns are zeroed.
     if (h0 == 0 && HT == H && HP == H && ((uintptr_t)WA % 16) == 0) {
-      for (int i = threadIdx.x; i < D * H / 4; i += blockDim.x)
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(ws + 4 * i)),
+      const int c4 = H / 4;   // 16-byte chunks a row
+      for (int i = threadIdx.x; i < D * c4; i += blockDim.x) {
+        const int d = i / c4, c = i - d * c4;
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                         smem_addr(ws + w_row(d, HP, pad) + 4 * c)),
                      "l"(__cvta_generic_to_global(WA + 4 * i))
                      : "memory");
+      }
     } else {
       for (int i = threadIdx.x; i < D * HP; i += blockDim.x) {
         const int d = i / HP, h = i - d * HP;
+        float* dst = ws + w_row(d, HP, pad) + h;
         if (h < HT)
-          asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(ws + i)),
+          asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)),
                        "l"(__cvta_generic_to_global(WA + (size_t)d * H + h0 + h))
                        : "memory");
         else
-          ws[i] = 0.f;
+          *dst = 0.f;
       }
     }
     // Without `wait` the caller waits (cp_async_wait_all) before the
@@ -119,7 +131,8 @@ __device__ __forceinline__ void stage_w_f32(float* ws, const T* __restrict__ WA,
 #pragma unroll
     for (int j = 0; j < kBatch; ++j) {
       const int i = i0 + j * blockDim.x;
-      if (i < total) ws[i] = v[j];
+      const int d = i / HP, h = i - d * HP;
+      if (i < total) ws[w_row(d, HP, pad) + h] = v[j];
     }
   }
 }
@@ -243,7 +256,7 @@ score_split_kernel(const T* __restrict__ X, const T* __restrict__ WA, float2* __
   const int b = b0 + blockIdx.y;
   // W_A's copies are issued first and waited for after the first X loads,
   // so the two latencies overlap.
-  stage_w_f32(ws, WA, D, H, h0, HT, HP, false);
+  stage_w_f32(ws, WA, D, H, h0, HT, HP, false, true);
   const int q = threadIdx.x % kSplit;
   const int slot = threadIdx.x / kSplit;              // 0 .. kScoreThreads/kSplit - 1
   int n[TT];
@@ -284,7 +297,7 @@ score_split_kernel(const T* __restrict__ X, const T* __restrict__ WA, float2* __
       if (v < nvec) {
 #pragma unroll
         for (int j = 0; j < V; ++j) {
-          const float4* wrow = ws4 + (size_t)(v * V + j) * (HP / 4);
+          const float4* wrow = ws4 + w_row(v * V + j, HP, true) / 4;
 #pragma unroll
           for (int c = 0; c < HP / 4; ++c) {
             const float4 w = wrow[c];
@@ -717,7 +730,9 @@ static cudaError_t run_score(const cat_plan_s* p, const T* X, const T* WA, int h
   if (VEC && p->D % (4 * Vec16<T>::n) == 0) {
     constexpr int tok = split_tokens<4>();
     dim3 grid((p->N + tok - 1) / tok, sp.nb(p));
-    ks4<<<grid, kScoreThreads, smem, sp.stream(p)>>>(X, WA, p->z2, p->N, p->D, p->H, h0, sp.b0);
+    const size_t smem_split = (size_t)w_row(p->D, HP, true) * sizeof(float);   // padded rows
+    ks4<<<grid, kScoreThreads, smem_split, sp.stream(p)>>>(X, WA, p->z2, p->N, p->D, p->H, h0,
+                                                            sp.b0);
     return cudaGetLastError();
   }
   dim3 grid((p->N + kScoreTokPerCta - 1) / kScoreTokPerCta, sp.nb(p));
