@@ -638,15 +638,33 @@ cudaError_t launch_corr_reg_split(const cat_plan_s* p, const void* G, const void
   return cudaGetLastError();
 }
 
+// An ordinary launch, or (dep) one as the programmatic dependent of the
+// kernel ahead on the stream.
+template <typename... KArgs, typename... Args>
+static cudaError_t spec_launch(bool dep, void (*kernel)(KArgs...), dim3 grid, dim3 block,
+                               size_t smem, cudaStream_t st, Args... args) {
+  if (dep) return launch_dependent(kernel, grid, block, smem, st, args...);
+  kernel<<<grid, block, smem, st>>>(args...);
+  return cudaGetLastError();
+}
+
+// The spectrum kernel follows the scores; the product kernel behind it is
+// its programmatic dependent.  After the 1-D score it is an ordinary
+// launch: as the score's dependent it let the product kernel start while
+// the score still ran, and the product's value loads and first transforms
+// then slowed the score, which every later step waits for (per forward,
+// vit196 30.1 -> 26.7 us, gpt2_f32 66.1 -> 61.8 us, gpt2_bf16 47.8 ->
+// 43.1 us once it waits).  After the 2-D scores (few long CTAs) the
+// dependent launch still pays (ca_vit196 39.0 against 41.0 us).
 template <bool TW>
 static cudaError_t spectrum_reg_t(const cat_plan_s* p) {
   const int rows = p->B * p->H;
   if (rows == 0) return cudaSuccess;
   const int M = p->sm.reg_m;
+  const bool dep = !TW;
   if (M == 32)
-    return launch_dependent(softmax_spectrum_q4<TW>, dim3(rows), dim3(kSpecQ4Threads), 0,
-                            p->stream, (const float2*)p->z2, p->zs, p->zf,
-                            (const float2*)p->tw);
+    return spec_launch(dep, softmax_spectrum_q4<TW>, dim3(rows), dim3(kSpecQ4Threads), 0,
+                       p->stream, (const float2*)p->z2, p->zs, p->zf, (const float2*)p->tw);
   const int GL = M <= 8 ? 8 : (M <= 16 ? 16 : 32);
   const int per = spectrum_reg_rows(M, rows, p->sms);
   const int ctas = (rows + per - 1) / per;
@@ -654,9 +672,9 @@ static cudaError_t spectrum_reg_t(const cat_plan_s* p) {
   switch (M) {
 #define CAT_M(m)                                                                         \
   case m:                                                                                \
-    return launch_dependent(softmax_spectrum_reg<m, TW>, dim3(ctas), dim3(per * GL), smem, \
-                            p->stream, (const float2*)p->z2, p->zs, p->zf,                 \
-                            (const float2*)p->tw, rows);
+    return spec_launch(dep, softmax_spectrum_reg<m, TW>, dim3(ctas), dim3(per * GL), smem,  \
+                       p->stream, (const float2*)p->z2, p->zs, p->zf, (const float2*)p->tw, \
+                       rows);
     CAT_M(8) CAT_M(14) CAT_M(16) CAT_M(32)
 #undef CAT_M
     default: return cudaErrorInvalidValue;
