@@ -1199,6 +1199,19 @@ cudaError_t backward_schedule(cat_plan_s* p, const void* X, const void* WA, cons
     if (e == cudaSuccess) e = cat::launch_backward_dense(p, X, WA, dX, dWA);
     return e;
   }
+  if (p->path == cat::PATH_SMEM && p->sm.reg_m && !p->twod) {
+    // Register path: one spectrum kernel gives z* (for the softmax
+    // backward) and FFT(z*)/N.  circ(z*)^T = circ(r) with r[n] = z*[(-n)
+    // mod N], and z* is real, so FFT(r) = conj(FFT(z*)): the product kernel
+    // takes the spectrum conjugated, with no second softmax and spectrum of
+    // the scores reversed.
+    cudaError_t e = cat::launch_score(p, X, WA);
+    if (e == cudaSuccess) e = cat::launch_softmax_spectrum(p);
+    if (e == cudaSuccess) e = cat::launch_backward_dz(p, dO, V);
+    if (e == cudaSuccess) e = cat::launch_backward_dense(p, X, WA, dX, dWA);
+    if (e == cudaSuccess) e = cat::launch_conv_reg(p, dO, dV, true);
+    return e;
+  }
   if (run_backward_front(p, X, WA, V, dO) != CAT_OK) return cudaErrorLaunchFailure;
   if (p->path == cat::PATH_FAST) {
     cudaError_t e = cat::launch_reverse_scores(p);

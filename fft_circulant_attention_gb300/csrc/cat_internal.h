@@ -241,7 +241,8 @@ cudaError_t launch_softmax_spectrum(const cat_plan_s* p);
 cudaError_t launch_conv_smem(const cat_plan_s* p, const void* V, void* O);
 // Register two-step circulant product for N = M² (M in {8, 14, 16, 32}).
 cudaError_t setup_conv_reg(const cat_plan_s* p);
-cudaError_t launch_conv_reg(const cat_plan_s* p, const void* V, void* O);
+// conj: the product takes conj(FFT(z*)) (dV = circ(z*)^T dO of the backward).
+cudaError_t launch_conv_reg(const cat_plan_s* p, const void* V, void* O, bool conj = false);
 cudaError_t launch_softmax_spectrum_reg(const cat_plan_s* p);
 // 2-D plan with reg2d: the scores a (channel-averaged 2-D correlation of Q
 // and K) into z2 as (a, 0), and into out if given.

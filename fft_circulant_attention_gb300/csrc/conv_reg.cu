@@ -86,7 +86,7 @@ template <typename T, int M, bool TW = true>
 __global__ void __launch_bounds__(512)
 conv_reg_kernel(const T* __restrict__ V, T* __restrict__ O, const float2* zf,
                 const float2* __restrict__ W, int D, int H, int dh, int npair, int P,
-                int groups) {
+                int groups, int conj) {
   constexpr int N = M * M, TWS = reg_tws(M);
   if (M == 32) P = 8;
   const int RS = reg_rs(M, P);
@@ -142,7 +142,7 @@ conv_reg_kernel(const T* __restrict__ V, T* __restrict__ O, const float2* zf,
 #pragma unroll
     for (int u = 0; u < kPro; ++u) {
       const int e = e0 + u * blockDim.x;
-      if (e < N) zs[e] = zv[u];
+      if (e < N) zs[e] = conj ? make_float2(zv[u].x, -zv[u].y) : zv[u];
     }
   }
   __syncthreads();   // twiddles and spectrum ready
@@ -363,8 +363,8 @@ softmax_spectrum_reg(const float2* z, float* __restrict__ zs,
   // count.  Lane i reads its twiddles w_N^{i·k2} straight from the table.
   const int i = threadIdx.x % GL, r = threadIdx.x / GL;
   const int row = blockIdx.x * (blockDim.x / GL) + r;
-  // Launched as the score's programmatic dependent: let the product kernel
-  // behind launch, then wait for the scores.
+  // Let the product kernel behind (its programmatic dependent) launch, then
+  // wait for the scores (a no-op after an ordinary launch).
   pdl_trigger();
   pdl_wait();
   const bool act = i < M && row < rows;
@@ -726,7 +726,7 @@ cudaError_t setup_conv_reg(const cat_plan_s* p) {
 }
 
 template <typename T, bool TW>
-static cudaError_t launch_tw(const cat_plan_s* p, const T* V, T* O) {
+static cudaError_t launch_tw(const cat_plan_s* p, const T* V, T* O, bool conj) {
   const int M = p->sm.reg_m, P = p->sm.G, groups = p->sm.groups;
   const int ctas = p->B * p->H * groups;
   const dim3 block(M * P);
@@ -736,7 +736,7 @@ static cudaError_t launch_tw(const cat_plan_s* p, const T* V, T* O) {
   case m:                                                                                    \
     return launch_dependent(conv_reg_kernel<T, m, TW>, dim3(ctas), block, smem, p->stream, V, \
                             O, (const float2*)p->zf, (const float2*)p->tw, p->D, p->H, p->dh, \
-                            p->npair, P, groups);
+                            p->npair, P, groups, (int)conj);
     CAT_M(8) CAT_M(14) CAT_M(16) CAT_M(32)
 #undef CAT_M
     default: return cudaErrorInvalidValue;
@@ -744,14 +744,14 @@ static cudaError_t launch_tw(const cat_plan_s* p, const T* V, T* O) {
 }
 
 template <typename T>
-static cudaError_t launch_t(const cat_plan_s* p, const T* V, T* O) {
-  return p->twod ? launch_tw<T, false>(p, V, O) : launch_tw<T, true>(p, V, O);
+static cudaError_t launch_t(const cat_plan_s* p, const T* V, T* O, bool conj) {
+  return p->twod ? launch_tw<T, false>(p, V, O, conj) : launch_tw<T, true>(p, V, O, conj);
 }
 
-cudaError_t launch_conv_reg(const cat_plan_s* p, const void* V, void* O) {
+cudaError_t launch_conv_reg(const cat_plan_s* p, const void* V, void* O, bool conj) {
   if (p->B == 0) return cudaSuccess;
-  if (p->dtype == 1) return launch_t(p, (const __nv_bfloat16*)V, (__nv_bfloat16*)O);
-  return launch_t(p, (const float*)V, (float*)O);
+  if (p->dtype == 1) return launch_t(p, (const __nv_bfloat16*)V, (__nv_bfloat16*)O, conj);
+  return launch_t(p, (const float*)V, (float*)O, conj);
 }
 
 }  // namespace cat
