@@ -1188,13 +1188,12 @@ namespace {
 cudaError_t backward_schedule(cat_plan_s* p, const void* X, const void* WA, const void* V,
                               const void* dO, void* dX, void* dWA, void* dV) {
   if (p->path == cat::PATH_FAST && cat::backward_dv_in_corr(p)) {
-    // z* (zs) from the scores, then the scores reversed and their spectrum,
-    // so that the correlation's chunks give dV from their own transform of
-    // dO; dW_A and dX once dz is complete.
+    // z* (zs) and its spectrum from the row spectrum kernel, so that the
+    // correlation's chunks give dV from their own transform of dO (pass B
+    // with the spectrum conjugated: that of z* reversed); dW_A and dX once
+    // dz is complete.
     cudaError_t e = cat::launch_score(p, X, WA);
-    if (e == cudaSuccess) e = cat::launch_softmax(p);
-    if (e == cudaSuccess) e = cat::launch_reverse_scores(p);
-    if (e == cudaSuccess) e = cat::launch_fast_zspec(p, 0, p->B * p->H, p->stream);
+    if (e == cudaSuccess) e = cat::launch_fast_zspec(p, 0, p->B * p->H, p->stream, true, p->zs);
     if (e == cudaSuccess) e = cat::launch_backward_dz(p, dO, V, dV);
     if (e == cudaSuccess) e = cat::launch_backward_dense(p, X, WA, dX, dWA);
     return e;

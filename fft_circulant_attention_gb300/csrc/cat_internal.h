@@ -273,9 +273,9 @@ int fast_chunks(const cat_plan_s* p);
 // chunk's pass C (pass A may then launch as its programmatic dependent).
 // dependent: at N2 = 32 the spectrum kernel launches as the programmatic
 // dependent of the kernel ahead (off for the stage-timed forward, whose
-// events sit between them).
+// events sit between them).  zs (N2 = 32 only): z* is written there too.
 cudaError_t launch_fast_zspec(const cat_plan_s* p, int row0, int nrows, cudaStream_t st,
-                              bool dependent = true);
+                              bool dependent = true, float* zs = nullptr);
 cudaError_t launch_fast_chunk(const cat_plan_s* p, const void* V, void* O, int bh0, int nb,
                               int slot, cudaStream_t st, cudaEvent_t before_b = nullptr,
                               cudaEvent_t* after = nullptr, bool dep_a = false);

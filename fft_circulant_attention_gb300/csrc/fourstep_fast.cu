@@ -470,7 +470,7 @@ constexpr size_t kSmemB =
 
 __global__ void __launch_bounds__(kBPairs * 16, 2)
 fsf_pass_b(float2* __restrict__ scr, const float2* __restrict__ zft,
-           const float2* __restrict__ tabs, int N2, int bh0, int early) {
+           const float2* __restrict__ tabs, int N2, int bh0, int early, int conj) {
   if (early) pdl_trigger();
   extern __shared__ float4 smem4[];
   float2* buf = reinterpret_cast<float2*>(smem4);
@@ -498,8 +498,12 @@ fsf_pass_b(float2* __restrict__ scr, const float2* __restrict__ zft,
   const float4 q0 = __ldg(g4 + t);                                   // tf, ti
   const float4 q1 = __ldg(g4 + 256 + t);
   const float4 q2 = __ldg(g4 + 512 + (size_t)k2 * 256 + t);          // tx of this k2
-  const float4 q3 = __ldg(reinterpret_cast<const float4*>(zft) +
-                          ((size_t)(bh0 + bhl) * N2 + k2) * (kFastN1 / 2) + t);
+  float4 q3 = __ldg(reinterpret_cast<const float4*>(zft) +
+                    ((size_t)(bh0 + bhl) * N2 + k2) * (kFastN1 / 2) + t);
+  if (conj) {   // conj(FFT(z*)): the spectrum of the reversed z* (dV of the backward)
+    q3.y = -q3.y;
+    q3.w = -q3.w;
+  }
   pdl_wait();
   float2 a[32];
 #pragma unroll
@@ -901,7 +905,7 @@ constexpr size_t kSmemZRow = kZRowBuf + kTabB * sizeof(float2) + 16;
 
 __global__ void __launch_bounds__(kZRowThreads, 1)
 fsf_zspec_row(const float2* z2, float2* __restrict__ zft, const float2* __restrict__ tabs, int N,
-              unsigned int* status) {
+              unsigned int* status, float* __restrict__ zs) {
   extern __shared__ float4 smem4[];
   float2* buf = reinterpret_cast<float2*>(smem4);
   float2* tfs = buf + 32 * kZRowStride;                        // tf[k][u] = w_512^{u·k}
@@ -943,6 +947,11 @@ fsf_zspec_row(const float2* z2, float2* __restrict__ zft, const float2* __restri
   const float inv = 1.0f / S;
 #pragma unroll
   for (int u = 0; u < 32; ++u) a[u].x *= inv;
+  if (zs) {   // z* itself (the backward's softmax backward reads it)
+    float* zr = zs + (size_t)row * N + t;
+#pragma unroll
+    for (int u = 0; u < 32; ++u) zr[kFastN1 * u] = a[u].x;
+  }
   dft<32, false, CxPaired>(a);
   const bool ok = __syncthreads_and(mbar_wait(bar, 0, status, 0x503));
   // Twiddle w_N^{n1·k2} (n1 = t) and store [k2][n1].
@@ -1145,13 +1154,15 @@ static cudaError_t launch_ac(const cat_plan_s* p, const T* V, T* O, float2* scr,
 }
 
 cudaError_t launch_fast_zspec(const cat_plan_s* p, int row0, int nrows, cudaStream_t st,
-                              bool dependent) {
+                              bool dependent, float* zs) {
   const int N2 = p->fs.N2;
   if (nrows <= 0) return cudaSuccess;
   if (N2 == 32)
     return fast_launch(dependent && p->fast_pdl != 0, fsf_zspec_row, nrows, kZRowThreads,
                        kSmemZRow, st, (const float2*)(p->z2 + (size_t)row0 * p->N),
-                       p->zf + (size_t)row0 * p->N, (const float2*)p->tabs, p->N, p->status);
+                       p->zf + (size_t)row0 * p->N, (const float2*)p->tabs, p->N, p->status,
+                       zs ? zs + (size_t)row0 * p->N : nullptr);
+  if (zs) return cudaErrorInvalidValue;
   // Longer rows: the multi-CTA softmax's chunk partials, then the two passes
   // (as programmatic dependents their early CTAs held SMs the kernel ahead
   // still needed: long128k 541 against 552 us).
@@ -1227,7 +1238,8 @@ static cudaError_t chunk_t(const cat_plan_s* p, const T* V, T* O, int bh0, int n
     if (e != cudaSuccess) return e;
   }
   e = fast_launch(pdl && !before_b, fsf_pass_b, nb * N2 * (kFastPairs / kBPairs), kBPairs * 16,
-                  kSmemB, st, scr, (const float2*)p->zf, (const float2*)p->tabs, N2, bh0, early);
+                  kSmemB, st, scr, (const float2*)p->zf, (const float2*)p->tabs, N2, bh0, early,
+                  0);
   if (e != cudaSuccess) return e;
   if (after) cudaEventRecord(after[1], st);
   e = ac(false, pdl);
@@ -1250,16 +1262,18 @@ cudaError_t launch_fast_chunk(const cat_plan_s* p, const void* V, void* O, int b
   return chunk_t(p, (const float*)V, (float*)O, bh0, nb, slot, st, &tmV, before_b, after, dep_a);
 }
 
-// Passes B and C (N2 = 32) of the product on rows [bh0, bh0 + nb) whose
-// pass-A output is already at scr: rows row_off .. row_off + nb - 1 of
-// scratch slot 0 (the backward's correlation leaves dO's transform there).
-// Pass B multiplies by the spectrum in p->zf; pass C writes O.
+// Passes B and C (N2 = 32) of the backward's dV = circ(z*)^T dO on rows
+// [bh0, bh0 + nb) whose pass-A output is already at scr: rows row_off ..
+// row_off + nb - 1 of scratch slot 0 (the correlation leaves dO's transform
+// there).  circ(z*)^T = circ(r) with r[n] = z*[(-n) mod N], whose spectrum
+// is conj(FFT(z*)) (z* is real): pass B multiplies by the spectrum in p->zf
+// conjugated; pass C writes O.
 template <typename T>
 static cudaError_t bc32_t(const cat_plan_s* p, float2* scr, T* O, int bh0, int nb, int row_off,
                           cudaStream_t st) {
   const int early = p->fast_pdl == 2;
   fsf_pass_b<<<nb * 32 * (kFastPairs / kBPairs), kBPairs * 16, kSmemB, st>>>(
-      scr, p->zf, p->tabs, 32, bh0, early);
+      scr, p->zf, p->tabs, 32, bh0, early, 1);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   int grid = (nb * kFastN1 + PipeC::kWarps - 1) / PipeC::kWarps;
