@@ -22,6 +22,7 @@
 #include "cat_internal.h"
 #include "elem.cuh"
 #include "fft_reg.cuh"
+#include "tc.cuh"
 
 namespace cat {
 
@@ -295,6 +296,119 @@ corr_reg_kernel(const T* __restrict__ Q, const T* __restrict__ K, float2* __rest
       if (z2) z2[(size_t)bh * N + t + M * n2] = make_float2(v, 0.f);
       if (out) out[(size_t)bh * N + t + M * n2] = v;
     }
+  }
+}
+
+// The split correlation at N = 32² (the backward's dz*, partial spectra of
+// G CTAs a row as corr_reg_kernel leaves them) through one exchange block
+// instead of two: after Q's two forward steps, each thread's 32 bins
+// (k2 = i, k1 = 0..31 of its pair) wait in tensor memory while K takes the
+// same shared block, and K's second step multiplies by them as it reads
+// them back.  A CTA then needs 84 KB of shared memory instead of 152 KB, and
+// two CTAs (16 warps) share an SM instead of one.  Tensor memory: 128
+// columns a CTA, two CTAs 256 of the SM's 512; warp w keeps its threads'
+// 64 floats in lanes 32·(w mod 4) + lane, columns 64·(w / 4) ...
+constexpr int kCorrTmCols = 128;
+constexpr int kCorrTmP = 8;   // pairs a CTA, as conv_reg_pairs(32)
+constexpr size_t kSmemCorrTm =
+    ((size_t)32 * (32 * kCorrTmP + 8) + 1024 + 32 * 33) * sizeof(float2) + 16;
+
+template <typename T>
+__global__ void __launch_bounds__(32 * kCorrTmP, 2)
+corr_reg_tm_kernel(const T* __restrict__ Q, const T* __restrict__ K,
+                   const float2* __restrict__ W, int D, int H, int dh, int npair,
+                   float2* __restrict__ part, int G) {
+  constexpr int M = 32, N = M * M, P = kCorrTmP, TWS = reg_tws(M), RS = M * P + 8;
+  static_assert(RS == M * P + (P == 8 ? 8 : 0), "row stride as reg_rs(32, 8)");
+  extern __shared__ float4 smem4[];
+  float2* buf = reinterpret_cast<float2*>(smem4);   // [M][M][P], rows RS apart
+  float2* S = buf + M * RS;                         // [k2][k1] running sum
+  float2* tw = S + N;                               // tw[n1·TWS + k2] = w_N^{n1·k2}
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(tw + M * TWS);
+  const int warp = threadIdx.x >> 5;
+  if (warp == 0) tmem_alloc(tslot, kCorrTmCols);
+  const int bh = blockIdx.x / G, gi = blockIdx.x - bh * G;
+  const int b = bh / H, h = bh - b * H;
+  const int share = (npair + P * G - 1) / (P * G) * P;
+  const int pbeg = gi * share, pend = min(npair, pbeg + share);
+  const int p = threadIdx.x % P, i = threadIdx.x / P;
+  for (int e0 = threadIdx.x; e0 < N; e0 += 8 * blockDim.x) {
+    float2 w[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int e = e0 + u * blockDim.x;
+      if (e < N) w[u] = __ldg(&W[(e / M) * (e % M)]);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int e = e0 + u * blockDim.x;
+      if (e < N) {
+        S[e] = make_float2(0.f, 0.f);
+        tw[(e / M) * TWS + e % M] = w[u];
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();   // tensor-memory address, twiddles and sums ready
+  tc_fence_after();
+  const uint32_t tq = *tslot + ((uint32_t)(32 * (warp & 3)) << 16) + 64u * (uint32_t)(warp >> 2);
+  for (int g0 = pbeg; g0 < pend; g0 += P) {
+    const int g = g0 + p;
+    const bool active = g < pend;
+    const bool pair = 2 * g + 1 < dh;
+    const int col = h * dh + 2 * (active ? g : 0);
+    const bool aligned = (col & 1) == 0 && (D & 1) == 0;
+    const size_t base = (size_t)b * N * D + col;
+    float2 a[M];
+    // Q: step 1 (n1 = i) into the block, step 2 (k2 = i) out of it.
+    ld_rows<T, M>(a, Q + base, (size_t)M * D, (size_t)i * D, active, pair, aligned);
+    dft<M, false, CxPaired>(a);
+    __syncthreads();   // the previous pass's sums have read the block
+#pragma unroll
+    for (int k2 = 0; k2 < M; ++k2) buf[k2 * RS + i * P + p] = cmul(a[k2], tw[i * TWS + k2]);
+    __syncthreads();
+#pragma unroll
+    for (int n1 = 0; n1 < M; ++n1) a[n1] = buf[i * RS + n1 * P + p];
+    dft<M, false, CxPaired>(a);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) tc_st8c(tq + 16 * c, a + 8 * c);
+    tc_wait_st();
+    // K: the same two steps through the same block.
+    ld_rows<T, M>(a, K + base, (size_t)M * D, (size_t)i * D, active, pair, aligned);
+    dft<M, false, CxPaired>(a);
+    __syncthreads();   // every thread has read its Q slots
+#pragma unroll
+    for (int k2 = 0; k2 < M; ++k2) buf[k2 * RS + i * P + p] = cmul(a[k2], tw[i * TWS + k2]);
+    __syncthreads();
+#pragma unroll
+    for (int n1 = 0; n1 < M; ++n1) a[n1] = buf[i * RS + n1 * P + p];
+    dft<M, false, CxPaired>(a);
+    // FFT(q)·conj(FFT(k)) into the thread's own slots.
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      float qv[16];
+      tc_ld16(tq + 16 * c, qv);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        buf[i * RS + (8 * c + j) * P + p] = cmulc(make_float2(qv[2 * j], qv[2 * j + 1]), a[8 * c + j]);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < N; e += blockDim.x) {
+      float2 s = S[e];
+      const float2* pr = buf + (e / M) * RS + (e % M) * P;   // S[k2][k1]: row k2, slot k1
+#pragma unroll
+      for (int q = 0; q < P; ++q) s = cadd(s, pr[q]);
+      S[e] = s;
+    }
+  }
+  __syncthreads();
+  float2* dst = part + (size_t)blockIdx.x * N;   // [k2][k1], as S
+  for (int e = threadIdx.x; e < N; e += blockDim.x) dst[e] = S[e];
+  tc_fence_before();
+  __syncthreads();   // every tensor-memory access of the CTA is done
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(*tslot, kCorrTmCols);
   }
 }
 
@@ -625,13 +739,16 @@ bool corr_reg_split_fits(const cat_plan_s* p) {
 cudaError_t launch_corr_reg_split(const cat_plan_s* p, const void* G, const void* V) {
   const int rows = p->B * p->H;
   if (rows == 0) return cudaSuccess;
-  const float scale = 1.0f / (float)p->N;
   float2* part = p->bw_scr;
-  cudaError_t e = p->dtype == 1
-      ? corr_t<__nv_bfloat16, true>(p, (const __nv_bfloat16*)G, (const __nv_bfloat16*)V, nullptr,
-                                    nullptr, scale, part, kCorrSplitG)
-      : corr_t<float, true>(p, (const float*)G, (const float*)V, nullptr, nullptr, scale, part,
-                            kCorrSplitG);
+  const dim3 grid(rows * kCorrSplitG), block(32 * kCorrTmP);
+  if (p->dtype == 1)
+    corr_reg_tm_kernel<__nv_bfloat16><<<grid, block, kSmemCorrTm, p->stream>>>(
+        (const __nv_bfloat16*)G, (const __nv_bfloat16*)V, p->tw, p->D, p->H, p->dh, p->npair,
+        part, kCorrSplitG);
+  else
+    corr_reg_tm_kernel<float><<<grid, block, kSmemCorrTm, p->stream>>>(
+        (const float*)G, (const float*)V, p->tw, p->D, p->H, p->dh, p->npair, part, kCorrSplitG);
+  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   corr_finish_q4<<<rows, kSpecQ4Threads, 0, p->stream>>>(part, kCorrSplitG, p->zs, p->bw_dzs,
                                                          p->bw_dz, p->tw);
@@ -718,6 +835,7 @@ static cudaError_t setup_t() {
   if (e == cudaSuccess) e = allow_max_smem(corr_reg_kernel<T, 14, true>);
   if (e == cudaSuccess) e = allow_max_smem(corr_reg_kernel<T, 16, true>);
   if (e == cudaSuccess) e = allow_max_smem(corr_reg_kernel<T, 32, true>);
+  if (e == cudaSuccess) e = allow_max_smem(corr_reg_tm_kernel<T>);
   return e;
 }
 
