@@ -83,8 +83,13 @@ __host__ __device__ constexpr int reg_tws(int M) { return M == 32 ? M + 1 : M; }
 // TW = false: no twiddle between the two steps, i.e. the 2-D DFT of an
 // M x M token grid (n1 = x, n2 = y): the 2-D circular convolution of the
 // second page's circulant attention.
+// Below M = 32 a CTA is M·16 threads (16 pairs) and three should share an
+// SM (short transforms need few registers); at M = 32 it is the plain
+// 512-thread bound (128 registers a thread).
+#define CAT_REG_BOUNDS(M) __launch_bounds__((M) == 32 ? 512 : (M) * 16, (M) == 32 ? 0 : 3)
+
 template <typename T, int M, bool TW = true>
-__global__ void __launch_bounds__(512)
+__global__ void CAT_REG_BOUNDS(M)
 conv_reg_kernel(const T* __restrict__ V, T* __restrict__ O, const float2* zf,
                 const float2* __restrict__ W, int D, int H, int dh, int npair, int P,
                 int groups, int conj) {
@@ -193,7 +198,7 @@ conv_reg_kernel(const T* __restrict__ V, T* __restrict__ O, const float2* zf,
 // order, and M threads run the inverse of the sum.  Writes out (fp32) and,
 // if z2 is given, (value, 0) into it.
 template <typename T, int M, bool TW>
-__global__ void __launch_bounds__(512)
+__global__ void CAT_REG_BOUNDS(M)
 corr_reg_kernel(const T* __restrict__ Q, const T* __restrict__ K, float2* __restrict__ z2,
                 float* __restrict__ out, const float2* __restrict__ W, int D, int H, int dh,
                 int npair, int P, float scale, float2* __restrict__ part, int G) {
