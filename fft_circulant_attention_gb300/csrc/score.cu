@@ -506,13 +506,18 @@ score_mma_kernel(const __nv_bfloat16* __restrict__ X, const __nv_bfloat16* __res
 // ---------------------------------------------------------------------------
 // TMA-fed bf16 score (the long workloads).  A persistent CTA streams tiles of
 // 64 tokens × 64 d of X through an 8-stage shared-memory ring: one producer
-// warp issues a 2-D tensor copy (128-byte swizzle) per stage, four consumer
-// warps (16 tokens each) read their A fragments with ldmatrix and run the
-// same slice-wise MMA + TwoSum as score_mma_kernel.  Loads thus run up to
-// eight stages ahead of the math, independent of the consumer registers.
+// warp issues a 2-D tensor copy (128-byte swizzle) per stage, and 4·NT
+// consumer warps, one per 16 tokens and n-tile of 8 heads, read their A
+// fragments with ldmatrix and run the same slice-wise MMA + TwoSum as
+// score_mma_kernel.  Loads thus run up to eight stages ahead of the math,
+// independent of the consumer registers; a warp per n-tile halves each
+// warp's chain of MMAs and TwoSums at NT = 2.
 // ---------------------------------------------------------------------------
-constexpr int kTsRows = 64, kTsCols = 64, kTsStages = 8, kTsConsumers = 4;
-constexpr int kTsThreads = (kTsConsumers + 1) * 32;
+constexpr int kTsRows = 64, kTsCols = 64, kTsStages = 8;
+template <int NT>
+constexpr int ts_consumers() { return 4 * NT; }
+template <int NT>
+constexpr int ts_threads() { return (ts_consumers<NT>() + 1) * 32; }
 constexpr int kTsStageBytes = kTsRows * kTsCols * 2;
 
 __host__ __device__ inline int ts_wt_stride(int D) { return D + 8; }
@@ -522,10 +527,11 @@ static size_t score_tma_smem(int D) {
 }
 
 template <int NT>
-__global__ void __launch_bounds__(kTsThreads)
+__global__ void __launch_bounds__(ts_threads<NT>())
 score_tma_kernel(const __grid_constant__ CUtensorMap tmX, const __nv_bfloat16* __restrict__ WA,
                  float2* __restrict__ z, int N, int D, int H, int h0, int HT, int row0,
                  int rows_total, unsigned int* status) {
+  constexpr int kTsConsumers = ts_consumers<NT>();
   pdl_trigger();   // the softmax kernel behind may launch (it waits for the scores)
   extern __shared__ __align__(1024) unsigned char sm_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
@@ -573,65 +579,54 @@ score_tma_kernel(const __grid_constant__ CUtensorMap tmX, const __nv_bfloat16* _
     return;
   }
 
+  // Consumer warp: tokens 16·tg .. of the tile, heads 8·nt .. (n-tile nt).
+  const int tg = warp & 3, nt = warp >> 2;
   const int c = lane & 3, mrow = lane >> 2;
   const int lm = lane >> 3, li = lane & 7;
-  const int arow = warp * 16 + (lm & 1) * 8 + li;   // ldmatrix row this lane addresses
+  const int arow = tg * 16 + (lm & 1) * 8 + li;   // ldmatrix row this lane addresses
+  const unsigned short* wrow = wt + (nt * 8 + mrow) * ws + 2 * c;
   int it = 0;
   for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-    // Accumulators in pairs: [nt][r] holds fragment elements 2r, 2r + 1.
-    float2 hi[NT][2], lo[NT][2];
+    // Accumulators in pairs: [r] holds fragment elements 2r, 2r + 1.
+    float2 hi[2], lo[2];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int r = 0; r < 2; ++r) hi[nt][r] = lo[nt][r] = make_float2(0.f, 0.f);
+    for (int r = 0; r < 2; ++r) hi[r] = lo[r] = make_float2(0.f, 0.f);
     for (int kb = 0; kb < nkb; ++kb, ++it) {
       const int s = it % kTsStages;
       if (!mbar_wait(full + s, (it / kTsStages) & 1, status, 0x602)) return;
       const uint32_t base = smem_addr(stages + s * kTsStageBytes) + arow * 128;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
-        float acc[NT][4];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int i = 0; i < 4; ++i) acc[nt][i] = 0.f;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
           const int t = 2 * half + q;            // 16-wide k step within the 64
           const int chunk = 2 * t + (lm >> 1);
           unsigned a[4];
           ldmatrix_x4(a, base + ((chunk ^ (arow & 7)) << 4));
-          const int k0 = kb * kTsCols + 16 * t + 2 * c;
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            const unsigned short* wr = wt + (nt * 8 + mrow) * ws + k0;
-            const unsigned b0 = *reinterpret_cast<const unsigned*>(wr);
-            const unsigned b1 = *reinterpret_cast<const unsigned*>(wr + 8);
-            mma_bf16(acc[nt], a, b0, b1);
-          }
+          const unsigned short* wr = wrow + kb * kTsCols + 16 * t;
+          const unsigned b0 = *reinterpret_cast<const unsigned*>(wr);
+          const unsigned b1 = *reinterpret_cast<const unsigned*>(wr + 8);
+          mma_bf16(acc, a, b0, b1);
         }
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int r = 0; r < 2; ++r)
-            two_sum_acc2(hi[nt][r], lo[nt][r], make_float2(acc[nt][2 * r], acc[nt][2 * r + 1]));
+        for (int r = 0; r < 2; ++r)
+          two_sum_acc2(hi[r], lo[r], make_float2(acc[2 * r], acc[2 * r + 1]));
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(empty + s);
     }
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int r = row0 + tile * kTsRows + warp * 16 + mrow + 8 * (i >> 1);
-        const int hh = nt * 8 + 2 * c + (i & 1);
-        if (r < rows_total && hh < HT) {
-          const int b = r / N, n = r - b * N;
-          const float2 hv = hi[nt][i >> 1], lv = lo[nt][i >> 1];
-          z[((size_t)b * H + h0 + hh) * N + n] =
-              (i & 1) ? make_float2(hv.y, lv.y) : make_float2(hv.x, lv.x);
-        }
+    for (int i = 0; i < 4; ++i) {
+      const int r = row0 + tile * kTsRows + tg * 16 + mrow + 8 * (i >> 1);
+      const int hh = nt * 8 + 2 * c + (i & 1);
+      if (r < rows_total && hh < HT) {
+        const int b = r / N, n = r - b * N;
+        const float2 hv = hi[i >> 1], lv = lo[i >> 1];
+        z[((size_t)b * H + h0 + hh) * N + n] =
+            (i & 1) ? make_float2(hv.y, lv.y) : make_float2(hv.x, lv.x);
       }
+    }
   }
 }
 
@@ -666,10 +661,10 @@ static cudaError_t score_tma(const cat_plan_s* p, const void* X, const void* WA,
   for (int h0 = 0; h0 < p->H; h0 += 16) {
     const int ht = p->H - h0 < 16 ? p->H - h0 : 16;
     if (ht > 8)
-      score_tma_kernel<2><<<grid, kTsThreads, smem, st>>>(
+      score_tma_kernel<2><<<grid, ts_threads<2>(), smem, st>>>(
           tm, (const __nv_bfloat16*)WA, p->z2, p->N, p->D, p->H, h0, ht, row0, row_end, p->status);
     else
-      score_tma_kernel<1><<<grid, kTsThreads, smem, st>>>(
+      score_tma_kernel<1><<<grid, ts_threads<1>(), smem, st>>>(
           tm, (const __nv_bfloat16*)WA, p->z2, p->N, p->D, p->H, h0, ht, row0, row_end, p->status);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
