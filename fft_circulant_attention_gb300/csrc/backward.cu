@@ -581,15 +581,22 @@ static cudaError_t corr_t(const cat_plan_s* p, const T* G, const T* V) {
 // half c mod 2 of both scratch slots (dO's and V's spectra) and of the
 // one-signal buffer y, so two chunks are in flight in the same 64 MB.
 // With dV given, each chunk then runs the forward's passes B and C on dO's
-// transform, still in its half slot (the spectrum of the reversed scores
-// must be in zf): dV = circ(z*)^T dO without transforming dO a second time.
+// transform, still in its half slot, with the spectrum of z* conjugated
+// (that of z* reversed): dV = circ(z*)^T dO without transforming dO a
+// second time.  The plan's stream then waits only for the streams'
+// correlation work (event ev_front[k] after each chunk's), so that the last
+// chunks' dV passes run beside pass C, the softmax backward and dW_A, dX;
+// backward_join_dv joins the streams at the end.
 static cudaError_t corr_fast_overlapped(const cat_plan_s* p, const void* G, const void* V,
                                         void* dV) {
   const int rows = p->B * p->H;
   const int cb = p->fs.chunk_bh / 2;
   const size_t half = p->scratch_bytes / 4 / sizeof(float2);   // a half slot
   cudaError_t e = cudaEventRecord(p->ev_fork, p->stream);
-  for (int k = 0; k < 2 && e == cudaSuccess; ++k) e = cudaStreamWaitEvent(p->side[k], p->ev_fork, 0);
+  for (int k = 0; k < 2 && e == cudaSuccess; ++k) {
+    e = cudaStreamWaitEvent(p->side[k], p->ev_fork, 0);
+    if (e == cudaSuccess && dV) e = cudaEventRecord(p->ev_front[k], p->side[k]);
+  }
   for (int bh0 = 0, c = 0; bh0 < rows && e == cudaSuccess; bh0 += cb, ++c) {
     const int nb = rows - bh0 < cb ? rows - bh0 : cb;
     const int k = c & 1;
@@ -597,14 +604,22 @@ static cudaError_t corr_fast_overlapped(const cat_plan_s* p, const void* G, cons
     float2* s1 = p->scratch + 2 * half + (size_t)k * half;
     // Each chunk's y at its own rows: pass C runs once for all rows below.
     e = launch_fast_corr(p, G, V, p->bw_scr + (size_t)bh0 * p->N, bh0, nb, p->side[k], s0, s1);
+    if (e == cudaSuccess && dV) e = cudaEventRecord(p->ev_front[k], p->side[k]);
     if (e == cudaSuccess && dV) e = launch_fast_bc32(p, s0, dV, bh0, nb, k * cb, p->side[k]);
   }
   for (int k = 0; k < 2; ++k) {
     cudaError_t e2 = cudaEventRecord(p->ev_join[k], p->side[k]);
-    if (e2 == cudaSuccess) e2 = cudaStreamWaitEvent(p->stream, p->ev_join[k], 0);
+    if (e2 == cudaSuccess)
+      e2 = cudaStreamWaitEvent(p->stream, dV ? p->ev_front[k] : p->ev_join[k], 0);
     if (e == cudaSuccess) e = e2;
   }
   if (e == cudaSuccess) e = launch_fast_corr_c32(p, p->bw_scr, p->bw_dzs, 0, rows, p->stream);
+  return e;
+}
+
+cudaError_t backward_join_dv(const cat_plan_s* p) {
+  cudaError_t e = cudaSuccess;
+  for (int k = 0; k < 2 && e == cudaSuccess; ++k) e = cudaStreamWaitEvent(p->stream, p->ev_join[k], 0);
   return e;
 }
 

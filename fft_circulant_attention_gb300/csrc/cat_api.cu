@@ -1196,7 +1196,8 @@ cudaError_t backward_schedule(cat_plan_s* p, const void* X, const void* WA, cons
     if (e == cudaSuccess) e = cat::launch_fast_zspec(p, 0, p->B * p->H, p->stream, true, p->zs);
     if (e == cudaSuccess) e = cat::launch_backward_dz(p, dO, V, dV);
     if (e == cudaSuccess) e = cat::launch_backward_dense(p, X, WA, dX, dWA);
-    return e;
+    const cudaError_t ej = cat::backward_join_dv(p);   // also after an error: close the fork
+    return e == cudaSuccess ? ej : e;
   }
   if (p->path == cat::PATH_SMEM && p->sm.reg_m && !p->twod) {
     // Register path: one spectrum kernel gives z* (for the softmax

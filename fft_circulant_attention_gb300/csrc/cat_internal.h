@@ -321,12 +321,17 @@ size_t fast_tables_bytes(int N2);
 // Backward pass (backward.cu).  launch_backward_dz: correlation passes and
 // softmax backward into bw_dzs and bw_dz (needs z* in zs); with dV, also
 // dV from the correlation's own transform of G (only where
-// backward_dv_in_corr holds, and with the reversed scores' spectrum in zf).
+// backward_dv_in_corr holds, with the spectrum of z* in zf, which its passes
+// B take conjugated; the plan's stream joins the dV passes only at
+// backward_join_dv).
 // launch_backward_dense: dW_A and dX from bw_dz.  launch_reverse_scores:
 // z2[n] <-> z2[(-n) mod N] in every row, so that the forward's spectrum and
 // product kernels then give circ(z*)^T.
 cudaError_t setup_backward_kernels(const cat_plan_s* p);
 bool backward_dv_in_corr(const cat_plan_s* p);
+// After a backward_dz with dV on the overlapped fast path: the plan's stream
+// waits for the internal streams' last dV passes.
+cudaError_t backward_join_dv(const cat_plan_s* p);
 cudaError_t launch_backward_dz(const cat_plan_s* p, const void* G, const void* V,
                                void* dV = nullptr);
 cudaError_t launch_backward_dense(const cat_plan_s* p, const void* X, const void* WA, void* dX,
