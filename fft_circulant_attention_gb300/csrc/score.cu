@@ -373,6 +373,15 @@ score_split_kernel(const T* __restrict__ X, const T* __restrict__ WA, float2* __
 // the threads read consecutive vectors of W_A — one coalesced stream — and
 // scatter their 8 heads into the transposed layout; otherwise each thread
 // copies whole rows element by element.
+// PAIRED: within each 16 columns the order 0 1 8 9 2 3 10 11 ..., so that a
+// lane's two B-fragment words of an m16n8k16 MMA (k0, k0 + 1 and k0 + 8,
+// k0 + 9, k0 = 2c) are one 8-byte load.
+__device__ __forceinline__ int wt_col(int d, bool paired) {
+  if (!paired) return d;
+  const int r = d & 15;
+  return (d & ~15) + ((r & 7) >> 1) * 4 + (r >> 3) * 2 + (r & 1);
+}
+template <bool PAIRED = false>
 __device__ __forceinline__ void stage_wt(unsigned short* wt, int ws, const unsigned short* wa,
                                          int D, int H, int h0, int HT, int rows, int tid,
                                          int nthr) {
@@ -403,7 +412,7 @@ __device__ __forceinline__ void stage_wt(unsigned short* wt, int ws, const unsig
         for (int q = 0; q < 8; ++q) {
           const int hh = hb + q;
           if (hh >= 0 && hh < HT && hh < rows)
-            wt[hh * ws + d] =
+            wt[hh * ws + wt_col(d, PAIRED)] =
                 (unsigned short)((q & 1) ? (w[q >> 1] >> 16) : (w[q >> 1] & 0xffffu));
         }
       }
@@ -416,7 +425,7 @@ __device__ __forceinline__ void stage_wt(unsigned short* wt, int ws, const unsig
       for (int hh = 0; hh < 16; ++hh) v[hh] = hh < HT ? __ldg(src + hh) : (unsigned short)0;
 #pragma unroll
       for (int hh = 0; hh < 16; ++hh)
-        if (hh < rows && hh < HT) wt[hh * ws + d] = v[hh];
+        if (hh < rows && hh < HT) wt[hh * ws + wt_col(d, PAIRED)] = v[hh];
     }
   }
 }
@@ -520,7 +529,9 @@ template <int NT>
 constexpr int ts_threads() { return (ts_consumers<NT>() + 1) * 32; }
 constexpr int kTsStageBytes = kTsRows * kTsCols * 2;
 
-__host__ __device__ inline int ts_wt_stride(int D) { return D + 8; }
+// D + 16: a row is 8 words past a multiple of 32, so the 8-byte B-fragment
+// loads of a half warp (4 rows × 4 lanes) fall in distinct banks.
+__host__ __device__ inline int ts_wt_stride(int D) { return D + 16; }
 static size_t score_tma_smem(int D) {
   return (size_t)kTsStages * kTsStageBytes + (size_t)16 * ts_wt_stride(D) * 2 + 2 * kTsStages * 8 +
          1024;
@@ -553,8 +564,8 @@ score_tma_kernel(const __grid_constant__ CUtensorMap tmX, const __nv_bfloat16* _
   // The producer starts streaming X at once; the consumer warps stage W_A^T
   // meanwhile and sync among themselves (named barrier 1) before using it.
   if (warp < kTsConsumers) {
-    stage_wt(wt, ws, reinterpret_cast<const unsigned short*>(WA), D, H, h0, HT, 16, threadIdx.x,
-             kTsConsumers * 32);
+    stage_wt<true>(wt, ws, reinterpret_cast<const unsigned short*>(WA), D, H, h0, HT, 16,
+                   threadIdx.x, kTsConsumers * 32);
     asm volatile("bar.sync 1, %0;" ::"n"(kTsConsumers * 32) : "memory");
   }
   const int nkb = D / kTsCols;
@@ -584,7 +595,7 @@ score_tma_kernel(const __grid_constant__ CUtensorMap tmX, const __nv_bfloat16* _
   const int c = lane & 3, mrow = lane >> 2;
   const int lm = lane >> 3, li = lane & 7;
   const int arow = tg * 16 + (lm & 1) * 8 + li;   // ldmatrix row this lane addresses
-  const unsigned short* wrow = wt + (nt * 8 + mrow) * ws + 2 * c;
+  const unsigned short* wrow = wt + (nt * 8 + mrow) * ws + 4 * c;   // paired columns
   int it = 0;
   for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
     // Accumulators in pairs: [r] holds fragment elements 2r, 2r + 1.
@@ -604,10 +615,8 @@ score_tma_kernel(const __grid_constant__ CUtensorMap tmX, const __nv_bfloat16* _
           const int chunk = 2 * t + (lm >> 1);
           unsigned a[4];
           ldmatrix_x4(a, base + ((chunk ^ (arow & 7)) << 4));
-          const unsigned short* wr = wrow + kb * kTsCols + 16 * t;
-          const unsigned b0 = *reinterpret_cast<const unsigned*>(wr);
-          const unsigned b1 = *reinterpret_cast<const unsigned*>(wr + 8);
-          mma_bf16(acc, a, b0, b1);
+          const uint2 bw = *reinterpret_cast<const uint2*>(wrow + kb * kTsCols + 16 * t);
+          mma_bf16(acc, a, bw.x, bw.y);
         }
 #pragma unroll
         for (int r = 0; r < 2; ++r)
