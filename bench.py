@@ -62,8 +62,8 @@ FALLBACK_HBM_GBS = 6800.0
 NCU_TRAFFIC = {
     # the launch-list captures: the median of their pass-B launches (8 at
     # long16k, 16 at long128k)
-    ("long16k", "43d02c8c03ce"): 34773888,
-    ("long128k", "43d02c8c03ce"): 35691392,
+    ("long16k", "43d02c8c03ce"): 34773632,
+    ("long128k", "43d02c8c03ce"): 35691264,
 }
 KERNEL_SOURCES = ["fourstep_fast.cu", "fft_reg.cuh", "fft_device.cuh", "bulk.cuh", "elem.cuh"]
 # Pass B's transforms: per (pair, k2) signal one forward and one inverse DFT
