@@ -267,10 +267,12 @@ corr_reg_kernel(const T* __restrict__ Q, const T* __restrict__ K, float2* __rest
     for (int k1 = 0; k1 < M; ++k1)
       bq[i * RS + k1 * P + p] = cmulc(bq[i * RS + k1 * P + p], a[k1]);
     __syncthreads();
+    // Sum over the pairs, element e starting at pair e mod P (P a power of
+    // two): consecutive lanes' rows of P slots would otherwise share banks.
     for (int e = threadIdx.x; e < N; e += blockDim.x) {
       float2 s = S[e];
       const float2* pr = bq + (e / M) * RS + (e % M) * P;   // S[k2][k1]: row k2, slot k1
-      for (int q = 0; q < P; ++q) s = cadd(s, pr[q]);
+      for (int q = 0; q < P; ++q) s = cadd(s, pr[(q + e) & (P - 1)]);
       S[e] = s;
     }
   }
@@ -398,11 +400,13 @@ corr_reg_tm_kernel(const T* __restrict__ Q, const T* __restrict__ K,
         buf[i * RS + (8 * c + j) * P + p] = cmulc(make_float2(qv[2 * j], qv[2 * j + 1]), a[8 * c + j]);
     }
     __syncthreads();
+    // Sum over the pairs, element e starting at pair e mod P: the lanes of
+    // a warp (consecutive k1, 16 words apart) then read distinct banks.
     for (int e = threadIdx.x; e < N; e += blockDim.x) {
       float2 s = S[e];
       const float2* pr = buf + (e / M) * RS + (e % M) * P;   // S[k2][k1]: row k2, slot k1
 #pragma unroll
-      for (int q = 0; q < P; ++q) s = cadd(s, pr[q]);
+      for (int q = 0; q < P; ++q) s = cadd(s, pr[(q + e) & (P - 1)]);
       S[e] = s;
     }
   }
