@@ -134,7 +134,7 @@ proj_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
       const int NT = ztile ? kPjNZ : min(kPjNV, D - nti * kPjNV);
       const uint32_t idesc = idesc_bf16_f32(kPjM, NT);
       const int b = it & 1;
-      // Lane 0 waits and issues; the warp follows its verdict, so that the
+      // Lane 0 waits and issues; the warp follows its result, so that the
       // whole warp leaves a loop together.
       bool w = true;
       if (it >= 2 && lane == 0) w = mbar_wait(tempty + b, ((it >> 1) - 1) & 1, status, 0x605);

@@ -58,7 +58,7 @@ enum {
   CAT_ERR_TOO_LARGE = -9      /* beyond cat_forward_noalloc's fixed workspace */
 };
 
-/* Limits of this build. */
+/* Size limits of the library. */
 #define CAT_MAX_N (1 << 22)   /* longest sequence                          */
 #define CAT_MAX_D 8192        /* widest model dimension                    */
 
